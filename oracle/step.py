@@ -1,0 +1,92 @@
+"""One llama-style batched decode step composed from the oracle's pieces.
+
+The ds4 page ("What", "Design note") runs the dense stages once for all live
+sessions with n_tokens = n_seqs and keeps KV append and attention per
+sequence; the QAIC page ("Objective") addresses a retained cache of
+full_batch_size slots through batch_index.  The layer order used here (the
+pages do not print one) is the plain pre-norm llama layer:
+
+    h   = embedding(token)
+    per layer:
+        x = quant(rmsnorm(h));  [q|k|v] = Wqkv x;  q, k <- rope(pos)
+        cache[batch_index] <- k, v at pos;  a = attention(q, cache, seq_lens)
+        h = h + Wo quant(a)
+        x = quant(rmsnorm(h));  [g|u] = Wgu x;  h = h + Wdown quant(silu(g) u)
+    logits = Whead quant(rmsnorm(h))
+
+``quant`` rounds the float64 activation to float32 and applies the q8_0
+codec: activations enter every matmul pre-quantised, as on the ds4 page.
+
+Parity unpinned as a composition: each stage is pinned on its own by the
+oracle tests, but no printed end-to-end value exists to pin the composed
+step; the step comparison is a looser, derived tolerance.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import attention, glue, kv, matmul, q8_0, rope
+
+
+@dataclass(frozen=True)
+class Shape:
+    hidden: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    ffn: int
+    vocab: int
+    n_layers: int
+    eps: float = 1e-6
+    theta: float = 10000.0
+
+
+def quant(x: np.ndarray) -> np.ndarray:
+    return q8_0.quantize_rows(np.asarray(x, dtype=np.float64).astype(np.float32))
+
+
+def positions(seq_lens, tokens_per_seq: int) -> np.ndarray:
+    """pos[s*T + j] = seq_lens[s] - T + j."""
+    return np.array([int(L) - tokens_per_seq + j for L in seq_lens for j in range(tokens_per_seq)],
+                    dtype=np.int64)
+
+
+def decode_step(shape: Shape, w: dict, k_caches: list, v_caches: list, cache_dtype: str,
+                token_ids, batch_index, tokens_per_seq: int, seq_lens):
+    """Returns ``(logits float64 [n_tok, vocab], new k_caches, new v_caches)``.
+
+    ``w`` holds q8_0 byte arrays ``embed, head`` and per layer ``wqkv[l],
+    wo[l], wgu[l], wdown[l]`` plus float32 norm weights ``attn_norm[l],
+    ffn_norm[l], final_norm``.  Caches are uint16 bit arrays ``[F, Hkv, C, D]``.
+    """
+    sh = shape
+    pos = positions(seq_lens, tokens_per_seq)
+    n_tok = len(pos)
+    hq, hkv, d = sh.n_q_heads, sh.n_kv_heads, sh.head_dim
+    h = glue.embedding(w["embed"], token_ids)
+    new_k, new_v = [], []
+    for layer in range(sh.n_layers):
+        x = glue.rmsnorm(h, w["attn_norm"][layer], sh.eps)
+        qkv = matmul.matmul_q8_0(w["wqkv"][layer], quant(x))
+        q = qkv[:, :hq * d].reshape(n_tok, hq, d)
+        k = qkv[:, hq * d:(hq + hkv) * d].reshape(n_tok, hkv, d)
+        v = qkv[:, (hq + hkv) * d:].reshape(n_tok, hkv, d)
+        q = rope.rope_posvec(q, pos, sh.theta)
+        k = rope.rope_posvec(k, pos, sh.theta)
+        kc, vc = kv.kv_scatter(k_caches[layer], v_caches[layer], batch_index, tokens_per_seq, pos,
+                               k.astype(np.float32), v.astype(np.float32), cache_dtype)
+        new_k.append(kc)
+        new_v.append(vc)
+        a = attention.attention_decode_multi(q, kv.bits_to_f64(kc, cache_dtype),
+                                             kv.bits_to_f64(vc, cache_dtype),
+                                             batch_index, tokens_per_seq, seq_lens)
+        h = glue.residual_add(h, matmul.matmul_q8_0(w["wo"][layer], quant(a.reshape(n_tok, hq * d))))
+        x = glue.rmsnorm(h, w["ffn_norm"][layer], sh.eps)
+        gu = matmul.matmul_q8_0(w["wgu"][layer], quant(x))
+        act = glue.silu_mul(gu[:, :sh.ffn], gu[:, sh.ffn:])
+        h = glue.residual_add(h, matmul.matmul_q8_0(w["wdown"][layer], quant(act)))
+    x = glue.rmsnorm(h, w["final_norm"], sh.eps)
+    logits = matmul.matmul_q8_0(w["head"], quant(x))
+    return logits, new_k, new_v

@@ -1,0 +1,75 @@
+"""Workload shapes and seeded draws shared by the tests.
+
+Shapes follow the workloads the pages measure on (llama-68m-shaped decode on
+the QAIC page, Qwen3-14B-shaped decode on the pypto page, DeepSeek-class
+dense stages and long context on the ds4 page).  Every value is drawn by
+``session_decode_step_dsb_gb300.synth`` and is a pure function of the seed.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+from session_decode_step_dsb_gb300 import synth
+
+
+@dataclass(frozen=True)
+class ModelShape:
+    hidden: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    ffn: int
+    vocab: int
+    n_layers: int
+    full_batch_size: int
+    ctx: int
+    cache_dtype: str
+    eps: float = 1e-6
+    theta: float = 10000.0
+
+    @property
+    def qkv_rows(self):
+        return (self.n_q_heads + 2 * self.n_kv_heads) * self.head_dim
+
+
+LLAMA68M = ModelShape(768, 12, 12, 64, 3072, 32000, 2, 8, 2048, "f16")
+QWEN3_14B_1L = ModelShape(5120, 40, 8, 128, 17408, 151936, 1, 16, 4096, "bf16")
+TINY = ModelShape(256, 4, 2, 64, 512, 1000, 2, 4, 96, "f16")
+TINY_BF16 = ModelShape(256, 8, 2, 32, 384, 700, 1, 5, 80, "bf16")
+
+W_STD = 0.02
+
+
+def weight_f32(seed: int, shape: ModelShape):
+    """float32 weight draws {name: array}; per layer lists for layered ones."""
+    sid = synth.stream_id
+    out = {"wqkv": [], "wo": [], "wgu": [], "wdown": []}
+    for layer in range(shape.n_layers):
+        out["wqkv"].append(synth.normal_rows(seed, sid(synth.STREAM_W, 10 * layer + 0), shape.qkv_rows, shape.hidden, W_STD))
+        out["wo"].append(synth.normal_rows(seed, sid(synth.STREAM_W, 10 * layer + 1), shape.hidden, shape.n_q_heads * shape.head_dim, W_STD))
+        out["wgu"].append(synth.normal_rows(seed, sid(synth.STREAM_W, 10 * layer + 2), 2 * shape.ffn, shape.hidden, W_STD))
+        out["wdown"].append(synth.normal_rows(seed, sid(synth.STREAM_W, 10 * layer + 3), shape.hidden, shape.ffn, W_STD))
+    out["head"] = synth.normal_rows(seed, sid(synth.STREAM_W, 999_000), shape.vocab, shape.hidden, W_STD)
+    out["embed"] = synth.normal_rows(seed, sid(synth.STREAM_EMBED, 0), shape.vocab, shape.hidden, W_STD)
+    out["attn_norm"] = [np.ones(shape.hidden, np.float32) for _ in range(shape.n_layers)]
+    out["ffn_norm"] = [np.ones(shape.hidden, np.float32) for _ in range(shape.n_layers)]
+    out["final_norm"] = np.ones(shape.hidden, np.float32)
+    return out
+
+
+def cache_bits(seed: int, shape: ModelShape, layer: int, which: str):
+    kind = synth.STREAM_KCACHE if which == "k" else synth.STREAM_VCACHE
+    dims = (shape.full_batch_size, shape.n_kv_heads, shape.ctx, shape.head_dim)
+    return synth.cache_bits(seed, synth.stream_id(kind, layer), dims, shape.cache_dtype)
+
+
+def step_meta(seed: int, shape: ModelShape, b: int, T: int, min_len: int | None = None):
+    """batch_index (distinct), seq_lens (>= T) and token ids for one step."""
+    sid = synth.stream_id
+    bi = synth.distinct_slots(seed, sid(synth.STREAM_META, 1), b, shape.full_batch_size)
+    lo = max(T, min_len if min_len is not None else T)
+    lens = synth.uniform_int(seed, sid(synth.STREAM_META, 2), lo, shape.ctx, b)
+    toks = synth.uniform_int(seed, sid(synth.STREAM_TOKENS, 0), 0, shape.vocab - 1, b * T)
+    return bi, lens, toks

@@ -1,0 +1,68 @@
+"""Pins for the oracle's pos-vector RoPE (CPU only)."""
+import math
+import os
+
+import numpy as np
+
+from oracle import rope
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "rope_d4.txt")
+
+
+def test_hand_values_d4():
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        p, xs, ys = (s.strip() for s in line.split("|"))
+        x = np.array([float(v) for v in xs.split()]).reshape(1, 1, 4)
+        want = np.array([float(v) for v in ys.split()])
+        got = rope.rope_posvec(x, np.array([int(p)]), 10000.0)[0, 0]
+        assert np.allclose(got, want, rtol=0, atol=1e-15), (line, got)
+
+
+def test_position_zero_is_identity():
+    x = np.random.default_rng(0).standard_normal((3, 4, 64))
+    assert np.array_equal(rope.rope_posvec(x, np.zeros(3, int), 10000.0), x)
+
+
+def test_pair_norms_preserved():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((5, 3, 128))
+    pos = rng.integers(0, 65536, 5)
+    y = rope.rope_posvec(x, pos, 10000.0)
+    n_in = x[..., :64] ** 2 + x[..., 64:] ** 2
+    n_out = y[..., :64] ** 2 + y[..., 64:] ** 2
+    assert np.allclose(n_in, n_out, rtol=1e-12, atol=0)
+
+
+def test_relative_position_invariance():
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((1, 1, 64))
+    k = rng.standard_normal((1, 1, 64))
+    dots = []
+    for p in [0, 17, 1000, 40000]:
+        qr = rope.rope_posvec(q, np.array([p + 5]), 10000.0)
+        kr = rope.rope_posvec(k, np.array([p]), 10000.0)
+        dots.append(float(np.sum(qr * kr)))
+    assert np.allclose(dots, dots[0], rtol=0, atol=1e-10)
+
+
+def test_d2_is_textbook_rotation():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((6, 1, 2))
+    pos = np.array([0, 1, 2, 5, 100, 12345])
+    y = rope.rope_posvec(x, pos, 10000.0)
+    for t, p in enumerate(pos):
+        c, s = math.cos(p), math.sin(p)
+        m = np.array([[c, -s], [s, c]])
+        assert np.allclose(y[t, 0], m @ x[t, 0], rtol=0, atol=1e-12)
+
+
+def test_each_row_uses_its_own_position():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((4, 2, 16))
+    pos = np.array([9, 0, 300, 9])
+    y = rope.rope_posvec(x, pos, 10000.0)
+    for t in range(4):
+        assert np.array_equal(y[t], rope.rope_posvec(x[t:t + 1], pos[t:t + 1], 10000.0)[0])
