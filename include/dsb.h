@@ -1,0 +1,195 @@
+/*
+ * dsb.h -- C ABI of libdsb.so: the batched multi-session decode step on
+ * GB300 (sm_103a).
+ *
+ * One decode step advances b live sessions (1 <= b <= full_batch_size) by one
+ * token each, or by T = K+1 tokens each under speculative decode, in one GPU
+ * pass.  Sources of the operations (the pages this library restates):
+ *
+ *   [DS4]  antirez/ds4 PR #530, "Batched decode: co-decode N live sessions in
+ *          one GPU pass (opt-in)": the narrow-batch q8_0 matmul ("Why it's
+ *          worth it -- the narrow-batch matmul"), the pos-vector RoPE, the
+ *          multi-sequence decode attention and the engine-owned scratch vs
+ *          per-session state split (commit bodies of the walk-through).
+ *   [QAIC] quic/efficient-transformers PR #1305, "[feature] Enable Dynamic
+ *          Batching": KV cache always sized for full_batch_size, addressed by
+ *          batch_index ("Objective"); K+1 speculative tokens per sequence and
+ *          rejecting bad combinations with clear errors before execution
+ *          ("Assumptions and limitations").
+ *   [PTO]  hw-native-sys/pypto-lib PR #841, "Add: dynamic public batch (1..16)
+ *          for Qwen3-14B decode": live batch taken from the seq_lens
+ *          descriptor; contract 1 <= batch <= batch_pad (commit message).
+ *
+ * Conventions for every call
+ *   - Device pointers point to memory the caller owns (e.g. torch tensors);
+ *     the library never frees them.  Host arrays (batch_index, pos, seq_lens)
+ *     are read during the call only; the caller may reuse them on return.
+ *   - Every call validates all arguments on the host BEFORE any CUDA call and
+ *     returns a status; on a non-OK status no device memory has been written.
+ *     It never aborts.  dsb_last_error() gives a message for the last non-OK
+ *     status of the calling thread.
+ *   - Work is enqueued on the given stream (a cudaStream_t; NULL = legacy
+ *     default stream) and runs asynchronously.  Device pointers must be 16-byte
+ *     aligned.  Kernels never spin on other CTAs; the mbarrier waits inside a
+ *     CTA are bounded and, if exceeded, set a device error word reported by
+ *     dsb_device_error().
+ *   - A workspace serves one stream at a time (the engine-owned scratch shared
+ *     by the sessions one thread drives, [DS4] session-split commit).
+ */
+#ifndef DSB_H
+#define DSB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSB_OK = 0,
+  DSB_ERR_INVALID_ARG = 1, /* bad pointer, size, index or combination     */
+  DSB_ERR_UNSUPPORTED = 2, /* valid but not served by this build          */
+  DSB_ERR_WORKSPACE = 3,   /* workspace missing or too small              */
+  DSB_ERR_CUDA = 4,        /* a CUDA runtime call failed (see last_error) */
+  DSB_ERR_TIMEOUT = 5,     /* a bounded host wait ran out                 */
+  DSB_ERR_DEVICE = 6       /* a kernel reported a bounded wait that ran out */
+} dsb_status;
+
+typedef enum { DSB_F16 = 0, DSB_BF16 = 1 } dsb_dtype;
+
+/* Largest live batch and token count one call accepts (metadata capacity). */
+#define DSB_MAX_SEQS 1024
+#define DSB_MAX_TOKENS 8192
+/* Largest n_tok of the narrow matmul (one weight read serves all tokens). */
+#define DSB_NARROW_MAX 16
+/* Keys per split-K chunk of the decode attention (independent of b, n_tok). */
+#define DSB_ATTN_CHUNK 128
+
+/* A q8_0 matrix on the device: rows x cols values, cols % 32 == 0, stored as
+ * rows x (cols/32) blocks of 34 bytes laid end to end; block i of row r sits
+ * at byte (r*(cols/32) + i)*34 and holds the fp16 scale d (little-endian)
+ * followed by 32 int8 codes; value k of the block is d * q[k].
+ * ([DS4] "Why it's worth it": 32-weight blocks, int8 plus an fp16 scale.) */
+typedef struct {
+  const void* blocks;
+  int64_t rows;
+  int64_t cols;
+} dsb_q8_0_mat;
+
+/* A retained KV cache on the device ([QAIC] "Objective"): K and V each
+ * [full_batch_size][n_kv_heads][ctx][head_dim] in dtype, row-major. */
+typedef struct {
+  void* k;
+  void* v;
+  int32_t dtype; /* dsb_dtype */
+  int32_t full_batch_size;
+  int32_t n_kv_heads;
+  int32_t ctx;
+  int32_t head_dim;
+} dsb_kv_cache;
+
+/* Opaque caller-sized scratch: split-K attention partials and the staged
+ * per-call metadata ([DS4] session-split commit: engine-owned scratch). */
+typedef struct dsb_workspace dsb_workspace;
+
+/* ---- library / workspace ------------------------------------------------ */
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char* dsb_last_error(void);
+
+/* Build string: compile-time architecture and version. */
+const char* dsb_version(void);
+
+/* Device bytes a workspace needs to serve calls with up to max_tokens token
+ * rows, n_q_heads query heads of width head_dim, against caches of length
+ * ctx.  Returns 0 if an argument is out of range. */
+size_t dsb_workspace_bytes(int max_tokens, int n_q_heads, int head_dim, int ctx);
+
+/* Wrap caller-owned device memory [device_ptr, device_ptr + device_bytes) as a
+ * workspace bound to the current CUDA device.  Allocates the workspace's small
+ * pinned host staging ring and its events (set-up time only).  *out is NULL on
+ * failure. */
+dsb_status dsb_workspace_create(void* device_ptr, size_t device_bytes, dsb_workspace** out);
+
+/* Waits (bounded) for the workspace's staged copies, then frees the host-side
+ * resources.  Does not free the device memory. */
+dsb_status dsb_workspace_destroy(dsb_workspace* ws);
+
+/* Reads and clears the device error word set by a kernel whose bounded
+ * mbarrier wait ran out (synchronises the current device).  DSB_OK if none. */
+dsb_status dsb_device_error(void);
+
+/* ---- the hot path --------------------------------------------------------- */
+
+/* q8_0-quantise n_rows float32 rows of length cols (cols % 32 == 0) into
+ * xq (n_rows * cols/32 blocks of 34 bytes).  Per 32 values: d = max|x|/127 in
+ * float32, q = round-half-away(x/d) clamped to [-127,127] (0 if d == 0), scale
+ * stored as fp16(d) round-to-nearest-even.  Bit-identical to the host codec.
+ * x: device float32 [n_rows][cols].  xq: device, 16-byte aligned. */
+dsb_status dsb_quantize_q8_0(const float* x, int64_t n_rows, int64_t cols, void* xq, void* stream);
+
+/* Narrow-batch q8_0 matmul ([DS4] "Why it's worth it -- the narrow-batch
+ * matmul"; the narrow-batch q8_0 matmul commit):
+ *   y[t][r] = sum_i fp32(dW[r,i]) * fp32(dX[t,i]) * sum_k qW[r,i,k] qX[t,i,k]
+ * for 1 <= n_tok <= DSB_NARROW_MAX.  Each weight block is read from HBM once
+ * per call and dotted against all n_tok activation blocks.  xq: device q8_0
+ * [n_tok][cols/32 blocks]; y: device float32 [n_tok][rows] (token-major).
+ * Column t of y is bitwise equal to the same input run with n_tok = 1.
+ * Requires cols % 256 == 0 (rows of 16-byte-aligned 8-block chunks). */
+dsb_status dsb_matmul_q8_0_narrow(const dsb_q8_0_mat* w, const void* xq, int n_tok, float* y,
+                                  void* stream);
+
+/* Same product for any n_tok >= 1: tokens in chunks of DSB_NARROW_MAX through
+ * the narrow kernel (weights re-read ceil(n_tok/16) times).  Columns are
+ * bitwise equal to the narrow call's. */
+dsb_status dsb_matmul_q8_0(const dsb_q8_0_mat* w, const void* xq, int n_tok, float* y, void* stream);
+
+/* Debug emission of the narrow kernel: instead of y it writes the exact int32
+ * block dot products isum[t][r][i] = sum_k qW[r,i,k] qX[t,i,k]
+ * (device int32 [n_tok][rows][cols/32]), through the same loads and dp4a
+ * chain as dsb_matmul_q8_0_narrow. */
+dsb_status dsb_matmul_q8_0_block_dots(const dsb_q8_0_mat* w, const void* xq, int n_tok,
+                                      int32_t* isum, void* stream);
+
+/* Pos-vector RoPE ([DS4] pos-vector RoPE commit): every token row t carries
+ * its own position pos[t] (host int32[n_tok], each in [0, 2^24)).  In place
+ * on q (device float32 [n_tok][n_q_heads][head_dim]) and k (device float32
+ * [n_tok][n_kv_heads][head_dim]; may be NULL with n_kv_heads = 0).  Rotate-half
+ * pairs (i, i + D/2), angle pos * theta^(-2i/D), angle and its sine/cosine in
+ * float64, rotation in float32.  Row t is bitwise equal to an n_tok = 1 call. */
+dsb_status dsb_rope_posvec(float* q, int n_q_heads, float* k, int n_kv_heads, int head_dim,
+                           int n_tok, const int32_t* pos, float theta, dsb_workspace* ws,
+                           void* stream);
+
+/* KV write through batch_index ([QAIC] "Objective"; [DS4] batched-decode
+ * encoder commit).  For s < n_seq, j < tokens_per_seq, t = s*T + j:
+ *   K[batch_index[s]][h][pos[t]][:] = cvt(k[t][h][:]),  same for V,
+ * cvt = float32 -> cache dtype, round to nearest even.  Nothing else in the
+ * cache is written.  batch_index: host int32[n_seq], distinct, in
+ * [0, full_batch_size); pos: host int32[n_seq*T] in [0, ctx).  k, v: device
+ * float32 [n_tok][n_kv_heads][head_dim]. */
+dsb_status dsb_kv_scatter(const dsb_kv_cache* kv, const int32_t* batch_index, int n_seq,
+                          int tokens_per_seq, const int32_t* pos, const float* k, const float* v,
+                          dsb_workspace* ws, void* stream);
+
+/* Multi-sequence GQA decode attention ([DS4] multi-sequence decode attention
+ * commit; [PTO] live batch from seq_lens).  Sequence s (cache slot
+ * batch_index[s], KV length seq_lens[s] after this step's writes) has query
+ * rows t = s*T + j; token j sees keys 0 .. seq_lens[s]-T+j.  Query head h
+ * reads kv head h / (n_q_heads / n_kv_heads).  score = q.k / sqrt(head_dim);
+ * out = softmax(score) V.  Split-K: keys are cut into DSB_ATTN_CHUNK chunks,
+ * one partial (max, sum, acc) per chunk, merged in chunk order by a second
+ * kernel; no atomics, so row t is bitwise equal to a single-sequence call.
+ * q: device float32 [n_tok][n_q_heads][head_dim]; out: device float32, same
+ * shape.  seq_lens: host int32[n_seq], each in [T, ctx].  head_dim in
+ * {64, 128}; n_q_heads/n_kv_heads * T <= 64. */
+dsb_status dsb_attention_decode_multi(const float* q, int n_q_heads, const dsb_kv_cache* kv,
+                                      const int32_t* batch_index, int n_seq, int tokens_per_seq,
+                                      const int32_t* seq_lens, float* out, dsb_workspace* ws,
+                                      void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSB_H */

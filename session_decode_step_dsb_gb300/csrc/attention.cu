@@ -1,0 +1,339 @@
+// Multi-sequence GQA decode attention, split-K (flash-decode), sm_103a.
+//
+// What it computes (antirez/ds4 PR #530, "Batched decode: co-decode N live
+// sessions in one GPU pass", the multi-sequence decode attention commit: one
+// launch serves several sequences, each reading its own query rows and its own
+// cache and writing its own output rows; hw-native-sys/pypto-lib PR #841: the
+// live batch comes from the seq_lens descriptor).  For sequence s (cache slot
+// batch_index[s], seq_lens[s] keys after this step's writes), draft token j of
+// T (quic/efficient-transformers PR #1305, K+1 tokens per sequence) and query
+// head h (kv head g = h / G):
+//     score_k = q . K_k / sqrt(D)  for k <= seq_lens[s] - T + j
+//     out     = sum_k softmax(score)_k V_k
+//
+// GB300 design.  The ds4 page's kernel keeps every score of a sequence in one
+// shared buffer and gives up past ~31k compressed rows ("Known limitation");
+// here the keys of each (sequence, kv head) are cut into DSB_ATTN_CHUNK = 128
+// key chunks, so long contexts and b = 1 both fill the 152 SMs:
+//  * partial kernel, one CTA per (sequence, chunk, kv head): the V chunk is
+//    brought into shared memory by one 1-D TMA bulk copy (contiguous in the
+//    [F][Hkv][C][D] cache) while the CTA computes scores; thread k owns key k,
+//    holds its K row in registers (16-byte read-only loads) and dots it against
+//    the G*T query rows of the GQA group, which are read from shared memory by
+//    broadcast.  Every K/V byte is read once for all G*T query rows.  Per row
+//    it writes (max, sum of exp, sum of exp * V) for the chunk.
+//  * merge kernel, one warp per (token row, head): rescales the chunk partials
+//    by exp(m_c - max_c m_c) and adds them in chunk order.
+// No atomics and no inter-CTA waits; the chunking depends only on each
+// sequence's own length, so a sequence's rows are bitwise equal whether it runs
+// alone or inside a batch.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "dsb_kernels.h"
+#include "dsb_ptx.cuh"
+
+namespace dsbk {
+
+namespace {
+
+constexpr int kCh = 128;  // keys per chunk (DSB_ATTN_CHUNK)
+constexpr int kThreads = 128;
+constexpr int kRowGroup = 8;
+
+__device__ unsigned int g_err_attention = 0;
+
+template <typename T>
+struct Cvt;
+template <>
+struct Cvt<__half> {
+  static __device__ __forceinline__ float2 two(uint32_t w) { return __half22float2(*reinterpret_cast<__half2*>(&w)); }
+};
+template <>
+struct Cvt<__nv_bfloat16> {
+  static __device__ __forceinline__ float2 two(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w));
+  }
+};
+
+template <int D, typename T>
+__global__ void __launch_bounds__(kThreads) attention_partial_kernel(
+    const float* __restrict__ q, int n_q_heads, const T* __restrict__ kc, const T* __restrict__ vc, int n_kv_heads,
+    int ctx, const int32_t* __restrict__ batch_index, const int32_t* __restrict__ seq_lens,
+    const int32_t* __restrict__ chunk_off, int n_seq, int tps, int max_chunks, float scale,
+    float* __restrict__ partials) {
+  constexpr int NPAIR = D / 2;
+  constexpr int NPART = kThreads / NPAIR;
+  constexpr int KPP = kCh / NPART;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int w = blockIdx.x, g = blockIdx.y;
+  int lo = 0, hi = n_seq - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (chunk_off[mid] <= w)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int s = lo, c = w - chunk_off[s];
+  const int slot = batch_index[s], L = seq_lens[s];
+  const int key0 = c * kCh;
+  const int nkeys = min(kCh, L - key0);
+  const int G = n_q_heads / n_kv_heads, R = G * tps;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  T* Vs = reinterpret_cast<T*>(smem);                                   // [kCh][D]
+  float* qs = reinterpret_cast<float*>(smem + (size_t)kCh * D * sizeof(T));  // [R][D]
+  float* ps = qs + (size_t)R * D;                                        // [R][kCh]
+  float* ms = ps + (size_t)R * kCh;                                      // [R]
+  float* ls = ms + R;                                                    // [R]
+  float* red = ls + R;                                                   // [NPART-1][kRowGroup][D]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(red + (NPART - 1) * kRowGroup * D);
+
+  const size_t head_row0 = ((size_t)slot * n_kv_heads + g) * (size_t)ctx;  // cache row of key 0
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const uint32_t bytes = (uint32_t)nkeys * D * sizeof(T);
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(Vs, vc + (head_row0 + key0) * D, bytes, bar);
+  }
+  for (int idx = tid; idx < R * D; idx += kThreads) {
+    const int r = idx / D, d = idx - r * D;
+    const int j = r / G, gi = r - j * G;
+    qs[idx] = q[((size_t)(s * tps + j) * n_q_heads + g * G + gi) * D + d];
+  }
+  __syncthreads();
+
+  // ---- scores: thread tid owns key key0 + tid
+  {
+    uint4 kreg[D / 8];
+    if (tid < nkeys) {
+      const uint4* kp = reinterpret_cast<const uint4*>(kc + (head_row0 + key0 + tid) * D);
+#pragma unroll
+      for (int cc = 0; cc < D / 8; ++cc) kreg[cc] = ld_nc_v4(kp + cc);
+    } else {
+#pragma unroll
+      for (int cc = 0; cc < D / 8; ++cc) kreg[cc] = make_uint4(0, 0, 0, 0);
+    }
+    for (int r0 = 0; r0 < R; r0 += kRowGroup) {
+      float dot[kRowGroup];
+#pragma unroll
+      for (int r = 0; r < kRowGroup; ++r) dot[r] = 0.0f;
+#pragma unroll
+      for (int cc = 0; cc < D / 8; ++cc) {
+        float kf[8];
+        const float2 k01 = Cvt<T>::two(kreg[cc].x), k23 = Cvt<T>::two(kreg[cc].y);
+        const float2 k45 = Cvt<T>::two(kreg[cc].z), k67 = Cvt<T>::two(kreg[cc].w);
+        kf[0] = k01.x; kf[1] = k01.y; kf[2] = k23.x; kf[3] = k23.y;
+        kf[4] = k45.x; kf[5] = k45.y; kf[6] = k67.x; kf[7] = k67.y;
+#pragma unroll
+        for (int r = 0; r < kRowGroup; ++r) {
+          if (r0 + r < R) {
+            const float4 qa = *reinterpret_cast<const float4*>(qs + (size_t)(r0 + r) * D + cc * 8);
+            const float4 qb = *reinterpret_cast<const float4*>(qs + (size_t)(r0 + r) * D + cc * 8 + 4);
+            float a = dot[r];
+            a = __fmaf_rn(qa.x, kf[0], a); a = __fmaf_rn(qa.y, kf[1], a);
+            a = __fmaf_rn(qa.z, kf[2], a); a = __fmaf_rn(qa.w, kf[3], a);
+            a = __fmaf_rn(qb.x, kf[4], a); a = __fmaf_rn(qb.y, kf[5], a);
+            a = __fmaf_rn(qb.z, kf[6], a); a = __fmaf_rn(qb.w, kf[7], a);
+            dot[r] = a;
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kRowGroup; ++r) {
+        if (r0 + r < R) {
+          const int j = (r0 + r) / G;
+          const int vis = L - tps + j + 1;
+          ps[(size_t)(r0 + r) * kCh + tid] = (key0 + tid < vis) ? __fmul_rn(dot[r], scale) : -INFINITY;
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- chunk softmax statistics, one warp per row
+  for (int r = warp; r < R; r += kThreads / 32) {
+    float v[kCh / 32];
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kCh / 32; ++i) {
+      v[i] = ps[(size_t)r * kCh + lane + 32 * i];
+      m = fmaxf(m, v[i]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float l = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kCh / 32; ++i) {
+      const float p = (m == -INFINITY) ? 0.0f : expf(v[i] - m);
+      ps[(size_t)r * kCh + lane + 32 * i] = p;
+      l = __fadd_rn(l, p);
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, o));
+    if (lane == 0) {
+      ms[r] = m;
+      ls[r] = l;
+    }
+  }
+  const bool ok = mbar_wait(bar, 0);
+  if (!ok) g_err_attention = 1u;
+  __syncthreads();
+
+  // ---- P V: thread = (pair of dims, key part); parts added in order
+  const int pr = tid % NPAIR, part = tid / NPAIR;
+  for (int r0 = 0; r0 < R; r0 += kRowGroup) {
+    float a0[kRowGroup], a1[kRowGroup];
+#pragma unroll
+    for (int r = 0; r < kRowGroup; ++r) a0[r] = a1[r] = 0.0f;
+    for (int kk = 0; kk < KPP; ++kk) {
+      const int key = part * KPP + kk;
+      if (key < nkeys) {
+        const float2 vf = Cvt<T>::two(*reinterpret_cast<const uint32_t*>(Vs + (size_t)key * D + 2 * pr));
+#pragma unroll
+        for (int r = 0; r < kRowGroup; ++r) {
+          if (r0 + r < R) {
+            const float p = ps[(size_t)(r0 + r) * kCh + key];
+            a0[r] = __fmaf_rn(p, vf.x, a0[r]);
+            a1[r] = __fmaf_rn(p, vf.y, a1[r]);
+          }
+        }
+      }
+    }
+    if (part > 0) {
+#pragma unroll
+      for (int r = 0; r < kRowGroup; ++r) {
+        red[((part - 1) * kRowGroup + r) * D + 2 * pr] = a0[r];
+        red[((part - 1) * kRowGroup + r) * D + 2 * pr + 1] = a1[r];
+      }
+    }
+    __syncthreads();
+    if (part == 0) {
+#pragma unroll
+      for (int r = 0; r < kRowGroup; ++r) {
+        if (r0 + r < R) {
+          float x0 = a0[r], x1 = a1[r];
+#pragma unroll
+          for (int pp = 1; pp < NPART; ++pp) {
+            x0 = __fadd_rn(x0, red[((pp - 1) * kRowGroup + r) * D + 2 * pr]);
+            x1 = __fadd_rn(x1, red[((pp - 1) * kRowGroup + r) * D + 2 * pr + 1]);
+          }
+          const int j = (r0 + r) / G, gi = (r0 + r) - j * G;
+          const int t = s * tps + j, h = g * G + gi;
+          float* dst = partials + (((size_t)t * n_q_heads + h) * max_chunks + c) * (D + 2);
+          dst[2 + 2 * pr] = x0;
+          dst[3 + 2 * pr] = x1;
+          if (pr == 0) {
+            dst[0] = ms[r0 + r];
+            dst[1] = ls[r0 + r];
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) attention_merge_kernel(const float* __restrict__ partials, int n_q_heads,
+                                                              int tps, const int32_t* __restrict__ seq_lens,
+                                                              int max_chunks, int n_tok, float* __restrict__ out) {
+  const int wg = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wg >= n_tok * n_q_heads) return;
+  const int t = wg / n_q_heads, h = wg - t * n_q_heads;
+  const int s = t / tps, j = t - s * tps;
+  const int vis = seq_lens[s] - tps + j + 1;
+  const int nch = (vis + kCh - 1) / kCh;
+  const float* base = partials + ((size_t)t * n_q_heads + h) * max_chunks * (D + 2);
+  float M = -INFINITY;
+  for (int c = 0; c < nch; ++c) M = fmaxf(M, base[(size_t)c * (D + 2)]);
+  float Lsum = 0.0f;
+  float acc[D / 32];
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e) acc[e] = 0.0f;
+  for (int c = 0; c < nch; ++c) {
+    const float* pc = base + (size_t)c * (D + 2);
+    const float wgt = expf(pc[0] - M);
+    Lsum = __fmaf_rn(wgt, pc[1], Lsum);
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) acc[e] = __fmaf_rn(wgt, pc[2 + lane + 32 * e], acc[e]);
+  }
+  float* o = out + ((size_t)t * n_q_heads + h) * D;
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e) o[lane + 32 * e] = __fdiv_rn(acc[e], Lsum);
+}
+
+template <int D, typename T>
+size_t partial_smem(int R) {
+  constexpr int NPART = kThreads / (D / 2);
+  return (size_t)kCh * D * sizeof(T) + (size_t)R * D * 4 + (size_t)R * kCh * 4 + (size_t)2 * R * 4 +
+         (size_t)(NPART - 1) * kRowGroup * D * 4 + 16;
+}
+
+template <int D, typename T>
+cudaError_t launch_typed(const float* q, int n_q_heads, const void* kc, const void* vc, int n_kv_heads, int ctx,
+                         MetaView meta, int n_seq, int tps, int total_chunks, int max_chunks, float* partials,
+                         float* out, cudaStream_t st) {
+  const int R = (n_q_heads / n_kv_heads) * tps;
+  const size_t smem = partial_smem<D, T>(R);
+  auto kern = attention_partial_kernel<D, T>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const float scale = (float)(1.0 / sqrt((double)D));
+  kern<<<dim3((unsigned)total_chunks, (unsigned)n_kv_heads), kThreads, smem, st>>>(
+      q, n_q_heads, static_cast<const T*>(kc), static_cast<const T*>(vc), n_kv_heads, ctx, meta.batch_index,
+      meta.seq_lens, meta.chunk_off, n_seq, tps, max_chunks, scale, partials);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int n_tok = n_seq * tps;
+  const unsigned mgrid = (unsigned)((n_tok * n_q_heads + 3) / 4);
+  attention_merge_kernel<D><<<mgrid, 128, 0, st>>>(partials, n_q_heads, tps, meta.seq_lens, max_chunks, n_tok, out);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attention_partial_bytes(int n_tok, int n_q_heads, int head_dim, int ctx) {
+  const size_t max_chunks = (size_t)(ctx + kCh - 1) / kCh;
+  return (size_t)n_tok * n_q_heads * max_chunks * (head_dim + 2) * sizeof(float);
+}
+
+cudaError_t launch_attention_decode_multi(const float* q, int n_q_heads, const void* kc, const void* vc, int dtype,
+                                          int n_kv_heads, int ctx, int head_dim, MetaView meta, int n_seq,
+                                          int tokens_per_seq, int total_chunks, int max_chunks, float* partials,
+                                          float* out, cudaStream_t st) {
+  if (n_seq == 0) return cudaSuccess;
+  if (head_dim == 128) {
+    if (dtype == 0)
+      return launch_typed<128, __half>(q, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
+                                       total_chunks, max_chunks, partials, out, st);
+    return launch_typed<128, __nv_bfloat16>(q, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
+                                            total_chunks, max_chunks, partials, out, st);
+  }
+  if (head_dim == 64) {
+    if (dtype == 0)
+      return launch_typed<64, __half>(q, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
+                                      total_chunks, max_chunks, partials, out, st);
+    return launch_typed<64, __nv_bfloat16>(q, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
+                                           total_chunks, max_chunks, partials, out, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+unsigned int read_clear_error_attention() {
+  unsigned int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_attention, sizeof v) != cudaSuccess) return 0xFFFFFFFFu;
+  cudaMemcpyToSymbol(g_err_attention, &z, sizeof z);
+  return v;
+}
+
+}  // namespace dsbk

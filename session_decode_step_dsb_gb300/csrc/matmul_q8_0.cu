@@ -1,0 +1,317 @@
+// Narrow-batch q8_0 matmul for sm_103a.
+//
+// What it computes (antirez/ds4 PR #530, "Batched decode: co-decode N live
+// sessions in one GPU pass", section "Why it's worth it -- the narrow-batch
+// matmul", and the narrow-batch q8_0 matmul commit): for n_tok <= 16
+// pre-quantised q8_0 activation rows,
+//     y[t][r] = sum_i dW[r,i] * dX[t,i] * sum_k qW[r,i,k] * qX[t,i,k].
+// The page's point is that in decode the weights are the whole cost, so each
+// weight block must cross HBM once and serve every token.
+//
+// GB300 design (differs from the page's one-warp-per-row kernel):
+//  * A CTA owns 32 weight rows (lane = row) and a contiguous range of 8-block
+//    k-steps; its 4 warps take interleaved k-steps.  A k-step of one row is
+//    8 blocks = 272 bytes = 17 x 16 bytes, so every row chunk is 16-byte
+//    aligned whenever cols % 256 == 0.
+//  * Each warp streams its 32 row chunks with 1-D TMA bulk copies
+//    (cp.async.bulk, one 272-byte copy per lane) into a private NSTAGE-deep
+//    shared-memory ring guarded by mbarriers; no thread spends instructions on
+//    global loads of weights.  A lane reads its chunk back with 17 conflict-free
+//    16-byte shared loads (the 272-byte stride is an odd number of 16-byte
+//    bank groups) and unpacks the 34-byte blocks with funnel shifts.
+//  * Activation blocks of the CTA's k-range are unpacked once, at kernel start,
+//    into an aligned layout (32 code bytes + fp32 scale per block and token),
+//    so the inner loop reads them with warp-uniform (broadcast) 16-byte loads.
+//  * Block dots are __dp4a chains started from the bit pattern of 1.5 * 2^23:
+//    |isum| <= 32*127*127 < 2^22, so the int32 result read as a float is
+//    1.5*2^23 + isum exactly and one FADD converts it (no I2F).
+//  * When rows alone give too few CTAs, k is split over the CTAs of a thread
+//    block cluster (<= 8) and the partial sums are added through distributed
+//    shared memory in cluster-rank order.  No atomics; every reduction order
+//    depends only on (rows, cols) and the device's SM count, never on n_tok,
+//    so column t of an n_tok = k call is bitwise equal to the n_tok = 1 call.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "dsb_kernels.h"
+#include "dsb_ptx.cuh"
+
+namespace dsbk {
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRowsPerCta = 32;
+constexpr int kChunkBytes = 272;  // 8 blocks of 34 bytes
+constexpr int kStage = kRowsPerCta * kChunkBytes;
+constexpr int kNStage = 2;
+constexpr uint32_t kMagic = 0x4B400000u;  // bits of 12582912.0f = 1.5 * 2^23
+constexpr float kMagicF = 12582912.0f;
+
+__device__ unsigned int g_err_matmul = 0;
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));
+}
+
+struct Split {
+  int ks0, ks1;
+};
+
+__device__ __forceinline__ Split kstep_range(int nks, int S, int rank) {
+  // balanced contiguous split of nks k-steps over S CTAs
+  Split s;
+  s.ks0 = (int)(((long long)nks * rank) / S);
+  s.ks1 = (int)(((long long)nks * (rank + 1)) / S);
+  return s;
+}
+
+template <int NT, bool EMIT>
+__global__ void __launch_bounds__(kThreads, 2)
+    matmul_q8_0_narrow_kernel(const uint8_t* __restrict__ W, int rows, int nb, const uint8_t* __restrict__ xq,
+                              float* __restrict__ y, int32_t* __restrict__ isum_out) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int nks = nb >> 3;
+  const int S = gridDim.y;
+  const int rank = blockIdx.y;  // cluster dims (1, S, 1): rank within the cluster
+  const Split ksr = kstep_range(nks, S, rank);
+  const int kr = ksr.ks1 - ksr.ks0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row0 = blockIdx.x * kRowsPerCta;
+  const int row = row0 + lane;
+  const bool row_ok = row < rows;
+  const int rows_here = min(kRowsPerCta, rows - row0);
+  const size_t row_bytes = (size_t)nb * 34;
+
+  // shared layout: act codes | act scales | stages | barriers
+  uint32_t* act_q = reinterpret_cast<uint32_t*>(smem);                 // [kr*8][NT][8]
+  float* act_s = reinterpret_cast<float*>(act_q + (size_t)kr * 8 * NT * 8);  // [kr*8][NT]
+  uint8_t* stages = reinterpret_cast<uint8_t*>(act_s + (size_t)kr * 8 * NT);  // [kWarps][kNStage][kStage]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stages + (size_t)kWarps * kNStage * kStage);  // [kWarps][kNStage]
+  uint8_t* my_stages = stages + (size_t)warp * kNStage * kStage;
+  uint64_t* my_bars = bars + warp * kNStage;
+
+  if (lane == 0) {
+    for (int s = 0; s < kNStage; ++s) mbar_init(&my_bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  // k-steps of this warp: ks0 + warp + kWarps*m
+  const int n_mine = kr > warp ? (kr - warp + kWarps - 1) / kWarps : 0;
+  auto issue = [&](int m) {
+    const int ks = ksr.ks0 + warp + kWarps * m;
+    uint64_t* bar = &my_bars[m % kNStage];
+    uint8_t* dst = my_stages + (size_t)(m % kNStage) * kStage;
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(rows_here * kChunkBytes));
+    __syncwarp();
+    if (row_ok) bulk_g2s(dst + lane * kChunkBytes, W + (size_t)row * row_bytes + (size_t)ks * kChunkBytes, kChunkBytes, bar);
+  };
+  for (int m = 0; m < kNStage && m < n_mine; ++m) issue(m);
+
+  // Unpack the CTA's activation blocks [ks0*8, ks1*8) x NT into aligned form.
+  {
+    const int nblk = kr * 8;
+    for (int idx = threadIdx.x; idx < nblk * NT; idx += kThreads) {
+      const int b = idx / NT, t = idx - b * NT;
+      const long long g = (long long)t * nb + (long long)ksr.ks0 * 8 + b;  // global block index
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(xq + ((34 * g) & ~3LL));
+      uint32_t wv[9];
+#pragma unroll
+      for (int k = 0; k < 9; ++k) wv[k] = __ldg(src + k);
+      const bool odd = (g & 1) != 0;  // odd blocks start 2 bytes into a word
+      const uint32_t sh = odd ? 32u : 16u;
+      uint32_t* dq = act_q + ((size_t)b * NT + t) * 8;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) dq[k] = __funnelshift_rc(wv[k], wv[k + 1], sh);
+      act_s[(size_t)b * NT + t] = half_bits_to_float(odd ? (wv[0] >> 16) : wv[0]);
+    }
+  }
+  __syncthreads();
+
+  float acc[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
+  bool dead = false;
+
+  for (int m = 0; m < n_mine; ++m) {
+    const int ks = ksr.ks0 + warp + kWarps * m;
+    const int kl = ks - ksr.ks0;
+    uint64_t* bar = &my_bars[m % kNStage];
+    if (!dead) {
+      const bool ok = mbar_wait(bar, (uint32_t)((m / kNStage) & 1));
+      dead = __any_sync(0xffffffffu, !ok);  // warp-uniform
+      if (dead && lane == 0) g_err_matmul = 1u;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(my_stages + (size_t)(m % kNStage) * kStage + lane * kChunkBytes);
+    uint32_t w[68];
+#pragma unroll
+    for (int i = 0; i < 17; ++i) {
+      const uint4 v = src[i];
+      w[4 * i + 0] = v.x;
+      w[4 * i + 1] = v.y;
+      w[4 * i + 2] = v.z;
+      w[4 * i + 3] = v.w;
+    }
+    __syncwarp();
+    fence_proxy_async_smem();
+    if (!dead && m + kNStage < n_mine) issue(m + kNStage);
+
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      uint32_t q[8];
+      float dw;
+      if ((b & 1) == 0) {
+        const int base = (17 * b) / 2;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = __funnelshift_r(w[base + k], w[base + k + 1], 16);
+        dw = half_bits_to_float(w[base]);
+      } else {
+        const int base = (17 * b - 1) / 2;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = w[base + 1 + k];
+        dw = half_bits_to_float(w[base] >> 16);
+      }
+      const uint32_t* aq = act_q + ((size_t)(kl * 8 + b) * NT) * 8;
+      const float* as = act_s + (size_t)(kl * 8 + b) * NT;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const uint4 x0 = *reinterpret_cast<const uint4*>(aq + t * 8);
+        const uint4 x1 = *reinterpret_cast<const uint4*>(aq + t * 8 + 4);
+        int s = (int)kMagic;
+        s = __dp4a((int)q[0], (int)x0.x, s);
+        s = __dp4a((int)q[1], (int)x0.y, s);
+        s = __dp4a((int)q[2], (int)x0.z, s);
+        s = __dp4a((int)q[3], (int)x0.w, s);
+        s = __dp4a((int)q[4], (int)x1.x, s);
+        s = __dp4a((int)q[5], (int)x1.y, s);
+        s = __dp4a((int)q[6], (int)x1.z, s);
+        s = __dp4a((int)q[7], (int)x1.w, s);
+        if constexpr (EMIT) {
+          if (row_ok)
+            isum_out[((size_t)t * rows + row) * nb + (size_t)ks * 8 + b] = s - (int)kMagic;
+        } else {
+          const float f = __fsub_rn(__int_as_float(s), kMagicF);
+          acc[t] = __fmaf_rn(f, __fmul_rn(dw, as[t]), acc[t]);
+        }
+      }
+    }
+  }
+
+  if constexpr (!EMIT) {
+    // Intra-CTA: warp partials [kWarps][NT][32] summed in warp order, then the
+    // cluster's CTA sums added in rank order by rank 0.  The reduction buffers
+    // reuse the stage ring (every copy into it has been waited on).
+    __syncthreads();
+    float* red = reinterpret_cast<float*>(stages);
+    float* red_sum = red + kWarps * NT * 32;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) red[(warp * NT + t) * 32 + lane] = acc[t];
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < NT * 32; idx += kThreads) {
+      float v = red[idx];
+#pragma unroll
+      for (int w2 = 1; w2 < kWarps; ++w2) v = __fadd_rn(v, red[w2 * NT * 32 + idx]);
+      red_sum[idx] = v;
+    }
+    cluster_sync();
+    if (rank == 0) {
+      for (int idx = threadIdx.x; idx < NT * 32; idx += kThreads) {
+        float v = red_sum[idx];
+        for (int r = 1; r < S; ++r) v = __fadd_rn(v, ld_dsmem_f32(&red_sum[idx], (uint32_t)r));
+        const int t = idx >> 5, rr = row0 + (idx & 31);
+        if (rr < rows) y[(size_t)t * rows + rr] = v;
+      }
+    }
+    cluster_sync();
+  }
+}
+
+size_t smem_bytes(int kr, int nt) {
+  return (size_t)kr * 8 * nt * 36 + (size_t)kWarps * kNStage * kStage + (size_t)kWarps * kNStage * 8;
+}
+
+template <int NT, bool EMIT>
+cudaError_t launch_nt(const uint8_t* W, int rows, int nb, const uint8_t* xq, float* y, int32_t* isum, int S,
+                      size_t smem, cudaStream_t st) {
+  auto kern = matmul_q8_0_narrow_kernel<NT, EMIT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((rows + kRowsPerCta - 1) / kRowsPerCta), (unsigned)S, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)S;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, W, rows, nb, xq, y, isum);
+}
+
+template <bool EMIT>
+cudaError_t dispatch(int nt, const uint8_t* W, int rows, int nb, const uint8_t* xq, float* y, int32_t* isum, int S,
+                     size_t smem, cudaStream_t st) {
+  switch (nt) {
+#define DSB_CASE(N) \
+  case N:           \
+    return launch_nt<N, EMIT>(W, rows, nb, xq, y, isum, S, smem, st);
+    DSB_CASE(1) DSB_CASE(2) DSB_CASE(3) DSB_CASE(4) DSB_CASE(5) DSB_CASE(6) DSB_CASE(7) DSB_CASE(8)
+    DSB_CASE(9) DSB_CASE(10) DSB_CASE(11) DSB_CASE(12) DSB_CASE(13) DSB_CASE(14) DSB_CASE(15) DSB_CASE(16)
+#undef DSB_CASE
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+int matmul_split(int64_t rows, int64_t cols, int num_sms) {
+  // Depends on (rows, cols, SM count) only -- never on n_tok -- so that the
+  // summation order of every output is the same for every n_tok.
+  const int nks = (int)(cols / 256);
+  const int tiles = (int)((rows + kRowsPerCta - 1) / kRowsPerCta);
+  // activation shared memory at n_tok = 16: kr*8*16*36 bytes <= 36 KiB -> kr <= 8,
+  // which keeps two CTAs resident per SM next to the weight rings.
+  int s_smem = (nks + 7) / 8;
+  int s_fill = (2 * num_sms + tiles - 1) / tiles;
+  int S = s_smem > s_fill ? s_smem : s_fill;
+  if (S > nks) S = nks;
+  if (S > 8) S = 8;
+  if (S < 1) S = 1;
+  return S;
+}
+
+size_t matmul_smem_bytes(int64_t rows, int64_t cols, int n_tok, int num_sms) {
+  const int S = matmul_split(rows, cols, num_sms);
+  const int nks = (int)(cols / 256);
+  const int kr_max = (nks + S - 1) / S;
+  return smem_bytes(kr_max, n_tok);
+}
+
+cudaError_t launch_matmul_q8_0_narrow(const void* W, int64_t rows, int64_t cols, const void* xq, int n_tok,
+                                      float* y, int32_t* isum, int num_sms, cudaStream_t st) {
+  const int S = matmul_split(rows, cols, num_sms);
+  const size_t smem = matmul_smem_bytes(rows, cols, n_tok, num_sms);
+  const int nb = (int)(cols / 32);
+  if (isum)
+    return dispatch<true>(n_tok, static_cast<const uint8_t*>(W), (int)rows, nb, static_cast<const uint8_t*>(xq), y,
+                          isum, S, smem, st);
+  return dispatch<false>(n_tok, static_cast<const uint8_t*>(W), (int)rows, nb, static_cast<const uint8_t*>(xq), y,
+                         isum, S, smem, st);
+}
+
+unsigned int read_clear_error_matmul() {
+  unsigned int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_matmul, sizeof v) != cudaSuccess) return 0xFFFFFFFFu;
+  cudaMemcpyToSymbol(g_err_matmul, &z, sizeof z);
+  return v;
+}
+
+}  // namespace dsbk
