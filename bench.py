@@ -1,0 +1,519 @@
+#!/usr/bin/env python3
+"""Benchmark of the batched multi-session decode step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {dsb,reference}]
+                    [--workload llama-68m|qwen3-14b] [--b B] [--T T]
+
+Default workload: the llama-68m-shaped decode step (hidden 768, 12 heads,
+head_dim 64, 2 layers, FFN 3072, vocab 32000, fp16 KV cache of
+full_batch_size 8 at ctx 2048, seq_lens uniform in [128, 2048]) with a live
+batch of b = 8 sessions advancing one token each -- the largest point of the
+b in {1, 2, 4, 8} sweep the QAIC page runs on llama-68m.  Weights are random
+N(0, 0.02) q8_0 of that shape (no trained weights), drawn on the device and
+quantised by the library's own kernel.
+
+One "step" is one replay of the captured decode-step graph (every kernel of
+the hot path: embedding, RMSNorm+q8_0, narrow q8_0 matmuls, pos-vector RoPE,
+KV write through batch_index, split-K attention + merge, SiLU-gate, head).
+L2 is flushed (a 512 MiB write) before every timed step and each step is
+timed on its stream with CUDA events.  Prints ONE JSON line on rank 0.
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+on its own GPU (sessions are independent: weak scaling, no collective on the
+data path); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------- distributed
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _maybe_init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+        return dist
+    return None
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def _max_over_ranks(dist, value: float, device) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="dsb_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- workloads
+def _shape(name):
+    from session_decode_step_dsb_gb300 import workloads
+    return {"llama-68m": workloads.LLAMA68M, "qwen3-14b": workloads.QWEN3_14B}[name]
+
+
+def _make_model(ms, seed: int):
+    """Random N(0, 0.02) q8_0 weights of the shape, drawn on the device and
+    quantised by the library's kernel; caches N(0, 1) in the cache dtype."""
+    import torch
+    from session_decode_step_dsb_gb300 import dsb
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+
+    def q8(rows, cols):
+        out = torch.empty((rows, cols // 32 * 34), dtype=torch.uint8, device="cuda")
+        step = max(1, (1 << 26) // cols)   # bound the float32 staging to 256 MiB
+        for r0 in range(0, rows, step):
+            r1 = min(rows, r0 + step)
+            w = torch.randn((r1 - r0, cols), generator=g, device="cuda") * 0.02
+            dsb.quantize_q8_0(w, out[r0:r1])
+        return out
+
+    w = {"wqkv": [], "wo": [], "wgu": [], "wdown": [], "attn_norm": [], "ffn_norm": []}
+    for _ in range(ms.n_layers):
+        w["wqkv"].append(q8(ms.qkv_rows, ms.hidden))
+        w["wo"].append(q8(ms.hidden, ms.n_q_heads * ms.head_dim))
+        w["wgu"].append(q8(2 * ms.ffn, ms.hidden))
+        w["wdown"].append(q8(ms.hidden, ms.ffn))
+        w["attn_norm"].append(torch.ones(ms.hidden, device="cuda"))
+        w["ffn_norm"].append(torch.ones(ms.hidden, device="cuda"))
+    w["embed"] = q8(ms.vocab, ms.hidden)
+    w["head"] = q8(ms.vocab, ms.hidden)
+    w["final_norm"] = torch.ones(ms.hidden, device="cuda")
+    cdt = torch.float16 if ms.cache_dtype == "f16" else torch.bfloat16
+    kc, vc = [], []
+    for _ in range(ms.n_layers):
+        shape = (ms.full_batch_size, ms.n_kv_heads, ms.ctx, ms.head_dim)
+        kc.append(torch.randn(shape, generator=g, device="cuda").to(cdt).view(torch.int16))
+        vc.append(torch.randn(shape, generator=g, device="cuda").to(cdt).view(torch.int16))
+    model = dsb.DecodeModel(ms.hidden, ms.n_q_heads, ms.n_kv_heads, ms.head_dim, ms.ffn, ms.vocab, ms.n_layers, w,
+                            kc, vc, 0 if ms.cache_dtype == "f16" else 1, ms.eps, ms.theta)
+    return model
+
+
+def _meta(ms, b, T, seed):
+    from session_decode_step_dsb_gb300 import synth
+    sid = synth.stream_id
+    bi = synth.distinct_slots(seed, sid(synth.STREAM_META, 1), b, ms.full_batch_size)
+    lens = synth.uniform_int(seed, sid(synth.STREAM_META, 2), max(128, T), ms.ctx, b)
+    toks = synth.uniform_int(seed, sid(synth.STREAM_TOKENS, 0), 0, ms.vocab - 1, b * T)
+    return bi, lens, toks
+
+
+def step_bytes(ms, b, T, lens):
+    """Algorithmic HBM bytes of one step: every q8_0 weight byte once, plus the
+    K and V bytes attention must read (each kv head's rows once for its G*T
+    query rows), plus the embedding rows and the logits."""
+    nb = lambda cols: cols // 32 * 34
+    per_layer = (ms.qkv_rows * nb(ms.hidden) + ms.hidden * nb(ms.n_q_heads * ms.head_dim) +
+                 2 * ms.ffn * nb(ms.hidden) + ms.hidden * nb(ms.ffn))
+    weights = ms.n_layers * per_layer + ms.vocab * nb(ms.hidden)
+    e = 2
+    kv = ms.n_layers * int(np.sum(lens)) * ms.n_kv_heads * ms.head_dim * 2 * e
+    io = b * T * (nb(ms.hidden) + 4 * ms.vocab)
+    return weights + kv + io, weights, kv
+
+
+# ----------------------------------------------------------------- timing helpers
+def _time_device(fn, iters, flush, stream):
+    """Median and mean device time (ms) of fn(), L2 flushed before each call."""
+    import torch
+    ts = []
+    for _ in range(iters):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts), sum(ts) / len(ts), ts
+
+
+MATMUL_SHAPES = [(7168, 7168), (18432, 7168), (129280, 7168)]
+MATMUL_NTOK = [1, 2, 3, 4, 8, 16]
+
+
+def matmul_sweep(flush, stream, peak, iters=5):
+    """Narrow q8_0 matmul GB/s on the DeepSeek-class dense-stage shapes at
+    every n_tok the method targets (algorithmic bytes: weights once + q8_0
+    activations + float32 outputs)."""
+    import torch
+    from session_decode_step_dsb_gb300 import dsb
+    out = []
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1234)
+    for rows, cols in MATMUL_SHAPES:
+        w = torch.empty((rows, cols // 32 * 34), dtype=torch.uint8, device="cuda")
+        step = max(1, (1 << 26) // cols)
+        for r0 in range(0, rows, step):
+            r1 = min(rows, r0 + step)
+            dsb.quantize_q8_0(torch.randn((r1 - r0, cols), generator=g, device="cuda") * 0.02, w[r0:r1])
+        x = dsb.quantize_q8_0(torch.randn((16, cols), generator=g, device="cuda"))
+        for nt in MATMUL_NTOK:
+            xs = x[:nt].contiguous()
+            y = torch.empty((nt, rows), device="cuda")
+            for _ in range(2):
+                dsb.matmul_q8_0_narrow(w, rows, cols, xs, nt, y)
+            med, mean, _ = _time_device(lambda: dsb.matmul_q8_0_narrow(w, rows, cols, xs, nt, y), iters, flush, stream)
+            byts = 34 * rows * (cols // 32) + 34 * nt * (cols // 32) + 4 * nt * rows
+            gbs = byts / (med * 1e-3) / 1e9
+            out.append({"rows": rows, "cols": cols, "n_tok": nt, "us": round(med * 1e3, 2), "gbs": round(gbs, 1),
+                        "frac": round(gbs / peak, 4)})
+        del w, x
+    return out
+
+
+# ----------------------------------------------------------------- dsb arm
+def run_dsb(args):
+    import torch
+    from session_decode_step_dsb_gb300 import dsb
+    world, rank, local = _dist_env()
+    torch.cuda.set_device(local)
+    dist = _maybe_init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    ms = _shape(args.workload)
+    b, T = args.b, args.T
+    peak, peak_kind = _peaks()
+
+    model = _make_model(ms, seed=1000 + rank)
+    bi, lens, toks = _meta(ms, b, T, seed=7 + rank)
+    n_tok = b * T
+    ws = model.workspace(max(n_tok, 8))
+    logits = torch.empty((n_tok, ms.vocab), dtype=torch.float32, device=dev)
+    graph = model.graph(b, T, logits, ws)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    step = lambda: graph.launch(toks, bi, lens)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    dsb.device_error()
+
+    # ---- timed region: K steps, each after an L2 flush, device-timed
+    _barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        med, mean, ts = _time_device(step, args.steps, flush, stream)
+    torch.cuda.synchronize()
+    _barrier(dist)
+    clocks = clk.summary()
+    ms_step = _max_over_ranks(dist, mean, dev)
+    dsb.device_error()
+
+    # ---- b sweep (same model, fresh graphs), tokens/s per b
+    sweep = {}
+    if world == 1 and args.workload == "llama-68m" and T == 1:
+        for bb in (1, 2, 4, 8):
+            bi2, lens2, toks2 = _meta(ms, bb, 1, seed=7)
+            lg = torch.empty((bb, ms.vocab), dtype=torch.float32, device=dev)
+            g2 = model.graph(bb, 1, lg, ws)
+            for _ in range(3):
+                g2.launch(toks2, bi2, lens2)
+            m2, mean2, _ = _time_device(lambda: g2.launch(toks2, bi2, lens2), 20, flush, stream)
+            sweep[str(bb)] = {"ms_per_step": round(mean2, 4), "tokens_per_s": round(bb / (mean2 * 1e-3), 1)}
+            g2.close()
+
+    # ---- dominant kernel roofline: the narrow q8_0 matmul.  Its launches in
+    # the step (the workload's own matrices at n_tok = b*T) are timed one by
+    # one with CUDA events on the launching stream, L2 flushed before each.
+    nbk = lambda cols: cols // 32 * 34
+    mats = [(ms.qkv_rows, ms.hidden, model.w["wqkv"][0]), (ms.hidden, ms.n_q_heads * ms.head_dim, model.w["wo"][0]),
+            (2 * ms.ffn, ms.hidden, model.w["wgu"][0]), (ms.hidden, ms.ffn, model.w["wdown"][0]),
+            (ms.vocab, ms.hidden, model.w["head"])]
+    tot_bytes = 0.0
+    tot_ms = 0.0
+    per_kernel = []
+    nt = min(n_tok, 16)
+    for rows, cols, wmat in mats:
+        x = dsb.quantize_q8_0(torch.randn((nt, cols), device=dev))
+        y = torch.empty((nt, rows), device=dev)
+        for _ in range(2):
+            dsb.matmul_q8_0_narrow(wmat, rows, cols, x, nt, y)
+        m_, mean_, _ = _time_device(lambda: dsb.matmul_q8_0_narrow(wmat, rows, cols, x, nt, y), 10, flush, stream)
+        byts = rows * nbk(cols) + nt * nbk(cols) + 4 * nt * rows
+        reps = ms.n_layers if rows != ms.vocab else 1
+        tot_bytes += byts * reps
+        tot_ms += mean_ * reps
+        per_kernel.append({"rows": rows, "cols": cols, "n_tok": nt, "us": round(mean_ * 1e3, 2),
+                           "gbs": round(byts / (mean_ * 1e-3) / 1e9, 1)})
+    achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
+    traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            traffic = json.load(f).get(f"{args.workload}:b{b}:T{T}")
+    except Exception:
+        traffic = None
+
+    sweep_mm = matmul_sweep(flush, stream, peak) if (world == 1 and not args.no_matmul_sweep) else []
+
+    # ---- end to end through the C ABI with host buffers: token ids, slots
+    # and lengths from host arrays (staged by the library), logits copied back
+    # to pinned host memory, every step inside the timed region.
+    host_logits = torch.empty((n_tok, ms.vocab), dtype=torch.float32, pin_memory=True)
+    e2e_steps = max(10, min(args.steps, 100))
+    for _ in range(3):
+        graph.launch(toks, bi, lens)
+        host_logits.copy_(logits, non_blocking=True)
+    torch.cuda.synchronize()
+    _barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        graph.launch(toks, bi, lens)
+        host_logits.copy_(logits, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_s = _max_over_ranks(dist, e2e_s, dev)
+    meta_words = 2 * n_tok + 3 * b + 1
+    e2e = {"value": round(world * n_tok / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": 4 * meta_words,
+           "d2h_bytes_per_step": 4 * n_tok * ms.vocab, "steps": e2e_steps,
+           "note": "host int32 token ids/slots/seq_lens staged by the library; logits copied to pinned host"}
+
+    # ---- CPU baseline: the oracle as it stands, bounded sample, rank 0 only
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(ms, b, T, budget_s=args.cpu_budget)
+
+    graph.close()
+    total_bytes, wbytes, kvbytes = step_bytes(ms, b, T, lens)
+    value = world * n_tok / (ms_step * 1e-3)
+    if rank == 0:
+        line = {
+            "metric": "decode-step tokens/s and q8_0 narrow-matmul HBM GB/s (% of peak), n_tok=1..16",
+            "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8xint8->int32 dot (q8_0), f32 accumulate; f16 KV",
+            "data": "synthetic (seeded random weights/caches of the workload's shapes; no trained weights)",
+            "config": {"workload": ms.name, "b": b, "tokens_per_seq": T, "n_tok": n_tok,
+                       "full_batch_size": ms.full_batch_size, "ctx": ms.ctx, "seq_lens": [int(v) for v in lens],
+                       "layers": ms.n_layers, "hidden": ms.hidden, "vocab": ms.vocab,
+                       "l2": "flushed (512 MiB write) before every timed step", "parallelism": f"replicas x{world}",
+                       "step_bytes": total_bytes, "weight_bytes": wbytes, "kv_bytes": kvbytes},
+            "step_roofline": {"bytes": total_bytes, "achieved_gbs": round(total_bytes / (ms_step * 1e-3) / 1e9, 1),
+                              "peak_gbs": peak, "frac": round(total_bytes / (ms_step * 1e-3) / 1e9 / peak, 4)},
+            "roofline": {"kernel": "matmul_q8_0_narrow_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+                         "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "peak_kind": f"{peak_kind} hbm_gbs", "launches": per_kernel},
+            "b_sweep": sweep,
+            "matmul_q8_0_narrow": sweep_mm,
+            "e2e": e2e,
+            "gpu_launches": None,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        line["gpu_launches"] = args.steps * launches_per_step(ms)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def launches_per_step(ms) -> int:
+    """Kernels of one step: embed + per layer (rmsnorm-q8, QKV, rope, KV write,
+    attention partial + merge, quantise, O, rmsnorm-q8, gate|up, silu-q8,
+    down) + final rmsnorm-q8 + head."""
+    return 1 + 12 * ms.n_layers + 2
+
+
+# ----------------------------------------------------------------- CPU oracle
+def _oracle_model(ms, seed):
+    from oracle import q8_0 as oq
+    from session_decode_step_dsb_gb300 import synth
+    sid = synth.stream_id
+    w = {"wqkv": [], "wo": [], "wgu": [], "wdown": []}
+    for l in range(ms.n_layers):
+        w["wqkv"].append(oq.quantize_rows(synth.normal_rows(seed, sid(synth.STREAM_W, 10 * l), ms.qkv_rows, ms.hidden, 0.02)))
+        w["wo"].append(oq.quantize_rows(synth.normal_rows(seed, sid(synth.STREAM_W, 10 * l + 1), ms.hidden, ms.n_q_heads * ms.head_dim, 0.02)))
+        w["wgu"].append(oq.quantize_rows(synth.normal_rows(seed, sid(synth.STREAM_W, 10 * l + 2), 2 * ms.ffn, ms.hidden, 0.02)))
+        w["wdown"].append(oq.quantize_rows(synth.normal_rows(seed, sid(synth.STREAM_W, 10 * l + 3), ms.hidden, ms.ffn, 0.02)))
+    w["head"] = oq.quantize_rows(synth.normal_rows(seed, sid(synth.STREAM_W, 999_000), ms.vocab, ms.hidden, 0.02))
+    w["embed"] = oq.quantize_rows(synth.normal_rows(seed, sid(synth.STREAM_EMBED, 0), ms.vocab, ms.hidden, 0.02))
+    w["attn_norm"] = [np.ones(ms.hidden, np.float32)] * ms.n_layers
+    w["ffn_norm"] = [np.ones(ms.hidden, np.float32)] * ms.n_layers
+    w["final_norm"] = np.ones(ms.hidden, np.float32)
+    dims = (ms.full_batch_size, ms.n_kv_heads, ms.ctx, ms.head_dim)
+    kc = [synth.cache_bits(seed, sid(synth.STREAM_KCACHE, l), dims, ms.cache_dtype) for l in range(ms.n_layers)]
+    vc = [synth.cache_bits(seed, sid(synth.STREAM_VCACHE, l), dims, ms.cache_dtype) for l in range(ms.n_layers)]
+    return w, kc, vc
+
+
+def cpu_baseline(ms, b, T, budget_s=20.0):
+    """The oracle's decode step (numpy, float64) timed on the host: one
+    sequence of the b-sequence batch per sample (a bounded sample of the same
+    workload), repeated until ~budget_s of CPU work."""
+    from oracle import step as ostep
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    w, kc, vc = _oracle_model(ms, seed=0)
+    bi, lens, toks = _meta(ms, b, T, seed=7)
+    shape = ostep.Shape(ms.hidden, ms.n_q_heads, ms.n_kv_heads, ms.head_dim, ms.ffn, ms.vocab, ms.n_layers, ms.eps,
+                        ms.theta)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        s = n % b
+        ostep.decode_step(shape, w, kc, vc, ms.cache_dtype, toks[s * T:(s + 1) * T], bi[s:s + 1], T, lens[s:s + 1])
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(n * T / dt, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} single-sequence steps (1 of the {b} sessions each, {T} token(s)) of the {ms.name} "
+                      f"workload, float64 numpy, {dt:.1f} s"}
+
+
+def run_reference(args):
+    """The oracle timed as the reference arm: each step is one single-sequence
+    oracle decode step of the workload (a bounded sample of the b-sequence
+    step), on the host cores."""
+    world, rank, _ = _dist_env()
+    if rank != 0:
+        return
+    from oracle import step as ostep
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    ms = _shape(args.workload)
+    b, T = args.b, args.T
+    w, kc, vc = _oracle_model(ms, seed=0)
+    bi, lens, toks = _meta(ms, b, T, seed=7)
+    shape = ostep.Shape(ms.hidden, ms.n_q_heads, ms.n_kv_heads, ms.head_dim, ms.ffn, ms.vocab, ms.n_layers, ms.eps,
+                        ms.theta)
+
+    def one(i):
+        s = i % b
+        ostep.decode_step(shape, w, kc, vc, ms.cache_dtype, toks[s * T:(s + 1) * T], bi[s:s + 1], T, lens[s:s + 1])
+
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(i)
+    dt = time.perf_counter() - t0
+    value = args.steps * T / dt
+    line = {"impl": "reference", "metric": "decode-step tokens/s and q8_0 narrow-matmul HBM GB/s (% of peak), n_tok=1..16",
+            "value": round(value, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+            "config": {"workload": ms.name, "b": b, "tokens_per_seq": T,
+                       "sample": f"one of the {b} sessions per step ({T} token(s))"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} single-sequence oracle steps of the {ms.name} workload"},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["dsb", "reference"], default="dsb")
+    ap.add_argument("--workload", choices=["llama-68m", "qwen3-14b"], default="llama-68m")
+    ap.add_argument("--b", type=int, default=8)
+    ap.add_argument("--T", type=int, default=1)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-matmul-sweep", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_dsb(args)
+
+
+if __name__ == "__main__":
+    main()

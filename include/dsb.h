@@ -189,6 +189,71 @@ dsb_status dsb_attention_decode_multi(const float* q, int n_q_heads, const dsb_k
                                       const int32_t* seq_lens, float* out, dsb_workspace* ws,
                                       void* stream);
 
+/* ---- the whole decode step -------------------------------------------------
+ * A llama-style pre-norm decoder driven through the kernels above, one pass
+ * for all live sessions ([DS4] "What" and "Design note": dense stages batched
+ * with n_tokens = n_seqs, KV append and attention per sequence; [QAIC]
+ * "Objective": cache slots addressed by batch_index).  Per layer:
+ *   x = q8(rmsnorm(h)); [q|k|v] = Wqkv x; rope(q, k, pos); KV write;
+ *   a = attention; h += Wo q8(a); x = q8(rmsnorm(h)); [g|u] = Wgu x;
+ *   h += Wdown q8(silu(g) u)
+ * then logits = Whead q8(rmsnorm(h)).  Token row t = s*T + j of sequence s
+ * sits at position seq_lens[s] - T + j.  Embedding, head and every matrix are
+ * q8_0; norms are float32 weights; the step's float32 activations live in the
+ * workspace. */
+typedef struct {
+  int32_t hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, n_layers;
+  float rms_eps;    /* e.g. 1e-6 */
+  float rope_theta; /* e.g. 10000 */
+} dsb_model_shape;
+
+typedef struct {
+  dsb_q8_0_mat wqkv;      /* rows (Hq + 2 Hkv) * D (q rows, then k, then v), cols hidden */
+  dsb_q8_0_mat wo;        /* rows hidden, cols Hq * D */
+  dsb_q8_0_mat wgu;       /* rows 2 * ffn (gate rows, then up rows), cols hidden */
+  dsb_q8_0_mat wdown;     /* rows hidden, cols ffn */
+  const float* attn_norm; /* device [hidden] */
+  const float* ffn_norm;  /* device [hidden] */
+  dsb_kv_cache kv;        /* this layer's retained cache */
+} dsb_layer;
+
+typedef struct {
+  dsb_model_shape shape;
+  const void* embed;        /* device q8_0 [vocab][hidden] */
+  const dsb_layer* layers;  /* HOST array [n_layers], read during the call */
+  const float* final_norm;  /* device [hidden] */
+  dsb_q8_0_mat head;        /* rows vocab, cols hidden */
+} dsb_model;
+
+/* Device bytes a workspace needs for decode steps of up to max_tokens token
+ * rows against caches of length ctx (activations + attention partials +
+ * staged metadata).  0 if an argument is out of range. */
+size_t dsb_step_workspace_bytes(const dsb_model_shape* shape, int max_tokens, int ctx);
+
+/* One batched decode step.  token_ids: host int32[n_seq*T] in [0, vocab);
+ * batch_index: host int32[n_seq], distinct; seq_lens: host int32[n_seq] in
+ * [T, ctx] (KV length after this step).  Writes the step's K/V rows into each
+ * layer's cache and logits (device float32 [n_seq*T][vocab]).  Shapes must
+ * satisfy hidden, Hq*D and ffn % 256 == 0, head_dim in {64, 128}. */
+dsb_status dsb_decode_step(const dsb_model* model, const int32_t* token_ids, const int32_t* batch_index, int n_seq,
+                           int tokens_per_seq, const int32_t* seq_lens, float* logits, dsb_workspace* ws,
+                           void* stream);
+
+/* The same step captured once into a CUDA graph for a fixed (n_seq, T) and
+ * replayed.  The graph owns a pinned copy of the step metadata that its first
+ * node copies to the device, so a replay serves new token ids, slots and
+ * seq_lens without re-capture; the attention kernel reads its work count on the
+ * device.  The model, logits and workspace must stay valid for the graph's
+ * lifetime; one graph per workspace at a time. */
+typedef struct dsb_step_graph dsb_step_graph;
+dsb_status dsb_step_graph_create(const dsb_model* model, int n_seq, int tokens_per_seq, float* logits,
+                                 dsb_workspace* ws, void* stream, dsb_step_graph** out);
+/* Validates and stages the metadata (waiting, bounded, for the previous
+ * replay's metadata copy when it changes), then launches the graph. */
+dsb_status dsb_step_graph_launch(dsb_step_graph* g, const int32_t* token_ids, const int32_t* batch_index,
+                                 const int32_t* seq_lens, void* stream);
+dsb_status dsb_step_graph_destroy(dsb_step_graph* g);
+
 #ifdef __cplusplus
 }
 #endif

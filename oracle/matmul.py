@@ -20,6 +20,9 @@ from . import q8_0
 ISUM_BOUND = 32 * 127 * 127
 
 
+ROW_CHUNK = 4096  # output rows evaluated per pass (memory bound only; rows are independent)
+
+
 def block_dots(w_blocks: np.ndarray, x_blocks: np.ndarray, rows=None) -> np.ndarray:
     """int64 ``isum[n_tok, R', nb]`` for weight rows ``rows`` (default all)."""
     qw, _ = q8_0.unpack(w_blocks)
@@ -28,9 +31,12 @@ def block_dots(w_blocks: np.ndarray, x_blocks: np.ndarray, rows=None) -> np.ndar
         qw = qw[np.asarray(rows)]
     if qw.shape[1] != qx.shape[1]:
         raise ValueError("weight and activation rows have different block counts")
-    isum = np.einsum("rik,tik->tri", qw.astype(np.int64), qx.astype(np.int64))
-    assert np.all(np.abs(isum) <= ISUM_BOUND)
-    return isum
+    qx64 = qx.astype(np.int64)
+    out = np.empty((qx.shape[0], qw.shape[0], qw.shape[1]), dtype=np.int64)
+    for r0 in range(0, qw.shape[0], ROW_CHUNK):
+        out[:, r0:r0 + ROW_CHUNK] = np.einsum("rik,tik->tri", qw[r0:r0 + ROW_CHUNK].astype(np.int64), qx64)
+    assert np.all(np.abs(out) <= ISUM_BOUND)
+    return out
 
 
 def matmul_q8_0(w_blocks: np.ndarray, x_blocks: np.ndarray, rows=None) -> np.ndarray:
@@ -39,7 +45,13 @@ def matmul_q8_0(w_blocks: np.ndarray, x_blocks: np.ndarray, rows=None) -> np.nda
     _, dw = q8_0.unpack(w_blocks)
     _, dx = q8_0.unpack(x_blocks)
     if rows is not None:
-        dw = dw[np.asarray(rows)]
-    isum = block_dots(w_blocks, x_blocks, rows).astype(np.float64)
-    scale = dx.astype(np.float64)[:, None, :] * dw.astype(np.float64)[None, :, :]
-    return np.sum(scale * isum, axis=2)
+        rows = np.asarray(rows)
+        dw = dw[rows]
+        w_blocks = np.asarray(w_blocks)[rows]
+    y = np.empty((dx.shape[0], dw.shape[0]), dtype=np.float64)
+    dx64 = dx.astype(np.float64)
+    for r0 in range(0, dw.shape[0], ROW_CHUNK):
+        isum = block_dots(w_blocks[r0:r0 + ROW_CHUNK], x_blocks).astype(np.float64)
+        scale = dx64[:, None, :] * dw[r0:r0 + ROW_CHUNK].astype(np.float64)[None, :, :]
+        y[:, r0:r0 + ROW_CHUNK] = np.sum(scale * isum, axis=2)
+    return y

@@ -61,7 +61,8 @@ struct Cvt<__nv_bfloat16> {
 
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
-    const float* __restrict__ q, int n_q_heads, const T* __restrict__ kc, const T* __restrict__ vc, int n_kv_heads,
+    const float* __restrict__ q, long long q_stride, int n_q_heads, const T* __restrict__ kc, const T* __restrict__ vc,
+    int n_kv_heads,
     int ctx, const int32_t* __restrict__ batch_index, const int32_t* __restrict__ seq_lens,
     const int32_t* __restrict__ chunk_off, int n_seq, int tps, int max_chunks, float scale,
     float* __restrict__ partials) {
@@ -69,7 +70,27 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
   constexpr int NPART = kThreads / NPAIR;
   constexpr int KPP = kCh / NPART;
   extern __shared__ __align__(128) uint8_t smem[];
-  const int w = blockIdx.x, g = blockIdx.y;
+  const int G = n_q_heads / n_kv_heads, R = G * tps;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  T* Vs = reinterpret_cast<T*>(smem);                                        // [kCh][D]
+  float* qs = reinterpret_cast<float*>(smem + (size_t)kCh * D * sizeof(T));  // [R][D]
+  float* ps = qs + (size_t)R * D;                                            // [R][kCh]
+  float* ms = ps + (size_t)R * kCh;                                          // [R]
+  float* ls = ms + R;                                                        // [R]
+  float* red = ls + R;                                                       // [NPART-1][kRowGroup][D]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(red + (NPART - 1) * kRowGroup * D);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+
+  // Persistent loop over work items (chunk, kv head); the item count comes
+  // from the device metadata, so a captured launch serves any seq_lens.
+  const int total_items = chunk_off[n_seq] * n_kv_heads;
+  uint32_t phase = 0;
+  for (int item = blockIdx.x; item < total_items; item += gridDim.x, phase ^= 1u) {
+  const int w = item / n_kv_heads, g = item - w * n_kv_heads;
   int lo = 0, hi = n_seq - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -82,23 +103,9 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
   const int slot = batch_index[s], L = seq_lens[s];
   const int key0 = c * kCh;
   const int nkeys = min(kCh, L - key0);
-  const int G = n_q_heads / n_kv_heads, R = G * tps;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  T* Vs = reinterpret_cast<T*>(smem);                                   // [kCh][D]
-  float* qs = reinterpret_cast<float*>(smem + (size_t)kCh * D * sizeof(T));  // [R][D]
-  float* ps = qs + (size_t)R * D;                                        // [R][kCh]
-  float* ms = ps + (size_t)R * kCh;                                      // [R]
-  float* ls = ms + R;                                                    // [R]
-  float* red = ls + R;                                                   // [NPART-1][kRowGroup][D]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(red + (NPART - 1) * kRowGroup * D);
 
   const size_t head_row0 = ((size_t)slot * n_kv_heads + g) * (size_t)ctx;  // cache row of key 0
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
+  __syncthreads();  // the previous item is done with every shared buffer
   if (tid == 0) {
     const uint32_t bytes = (uint32_t)nkeys * D * sizeof(T);
     mbar_arrive_expect_tx(bar, bytes);
@@ -107,7 +114,7 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
   for (int idx = tid; idx < R * D; idx += kThreads) {
     const int r = idx / D, d = idx - r * D;
     const int j = r / G, gi = r - j * G;
-    qs[idx] = q[((size_t)(s * tps + j) * n_q_heads + g * G + gi) * D + d];
+    qs[idx] = q[(size_t)(s * tps + j) * q_stride + (size_t)(g * G + gi) * D + d];
   }
   __syncthreads();
 
@@ -184,7 +191,7 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
       ls[r] = l;
     }
   }
-  const bool ok = mbar_wait(bar, 0);
+  const bool ok = mbar_wait(bar, phase);
   if (!ok) g_err_attention = 1u;
   __syncthreads();
 
@@ -240,6 +247,7 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
     }
     __syncthreads();
   }
+  }  // work items
 }
 
 template <int D>
@@ -280,8 +288,9 @@ size_t partial_smem(int R) {
 }
 
 template <int D, typename T>
-cudaError_t launch_typed(const float* q, int n_q_heads, const void* kc, const void* vc, int n_kv_heads, int ctx,
-                         MetaView meta, int n_seq, int tps, int total_chunks, int max_chunks, float* partials,
+cudaError_t launch_typed(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc,
+                         int n_kv_heads, int ctx,
+                         MetaView meta, int n_seq, int tps, long long max_items, int max_chunks, float* partials,
                          float* out, cudaStream_t st) {
   const int R = (n_q_heads / n_kv_heads) * tps;
   const size_t smem = partial_smem<D, T>(R);
@@ -289,13 +298,31 @@ cudaError_t launch_typed(const float* q, int n_q_heads, const void* kc, const vo
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const float scale = (float)(1.0 / sqrt((double)D));
-  kern<<<dim3((unsigned)total_chunks, (unsigned)n_kv_heads), kThreads, smem, st>>>(
-      q, n_q_heads, static_cast<const T*>(kc), static_cast<const T*>(vc), n_kv_heads, ctx, meta.batch_index,
+  // Persistent grid: as many CTAs as fit at once, capped by the item count.
+  static int resident = 0;
+  static size_t resident_smem = 0;
+  if (resident == 0 || resident_smem != smem) {
+    int per_sm = 0, dev = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    resident = (per_sm > 0 ? per_sm : 1) * sms;
+    resident_smem = smem;
+  }
+  const long long items = (long long)max_items;
+  const unsigned grid = (unsigned)(items < resident ? (items > 0 ? items : 1) : resident);
+  if (dry_run()) return cudaSuccess;
+  kern<<<grid, kThreads, smem, st>>>(
+      q, q_stride, n_q_heads, static_cast<const T*>(kc), static_cast<const T*>(vc), n_kv_heads, ctx, meta.batch_index,
       meta.seq_lens, meta.chunk_off, n_seq, tps, max_chunks, scale, partials);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int n_tok = n_seq * tps;
   const unsigned mgrid = (unsigned)((n_tok * n_q_heads + 3) / 4);
+  if (dry_run()) return cudaSuccess;
   attention_merge_kernel<D><<<mgrid, 128, 0, st>>>(partials, n_q_heads, tps, meta.seq_lens, max_chunks, n_tok, out);
   return cudaGetLastError();
 }
@@ -307,24 +334,25 @@ size_t attention_partial_bytes(int n_tok, int n_q_heads, int head_dim, int ctx) 
   return (size_t)n_tok * n_q_heads * max_chunks * (head_dim + 2) * sizeof(float);
 }
 
-cudaError_t launch_attention_decode_multi(const float* q, int n_q_heads, const void* kc, const void* vc, int dtype,
+cudaError_t launch_attention_decode_multi(const float* q, long long q_stride, int n_q_heads, const void* kc,
+                                          const void* vc, int dtype,
                                           int n_kv_heads, int ctx, int head_dim, MetaView meta, int n_seq,
-                                          int tokens_per_seq, int total_chunks, int max_chunks, float* partials,
+                                          int tokens_per_seq, long long max_items, int max_chunks, float* partials,
                                           float* out, cudaStream_t st) {
   if (n_seq == 0) return cudaSuccess;
   if (head_dim == 128) {
     if (dtype == 0)
-      return launch_typed<128, __half>(q, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
-                                       total_chunks, max_chunks, partials, out, st);
-    return launch_typed<128, __nv_bfloat16>(q, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
-                                            total_chunks, max_chunks, partials, out, st);
+      return launch_typed<128, __half>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
+                                       max_items, max_chunks, partials, out, st);
+    return launch_typed<128, __nv_bfloat16>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
+                                            max_items, max_chunks, partials, out, st);
   }
   if (head_dim == 64) {
     if (dtype == 0)
-      return launch_typed<64, __half>(q, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
-                                      total_chunks, max_chunks, partials, out, st);
-    return launch_typed<64, __nv_bfloat16>(q, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
-                                           total_chunks, max_chunks, partials, out, st);
+      return launch_typed<64, __half>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
+                                      max_items, max_chunks, partials, out, st);
+    return launch_typed<64, __nv_bfloat16>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
+                                           max_items, max_chunks, partials, out, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -270,7 +270,8 @@ static dsb_status matmul_common(const dsb_q8_0_mat* w, const void* xq, int n_tok
     const int nt = std::min(DSB_NARROW_MAX, n_tok - t0);
     cudaError_t e = dsbk::launch_matmul_q8_0_narrow(
         w->blocks, w->rows, w->cols, static_cast<const char*>(xq) + (size_t)t0 * blk_row, nt,
-        y ? y + (size_t)t0 * w->rows : nullptr, isum ? isum + (size_t)t0 * w->rows * (w->cols / 32) : nullptr,
+        y ? y + (size_t)t0 * w->rows : nullptr, nullptr,
+        isum ? isum + (size_t)t0 * w->rows * (w->cols / 32) : nullptr,
         di.sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "matmul_q8_0 launch");
   }
@@ -312,7 +313,8 @@ dsb_status dsb_rope_posvec(float* q, int n_q_heads, float* k, int n_kv_heads, in
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   dsb_status s = stage(ws, words, st, &dev);
   if (s != DSB_OK) return s;
-  cudaError_t e = dsbk::launch_rope_posvec(q, n_q_heads, k, n_kv_heads, head_dim, n_tok, dev, theta, st);
+  cudaError_t e = dsbk::launch_rope_posvec(q, (long long)n_q_heads * head_dim, n_q_heads, k,
+                                           (long long)n_kv_heads * head_dim, n_kv_heads, head_dim, n_tok, dev, theta, st);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "rope_posvec launch");
 }
 
@@ -345,7 +347,8 @@ dsb_status dsb_kv_scatter(const dsb_kv_cache* kv, const int32_t* batch_index, in
   st = stage(ws, words, cs, &dev);
   if (st != DSB_OK) return st;
   cudaError_t e = dsbk::launch_kv_scatter(kv->k, kv->v, kv->dtype, kv->n_kv_heads, kv->ctx, kv->head_dim, dev,
-                                          tokens_per_seq, dev + n_seq, n_tok, k, v, cs);
+                                          tokens_per_seq, dev + n_seq, n_tok, k, v,
+                                          (long long)kv->n_kv_heads * kv->head_dim, cs);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "kv_scatter launch");
 }
 
@@ -392,9 +395,399 @@ dsb_status dsb_attention_decode_multi(const float* q, int n_q_heads, const dsb_k
   dsbk::MetaView mv{dev, dev + n_seq, dev + 2 * n_seq, nullptr};
   const int max_chunks = (kv->ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
   cudaError_t e = dsbk::launch_attention_decode_multi(
-      q, n_q_heads, kv->k, kv->v, kv->dtype, kv->n_kv_heads, kv->ctx, kv->head_dim, mv, n_seq, tokens_per_seq,
-      (int)total, max_chunks, reinterpret_cast<float*>(partial_base(ws)), out, cs);
+      q, (long long)n_q_heads * kv->head_dim, n_q_heads, kv->k, kv->v, kv->dtype, kv->n_kv_heads, kv->ctx, kv->head_dim, mv, n_seq, tokens_per_seq,
+      total * kv->n_kv_heads, max_chunks, reinterpret_cast<float*>(partial_base(ws)), out, cs);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "attention_decode_multi launch");
+}
+
+}  // extern "C"
+
+// ===========================================================================
+// The whole decode step (declared at the end of include/dsb.h).
+// ===========================================================================
+namespace {
+
+struct StepLayout {
+  size_t h = 0, qkv = 0, att = 0, gu = 0, xq = 0, graph_meta = 0, partials = 0, total = 0;
+};
+
+StepLayout step_layout(const dsb_model_shape& sh, int n_tok, int ctx) {
+  StepLayout L;
+  size_t off = kMetaBytes;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += round_up(bytes, 256);
+    return o;
+  };
+  const size_t nt = (size_t)n_tok;
+  const size_t qkv_cols = (size_t)(sh.n_q_heads + 2 * sh.n_kv_heads) * sh.head_dim;
+  const size_t att_cols = (size_t)sh.n_q_heads * sh.head_dim;
+  size_t max_cols = (size_t)sh.hidden;
+  if (att_cols > max_cols) max_cols = att_cols;
+  if ((size_t)sh.ffn > max_cols) max_cols = (size_t)sh.ffn;
+  L.h = take(nt * sh.hidden * 4);
+  L.qkv = take(nt * qkv_cols * 4);
+  L.att = take(nt * att_cols * 4);
+  L.gu = take(nt * 2 * (size_t)sh.ffn * 4);
+  L.xq = take(nt * (max_cols / 32) * 34);
+  L.graph_meta = take(kMetaSlotBytes);
+  L.partials = take(dsbk::attention_partial_bytes(n_tok, sh.n_q_heads, sh.head_dim, ctx));
+  L.total = off;
+  return L;
+}
+
+dsb_status check_mat_shape(const dsb_q8_0_mat& m, long long rows, long long cols, const char* what, int layer) {
+  dsb_status st = check_mat(&m);
+  if (st != DSB_OK) return fail(st, "layer %d %s: %s", layer, what, dsb_last_error());
+  if (m.rows != rows || m.cols != cols)
+    return fail(DSB_ERR_INVALID_ARG, "layer %d %s is %lldx%lld, expected %lldx%lld", layer, what, (long long)m.rows,
+                (long long)m.cols, rows, cols);
+  return DSB_OK;
+}
+
+// Validates the model description; on success *kv0 is layer 0's cache (all
+// layers share its geometry).
+dsb_status check_model(const dsb_model* m, const dsb_kv_cache** kv0) {
+  if (!m) return fail(DSB_ERR_INVALID_ARG, "model is NULL");
+  const dsb_model_shape& s = m->shape;
+  if (s.hidden < 256 || s.n_q_heads < 1 || s.n_kv_heads < 1 || s.head_dim < 2 || s.ffn < 256 || s.vocab < 1 ||
+      s.n_layers < 1)
+    return fail(DSB_ERR_INVALID_ARG, "model shape has a non-positive or too small dimension");
+  if (s.n_q_heads % s.n_kv_heads) return fail(DSB_ERR_INVALID_ARG, "n_q_heads %% n_kv_heads != 0");
+  if (s.hidden % 256 || s.ffn % 256 || (s.n_q_heads * s.head_dim) % 256)
+    return fail(DSB_ERR_UNSUPPORTED, "hidden, ffn and n_q_heads*head_dim must be multiples of 256");
+  if (s.head_dim != 64 && s.head_dim != 128) return fail(DSB_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (!(s.rms_eps > 0.0f) || !std::isfinite(s.rms_eps)) return fail(DSB_ERR_INVALID_ARG, "rms_eps must be > 0");
+  if (!(s.rope_theta > 0.0f) || !std::isfinite(s.rope_theta)) return fail(DSB_ERR_INVALID_ARG, "rope_theta must be > 0");
+  if (!m->embed || !aligned16(m->embed)) return fail(DSB_ERR_INVALID_ARG, "embed is NULL or not 16-byte aligned");
+  if (!m->final_norm) return fail(DSB_ERR_INVALID_ARG, "final_norm is NULL");
+  if (!m->layers) return fail(DSB_ERR_INVALID_ARG, "layers is NULL");
+  const long long qkv_rows = (long long)(s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim;
+  for (int l = 0; l < s.n_layers; ++l) {
+    const dsb_layer& L = m->layers[l];
+    dsb_status st;
+    if ((st = check_mat_shape(L.wqkv, qkv_rows, s.hidden, "wqkv", l)) != DSB_OK) return st;
+    if ((st = check_mat_shape(L.wo, s.hidden, (long long)s.n_q_heads * s.head_dim, "wo", l)) != DSB_OK) return st;
+    if ((st = check_mat_shape(L.wgu, 2LL * s.ffn, s.hidden, "wgu", l)) != DSB_OK) return st;
+    if ((st = check_mat_shape(L.wdown, s.hidden, s.ffn, "wdown", l)) != DSB_OK) return st;
+    if (!L.attn_norm || !L.ffn_norm) return fail(DSB_ERR_INVALID_ARG, "layer %d norm weights are NULL", l);
+    if ((st = check_kv(&L.kv)) != DSB_OK) return fail(st, "layer %d kv: %s", l, dsb_last_error());
+    if (L.kv.n_kv_heads != s.n_kv_heads || L.kv.head_dim != s.head_dim)
+      return fail(DSB_ERR_INVALID_ARG, "layer %d kv heads/head_dim do not match the shape", l);
+    const dsb_kv_cache& k0 = m->layers[0].kv;
+    if (L.kv.full_batch_size != k0.full_batch_size || L.kv.ctx != k0.ctx || L.kv.dtype != k0.dtype)
+      return fail(DSB_ERR_INVALID_ARG, "layer %d kv geometry differs from layer 0", l);
+  }
+  dsb_status st = check_mat_shape(m->head, s.vocab, s.hidden, "head", -1);
+  if (st != DSB_OK) return st;
+  *kv0 = &m->layers[0].kv;
+  return DSB_OK;
+}
+
+dsb_status check_step_meta(const dsb_model* m, const dsb_kv_cache* kv0, const int32_t* tokens, const int32_t* bi,
+                           int n_seq, int tps, const int32_t* seq_lens) {
+  dsb_status st = check_batch(kv0, bi, n_seq, tps);
+  if (st != DSB_OK) return st;
+  if (!tokens || !seq_lens) return fail(DSB_ERR_INVALID_ARG, "token_ids / seq_lens is NULL");
+  for (int t = 0; t < n_seq * tps; ++t)
+    if (tokens[t] < 0 || tokens[t] >= m->shape.vocab)
+      return fail(DSB_ERR_INVALID_ARG, "token_ids[%d]=%d out of [0, vocab=%d)", t, tokens[t], m->shape.vocab);
+  for (int s = 0; s < n_seq; ++s)
+    if (seq_lens[s] < tps || seq_lens[s] > kv0->ctx)
+      return fail(DSB_ERR_INVALID_ARG, "seq_lens[%d]=%d out of [T=%d, ctx=%d]", s, seq_lens[s], tps, kv0->ctx);
+  return DSB_OK;
+}
+
+// tokens[n_tok] | batch_index[n_seq] | seq_lens[n_seq] | chunk_off[n_seq+1] | pos[n_tok]
+std::vector<int32_t> step_words(const int32_t* tokens, const int32_t* bi, int n_seq, int tps, const int32_t* seq_lens,
+                                long long* total_chunks) {
+  const int n_tok = n_seq * tps;
+  std::vector<int32_t> w;
+  w.reserve((size_t)2 * n_tok + 3 * n_seq + 1);
+  w.insert(w.end(), tokens, tokens + n_tok);
+  w.insert(w.end(), bi, bi + n_seq);
+  w.insert(w.end(), seq_lens, seq_lens + n_seq);
+  long long tot = 0;
+  w.push_back(0);
+  for (int s = 0; s < n_seq; ++s) {
+    tot += (seq_lens[s] + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
+    w.push_back((int32_t)tot);
+  }
+  for (int s = 0; s < n_seq; ++s)
+    for (int j = 0; j < tps; ++j) w.push_back(seq_lens[s] - tps + j);
+  *total_chunks = tot;
+  return w;
+}
+
+cudaError_t run_matmul(const dsb_q8_0_mat& w, const void* xq, int n_tok, float* y, const float* residual, int sms,
+                       cudaStream_t st) {
+  const size_t blk_row = (size_t)(w.cols / 32) * 34;
+  for (int t0 = 0; t0 < n_tok; t0 += DSB_NARROW_MAX) {
+    const int nt = std::min(DSB_NARROW_MAX, n_tok - t0);
+    cudaError_t e = dsbk::launch_matmul_q8_0_narrow(w.blocks, w.rows, w.cols,
+                                                    static_cast<const char*>(xq) + (size_t)t0 * blk_row, nt,
+                                                    y + (size_t)t0 * w.rows,
+                                                    residual ? residual + (size_t)t0 * w.rows : nullptr, nullptr, sms, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// Enqueue every kernel of one step; metadata already on the device at meta_dev.
+dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, int tps, long long max_items,
+                        float* logits, dsb_workspace* ws, int sms, cudaStream_t st) {
+  const dsb_model_shape& s = m->shape;
+  const dsb_kv_cache& kv0 = m->layers[0].kv;
+  const int n_tok = n_seq * tps;
+  const StepLayout L = step_layout(s, n_tok, kv0.ctx);
+  const int32_t* tokens_dev = meta_dev;
+  const int32_t* bi_dev = tokens_dev + n_tok;
+  const int32_t* sl_dev = bi_dev + n_seq;
+  const int32_t* co_dev = sl_dev + n_seq;
+  const int32_t* pos_dev = co_dev + n_seq + 1;
+  float* h = reinterpret_cast<float*>(ws->dev + L.h);
+  float* qkv = reinterpret_cast<float*>(ws->dev + L.qkv);
+  float* att = reinterpret_cast<float*>(ws->dev + L.att);
+  float* gu = reinterpret_cast<float*>(ws->dev + L.gu);
+  void* xq = ws->dev + L.xq;
+  float* partials = reinterpret_cast<float*>(ws->dev + L.partials);
+  const int D = s.head_dim, Hq = s.n_q_heads, Hkv = s.n_kv_heads;
+  const long long qkv_stride = (long long)(Hq + 2 * Hkv) * D;
+  const int max_chunks = (kv0.ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
+  const dsbk::MetaView mv{bi_dev, sl_dev, co_dev, pos_dev};
+  cudaError_t e = dsbk::launch_embed(m->embed, s.hidden, tokens_dev, n_tok, h, st);
+  for (int l = 0; l < s.n_layers && e == cudaSuccess; ++l) {
+    const dsb_layer& Ly = m->layers[l];
+    if ((e = dsbk::launch_rmsnorm_quant(h, Ly.attn_norm, n_tok, s.hidden, s.rms_eps, xq, st)) != cudaSuccess) break;
+    if ((e = run_matmul(Ly.wqkv, xq, n_tok, qkv, nullptr, sms, st)) != cudaSuccess) break;
+    if ((e = dsbk::launch_rope_posvec(qkv, qkv_stride, Hq, qkv + (size_t)Hq * D, qkv_stride, Hkv, D, n_tok, pos_dev,
+                                      s.rope_theta, st)) != cudaSuccess)
+      break;
+    if ((e = dsbk::launch_kv_scatter(Ly.kv.k, Ly.kv.v, Ly.kv.dtype, Hkv, Ly.kv.ctx, D, bi_dev, tps, pos_dev, n_tok,
+                                     qkv + (size_t)Hq * D, qkv + (size_t)(Hq + Hkv) * D, qkv_stride, st)) != cudaSuccess)
+      break;
+    if ((e = dsbk::launch_attention_decode_multi(qkv, qkv_stride, Hq, Ly.kv.k, Ly.kv.v, Ly.kv.dtype, Hkv, Ly.kv.ctx, D,
+                                                 mv, n_seq, tps, max_items, max_chunks, partials, att, st)) !=
+        cudaSuccess)
+      break;
+    if ((e = dsbk::launch_quantize_q8_0(att, n_tok, (int64_t)Hq * D, xq, st)) != cudaSuccess) break;
+    if ((e = run_matmul(Ly.wo, xq, n_tok, h, h, sms, st)) != cudaSuccess) break;
+    if ((e = dsbk::launch_rmsnorm_quant(h, Ly.ffn_norm, n_tok, s.hidden, s.rms_eps, xq, st)) != cudaSuccess) break;
+    if ((e = run_matmul(Ly.wgu, xq, n_tok, gu, nullptr, sms, st)) != cudaSuccess) break;
+    if ((e = dsbk::launch_silu_mul_quant(gu, n_tok, s.ffn, xq, st)) != cudaSuccess) break;
+    if ((e = run_matmul(Ly.wdown, xq, n_tok, h, h, sms, st)) != cudaSuccess) break;
+  }
+  if (e == cudaSuccess) e = dsbk::launch_rmsnorm_quant(h, m->final_norm, n_tok, s.hidden, s.rms_eps, xq, st);
+  if (e == cudaSuccess) e = run_matmul(m->head, xq, n_tok, logits, nullptr, sms, st);
+  return e == cudaSuccess ? DSB_OK : cuda_fail(e, "decode step launch");
+}
+
+dsb_status check_step_resources(const dsb_model* m, int n_tok, float* logits, dsb_workspace* ws, int* sms) {
+  if (!logits || !aligned16(logits)) return fail(DSB_ERR_INVALID_ARG, "logits is NULL or not 16-byte aligned");
+  if (!ws) return fail(DSB_ERR_WORKSPACE, "workspace is NULL");
+  const StepLayout L = step_layout(m->shape, n_tok, m->layers[0].kv.ctx);
+  if (L.total > ws->dev_bytes)
+    return fail(DSB_ERR_WORKSPACE, "decode step needs %zu workspace bytes, have %zu", L.total, ws->dev_bytes);
+  DeviceInfo di;
+  dsb_status st = device_info(&di);
+  if (st != DSB_OK) return st;
+  const dsb_model_shape& s = m->shape;
+  const long long mats[4][2] = {{(long long)(s.n_q_heads + 2 * s.n_kv_heads) * s.head_dim, s.hidden},
+                                {s.hidden, (long long)s.n_q_heads * s.head_dim},
+                                {2LL * s.ffn, s.hidden},
+                                {s.hidden, s.ffn}};
+  const int nt = n_tok < DSB_NARROW_MAX ? n_tok : DSB_NARROW_MAX;
+  for (auto& mm : mats)
+    if (dsbk::matmul_smem_bytes(mm[0], mm[1], nt, di.sms) > (size_t)di.max_smem_optin)
+      return fail(DSB_ERR_UNSUPPORTED, "a %lldx%lld matmul exceeds shared memory", mm[0], mm[1]);
+  *sms = di.sms;
+  return DSB_OK;
+}
+
+}  // namespace
+
+struct dsb_step_graph {
+  dsb_model_shape shape{};
+  dsb_kv_cache kv0{};
+  int n_seq = 0, tps = 0;
+  dsb_workspace* ws = nullptr;
+  int32_t* pinned = nullptr;
+  int32_t* dev_meta = nullptr;
+  size_t n_words = 0;
+  std::vector<int32_t> last;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  cudaEvent_t done = nullptr;
+  bool launched = false;
+};
+
+extern "C" {
+
+size_t dsb_step_workspace_bytes(const dsb_model_shape* shape, int max_tokens, int ctx) {
+  if (!shape || max_tokens < 1 || max_tokens > DSB_MAX_TOKENS || ctx < 1 || shape->hidden < 1 || shape->ffn < 1 ||
+      shape->n_q_heads < 1 || shape->n_kv_heads < 0 || shape->head_dim < 1 || shape->head_dim > 1024)
+    return 0;
+  return step_layout(*shape, max_tokens, ctx).total;
+}
+
+dsb_status dsb_decode_step(const dsb_model* model, const int32_t* token_ids, const int32_t* batch_index, int n_seq,
+                           int tokens_per_seq, const int32_t* seq_lens, float* logits, dsb_workspace* ws,
+                           void* stream) {
+  const dsb_kv_cache* kv0 = nullptr;
+  dsb_status st = check_model(model, &kv0);
+  if (st != DSB_OK) return st;
+  st = check_step_meta(model, kv0, token_ids, batch_index, n_seq, tokens_per_seq, seq_lens);
+  if (st != DSB_OK) return st;
+  if ((long long)(model->shape.n_q_heads / model->shape.n_kv_heads) * tokens_per_seq > 64)
+    return fail(DSB_ERR_UNSUPPORTED, "query rows per kv head (G*T) exceed 64");
+  int sms = 0;
+  st = check_step_resources(model, n_seq * tokens_per_seq, logits, ws, &sms);
+  if (st != DSB_OK) return st;
+  long long total = 0;
+  const std::vector<int32_t> words = step_words(token_ids, batch_index, n_seq, tokens_per_seq, seq_lens, &total);
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const int32_t* dev = nullptr;
+  st = stage(ws, words, cs, &dev);
+  if (st != DSB_OK) return st;
+  return enqueue_step(model, dev, n_seq, tokens_per_seq, total * model->shape.n_kv_heads, logits, ws, sms, cs);
+}
+
+dsb_status dsb_step_graph_create(const dsb_model* model, int n_seq, int tokens_per_seq, float* logits,
+                                 dsb_workspace* ws, void* stream, dsb_step_graph** out) {
+  if (!out) return fail(DSB_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  const dsb_kv_cache* kv0 = nullptr;
+  dsb_status st = check_model(model, &kv0);
+  if (st != DSB_OK) return st;
+  if (n_seq < 1 || n_seq > kv0->full_batch_size || n_seq > DSB_MAX_SEQS || tokens_per_seq < 1 ||
+      (long long)n_seq * tokens_per_seq > DSB_MAX_TOKENS)
+    return fail(DSB_ERR_INVALID_ARG, "n_seq=%d / tokens_per_seq=%d out of range", n_seq, tokens_per_seq);
+  if ((long long)(model->shape.n_q_heads / model->shape.n_kv_heads) * tokens_per_seq > 64)
+    return fail(DSB_ERR_UNSUPPORTED, "query rows per kv head (G*T) exceed 64");
+  int sms = 0;
+  const int n_tok = n_seq * tokens_per_seq;
+  st = check_step_resources(model, n_tok, logits, ws, &sms);
+  if (st != DSB_OK) return st;
+  dsb_step_graph* g = new (std::nothrow) dsb_step_graph();
+  if (!g) return fail(DSB_ERR_INVALID_ARG, "out of host memory");
+  g->shape = model->shape;
+  g->kv0 = *kv0;
+  g->n_seq = n_seq;
+  g->tps = tokens_per_seq;
+  g->ws = ws;
+  g->n_words = (size_t)2 * n_tok + 3 * (size_t)n_seq + 1;
+  const StepLayout L = step_layout(model->shape, n_tok, kv0->ctx);
+  g->dev_meta = reinterpret_cast<int32_t*>(ws->dev + L.graph_meta);
+  (void)stream;  // the graph is captured on a private stream and replayed on the caller's
+  cudaStream_t cs = nullptr;
+  cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&g->pinned), g->n_words * sizeof(int32_t), cudaHostAllocDefault);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g->done, cudaEventDisableTiming);
+  // The legacy default stream cannot be captured, so capture on a private
+  // non-blocking stream; work already queued elsewhere is not part of the graph.
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    if (cs) cudaStreamDestroy(cs);
+    if (g->done) cudaEventDestroy(g->done);
+    if (g->pinned) cudaFreeHost(g->pinned);
+    delete g;
+    return cuda_fail(e, "dsb_step_graph_create");
+  }
+  // Placeholder metadata for the capture: one chunk per sequence; the real
+  // values are written before every launch.
+  std::memset(g->pinned, 0, g->n_words * sizeof(int32_t));
+  const long long max_items =
+      (long long)n_seq * ((kv0->ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK) * model->shape.n_kv_heads;
+  // Warm every launcher's one-time set-up outside the capture.
+  dsbk::set_dry_run(true);
+  dsb_status dry = enqueue_step(model, g->dev_meta, n_seq, tokens_per_seq, max_items, logits, ws, sms, cs);
+  dsbk::set_dry_run(false);
+  if (dry != DSB_OK) {
+    cudaStreamDestroy(cs);
+    cudaEventDestroy(g->done);
+    cudaFreeHost(g->pinned);
+    delete g;
+    return dry;
+  }
+  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  if (e == cudaSuccess) {
+    e = cudaMemcpyAsync(g->dev_meta, g->pinned, g->n_words * sizeof(int32_t), cudaMemcpyHostToDevice, cs);
+    dsb_status es = DSB_OK;
+    if (e == cudaSuccess) es = enqueue_step(model, g->dev_meta, n_seq, tokens_per_seq, max_items, logits, ws, sms, cs);
+    cudaError_t e2 = cudaStreamEndCapture(cs, &g->graph);
+    if (e == cudaSuccess && es != DSB_OK) {
+      if (g->graph) cudaGraphDestroy(g->graph);
+      cudaStreamDestroy(cs);
+      cudaEventDestroy(g->done);
+      cudaFreeHost(g->pinned);
+      delete g;
+      return es;
+    }
+    if (e == cudaSuccess) e = e2;
+  }
+  cudaStreamDestroy(cs);
+  if (e == cudaSuccess) e = cudaGraphInstantiate(&g->exec, g->graph, 0);
+  if (e != cudaSuccess) {
+    if (g->graph) cudaGraphDestroy(g->graph);
+    cudaEventDestroy(g->done);
+    cudaFreeHost(g->pinned);
+    delete g;
+    return cuda_fail(e, "step graph capture");
+  }
+  *out = g;
+  return DSB_OK;
+}
+
+dsb_status dsb_step_graph_launch(dsb_step_graph* g, const int32_t* token_ids, const int32_t* batch_index,
+                                 const int32_t* seq_lens, void* stream) {
+  if (!g) return fail(DSB_ERR_INVALID_ARG, "graph is NULL");
+  dsb_model fake{};
+  fake.shape = g->shape;
+  dsb_status st = check_step_meta(&fake, &g->kv0, token_ids, batch_index, g->n_seq, g->tps, seq_lens);
+  if (st != DSB_OK) return st;
+  long long total = 0;
+  std::vector<int32_t> words = step_words(token_ids, batch_index, g->n_seq, g->tps, seq_lens, &total);
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (words != g->last) {
+    if (g->launched) {  // the previous replay may still be reading the pinned copy
+      const auto t0 = std::chrono::steady_clock::now();
+      for (;;) {
+        cudaError_t q = cudaEventQuery(g->done);
+        if (q == cudaSuccess) break;
+        if (q != cudaErrorNotReady) return cuda_fail(q, "cudaEventQuery(step graph)");
+        if (std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count() > kHostWaitSeconds)
+          return fail(DSB_ERR_TIMEOUT, "previous step graph replay still running after %.0f s", kHostWaitSeconds);
+        std::this_thread::yield();
+      }
+    }
+    std::memcpy(g->pinned, words.data(), words.size() * sizeof(int32_t));
+    g->last.swap(words);
+  }
+  cudaError_t e = cudaGraphLaunch(g->exec, cs);
+  if (e == cudaSuccess) e = cudaEventRecord(g->done, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGraphLaunch(step)");
+  g->launched = true;
+  return DSB_OK;
+}
+
+dsb_status dsb_step_graph_destroy(dsb_step_graph* g) {
+  if (!g) return DSB_OK;
+  dsb_status st = DSB_OK;
+  if (g->launched) {
+    const auto t0 = std::chrono::steady_clock::now();
+    while (cudaEventQuery(g->done) == cudaErrorNotReady) {
+      if (std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count() > kHostWaitSeconds) {
+        st = fail(DSB_ERR_TIMEOUT, "step graph still running at destroy");
+        break;
+      }
+      std::this_thread::yield();
+    }
+  }
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  if (g->done) cudaEventDestroy(g->done);
+  if (g->pinned) cudaFreeHost(g->pinned);
+  delete g;
+  return st;
 }
 
 }  // extern "C"

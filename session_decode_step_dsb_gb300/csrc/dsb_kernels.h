@@ -8,6 +8,12 @@
 
 namespace dsbk {
 
+// When set (per host thread), every launch_* function performs its one-time
+// set-up (shared-memory attribute, occupancy query) but enqueues nothing.
+// Used to warm those caches before a CUDA graph capture.
+void set_dry_run(bool on);
+bool dry_run();
+
 // Per-call metadata staged in device memory (workspace), int32 words:
 //   [0] n_seq  [1] tokens_per_seq  [2] n_tok  [3] total attention chunks
 //   then batch_index[n_seq], seq_lens[n_seq], chunk_off[n_seq + 1], pos[n_tok]
@@ -21,26 +27,38 @@ struct MetaView {
 
 int matmul_split(int64_t rows, int64_t cols, int num_sms);
 size_t matmul_smem_bytes(int64_t rows, int64_t cols, int n_tok, int num_sms);
+// residual (may alias y, may be NULL): y = residual + W x.
 cudaError_t launch_matmul_q8_0_narrow(const void* W, int64_t rows, int64_t cols, const void* xq, int n_tok, float* y,
-                                      int32_t* isum, int num_sms, cudaStream_t st);
+                                      const float* residual, int32_t* isum, int num_sms, cudaStream_t st);
 
 cudaError_t launch_quantize_q8_0(const float* x, int64_t n_rows, int64_t cols, void* xq, cudaStream_t st);
 
-cudaError_t launch_rope_posvec(float* q, int n_q_heads, float* k, int n_kv_heads, int head_dim, int n_tok,
-                               const int32_t* pos_dev, float theta, cudaStream_t st);
+// q_stride / k_stride: floats between consecutive token rows.
+cudaError_t launch_rope_posvec(float* q, long long q_stride, int n_q_heads, float* k, long long k_stride,
+                               int n_kv_heads, int head_dim, int n_tok, const int32_t* pos_dev, float theta,
+                               cudaStream_t st);
 
 cudaError_t launch_kv_scatter(void* kc, void* vc, int dtype, int n_kv_heads, int ctx, int head_dim,
                               const int32_t* batch_index_dev, int tokens_per_seq, const int32_t* pos_dev, int n_tok,
-                              const float* k, const float* v, cudaStream_t st);
+                              const float* k, const float* v, long long kv_stride, cudaStream_t st);
 
-// Split-K decode attention: partial kernel over (sequence, chunk) x kv head,
-// then the chunk-order merge.  partials: float [n_tok][n_q_heads][max_chunks][head_dim + 2].
-cudaError_t launch_attention_decode_multi(const float* q, int n_q_heads, const void* kc, const void* vc, int dtype,
+// Split-K decode attention: persistent partial kernel over the (chunk, kv head)
+// items listed by meta.chunk_off (count read on the device), then the
+// chunk-order merge.  max_items bounds the item count (sizes the grid);
+// partials: float [n_tok][n_q_heads][max_chunks][head_dim + 2].
+cudaError_t launch_attention_decode_multi(const float* q, long long q_stride, int n_q_heads, const void* kc,
+                                          const void* vc, int dtype,
                                           int n_kv_heads, int ctx, int head_dim, MetaView meta, int n_seq,
-                                          int tokens_per_seq, int total_chunks, int max_chunks, float* partials,
+                                          int tokens_per_seq, long long max_items, int max_chunks, float* partials,
                                           float* out, cudaStream_t st);
 
 size_t attention_partial_bytes(int n_tok, int n_q_heads, int head_dim, int ctx);
+
+cudaError_t launch_rmsnorm_quant(const float* x, const float* w, int n_tok, int hidden, float eps, void* xq,
+                                 cudaStream_t st);
+cudaError_t launch_silu_mul_quant(const float* gu, int n_tok, int ffn, void* xq, cudaStream_t st);
+cudaError_t launch_embed(const void* table, int hidden, const int32_t* tokens_dev, int n_tok, float* h,
+                         cudaStream_t st);
 
 unsigned int read_clear_error_matmul();
 unsigned int read_clear_error_attention();

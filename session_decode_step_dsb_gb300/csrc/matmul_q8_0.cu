@@ -72,25 +72,31 @@ __device__ __forceinline__ Split kstep_range(int nks, int S, int rank) {
 template <int NT, bool EMIT>
 __global__ void __launch_bounds__(kThreads, 2)
     matmul_q8_0_narrow_kernel(const uint8_t* __restrict__ W, int rows, int nb, const uint8_t* __restrict__ xq,
-                              float* __restrict__ y, int32_t* __restrict__ isum_out) {
+                              float* y, const float* residual, int32_t* __restrict__ isum_out) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int nks = nb >> 3;
   const int S = gridDim.y;
   const int rank = blockIdx.y;  // cluster dims (1, S, 1): rank within the cluster
+  const int n_clusters = gridDim.x;
   const Split ksr = kstep_range(nks, S, rank);
   const int kr = ksr.ks1 - ksr.ks0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row0 = blockIdx.x * kRowsPerCta;
-  const int row = row0 + lane;
-  const bool row_ok = row < rows;
-  const int rows_here = min(kRowsPerCta, rows - row0);
   const size_t row_bytes = (size_t)nb * 34;
+  const int tiles = (rows + kRowsPerCta - 1) / kRowsPerCta;
+  const int n_tiles = blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / n_clusters + 1 : 0;
 
-  // shared layout: act codes | act scales | stages | barriers
-  uint32_t* act_q = reinterpret_cast<uint32_t*>(smem);                 // [kr*8][NT][8]
-  float* act_s = reinterpret_cast<float*>(act_q + (size_t)kr * 8 * NT * 8);  // [kr*8][NT]
-  uint8_t* stages = reinterpret_cast<uint8_t*>(act_s + (size_t)kr * 8 * NT);  // [kWarps][kNStage][kStage]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stages + (size_t)kWarps * kNStage * kStage);  // [kWarps][kNStage]
+  // Shared layout: act codes | act scales | stage rings | warp partials |
+  // CTA sums (double-buffered) | barriers.  The act region is sized for the
+  // largest k-range of the cluster in every CTA, so all CTAs of a cluster put
+  // the CTA sums at the same offset -- the distributed-shared-memory reads of
+  // rank 0 rely on that.
+  const int kr_alloc = (nks + S - 1) / S;
+  uint32_t* act_q = reinterpret_cast<uint32_t*>(smem);                              // [kr*8][NT][8]
+  float* act_s = reinterpret_cast<float*>(act_q + (size_t)kr_alloc * 8 * NT * 8);  // [kr*8][NT]
+  uint8_t* stages = reinterpret_cast<uint8_t*>(act_s + (size_t)kr_alloc * 8 * NT);  // [kWarps][kNStage][kStage]
+  float* red = reinterpret_cast<float*>(stages + (size_t)kWarps * kNStage * kStage);  // [kWarps][NT][32]
+  float* red_sum = red + kWarps * NT * 32;                                            // [2][NT][32]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red_sum + 2 * NT * 32);                // [kWarps][kNStage]
   uint8_t* my_stages = stages + (size_t)warp * kNStage * kStage;
   uint64_t* my_bars = bars + warp * kNStage;
 
@@ -100,151 +106,177 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncwarp();
 
-  // k-steps of this warp: ks0 + warp + kWarps*m
+  // This warp's units: for each of the CTA's tiles m, its k-steps
+  // ks0 + warp + kWarps*i, i < n_mine.  Unit u = m*n_mine + i.
   const int n_mine = kr > warp ? (kr - warp + kWarps - 1) / kWarps : 0;
-  auto issue = [&](int m) {
-    const int ks = ksr.ks0 + warp + kWarps * m;
-    uint64_t* bar = &my_bars[m % kNStage];
-    uint8_t* dst = my_stages + (size_t)(m % kNStage) * kStage;
-    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(rows_here * kChunkBytes));
+  const int n_units = n_tiles * n_mine;
+  auto issue = [&](int u) {
+    const int m = u / n_mine, i = u - m * n_mine;
+    const int row0 = ((int)blockIdx.x + m * n_clusters) * kRowsPerCta;
+    const int row = row0 + lane;
+    const int ks = ksr.ks0 + warp + kWarps * i;
+    uint64_t* bar = &my_bars[u % kNStage];
+    uint8_t* dst = my_stages + (size_t)(u % kNStage) * kStage;
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(min(kRowsPerCta, rows - row0) * kChunkBytes));
     __syncwarp();
-    if (row_ok) bulk_g2s(dst + lane * kChunkBytes, W + (size_t)row * row_bytes + (size_t)ks * kChunkBytes, kChunkBytes, bar);
+    if (row < rows)
+      bulk_g2s(dst + lane * kChunkBytes, W + (size_t)row * row_bytes + (size_t)ks * kChunkBytes, kChunkBytes, bar);
   };
-  for (int m = 0; m < kNStage && m < n_mine; ++m) issue(m);
+  for (int u = 0; u < kNStage && u < n_units; ++u) issue(u);
 
   // Unpack the CTA's activation blocks [ks0*8, ks1*8) x NT into aligned form.
-  {
-    const int nblk = kr * 8;
-    for (int idx = threadIdx.x; idx < nblk * NT; idx += kThreads) {
-      const int b = idx / NT, t = idx - b * NT;
-      const long long g = (long long)t * nb + (long long)ksr.ks0 * 8 + b;  // global block index
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(xq + ((34 * g) & ~3LL));
-      uint32_t wv[9];
+  for (int idx = threadIdx.x; idx < kr * 8 * NT; idx += kThreads) {
+    const int b = idx / NT, t = idx - b * NT;
+    const long long g = (long long)t * nb + (long long)ksr.ks0 * 8 + b;  // global block index
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(xq + ((34 * g) & ~3LL));
+    uint32_t wv[9];
 #pragma unroll
-      for (int k = 0; k < 9; ++k) wv[k] = __ldg(src + k);
-      const bool odd = (g & 1) != 0;  // odd blocks start 2 bytes into a word
-      const uint32_t sh = odd ? 32u : 16u;
-      uint32_t* dq = act_q + ((size_t)b * NT + t) * 8;
+    for (int k = 0; k < 9; ++k) wv[k] = __ldg(src + k);
+    const bool odd = (g & 1) != 0;  // odd blocks start 2 bytes into a word
+    const uint32_t sh = odd ? 32u : 16u;
+    uint32_t* dq = act_q + ((size_t)b * NT + t) * 8;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) dq[k] = __funnelshift_rc(wv[k], wv[k + 1], sh);
-      act_s[(size_t)b * NT + t] = half_bits_to_float(odd ? (wv[0] >> 16) : wv[0]);
-    }
+    for (int k = 0; k < 8; ++k) dq[k] = __funnelshift_rc(wv[k], wv[k + 1], sh);
+    act_s[(size_t)b * NT + t] = half_bits_to_float(odd ? (wv[0] >> 16) : wv[0]);
   }
   __syncthreads();
 
-  float acc[NT];
-#pragma unroll
-  for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
   bool dead = false;
+  int u = 0;
+  for (int m = 0; m < n_tiles; ++m) {
+    const int row0 = ((int)blockIdx.x + m * n_clusters) * kRowsPerCta;
+    const int row = row0 + lane;
+    float acc[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
 
-  for (int m = 0; m < n_mine; ++m) {
-    const int ks = ksr.ks0 + warp + kWarps * m;
-    const int kl = ks - ksr.ks0;
-    uint64_t* bar = &my_bars[m % kNStage];
-    if (!dead) {
-      const bool ok = mbar_wait(bar, (uint32_t)((m / kNStage) & 1));
-      dead = __any_sync(0xffffffffu, !ok);  // warp-uniform
-      if (dead && lane == 0) g_err_matmul = 1u;
-    }
-    const uint4* src = reinterpret_cast<const uint4*>(my_stages + (size_t)(m % kNStage) * kStage + lane * kChunkBytes);
-    uint32_t w[68];
-#pragma unroll
-    for (int i = 0; i < 17; ++i) {
-      const uint4 v = src[i];
-      w[4 * i + 0] = v.x;
-      w[4 * i + 1] = v.y;
-      w[4 * i + 2] = v.z;
-      w[4 * i + 3] = v.w;
-    }
-    __syncwarp();
-    fence_proxy_async_smem();
-    if (!dead && m + kNStage < n_mine) issue(m + kNStage);
-
-#pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      uint32_t q[8];
-      float dw;
-      if ((b & 1) == 0) {
-        const int base = (17 * b) / 2;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) q[k] = __funnelshift_r(w[base + k], w[base + k + 1], 16);
-        dw = half_bits_to_float(w[base]);
-      } else {
-        const int base = (17 * b - 1) / 2;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) q[k] = w[base + 1 + k];
-        dw = half_bits_to_float(w[base] >> 16);
+    for (int i = 0; i < n_mine; ++i, ++u) {
+      const int ks = ksr.ks0 + warp + kWarps * i;
+      const int kl = ks - ksr.ks0;
+      uint64_t* bar = &my_bars[u % kNStage];
+      if (!dead) {
+        const bool ok = mbar_wait(bar, (uint32_t)((u / kNStage) & 1));
+        dead = __any_sync(0xffffffffu, !ok);  // warp-uniform
+        if (dead && lane == 0) g_err_matmul = 1u;
       }
-      const uint32_t* aq = act_q + ((size_t)(kl * 8 + b) * NT) * 8;
-      const float* as = act_s + (size_t)(kl * 8 + b) * NT;
+      const uint4* src = reinterpret_cast<const uint4*>(my_stages + (size_t)(u % kNStage) * kStage + lane * kChunkBytes);
+      uint32_t w[68];
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const uint4 x0 = *reinterpret_cast<const uint4*>(aq + t * 8);
-        const uint4 x1 = *reinterpret_cast<const uint4*>(aq + t * 8 + 4);
-        int s = (int)kMagic;
-        s = __dp4a((int)q[0], (int)x0.x, s);
-        s = __dp4a((int)q[1], (int)x0.y, s);
-        s = __dp4a((int)q[2], (int)x0.z, s);
-        s = __dp4a((int)q[3], (int)x0.w, s);
-        s = __dp4a((int)q[4], (int)x1.x, s);
-        s = __dp4a((int)q[5], (int)x1.y, s);
-        s = __dp4a((int)q[6], (int)x1.z, s);
-        s = __dp4a((int)q[7], (int)x1.w, s);
-        if constexpr (EMIT) {
-          if (row_ok)
-            isum_out[((size_t)t * rows + row) * nb + (size_t)ks * 8 + b] = s - (int)kMagic;
+      for (int c = 0; c < 17; ++c) {
+        const uint4 v = src[c];
+        w[4 * c + 0] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+      }
+      __syncwarp();  // every lane has read the stage: it may be refilled
+      if (!dead && u + kNStage < n_units) issue(u + kNStage);
+
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        uint32_t q[8];
+        float dw;
+        if ((b & 1) == 0) {
+          const int base = (17 * b) / 2;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) q[k] = __funnelshift_r(w[base + k], w[base + k + 1], 16);
+          dw = half_bits_to_float(w[base]);
         } else {
-          const float f = __fsub_rn(__int_as_float(s), kMagicF);
-          acc[t] = __fmaf_rn(f, __fmul_rn(dw, as[t]), acc[t]);
+          const int base = (17 * b - 1) / 2;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) q[k] = w[base + 1 + k];
+          dw = half_bits_to_float(w[base] >> 16);
+        }
+        const uint32_t* aq = act_q + ((size_t)(kl * 8 + b) * NT) * 8;
+        const float* as = act_s + (size_t)(kl * 8 + b) * NT;
+        float sx[NT];
+        if constexpr (NT % 4 == 0) {
+#pragma unroll
+          for (int t = 0; t < NT; t += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(as + t);
+            sx[t] = v.x; sx[t + 1] = v.y; sx[t + 2] = v.z; sx[t + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int t = 0; t < NT; ++t) sx[t] = as[t];
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const uint4 x0 = *reinterpret_cast<const uint4*>(aq + t * 8);
+          const uint4 x1 = *reinterpret_cast<const uint4*>(aq + t * 8 + 4);
+          int s = (int)kMagic;
+          s = __dp4a((int)q[0], (int)x0.x, s);
+          s = __dp4a((int)q[1], (int)x0.y, s);
+          s = __dp4a((int)q[2], (int)x0.z, s);
+          s = __dp4a((int)q[3], (int)x0.w, s);
+          s = __dp4a((int)q[4], (int)x1.x, s);
+          s = __dp4a((int)q[5], (int)x1.y, s);
+          s = __dp4a((int)q[6], (int)x1.z, s);
+          s = __dp4a((int)q[7], (int)x1.w, s);
+          if constexpr (EMIT) {
+            if (row < rows) isum_out[((size_t)t * rows + row) * nb + (size_t)ks * 8 + b] = s - (int)kMagic;
+          } else {
+            const float f = __fsub_rn(__int_as_float(s), kMagicF);
+            acc[t] = __fmaf_rn(f, __fmul_rn(dw, sx[t]), acc[t]);
+          }
+        }
+      }
+    }
+
+    if constexpr (!EMIT) {
+      // Tile end: warp partials summed in warp order into this CTA's sum,
+      // then rank 0 adds the cluster's CTA sums in rank order.  The CTA sums
+      // are double-buffered by tile parity, so one cluster barrier per tile
+      // suffices: a buffer is rewritten two tiles later, after the next
+      // barrier, which rank 0 reaches only once it has read this one.
+#pragma unroll
+      for (int t = 0; t < NT; ++t) red[(warp * NT + t) * 32 + lane] = acc[t];
+      __syncthreads();
+      float* rs = red_sum + (m & 1) * NT * 32;
+      for (int idx = threadIdx.x; idx < NT * 32; idx += kThreads) {
+        float v = red[idx];
+#pragma unroll
+        for (int w2 = 1; w2 < kWarps; ++w2) v = __fadd_rn(v, red[w2 * NT * 32 + idx]);
+        rs[idx] = v;
+      }
+      cluster_sync();
+      if (rank == 0) {
+        for (int idx = threadIdx.x; idx < NT * 32; idx += kThreads) {
+          float v = rs[idx];
+          for (int r = 1; r < S; ++r) v = __fadd_rn(v, ld_dsmem_f32(&rs[idx], (uint32_t)r));
+          const int t = idx >> 5, rr = row0 + (idx & 31);
+          if (rr < rows) {
+            const size_t o = (size_t)t * rows + rr;
+            y[o] = residual ? __fadd_rn(residual[o], v) : v;  // residual may alias y
+          }
         }
       }
     }
   }
-
-  if constexpr (!EMIT) {
-    // Intra-CTA: warp partials [kWarps][NT][32] summed in warp order, then the
-    // cluster's CTA sums added in rank order by rank 0.  The reduction buffers
-    // reuse the stage ring (every copy into it has been waited on).
-    __syncthreads();
-    float* red = reinterpret_cast<float*>(stages);
-    float* red_sum = red + kWarps * NT * 32;
-#pragma unroll
-    for (int t = 0; t < NT; ++t) red[(warp * NT + t) * 32 + lane] = acc[t];
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < NT * 32; idx += kThreads) {
-      float v = red[idx];
-#pragma unroll
-      for (int w2 = 1; w2 < kWarps; ++w2) v = __fadd_rn(v, red[w2 * NT * 32 + idx]);
-      red_sum[idx] = v;
-    }
-    cluster_sync();
-    if (rank == 0) {
-      for (int idx = threadIdx.x; idx < NT * 32; idx += kThreads) {
-        float v = red_sum[idx];
-        for (int r = 1; r < S; ++r) v = __fadd_rn(v, ld_dsmem_f32(&red_sum[idx], (uint32_t)r));
-        const int t = idx >> 5, rr = row0 + (idx & 31);
-        if (rr < rows) y[(size_t)t * rows + rr] = v;
-      }
-    }
-    cluster_sync();
-  }
+  if constexpr (!EMIT) cluster_sync();  // keep this CTA's sums alive until rank 0 has read them
 }
 
 size_t smem_bytes(int kr, int nt) {
-  return (size_t)kr * 8 * nt * 36 + (size_t)kWarps * kNStage * kStage + (size_t)kWarps * kNStage * 8;
+  return (size_t)kr * 8 * nt * 36 + (size_t)kWarps * kNStage * kStage + (size_t)(kWarps + 2) * nt * 32 * 4 +
+         (size_t)kWarps * kNStage * 8;
 }
 
 template <int NT, bool EMIT>
-cudaError_t launch_nt(const uint8_t* W, int rows, int nb, const uint8_t* xq, float* y, int32_t* isum, int S,
-                      size_t smem, cudaStream_t st) {
+cudaError_t launch_nt(const uint8_t* W, int rows, int nb, const uint8_t* xq, float* y, const float* residual,
+                      int32_t* isum, int S, size_t smem, cudaStream_t st) {
   auto kern = matmul_q8_0_narrow_kernel<NT, EMIT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  // Per-instantiation caches (not thread-safe; one host thread drives a
+  // device): the largest dynamic shared memory granted so far, and the number
+  // of co-resident clusters for each (S, smem) seen -- the persistent grid.
+  struct Entry {
+    int S;
+    size_t smem;
+    int clusters;
+  };
+  static Entry cache[8];
+  static int n_cache = 0;
+  static size_t granted = 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((rows + kRowsPerCta - 1) / kRowsPerCta), (unsigned)S, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
@@ -252,16 +284,38 @@ cudaError_t launch_nt(const uint8_t* W, int rows, int nb, const uint8_t* xq, flo
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, W, rows, nb, xq, y, isum);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  if (smem > granted) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    granted = smem;
+  }
+  int resident = 0;
+  for (int i = 0; i < n_cache; ++i)
+    if (cache[i].S == S && cache[i].smem == smem) resident = cache[i].clusters;
+  if (resident == 0) {
+    cfg.gridDim = dim3(1, (unsigned)S, 1);
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&resident, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (resident < 1) return cudaErrorInvalidConfiguration;
+    cache[n_cache < 8 ? n_cache++ : 7] = Entry{S, smem, resident};
+  }
+  const int tiles = (rows + kRowsPerCta - 1) / kRowsPerCta;
+  const int n_clusters = tiles < resident ? tiles : resident;
+  cfg.gridDim = dim3((unsigned)n_clusters, (unsigned)S, 1);
+  if (dry_run()) return cudaSuccess;
+  return cudaLaunchKernelEx(&cfg, kern, W, rows, nb, xq, y, residual, isum);
 }
 
 template <bool EMIT>
-cudaError_t dispatch(int nt, const uint8_t* W, int rows, int nb, const uint8_t* xq, float* y, int32_t* isum, int S,
-                     size_t smem, cudaStream_t st) {
+cudaError_t dispatch(int nt, const uint8_t* W, int rows, int nb, const uint8_t* xq, float* y, const float* residual,
+                     int32_t* isum, int S, size_t smem, cudaStream_t st) {
   switch (nt) {
 #define DSB_CASE(N) \
   case N:           \
-    return launch_nt<N, EMIT>(W, rows, nb, xq, y, isum, S, smem, st);
+    return launch_nt<N, EMIT>(W, rows, nb, xq, y, residual, isum, S, smem, st);
     DSB_CASE(1) DSB_CASE(2) DSB_CASE(3) DSB_CASE(4) DSB_CASE(5) DSB_CASE(6) DSB_CASE(7) DSB_CASE(8)
     DSB_CASE(9) DSB_CASE(10) DSB_CASE(11) DSB_CASE(12) DSB_CASE(13) DSB_CASE(14) DSB_CASE(15) DSB_CASE(16)
 #undef DSB_CASE
@@ -274,18 +328,31 @@ cudaError_t dispatch(int nt, const uint8_t* W, int rows, int nb, const uint8_t* 
 
 int matmul_split(int64_t rows, int64_t cols, int num_sms) {
   // Depends on (rows, cols, SM count) only -- never on n_tok -- so that the
-  // summation order of every output is the same for every n_tok.
+  // summation order of every output is the same for every n_tok.  Each CTA of
+  // a cluster keeps the activations of its k-range in shared memory, which at
+  // n_tok = 16 allows at most 8 k-steps (36 KiB) next to the weight rings; among
+  // the admissible S the one with the smallest estimated makespan (tiles per
+  // cluster x k-steps per CTA, plus a per-tile reduction cost) wins, assuming
+  // two resident CTAs per SM.
   const int nks = (int)(cols / 256);
   const int tiles = (int)((rows + kRowsPerCta - 1) / kRowsPerCta);
-  // activation shared memory at n_tok = 16: kr*8*16*36 bytes <= 36 KiB -> kr <= 8,
-  // which keeps two CTAs resident per SM next to the weight rings.
-  int s_smem = (nks + 7) / 8;
-  int s_fill = (2 * num_sms + tiles - 1) / tiles;
-  int S = s_smem > s_fill ? s_smem : s_fill;
-  if (S > nks) S = nks;
-  if (S > 8) S = 8;
-  if (S < 1) S = 1;
-  return S;
+  int s_max = nks < 8 ? nks : 8;
+  int s_min = (nks + 7) / 8;
+  if (s_min > s_max) s_min = s_max;
+  if (s_min < 1) s_min = 1;
+  const int P = 2 * num_sms;
+  int best = s_min;
+  double best_cost = 1e30;
+  for (int S = s_min; S <= s_max; ++S) {
+    const int clusters = P / S > 0 ? P / S : 1;
+    const int per = (tiles + clusters - 1) / clusters;
+    const double cost = per * (((nks + S - 1) / S) + 0.5);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  return best;
 }
 
 size_t matmul_smem_bytes(int64_t rows, int64_t cols, int n_tok, int num_sms) {
@@ -296,16 +363,22 @@ size_t matmul_smem_bytes(int64_t rows, int64_t cols, int n_tok, int num_sms) {
 }
 
 cudaError_t launch_matmul_q8_0_narrow(const void* W, int64_t rows, int64_t cols, const void* xq, int n_tok,
-                                      float* y, int32_t* isum, int num_sms, cudaStream_t st) {
+                                      float* y, const float* residual, int32_t* isum, int num_sms, cudaStream_t st) {
   const int S = matmul_split(rows, cols, num_sms);
   const size_t smem = matmul_smem_bytes(rows, cols, n_tok, num_sms);
   const int nb = (int)(cols / 32);
   if (isum)
     return dispatch<true>(n_tok, static_cast<const uint8_t*>(W), (int)rows, nb, static_cast<const uint8_t*>(xq), y,
-                          isum, S, smem, st);
+                          residual, isum, S, smem, st);
   return dispatch<false>(n_tok, static_cast<const uint8_t*>(W), (int)rows, nb, static_cast<const uint8_t*>(xq), y,
-                         isum, S, smem, st);
+                         residual, isum, S, smem, st);
 }
+
+namespace {
+thread_local bool g_dry_run = false;
+}
+void set_dry_run(bool on) { g_dry_run = on; }
+bool dry_run() { return g_dry_run; }
 
 unsigned int read_clear_error_matmul() {
   unsigned int v = 0, z = 0;

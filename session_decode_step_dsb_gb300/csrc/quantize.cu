@@ -10,7 +10,7 @@
 // correctly rounded float32 operation, so the bytes equal the host codec's.
 //
 // One warp per block: lane k owns value k; the max is a butterfly over the
-// warp; lane k writes code byte k and lane 0 the two scale bytes.
+// warp; even lanes write two code bytes each and lane 0 the scale.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -37,13 +37,13 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float* __restr
     const float r = roundf(__fdiv_rn(v, d));
     q = (int)fminf(fmaxf(r, -127.0f), 127.0f);
   }
-  uint8_t* out = xq + blk * 34;
-  out[2 + lane] = (uint8_t)(int8_t)q;
-  if (lane == 0) {
-    const unsigned short h = __half_as_ushort(__float2half_rn(d));
-    out[0] = (uint8_t)(h & 0xFF);
-    out[1] = (uint8_t)(h >> 8);
-  }
+  // Stores are 16-bit and 2-byte aligned (a block starts at an even byte):
+  // lane 0 writes the fp16 scale, every even lane the code pair (l, l+1).
+  const int q_next = __shfl_down_sync(0xffffffffu, q, 1);
+  unsigned short* out16 = reinterpret_cast<unsigned short*>(xq + blk * 34);
+  if ((lane & 1) == 0)
+    out16[1 + (lane >> 1)] = (unsigned short)(((unsigned)q & 0xFFu) | (((unsigned)q_next & 0xFFu) << 8));
+  if (lane == 0) out16[0] = __half_as_ushort(__float2half_rn(d));
 }
 
 }  // namespace
@@ -52,6 +52,7 @@ cudaError_t launch_quantize_q8_0(const float* x, int64_t n_rows, int64_t cols, v
   const long long n_blocks = (long long)n_rows * (cols / 32);
   if (n_blocks == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((n_blocks + 7) / 8);
+  if (dry_run()) return cudaSuccess;
   quantize_q8_0_kernel<<<grid, 256, 0, st>>>(x, n_blocks, static_cast<uint8_t*>(xq));
   return cudaGetLastError();
 }

@@ -26,8 +26,9 @@ namespace dsbk {
 
 namespace {
 
-__global__ void rope_posvec_kernel(float* __restrict__ q, int n_q_heads, float* __restrict__ k, int n_kv_heads,
-                                   int head_dim, const int32_t* __restrict__ pos, double theta) {
+__global__ void rope_posvec_kernel(float* __restrict__ q, long long q_stride, int n_q_heads, float* __restrict__ k,
+                                   long long k_stride, int n_kv_heads, int head_dim, const int32_t* __restrict__ pos,
+                                   double theta) {
   const int t = blockIdx.x;
   const int half = head_dim >> 1;
   const int i = threadIdx.x;
@@ -37,7 +38,7 @@ __global__ void rope_posvec_kernel(float* __restrict__ q, int n_q_heads, float* 
   double sd, cd;
   sincos(ang, &sd, &cd);
   const float s = (float)sd, c = (float)cd;
-  float* qt = q + (size_t)t * n_q_heads * head_dim;
+  float* qt = q + (size_t)t * q_stride;
   for (int h = 0; h < n_q_heads; ++h) {
     float* x = qt + (size_t)h * head_dim;
     const float x1 = x[i], x2 = x[i + half];
@@ -45,7 +46,7 @@ __global__ void rope_posvec_kernel(float* __restrict__ q, int n_q_heads, float* 
     x[i + half] = __fmaf_rn(x1, s, __fmul_rn(x2, c));
   }
   if (k) {
-    float* kt = k + (size_t)t * n_kv_heads * head_dim;
+    float* kt = k + (size_t)t * k_stride;
     for (int h = 0; h < n_kv_heads; ++h) {
       float* x = kt + (size_t)h * head_dim;
       const float x1 = x[i], x2 = x[i + half];
@@ -71,12 +72,12 @@ template <typename T>
 __global__ void kv_scatter_kernel(T* __restrict__ kc, T* __restrict__ vc, int n_kv_heads, int ctx, int head_dim,
                                   const int32_t* __restrict__ batch_index, int tokens_per_seq,
                                   const int32_t* __restrict__ pos, const float* __restrict__ k,
-                                  const float* __restrict__ v) {
+                                  const float* __restrict__ v, long long kv_stride) {
   const int t = blockIdx.x, h = blockIdx.y;
   const int slot = batch_index[t / tokens_per_seq];
   const int p = pos[t];
   const size_t dst = (((size_t)slot * n_kv_heads + h) * ctx + p) * head_dim;
-  const size_t src = ((size_t)t * n_kv_heads + h) * head_dim;
+  const size_t src = (size_t)t * kv_stride + (size_t)h * head_dim;
   for (int d = threadIdx.x; d < head_dim; d += blockDim.x) {
     kc[dst + d] = cvt_rn<T>(k[src + d]);
     vc[dst + d] = cvt_rn<T>(v[src + d]);
@@ -85,30 +86,34 @@ __global__ void kv_scatter_kernel(T* __restrict__ kc, T* __restrict__ vc, int n_
 
 }  // namespace
 
-cudaError_t launch_rope_posvec(float* q, int n_q_heads, float* k, int n_kv_heads, int head_dim, int n_tok,
-                               const int32_t* pos_dev, float theta, cudaStream_t st) {
+cudaError_t launch_rope_posvec(float* q, long long q_stride, int n_q_heads, float* k, long long k_stride,
+                               int n_kv_heads, int head_dim, int n_tok, const int32_t* pos_dev, float theta,
+                               cudaStream_t st) {
   if (n_tok == 0) return cudaSuccess;
   const int half = head_dim / 2;
   const int threads = ((half + 31) / 32) * 32;
-  rope_posvec_kernel<<<n_tok, threads, 0, st>>>(q, n_q_heads, k, n_kv_heads, head_dim, pos_dev, (double)theta);
+  if (dry_run()) return cudaSuccess;
+  rope_posvec_kernel<<<n_tok, threads, 0, st>>>(q, q_stride, n_q_heads, k, k_stride, n_kv_heads, head_dim, pos_dev,
+                                                 (double)theta);
   return cudaGetLastError();
 }
 
 cudaError_t launch_kv_scatter(void* kc, void* vc, int dtype, int n_kv_heads, int ctx, int head_dim,
                               const int32_t* batch_index_dev, int tokens_per_seq, const int32_t* pos_dev, int n_tok,
-                              const float* k, const float* v, cudaStream_t st) {
+                              const float* k, const float* v, long long kv_stride, cudaStream_t st) {
   if (n_tok == 0) return cudaSuccess;
   const dim3 grid((unsigned)n_tok, (unsigned)n_kv_heads);
   const int threads = head_dim < 256 ? ((head_dim + 31) / 32) * 32 : 256;
+  if (dry_run()) return cudaSuccess;
   if (dtype == 0)
     kv_scatter_kernel<__half><<<grid, threads, 0, st>>>(static_cast<__half*>(kc), static_cast<__half*>(vc),
                                                          n_kv_heads, ctx, head_dim, batch_index_dev, tokens_per_seq,
-                                                         pos_dev, k, v);
+                                                         pos_dev, k, v, kv_stride);
   else
     kv_scatter_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(static_cast<__nv_bfloat16*>(kc),
                                                                 static_cast<__nv_bfloat16*>(vc), n_kv_heads, ctx,
                                                                 head_dim, batch_index_dev, tokens_per_seq, pos_dev,
-                                                                k, v);
+                                                                k, v, kv_stride);
   return cudaGetLastError();
 }
 

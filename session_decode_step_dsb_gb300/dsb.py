@@ -204,8 +204,12 @@ def rope_posvec(q, k, pos, theta: float, ws: Workspace, stream=None):
 
 
 def kv_cache(k_cache, v_cache, dtype: int) -> KVCache:
+    """Describe device caches ``[F, Hkv, ctx, D]``; the returned struct keeps
+    the two tensors alive for as long as it lives."""
     f, hkv, ctx, d = k_cache.shape
-    return KVCache(_ptr(k_cache), _ptr(v_cache), dtype, f, hkv, ctx, d)
+    kv = KVCache(_ptr(k_cache), _ptr(v_cache), dtype, f, hkv, ctx, d)
+    kv._tensors = (k_cache, v_cache)
+    return kv
 
 
 def kv_scatter(kv: KVCache, batch_index, tokens_per_seq: int, pos, k, v, ws: Workspace, stream=None):
@@ -226,3 +230,125 @@ def attention_decode_multi(q, kv: KVCache, batch_index, tokens_per_seq: int, seq
     _check(lib().dsb_attention_decode_multi(_ptr(q), hq, ctypes.byref(kv), pbi, len(bi), tokens_per_seq, psl,
                                             _ptr(out), ws.handle, _stream(stream)))
     return out
+
+
+# ---------------------------------------------------------------- decode step
+class ModelShapeC(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("ffn", ctypes.c_int32), ("vocab", ctypes.c_int32),
+                ("n_layers", ctypes.c_int32), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)]
+
+
+class LayerC(ctypes.Structure):
+    _fields_ = [("wqkv", Q8Mat), ("wo", Q8Mat), ("wgu", Q8Mat), ("wdown", Q8Mat), ("attn_norm", ctypes.c_void_p),
+                ("ffn_norm", ctypes.c_void_p), ("kv", KVCache)]
+
+
+class ModelC(ctypes.Structure):
+    _fields_ = [("shape", ModelShapeC), ("embed", ctypes.c_void_p), ("layers", ctypes.POINTER(LayerC)),
+                ("final_norm", ctypes.c_void_p), ("head", Q8Mat)]
+
+
+SIGNATURES.update({
+    "dsb_step_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(ModelShapeC), _I, _I]),
+    "dsb_decode_step": (_I, [ctypes.POINTER(ModelC), _PI32, _PI32, _I, _I, _PI32, _P, _P, _P]),
+    "dsb_step_graph_create": (_I, [ctypes.POINTER(ModelC), _I, _I, _P, _P, _P, ctypes.POINTER(_P)]),
+    "dsb_step_graph_launch": (_I, [_P, _PI32, _PI32, _PI32, _P]),
+    "dsb_step_graph_destroy": (_I, [_P]),
+})
+
+
+class StepWorkspace(Workspace):
+    """Workspace sized for decode steps of up to ``max_tokens`` rows."""
+
+    def __init__(self, shape: ModelShapeC, max_tokens: int, ctx: int, device=None):
+        import torch
+        nbytes = lib().dsb_step_workspace_bytes(ctypes.byref(shape), max_tokens, ctx)
+        if nbytes == 0:
+            raise ValueError("step workspace size arguments out of range")
+        self.buffer = torch.empty(nbytes + 256, dtype=torch.uint8, device=device or "cuda")
+        aligned = (self.buffer.data_ptr() + 255) // 256 * 256
+        handle = _P()
+        _check(lib().dsb_workspace_create(_P(aligned), nbytes, ctypes.byref(handle)))
+        self.handle = handle
+        self.nbytes = nbytes
+
+
+class DecodeModel:
+    """Device tensors of a llama-style q8_0 model plus its retained KV caches,
+    described to the library as a ``dsb_model``.
+
+    ``weights`` maps names to *device* tensors: q8_0 byte matrices ``embed,
+    head`` and per-layer lists ``wqkv, wo, wgu, wdown``; float32 ``final_norm``
+    and per-layer ``attn_norm, ffn_norm``.  ``k_caches / v_caches`` are per-layer
+    device tensors ``[F, Hkv, ctx, D]`` of a 16-bit dtype.
+    """
+
+    def __init__(self, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, n_layers, weights, k_caches, v_caches,
+                 cache_dtype: int, rms_eps=1e-6, rope_theta=10000.0):
+        self.shape = ModelShapeC(hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, n_layers, rms_eps, rope_theta)
+        self.w = weights
+        self.k_caches, self.v_caches = k_caches, v_caches
+        qkv_rows = (n_q_heads + 2 * n_kv_heads) * head_dim
+        layers = (LayerC * n_layers)()
+        for l in range(n_layers):
+            layers[l].wqkv = _mat(weights["wqkv"][l], qkv_rows, hidden)
+            layers[l].wo = _mat(weights["wo"][l], hidden, n_q_heads * head_dim)
+            layers[l].wgu = _mat(weights["wgu"][l], 2 * ffn, hidden)
+            layers[l].wdown = _mat(weights["wdown"][l], hidden, ffn)
+            layers[l].attn_norm = _ptr(weights["attn_norm"][l])
+            layers[l].ffn_norm = _ptr(weights["ffn_norm"][l])
+            layers[l].kv = kv_cache(k_caches[l], v_caches[l], cache_dtype)
+        self._layers = layers
+        self.c = ModelC(self.shape, _ptr(weights["embed"]), layers, _ptr(weights["final_norm"]),
+                        _mat(weights["head"], vocab, hidden))
+        self.vocab = vocab
+        self.ctx = k_caches[0].shape[2]
+        self.full_batch_size = k_caches[0].shape[0]
+
+    def workspace(self, max_tokens: int) -> StepWorkspace:
+        return StepWorkspace(self.shape, max_tokens, self.ctx)
+
+    def step(self, token_ids, batch_index, tokens_per_seq: int, seq_lens, ws: Workspace, logits=None, stream=None):
+        import torch
+        n_seq = len(batch_index)
+        if logits is None:
+            logits = torch.empty((n_seq * tokens_per_seq, self.vocab), dtype=torch.float32, device="cuda")
+        tk, ptk = _i32(token_ids)
+        bi, pbi = _i32(batch_index)
+        sl, psl = _i32(seq_lens)
+        _check(lib().dsb_decode_step(ctypes.byref(self.c), ptk, pbi, n_seq, tokens_per_seq, psl, _ptr(logits),
+                                     ws.handle, _stream(stream)))
+        return logits
+
+    def graph(self, n_seq: int, tokens_per_seq: int, logits, ws: Workspace, stream=None) -> "StepGraph":
+        return StepGraph(self, n_seq, tokens_per_seq, logits, ws, stream)
+
+
+class StepGraph:
+    """A decode step captured once for a fixed (n_seq, T) and replayed."""
+
+    def __init__(self, model: DecodeModel, n_seq: int, tokens_per_seq: int, logits, ws: Workspace, stream=None):
+        self.model, self.logits, self.ws = model, logits, ws
+        handle = _P()
+        _check(lib().dsb_step_graph_create(ctypes.byref(model.c), n_seq, tokens_per_seq, _ptr(logits), ws.handle,
+                                           _stream(stream), ctypes.byref(handle)))
+        self.handle = handle
+
+    def launch(self, token_ids, batch_index, seq_lens, stream=None):
+        tk, ptk = _i32(token_ids)
+        bi, pbi = _i32(batch_index)
+        sl, psl = _i32(seq_lens)
+        _check(lib().dsb_step_graph_launch(self.handle, ptk, pbi, psl, _stream(stream)))
+        return self.logits
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().dsb_step_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -7,37 +7,16 @@ dense stages and long context on the ds4 page).  Every value is drawn by
 """
 from __future__ import annotations
 
-from dataclasses import dataclass
-
 import numpy as np
 
 from session_decode_step_dsb_gb300 import synth
 
 
-@dataclass(frozen=True)
-class ModelShape:
-    hidden: int
-    n_q_heads: int
-    n_kv_heads: int
-    head_dim: int
-    ffn: int
-    vocab: int
-    n_layers: int
-    full_batch_size: int
-    ctx: int
-    cache_dtype: str
-    eps: float = 1e-6
-    theta: float = 10000.0
+from session_decode_step_dsb_gb300.workloads import LLAMA68M, ModelShape  # noqa: F401
 
-    @property
-    def qkv_rows(self):
-        return (self.n_q_heads + 2 * self.n_kv_heads) * self.head_dim
-
-
-LLAMA68M = ModelShape(768, 12, 12, 64, 3072, 32000, 2, 8, 2048, "f16")
-QWEN3_14B_1L = ModelShape(5120, 40, 8, 128, 17408, 151936, 1, 16, 4096, "bf16")
-TINY = ModelShape(256, 4, 2, 64, 512, 1000, 2, 4, 96, "f16")
-TINY_BF16 = ModelShape(256, 8, 2, 32, 384, 700, 1, 5, 80, "bf16")
+QWEN3_14B_1L = ModelShape("qwen3-14b-shaped-1-layer", 5120, 40, 8, 128, 17408, 151936, 1, 16, 4096, "bf16")
+TINY = ModelShape("tiny", 256, 4, 2, 64, 512, 1000, 2, 4, 96, "f16")
+TINY_BF16 = ModelShape("tiny-bf16", 512, 8, 2, 128, 768, 700, 1, 5, 300, "bf16")
 
 W_STD = 0.02
 
