@@ -208,12 +208,19 @@ def step_bytes(ms, b, T, lens):
 
 
 # ----------------------------------------------------------------- timing helpers
+# GPU cycles of busy-wait enqueued before each start event, so that the host
+# (Python, ctypes, argument checks, graph launch) has enqueued the timed work
+# before the device reaches it: the events then bracket device time only.
+HOST_SLACK_CYCLES = 200_000
+
+
 def _time_device(fn, iters, flush, stream):
     """Median and mean device time (ms) of fn(), L2 flushed before each call."""
     import torch
     ts = []
     for _ in range(iters):
         flush.zero_()
+        torch.cuda._sleep(HOST_SLACK_CYCLES)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
