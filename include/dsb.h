@@ -189,6 +189,26 @@ dsb_status dsb_attention_decode_multi(const float* q, int n_q_heads, const dsb_k
                                       const int32_t* seq_lens, float* out, dsb_workspace* ws,
                                       void* stream);
 
+/* Decode attention for callers that cannot allocate device memory: code
+ * running inside an allocator hook or memory-pool callback, processes whose
+ * device allocator belongs to another framework that forbids outside
+ * allocations, or latency-critical loops that must not take allocator locks.
+ * The pages describe no such entry point; it is an addition of this library.
+ * Same arguments, result and error behaviour as dsb_attention_decode_multi, but
+ * no workspace: the split-K partials and the sequence table live in one static
+ * 16 MiB device array that every device holds while the library is loaded.
+ *   - The first call on a device looks up that array's address (with the
+ *     device current); make that first call before any stream capture.
+ *   - Limits: n_seq <= 256, and n_tok * n_q_heads * ceil(ctx/128) *
+ *     (head_dim + 2) * 4 bytes of partials must fit in 16 MiB - 4 KiB;
+ *     larger calls return DSB_ERR_UNSUPPORTED with a message.
+ *   - All calls share the array: calls that overlap on the GPU (other streams,
+ *     other threads) race; serialise them.  Nothing in it needs zeroing.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine. */
+dsb_status dsb_attention_decode_multi_noalloc(const float* q, int n_q_heads, const dsb_kv_cache* kv,
+                                              const int32_t* batch_index, int n_seq, int tokens_per_seq,
+                                              const int32_t* seq_lens, float* out, void* stream);
+
 /* ---- the whole decode step -------------------------------------------------
  * A llama-style pre-norm decoder driven through the kernels above, one pass
  * for all live sessions ([DS4] "What" and "Design note": dense stages batched

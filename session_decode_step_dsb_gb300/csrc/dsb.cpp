@@ -791,3 +791,57 @@ dsb_status dsb_step_graph_destroy(dsb_step_graph* g) {
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// Attention for callers that cannot allocate (declared in include/dsb.h).
+// ===========================================================================
+extern "C" dsb_status dsb_attention_decode_multi_noalloc(const float* q, int n_q_heads, const dsb_kv_cache* kv,
+                                                         const int32_t* batch_index, int n_seq, int tokens_per_seq,
+                                                         const int32_t* seq_lens, float* out, void* stream) {
+  dsb_status st = check_kv(kv);
+  if (st != DSB_OK) return st;
+  if (n_q_heads < 1 || n_q_heads % kv->n_kv_heads)
+    return fail(DSB_ERR_INVALID_ARG, "n_q_heads=%d is not a positive multiple of n_kv_heads=%d", n_q_heads,
+                kv->n_kv_heads);
+  st = check_batch(kv, batch_index, n_seq, tokens_per_seq);
+  if (st != DSB_OK) return st;
+  if (n_seq > dsbk::kNoAllocMaxSeqs)
+    return fail(DSB_ERR_UNSUPPORTED, "n_seq=%d exceeds the no-allocation limit of %d sequences", n_seq,
+                dsbk::kNoAllocMaxSeqs);
+  if (kv->head_dim != 64 && kv->head_dim != 128)
+    return fail(DSB_ERR_UNSUPPORTED, "head_dim=%d: attention serves 64 and 128", kv->head_dim);
+  const long long R = (long long)(n_q_heads / kv->n_kv_heads) * tokens_per_seq;
+  if (R > 64) return fail(DSB_ERR_UNSUPPORTED, "query rows per kv head (G*T=%lld) exceed 64", R);
+  if (!q || !out || !seq_lens) return fail(DSB_ERR_INVALID_ARG, "q / out / seq_lens is NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(DSB_ERR_INVALID_ARG, "q / out not 16-byte aligned");
+  for (int s = 0; s < n_seq; ++s)
+    if (seq_lens[s] < tokens_per_seq || seq_lens[s] > kv->ctx)
+      return fail(DSB_ERR_INVALID_ARG, "seq_lens[%d]=%d out of [T=%d, ctx=%d]", s, seq_lens[s], tokens_per_seq, kv->ctx);
+  const int n_tok = n_seq * tokens_per_seq;
+  const size_t need = dsbk::attention_partial_bytes(n_tok, n_q_heads, kv->head_dim, kv->ctx);
+  if (need > dsbk::kNoAllocScratchBytes - dsbk::kNoAllocTableBytes)
+    return fail(DSB_ERR_UNSUPPORTED,
+                "attention needs %zu bytes of partials; the no-allocation scratch holds %zu (use "
+                "dsb_attention_decode_multi with a workspace)",
+                need, dsbk::kNoAllocScratchBytes - dsbk::kNoAllocTableBytes);
+  std::vector<int32_t> chunk_off((size_t)n_seq + 1, 0);
+  long long total = 0;
+  for (int s = 0; s < n_seq; ++s) {
+    total += (seq_lens[s] + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
+    chunk_off[(size_t)s + 1] = (int32_t)total;
+  }
+  void* scratch = nullptr;
+  cudaError_t e = dsbk::noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  e = dsbk::launch_noalloc_table(batch_index, seq_lens, chunk_off.data(), n_seq, scratch, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "no-allocation sequence table");
+  const int32_t* table = static_cast<const int32_t*>(scratch);
+  dsbk::MetaView mv{table, table + n_seq, table + 2 * n_seq, nullptr};
+  float* partials = reinterpret_cast<float*>(static_cast<char*>(scratch) + dsbk::kNoAllocTableBytes);
+  const int max_chunks = (kv->ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
+  e = dsbk::launch_attention_decode_multi(q, (long long)n_q_heads * kv->head_dim, n_q_heads, kv->k, kv->v, kv->dtype,
+                                          kv->n_kv_heads, kv->ctx, kv->head_dim, mv, n_seq, tokens_per_seq,
+                                          total * kv->n_kv_heads, max_chunks, partials, out, cs);
+  return e == cudaSuccess ? DSB_OK : cuda_fail(e, "attention_decode_multi_noalloc launch");
+}

@@ -60,6 +60,15 @@ cudaError_t launch_silu_mul_quant(const float* gu, int n_tok, int ffn, void* xq,
 cudaError_t launch_embed(const void* table, int hidden, const int32_t* tokens_dev, int n_tok, float* h,
                          cudaStream_t st);
 
+// Scratch of dsb_attention_decode_multi_noalloc (csrc/noalloc.cu): a static
+// device array, looked up once per device.
+constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
+constexpr int kNoAllocMaxSeqs = 256;
+constexpr size_t kNoAllocTableBytes = 4096;  // the sequence table at the start of the array
+cudaError_t noalloc_scratch(void** out);
+cudaError_t launch_noalloc_table(const int32_t* batch_index, const int32_t* seq_lens, const int32_t* chunk_off,
+                                 int n_seq, void* scratch, cudaStream_t st);
+
 unsigned int read_clear_error_matmul();
 unsigned int read_clear_error_attention();
 

@@ -64,6 +64,7 @@ SIGNATURES = {
     "dsb_rope_posvec": (_I, [_P, _I, _P, _I, _I, _I, _PI32, _F, _P, _P]),
     "dsb_kv_scatter": (_I, [ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P, _P, _P]),
     "dsb_attention_decode_multi": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P, _P]),
+    "dsb_attention_decode_multi_noalloc": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P]),
 }
 
 
@@ -201,6 +202,21 @@ def rope_posvec(q, k, pos, theta: float, ws: Workspace, stream=None):
     hkv = 0 if k is None else k.shape[1]
     arr, p = _i32(pos)
     _check(lib().dsb_rope_posvec(_ptr(q), hq, _ptr(k), hkv, d, n_tok, p, float(theta), ws.handle, _stream(stream)))
+
+
+def attention_decode_multi_noalloc(q, kv: KVCache, batch_index, tokens_per_seq: int, seq_lens, out=None,
+                                   stream=None):
+    """Same as :func:`attention_decode_multi` without a workspace: for callers
+    that cannot allocate device memory (the library's static scratch is used;
+    calls that overlap on the GPU must be serialised)."""
+    import torch
+    if out is None:
+        out = torch.empty_like(q)
+    bi, pbi = _i32(batch_index)
+    sl, psl = _i32(seq_lens)
+    _check(lib().dsb_attention_decode_multi_noalloc(_ptr(q), q.shape[1], ctypes.byref(kv), pbi, len(bi),
+                                                    tokens_per_seq, psl, _ptr(out), _stream(stream)))
+    return out
 
 
 def kv_cache(k_cache, v_cache, dtype: int) -> KVCache:
