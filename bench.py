@@ -410,10 +410,10 @@ def run_dsb(args):
 
 
 def launches_per_step(ms) -> int:
-    """Kernels of one step: embed + per layer (rmsnorm-q8, QKV, rope, KV write,
-    attention partial + merge, quantise, O, rmsnorm-q8, gate|up, silu-q8,
-    down) + final rmsnorm-q8 + head."""
-    return 1 + 12 * ms.n_layers + 2
+    """Kernels of one step: embed + per layer (rmsnorm-q8, QKV, RoPE+KV write,
+    attention partial, merge-q8, O, rmsnorm-q8, gate|up, silu-q8, down) +
+    final rmsnorm-q8 + head."""
+    return 1 + 10 * ms.n_layers + 2
 
 
 # ----------------------------------------------------------------- CPU oracle

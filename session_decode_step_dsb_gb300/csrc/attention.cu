@@ -35,6 +35,7 @@
 
 #include "dsb_kernels.h"
 #include "dsb_ptx.cuh"
+#include "dsb_q8.cuh"
 
 namespace dsbk {
 
@@ -72,6 +73,8 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
   extern __shared__ __align__(128) uint8_t smem[];
   const int G = n_q_heads / n_kv_heads, R = G * tps;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();
+  pdl_wait();  // q and the cache rows of this step come from the previous kernels
 
   T* Vs = reinterpret_cast<T*>(smem);                                        // [kCh][D]
   float* qs = reinterpret_cast<float*>(smem + (size_t)kCh * D * sizeof(T));  // [R][D]
@@ -250,10 +253,18 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
   }  // work items
 }
 
-template <int D>
+// One warp per (token row, query head).  Lanes first take the chunks 32 at a
+// time (max of m_c, then w_c = exp(m_c - M) and the partial sum of w_c l_c);
+// the sums over lanes use a fixed xor tree; then the warp walks the chunks in
+// order, lane d accumulating w_c * acc_c[d].  With QOUT the normalised row is
+// q8_0-quantised (D / 32 blocks per head) straight into xq.
+template <int D, bool QOUT>
 __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __restrict__ partials, int n_q_heads,
                                                               int tps, const int32_t* __restrict__ seq_lens,
-                                                              int max_chunks, int n_tok, float* __restrict__ out) {
+                                                              int max_chunks, int n_tok, float* __restrict__ out,
+                                                              uint8_t* __restrict__ xq) {
+  pdl_trigger();
+  pdl_wait();
   const int wg = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (wg >= n_tok * n_q_heads) return;
@@ -263,21 +274,39 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
   const int nch = (vis + kCh - 1) / kCh;
   const float* base = partials + ((size_t)t * n_q_heads + h) * max_chunks * (D + 2);
   float M = -INFINITY;
-  for (int c = 0; c < nch; ++c) M = fmaxf(M, base[(size_t)c * (D + 2)]);
-  float Lsum = 0.0f;
+  for (int c = lane; c < nch; c += 32) M = fmaxf(M, base[(size_t)c * (D + 2)]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float lsum = 0.0f;
   float acc[D / 32];
 #pragma unroll
   for (int e = 0; e < D / 32; ++e) acc[e] = 0.0f;
-  for (int c = 0; c < nch; ++c) {
-    const float* pc = base + (size_t)c * (D + 2);
-    const float wgt = expf(pc[0] - M);
-    Lsum = __fmaf_rn(wgt, pc[1], Lsum);
+  for (int c0 = 0; c0 < nch; c0 += 32) {
+    float wl = 0.0f;
+    if (c0 + lane < nch) {
+      const float* pc = base + (size_t)(c0 + lane) * (D + 2);
+      wl = expf(pc[0] - M);
+      lsum = __fmaf_rn(wl, pc[1], lsum);
+    }
+    const int n = min(32, nch - c0);
+    for (int cc = 0; cc < n; ++cc) {
+      const float wc = __shfl_sync(0xffffffffu, wl, cc);
+      const float* pc = base + (size_t)(c0 + cc) * (D + 2) + 2;
 #pragma unroll
-    for (int e = 0; e < D / 32; ++e) acc[e] = __fmaf_rn(wgt, pc[2 + lane + 32 * e], acc[e]);
+      for (int e = 0; e < D / 32; ++e) acc[e] = __fmaf_rn(wc, pc[lane + 32 * e], acc[e]);
+    }
   }
-  float* o = out + ((size_t)t * n_q_heads + h) * D;
 #pragma unroll
-  for (int e = 0; e < D / 32; ++e) o[lane + 32 * e] = __fdiv_rn(acc[e], Lsum);
+  for (int o = 1; o < 32; o <<= 1) lsum = __fadd_rn(lsum, __shfl_xor_sync(0xffffffffu, lsum, o));
+  if constexpr (QOUT) {
+    uint8_t* dst = xq + ((size_t)t * n_q_heads + h) * (D / 32) * 34;
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) q8_block_store(__fdiv_rn(acc[e], lsum), dst + (size_t)e * 34, lane);
+  } else {
+    float* o = out + ((size_t)t * n_q_heads + h) * D;
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) o[lane + 32 * e] = __fdiv_rn(acc[e], lsum);
+  }
 }
 
 template <int D, typename T>
@@ -291,7 +320,7 @@ template <int D, typename T>
 cudaError_t launch_typed(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc,
                          int n_kv_heads, int ctx,
                          MetaView meta, int n_seq, int tps, long long max_items, int max_chunks, float* partials,
-                         float* out, cudaStream_t st) {
+                         float* out, void* xq_out, cudaStream_t st) {
   const int R = (n_q_heads / n_kv_heads) * tps;
   const size_t smem = partial_smem<D, T>(R);
   auto kern = attention_partial_kernel<D, T>;
@@ -314,17 +343,17 @@ cudaError_t launch_typed(const float* q, long long q_stride, int n_q_heads, cons
   }
   const long long items = (long long)max_items;
   const unsigned grid = (unsigned)(items < resident ? (items > 0 ? items : 1) : resident);
-  if (dry_run()) return cudaSuccess;
-  kern<<<grid, kThreads, smem, st>>>(
-      q, q_stride, n_q_heads, static_cast<const T*>(kc), static_cast<const T*>(vc), n_kv_heads, ctx, meta.batch_index,
-      meta.seq_lens, meta.chunk_off, n_seq, tps, max_chunks, scale, partials);
-  e = cudaGetLastError();
+  e = launch_kernel(kern, dim3(grid), dim3(kThreads), smem, st, q, q_stride, n_q_heads, static_cast<const T*>(kc),
+                    static_cast<const T*>(vc), n_kv_heads, ctx, meta.batch_index, meta.seq_lens, meta.chunk_off,
+                    n_seq, tps, max_chunks, scale, partials);
   if (e != cudaSuccess) return e;
   const int n_tok = n_seq * tps;
   const unsigned mgrid = (unsigned)((n_tok * n_q_heads + 3) / 4);
-  if (dry_run()) return cudaSuccess;
-  attention_merge_kernel<D><<<mgrid, 128, 0, st>>>(partials, n_q_heads, tps, meta.seq_lens, max_chunks, n_tok, out);
-  return cudaGetLastError();
+  if (xq_out)
+    return launch_kernel(attention_merge_kernel<D, true>, dim3(mgrid), dim3(128), 0, st, partials, n_q_heads, tps,
+                         meta.seq_lens, max_chunks, n_tok, out, static_cast<uint8_t*>(xq_out));
+  return launch_kernel(attention_merge_kernel<D, false>, dim3(mgrid), dim3(128), 0, st, partials, n_q_heads, tps,
+                       meta.seq_lens, max_chunks, n_tok, out, static_cast<uint8_t*>(nullptr));
 }
 
 }  // namespace
@@ -338,21 +367,21 @@ cudaError_t launch_attention_decode_multi(const float* q, long long q_stride, in
                                           const void* vc, int dtype,
                                           int n_kv_heads, int ctx, int head_dim, MetaView meta, int n_seq,
                                           int tokens_per_seq, long long max_items, int max_chunks, float* partials,
-                                          float* out, cudaStream_t st) {
+                                          float* out, void* xq_out, cudaStream_t st) {
   if (n_seq == 0) return cudaSuccess;
   if (head_dim == 128) {
     if (dtype == 0)
       return launch_typed<128, __half>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
-                                       max_items, max_chunks, partials, out, st);
+                                       max_items, max_chunks, partials, out, xq_out, st);
     return launch_typed<128, __nv_bfloat16>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
-                                            max_items, max_chunks, partials, out, st);
+                                            max_items, max_chunks, partials, out, xq_out, st);
   }
   if (head_dim == 64) {
     if (dtype == 0)
       return launch_typed<64, __half>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
-                                      max_items, max_chunks, partials, out, st);
+                                      max_items, max_chunks, partials, out, xq_out, st);
     return launch_typed<64, __nv_bfloat16>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
-                                           max_items, max_chunks, partials, out, st);
+                                           max_items, max_chunks, partials, out, xq_out, st);
   }
   return cudaErrorInvalidValue;
 }

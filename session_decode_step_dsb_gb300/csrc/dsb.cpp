@@ -313,8 +313,10 @@ dsb_status dsb_rope_posvec(float* q, int n_q_heads, float* k, int n_kv_heads, in
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   dsb_status s = stage(ws, words, st, &dev);
   if (s != DSB_OK) return s;
+  static thread_local dsbk::RopeFreqs freqs;
+  dsbk::rope_freqs((double)theta, head_dim, &freqs);
   cudaError_t e = dsbk::launch_rope_posvec(q, (long long)n_q_heads * head_dim, n_q_heads, k,
-                                           (long long)n_kv_heads * head_dim, n_kv_heads, head_dim, n_tok, dev, theta, st);
+                                           (long long)n_kv_heads * head_dim, n_kv_heads, head_dim, n_tok, dev, freqs, st);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "rope_posvec launch");
 }
 
@@ -396,7 +398,7 @@ dsb_status dsb_attention_decode_multi(const float* q, int n_q_heads, const dsb_k
   const int max_chunks = (kv->ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
   cudaError_t e = dsbk::launch_attention_decode_multi(
       q, (long long)n_q_heads * kv->head_dim, n_q_heads, kv->k, kv->v, kv->dtype, kv->n_kv_heads, kv->ctx, kv->head_dim, mv, n_seq, tokens_per_seq,
-      total * kv->n_kv_heads, max_chunks, reinterpret_cast<float*>(partial_base(ws)), out, cs);
+      total * kv->n_kv_heads, max_chunks, reinterpret_cast<float*>(partial_base(ws)), out, nullptr, cs);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "attention_decode_multi launch");
 }
 
@@ -555,22 +557,23 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
   const long long qkv_stride = (long long)(Hq + 2 * Hkv) * D;
   const int max_chunks = (kv0.ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
   const dsbk::MetaView mv{bi_dev, sl_dev, co_dev, pos_dev};
+  static thread_local dsbk::RopeFreqs freqs;
+  dsbk::rope_freqs((double)s.rope_theta, D, &freqs);
+  // The first kernel follows the metadata copy; every later kernel may be
+  // scheduled while its predecessor finishes (programmatic dependent launch).
   cudaError_t e = dsbk::launch_embed(m->embed, s.hidden, tokens_dev, n_tok, h, st);
+  dsbk::set_pdl(true);
   for (int l = 0; l < s.n_layers && e == cudaSuccess; ++l) {
     const dsb_layer& Ly = m->layers[l];
     if ((e = dsbk::launch_rmsnorm_quant(h, Ly.attn_norm, n_tok, s.hidden, s.rms_eps, xq, st)) != cudaSuccess) break;
     if ((e = run_matmul(Ly.wqkv, xq, n_tok, qkv, nullptr, sms, st)) != cudaSuccess) break;
-    if ((e = dsbk::launch_rope_posvec(qkv, qkv_stride, Hq, qkv + (size_t)Hq * D, qkv_stride, Hkv, D, n_tok, pos_dev,
-                                      s.rope_theta, st)) != cudaSuccess)
-      break;
-    if ((e = dsbk::launch_kv_scatter(Ly.kv.k, Ly.kv.v, Ly.kv.dtype, Hkv, Ly.kv.ctx, D, bi_dev, tps, pos_dev, n_tok,
-                                     qkv + (size_t)Hq * D, qkv + (size_t)(Hq + Hkv) * D, qkv_stride, st)) != cudaSuccess)
+    if ((e = dsbk::launch_rope_kv_write(qkv, qkv_stride, Hq, Hkv, D, pos_dev, bi_dev, tps, n_tok, Ly.kv.k, Ly.kv.v,
+                                        Ly.kv.dtype, Ly.kv.ctx, freqs, st)) != cudaSuccess)
       break;
     if ((e = dsbk::launch_attention_decode_multi(qkv, qkv_stride, Hq, Ly.kv.k, Ly.kv.v, Ly.kv.dtype, Hkv, Ly.kv.ctx, D,
-                                                 mv, n_seq, tps, max_items, max_chunks, partials, att, st)) !=
+                                                 mv, n_seq, tps, max_items, max_chunks, partials, att, xq, st)) !=
         cudaSuccess)
       break;
-    if ((e = dsbk::launch_quantize_q8_0(att, n_tok, (int64_t)Hq * D, xq, st)) != cudaSuccess) break;
     if ((e = run_matmul(Ly.wo, xq, n_tok, h, h, sms, st)) != cudaSuccess) break;
     if ((e = dsbk::launch_rmsnorm_quant(h, Ly.ffn_norm, n_tok, s.hidden, s.rms_eps, xq, st)) != cudaSuccess) break;
     if ((e = run_matmul(Ly.wgu, xq, n_tok, gu, nullptr, sms, st)) != cudaSuccess) break;
@@ -579,6 +582,7 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
   }
   if (e == cudaSuccess) e = dsbk::launch_rmsnorm_quant(h, m->final_norm, n_tok, s.hidden, s.rms_eps, xq, st);
   if (e == cudaSuccess) e = run_matmul(m->head, xq, n_tok, logits, nullptr, sms, st);
+  dsbk::set_pdl(false);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "decode step launch");
 }
 
@@ -842,6 +846,6 @@ extern "C" dsb_status dsb_attention_decode_multi_noalloc(const float* q, int n_q
   const int max_chunks = (kv->ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
   e = dsbk::launch_attention_decode_multi(q, (long long)n_q_heads * kv->head_dim, n_q_heads, kv->k, kv->v, kv->dtype,
                                           kv->n_kv_heads, kv->ctx, kv->head_dim, mv, n_seq, tokens_per_seq,
-                                          total * kv->n_kv_heads, max_chunks, partials, out, cs);
+                                          total * kv->n_kv_heads, max_chunks, partials, out, nullptr, cs);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "attention_decode_multi_noalloc launch");
 }

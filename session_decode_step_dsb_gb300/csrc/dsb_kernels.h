@@ -14,6 +14,32 @@ namespace dsbk {
 void set_dry_run(bool on);
 bool dry_run();
 
+// When set (per host thread), kernels launched through launch_kernel carry the
+// programmatic-stream-serialization attribute, so that each kernel of the
+// decode step may be scheduled while its predecessor finishes (its CTAs wait
+// in pdl_wait() before touching the predecessor's results).
+void set_pdl(bool on);
+bool pdl();
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                 Args... args) {
+  if (dry_run()) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (pdl()) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Per-call metadata staged in device memory (workspace), int32 words:
 //   [0] n_seq  [1] tokens_per_seq  [2] n_tok  [3] total attention chunks
 //   then batch_index[n_seq], seq_lens[n_seq], chunk_off[n_seq + 1], pos[n_tok]
@@ -33,11 +59,23 @@ cudaError_t launch_matmul_q8_0_narrow(const void* W, int64_t rows, int64_t cols,
 
 cudaError_t launch_quantize_q8_0(const float* x, int64_t n_rows, int64_t cols, void* xq, cudaStream_t st);
 
+// Float64 frequencies theta^(-2i/D) of the rotate-half pairs (a model
+// constant), passed to the RoPE kernels by value.
+constexpr int kRopeMaxPairs = 512;
+struct RopeFreqs {
+  double f[kRopeMaxPairs];
+};
+void rope_freqs(double theta, int head_dim, RopeFreqs* out);
+
 // q_stride / k_stride: floats between consecutive token rows.
 cudaError_t launch_rope_posvec(float* q, long long q_stride, int n_q_heads, float* k, long long k_stride,
-                               int n_kv_heads, int head_dim, int n_tok, const int32_t* pos_dev, float theta,
-                               cudaStream_t st);
-
+                               int n_kv_heads, int head_dim, int n_tok, const int32_t* pos_dev,
+                               const RopeFreqs& freqs, cudaStream_t st);
+// Step-fused RoPE + KV write on the [q | k | v] rows of qkv (row stride `stride`).
+cudaError_t launch_rope_kv_write(float* qkv, long long stride, int n_q_heads, int n_kv_heads, int head_dim,
+                                 const int32_t* pos_dev, const int32_t* batch_index_dev, int tokens_per_seq,
+                                 int n_tok, void* kc, void* vc, int dtype, int ctx, const RopeFreqs& freqs,
+                                 cudaStream_t st);
 cudaError_t launch_kv_scatter(void* kc, void* vc, int dtype, int n_kv_heads, int ctx, int head_dim,
                               const int32_t* batch_index_dev, int tokens_per_seq, const int32_t* pos_dev, int n_tok,
                               const float* k, const float* v, long long kv_stride, cudaStream_t st);
@@ -45,12 +83,14 @@ cudaError_t launch_kv_scatter(void* kc, void* vc, int dtype, int n_kv_heads, int
 // Split-K decode attention: persistent partial kernel over the (chunk, kv head)
 // items listed by meta.chunk_off (count read on the device), then the
 // chunk-order merge.  max_items bounds the item count (sizes the grid);
-// partials: float [n_tok][n_q_heads][max_chunks][head_dim + 2].
+// partials: float [n_tok][n_q_heads][max_chunks][head_dim + 2].  With xq_out
+// non-NULL the merge writes q8_0 rows [n_tok][n_q_heads*head_dim/32 blocks]
+// instead of float32 out.
 cudaError_t launch_attention_decode_multi(const float* q, long long q_stride, int n_q_heads, const void* kc,
                                           const void* vc, int dtype,
                                           int n_kv_heads, int ctx, int head_dim, MetaView meta, int n_seq,
                                           int tokens_per_seq, long long max_items, int max_chunks, float* partials,
-                                          float* out, cudaStream_t st);
+                                          float* out, void* xq_out, cudaStream_t st);
 
 size_t attention_partial_bytes(int n_tok, int n_q_heads, int head_dim, int ctx);
 

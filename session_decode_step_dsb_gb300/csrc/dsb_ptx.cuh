@@ -93,6 +93,14 @@ __device__ __forceinline__ float ld_dsmem_f32(const float* p, uint32_t rank) {
   return v;
 }
 
+// Programmatic dependent launch.  pdl_wait() blocks until the grid this one
+// depends on has completed and its writes are visible (a no-op when the launch
+// carries no programmatic dependency); pdl_trigger() lets the dependent grid be
+// scheduled once every CTA of this grid has issued it or exited.  A kernel
+// writes no global memory before its pdl_wait().
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   uint4 r;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -15,25 +15,12 @@
 #include <cstdint>
 
 #include "dsb_kernels.h"
+#include "dsb_ptx.cuh"
+#include "dsb_q8.cuh"
 
 namespace dsbk {
 
 namespace {
-
-// q8_0-quantise one 32-value block held one value per lane and store it.
-__device__ __forceinline__ void quant_block_store(float v, uint8_t* out_block, int lane) {
-  float a = fabsf(v);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-  const float d = __fdiv_rn(a, 127.0f);
-  int q = 0;
-  if (d != 0.0f) q = (int)fminf(fmaxf(roundf(__fdiv_rn(v, d)), -127.0f), 127.0f);
-  const int q_next = __shfl_down_sync(0xffffffffu, q, 1);
-  unsigned short* out16 = reinterpret_cast<unsigned short*>(out_block);
-  if ((lane & 1) == 0)
-    out16[1 + (lane >> 1)] = (unsigned short)(((unsigned)q & 0xFFu) | (((unsigned)q_next & 0xFFu) << 8));
-  if (lane == 0) out16[0] = __half_as_ushort(__float2half_rn(d));
-}
 
 constexpr int kGlueThreads = 256;
 
@@ -43,6 +30,8 @@ __global__ void __launch_bounds__(kGlueThreads) rmsnorm_quant_kernel(const float
                                                                      const float* __restrict__ w, int hidden,
                                                                      float eps, uint8_t* __restrict__ xq) {
   __shared__ float part[kGlueThreads / 32];
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   const float* xr = x + (size_t)t * hidden;
   float ss = 0.0f;
@@ -60,13 +49,15 @@ __global__ void __launch_bounds__(kGlueThreads) rmsnorm_quant_kernel(const float
   for (int b = warp; b < hidden / 32; b += kGlueThreads / 32) {
     const int i = b * 32 + lane;
     const float v = __fmul_rn(__fmul_rn(xr[i], inv), w[i]);
-    quant_block_store(v, out + (size_t)b * 34, lane);
+    q8_block_store(v, out + (size_t)b * 34, lane);
   }
 }
 
 // gu: [n_tok][2*ffn] = [gate | up]; out: q8_0 [n_tok][ffn].  One warp per block.
 __global__ void __launch_bounds__(kGlueThreads) silu_mul_quant_kernel(const float* __restrict__ gu, int ffn,
                                                                       long long n_blocks, uint8_t* __restrict__ xq) {
+  pdl_trigger();
+  pdl_wait();
   const long long blk = (long long)blockIdx.x * (kGlueThreads / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (blk >= n_blocks) return;
@@ -76,13 +67,15 @@ __global__ void __launch_bounds__(kGlueThreads) silu_mul_quant_kernel(const floa
   const float g = gu[(size_t)t * 2 * ffn + i];
   const float u = gu[(size_t)t * 2 * ffn + ffn + i];
   const float s = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
-  quant_block_store(__fmul_rn(s, u), xq + (size_t)blk * 34, lane);
+  q8_block_store(__fmul_rn(s, u), xq + (size_t)blk * 34, lane);
 }
 
 // h[t][:] = dequantised q8_0 row token[t] of the embedding table.  One warp per block.
 __global__ void __launch_bounds__(kGlueThreads) embed_kernel(const uint8_t* __restrict__ table, int hidden,
                                                              const int32_t* __restrict__ tokens, long long n_blocks,
                                                              float* __restrict__ h) {
+  pdl_trigger();
+  pdl_wait();
   const long long blk = (long long)blockIdx.x * (kGlueThreads / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (blk >= n_blocks) return;
@@ -101,18 +94,16 @@ __global__ void __launch_bounds__(kGlueThreads) embed_kernel(const uint8_t* __re
 cudaError_t launch_rmsnorm_quant(const float* x, const float* w, int n_tok, int hidden, float eps, void* xq,
                                  cudaStream_t st) {
   if (n_tok == 0) return cudaSuccess;
-  if (dry_run()) return cudaSuccess;
-  rmsnorm_quant_kernel<<<n_tok, kGlueThreads, 0, st>>>(x, w, hidden, eps, static_cast<uint8_t*>(xq));
-  return cudaGetLastError();
+  return launch_kernel(rmsnorm_quant_kernel, dim3(n_tok), dim3(kGlueThreads), 0, st, x, w, hidden, eps,
+                       static_cast<uint8_t*>(xq));
 }
 
 cudaError_t launch_silu_mul_quant(const float* gu, int n_tok, int ffn, void* xq, cudaStream_t st) {
   const long long n_blocks = (long long)n_tok * (ffn / 32);
   if (n_blocks == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((n_blocks + 7) / 8);
-  if (dry_run()) return cudaSuccess;
-  silu_mul_quant_kernel<<<grid, kGlueThreads, 0, st>>>(gu, ffn, n_blocks, static_cast<uint8_t*>(xq));
-  return cudaGetLastError();
+  return launch_kernel(silu_mul_quant_kernel, dim3(grid), dim3(kGlueThreads), 0, st, gu, ffn, n_blocks,
+                       static_cast<uint8_t*>(xq));
 }
 
 cudaError_t launch_embed(const void* table, int hidden, const int32_t* tokens_dev, int n_tok, float* h,
@@ -120,9 +111,8 @@ cudaError_t launch_embed(const void* table, int hidden, const int32_t* tokens_de
   const long long n_blocks = (long long)n_tok * (hidden / 32);
   if (n_blocks == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((n_blocks + 7) / 8);
-  if (dry_run()) return cudaSuccess;
-  embed_kernel<<<grid, kGlueThreads, 0, st>>>(static_cast<const uint8_t*>(table), hidden, tokens_dev, n_blocks, h);
-  return cudaGetLastError();
+  return launch_kernel(embed_kernel, dim3(grid), dim3(kGlueThreads), 0, st, static_cast<const uint8_t*>(table), hidden,
+                       tokens_dev, n_blocks, h);
 }
 
 }  // namespace dsbk

@@ -277,13 +277,15 @@ cudaError_t launch_nt(const uint8_t* W, int rows, int nb, const uint8_t* xq, flo
   static int n_cache = 0;
   static size_t granted = 0;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = (unsigned)S;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl() ? 2 : 1;
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -377,8 +379,11 @@ cudaError_t launch_matmul_q8_0_narrow(const void* W, int64_t rows, int64_t cols,
 namespace {
 thread_local bool g_dry_run = false;
 }
+thread_local bool g_pdl = false;
 void set_dry_run(bool on) { g_dry_run = on; }
 bool dry_run() { return g_dry_run; }
+void set_pdl(bool on) { g_pdl = on; }
+bool pdl() { return g_pdl; }
 
 unsigned int read_clear_error_matmul() {
   unsigned int v = 0, z = 0;

@@ -17,6 +17,7 @@
 #include <cstdint>
 
 #include "dsb_kernels.h"
+#include "dsb_ptx.cuh"
 
 namespace dsbk {
 
@@ -24,6 +25,8 @@ namespace {
 
 __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float* __restrict__ x, long long n_blocks,
                                                            uint8_t* __restrict__ xq) {
+  pdl_trigger();
+  pdl_wait();
   const long long blk = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (blk >= n_blocks) return;
@@ -52,9 +55,7 @@ cudaError_t launch_quantize_q8_0(const float* x, int64_t n_rows, int64_t cols, v
   const long long n_blocks = (long long)n_rows * (cols / 32);
   if (n_blocks == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((n_blocks + 7) / 8);
-  if (dry_run()) return cudaSuccess;
-  quantize_q8_0_kernel<<<grid, 256, 0, st>>>(x, n_blocks, static_cast<uint8_t*>(xq));
-  return cudaGetLastError();
+  return launch_kernel(quantize_q8_0_kernel, dim3(grid), dim3(256), 0, st, x, n_blocks, static_cast<uint8_t*>(xq));
 }
 
 }  // namespace dsbk

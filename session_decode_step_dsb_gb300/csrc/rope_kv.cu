@@ -3,17 +3,23 @@
 // RoPE (antirez/ds4 PR #530, the pos-vector RoPE commit): a batched step
 // evaluates each token row at its own position, so the kernel takes a position
 // per token row instead of pos0 + t.  Rotate-half pairs (i, i + D/2) turn by
-// pos[t] * theta^(-2i/D).  The angle, its reduction and its sine/cosine are
-// evaluated in float64 (positions reach 65535 and a float32 product would be
-// off by ~4e-3 rad there); the rotation itself is float32.  One CTA per token
-// row, one thread per pair, looping over the heads of q and k, so each row's
-// arithmetic is independent of n_tok (row t equals an n_tok = 1 launch).
+// a = pos[t] * theta^(-2i/D).  Positions reach 65535, where a float32 product
+// would be off by ~4e-3 rad, so the angle is formed and reduced in float64:
+// the per-pair frequency theta^(-2i/D) is a float64 table of the model (built
+// on the host from theta and D), a = pos * f is one float64 multiply, and the
+// reduction a - 2 pi k, k = rint(a / 2 pi), uses 2 pi split into two doubles
+// (Cody and Waite's two-constant reduction) so that the remainder is exact to
+// float64 rounding.  sincosf of the reduced float32 angle (|r| <= pi) and the
+// float32 rotation follow.  Each token row's arithmetic is independent of
+// n_tok, so row t equals an n_tok = 1 launch bitwise.
 //
 // KV write (quic/efficient-transformers PR #1305, "Objective": the retained
 // cache is sized for full_batch_size and the live batch addresses it through
 // batch_index; antirez/ds4 PR #530: per-sequence KV append inside the batched
 // step): K[batch_index[s]][h][pos[t]][:] = cvt(k[t][h][:]) for t = s*T + j,
 // cvt = round to nearest even into fp16 or bf16.  Nothing else is written.
+// The decode step uses a fused kernel: RoPE of q and k and the KV write of
+// the rotated k and of v in one pass over the token rows.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -21,38 +27,48 @@
 #include <cstdint>
 
 #include "dsb_kernels.h"
+#include "dsb_ptx.cuh"
 
 namespace dsbk {
 
 namespace {
 
+// 2 pi = kTwoPiHi + kTwoPiLo to ~2^-106 (kTwoPiHi is the double nearest 2 pi).
+constexpr double kTwoPiHi = 6.283185307179586232;
+constexpr double kTwoPiLo = 2.4492935982947064e-16;
+constexpr double kInvTwoPi = 0.15915494309189533577;
+
+__device__ __forceinline__ void rope_cs(int pos, double freq, float* c, float* s) {
+  const double a = (double)pos * freq;
+  const double k = rint(a * kInvTwoPi);
+  double r = fma(-k, kTwoPiHi, a);
+  r = fma(-k, kTwoPiLo, r);
+  sincosf((float)r, s, c);
+}
+
+__device__ __forceinline__ void rotate(float* x, int i, int half, float c, float s) {
+  const float x1 = x[i], x2 = x[i + half];
+  x[i] = __fmaf_rn(x1, c, __fmul_rn(-x2, s));
+  x[i + half] = __fmaf_rn(x1, s, __fmul_rn(x2, c));
+}
+
+// One CTA per token row, one thread per pair, looping over the heads.
 __global__ void rope_posvec_kernel(float* __restrict__ q, long long q_stride, int n_q_heads, float* __restrict__ k,
                                    long long k_stride, int n_kv_heads, int head_dim, const int32_t* __restrict__ pos,
-                                   double theta) {
+                                   const __grid_constant__ RopeFreqs freqs) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   const int half = head_dim >> 1;
   const int i = threadIdx.x;
   if (i >= half) return;
-  const double inv_freq = pow(theta, -2.0 * (double)i / (double)head_dim);
-  const double ang = (double)pos[t] * inv_freq;
-  double sd, cd;
-  sincos(ang, &sd, &cd);
-  const float s = (float)sd, c = (float)cd;
+  float c, s;
+  rope_cs(pos[t], freqs.f[i], &c, &s);
   float* qt = q + (size_t)t * q_stride;
-  for (int h = 0; h < n_q_heads; ++h) {
-    float* x = qt + (size_t)h * head_dim;
-    const float x1 = x[i], x2 = x[i + half];
-    x[i] = __fmaf_rn(x1, c, __fmul_rn(-x2, s));
-    x[i + half] = __fmaf_rn(x1, s, __fmul_rn(x2, c));
-  }
+  for (int h = 0; h < n_q_heads; ++h) rotate(qt + (size_t)h * head_dim, i, half, c, s);
   if (k) {
     float* kt = k + (size_t)t * k_stride;
-    for (int h = 0; h < n_kv_heads; ++h) {
-      float* x = kt + (size_t)h * head_dim;
-      const float x1 = x[i], x2 = x[i + half];
-      x[i] = __fmaf_rn(x1, c, __fmul_rn(-x2, s));
-      x[i + half] = __fmaf_rn(x1, s, __fmul_rn(x2, c));
-    }
+    for (int h = 0; h < n_kv_heads; ++h) rotate(kt + (size_t)h * head_dim, i, half, c, s);
   }
 }
 
@@ -73,6 +89,8 @@ __global__ void kv_scatter_kernel(T* __restrict__ kc, T* __restrict__ vc, int n_
                                   const int32_t* __restrict__ batch_index, int tokens_per_seq,
                                   const int32_t* __restrict__ pos, const float* __restrict__ k,
                                   const float* __restrict__ v, long long kv_stride) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x, h = blockIdx.y;
   const int slot = batch_index[t / tokens_per_seq];
   const int p = pos[t];
@@ -84,18 +102,47 @@ __global__ void kv_scatter_kernel(T* __restrict__ kc, T* __restrict__ vc, int n_
   }
 }
 
+// The step's fused pass: one CTA per token row, one thread per pair; rotates
+// q (in place) and k, writes the rotated k and the v row into the cache slot.
+template <typename T>
+__global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, int n_q_heads, int n_kv_heads,
+                                     int head_dim, const int32_t* __restrict__ pos,
+                                     const int32_t* __restrict__ batch_index, int tokens_per_seq, T* __restrict__ kc,
+                                     T* __restrict__ vc, int ctx, const __grid_constant__ RopeFreqs freqs) {
+  pdl_trigger();
+  pdl_wait();
+  const int t = blockIdx.x;
+  const int half = head_dim >> 1;
+  const int i = threadIdx.x;
+  if (i >= half) return;
+  const int p = pos[t];
+  float c, s;
+  rope_cs(p, freqs.f[i], &c, &s);
+  float* row = qkv + (size_t)t * stride;
+  for (int h = 0; h < n_q_heads; ++h) rotate(row + (size_t)h * head_dim, i, half, c, s);
+  const int slot = batch_index[t / tokens_per_seq];
+  const float* kr = row + (size_t)n_q_heads * head_dim;
+  const float* vr = kr + (size_t)n_kv_heads * head_dim;
+  for (int h = 0; h < n_kv_heads; ++h) {
+    const float x1 = kr[(size_t)h * head_dim + i], x2 = kr[(size_t)h * head_dim + i + half];
+    const size_t dst = (((size_t)slot * n_kv_heads + h) * ctx + p) * head_dim;
+    kc[dst + i] = cvt_rn<T>(__fmaf_rn(x1, c, __fmul_rn(-x2, s)));
+    kc[dst + i + half] = cvt_rn<T>(__fmaf_rn(x1, s, __fmul_rn(x2, c)));
+    vc[dst + i] = cvt_rn<T>(vr[(size_t)h * head_dim + i]);
+    vc[dst + i + half] = cvt_rn<T>(vr[(size_t)h * head_dim + i + half]);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_rope_posvec(float* q, long long q_stride, int n_q_heads, float* k, long long k_stride,
-                               int n_kv_heads, int head_dim, int n_tok, const int32_t* pos_dev, float theta,
-                               cudaStream_t st) {
+                               int n_kv_heads, int head_dim, int n_tok, const int32_t* pos_dev,
+                               const RopeFreqs& freqs, cudaStream_t st) {
   if (n_tok == 0) return cudaSuccess;
   const int half = head_dim / 2;
   const int threads = ((half + 31) / 32) * 32;
-  if (dry_run()) return cudaSuccess;
-  rope_posvec_kernel<<<n_tok, threads, 0, st>>>(q, q_stride, n_q_heads, k, k_stride, n_kv_heads, head_dim, pos_dev,
-                                                 (double)theta);
-  return cudaGetLastError();
+  return launch_kernel(rope_posvec_kernel, dim3(n_tok), dim3(threads), 0, st, q, q_stride, n_q_heads, k, k_stride,
+                       n_kv_heads, head_dim, pos_dev, freqs);
 }
 
 cudaError_t launch_kv_scatter(void* kc, void* vc, int dtype, int n_kv_heads, int ctx, int head_dim,
@@ -104,17 +151,32 @@ cudaError_t launch_kv_scatter(void* kc, void* vc, int dtype, int n_kv_heads, int
   if (n_tok == 0) return cudaSuccess;
   const dim3 grid((unsigned)n_tok, (unsigned)n_kv_heads);
   const int threads = head_dim < 256 ? ((head_dim + 31) / 32) * 32 : 256;
-  if (dry_run()) return cudaSuccess;
   if (dtype == 0)
-    kv_scatter_kernel<__half><<<grid, threads, 0, st>>>(static_cast<__half*>(kc), static_cast<__half*>(vc),
-                                                         n_kv_heads, ctx, head_dim, batch_index_dev, tokens_per_seq,
-                                                         pos_dev, k, v, kv_stride);
-  else
-    kv_scatter_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(static_cast<__nv_bfloat16*>(kc),
-                                                                static_cast<__nv_bfloat16*>(vc), n_kv_heads, ctx,
-                                                                head_dim, batch_index_dev, tokens_per_seq, pos_dev,
-                                                                k, v, kv_stride);
-  return cudaGetLastError();
+    return launch_kernel(kv_scatter_kernel<__half>, grid, dim3(threads), 0, st, static_cast<__half*>(kc),
+                         static_cast<__half*>(vc), n_kv_heads, ctx, head_dim, batch_index_dev, tokens_per_seq, pos_dev,
+                         k, v, kv_stride);
+  return launch_kernel(kv_scatter_kernel<__nv_bfloat16>, grid, dim3(threads), 0, st, static_cast<__nv_bfloat16*>(kc),
+                       static_cast<__nv_bfloat16*>(vc), n_kv_heads, ctx, head_dim, batch_index_dev, tokens_per_seq,
+                       pos_dev, k, v, kv_stride);
+}
+
+cudaError_t launch_rope_kv_write(float* qkv, long long stride, int n_q_heads, int n_kv_heads, int head_dim,
+                                 const int32_t* pos_dev, const int32_t* batch_index_dev, int tokens_per_seq,
+                                 int n_tok, void* kc, void* vc, int dtype, int ctx, const RopeFreqs& freqs,
+                                 cudaStream_t st) {
+  if (n_tok == 0) return cudaSuccess;
+  const int threads = ((head_dim / 2 + 31) / 32) * 32;
+  if (dtype == 0)
+    return launch_kernel(rope_kv_write_kernel<__half>, dim3(n_tok), dim3(threads), 0, st, qkv, stride, n_q_heads,
+                         n_kv_heads, head_dim, pos_dev, batch_index_dev, tokens_per_seq, static_cast<__half*>(kc),
+                         static_cast<__half*>(vc), ctx, freqs);
+  return launch_kernel(rope_kv_write_kernel<__nv_bfloat16>, dim3(n_tok), dim3(threads), 0, st, qkv, stride, n_q_heads,
+                       n_kv_heads, head_dim, pos_dev, batch_index_dev, tokens_per_seq,
+                       static_cast<__nv_bfloat16*>(kc), static_cast<__nv_bfloat16*>(vc), ctx, freqs);
+}
+
+void rope_freqs(double theta, int head_dim, RopeFreqs* out) {
+  for (int i = 0; i < head_dim / 2 && i < kRopeMaxPairs; ++i) out->f[i] = pow(theta, -2.0 * i / head_dim);
 }
 
 }  // namespace dsbk
