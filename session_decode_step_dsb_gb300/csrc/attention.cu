@@ -62,7 +62,7 @@ struct Cvt<__nv_bfloat16> {
 
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
-    const float* __restrict__ q, long long q_stride, int n_q_heads, const T* __restrict__ kc, const T* __restrict__ vc,
+    const float* __restrict__ q, long long q_stride, int n_q_heads, const T* kc, const T* __restrict__ vc,
     int n_kv_heads,
     int ctx, const int32_t* __restrict__ batch_index, const int32_t* __restrict__ seq_lens,
     const int32_t* __restrict__ chunk_off, int n_seq, int tps, int max_chunks, float scale,
@@ -73,8 +73,8 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
   extern __shared__ __align__(128) uint8_t smem[];
   const int G = n_q_heads / n_kv_heads, R = G * tps;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_trigger();
   pdl_wait();  // q and the cache rows of this step come from the previous kernels
+  pdl_trigger();
 
   T* Vs = reinterpret_cast<T*>(smem);                                        // [kCh][D]
   float* qs = reinterpret_cast<float*>(smem + (size_t)kCh * D * sizeof(T));  // [R][D]
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
   for (int idx = tid; idx < R * D; idx += kThreads) {
     const int r = idx / D, d = idx - r * D;
     const int j = r / G, gi = r - j * G;
-    qs[idx] = q[(size_t)(s * tps + j) * q_stride + (size_t)(g * G + gi) * D + d];
+    qs[idx] = __ldcg(q + (size_t)(s * tps + j) * q_stride + (size_t)(g * G + gi) * D + d);
   }
   __syncthreads();
 
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
     if (tid < nkeys) {
       const uint4* kp = reinterpret_cast<const uint4*>(kc + (head_row0 + key0 + tid) * D);
 #pragma unroll
-      for (int cc = 0; cc < D / 8; ++cc) kreg[cc] = ld_nc_v4(kp + cc);
+      for (int cc = 0; cc < D / 8; ++cc) kreg[cc] = ld_v4(kp + cc);  // this step's rows were written by the previous kernel
     } else {
 #pragma unroll
       for (int cc = 0; cc < D / 8; ++cc) kreg[cc] = make_uint4(0, 0, 0, 0);
@@ -263,8 +263,8 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
                                                               int tps, const int32_t* __restrict__ seq_lens,
                                                               int max_chunks, int n_tok, float* __restrict__ out,
                                                               uint8_t* __restrict__ xq) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int wg = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (wg >= n_tok * n_q_heads) return;
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
   const int nch = (vis + kCh - 1) / kCh;
   const float* base = partials + ((size_t)t * n_q_heads + h) * max_chunks * (D + 2);
   float M = -INFINITY;
-  for (int c = lane; c < nch; c += 32) M = fmaxf(M, base[(size_t)c * (D + 2)]);
+  for (int c = lane; c < nch; c += 32) M = fmaxf(M, __ldcg(base + (size_t)c * (D + 2)));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float lsum = 0.0f;
@@ -285,15 +285,15 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
     float wl = 0.0f;
     if (c0 + lane < nch) {
       const float* pc = base + (size_t)(c0 + lane) * (D + 2);
-      wl = expf(pc[0] - M);
-      lsum = __fmaf_rn(wl, pc[1], lsum);
+      wl = expf(__ldcg(pc) - M);
+      lsum = __fmaf_rn(wl, __ldcg(pc + 1), lsum);
     }
     const int n = min(32, nch - c0);
     for (int cc = 0; cc < n; ++cc) {
       const float wc = __shfl_sync(0xffffffffu, wl, cc);
       const float* pc = base + (size_t)(c0 + cc) * (D + 2) + 2;
 #pragma unroll
-      for (int e = 0; e < D / 32; ++e) acc[e] = __fmaf_rn(wc, pc[lane + 32 * e], acc[e]);
+      for (int e = 0; e < D / 32; ++e) acc[e] = __fmaf_rn(wc, __ldcg(pc + lane + 32 * e), acc[e]);
     }
   }
 #pragma unroll

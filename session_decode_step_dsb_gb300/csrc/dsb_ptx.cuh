@@ -96,16 +96,27 @@ __device__ __forceinline__ float ld_dsmem_f32(const float* p, uint32_t rank) {
 // Programmatic dependent launch.  pdl_wait() blocks until the grid this one
 // depends on has completed and its writes are visible (a no-op when the launch
 // carries no programmatic dependency); pdl_trigger() lets the dependent grid be
-// scheduled once every CTA of this grid has issued it or exited.  A kernel
-// writes no global memory before its pdl_wait().
+// scheduled once every CTA of this grid has issued it or exited.  Every kernel
+// calls pdl_trigger() only after its pdl_wait(), so at most two grids of a
+// chain overlap, and writes no global memory before its pdl_wait().
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+// L2-coherent global loads (.cg: not cached in L1, never the read-only .nc
+// path): for data written by an earlier kernel of a programmatic-dependent
+// chain, whose lines another kernel may have left in this SM's L1.
+__device__ __forceinline__ uint4 ld_v4(const void* p) {
   uint4 r;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
+               : "l"(p)
+               : "memory");
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ld_u32(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(r) : "l"(p) : "memory");
   return r;
 }
 

@@ -30,12 +30,15 @@ __global__ void __launch_bounds__(kGlueThreads) rmsnorm_quant_kernel(const float
                                                                      const float* __restrict__ w, int hidden,
                                                                      float eps, uint8_t* __restrict__ xq) {
   __shared__ float part[kGlueThreads / 32];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   const float* xr = x + (size_t)t * hidden;
   float ss = 0.0f;
-  for (int i = threadIdx.x; i < hidden; i += kGlueThreads) ss = __fmaf_rn(xr[i], xr[i], ss);
+  for (int i = threadIdx.x; i < hidden; i += kGlueThreads) {
+    const float v = __ldcg(xr + i);
+    ss = __fmaf_rn(v, v, ss);
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
@@ -48,7 +51,7 @@ __global__ void __launch_bounds__(kGlueThreads) rmsnorm_quant_kernel(const float
   uint8_t* out = xq + (size_t)t * (hidden / 32) * 34;
   for (int b = warp; b < hidden / 32; b += kGlueThreads / 32) {
     const int i = b * 32 + lane;
-    const float v = __fmul_rn(__fmul_rn(xr[i], inv), w[i]);
+    const float v = __fmul_rn(__fmul_rn(__ldcg(xr + i), inv), w[i]);
     q8_block_store(v, out + (size_t)b * 34, lane);
   }
 }
@@ -56,16 +59,16 @@ __global__ void __launch_bounds__(kGlueThreads) rmsnorm_quant_kernel(const float
 // gu: [n_tok][2*ffn] = [gate | up]; out: q8_0 [n_tok][ffn].  One warp per block.
 __global__ void __launch_bounds__(kGlueThreads) silu_mul_quant_kernel(const float* __restrict__ gu, int ffn,
                                                                       long long n_blocks, uint8_t* __restrict__ xq) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const long long blk = (long long)blockIdx.x * (kGlueThreads / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (blk >= n_blocks) return;
   const int per_row = ffn / 32;
   const long long t = blk / per_row;
   const int i = (int)(blk - t * per_row) * 32 + lane;
-  const float g = gu[(size_t)t * 2 * ffn + i];
-  const float u = gu[(size_t)t * 2 * ffn + ffn + i];
+  const float g = __ldcg(gu + (size_t)t * 2 * ffn + i);
+  const float u = __ldcg(gu + (size_t)t * 2 * ffn + ffn + i);
   const float s = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
   q8_block_store(__fmul_rn(s, u), xq + (size_t)blk * 34, lane);
 }
@@ -74,8 +77,8 @@ __global__ void __launch_bounds__(kGlueThreads) silu_mul_quant_kernel(const floa
 __global__ void __launch_bounds__(kGlueThreads) embed_kernel(const uint8_t* __restrict__ table, int hidden,
                                                              const int32_t* __restrict__ tokens, long long n_blocks,
                                                              float* __restrict__ h) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const long long blk = (long long)blockIdx.x * (kGlueThreads / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (blk >= n_blocks) return;

@@ -71,7 +71,7 @@ __device__ __forceinline__ Split kstep_range(int nks, int S, int rank) {
 
 template <int NT, bool EMIT>
 __global__ void __launch_bounds__(kThreads, 2)
-    matmul_q8_0_narrow_kernel(const uint8_t* __restrict__ W, int rows, int nb, const uint8_t* __restrict__ xq,
+    matmul_q8_0_narrow_kernel(const uint8_t* __restrict__ W, int rows, int nb, const uint8_t* xq,
                               float* y, const float* residual, int32_t* __restrict__ isum_out) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int nks = nb >> 3;
@@ -122,7 +122,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (row < rows)
       bulk_g2s(dst + lane * kChunkBytes, W + (size_t)row * row_bytes + (size_t)ks * kChunkBytes, kChunkBytes, bar);
   };
-  for (int u = 0; u < kNStage && u < n_units; ++u) issue(u);
+  for (int u = 0; u < kNStage && u < n_units; ++u) issue(u);  // weights do not depend on the previous kernel
+  pdl_wait();  // the activations (and y / residual) may be the previous kernel's results
+  pdl_trigger();
 
   // Unpack the CTA's activation blocks [ks0*8, ks1*8) x NT into aligned form.
   for (int idx = threadIdx.x; idx < kr * 8 * NT; idx += kThreads) {
@@ -131,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t* src = reinterpret_cast<const uint32_t*>(xq + ((34 * g) & ~3LL));
     uint32_t wv[9];
 #pragma unroll
-    for (int k = 0; k < 9; ++k) wv[k] = __ldg(src + k);
+    for (int k = 0; k < 9; ++k) wv[k] = ld_u32(src + k);  // written by the previous kernel
     const bool odd = (g & 1) != 0;  // odd blocks start 2 bytes into a word
     const uint32_t sh = odd ? 32u : 16u;
     uint32_t* dq = act_q + ((size_t)b * NT + t) * 8;
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int t = idx >> 5, rr = row0 + (idx & 31);
           if (rr < rows) {
             const size_t o = (size_t)t * rows + rr;
-            y[o] = residual ? __fadd_rn(residual[o], v) : v;  // residual may alias y
+            y[o] = residual ? __fadd_rn(__ldcg(residual + o), v) : v;  // residual may alias y
           }
         }
       }

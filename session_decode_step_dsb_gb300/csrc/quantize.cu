@@ -25,12 +25,12 @@ namespace {
 
 __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float* __restrict__ x, long long n_blocks,
                                                            uint8_t* __restrict__ xq) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const long long blk = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (blk >= n_blocks) return;
-  const float v = x[blk * 32 + lane];
+  const float v = __ldcg(x + blk * 32 + lane);
   float a = fabsf(v);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));

@@ -47,7 +47,7 @@ __device__ __forceinline__ void rope_cs(int pos, double freq, float* c, float* s
 }
 
 __device__ __forceinline__ void rotate(float* x, int i, int half, float c, float s) {
-  const float x1 = x[i], x2 = x[i + half];
+  const float x1 = __ldcg(x + i), x2 = __ldcg(x + i + half);
   x[i] = __fmaf_rn(x1, c, __fmul_rn(-x2, s));
   x[i + half] = __fmaf_rn(x1, s, __fmul_rn(x2, c));
 }
@@ -56,8 +56,8 @@ __device__ __forceinline__ void rotate(float* x, int i, int half, float c, float
 __global__ void rope_posvec_kernel(float* __restrict__ q, long long q_stride, int n_q_heads, float* __restrict__ k,
                                    long long k_stride, int n_kv_heads, int head_dim, const int32_t* __restrict__ pos,
                                    const __grid_constant__ RopeFreqs freqs) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   const int half = head_dim >> 1;
   const int i = threadIdx.x;
@@ -89,16 +89,16 @@ __global__ void kv_scatter_kernel(T* __restrict__ kc, T* __restrict__ vc, int n_
                                   const int32_t* __restrict__ batch_index, int tokens_per_seq,
                                   const int32_t* __restrict__ pos, const float* __restrict__ k,
                                   const float* __restrict__ v, long long kv_stride) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x, h = blockIdx.y;
   const int slot = batch_index[t / tokens_per_seq];
   const int p = pos[t];
   const size_t dst = (((size_t)slot * n_kv_heads + h) * ctx + p) * head_dim;
   const size_t src = (size_t)t * kv_stride + (size_t)h * head_dim;
   for (int d = threadIdx.x; d < head_dim; d += blockDim.x) {
-    kc[dst + d] = cvt_rn<T>(k[src + d]);
-    vc[dst + d] = cvt_rn<T>(v[src + d]);
+    kc[dst + d] = cvt_rn<T>(__ldcg(k + src + d));
+    vc[dst + d] = cvt_rn<T>(__ldcg(v + src + d));
   }
 }
 
@@ -109,8 +109,8 @@ __global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, 
                                      int head_dim, const int32_t* __restrict__ pos,
                                      const int32_t* __restrict__ batch_index, int tokens_per_seq, T* __restrict__ kc,
                                      T* __restrict__ vc, int ctx, const __grid_constant__ RopeFreqs freqs) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   const int half = head_dim >> 1;
   const int i = threadIdx.x;
@@ -124,12 +124,12 @@ __global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, 
   const float* kr = row + (size_t)n_q_heads * head_dim;
   const float* vr = kr + (size_t)n_kv_heads * head_dim;
   for (int h = 0; h < n_kv_heads; ++h) {
-    const float x1 = kr[(size_t)h * head_dim + i], x2 = kr[(size_t)h * head_dim + i + half];
+    const float x1 = __ldcg(kr + (size_t)h * head_dim + i), x2 = __ldcg(kr + (size_t)h * head_dim + i + half);
     const size_t dst = (((size_t)slot * n_kv_heads + h) * ctx + p) * head_dim;
     kc[dst + i] = cvt_rn<T>(__fmaf_rn(x1, c, __fmul_rn(-x2, s)));
     kc[dst + i + half] = cvt_rn<T>(__fmaf_rn(x1, s, __fmul_rn(x2, c)));
-    vc[dst + i] = cvt_rn<T>(vr[(size_t)h * head_dim + i]);
-    vc[dst + i + half] = cvt_rn<T>(vr[(size_t)h * head_dim + i + half]);
+    vc[dst + i] = cvt_rn<T>(__ldcg(vr + (size_t)h * head_dim + i));
+    vc[dst + i + half] = cvt_rn<T>(__ldcg(vr + (size_t)h * head_dim + i + half));
   }
 }
 
