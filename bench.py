@@ -395,6 +395,8 @@ def run_dsb(args):
                               "peak_gbs": peak, "frac": round(total_bytes / (ms_step * 1e-3) / 1e9 / peak, 4)},
             "roofline": {"kernel": "matmul_q8_0_narrow_kernel", "bound": "hbm", "achieved": round(achieved, 1),
                          "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "per": "one step's matmul launches (2 layers x 4 + head)",
+                         "algorithmic_bytes": int(tot_bytes),
                          "peak_kind": f"{peak_kind} hbm_gbs", "launches": per_kernel},
             "b_sweep": sweep,
             "matmul_q8_0_narrow": sweep_mm,

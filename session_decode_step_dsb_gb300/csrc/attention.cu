@@ -114,6 +114,17 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
     mbar_arrive_expect_tx(bar, bytes);
     bulk_g2s(Vs, vc + (head_row0 + key0) * D, bytes, bar);
   }
+  // Thread tid owns key key0 + tid: its K row goes into registers first, so
+  // that the K loads and the q staging below are in flight together.
+  uint4 kreg[D / 8];
+  if (tid < nkeys) {
+    const uint4* kp = reinterpret_cast<const uint4*>(kc + (head_row0 + key0 + tid) * D);
+#pragma unroll
+    for (int cc = 0; cc < D / 8; ++cc) kreg[cc] = ld_v4(kp + cc);  // this step's rows were written by the previous kernel
+  } else {
+#pragma unroll
+    for (int cc = 0; cc < D / 8; ++cc) kreg[cc] = make_uint4(0, 0, 0, 0);
+  }
   for (int idx = tid; idx < R * D; idx += kThreads) {
     const int r = idx / D, d = idx - r * D;
     const int j = r / G, gi = r - j * G;
@@ -121,17 +132,8 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
   }
   __syncthreads();
 
-  // ---- scores: thread tid owns key key0 + tid
+  // ---- scores
   {
-    uint4 kreg[D / 8];
-    if (tid < nkeys) {
-      const uint4* kp = reinterpret_cast<const uint4*>(kc + (head_row0 + key0 + tid) * D);
-#pragma unroll
-      for (int cc = 0; cc < D / 8; ++cc) kreg[cc] = ld_v4(kp + cc);  // this step's rows were written by the previous kernel
-    } else {
-#pragma unroll
-      for (int cc = 0; cc < D / 8; ++cc) kreg[cc] = make_uint4(0, 0, 0, 0);
-    }
     for (int r0 = 0; r0 < R; r0 += kRowGroup) {
       float dot[kRowGroup];
 #pragma unroll

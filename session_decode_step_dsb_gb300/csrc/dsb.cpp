@@ -456,6 +456,7 @@ dsb_status check_model(const dsb_model* m, const dsb_kv_cache** kv0) {
       s.n_layers < 1)
     return fail(DSB_ERR_INVALID_ARG, "model shape has a non-positive or too small dimension");
   if (s.n_q_heads % s.n_kv_heads) return fail(DSB_ERR_INVALID_ARG, "n_q_heads %% n_kv_heads != 0");
+  if (s.hidden > 8192) return fail(DSB_ERR_UNSUPPORTED, "hidden=%d: the step serves hidden <= 8192", s.hidden);
   if (s.hidden % 256 || s.ffn % 256 || (s.n_q_heads * s.head_dim) % 256)
     return fail(DSB_ERR_UNSUPPORTED, "hidden, ffn and n_q_heads*head_dim must be multiples of 256");
   if (s.head_dim != 64 && s.head_dim != 128) return fail(DSB_ERR_UNSUPPORTED, "head_dim must be 64 or 128");

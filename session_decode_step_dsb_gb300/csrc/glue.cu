@@ -24,8 +24,12 @@ namespace {
 
 constexpr int kGlueThreads = 256;
 
-// One CTA per token row: sum of squares in a fixed tree order, then each warp
-// normalises, scales and quantises 32-value blocks.
+constexpr int kMaxPerThread = 32;  // hidden <= 8192
+
+// One CTA per token row.  Thread j holds elements j, j + 256, ... in registers
+// (one memory round trip); the sum of squares goes through a fixed tree; then
+// warp w quantises blocks w, w + 8, ... -- element 32b + lane of block b is
+// exactly the value thread 32w + lane already holds.
 __global__ void __launch_bounds__(kGlueThreads) rmsnorm_quant_kernel(const float* __restrict__ x,
                                                                      const float* __restrict__ w, int hidden,
                                                                      float eps, uint8_t* __restrict__ xq) {
@@ -34,11 +38,15 @@ __global__ void __launch_bounds__(kGlueThreads) rmsnorm_quant_kernel(const float
   pdl_trigger();
   const int t = blockIdx.x;
   const float* xr = x + (size_t)t * hidden;
+  const int n = hidden / kGlueThreads;  // hidden % 256 == 0 on this path
+  float v[kMaxPerThread];
+#pragma unroll
+  for (int k = 0; k < kMaxPerThread; ++k)
+    if (k < n) v[k] = __ldcg(xr + threadIdx.x + k * kGlueThreads);
   float ss = 0.0f;
-  for (int i = threadIdx.x; i < hidden; i += kGlueThreads) {
-    const float v = __ldcg(xr + i);
-    ss = __fmaf_rn(v, v, ss);
-  }
+#pragma unroll
+  for (int k = 0; k < kMaxPerThread; ++k)
+    if (k < n) ss = __fmaf_rn(v[k], v[k], ss);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
@@ -49,10 +57,13 @@ __global__ void __launch_bounds__(kGlueThreads) rmsnorm_quant_kernel(const float
   for (int i = 0; i < kGlueThreads / 32; ++i) tot = __fadd_rn(tot, part[i]);
   const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)hidden), eps)));
   uint8_t* out = xq + (size_t)t * (hidden / 32) * 34;
-  for (int b = warp; b < hidden / 32; b += kGlueThreads / 32) {
-    const int i = b * 32 + lane;
-    const float v = __fmul_rn(__fmul_rn(__ldcg(xr + i), inv), w[i]);
-    q8_block_store(v, out + (size_t)b * 34, lane);
+#pragma unroll
+  for (int k = 0; k < kMaxPerThread; ++k) {
+    if (k < n) {
+      const int e = threadIdx.x + k * kGlueThreads;
+      const int b = e >> 5;
+      q8_block_store(__fmul_rn(__fmul_rn(v[k], inv), w[e]), out + (size_t)b * 34, lane);
+    }
   }
 }
 

@@ -49,6 +49,7 @@ constexpr int kChunkBytes = 272;  // 8 blocks of 34 bytes
 constexpr int kStage = kRowsPerCta * kChunkBytes;
 constexpr int kNStage = 2;
 constexpr uint32_t kMagic = 0x4B400000u;  // bits of 12582912.0f = 1.5 * 2^23
+constexpr unsigned long long kMagic2 = 0x4B4000004B400000ull;
 constexpr float kMagicF = 12582912.0f;
 
 __device__ unsigned int g_err_matmul = 0;
@@ -69,10 +70,51 @@ __device__ __forceinline__ Split kstep_range(int nks, int S, int rank) {
   return s;
 }
 
-template <int NT, bool EMIT>
+// acc2 += (bits2 - magic2) * s2 for two tokens with packed f32x2 instructions.
+__device__ __forceinline__ unsigned long long acc_pair(unsigned long long acc2, int bits_a, int bits_b,
+                                                       unsigned long long s2) {
+  unsigned long long f2;
+  asm("{\n .reg .b64 b;\n mov.b64 b, {%1, %2};\n sub.rn.f32x2 %0, b, %3;\n}\n"
+      : "=l"(f2)
+      : "r"(bits_a), "r"(bits_b), "l"(kMagic2));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2) : "l"(f2), "l"(s2));
+  return acc2;
+}
+
+__device__ __forceinline__ unsigned long long mul_pair(unsigned long long a2, unsigned long long b2) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a2), "l"(b2));
+  return r;
+}
+
+__device__ __forceinline__ unsigned long long dup_pair(float x) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ float2 unpack_pair(unsigned long long v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+
+// ROWS = false (few-row matrices): a CTA tile is 32 rows and its 4 warps
+//   take interleaved k-steps of the CTA's k-range; warp partials are added in
+//   warp order at each tile end.
+// ROWS = true (many-row matrices): a CTA tile is 128 rows, warp w owns rows
+//   32w..32w+31 over the whole k-range; no partials are exchanged between
+//   warps, and with S = 1 no barrier of any kind is taken after start-up.
+// In both modes the S CTAs of a cluster split k and rank 0 adds their sums in
+// rank order through distributed shared memory.
+template <int NT, bool EMIT, bool ROWS>
 __global__ void __launch_bounds__(kThreads, 2)
     matmul_q8_0_narrow_kernel(const uint8_t* __restrict__ W, int rows, int nb, const uint8_t* xq,
                               float* y, const float* residual, int32_t* __restrict__ isum_out) {
+  constexpr int kTile = ROWS ? kWarps * kRowsPerCta : kRowsPerCta;
+  constexpr int kRed = ROWS ? 0 : kWarps * NT * 32;          // warp partials (k-split mode)
+  constexpr int kSum = (ROWS ? kWarps : 1) * NT * 32;        // one CTA sum buffer
+  constexpr int kSumBufs = ROWS ? 1 : 2;  // rows mode: one buffer, a second barrier per tile
   extern __shared__ __align__(128) uint8_t smem[];
   const int nks = nb >> 3;
   const int S = gridDim.y;
@@ -82,8 +124,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int kr = ksr.ks1 - ksr.ks0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t row_bytes = (size_t)nb * 34;
-  const int tiles = (rows + kRowsPerCta - 1) / kRowsPerCta;
-  const int n_tiles = blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / n_clusters + 1 : 0;
+  const int tiles = (rows + kTile - 1) / kTile;
+  const int n_tiles = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / n_clusters + 1 : 0;
+  const int warp_row = ROWS ? warp * kRowsPerCta : 0;
 
   // Shared layout: act codes | act scales | stage rings | warp partials |
   // CTA sums (double-buffered) | barriers.  The act region is sized for the
@@ -95,8 +138,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* act_s = reinterpret_cast<float*>(act_q + (size_t)kr_alloc * 8 * NT * 8);  // [kr*8][NT]
   uint8_t* stages = reinterpret_cast<uint8_t*>(act_s + (size_t)kr_alloc * 8 * NT);  // [kWarps][kNStage][kStage]
   float* red = reinterpret_cast<float*>(stages + (size_t)kWarps * kNStage * kStage);  // [kWarps][NT][32]
-  float* red_sum = red + kWarps * NT * 32;                                            // [2][NT][32]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red_sum + 2 * NT * 32);                // [kWarps][kNStage]
+  float* red_sum = red + kRed;                                                        // [kSumBufs][kSum]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red_sum + kSumBufs * kSum);           // [kWarps][kNStage]
   uint8_t* my_stages = stages + (size_t)warp * kNStage * kStage;
   uint64_t* my_bars = bars + warp * kNStage;
 
@@ -106,18 +149,21 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncwarp();
 
-  // This warp's units: for each of the CTA's tiles m, its k-steps
-  // ks0 + warp + kWarps*i, i < n_mine.  Unit u = m*n_mine + i.
-  const int n_mine = kr > warp ? (kr - warp + kWarps - 1) / kWarps : 0;
+  // This warp's units: for each of the CTA's tiles m, its k-steps (all of the
+  // k-range in ROWS mode, every kWarps-th otherwise).  Unit u = m*n_mine + i.
+  const int n_mine = ROWS ? kr : (kr > warp ? (kr - warp + kWarps - 1) / kWarps : 0);
   const int n_units = n_tiles * n_mine;
+  auto kstep = [&](int i) { return ROWS ? ksr.ks0 + i : ksr.ks0 + warp + kWarps * i; };
   auto issue = [&](int u) {
     const int m = u / n_mine, i = u - m * n_mine;
-    const int row0 = ((int)blockIdx.x + m * n_clusters) * kRowsPerCta;
+    const int row0 = ((int)blockIdx.x + m * n_clusters) * kTile + warp_row;
     const int row = row0 + lane;
-    const int ks = ksr.ks0 + warp + kWarps * i;
+    const int ks = kstep(i);
     uint64_t* bar = &my_bars[u % kNStage];
     uint8_t* dst = my_stages + (size_t)(u % kNStage) * kStage;
-    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(min(kRowsPerCta, rows - row0) * kChunkBytes));
+    const int live = rows - row0 < kRowsPerCta ? rows - row0 : kRowsPerCta;
+    if (lane == 0 && live > 0) mbar_arrive_expect_tx(bar, (uint32_t)(live * kChunkBytes));
+    if (lane == 0 && live <= 0) mbar_arrive_expect_tx(bar, 0u);
     __syncwarp();
     if (row < rows)
       bulk_g2s(dst + lane * kChunkBytes, W + (size_t)row * row_bytes + (size_t)ks * kChunkBytes, kChunkBytes, bar);
@@ -126,7 +172,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   pdl_wait();  // the activations (and y / residual) may be the previous kernel's results
   pdl_trigger();
 
-  // Unpack the CTA's activation blocks [ks0*8, ks1*8) x NT into aligned form.
+  // Unpack the CTA's activation blocks [ks0*8, ks1*8) x NT into aligned form
+  // (unrolled so that several blocks' loads are in flight at once).
+#pragma unroll 4
   for (int idx = threadIdx.x; idx < kr * 8 * NT; idx += kThreads) {
     const int b = idx / NT, t = idx - b * NT;
     const long long g = (long long)t * nb + (long long)ksr.ks0 * 8 + b;  // global block index
@@ -146,14 +194,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   bool dead = false;
   int u = 0;
   for (int m = 0; m < n_tiles; ++m) {
-    const int row0 = ((int)blockIdx.x + m * n_clusters) * kRowsPerCta;
-    const int row = row0 + lane;
-    float acc[NT];
+    const int row0 = ((int)blockIdx.x + m * n_clusters) * kTile;
+    const int row = row0 + warp_row + lane;
+    unsigned long long acc2[(NT + 1) / 2];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
+    for (int p = 0; p < (NT + 1) / 2; ++p) acc2[p] = 0ull;
 
     for (int i = 0; i < n_mine; ++i, ++u) {
-      const int ks = ksr.ks0 + warp + kWarps * i;
+      const int ks = kstep(i);
       const int kl = ks - ksr.ks0;
       uint64_t* bar = &my_bars[u % kNStage];
       if (!dead) {
@@ -191,82 +239,122 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         const uint32_t* aq = act_q + ((size_t)(kl * 8 + b) * NT) * 8;
         const float* as = act_s + (size_t)(kl * 8 + b) * NT;
-        float sx[NT];
-        if constexpr (NT % 4 == 0) {
+        const unsigned long long dw2 = dup_pair(dw);
 #pragma unroll
-          for (int t = 0; t < NT; t += 4) {
-            const float4 v = *reinterpret_cast<const float4*>(as + t);
-            sx[t] = v.x; sx[t + 1] = v.y; sx[t + 2] = v.z; sx[t + 3] = v.w;
+        for (int t = 0; t < NT; t += 2) {
+          // two tokens' dp4a chains interleaved
+          const uint4 a0 = *reinterpret_cast<const uint4*>(aq + t * 8);
+          const uint4 a1 = *reinterpret_cast<const uint4*>(aq + t * 8 + 4);
+          uint4 b0 = make_uint4(0, 0, 0, 0), b1 = make_uint4(0, 0, 0, 0);
+          if (t + 1 < NT) {
+            b0 = *reinterpret_cast<const uint4*>(aq + (t + 1) * 8);
+            b1 = *reinterpret_cast<const uint4*>(aq + (t + 1) * 8 + 4);
           }
-        } else {
-#pragma unroll
-          for (int t = 0; t < NT; ++t) sx[t] = as[t];
-        }
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          const uint4 x0 = *reinterpret_cast<const uint4*>(aq + t * 8);
-          const uint4 x1 = *reinterpret_cast<const uint4*>(aq + t * 8 + 4);
-          int s = (int)kMagic;
-          s = __dp4a((int)q[0], (int)x0.x, s);
-          s = __dp4a((int)q[1], (int)x0.y, s);
-          s = __dp4a((int)q[2], (int)x0.z, s);
-          s = __dp4a((int)q[3], (int)x0.w, s);
-          s = __dp4a((int)q[4], (int)x1.x, s);
-          s = __dp4a((int)q[5], (int)x1.y, s);
-          s = __dp4a((int)q[6], (int)x1.z, s);
-          s = __dp4a((int)q[7], (int)x1.w, s);
+          int sa = (int)kMagic, sb = (int)kMagic;
+          sa = __dp4a((int)q[0], (int)a0.x, sa);
+          sb = __dp4a((int)q[0], (int)b0.x, sb);
+          sa = __dp4a((int)q[1], (int)a0.y, sa);
+          sb = __dp4a((int)q[1], (int)b0.y, sb);
+          sa = __dp4a((int)q[2], (int)a0.z, sa);
+          sb = __dp4a((int)q[2], (int)b0.z, sb);
+          sa = __dp4a((int)q[3], (int)a0.w, sa);
+          sb = __dp4a((int)q[3], (int)b0.w, sb);
+          sa = __dp4a((int)q[4], (int)a1.x, sa);
+          sb = __dp4a((int)q[4], (int)b1.x, sb);
+          sa = __dp4a((int)q[5], (int)a1.y, sa);
+          sb = __dp4a((int)q[5], (int)b1.y, sb);
+          sa = __dp4a((int)q[6], (int)a1.z, sa);
+          sb = __dp4a((int)q[6], (int)b1.z, sb);
+          sa = __dp4a((int)q[7], (int)a1.w, sa);
+          sb = __dp4a((int)q[7], (int)b1.w, sb);
           if constexpr (EMIT) {
-            if (row < rows) isum_out[((size_t)t * rows + row) * nb + (size_t)ks * 8 + b] = s - (int)kMagic;
+            if (row < rows) {
+              isum_out[((size_t)t * rows + row) * nb + (size_t)ks * 8 + b] = sa - (int)kMagic;
+              if (t + 1 < NT) isum_out[((size_t)(t + 1) * rows + row) * nb + (size_t)ks * 8 + b] = sb - (int)kMagic;
+            }
           } else {
-            const float f = __fsub_rn(__int_as_float(s), kMagicF);
-            acc[t] = __fmaf_rn(f, __fmul_rn(dw, sx[t]), acc[t]);
+            unsigned long long sx2;
+            if (t + 1 < NT)
+              sx2 = *reinterpret_cast<const unsigned long long*>(as + t);
+            else
+              sx2 = dup_pair(as[t]);
+            acc2[t / 2] = acc_pair(acc2[t / 2], sa, sb, mul_pair(dw2, sx2));
           }
         }
       }
     }
 
     if constexpr (!EMIT) {
-      // Tile end: warp partials summed in warp order into this CTA's sum,
-      // then rank 0 adds the cluster's CTA sums in rank order.  The CTA sums
-      // are double-buffered by tile parity, so one cluster barrier per tile
-      // suffices: a buffer is rewritten two tiles later, after the next
-      // barrier, which rank 0 reaches only once it has read this one.
+      float acc[NT];
 #pragma unroll
-      for (int t = 0; t < NT; ++t) red[(warp * NT + t) * 32 + lane] = acc[t];
-      __syncthreads();
-      float* rs = red_sum + (m & 1) * NT * 32;
-      for (int idx = threadIdx.x; idx < NT * 32; idx += kThreads) {
-        float v = red[idx];
-#pragma unroll
-        for (int w2 = 1; w2 < kWarps; ++w2) v = __fadd_rn(v, red[w2 * NT * 32 + idx]);
-        rs[idx] = v;
+      for (int p = 0; p < (NT + 1) / 2; ++p) {
+        const float2 v = unpack_pair(acc2[p]);
+        acc[2 * p] = v.x;
+        if (2 * p + 1 < NT) acc[2 * p + 1] = v.y;
       }
-      cluster_sync();
-      if (rank == 0) {
-        for (int idx = threadIdx.x; idx < NT * 32; idx += kThreads) {
-          float v = rs[idx];
-          for (int r = 1; r < S; ++r) v = __fadd_rn(v, ld_dsmem_f32(&rs[idx], (uint32_t)r));
-          const int t = idx >> 5, rr = row0 + (idx & 31);
-          if (rr < rows) {
-            const size_t o = (size_t)t * rows + rr;
-            y[o] = residual ? __fadd_rn(__ldcg(residual + o), v) : v;  // residual may alias y
+      if (ROWS && S == 1) {
+        // One warp owns these rows over the whole k: write them directly.
+        if (row < rows) {
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const size_t o = (size_t)t * rows + row;
+            y[o] = residual ? __fadd_rn(__ldcg(residual + o), acc[t]) : acc[t];  // residual may alias y
           }
         }
+      } else {
+        // The CTA's sum for this tile (k-split mode: warp partials added in
+        // warp order), then rank 0 adds the cluster's CTA sums in rank order.
+        // k-split mode double-buffers the sums by tile parity, so one cluster
+        // barrier per tile suffices (a buffer is rewritten two tiles later,
+        // after the next barrier, which rank 0 reaches only once it has read
+        // this one); rows mode keeps one larger buffer and takes a second
+        // barrier after rank 0's reads.
+        float* rs = red_sum + (kSumBufs == 2 ? (m & 1) : 0) * kSum;
+        if constexpr (ROWS) {
+#pragma unroll
+          for (int t = 0; t < NT; ++t) rs[(warp * NT + t) * 32 + lane] = acc[t];
+        } else {
+#pragma unroll
+          for (int t = 0; t < NT; ++t) red[(warp * NT + t) * 32 + lane] = acc[t];
+          __syncthreads();
+          for (int idx = threadIdx.x; idx < NT * 32; idx += kThreads) {
+            float v = red[idx];
+#pragma unroll
+            for (int w2 = 1; w2 < kWarps; ++w2) v = __fadd_rn(v, red[w2 * NT * 32 + idx]);
+            rs[idx] = v;
+          }
+        }
+        cluster_sync();
+        if (rank == 0) {
+          for (int idx = threadIdx.x; idx < kSum; idx += kThreads) {
+            float v = rs[idx];
+            for (int r = 1; r < S; ++r) v = __fadd_rn(v, ld_dsmem_f32(&rs[idx], (uint32_t)r));
+            const int wq = ROWS ? idx / (NT * 32) : 0;
+            const int t = (idx / 32) % NT, rr = row0 + wq * kRowsPerCta + (idx & 31);
+            if (rr < rows) {
+              const size_t o = (size_t)t * rows + rr;
+              y[o] = residual ? __fadd_rn(__ldcg(residual + o), v) : v;  // residual may alias y
+            }
+          }
+        }
+        if constexpr (ROWS) cluster_sync();  // rank 0 is done with every CTA's buffer
       }
     }
   }
-  if constexpr (!EMIT) cluster_sync();  // keep this CTA's sums alive until rank 0 has read them
+  // keep this CTA's sums alive until rank 0 has read them
+  if (!EMIT && !ROWS) cluster_sync();
 }
 
-size_t smem_bytes(int kr, int nt) {
-  return (size_t)kr * 8 * nt * 36 + (size_t)kWarps * kNStage * kStage + (size_t)(kWarps + 2) * nt * 32 * 4 +
-         (size_t)kWarps * kNStage * 8;
+size_t smem_bytes(int kr, int nt, bool rows_mode) {
+  const size_t red = rows_mode ? 0 : (size_t)kWarps * nt * 32 * 4;
+  const size_t sums = rows_mode ? (size_t)kWarps * nt * 32 * 4 : 2 * (size_t)nt * 32 * 4;
+  return (size_t)kr * 8 * nt * 36 + (size_t)kWarps * kNStage * kStage + red + sums + (size_t)kWarps * kNStage * 8;
 }
 
-template <int NT, bool EMIT>
+template <int NT, bool EMIT, bool ROWS>
 cudaError_t launch_nt(const uint8_t* W, int rows, int nb, const uint8_t* xq, float* y, const float* residual,
                       int32_t* isum, int S, size_t smem, cudaStream_t st) {
-  auto kern = matmul_q8_0_narrow_kernel<NT, EMIT>;
+  auto kern = matmul_q8_0_narrow_kernel<NT, EMIT, ROWS>;
   // Per-instantiation caches (not thread-safe; one host thread drives a
   // device): the largest dynamic shared memory granted so far, and the number
   // of co-resident clusters for each (S, smem) seen -- the persistent grid.
@@ -287,7 +375,7 @@ cudaError_t launch_nt(const uint8_t* W, int rows, int nb, const uint8_t* xq, flo
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl() ? 2 : 1;
+  cfg.numAttrs = 1;
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -306,20 +394,22 @@ cudaError_t launch_nt(const uint8_t* W, int rows, int nb, const uint8_t* xq, flo
     if (resident < 1) return cudaErrorInvalidConfiguration;
     cache[n_cache < 8 ? n_cache++ : 7] = Entry{S, smem, resident};
   }
-  const int tiles = (rows + kRowsPerCta - 1) / kRowsPerCta;
+  const int tile = ROWS ? kWarps * kRowsPerCta : kRowsPerCta;
+  const int tiles = (rows + tile - 1) / tile;
   const int n_clusters = tiles < resident ? tiles : resident;
   cfg.gridDim = dim3((unsigned)n_clusters, (unsigned)S, 1);
+  cfg.numAttrs = pdl() ? 2 : 1;
   if (dry_run()) return cudaSuccess;
   return cudaLaunchKernelEx(&cfg, kern, W, rows, nb, xq, y, residual, isum);
 }
 
-template <bool EMIT>
+template <bool EMIT, bool ROWS>
 cudaError_t dispatch(int nt, const uint8_t* W, int rows, int nb, const uint8_t* xq, float* y, const float* residual,
                      int32_t* isum, int S, size_t smem, cudaStream_t st) {
   switch (nt) {
 #define DSB_CASE(N) \
   case N:           \
-    return launch_nt<N, EMIT>(W, rows, nb, xq, y, residual, isum, S, smem, st);
+    return launch_nt<N, EMIT, ROWS>(W, rows, nb, xq, y, residual, isum, S, smem, st);
     DSB_CASE(1) DSB_CASE(2) DSB_CASE(3) DSB_CASE(4) DSB_CASE(5) DSB_CASE(6) DSB_CASE(7) DSB_CASE(8)
     DSB_CASE(9) DSB_CASE(10) DSB_CASE(11) DSB_CASE(12) DSB_CASE(13) DSB_CASE(14) DSB_CASE(15) DSB_CASE(16)
 #undef DSB_CASE
@@ -328,54 +418,73 @@ cudaError_t dispatch(int nt, const uint8_t* W, int rows, int nb, const uint8_t* 
   }
 }
 
-}  // namespace
+struct Plan {
+  bool rows_mode;
+  int S;
+};
 
-int matmul_split(int64_t rows, int64_t cols, int num_sms) {
-  // Depends on (rows, cols, SM count) only -- never on n_tok -- so that the
-  // summation order of every output is the same for every n_tok.  Each CTA of
-  // a cluster keeps the activations of its k-range in shared memory, which at
-  // n_tok = 16 allows at most 8 k-steps (36 KiB) next to the weight rings; among
-  // the admissible S the one with the smallest estimated makespan (tiles per
-  // cluster x k-steps per CTA, plus a per-tile reduction cost) wins, assuming
-  // two resident CTAs per SM.
+// Depends on (rows, cols, SM count) only -- never on n_tok -- so that the
+// summation order of every output is the same for every n_tok.  Each CTA of
+// a cluster keeps the activations of its k-range in shared memory, which at
+// n_tok = 16 allows at most 8 k-steps (36 KiB) next to the weight rings.
+// Rows mode (128-row tiles, no cross-warp sums) when there are at least as
+// many 128-row tiles per cluster slot as SMs; otherwise k-split mode on
+// 32-row tiles.  Among the admissible S the smallest estimated makespan (tiles
+// per cluster x k-steps per CTA, plus a per-tile reduction cost) wins,
+// assuming two resident CTAs per SM.
+Plan matmul_plan(int64_t rows, int64_t cols, int num_sms) {
   const int nks = (int)(cols / 256);
-  const int tiles = (int)((rows + kRowsPerCta - 1) / kRowsPerCta);
   int s_max = nks < 8 ? nks : 8;
   int s_min = (nks + 7) / 8;
   if (s_min > s_max) s_min = s_max;
   if (s_min < 1) s_min = 1;
   const int P = 2 * num_sms;
-  int best = s_min;
+  Plan best{false, s_min};
   double best_cost = 1e30;
-  for (int S = s_min; S <= s_max; ++S) {
-    const int clusters = P / S > 0 ? P / S : 1;
-    const int per = (tiles + clusters - 1) / clusters;
-    const double cost = per * (((nks + S - 1) / S) + 0.5);
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = S;
+  for (int mode = 0; mode < 2; ++mode) {
+    const bool rm = mode == 1;
+    const int tile = rm ? kWarps * kRowsPerCta : kRowsPerCta;
+    const int tiles = (int)((rows + tile - 1) / tile);
+    for (int S = s_min; S <= s_max; ++S) {
+      const int clusters = P / S > 0 ? P / S : 1;
+      const int per = (tiles + clusters - 1) / clusters;
+      const int ksteps = (nks + S - 1) / S;
+      // time ~ tiles per cluster x (k-steps each warp runs + per-tile sync cost)
+      const double sync = (rm && S == 1) ? 0.0 : 0.5;
+      const double warp_steps = rm ? (double)ksteps : (double)((ksteps + kWarps - 1) / kWarps);
+      const double c = per * (warp_steps + sync);
+      if (c < best_cost - 1e-9) {
+        best_cost = c;
+        best = Plan{rm, S};
+      }
     }
   }
   return best;
 }
 
+}  // namespace
+
+int matmul_split(int64_t rows, int64_t cols, int num_sms) { return matmul_plan(rows, cols, num_sms).S; }
+
 size_t matmul_smem_bytes(int64_t rows, int64_t cols, int n_tok, int num_sms) {
-  const int S = matmul_split(rows, cols, num_sms);
+  const Plan pl = matmul_plan(rows, cols, num_sms);
   const int nks = (int)(cols / 256);
-  const int kr_max = (nks + S - 1) / S;
-  return smem_bytes(kr_max, n_tok);
+  const int kr_max = (nks + pl.S - 1) / pl.S;
+  return smem_bytes(kr_max, n_tok, pl.rows_mode);
 }
 
 cudaError_t launch_matmul_q8_0_narrow(const void* W, int64_t rows, int64_t cols, const void* xq, int n_tok,
                                       float* y, const float* residual, int32_t* isum, int num_sms, cudaStream_t st) {
-  const int S = matmul_split(rows, cols, num_sms);
+  const Plan pl = matmul_plan(rows, cols, num_sms);
   const size_t smem = matmul_smem_bytes(rows, cols, n_tok, num_sms);
   const int nb = (int)(cols / 32);
+  const uint8_t* w8 = static_cast<const uint8_t*>(W);
+  const uint8_t* x8 = static_cast<const uint8_t*>(xq);
   if (isum)
-    return dispatch<true>(n_tok, static_cast<const uint8_t*>(W), (int)rows, nb, static_cast<const uint8_t*>(xq), y,
-                          residual, isum, S, smem, st);
-  return dispatch<false>(n_tok, static_cast<const uint8_t*>(W), (int)rows, nb, static_cast<const uint8_t*>(xq), y,
-                         residual, isum, S, smem, st);
+    return pl.rows_mode ? dispatch<true, true>(n_tok, w8, (int)rows, nb, x8, y, residual, isum, pl.S, smem, st)
+                        : dispatch<true, false>(n_tok, w8, (int)rows, nb, x8, y, residual, isum, pl.S, smem, st);
+  return pl.rows_mode ? dispatch<false, true>(n_tok, w8, (int)rows, nb, x8, y, residual, isum, pl.S, smem, st)
+                      : dispatch<false, false>(n_tok, w8, (int)rows, nb, x8, y, residual, isum, pl.S, smem, st);
 }
 
 namespace {

@@ -46,13 +46,12 @@ __device__ __forceinline__ void rope_cs(int pos, double freq, float* c, float* s
   sincosf((float)r, s, c);
 }
 
-__device__ __forceinline__ void rotate(float* x, int i, int half, float c, float s) {
-  const float x1 = __ldcg(x + i), x2 = __ldcg(x + i + half);
-  x[i] = __fmaf_rn(x1, c, __fmul_rn(-x2, s));
-  x[i + half] = __fmaf_rn(x1, s, __fmul_rn(x2, c));
-}
+// Heads handled per thread in one pass: every load of a pass is issued before
+// any store, so the pass costs one memory round trip instead of one per head.
+constexpr int kRopeHeads = 8;
 
-// One CTA per token row, one thread per pair, looping over the heads.
+// grid (n_tok, ceil((Hq + Hkv) / kRopeHeads)), one thread per pair.  Head slot
+// hs < Hq is query head hs, otherwise kv head hs - Hq of k.
 __global__ void rope_posvec_kernel(float* __restrict__ q, long long q_stride, int n_q_heads, float* __restrict__ k,
                                    long long k_stride, int n_kv_heads, int head_dim, const int32_t* __restrict__ pos,
                                    const __grid_constant__ RopeFreqs freqs) {
@@ -64,11 +63,28 @@ __global__ void rope_posvec_kernel(float* __restrict__ q, long long q_stride, in
   if (i >= half) return;
   float c, s;
   rope_cs(pos[t], freqs.f[i], &c, &s);
-  float* qt = q + (size_t)t * q_stride;
-  for (int h = 0; h < n_q_heads; ++h) rotate(qt + (size_t)h * head_dim, i, half, c, s);
-  if (k) {
-    float* kt = k + (size_t)t * k_stride;
-    for (int h = 0; h < n_kv_heads; ++h) rotate(kt + (size_t)h * head_dim, i, half, c, s);
+  const int h0 = blockIdx.y * kRopeHeads;
+  float* ptr[kRopeHeads];
+  float x1[kRopeHeads], x2[kRopeHeads];
+#pragma unroll
+  for (int u = 0; u < kRopeHeads; ++u) {
+    const int hs = h0 + u;
+    ptr[u] = nullptr;
+    if (hs < n_q_heads)
+      ptr[u] = q + (size_t)t * q_stride + (size_t)hs * head_dim;
+    else if (k && hs < n_q_heads + n_kv_heads)
+      ptr[u] = k + (size_t)t * k_stride + (size_t)(hs - n_q_heads) * head_dim;
+    if (ptr[u]) {
+      x1[u] = __ldcg(ptr[u] + i);
+      x2[u] = __ldcg(ptr[u] + i + half);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kRopeHeads; ++u) {
+    if (ptr[u]) {
+      ptr[u][i] = __fmaf_rn(x1[u], c, __fmul_rn(-x2[u], s));
+      ptr[u][i + half] = __fmaf_rn(x1[u], s, __fmul_rn(x2[u], c));
+    }
   }
 }
 
@@ -102,8 +118,10 @@ __global__ void kv_scatter_kernel(T* __restrict__ kc, T* __restrict__ vc, int n_
   }
 }
 
-// The step's fused pass: one CTA per token row, one thread per pair; rotates
-// q (in place) and k, writes the rotated k and the v row into the cache slot.
+// The step's fused pass, grid (n_tok, ceil((Hq + Hkv) / kRopeHeads)), one
+// thread per pair.  Head slot hs < Hq rotates query head hs in place; slot
+// Hq + g rotates kv head g of k and writes it, and kv head g of v, into the
+// cache slot of the token's sequence.  Loads of a pass precede its stores.
 template <typename T>
 __global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, int n_q_heads, int n_kv_heads,
                                      int head_dim, const int32_t* __restrict__ pos,
@@ -119,17 +137,41 @@ __global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, 
   float c, s;
   rope_cs(p, freqs.f[i], &c, &s);
   float* row = qkv + (size_t)t * stride;
-  for (int h = 0; h < n_q_heads; ++h) rotate(row + (size_t)h * head_dim, i, half, c, s);
   const int slot = batch_index[t / tokens_per_seq];
-  const float* kr = row + (size_t)n_q_heads * head_dim;
-  const float* vr = kr + (size_t)n_kv_heads * head_dim;
-  for (int h = 0; h < n_kv_heads; ++h) {
-    const float x1 = __ldcg(kr + (size_t)h * head_dim + i), x2 = __ldcg(kr + (size_t)h * head_dim + i + half);
-    const size_t dst = (((size_t)slot * n_kv_heads + h) * ctx + p) * head_dim;
-    kc[dst + i] = cvt_rn<T>(__fmaf_rn(x1, c, __fmul_rn(-x2, s)));
-    kc[dst + i + half] = cvt_rn<T>(__fmaf_rn(x1, s, __fmul_rn(x2, c)));
-    vc[dst + i] = cvt_rn<T>(__ldcg(vr + (size_t)h * head_dim + i));
-    vc[dst + i + half] = cvt_rn<T>(__ldcg(vr + (size_t)h * head_dim + i + half));
+  const int h0 = blockIdx.y * kRopeHeads;
+  float x1[kRopeHeads], x2[kRopeHeads], v1[kRopeHeads], v2[kRopeHeads];
+#pragma unroll
+  for (int u = 0; u < kRopeHeads; ++u) {
+    const int hs = h0 + u;
+    if (hs < n_q_heads + n_kv_heads) {
+      const float* src = row + (size_t)hs * head_dim;  // q heads, then k heads
+      x1[u] = __ldcg(src + i);
+      x2[u] = __ldcg(src + i + half);
+      if (hs >= n_q_heads) {
+        const float* vsrc = row + (size_t)(n_q_heads + n_kv_heads + hs - n_q_heads) * head_dim;
+        v1[u] = __ldcg(vsrc + i);
+        v2[u] = __ldcg(vsrc + i + half);
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kRopeHeads; ++u) {
+    const int hs = h0 + u;
+    if (hs >= n_q_heads + n_kv_heads) continue;
+    const float y1 = __fmaf_rn(x1[u], c, __fmul_rn(-x2[u], s));
+    const float y2 = __fmaf_rn(x1[u], s, __fmul_rn(x2[u], c));
+    if (hs < n_q_heads) {
+      float* dst = row + (size_t)hs * head_dim;
+      dst[i] = y1;
+      dst[i + half] = y2;
+    } else {
+      const int g = hs - n_q_heads;
+      const size_t dst = (((size_t)slot * n_kv_heads + g) * ctx + p) * head_dim;
+      kc[dst + i] = cvt_rn<T>(y1);
+      kc[dst + i + half] = cvt_rn<T>(y2);
+      vc[dst + i] = cvt_rn<T>(v1[u]);
+      vc[dst + i + half] = cvt_rn<T>(v2[u]);
+    }
   }
 }
 
@@ -141,8 +183,9 @@ cudaError_t launch_rope_posvec(float* q, long long q_stride, int n_q_heads, floa
   if (n_tok == 0) return cudaSuccess;
   const int half = head_dim / 2;
   const int threads = ((half + 31) / 32) * 32;
-  return launch_kernel(rope_posvec_kernel, dim3(n_tok), dim3(threads), 0, st, q, q_stride, n_q_heads, k, k_stride,
-                       n_kv_heads, head_dim, pos_dev, freqs);
+  const int groups = (n_q_heads + (k ? n_kv_heads : 0) + kRopeHeads - 1) / kRopeHeads;
+  return launch_kernel(rope_posvec_kernel, dim3(n_tok, groups), dim3(threads), 0, st, q, q_stride, n_q_heads, k,
+                       k_stride, n_kv_heads, head_dim, pos_dev, freqs);
 }
 
 cudaError_t launch_kv_scatter(void* kc, void* vc, int dtype, int n_kv_heads, int ctx, int head_dim,
@@ -166,11 +209,12 @@ cudaError_t launch_rope_kv_write(float* qkv, long long stride, int n_q_heads, in
                                  cudaStream_t st) {
   if (n_tok == 0) return cudaSuccess;
   const int threads = ((head_dim / 2 + 31) / 32) * 32;
+  const dim3 grid((unsigned)n_tok, (unsigned)((n_q_heads + n_kv_heads + kRopeHeads - 1) / kRopeHeads));
   if (dtype == 0)
-    return launch_kernel(rope_kv_write_kernel<__half>, dim3(n_tok), dim3(threads), 0, st, qkv, stride, n_q_heads,
+    return launch_kernel(rope_kv_write_kernel<__half>, grid, dim3(threads), 0, st, qkv, stride, n_q_heads,
                          n_kv_heads, head_dim, pos_dev, batch_index_dev, tokens_per_seq, static_cast<__half*>(kc),
                          static_cast<__half*>(vc), ctx, freqs);
-  return launch_kernel(rope_kv_write_kernel<__nv_bfloat16>, dim3(n_tok), dim3(threads), 0, st, qkv, stride, n_q_heads,
+  return launch_kernel(rope_kv_write_kernel<__nv_bfloat16>, grid, dim3(threads), 0, st, qkv, stride, n_q_heads,
                        n_kv_heads, head_dim, pos_dev, batch_index_dev, tokens_per_seq,
                        static_cast<__nv_bfloat16*>(kc), static_cast<__nv_bfloat16*>(vc), ctx, freqs);
 }
