@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr int kRed = ROWS ? 0 : kWarps * NT * 32;          // warp partials (k-split mode)
   constexpr int kSum = (ROWS ? kWarps : 1) * NT * 32;        // one CTA sum buffer
   constexpr int kSumBufs = ROWS ? 1 : 2;  // rows mode: one buffer, a second barrier per tile
+  constexpr int NTP = NT + (NT & 1);      // scale row stride: even, so token pairs load as 8 bytes
   extern __shared__ __align__(128) uint8_t smem[];
   const int nks = nb >> 3;
   const int S = gridDim.y;
@@ -135,8 +136,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   // rank 0 rely on that.
   const int kr_alloc = (nks + S - 1) / S;
   uint32_t* act_q = reinterpret_cast<uint32_t*>(smem);                              // [kr*8][NT][8]
-  float* act_s = reinterpret_cast<float*>(act_q + (size_t)kr_alloc * 8 * NT * 8);  // [kr*8][NT]
-  uint8_t* stages = reinterpret_cast<uint8_t*>(act_s + (size_t)kr_alloc * 8 * NT);  // [kWarps][kNStage][kStage]
+  float* act_s = reinterpret_cast<float*>(act_q + (size_t)kr_alloc * 8 * NT * 8);  // [kr*8][NTP]
+  uint8_t* stages = reinterpret_cast<uint8_t*>(act_s + (size_t)kr_alloc * 8 * NTP);  // [kWarps][kNStage][kStage]
   float* red = reinterpret_cast<float*>(stages + (size_t)kWarps * kNStage * kStage);  // [kWarps][NT][32]
   float* red_sum = red + kRed;                                                        // [kSumBufs][kSum]
   uint64_t* bars = reinterpret_cast<uint64_t*>(red_sum + kSumBufs * kSum);           // [kWarps][kNStage]
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint32_t* dq = act_q + ((size_t)b * NT + t) * 8;
 #pragma unroll
     for (int k = 0; k < 8; ++k) dq[k] = __funnelshift_rc(wv[k], wv[k + 1], sh);
-    act_s[(size_t)b * NT + t] = half_bits_to_float(odd ? (wv[0] >> 16) : wv[0]);
+    act_s[(size_t)b * NTP + t] = half_bits_to_float(odd ? (wv[0] >> 16) : wv[0]);
   }
   __syncthreads();
 
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           dw = half_bits_to_float(w[base] >> 16);
         }
         const uint32_t* aq = act_q + ((size_t)(kl * 8 + b) * NT) * 8;
-        const float* as = act_s + (size_t)(kl * 8 + b) * NT;
+        const float* as = act_s + (size_t)(kl * 8 + b) * NTP;  // 8-byte aligned row
         const unsigned long long dw2 = dup_pair(dw);
 #pragma unroll
         for (int t = 0; t < NT; t += 2) {
@@ -348,7 +349,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 size_t smem_bytes(int kr, int nt, bool rows_mode) {
   const size_t red = rows_mode ? 0 : (size_t)kWarps * nt * 32 * 4;
   const size_t sums = rows_mode ? (size_t)kWarps * nt * 32 * 4 : 2 * (size_t)nt * 32 * 4;
-  return (size_t)kr * 8 * nt * 36 + (size_t)kWarps * kNStage * kStage + red + sums + (size_t)kWarps * kNStage * 8;
+  const size_t ntp = (size_t)nt + (nt & 1);
+  return (size_t)kr * 8 * (nt * 32 + ntp * 4) + (size_t)kWarps * kNStage * kStage + red + sums +
+         (size_t)kWarps * kNStage * 8;
 }
 
 template <int NT, bool EMIT, bool ROWS>
