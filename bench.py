@@ -265,6 +265,47 @@ def matmul_sweep(flush, stream, peak, iters=5):
     return out
 
 
+ATTN_CTX = [32768, 65536]
+
+
+def attention_sweep(flush, stream, peak, iters=5):
+    """Split-K decode attention on the long-context shapes (128 query and 128
+    kv heads, head_dim 128, fp16 cache of full_batch_size 8), b = 1..4,
+    seq_lens uniform in [16384, ctx]: GB/s over the K and V bytes it must read
+    (each kv head's rows once) plus q, out and the split-K partials."""
+    import torch
+    from session_decode_step_dsb_gb300 import dsb, synth
+    out = []
+    F, H, D = 8, 128, 128
+    g = torch.Generator(device="cuda")
+    g.manual_seed(99)
+    for C in ATTN_CTX:
+        kc = torch.empty((F, H, C, D), dtype=torch.float16, device="cuda")
+        vc = torch.empty((F, H, C, D), dtype=torch.float16, device="cuda")
+        for f in range(F):
+            kc[f].normal_(generator=g)
+            vc[f].normal_(generator=g)
+        kv = dsb.kv_cache(kc.view(torch.int16), vc.view(torch.int16), dsb.DSB_F16)
+        ws = dsb.Workspace(4, H, D, C)
+        for b in (1, 2, 4):
+            bi = synth.distinct_slots(5, synth.stream_id(synth.STREAM_META, 7), b, F)
+            lens = synth.uniform_int(5, synth.stream_id(synth.STREAM_META, 8), 16384, C, b)
+            q = torch.randn((b, H, D), generator=g, device="cuda")
+            o = torch.empty_like(q)
+            for _ in range(2):
+                dsb.attention_decode_multi(q, kv, bi, 1, lens, ws, out=o)
+            med, mean, _ = _time_device(lambda: dsb.attention_decode_multi(q, kv, bi, 1, lens, ws, out=o), iters,
+                                        flush, stream)
+            chunks = int(np.sum((lens + 127) // 128))
+            byts = int(np.sum(lens)) * H * D * 2 * 2 + 2 * b * H * D * 4 + 2 * chunks * H * (D + 2) * 4
+            gbs = byts / (med * 1e-3) / 1e9
+            out.append({"ctx": C, "b": b, "seq_lens": [int(v) for v in lens], "us": round(med * 1e3, 1),
+                        "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)})
+        del kc, vc, kv, ws
+        torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------- dsb arm
 def run_dsb(args):
     import torch
@@ -348,6 +389,7 @@ def run_dsb(args):
         traffic = None
 
     sweep_mm = matmul_sweep(flush, stream, peak) if (world == 1 and not args.no_matmul_sweep) else []
+    sweep_attn = attention_sweep(flush, stream, peak) if (world == 1 and args.attn_sweep) else []
 
     # ---- end to end through the C ABI with host buffers: token ids, slots
     # and lengths from host arrays (staged by the library), logits copied back
@@ -400,6 +442,7 @@ def run_dsb(args):
                          "peak_kind": f"{peak_kind} hbm_gbs", "launches": per_kernel},
             "b_sweep": sweep,
             "matmul_q8_0_narrow": sweep_mm,
+            "attention_long_context": sweep_attn,
             "e2e": e2e,
             "gpu_launches": None,
             "clocks": clocks,
@@ -515,6 +558,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-matmul-sweep", action="store_true")
+    ap.add_argument("--attn-sweep", action="store_true",
+                    help="also time the split-K attention at ctx 32768/65536 (allocates ~70 GB)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

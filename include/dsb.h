@@ -274,6 +274,36 @@ dsb_status dsb_step_graph_launch(dsb_step_graph* g, const int32_t* token_ids, co
                                  const int32_t* seq_lens, void* stream);
 dsb_status dsb_step_graph_destroy(dsb_step_graph* g);
 
+/* ---- live-batch former (host only) -----------------------------------------
+ * Hands out the retained cache's slots to sessions and builds each step's
+ * metadata ([QAIC] "Objective": cache sized for full_batch_size, addressed by
+ * batch_index; [PTO] commit message: the live batch is the seq_lens
+ * descriptor; [DS4] "What": sessions join and leave between steps).  A session
+ * is named by its slot.  Not thread-safe; pure host code, no CUDA calls. */
+typedef struct dsb_batch_former dsb_batch_former;
+/* All arguments in range (full_batch_size <= DSB_MAX_SEQS, T <= ctx, F*T <=
+ * DSB_MAX_TOKENS) or DSB_ERR_INVALID_ARG. */
+dsb_status dsb_batch_former_create(int full_batch_size, int ctx, int tokens_per_seq, dsb_batch_former** out);
+void dsb_batch_former_destroy(dsb_batch_former* b);
+/* Gives a free slot (the lowest) to a session whose first prefill_length KV
+ * rows are already in the cache; DSB_ERR_UNSUPPORTED if every slot is live. */
+dsb_status dsb_batch_join(dsb_batch_former* b, int prefill_length, int32_t* slot_out);
+/* Frees the slot (its KV rows become garbage); DSB_ERR_INVALID_ARG if not live. */
+dsb_status dsb_batch_leave(dsb_batch_former* b, int slot);
+/* Queues the session's next T token ids (host int32[T], copied);
+ * DSB_ERR_UNSUPPORTED if its KV length + T would exceed ctx. */
+dsb_status dsb_batch_submit(dsb_batch_former* b, int slot, const int32_t* token_ids);
+/* Lists the live sessions with queued tokens in slot order: batch_index[n],
+ * seq_lens[n] (length after the step) and token_ids[n*T]; host arrays of
+ * capacity full_batch_size (and full_batch_size*T).  Does not change state. */
+dsb_status dsb_batch_form(const dsb_batch_former* b, int32_t* batch_index, int32_t* seq_lens, int32_t* token_ids,
+                          int32_t* n_seq_out);
+/* After the step ran: advances the listed sessions' KV lengths by T and
+ * clears their queued tokens.  Checks every slot before changing anything. */
+dsb_status dsb_batch_commit(dsb_batch_former* b, const int32_t* batch_index, int n_seq);
+/* KV length of a live slot, or -1. */
+int dsb_batch_length(const dsb_batch_former* b, int slot);
+
 #ifdef __cplusplus
 }
 #endif

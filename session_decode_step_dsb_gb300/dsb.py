@@ -271,7 +271,63 @@ SIGNATURES.update({
     "dsb_step_graph_create": (_I, [ctypes.POINTER(ModelC), _I, _I, _P, _P, _P, ctypes.POINTER(_P)]),
     "dsb_step_graph_launch": (_I, [_P, _PI32, _PI32, _PI32, _P]),
     "dsb_step_graph_destroy": (_I, [_P]),
+    "dsb_batch_former_create": (_I, [_I, _I, _I, ctypes.POINTER(_P)]),
+    "dsb_batch_former_destroy": (None, [_P]),
+    "dsb_batch_join": (_I, [_P, _I, _PI32]),
+    "dsb_batch_leave": (_I, [_P, _I]),
+    "dsb_batch_submit": (_I, [_P, _I, _PI32]),
+    "dsb_batch_form": (_I, [_P, _PI32, _PI32, _PI32, _PI32]),
+    "dsb_batch_commit": (_I, [_P, _PI32, _I]),
+    "dsb_batch_length": (_I, [_P, _I]),
 })
+
+
+class BatchFormer:
+    """Slot hand-out and per-step metadata for a live batch (host only)."""
+
+    def __init__(self, full_batch_size: int, ctx: int, tokens_per_seq: int = 1):
+        h = _P()
+        _check(lib().dsb_batch_former_create(full_batch_size, ctx, tokens_per_seq, ctypes.byref(h)))
+        self.handle, self.F, self.T = h, full_batch_size, tokens_per_seq
+
+    def join(self, prefill_length: int) -> int:
+        slot = ctypes.c_int32()
+        _check(lib().dsb_batch_join(self.handle, prefill_length, ctypes.byref(slot)))
+        return slot.value
+
+    def leave(self, slot: int):
+        _check(lib().dsb_batch_leave(self.handle, slot))
+
+    def submit(self, slot: int, token_ids):
+        arr, p = _i32(token_ids)
+        if arr.size != self.T:
+            raise ValueError("one token id per draft token")
+        _check(lib().dsb_batch_submit(self.handle, slot, p))
+
+    def form(self):
+        bi = np.zeros(self.F, np.int32)
+        sl = np.zeros(self.F, np.int32)
+        tk = np.zeros(self.F * self.T, np.int32)
+        n = ctypes.c_int32()
+        _check(lib().dsb_batch_form(self.handle, bi.ctypes.data_as(_PI32), sl.ctypes.data_as(_PI32),
+                                    tk.ctypes.data_as(_PI32), ctypes.byref(n)))
+        k = n.value
+        return bi[:k].copy(), sl[:k].copy(), tk[:k * self.T].copy()
+
+    def commit(self, batch_index):
+        arr, p = _i32(batch_index)
+        _check(lib().dsb_batch_commit(self.handle, p, arr.size))
+
+    def length(self, slot: int) -> int:
+        return lib().dsb_batch_length(self.handle, slot)
+
+    def __del__(self):
+        try:
+            if getattr(self, "handle", None):
+                lib().dsb_batch_former_destroy(self.handle)
+                self.handle = None
+        except Exception:
+            pass
 
 
 class StepWorkspace(Workspace):
