@@ -15,6 +15,11 @@ from session_decode_step_dsb_gb300 import synth
 from session_decode_step_dsb_gb300.workloads import LLAMA68M, ModelShape  # noqa: F401
 
 QWEN3_14B_1L = ModelShape("qwen3-14b-shaped-1-layer", 5120, 40, 8, 128, 17408, 151936, 1, 16, 4096, "bf16")
+# One Qwen3-14B-shaped layer (GQA 40/8, head_dim 128, FFN 17408, bf16 cache
+# [16, 8, 4096, 128]) under a 4096-row head: the layer is the workload's, the
+# head is cut to keep the oracle's weight draws to seconds (the full 151936-row
+# head is a plain matmul shape, checked by the matmul tests).
+QWEN3_14B_LAYER = ModelShape("qwen3-14b-shaped-layer", 5120, 40, 8, 128, 17408, 4096, 1, 16, 4096, "bf16")
 TINY = ModelShape("tiny", 256, 4, 2, 64, 512, 1000, 2, 4, 96, "f16")
 TINY_BF16 = ModelShape("tiny-bf16", 512, 8, 2, 128, 768, 700, 1, 5, 300, "bf16")
 

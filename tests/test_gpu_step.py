@@ -5,7 +5,7 @@ Each side builds its own model from the same seeded float32 draws: the GPU
 quantises its weights with its own kernel, the oracle with its own codec, and
 the bytes must agree.  The composed step is "parity unpinned" as a whole (no
 page prints an end-to-end value); its tolerance is derived in
-``STEP_TOL``'s comment.  The per-sequence and per-slot invariants are exact.
+the comment above ``STEP_TOL_RMS``.  The per-sequence and per-slot invariants are exact.
 """
 import numpy as np
 import pytest
@@ -17,16 +17,27 @@ from tests.gpu_util import to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
-# Logit tolerance, relative to the RMS of the reference logits.  The GPU
-# accumulates in float32 where the oracle uses float64, so the activations
-# entering each re-quantisation differ by ~1e-6 relative; when that moves a
-# value across a rounding boundary of its q8_0 code (rare), that one code
-# changes by 1, i.e. by d = max|x|/127 of its block.  Through the following
-# matmul such a flip perturbs an output by ~|w| * d, about 1e-3 of the output
-# RMS, and a step has 4 re-quantisations per layer plus the head's.  2e-2 of
-# the logit RMS bounds a handful of flips per row with margin; errors from
-# wrong wiring (head mapping, positions, slots) are O(1) of the RMS.
-STEP_TOL = 2e-2
+# Logit tolerances, relative to the RMS of the reference logits.  Both sides
+# round every activation to q8_0 codes before each matmul; where the float32
+# GPU value and the float64 oracle value fall on opposite sides of a rounding
+# boundary, that code differs by one step d = max|x|/127 (about 3/127 of the
+# block's RMS).  A relative activation difference eps flips a fraction
+# p ~ eps * |x| / d ~ 42 eps of the codes, and the flips move the next matmul's
+# output by sigma_w * d * sqrt(p K), i.e. by ~ (3/127) sqrt(42 eps) ~
+# 0.15 sqrt(eps) of its RMS.  The step re-quantises five times per layer, and
+# the map eps -> 0.15 sqrt(eps) has its fixed point at eps ~ 2.3e-2: one early
+# flip (a float32 rounding of the RMS-norm sum crossing an fp16 scale boundary
+# suffices) grows toward a few percent of the RMS, while a wiring error (head,
+# position, slot, scale) is O(1).  So the logits are held to an RMS error of
+# 3e-2 and a maximum error of 0.2 of the logit RMS, and the stages before the
+# first attention are pinned tightly below (new layer-0 cache rows), with each
+# fused kernel's own parity checked in its op test.
+STEP_TOL_RMS = 3e-2
+STEP_TOL_MAX = 2e-1
+# The new layer-0 K/V rows pass one q8_0 rounding (of the RMS-normed
+# embedding) before they are written: within one ulp of the cache dtype plus
+# 1e-3 of their RMS.
+CACHE_ULP = {"f16": 2.0 ** -10, "bf16": 2.0 ** -7}
 
 DT = {"f16": 0, "bf16": 1}
 
@@ -49,6 +60,7 @@ def _build(ms, seed=0):
     for k in ("head", "embed"):
         dev[k] = d.quantize_q8_0(to_dev(wf[k]))
         orc[k] = oq.quantize_rows(wf[k])
+        assert to_host(dev[k]).tobytes() == orc[k].tobytes()
     for k in ("attn_norm", "ffn_norm"):
         dev[k] = [to_dev(v) for v in wf[k]]
         orc[k] = wf[k]
@@ -71,8 +83,17 @@ def _rel_err(got, ref):
     return float(np.max(np.abs(got - ref)) / np.sqrt(np.mean(ref * ref)))
 
 
+def _rms_err(got, ref):
+    return float(np.sqrt(np.mean((got - ref) ** 2)) / np.sqrt(np.mean(ref * ref)))
+
+
+# Speculative decode on the llama shapes: T = K + 1 in {8, 32} puts n_tok = 32
+# and 64 tokens through every matmul (beyond the narrow kernel's 16), and the
+# causal mask inside the drafts through the attention.
 CASES = [(_shapes.TINY, 3, 1), (_shapes.TINY, 2, 4), (_shapes.TINY_BF16, 5, 1), (_shapes.LLAMA68M, 4, 1),
-         (_shapes.LLAMA68M, 1, 1)]
+         (_shapes.LLAMA68M, 1, 1), (_shapes.LLAMA68M, 4, 8), (_shapes.LLAMA68M, 2, 32),
+         pytest.param(_shapes.QWEN3_14B_LAYER, 3, 1, marks=pytest.mark.slow),
+         pytest.param(_shapes.QWEN3_14B_LAYER, 16, 1, marks=pytest.mark.slow)]
 
 
 @pytest.mark.parametrize("ms,b,T", CASES, ids=lambda c: getattr(c, "name", str(c)))
@@ -82,13 +103,23 @@ def test_step_matches_oracle(cuda_device, ms, b, T):
     ws = model.workspace(b * T)
     logits = to_host(model.step(toks, bi, T, lens, ws))
     ref, nk, nv = ostep.decode_step(_oshape(ms), orc, kc, vc, ms.cache_dtype, toks, bi, T, lens)
-    err = _rel_err(logits, ref)
-    assert err < STEP_TOL, f"max |g - r| / rms(r) = {err:.3e}"
+    err_rms, err_max = _rms_err(logits, ref), _rel_err(logits, ref)
+    assert err_rms < STEP_TOL_RMS, f"rms |g - r| / rms(r) = {err_rms:.3e}"
+    assert err_max < STEP_TOL_MAX, f"max |g - r| / rms(r) = {err_max:.3e}"
     # the argmax of every row agrees unless the top two logits are within tolerance
     top = np.argmax(ref, axis=1)
     for t in range(len(toks)):
         g = int(np.argmax(logits[t]))
-        assert g == top[t] or abs(ref[t, g] - ref[t, top[t]]) < STEP_TOL * np.sqrt(np.mean(ref * ref))
+        assert g == top[t] or abs(ref[t, g] - ref[t, top[t]]) < STEP_TOL_MAX * np.sqrt(np.mean(ref * ref))
+    # the new layer-0 rows, before any attention: tight
+    from oracle import kv as okv
+    for cache_g, cache_o in ((model.k_caches[0], nk[0]), (model.v_caches[0], nv[0])):
+        bits = to_host(cache_g).view(np.uint16)
+        g_rows = np.stack([bits[slot][:, lens[s] - T + j] for s, slot in enumerate(bi) for j in range(T)])
+        o_rows = np.stack([cache_o[slot][:, lens[s] - T + j] for s, slot in enumerate(bi) for j in range(T)])
+        gv, ov = okv.bits_to_f64(g_rows, ms.cache_dtype), okv.bits_to_f64(o_rows, ms.cache_dtype)
+        bound = CACHE_ULP[ms.cache_dtype] * np.abs(ov) + 1e-3 * np.sqrt(np.mean(ov * ov))
+        assert np.all(np.abs(gv - ov) <= bound), float(np.max(np.abs(gv - ov) / bound))
     # slots the step does not name are untouched; named slots change only at pos
     untouched = np.ones(ms.full_batch_size, bool)
     untouched[bi] = False
@@ -114,11 +145,11 @@ def test_batched_step_rows_equal_single_sequence_steps(cuda_device, ms, b, T):
         assert np.array_equal(one.view(np.uint32), batched[s * T:(s + 1) * T].view(np.uint32)), s
 
 
-def test_graph_replay_equals_eager_step(cuda_device):
+@pytest.mark.parametrize("b,T", [(4, 1), (2, 32)])
+def test_graph_replay_equals_eager_step(cuda_device, b, T):
     import torch
     ms = _shapes.LLAMA68M
     model, _, _, _ = _build(ms)
-    b, T = 4, 1
     ws = model.workspace(b * T)
     logits = torch.empty((b * T, ms.vocab), dtype=torch.float32, device="cuda")
     g = model.graph(b, T, logits, ws)
