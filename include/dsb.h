@@ -152,6 +152,29 @@ dsb_status dsb_matmul_q8_0(const dsb_q8_0_mat* w, const void* xq, int n_tok, flo
 dsb_status dsb_matmul_q8_0_block_dots(const dsb_q8_0_mat* w, const void* xq, int n_tok,
                                       int32_t* isum, void* stream);
 
+/* Scratch bytes dsb_matmul_q8_0_wide needs: the token operands packed for the
+ * tensor cores, ceil(n_tok/128) * cols/32 * 16384 bytes.  0 if n_tok is out
+ * of [1, DSB_MAX_TOKENS] or cols is not a positive multiple of 256. */
+size_t dsb_matmul_q8_0_wide_scratch_bytes(int n_tok, int64_t cols);
+
+/* Wide-batch q8_0 matmul on the tensor cores: the product of
+ * dsb_matmul_q8_0_narrow for any 1 <= n_tok <= DSB_MAX_TOKENS.  Speculative
+ * decode puts K+1 token rows per sequence through every matmul ([QAIC]
+ * "Assumptions and limitations"), beyond the narrow kernel's 16 ([DS4] "Why
+ * it's worth it -- the narrow-batch matmul").  Every dequantised value d*q is
+ * split exactly into two f16 values and the products accumulate in float32
+ * over the whole row (so the result differs from the narrow kernel's in
+ * rounding order only).  Weights are read once per 128 token rows.  Values
+ * must satisfy |d*q| <= 65504, i.e. q8_0 scales up to 65504/127; a larger
+ * scale makes dsb_device_error report DSB_ERR_DEVICE.  xq: device q8_0
+ * [n_tok][cols/32 blocks]; y: device float32 [n_tok][rows]; scratch: device,
+ * 16-byte aligned, at least dsb_matmul_q8_0_wide_scratch_bytes(n_tok, cols)
+ * bytes, owned by the caller and free again once the stream has passed the
+ * call.  Requires cols % 256 == 0 (DSB_ERR_UNSUPPORTED otherwise); a short
+ * scratch is DSB_ERR_WORKSPACE. */
+dsb_status dsb_matmul_q8_0_wide(const dsb_q8_0_mat* w, const void* xq, int n_tok, float* y,
+                                void* scratch, size_t scratch_bytes, void* stream);
+
 /* Pos-vector RoPE ([DS4] pos-vector RoPE commit): every token row t carries
  * its own position pos[t] (host int32[n_tok], each in [0, 2^24)).  In place
  * on q (device float32 [n_tok][n_q_heads][head_dim]) and k (device float32
@@ -188,6 +211,49 @@ dsb_status dsb_attention_decode_multi(const float* q, int n_q_heads, const dsb_k
                                       const int32_t* batch_index, int n_seq, int tokens_per_seq,
                                       const int32_t* seq_lens, float* out, dsb_workspace* ws,
                                       void* stream);
+
+/* The same attention with its output q8_0-quantised in the merge, as the
+ * decode step feeds the O projection ([DS4] "What": activations enter every
+ * matmul pre-quantised): xq receives n_tok rows of n_q_heads*head_dim/32
+ * q8_0 blocks (device, 16-byte aligned), row t holding heads 0..Hq-1 in order.
+ * Arguments and errors otherwise as dsb_attention_decode_multi. */
+dsb_status dsb_attention_decode_multi_q8_0(const float* q, int n_q_heads, const dsb_kv_cache* kv,
+                                           const int32_t* batch_index, int n_seq, int tokens_per_seq,
+                                           const int32_t* seq_lens, void* xq, dsb_workspace* ws,
+                                           void* stream);
+
+/* ---- step glue, one fused kernel per call ([DS4] "What": RoPE/norm around
+ * the attention projections and the dense stages run once for all sessions;
+ * each emits the pre-quantised q8_0 activations the next matmul reads). ---- */
+
+/* xq[t] = q8_0(x[t] / sqrt(mean(x[t]^2) + eps) * w), float32 arithmetic, the
+ * q8_0 codec of dsb_quantize_q8_0.  x: device float32 [n_tok][hidden]; w:
+ * device float32 [hidden]; xq: device q8_0 [n_tok][hidden/32].  hidden must be
+ * a multiple of 256 in [256, 8192] (DSB_ERR_UNSUPPORTED otherwise). */
+dsb_status dsb_rmsnorm_q8_0(const float* x, const float* w, int n_tok, int hidden, float eps, void* xq,
+                            void* stream);
+
+/* xq[t] = q8_0(silu(g) * u) with g = gu[t][0:ffn], u = gu[t][ffn:2*ffn],
+ * silu(g) = g / (1 + exp(-g)) in float32.  gu: device float32 [n_tok][2*ffn];
+ * xq: device q8_0 [n_tok][ffn/32]; ffn % 32 == 0. */
+dsb_status dsb_silu_mul_q8_0(const float* gu, int n_tok, int ffn, void* xq, void* stream);
+
+/* h[t] = the dequantised q8_0 row token_ids[t] of the embedding table
+ * (device q8_0 [vocab][hidden/32]); exact in float32.  token_ids: host int32
+ * [n_tok], each in [0, vocab) (DSB_ERR_INVALID_ARG otherwise); staged through
+ * the workspace.  h: device float32 [n_tok][hidden]. */
+dsb_status dsb_embed_q8_0(const void* table, int vocab, int hidden, const int32_t* token_ids, int n_tok,
+                          float* h, dsb_workspace* ws, void* stream);
+
+/* The step's fused RoPE + KV write on the [q | k | v] rows of a QKV
+ * projection: qkv is device float32 [n_tok][(n_q_heads + 2*Hkv) * head_dim].
+ * q heads are rotated in place (as dsb_rope_posvec); k rotated and v as is are
+ * written, converted to the cache dtype, at K/V[batch_index[s]][h][pos[t]]
+ * (as dsb_kv_scatter).  The k and v parts of qkv are left as they were.
+ * Arguments and errors as those two calls. */
+dsb_status dsb_rope_kv_write(float* qkv, int n_q_heads, const dsb_kv_cache* kv, const int32_t* batch_index,
+                             int n_seq, int tokens_per_seq, const int32_t* pos, float theta,
+                             dsb_workspace* ws, void* stream);
 
 /* Decode attention for callers that cannot allocate device memory: code
  * running inside an allocator hook or memory-pool callback, processes whose

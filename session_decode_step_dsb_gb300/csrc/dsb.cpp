@@ -228,9 +228,10 @@ dsb_status dsb_device_error(void) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
   const unsigned int m = dsbk::read_clear_error_matmul();
+  const unsigned int mt = dsbk::read_clear_error_matmul_tc();
   const unsigned int a = dsbk::read_clear_error_attention();
-  if (m || a)
-    return fail(DSB_ERR_DEVICE, "a kernel's bounded wait ran out (matmul=%u attention=%u)", m, a);
+  if (m || mt || a)
+    return fail(DSB_ERR_DEVICE, "a kernel's bounded wait ran out (matmul=%u matmul_tc=%u attention=%u)", m, mt, a);
   return DSB_OK;
 }
 
@@ -291,6 +292,34 @@ dsb_status dsb_matmul_q8_0(const dsb_q8_0_mat* w, const void* xq, int n_tok, flo
 dsb_status dsb_matmul_q8_0_block_dots(const dsb_q8_0_mat* w, const void* xq, int n_tok, int32_t* isum, void* stream) {
   if (!isum) return fail(DSB_ERR_INVALID_ARG, "isum is NULL");
   return matmul_common(w, xq, n_tok, nullptr, isum, stream, true);
+}
+
+size_t dsb_matmul_q8_0_wide_scratch_bytes(int n_tok, int64_t cols) {
+  if (n_tok < 1 || n_tok > DSB_MAX_TOKENS || cols < 256 || cols % 256) return 0;
+  return dsbk::matmul_tc_scratch_bytes(n_tok, cols);
+}
+
+dsb_status dsb_matmul_q8_0_wide(const dsb_q8_0_mat* w, const void* xq, int n_tok, float* y, void* scratch,
+                                size_t scratch_bytes, void* stream) {
+  dsb_status st = check_mat(w);
+  if (st != DSB_OK) return st;
+  if (n_tok < 1 || n_tok > DSB_MAX_TOKENS)
+    return fail(DSB_ERR_INVALID_ARG, "n_tok=%d out of [1, %d]", n_tok, DSB_MAX_TOKENS);
+  if (w->rows > (1LL << 31) - 128) return fail(DSB_ERR_UNSUPPORTED, "rows=%lld too large", (long long)w->rows);
+  if (!xq || !aligned16(xq)) return fail(DSB_ERR_INVALID_ARG, "xq is NULL or not 16-byte aligned");
+  if (!y || !aligned16(y)) return fail(DSB_ERR_INVALID_ARG, "y is NULL or not 16-byte aligned");
+  const size_t need = dsbk::matmul_tc_scratch_bytes(n_tok, w->cols);
+  if (!scratch || !aligned16(scratch)) return fail(DSB_ERR_WORKSPACE, "scratch is NULL or not 16-byte aligned");
+  if (scratch_bytes < need) return fail(DSB_ERR_WORKSPACE, "scratch has %zu bytes, needs %zu", scratch_bytes, need);
+  DeviceInfo di;
+  st = device_info(&di);
+  if (st != DSB_OK) return st;
+  if (dsbk::matmul_tc_smem_bytes() > (size_t)di.max_smem_optin)
+    return fail(DSB_ERR_UNSUPPORTED, "the tensor-core matmul needs %zu bytes of shared memory (max %d)",
+                dsbk::matmul_tc_smem_bytes(), di.max_smem_optin);
+  cudaError_t e = dsbk::launch_matmul_q8_0_tc(w->blocks, w->rows, w->cols, xq, n_tok, y, nullptr, scratch,
+                                              static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSB_OK : cuda_fail(e, "matmul_q8_0_wide launch");
 }
 
 dsb_status dsb_rope_posvec(float* q, int n_q_heads, float* k, int n_kv_heads, int head_dim, int n_tok,
@@ -354,9 +383,9 @@ dsb_status dsb_kv_scatter(const dsb_kv_cache* kv, const int32_t* batch_index, in
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "kv_scatter launch");
 }
 
-dsb_status dsb_attention_decode_multi(const float* q, int n_q_heads, const dsb_kv_cache* kv,
-                                      const int32_t* batch_index, int n_seq, int tokens_per_seq,
-                                      const int32_t* seq_lens, float* out, dsb_workspace* ws, void* stream) {
+static dsb_status attention_common(const float* q, int n_q_heads, const dsb_kv_cache* kv,
+                                   const int32_t* batch_index, int n_seq, int tokens_per_seq,
+                                   const int32_t* seq_lens, float* out, void* xq, dsb_workspace* ws, void* stream) {
   dsb_status st = check_kv(kv);
   if (st != DSB_OK) return st;
   if (n_q_heads < 1 || n_q_heads % kv->n_kv_heads)
@@ -368,8 +397,9 @@ dsb_status dsb_attention_decode_multi(const float* q, int n_q_heads, const dsb_k
     return fail(DSB_ERR_UNSUPPORTED, "head_dim=%d: attention serves 64 and 128", kv->head_dim);
   const long long R = (long long)(n_q_heads / kv->n_kv_heads) * tokens_per_seq;
   if (R > 64) return fail(DSB_ERR_UNSUPPORTED, "query rows per kv head (G*T=%lld) exceed 64", R);
-  if (!q || !out || !seq_lens) return fail(DSB_ERR_INVALID_ARG, "q / out / seq_lens is NULL");
-  if (!aligned16(q) || !aligned16(out)) return fail(DSB_ERR_INVALID_ARG, "q / out not 16-byte aligned");
+  if (!q || !(out || xq) || !seq_lens) return fail(DSB_ERR_INVALID_ARG, "q / out / seq_lens is NULL");
+  if (!aligned16(q) || (out && !aligned16(out)) || (xq && !aligned16(xq)))
+    return fail(DSB_ERR_INVALID_ARG, "q / out not 16-byte aligned");
   if (!ws) return fail(DSB_ERR_WORKSPACE, "workspace is NULL");
   for (int s = 0; s < n_seq; ++s)
     if (seq_lens[s] < tokens_per_seq || seq_lens[s] > kv->ctx)
@@ -398,8 +428,109 @@ dsb_status dsb_attention_decode_multi(const float* q, int n_q_heads, const dsb_k
   const int max_chunks = (kv->ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
   cudaError_t e = dsbk::launch_attention_decode_multi(
       q, (long long)n_q_heads * kv->head_dim, n_q_heads, kv->k, kv->v, kv->dtype, kv->n_kv_heads, kv->ctx, kv->head_dim, mv, n_seq, tokens_per_seq,
-      total * kv->n_kv_heads, max_chunks, reinterpret_cast<float*>(partial_base(ws)), out, nullptr, cs);
+      total * kv->n_kv_heads, max_chunks, reinterpret_cast<float*>(partial_base(ws)), out, xq, cs);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "attention_decode_multi launch");
+}
+
+dsb_status dsb_attention_decode_multi(const float* q, int n_q_heads, const dsb_kv_cache* kv,
+                                      const int32_t* batch_index, int n_seq, int tokens_per_seq,
+                                      const int32_t* seq_lens, float* out, dsb_workspace* ws, void* stream) {
+  if (!out) return fail(DSB_ERR_INVALID_ARG, "out is NULL");
+  return attention_common(q, n_q_heads, kv, batch_index, n_seq, tokens_per_seq, seq_lens, out, nullptr, ws, stream);
+}
+
+dsb_status dsb_attention_decode_multi_q8_0(const float* q, int n_q_heads, const dsb_kv_cache* kv,
+                                           const int32_t* batch_index, int n_seq, int tokens_per_seq,
+                                           const int32_t* seq_lens, void* xq, dsb_workspace* ws, void* stream) {
+  if (!xq) return fail(DSB_ERR_INVALID_ARG, "xq is NULL");
+  return attention_common(q, n_q_heads, kv, batch_index, n_seq, tokens_per_seq, seq_lens, nullptr, xq, ws, stream);
+}
+
+// ---- step glue, exposed one kernel at a time --------------------------------
+
+dsb_status dsb_rmsnorm_q8_0(const float* x, const float* w, int n_tok, int hidden, float eps, void* xq,
+                            void* stream) {
+  if (n_tok < 0 || n_tok > DSB_MAX_TOKENS) return fail(DSB_ERR_INVALID_ARG, "n_tok=%d out of [0, %d]", n_tok, DSB_MAX_TOKENS);
+  if (hidden < 256 || hidden % 256 || hidden > 8192)
+    return fail(DSB_ERR_UNSUPPORTED, "hidden=%d: RMSNorm serves multiples of 256 up to 8192", hidden);
+  if (!(eps > 0.0f) || !std::isfinite(eps)) return fail(DSB_ERR_INVALID_ARG, "eps must be finite and > 0");
+  if (n_tok == 0) return DSB_OK;
+  if (!x || !w || !xq) return fail(DSB_ERR_INVALID_ARG, "x / w / xq is NULL");
+  if (!aligned16(x) || !aligned16(w) || !aligned16(xq)) return fail(DSB_ERR_INVALID_ARG, "x / w / xq not 16-byte aligned");
+  cudaError_t e = dsbk::launch_rmsnorm_quant(x, w, n_tok, hidden, eps, xq, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSB_OK : cuda_fail(e, "rmsnorm_q8_0 launch");
+}
+
+dsb_status dsb_silu_mul_q8_0(const float* gu, int n_tok, int ffn, void* xq, void* stream) {
+  if (n_tok < 0 || n_tok > DSB_MAX_TOKENS) return fail(DSB_ERR_INVALID_ARG, "n_tok=%d out of [0, %d]", n_tok, DSB_MAX_TOKENS);
+  if (ffn < 32 || ffn % 32) return fail(DSB_ERR_INVALID_ARG, "ffn=%d is not a positive multiple of 32", ffn);
+  if (n_tok == 0) return DSB_OK;
+  if (!gu || !xq) return fail(DSB_ERR_INVALID_ARG, "gu / xq is NULL");
+  if (!aligned16(gu) || !aligned16(xq)) return fail(DSB_ERR_INVALID_ARG, "gu / xq not 16-byte aligned");
+  cudaError_t e = dsbk::launch_silu_mul_quant(gu, n_tok, ffn, xq, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSB_OK : cuda_fail(e, "silu_mul_q8_0 launch");
+}
+
+dsb_status dsb_embed_q8_0(const void* table, int vocab, int hidden, const int32_t* token_ids, int n_tok, float* h,
+                          dsb_workspace* ws, void* stream) {
+  if (n_tok < 0 || n_tok > DSB_MAX_TOKENS) return fail(DSB_ERR_INVALID_ARG, "n_tok=%d out of [0, %d]", n_tok, DSB_MAX_TOKENS);
+  if (vocab < 1) return fail(DSB_ERR_INVALID_ARG, "vocab=%d < 1", vocab);
+  if (hidden < 32 || hidden % 32) return fail(DSB_ERR_INVALID_ARG, "hidden=%d is not a positive multiple of 32", hidden);
+  if (!ws) return fail(DSB_ERR_WORKSPACE, "workspace is NULL");
+  if (n_tok == 0) return DSB_OK;
+  if (!table || !token_ids || !h) return fail(DSB_ERR_INVALID_ARG, "table / token_ids / h is NULL");
+  if (!aligned16(table) || !aligned16(h)) return fail(DSB_ERR_INVALID_ARG, "table / h not 16-byte aligned");
+  for (int t = 0; t < n_tok; ++t)
+    if (token_ids[t] < 0 || token_ids[t] >= vocab)
+      return fail(DSB_ERR_INVALID_ARG, "token_ids[%d]=%d out of [0, vocab=%d)", t, token_ids[t], vocab);
+  std::vector<int32_t> words(token_ids, token_ids + n_tok);
+  const int32_t* dev = nullptr;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  dsb_status st = stage(ws, words, cs, &dev);
+  if (st != DSB_OK) return st;
+  cudaError_t e = dsbk::launch_embed(table, hidden, dev, n_tok, h, cs);
+  return e == cudaSuccess ? DSB_OK : cuda_fail(e, "embed_q8_0 launch");
+}
+
+dsb_status dsb_rope_kv_write(float* qkv, int n_q_heads, const dsb_kv_cache* kv, const int32_t* batch_index,
+                             int n_seq, int tokens_per_seq, const int32_t* pos, float theta, dsb_workspace* ws,
+                             void* stream) {
+  dsb_status st = check_kv(kv);
+  if (st != DSB_OK) return st;
+  if (n_q_heads < 1 || n_q_heads % kv->n_kv_heads)
+    return fail(DSB_ERR_INVALID_ARG, "n_q_heads=%d is not a positive multiple of n_kv_heads=%d", n_q_heads,
+                kv->n_kv_heads);
+  if (kv->head_dim % 2 || kv->head_dim > 1024) return fail(DSB_ERR_INVALID_ARG, "head_dim=%d must be even, <= 1024", kv->head_dim);
+  st = check_batch(kv, batch_index, n_seq, tokens_per_seq);
+  if (st != DSB_OK) return st;
+  if (!(theta > 0.0f) || !std::isfinite(theta)) return fail(DSB_ERR_INVALID_ARG, "theta must be finite and > 0");
+  if (!qkv || !pos) return fail(DSB_ERR_INVALID_ARG, "qkv / pos is NULL");
+  if (!aligned16(qkv)) return fail(DSB_ERR_INVALID_ARG, "qkv not 16-byte aligned");
+  if (!ws) return fail(DSB_ERR_WORKSPACE, "workspace is NULL");
+  const int n_tok = n_seq * tokens_per_seq;
+  for (int s = 0; s < n_seq; ++s) {
+    for (int j = 0; j < tokens_per_seq; ++j) {
+      const int p = pos[s * tokens_per_seq + j];
+      if (p < 0 || p >= kv->ctx) return fail(DSB_ERR_INVALID_ARG, "pos[%d]=%d out of [0, ctx=%d)", s * tokens_per_seq + j, p, kv->ctx);
+      for (int j2 = 0; j2 < j; ++j2)
+        if (pos[s * tokens_per_seq + j2] == p)
+          return fail(DSB_ERR_INVALID_ARG, "sequence %d writes position %d twice", s, p);
+    }
+  }
+  std::vector<int32_t> words;
+  words.reserve((size_t)n_seq + n_tok);
+  words.insert(words.end(), batch_index, batch_index + n_seq);
+  words.insert(words.end(), pos, pos + n_tok);
+  const int32_t* dev = nullptr;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  st = stage(ws, words, cs, &dev);
+  if (st != DSB_OK) return st;
+  static thread_local dsbk::RopeFreqs freqs;
+  dsbk::rope_freqs((double)theta, kv->head_dim, &freqs);
+  const long long stride = (long long)(n_q_heads + 2 * kv->n_kv_heads) * kv->head_dim;
+  cudaError_t e = dsbk::launch_rope_kv_write(qkv, stride, n_q_heads, kv->n_kv_heads, kv->head_dim, dev + n_seq, dev,
+                                             tokens_per_seq, n_tok, kv->k, kv->v, kv->dtype, kv->ctx, freqs, cs);
+  return e == cudaSuccess ? DSB_OK : cuda_fail(e, "rope_kv_write launch");
 }
 
 }  // extern "C"
@@ -410,7 +541,7 @@ dsb_status dsb_attention_decode_multi(const float* q, int n_q_heads, const dsb_k
 namespace {
 
 struct StepLayout {
-  size_t h = 0, qkv = 0, att = 0, gu = 0, xq = 0, graph_meta = 0, partials = 0, total = 0;
+  size_t h = 0, qkv = 0, att = 0, gu = 0, xq = 0, graph_meta = 0, partials = 0, pack = 0, total = 0;
 };
 
 StepLayout step_layout(const dsb_model_shape& sh, int n_tok, int ctx) {
@@ -434,6 +565,8 @@ StepLayout step_layout(const dsb_model_shape& sh, int n_tok, int ctx) {
   L.xq = take(nt * (max_cols / 32) * 34);
   L.graph_meta = take(kMetaSlotBytes);
   L.partials = take(dsbk::attention_partial_bytes(n_tok, sh.n_q_heads, sh.head_dim, ctx));
+  // packed token operands of the tensor-core matmul (n_tok > DSB_NARROW_MAX)
+  L.pack = take(n_tok > DSB_NARROW_MAX ? dsbk::matmul_tc_scratch_bytes(n_tok, (int64_t)max_cols) : 0);
   L.total = off;
   return L;
 }
@@ -522,8 +655,12 @@ std::vector<int32_t> step_words(const int32_t* tokens, const int32_t* bi, int n_
   return w;
 }
 
+// n_tok <= DSB_NARROW_MAX: the narrow dp4a kernel; more: the tensor-core
+// kernel, with its token operands packed into `pack`.
 cudaError_t run_matmul(const dsb_q8_0_mat& w, const void* xq, int n_tok, float* y, const float* residual, int sms,
-                       cudaStream_t st) {
+                       void* pack, cudaStream_t st) {
+  if (n_tok > DSB_NARROW_MAX)
+    return dsbk::launch_matmul_q8_0_tc(w.blocks, w.rows, w.cols, xq, n_tok, y, residual, pack, st);
   const size_t blk_row = (size_t)(w.cols / 32) * 34;
   for (int t0 = 0; t0 < n_tok; t0 += DSB_NARROW_MAX) {
     const int nt = std::min(DSB_NARROW_MAX, n_tok - t0);
@@ -554,6 +691,7 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
   float* gu = reinterpret_cast<float*>(ws->dev + L.gu);
   void* xq = ws->dev + L.xq;
   float* partials = reinterpret_cast<float*>(ws->dev + L.partials);
+  void* pack = ws->dev + L.pack;
   const int D = s.head_dim, Hq = s.n_q_heads, Hkv = s.n_kv_heads;
   const long long qkv_stride = (long long)(Hq + 2 * Hkv) * D;
   const int max_chunks = (kv0.ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
@@ -567,7 +705,7 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
   for (int l = 0; l < s.n_layers && e == cudaSuccess; ++l) {
     const dsb_layer& Ly = m->layers[l];
     if ((e = dsbk::launch_rmsnorm_quant(h, Ly.attn_norm, n_tok, s.hidden, s.rms_eps, xq, st)) != cudaSuccess) break;
-    if ((e = run_matmul(Ly.wqkv, xq, n_tok, qkv, nullptr, sms, st)) != cudaSuccess) break;
+    if ((e = run_matmul(Ly.wqkv, xq, n_tok, qkv, nullptr, sms, pack, st)) != cudaSuccess) break;
     if ((e = dsbk::launch_rope_kv_write(qkv, qkv_stride, Hq, Hkv, D, pos_dev, bi_dev, tps, n_tok, Ly.kv.k, Ly.kv.v,
                                         Ly.kv.dtype, Ly.kv.ctx, freqs, st)) != cudaSuccess)
       break;
@@ -575,14 +713,14 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
                                                  mv, n_seq, tps, max_items, max_chunks, partials, att, xq, st)) !=
         cudaSuccess)
       break;
-    if ((e = run_matmul(Ly.wo, xq, n_tok, h, h, sms, st)) != cudaSuccess) break;
+    if ((e = run_matmul(Ly.wo, xq, n_tok, h, h, sms, pack, st)) != cudaSuccess) break;
     if ((e = dsbk::launch_rmsnorm_quant(h, Ly.ffn_norm, n_tok, s.hidden, s.rms_eps, xq, st)) != cudaSuccess) break;
-    if ((e = run_matmul(Ly.wgu, xq, n_tok, gu, nullptr, sms, st)) != cudaSuccess) break;
+    if ((e = run_matmul(Ly.wgu, xq, n_tok, gu, nullptr, sms, pack, st)) != cudaSuccess) break;
     if ((e = dsbk::launch_silu_mul_quant(gu, n_tok, s.ffn, xq, st)) != cudaSuccess) break;
-    if ((e = run_matmul(Ly.wdown, xq, n_tok, h, h, sms, st)) != cudaSuccess) break;
+    if ((e = run_matmul(Ly.wdown, xq, n_tok, h, h, sms, pack, st)) != cudaSuccess) break;
   }
   if (e == cudaSuccess) e = dsbk::launch_rmsnorm_quant(h, m->final_norm, n_tok, s.hidden, s.rms_eps, xq, st);
-  if (e == cudaSuccess) e = run_matmul(m->head, xq, n_tok, logits, nullptr, sms, st);
+  if (e == cudaSuccess) e = run_matmul(m->head, xq, n_tok, logits, nullptr, sms, pack, st);
   dsbk::set_pdl(false);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "decode step launch");
 }
@@ -601,10 +739,14 @@ dsb_status check_step_resources(const dsb_model* m, int n_tok, float* logits, ds
                                 {s.hidden, (long long)s.n_q_heads * s.head_dim},
                                 {2LL * s.ffn, s.hidden},
                                 {s.hidden, s.ffn}};
-  const int nt = n_tok < DSB_NARROW_MAX ? n_tok : DSB_NARROW_MAX;
-  for (auto& mm : mats)
-    if (dsbk::matmul_smem_bytes(mm[0], mm[1], nt, di.sms) > (size_t)di.max_smem_optin)
-      return fail(DSB_ERR_UNSUPPORTED, "a %lldx%lld matmul exceeds shared memory", mm[0], mm[1]);
+  if (n_tok > DSB_NARROW_MAX) {
+    if (dsbk::matmul_tc_smem_bytes() > (size_t)di.max_smem_optin)
+      return fail(DSB_ERR_UNSUPPORTED, "the tensor-core matmul exceeds shared memory");
+  } else {
+    for (auto& mm : mats)
+      if (dsbk::matmul_smem_bytes(mm[0], mm[1], n_tok, di.sms) > (size_t)di.max_smem_optin)
+        return fail(DSB_ERR_UNSUPPORTED, "a %lldx%lld matmul exceeds shared memory", mm[0], mm[1]);
+  }
   *sms = di.sms;
   return DSB_OK;
 }

@@ -57,6 +57,16 @@ size_t matmul_smem_bytes(int64_t rows, int64_t cols, int n_tok, int num_sms);
 cudaError_t launch_matmul_q8_0_narrow(const void* W, int64_t rows, int64_t cols, const void* xq, int n_tok, float* y,
                                       const float* residual, int32_t* isum, int num_sms, cudaStream_t st);
 
+// Wide-batch matmul on the tensor cores (csrc/matmul_q8_0_tc.cu), any n_tok
+// >= 1, cols % 256 == 0.  scratch: matmul_tc_scratch_bytes(n_tok, cols) bytes,
+// 16-byte aligned (the packed token operands).  residual (may alias y, may be
+// NULL): y = residual + W x.
+size_t matmul_tc_scratch_bytes(int n_tok, int64_t cols);
+size_t matmul_tc_smem_bytes();
+cudaError_t launch_matmul_q8_0_tc(const void* W, int64_t rows, int64_t cols, const void* xq, int n_tok, float* y,
+                                  const float* residual, void* scratch, cudaStream_t st);
+unsigned int read_clear_error_matmul_tc();
+
 cudaError_t launch_quantize_q8_0(const float* x, int64_t n_rows, int64_t cols, void* xq, cudaStream_t st);
 
 // Float64 frequencies theta^(-2i/D) of the rotate-half pairs (a model

@@ -1,0 +1,529 @@
+// Wide-batch q8_0 matmul on the 5th-generation tensor cores (sm_103a), for
+// n_tok > 16 token rows: speculative decode with K+1 drafts per sequence over
+// many sequences (quic/efficient-transformers PR #1305, "Assumptions and
+// limitations": K+1 tokens per sequence), where the narrow kernel's dp4a pipe,
+// not HBM, would bound the step (antirez/ds4 PR #530, "Why it's worth it -- the
+// narrow-batch matmul": past 16 tokens the page hands the batch to its
+// batched path).
+//
+// Math (the product of the narrow kernel, accumulated in another order):
+//   y[t][r] = sum_i sum_k (dW[r,i] qW[r,i,k]) (dX[t,i] qX[t,i,k]).
+// Each dequantised value v = d*q (fp16 scale d, int8 code q) is split exactly
+// into two f16 values, hi = RN(d*q) and lo = d*q - hi: lo is a multiple of
+// ulp(d) no larger than ulp(hi)/2, so it has at most 7 significant bits and is
+// exact in f16 (subnormal or not).  Then
+//   v_w v_x = hi_w hi_x + hi_w lo_x + lo_w hi_x + lo_w lo_x,
+// every product exact in float32.  Three kind::f16 MMAs per K step (the last
+// term, below 2^-22 of the first, is dropped) accumulate a chunk of 8 q8_0
+// blocks (K = 256) in a float32 TMEM accumulator; the scales are folded into
+// the operands, so no per-block work follows the MMAs.  The tensor core's
+// accumulation rounds toward zero, a bias of about 2^-24 of the partial sum
+// per accumulation, so chunks stay short: two accumulators alternate, and the
+// workers add each finished chunk into float32 registers (round to nearest).
+// Values must satisfy |d*q| <= 65504 (scales up to 65504/127); a larger scale
+// is flagged as a device error.
+//
+// CTA tile: 128 weight rows (TMEM lanes) x 128 token rows (TMEM columns),
+// one tile per CTA.  Warp roles (10 warps):
+//   0..7  workers.  During the K loop worker w owns weight rows 16w..16w+15:
+//         it stages their raw q8_0 bytes by 1-D bulk copies (8 blocks = 272 B
+//         per row, 16-byte aligned when cols % 256 == 0) into its own part of
+//         a two-stage ring, refilling a stage as soon as it has converted it,
+//         and writes their hi and lo operands, one q8_0 block per slot.  It
+//         also drains the chunk accumulators for TMEM lanes 32*(w%4).. and
+//         columns 64*(w/4).. into registers, a few blocks behind the MMAs, and
+//         at the end stores y (+ residual).  Warp 0 also allocates and frees
+//         the TMEM.
+//   8     producer: bulk copies of the token operands (hi and lo), which a
+//         pack kernel laid out once per call.
+//   9     MMA issuer (one thread).
+// Operand layout (no swizzle, K-major): element (m, k) of a 128 x 32 f16
+// operand at byte (m/8)*512 + (k/8)*128 + (m%8)*16 + (k%8)*2, i.e. 8x8 core
+// matrices of 128 contiguous bytes, 128 B apart along K (LBO) and 512 B apart
+// along M/N (SBO).
+//
+// Every mbarrier wait is bounded and sleeps in mbarrier.try_wait (with a
+// suspend-time hint) rather than spinning; on a timeout the CTA records a
+// device error, every role leaves its loop, the MMA thread and the copy
+// issuers wait (bounded) for what they issued, and the TMEM is freed before
+// exit.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "dsb_kernels.h"
+#include "dsb_ptx.cuh"
+
+namespace dsbk {
+
+namespace {
+
+constexpr int kTcM = 128;            // weight rows per CTA
+constexpr int kTcN = 128;            // token rows per CTA
+constexpr int kTcStageBlocks = 8;    // q8_0 blocks per raw weight stage
+constexpr int kTcRawStages = 2;
+constexpr int kTcSlots = 4;          // operand slots, one q8_0 block each
+constexpr int kTcWorkWarps = 8;
+constexpr int kTcRowsPerWarp = kTcM / kTcWorkWarps;           // 16
+constexpr int kTcProducerWarp = kTcWorkWarps;                 // 8
+constexpr int kTcMmaWarp = kTcProducerWarp + 1;               // 9
+constexpr int kTcThreads = (kTcMmaWarp + 1) * 32;             // 320
+constexpr int kTcChunk = 8;                                   // blocks per TMEM accumulation chunk
+constexpr int kTcAccRegions = 2;
+constexpr int kTcTmemCols = kTcAccRegions * kTcN;             // 256
+constexpr int kOpBytes = kTcM * 32 * 2;                       // 8192: one 128 x 32 f16 operand
+constexpr int kRawRowBytes = kTcStageBlocks * 34;             // 272
+constexpr int kRawStageBytes = kTcM * kRawRowBytes;           // 34816
+constexpr uint32_t kLbo = 128;
+constexpr uint32_t kSbo = 512;
+constexpr uint32_t kSuspendHintNs = 100000;                   // per try_wait
+static_assert(kTcN == kTcM, "token operands share the weight operands' geometry");
+
+struct __align__(1024) TcSmem {
+  uint8_t a[kTcSlots][2][kOpBytes];            // weight hi, lo (written by the workers)
+  uint8_t b[kTcSlots][2][kOpBytes];            // token hi, lo (bulk-copied from the pack)
+  uint8_t raw[kTcRawStages][kRawStageBytes];   // raw q8_0 weight rows
+  uint64_t raw_full[kTcRawStages][kTcWorkWarps];
+  uint64_t slot_full[kTcSlots], slot_empty[kTcSlots];
+  uint64_t acc_full[kTcAccRegions], acc_empty[kTcAccRegions];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ unsigned int g_err_matmul_tc = 0;
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// One poll that may suspend the thread for up to kSuspendHintNs; it resumes as
+// soon as the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait that also gives up as soon as another role of the CTA has.
+__device__ __forceinline__ bool tc_wait(TcSmem& s, uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if ((i & 15u) == 15u) {
+      if (*reinterpret_cast<volatile int*>(&s.abort_flag)) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+  *reinterpret_cast<volatile int*>(&s.abort_flag) = 1;
+  atomicOr(&g_err_matmul_tc, 1u);
+  return false;
+}
+
+// Short bounded wait used only on the way out (for copies or MMAs issued).
+__device__ __forceinline__ void tc_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait_sleep(bar, parity)) return;
+    if ((i & 15u) == 15u && globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: start address, LBO, SBO (all >> 4), the
+// descriptor version (1) at bit 46, no swizzle.
+__device__ __forceinline__ uint64_t smem_desc(const void* p) {
+  const uint32_t a = smem_addr(p);
+  return (uint64_t)((a & 0x3FFFFu) >> 4) | ((uint64_t)(kLbo >> 4) << 16) | ((uint64_t)(kSbo >> 4) << 32) |
+         (1ull << 46);
+}
+
+// Instruction descriptor of kind::f16: f32 accumulator (bits 4-5 = 1), f16 A
+// and B (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bit
+// 17, M >> 4 at bit 24.
+__device__ __forceinline__ uint32_t idesc_f16(int m, int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+// 32 consecutive TMEM columns of this warp's 32 lanes, one 32-bit word each.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Four int8 codes (one 32-bit word) -> two f16x2 words, exactly: the byte
+// q ^ 0x80 = q + 128 becomes the low mantissa byte of the f16 1024 + (q+128)
+// (exponent of 1024, unit spacing), and subtracting 1152 leaves q.
+__device__ __forceinline__ void codes_to_f16(uint32_t w, uint32_t& c01, uint32_t& c23) {
+  const uint32_t x = w ^ 0x80808080u;
+  const uint32_t a = __byte_perm(x, 0x64646464u, 0x4140);
+  const uint32_t b = __byte_perm(x, 0x64646464u, 0x4342);
+  const uint32_t bias = 0x64806480u;  // f16x2 (1152, 1152)
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(c01) : "r"(a), "r"(bias));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(c23) : "r"(b), "r"(bias));
+}
+
+// The value d*q of a code pair, split exactly into f16 hi + lo: hi = RN(d*q)
+// and lo = d*q - hi, which the fused multiply-add forms exactly (the
+// remainder is a multiple of ulp(d) below ulp(hi)/2: at most 7 significant
+// bits, representable in f16, subnormal or not).
+__device__ __forceinline__ void split_pair(uint32_t d2, uint32_t q2, uint32_t& hi, uint32_t& lo) {
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(d2), "r"(q2));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(lo) : "r"(d2), "r"(q2), "r"(hi ^ 0x80008000u));
+}
+
+// Eight codes (two words) of a block with scale d2 = (d, d) -> hi and lo
+// halves of its 16-byte operand chunk.
+__device__ __forceinline__ void split8(uint32_t w0, uint32_t w1, uint32_t d2, uint4& hi, uint4& lo) {
+  uint32_t q0, q1, q2, q3;
+  codes_to_f16(w0, q0, q1);
+  codes_to_f16(w1, q2, q3);
+  split_pair(d2, q0, hi.x, lo.x);
+  split_pair(d2, q1, hi.y, lo.y);
+  split_pair(d2, q2, hi.z, lo.z);
+  split_pair(d2, q3, hi.w, lo.w);
+}
+
+// |d*q| <= 127 d must stay below the f16 maximum 65504.
+constexpr float kMaxScale = 65504.0f / 127.0f;
+
+__device__ __forceinline__ float half_bits_to_float_tc(uint32_t bits) {
+  return __half2float(__ushort_as_half((unsigned short)(bits & 0xFFFFu)));
+}
+
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    matmul_q8_0_tc_kernel(const uint8_t* __restrict__ W, int rows, int nb, const uint8_t* pack, int n_tok,
+                          float* y, const float* residual) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // Align by pointer arithmetic on the shared array itself (not through an
+  // integer round trip), so that every access below stays a shared-memory one.
+  TcSmem& s = *reinterpret_cast<TcSmem*>(smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row0 = (int)blockIdx.x * kTcM;
+  const int tile = (int)blockIdx.y;
+  const int tok0 = tile * kTcN;
+  const int n_valid = min(kTcN, n_tok - tok0);
+  const int n_cols = (n_valid + 15) & ~15;
+  const int rows_valid = min(kTcM, rows - row0);
+  const int n_stages = nb / kTcStageBlocks;
+  const size_t row_bytes = (size_t)nb * 34;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kTcRawStages; ++i)
+      for (int c = 0; c < kTcWorkWarps; ++c) mbar_init(&s.raw_full[i][c], 1);
+    for (int i = 0; i < kTcSlots; ++i) {
+      mbar_init(&s.slot_full[i], kTcWorkWarps + 1);
+      mbar_init(&s.slot_empty[i], 1);
+    }
+    for (int i = 0; i < kTcAccRegions; ++i) {
+      mbar_init(&s.acc_full[i], 1);
+      mbar_init(&s.acc_empty[i], kTcWorkWarps);
+    }
+    s.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&s.tmem_base)),
+                 "r"(kTcTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+
+  if (warp == kTcProducerWarp) {
+    // ---------------------------------------------------------------- producer
+    int issued = 0;
+    pdl_wait();  // the packed token operands are the previous kernel's output
+    pdl_trigger();
+    for (int i = 0; i < nb; ++i) {
+      const int sl = i % kTcSlots;
+      bool ok = true;
+      if (i >= kTcSlots) ok = tc_wait(s, &s.slot_empty[sl], (uint32_t)((i / kTcSlots - 1) & 1));
+      if (!__all_sync(0xffffffffu, ok)) break;  // the warp leaves together
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&s.slot_full[sl], (uint32_t)(2 * kOpBytes));
+        bulk_g2s(s.b[sl][0], pack + ((size_t)tile * nb + i) * (2 * kOpBytes), 2 * kOpBytes, &s.slot_full[sl]);
+      }
+      ++issued;
+      __syncwarp();
+    }
+    // on the way out: every copy issued has landed (already so unless a wait gave up)
+    if (lane == 0)
+      for (int i = issued - kTcSlots; i < issued; ++i)
+        if (i >= 0) tc_drain(&s.slot_full[i % kTcSlots], (uint32_t)((i / kTcSlots) & 1));
+    __syncwarp();
+  } else if (warp == kTcMmaWarp) {
+    // -------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(kTcM, n_cols);
+      int issued = 0;
+      for (int i = 0; i < nb; ++i) {
+        const int sl = i % kTcSlots;
+        const int c = i / kTcChunk, jc = i % kTcChunk, ac = c % kTcAccRegions;
+        if (jc == 0 && c >= kTcAccRegions &&
+            !tc_wait(s, &s.acc_empty[ac], (uint32_t)((c / kTcAccRegions - 1) & 1)))
+          break;
+        if (!tc_wait(s, &s.slot_full[sl], (uint32_t)((i / kTcSlots) & 1))) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(ac * kTcN);
+        const uint64_t a_hi = smem_desc(s.a[sl][0]), a_lo = smem_desc(s.a[sl][1]);
+        const uint64_t b_hi = smem_desc(s.b[sl][0]), b_lo = smem_desc(s.b[sl][1]);
+#pragma unroll
+        for (int kh = 0; kh < 2; ++kh) {
+          // k = 16*kh .. +15: core matrices 2kh, 2kh+1 along K, 2 * LBO = 256 bytes per half
+          const uint64_t dk = (uint64_t)(kh * (256u >> 4));
+          mma_f16(d, a_hi + dk, b_hi + dk, idesc, (jc > 0 || kh > 0) ? 1u : 0u);
+          mma_f16(d, a_hi + dk, b_lo + dk, idesc, 1u);
+          mma_f16(d, a_lo + dk, b_hi + dk, idesc, 1u);
+        }
+        mma_commit(&s.slot_empty[sl]);
+        if (jc == kTcChunk - 1 || i == nb - 1) mma_commit(&s.acc_full[ac]);
+        issued = i + 1;
+      }
+      // on the way out: the MMAs issued have completed
+      if (issued > 0) tc_drain(&s.slot_empty[(issued - 1) % kTcSlots], (uint32_t)(((issued - 1) / kTcSlots) & 1));
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- workers
+    const int r0 = warp * kTcRowsPerWarp;
+    const int my_rows = max(0, min(kTcRowsPerWarp, rows_valid - r0));
+    const int r_sub = lane >> 2, g = lane & 3;
+    int raw_issued = 0;
+    bool ok = true;
+    const int q = warp & 3, c0 = (warp >> 2) * 64;
+    const int n_chunks = (nb + kTcChunk - 1) / kTcChunk;
+    float acc[64];
+#pragma unroll
+    for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+    int drained = 0;
+    // Add the finished accumulator of chunk c (this warp's lanes and columns)
+    // into acc, then hand the accumulator back to the MMA issuer.
+    auto drain = [&](int c) -> bool {
+      const int ac = c % kTcAccRegions;
+      bool w_ok = __all_sync(0xffffffffu, tc_wait(s, &s.acc_full[ac], (uint32_t)((c / kTcAccRegions) & 1)));
+      if (!w_ok) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (c0 + 32 * h < n_cols) {  // warp-uniform
+          uint32_t v[32];
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ac * kTcN + c0 + 32 * h), v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[32 * h + j] = __fadd_rn(acc[32 * h + j], __uint_as_float(v[j]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.acc_empty[ac]);
+      return true;
+    };
+    auto issue_raw = [&](int st) {  // this warp's rows of raw stage st
+      uint64_t* bar = &s.raw_full[st & 1][warp];
+      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(my_rows * kRawRowBytes));
+      __syncwarp();
+      if (lane < my_rows)
+        bulk_g2s(s.raw[st & 1] + (r0 + lane) * kRawRowBytes,
+                 W + (size_t)(row0 + r0 + lane) * row_bytes + (size_t)st * kRawRowBytes, kRawRowBytes, bar);
+    };
+    // the weights do not depend on the previous kernel: start them first
+    for (; raw_issued < kTcRawStages && raw_issued < n_stages; ++raw_issued) issue_raw(raw_issued);
+    bool range_ok = true;
+    for (int i = 0; i < nb; ++i) {
+      const int st = i / kTcStageBlocks, jb = i % kTcStageBlocks, rb = st & 1, sl = i % kTcSlots;
+      if (jb == 0) ok = tc_wait(s, &s.raw_full[rb][warp], (uint32_t)((st >> 1) & 1));
+      if (ok && i >= kTcSlots) ok = tc_wait(s, &s.slot_empty[sl], (uint32_t)((i / kTcSlots - 1) & 1));
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const uint8_t* raw = s.raw[rb];
+      // load both of this lane's items first, then convert and store
+      uint32_t wv[2][2], dv[2];
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int r = r0 + it * 8 + r_sub;
+        wv[it][0] = wv[it][1] = 0u;
+        dv[it] = 0u;
+        if (r < rows_valid) {
+          const int off = r * kRawRowBytes + jb * 34 + 2 + 8 * g;  // first of this lane's 8 codes
+          if (jb & 1) {  // codes start on a word boundary
+            wv[it][0] = *reinterpret_cast<const uint32_t*>(raw + off);
+            wv[it][1] = *reinterpret_cast<const uint32_t*>(raw + off + 4);
+          } else {       // two bytes into a word
+            const uint32_t a = *reinterpret_cast<const uint32_t*>(raw + off - 2);
+            const uint32_t b = *reinterpret_cast<const uint32_t*>(raw + off + 2);
+            const uint32_t c = *reinterpret_cast<const uint32_t*>(raw + off + 6);
+            wv[it][0] = __funnelshift_r(a, b, 16);
+            wv[it][1] = __funnelshift_r(b, c, 16);
+          }
+          dv[it] = *reinterpret_cast<const uint16_t*>(raw + r * kRawRowBytes + jb * 34);
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < 2; ++it) {
+        const int r = r0 + it * 8 + r_sub;
+        range_ok &= half_bits_to_float_tc(dv[it]) <= kMaxScale;
+        uint4 hi, lo;
+        split8(wv[it][0], wv[it][1], dv[it] | (dv[it] << 16), hi, lo);
+        const int o = (r >> 3) * 512 + g * 128 + (r & 7) * 16;
+        *reinterpret_cast<uint4*>(s.a[sl][0] + o) = hi;
+        *reinterpret_cast<uint4*>(s.a[sl][1] + o) = lo;
+      }
+      fence_proxy_async_smem();  // the generic-proxy writes above feed the tensor core (async proxy)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.slot_full[sl]);
+      // this warp alone reads its rows of the stage: refill it at once
+      if (jb == kTcStageBlocks - 1 && raw_issued < n_stages) {
+        fence_proxy_async_smem();
+        issue_raw(raw_issued);
+        ++raw_issued;
+      }
+      // the previous chunk's MMAs trail the conversions by at most the slot depth
+      if (i % kTcChunk == kTcSlots - 1 && i >= kTcChunk) {
+        ok = drain(drained);
+        ++drained;
+        if (!ok) break;
+      }
+    }
+    if (!range_ok) atomicOr(&g_err_matmul_tc, 2u);
+    // on the way out: every raw copy issued has landed
+    if (lane == 0)
+      for (int st = raw_issued - kTcRawStages; st < raw_issued; ++st)
+        if (st >= 0) tc_drain(&s.raw_full[st & 1][warp], (uint32_t)((st >> 1) & 1));
+    __syncwarp();
+
+    // ------------------------------------------------------------- epilogue
+    while (ok && drained < n_chunks) {
+      ok = drain(drained);
+      ++drained;
+    }
+    pdl_wait();  // y and the residual may be the previous kernels' data
+    pdl_trigger();
+    const int row = row0 + q * 32 + lane;
+    if (ok && row < rows) {
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        const int t = c0 + j;
+        if (t < n_valid) {
+          const size_t o = (size_t)(tok0 + t) * rows + row;
+          y[o] = residual ? __fadd_rn(__ldcg(residual + o), acc[j]) : acc[j];
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols) : "memory");
+  }
+}
+
+// Token operand pack: for token tile T (128 rows, zero past n_tok) and q8_0
+// block i, the hi and lo f16 operands (8 KiB each, hi first) in the layout
+// above.  Thread j of a CTA writes the j-th 16 bytes of each: token
+// (j>>5)*8 + (j&7), codes 8*((j>>3)&3) .. +7.
+__global__ void __launch_bounds__(512) pack_tokens_tc_kernel(const uint8_t* xq, int n_tok, int nb,
+                                                             uint8_t* __restrict__ pack) {
+  pdl_wait();
+  pdl_trigger();
+  const int i = (int)blockIdx.x, tile = (int)blockIdx.y;
+  const int j = threadIdx.x;
+  const int t_loc = (j >> 5) * 8 + (j & 7), g = (j >> 3) & 3;
+  const int t = tile * kTcN + t_loc;
+  uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;
+  if (t < n_tok) {
+    const uint8_t* blk = xq + ((size_t)t * nb + i) * 34;
+    const uint16_t* c = reinterpret_cast<const uint16_t*>(blk + 2 + 8 * g);  // blocks are 34 B: 2-aligned
+    uint32_t h[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      unsigned short v;
+      asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(v) : "l"(c + k) : "memory");
+      h[k] = v;
+    }
+    unsigned short sb;
+    asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(sb) : "l"(blk) : "memory");
+    if (half_bits_to_float_tc(sb) > kMaxScale) atomicOr(&g_err_matmul_tc, 2u);
+    split8(h[0] | (h[1] << 16), h[2] | (h[3] << 16), (uint32_t)sb | ((uint32_t)sb << 16), hi, lo);
+  }
+  uint8_t* slot = pack + ((size_t)tile * nb + i) * (2 * kOpBytes);
+  reinterpret_cast<uint4*>(slot)[j] = hi;
+  reinterpret_cast<uint4*>(slot + kOpBytes)[j] = lo;
+}
+
+std::once_flag g_tc_attr_once;
+cudaError_t g_tc_attr_err = cudaSuccess;
+
+}  // namespace
+
+size_t matmul_tc_scratch_bytes(int n_tok, int64_t cols) {
+  if (n_tok < 1 || cols < 32) return 0;
+  const size_t tiles = (size_t)((n_tok + kTcN - 1) / kTcN);
+  return tiles * (size_t)(cols / 32) * 2 * kOpBytes;
+}
+
+size_t matmul_tc_smem_bytes() { return sizeof(TcSmem) + 1024; }
+
+cudaError_t launch_matmul_q8_0_tc(const void* W, int64_t rows, int64_t cols, const void* xq, int n_tok, float* y,
+                                  const float* residual, void* scratch, cudaStream_t st) {
+  if (n_tok <= 0 || rows <= 0) return cudaSuccess;
+  const size_t smem = matmul_tc_smem_bytes();
+  std::call_once(g_tc_attr_once, [&] {
+    g_tc_attr_err = cudaFuncSetAttribute(matmul_q8_0_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
+  if (g_tc_attr_err != cudaSuccess) return g_tc_attr_err;
+  const int nb = (int)(cols / 32);
+  const int tiles = (n_tok + kTcN - 1) / kTcN;
+  uint8_t* pack = static_cast<uint8_t*>(scratch);
+  cudaError_t e = launch_kernel(pack_tokens_tc_kernel, dim3((unsigned)nb, (unsigned)tiles), dim3(512), 0, st,
+                                static_cast<const uint8_t*>(xq), n_tok, nb, pack);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)((rows + kTcM - 1) / kTcM), (unsigned)tiles);
+  return launch_kernel(matmul_q8_0_tc_kernel, grid, dim3(kTcThreads), smem, st, static_cast<const uint8_t*>(W),
+                       (int)rows, nb, static_cast<const uint8_t*>(pack), n_tok, y, residual);
+}
+
+unsigned int read_clear_error_matmul_tc() {
+  unsigned int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_matmul_tc, sizeof v) != cudaSuccess) return 0xFFFFFFFFu;
+  cudaMemcpyToSymbol(g_err_matmul_tc, &z, sizeof z);
+  return v;
+}
+
+}  // namespace dsbk

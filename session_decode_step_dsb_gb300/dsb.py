@@ -16,6 +16,7 @@ import numpy as np
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libdsb.so")
 
 DSB_OK = 0
+DSB_ERR_UNSUPPORTED = 2
 STATUS_NAMES = {0: "DSB_OK", 1: "DSB_ERR_INVALID_ARG", 2: "DSB_ERR_UNSUPPORTED", 3: "DSB_ERR_WORKSPACE",
                 4: "DSB_ERR_CUDA", 5: "DSB_ERR_TIMEOUT", 6: "DSB_ERR_DEVICE"}
 DSB_F16, DSB_BF16 = 0, 1
@@ -61,10 +62,17 @@ SIGNATURES = {
     "dsb_matmul_q8_0_narrow": (_I, [ctypes.POINTER(Q8Mat), _P, _I, _P, _P]),
     "dsb_matmul_q8_0": (_I, [ctypes.POINTER(Q8Mat), _P, _I, _P, _P]),
     "dsb_matmul_q8_0_block_dots": (_I, [ctypes.POINTER(Q8Mat), _P, _I, _P, _P]),
+    "dsb_matmul_q8_0_wide_scratch_bytes": (ctypes.c_size_t, [_I, _I64]),
+    "dsb_matmul_q8_0_wide": (_I, [ctypes.POINTER(Q8Mat), _P, _I, _P, _P, ctypes.c_size_t, _P]),
     "dsb_rope_posvec": (_I, [_P, _I, _P, _I, _I, _I, _PI32, _F, _P, _P]),
     "dsb_kv_scatter": (_I, [ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P, _P, _P]),
     "dsb_attention_decode_multi": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P, _P]),
     "dsb_attention_decode_multi_noalloc": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P]),
+    "dsb_attention_decode_multi_q8_0": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P, _P]),
+    "dsb_rmsnorm_q8_0": (_I, [_P, _P, _I, _I, _F, _P, _P]),
+    "dsb_silu_mul_q8_0": (_I, [_P, _I, _I, _P, _P]),
+    "dsb_embed_q8_0": (_I, [_P, _I, _I, _PI32, _I, _P, _P, _P]),
+    "dsb_rope_kv_write": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _F, _P, _P]),
 }
 
 
@@ -196,6 +204,28 @@ def matmul_q8_0_block_dots(w_blocks, rows: int, cols: int, xq, n_tok: int, strea
     return isum
 
 
+def _wide_scratch(n_tok: int, cols: int, device):
+    import torch
+    nbytes = lib().dsb_matmul_q8_0_wide_scratch_bytes(n_tok, cols)
+    if nbytes == 0:
+        raise DsbError(DSB_ERR_UNSUPPORTED, f"no wide-matmul scratch size for n_tok={n_tok}, cols={cols}")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device), nbytes
+
+
+def matmul_q8_0_wide(w_blocks, rows: int, cols: int, xq, n_tok: int, y=None, scratch=None, stream=None):
+    """Same product on the tensor cores (any n_tok; cols % 256 == 0).  ``scratch``
+    (uint8 device tensor) is allocated when not given."""
+    import torch
+    if y is None:
+        y = torch.empty((n_tok, rows), dtype=torch.float32, device=w_blocks.device)
+    if scratch is None:
+        scratch, _ = _wide_scratch(n_tok, cols, w_blocks.device)
+    m = _mat(w_blocks, rows, cols)
+    _check(lib().dsb_matmul_q8_0_wide(ctypes.byref(m), _ptr(xq), n_tok, _ptr(y), _ptr(scratch), scratch.numel(),
+                                      _stream(stream)))
+    return y
+
+
 def rope_posvec(q, k, pos, theta: float, ws: Workspace, stream=None):
     """In-place RoPE on ``q[n_tok, Hq, D]`` and ``k[n_tok, Hkv, D]`` (k may be None)."""
     n_tok, hq, d = q.shape
@@ -246,6 +276,57 @@ def attention_decode_multi(q, kv: KVCache, batch_index, tokens_per_seq: int, seq
     _check(lib().dsb_attention_decode_multi(_ptr(q), hq, ctypes.byref(kv), pbi, len(bi), tokens_per_seq, psl,
                                             _ptr(out), ws.handle, _stream(stream)))
     return out
+
+
+def attention_decode_multi_q8_0(q, kv: KVCache, batch_index, tokens_per_seq: int, seq_lens, ws: Workspace,
+                                stream=None):
+    """The attention with its rows q8_0-quantised: uint8 ``[n_tok, Hq*D/32*34]``."""
+    import torch
+    n_tok, hq, d = q.shape
+    xq = torch.empty((n_tok, hq * d // 32 * 34), dtype=torch.uint8, device=q.device)
+    bi, pbi = _i32(batch_index)
+    sl, psl = _i32(seq_lens)
+    _check(lib().dsb_attention_decode_multi_q8_0(_ptr(q), hq, ctypes.byref(kv), pbi, len(bi), tokens_per_seq, psl,
+                                                 _ptr(xq), ws.handle, _stream(stream)))
+    return xq
+
+
+def rmsnorm_q8_0(x, w, eps: float, stream=None):
+    """q8_0 ``[n_tok, hidden/32*34]`` of the RMS-normed rows of ``x``."""
+    import torch
+    n_tok, hidden = x.shape
+    xq = torch.empty((n_tok, hidden // 32 * 34), dtype=torch.uint8, device=x.device)
+    _check(lib().dsb_rmsnorm_q8_0(_ptr(x), _ptr(w), n_tok, hidden, float(eps), _ptr(xq), _stream(stream)))
+    return xq
+
+
+def silu_mul_q8_0(gu, stream=None):
+    """q8_0 of silu(gate) * up for ``gu[n_tok, 2*ffn]`` = [gate | up]."""
+    import torch
+    n_tok, two_ffn = gu.shape
+    ffn = two_ffn // 2
+    xq = torch.empty((n_tok, ffn // 32 * 34), dtype=torch.uint8, device=gu.device)
+    _check(lib().dsb_silu_mul_q8_0(_ptr(gu), n_tok, ffn, _ptr(xq), _stream(stream)))
+    return xq
+
+
+def embed_q8_0(table, vocab: int, hidden: int, token_ids, ws: Workspace, stream=None):
+    """float32 ``[n_tok, hidden]``: dequantised embedding rows of the tokens."""
+    import torch
+    tk, ptk = _i32(token_ids)
+    h = torch.empty((len(tk), hidden), dtype=torch.float32, device=table.device)
+    _check(lib().dsb_embed_q8_0(_ptr(table), vocab, hidden, ptk, len(tk), _ptr(h), ws.handle, _stream(stream)))
+    return h
+
+
+def rope_kv_write(qkv, n_q_heads: int, kv: KVCache, batch_index, tokens_per_seq: int, pos, theta: float,
+                  ws: Workspace, stream=None):
+    """Fused RoPE + KV write on ``qkv[n_tok, (Hq + 2 Hkv) * D]`` (q rotated in place)."""
+    bi, pbi = _i32(batch_index)
+    ps, pp = _i32(pos)
+    _check(lib().dsb_rope_kv_write(_ptr(qkv), n_q_heads, ctypes.byref(kv), pbi, len(bi), tokens_per_seq, pp,
+                                   float(theta), ws.handle, _stream(stream)))
+    return qkv
 
 
 # ---------------------------------------------------------------- decode step
