@@ -23,8 +23,12 @@
 // Values must satisfy |d*q| <= 65504 (scales up to 65504/127); a larger scale
 // is flagged as a device error.
 //
-// CTA tile: 128 weight rows (TMEM lanes) x 128 token rows (TMEM columns),
-// one tile per CTA.  Warp roles (10 warps):
+// CTA tile: 128 weight rows (TMEM lanes) x 128 token rows (TMEM columns).
+// Narrow matrices are split along K over the S CTAs of a thread-block
+// cluster (grid z, S <= 8, each CTA a contiguous range of 8-block chunks) so
+// that the grid fills the SMs; rank 0 then adds the other ranks' float32
+// partial tiles through distributed shared memory in rank order (no atomics,
+// the same order on every run).  Warp roles (10 warps):
 //   0..7  workers.  During the K loop worker w owns weight rows 16w..16w+15:
 //         it stages their raw q8_0 bytes by 1-D bulk copies (8 blocks = 272 B
 //         per row, 16-byte aligned when cols % 256 == 0) into its own part of
@@ -90,7 +94,9 @@ struct __align__(1024) TcSmem {
   uint64_t acc_full[kTcAccRegions], acc_empty[kTcAccRegions];
   uint32_t tmem_base;
   int abort_flag;
+  int cta_ok;
 };
+static_assert(sizeof(((TcSmem*)nullptr)->a) >= (size_t)kTcM * kTcN * 4, "the partial tile reuses the weight slots");
 
 __device__ unsigned int g_err_matmul_tc = 0;
 
@@ -133,6 +139,13 @@ __device__ __forceinline__ void tc_drain(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait_sleep(bar, parity)) return;
     if ((i & 15u) == 15u && globaltimer_ns() - t0 > kWaitLimitNs) return;
   }
+}
+
+__device__ __forceinline__ uint32_t ld_dsmem_u32(const void* p, uint32_t rank) {
+  uint32_t remote, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(p)), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -236,8 +249,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int n_valid = min(kTcN, n_tok - tok0);
   const int n_cols = (n_valid + 15) & ~15;
   const int rows_valid = min(kTcM, rows - row0);
-  const int n_stages = nb / kTcStageBlocks;
   const size_t row_bytes = (size_t)nb * 34;
+  // this CTA's chunks of the K range (cluster rank = blockIdx.z)
+  const int S = (int)gridDim.z, rank = (int)blockIdx.z;
+  const int n_chunks_all = nb / kTcChunk;
+  const int c_lo = (int)((long long)n_chunks_all * rank / S);
+  const int c_hi = (int)((long long)n_chunks_all * (rank + 1) / S);
+  const int kb0 = c_lo * kTcChunk;           // first q8_0 block
+  const int nbl = (c_hi - c_lo) * kTcChunk;  // blocks of this CTA
+  const int n_stages = nbl / kTcStageBlocks;
+  static_assert(kTcStageBlocks == kTcChunk, "a raw stage is one accumulation chunk");
+  bool ok = true;
+  float acc[64];
+#pragma unroll
+  for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+  const int q = warp & 3, c0 = (warp >> 2) * 64;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kTcRawStages; ++i)
@@ -269,14 +295,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int issued = 0;
     pdl_wait();  // the packed token operands are the previous kernel's output
     pdl_trigger();
-    for (int i = 0; i < nb; ++i) {
+    for (int i = 0; i < nbl; ++i) {
       const int sl = i % kTcSlots;
-      bool ok = true;
       if (i >= kTcSlots) ok = tc_wait(s, &s.slot_empty[sl], (uint32_t)((i / kTcSlots - 1) & 1));
-      if (!__all_sync(0xffffffffu, ok)) break;  // the warp leaves together
+      ok = __all_sync(0xffffffffu, ok);  // the warp leaves together
+      if (!ok) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&s.slot_full[sl], (uint32_t)(2 * kOpBytes));
-        bulk_g2s(s.b[sl][0], pack + ((size_t)tile * nb + i) * (2 * kOpBytes), 2 * kOpBytes, &s.slot_full[sl]);
+        bulk_g2s(s.b[sl][0], pack + ((size_t)tile * nb + kb0 + i) * (2 * kOpBytes), 2 * kOpBytes, &s.slot_full[sl]);
       }
       ++issued;
       __syncwarp();
@@ -291,13 +317,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_f16(kTcM, n_cols);
       int issued = 0;
-      for (int i = 0; i < nb; ++i) {
+      for (int i = 0; i < nbl; ++i) {
         const int sl = i % kTcSlots;
         const int c = i / kTcChunk, jc = i % kTcChunk, ac = c % kTcAccRegions;
         if (jc == 0 && c >= kTcAccRegions &&
-            !tc_wait(s, &s.acc_empty[ac], (uint32_t)((c / kTcAccRegions - 1) & 1)))
+            !tc_wait(s, &s.acc_empty[ac], (uint32_t)((c / kTcAccRegions - 1) & 1))) {
+          ok = false;
           break;
-        if (!tc_wait(s, &s.slot_full[sl], (uint32_t)((i / kTcSlots) & 1))) break;
+        }
+        if (!tc_wait(s, &s.slot_full[sl], (uint32_t)((i / kTcSlots) & 1))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(ac * kTcN);
         const uint64_t a_hi = smem_desc(s.a[sl][0]), a_lo = smem_desc(s.a[sl][1]);
@@ -311,25 +342,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mma_f16(d, a_lo + dk, b_hi + dk, idesc, 1u);
         }
         mma_commit(&s.slot_empty[sl]);
-        if (jc == kTcChunk - 1 || i == nb - 1) mma_commit(&s.acc_full[ac]);
+        if (jc == kTcChunk - 1 || i == nbl - 1) mma_commit(&s.acc_full[ac]);
         issued = i + 1;
       }
       // on the way out: the MMAs issued have completed
       if (issued > 0) tc_drain(&s.slot_empty[(issued - 1) % kTcSlots], (uint32_t)(((issued - 1) / kTcSlots) & 1));
     }
-    __syncwarp();
+    ok = __shfl_sync(0xffffffffu, ok, 0);
   } else {
     // ---------------------------------------------------------------- workers
     const int r0 = warp * kTcRowsPerWarp;
     const int my_rows = max(0, min(kTcRowsPerWarp, rows_valid - r0));
     const int r_sub = lane >> 2, g = lane & 3;
     int raw_issued = 0;
-    bool ok = true;
-    const int q = warp & 3, c0 = (warp >> 2) * 64;
-    const int n_chunks = (nb + kTcChunk - 1) / kTcChunk;
-    float acc[64];
-#pragma unroll
-    for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+    const int n_chunks = nbl / kTcChunk;
     int drained = 0;
     // Add the finished accumulator of chunk c (this warp's lanes and columns)
     // into acc, then hand the accumulator back to the MMA issuer.
@@ -359,12 +385,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       if (lane < my_rows)
         bulk_g2s(s.raw[st & 1] + (r0 + lane) * kRawRowBytes,
-                 W + (size_t)(row0 + r0 + lane) * row_bytes + (size_t)st * kRawRowBytes, kRawRowBytes, bar);
+                 W + (size_t)(row0 + r0 + lane) * row_bytes + (size_t)(c_lo + st) * kRawRowBytes, kRawRowBytes, bar);
     };
     // the weights do not depend on the previous kernel: start them first
     for (; raw_issued < kTcRawStages && raw_issued < n_stages; ++raw_issued) issue_raw(raw_issued);
     bool range_ok = true;
-    for (int i = 0; i < nb; ++i) {
+    for (int i = 0; i < nbl; ++i) {
       const int st = i / kTcStageBlocks, jb = i % kTcStageBlocks, rb = st & 1, sl = i % kTcSlots;
       if (jb == 0) ok = tc_wait(s, &s.raw_full[rb][warp], (uint32_t)((st >> 1) & 1));
       if (ok && i >= kTcSlots) ok = tc_wait(s, &s.slot_empty[sl], (uint32_t)((i / kTcSlots - 1) & 1));
@@ -426,24 +452,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (st >= 0) tc_drain(&s.raw_full[st & 1][warp], (uint32_t)((st >> 1) & 1));
     __syncwarp();
 
-    // ------------------------------------------------------------- epilogue
     while (ok && drained < n_chunks) {
       ok = drain(drained);
       ++drained;
     }
+  }
+
+  // ---------------------------------------------------------------- epilogue
+  // Every role is done and every MMA has completed (the workers drained the
+  // last chunk).  Workers hold this CTA's partial sums in acc.
+  tc_fence_before();
+  const bool cta_ok = __syncthreads_and(ok ? 1 : 0) != 0;
+  const bool worker = warp < kTcWorkWarps;
+  const int row_l = q * 32 + lane, row = row0 + row_l;
+  auto store = [&](const float (&v)[64]) {
     pdl_wait();  // y and the residual may be the previous kernels' data
     pdl_trigger();
-    const int row = row0 + q * 32 + lane;
-    if (ok && row < rows) {
+    if (row < rows) {
 #pragma unroll
       for (int j = 0; j < 64; ++j) {
         const int t = c0 + j;
         if (t < n_valid) {
           const size_t o = (size_t)(tok0 + t) * rows + row;
-          y[o] = residual ? __fadd_rn(__ldcg(residual + o), acc[j]) : acc[j];
+          y[o] = residual ? __fadd_rn(__ldcg(residual + o), v[j]) : v[j];
         }
       }
     }
+  };
+  if (S == 1) {
+    if (worker && cta_ok) store(acc);
+  } else {
+    float* part = reinterpret_cast<float*>(&s.a[0][0][0]);  // [kTcN][kTcM], free once the MMAs are done
+    if (worker && rank > 0) {
+#pragma unroll
+      for (int j = 0; j < 64; ++j) part[(c0 + j) * kTcM + row_l] = acc[j];
+    }
+    if (threadIdx.x == 0) s.cta_ok = cta_ok ? 1 : 0;
+    cluster_sync();
+    if (worker && rank == 0) {
+      bool all_ok = cta_ok;
+      for (int r = 1; r < S; ++r) all_ok = all_ok && ld_dsmem_u32(&s.cta_ok, (uint32_t)r) != 0u;
+      if (all_ok) {
+        for (int r = 1; r < S; ++r) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) acc[j] = __fadd_rn(acc[j], ld_dsmem_f32(part + (c0 + j) * kTcM + row_l, (uint32_t)r));
+        }
+        store(acc);
+      }
+    }
+    cluster_sync();  // the other ranks keep their shared memory until rank 0 has read it
   }
 
   tc_fence_before();
@@ -487,8 +544,61 @@ __global__ void __launch_bounds__(512) pack_tokens_tc_kernel(const uint8_t* xq, 
   reinterpret_cast<uint4*>(slot + kOpBytes)[j] = lo;
 }
 
-std::once_flag g_tc_attr_once;
-cudaError_t g_tc_attr_err = cudaSuccess;
+std::mutex g_tc_mu;
+bool g_tc_attr = false;
+int g_tc_clusters[9] = {0};  // co-resident clusters of size S (0: not yet queried)
+
+// Co-resident CTAs when clusters have S CTAs each.
+cudaError_t tc_capacity(int S, size_t smem, int* out) {
+  std::lock_guard<std::mutex> lock(g_tc_mu);
+  if (!g_tc_attr) {
+    cudaError_t e = cudaFuncSetAttribute(matmul_q8_0_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    g_tc_attr = true;
+  }
+  if (g_tc_clusters[S] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = (unsigned)S;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(1, 1, (unsigned)S);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, matmul_q8_0_tc_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    g_tc_clusters[S] = n > 0 ? n : -1;
+  }
+  *out = g_tc_clusters[S] > 0 ? g_tc_clusters[S] * S : 0;
+  return cudaSuccess;
+}
+
+// K split: the S (1..8, at most one per chunk) that minimises waves x (chunks
+// per CTA + one chunk's worth of fixed cost per CTA: TMEM and barrier set-up,
+// pipeline fill), with a small charge per extra rank for the reduction.
+cudaError_t tc_split(int tiles, int n_chunks, size_t smem, int* S_out) {
+  int best = 1;
+  double best_t = 1e30;
+  for (int S = 1; S <= 8 && S <= n_chunks; ++S) {
+    int cap = 0;
+    cudaError_t e = tc_capacity(S, smem, &cap);
+    if (e != cudaSuccess) return e;
+    if (cap < S) continue;
+    const long long ctas = (long long)tiles * S;
+    const double waves = (double)((ctas + cap - 1) / cap);
+    const double t = waves * (double)((n_chunks + S - 1) / S + 1) + 0.25 * (S - 1);
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best = S;
+    }
+  }
+  *S_out = best;
+  return cudaSuccess;
+}
 
 }  // namespace
 
@@ -504,19 +614,38 @@ cudaError_t launch_matmul_q8_0_tc(const void* W, int64_t rows, int64_t cols, con
                                   const float* residual, void* scratch, cudaStream_t st) {
   if (n_tok <= 0 || rows <= 0) return cudaSuccess;
   const size_t smem = matmul_tc_smem_bytes();
-  std::call_once(g_tc_attr_once, [&] {
-    g_tc_attr_err = cudaFuncSetAttribute(matmul_q8_0_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  });
-  if (g_tc_attr_err != cudaSuccess) return g_tc_attr_err;
   const int nb = (int)(cols / 32);
   const int tiles = (n_tok + kTcN - 1) / kTcN;
+  const int row_tiles = (int)((rows + kTcM - 1) / kTcM);
+  int S = 1;
+  cudaError_t es = tc_split(row_tiles * tiles, nb / kTcChunk, smem, &S);
+  if (es != cudaSuccess) return es;
   uint8_t* pack = static_cast<uint8_t*>(scratch);
   cudaError_t e = launch_kernel(pack_tokens_tc_kernel, dim3((unsigned)nb, (unsigned)tiles), dim3(512), 0, st,
                                 static_cast<const uint8_t*>(xq), n_tok, nb, pack);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)((rows + kTcM - 1) / kTcM), (unsigned)tiles);
-  return launch_kernel(matmul_q8_0_tc_kernel, grid, dim3(kTcThreads), smem, st, static_cast<const uint8_t*>(W),
-                       (int)rows, nb, static_cast<const uint8_t*>(pack), n_tok, y, residual);
+  if (dry_run()) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int n_attr = 0;
+  attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+  attr[n_attr].val.clusterDim.x = 1;
+  attr[n_attr].val.clusterDim.y = 1;
+  attr[n_attr].val.clusterDim.z = (unsigned)S;
+  ++n_attr;
+  if (pdl()) {
+    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+    ++n_attr;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n_attr;
+  cfg.gridDim = dim3((unsigned)row_tiles, (unsigned)tiles, (unsigned)S);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  return cudaLaunchKernelEx(&cfg, matmul_q8_0_tc_kernel, static_cast<const uint8_t*>(W), (int)rows, nb,
+                            static_cast<const uint8_t*>(pack), n_tok, y, residual);
 }
 
 unsigned int read_clear_error_matmul_tc() {
