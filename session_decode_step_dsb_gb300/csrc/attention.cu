@@ -43,7 +43,10 @@ namespace {
 
 constexpr int kCh = 128;  // keys per chunk (DSB_ATTN_CHUNK)
 constexpr int kThreads = 128;
-constexpr int kRowGroup = 8;
+// Query rows handled together in the score and P.V loops: the widest row
+// group is 8, and each launch takes the narrowest power of two >= G*T, so a
+// one-row item (MHA, T = 1) issues no predicated-off work for absent rows.
+constexpr int kMaxRowGroup = 8;
 
 __device__ unsigned int g_err_attention = 0;
 
@@ -60,7 +63,7 @@ struct Cvt<__nv_bfloat16> {
   }
 };
 
-template <int D, typename T>
+template <int D, typename T, int kRowGroup>
 __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
     const float* __restrict__ q, long long q_stride, int n_q_heads, const T* kc, const T* __restrict__ vc,
     int n_kv_heads,
@@ -291,6 +294,7 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
       lsum = __fmaf_rn(wl, __ldcg(pc + 1), lsum);
     }
     const int n = min(32, nch - c0);
+#pragma unroll 4
     for (int cc = 0; cc < n; ++cc) {
       const float wc = __shfl_sync(0xffffffffu, wl, cc);
       const float* pc = base + (size_t)(c0 + cc) * (D + 2) + 2;
@@ -311,21 +315,21 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
   }
 }
 
-template <int D, typename T>
+template <int D, typename T, int kRowGroup>
 size_t partial_smem(int R) {
   constexpr int NPART = kThreads / (D / 2);
   return (size_t)kCh * D * sizeof(T) + (size_t)R * D * 4 + (size_t)R * kCh * 4 + (size_t)2 * R * 4 +
          (size_t)(NPART - 1) * kRowGroup * D * 4 + 16;
 }
 
-template <int D, typename T>
-cudaError_t launch_typed(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc,
+template <int D, typename T, int kRowGroup>
+cudaError_t launch_rg(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc,
                          int n_kv_heads, int ctx,
                          MetaView meta, int n_seq, int tps, long long max_items, int max_chunks, float* partials,
                          float* out, void* xq_out, cudaStream_t st) {
   const int R = (n_q_heads / n_kv_heads) * tps;
-  const size_t smem = partial_smem<D, T>(R);
-  auto kern = attention_partial_kernel<D, T>;
+  const size_t smem = partial_smem<D, T, kRowGroup>(R);
+  auto kern = attention_partial_kernel<D, T, kRowGroup>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const float scale = (float)(1.0 / sqrt((double)D));
@@ -356,6 +360,24 @@ cudaError_t launch_typed(const float* q, long long q_stride, int n_q_heads, cons
                          meta.seq_lens, max_chunks, n_tok, out, static_cast<uint8_t*>(xq_out));
   return launch_kernel(attention_merge_kernel<D, false>, dim3(mgrid), dim3(128), 0, st, partials, n_q_heads, tps,
                        meta.seq_lens, max_chunks, n_tok, out, static_cast<uint8_t*>(nullptr));
+}
+
+template <int D, typename T>
+cudaError_t launch_typed(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc,
+                         int n_kv_heads, int ctx, MetaView meta, int n_seq, int tps, long long max_items,
+                         int max_chunks, float* partials, float* out, void* xq_out, cudaStream_t st) {
+  const int R = (n_q_heads / n_kv_heads) * tps;
+  if (R <= 1)
+    return launch_rg<D, T, 1>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tps, max_items,
+                              max_chunks, partials, out, xq_out, st);
+  if (R <= 2)
+    return launch_rg<D, T, 2>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tps, max_items,
+                              max_chunks, partials, out, xq_out, st);
+  if (R <= 4)
+    return launch_rg<D, T, 4>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tps, max_items,
+                              max_chunks, partials, out, xq_out, st);
+  return launch_rg<D, T, kMaxRowGroup>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tps,
+                                       max_items, max_chunks, partials, out, xq_out, st);
 }
 
 }  // namespace
