@@ -488,7 +488,7 @@ dsb_status dsb_embed_q8_0(const void* table, int vocab, int hidden, const int32_
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   dsb_status st = stage(ws, words, cs, &dev);
   if (st != DSB_OK) return st;
-  cudaError_t e = dsbk::launch_embed(table, hidden, dev, n_tok, h, cs);
+  cudaError_t e = dsbk::launch_embed(table, hidden, dev, n_tok, h, nullptr, nullptr, 0, cs);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "embed_q8_0 launch");
 }
 
@@ -674,8 +674,12 @@ cudaError_t run_matmul(const dsb_q8_0_mat& w, const void* xq, int n_tok, float* 
 }
 
 // Enqueue every kernel of one step; metadata already on the device at meta_dev.
+// meta_src: NULL when the metadata already sits at meta_dev; otherwise a
+// device-readable copy (mapped pinned host memory) that the first kernel
+// copies to meta_dev (n_meta_words words) while it reads the token ids.
 dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, int tps, long long max_items,
-                        float* logits, dsb_workspace* ws, int sms, cudaStream_t st) {
+                        float* logits, dsb_workspace* ws, int sms, cudaStream_t st, const int32_t* meta_src = nullptr,
+                        size_t n_meta_words = 0) {
   const dsb_model_shape& s = m->shape;
   const dsb_kv_cache& kv0 = m->layers[0].kv;
   const int n_tok = n_seq * tps;
@@ -700,7 +704,8 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
   dsbk::rope_freqs((double)s.rope_theta, D, &freqs);
   // The first kernel follows the metadata copy; every later kernel may be
   // scheduled while its predecessor finishes (programmatic dependent launch).
-  cudaError_t e = dsbk::launch_embed(m->embed, s.hidden, tokens_dev, n_tok, h, st);
+  cudaError_t e = dsbk::launch_embed(m->embed, s.hidden, meta_src ? meta_src : tokens_dev, n_tok, h, meta_src,
+                                     const_cast<int32_t*>(meta_dev), (int)n_meta_words, st);
   dsbk::set_pdl(true);
   for (int l = 0; l < s.n_layers && e == cudaSuccess; ++l) {
     const dsb_layer& Ly = m->layers[l];
@@ -758,7 +763,8 @@ struct dsb_step_graph {
   dsb_kv_cache kv0{};
   int n_seq = 0, tps = 0;
   dsb_workspace* ws = nullptr;
-  int32_t* pinned = nullptr;
+  int32_t* pinned = nullptr;      // mapped pinned host memory, rewritten between replays
+  int32_t* pinned_dev = nullptr;  // its device address
   int32_t* dev_meta = nullptr;
   size_t n_words = 0;
   std::vector<int32_t> last;
@@ -827,7 +833,10 @@ dsb_status dsb_step_graph_create(const dsb_model* model, int n_seq, int tokens_p
   g->dev_meta = reinterpret_cast<int32_t*>(ws->dev + L.graph_meta);
   (void)stream;  // the graph is captured on a private stream and replayed on the caller's
   cudaStream_t cs = nullptr;
-  cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&g->pinned), g->n_words * sizeof(int32_t), cudaHostAllocDefault);
+  // The step's metadata is read by the first kernel straight from mapped
+  // pinned host memory (no copy node at the head of the graph).
+  cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&g->pinned), g->n_words * sizeof(int32_t), cudaHostAllocMapped);
+  if (e == cudaSuccess) e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&g->pinned_dev), g->pinned, 0);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g->done, cudaEventDisableTiming);
   // The legacy default stream cannot be captured, so capture on a private
   // non-blocking stream; work already queued elsewhere is not part of the graph.
@@ -846,7 +855,8 @@ dsb_status dsb_step_graph_create(const dsb_model* model, int n_seq, int tokens_p
       (long long)n_seq * ((kv0->ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK) * model->shape.n_kv_heads;
   // Warm every launcher's one-time set-up outside the capture.
   dsbk::set_dry_run(true);
-  dsb_status dry = enqueue_step(model, g->dev_meta, n_seq, tokens_per_seq, max_items, logits, ws, sms, cs);
+  dsb_status dry = enqueue_step(model, g->dev_meta, n_seq, tokens_per_seq, max_items, logits, ws, sms, cs,
+                                g->pinned_dev, g->n_words);
   dsbk::set_dry_run(false);
   if (dry != DSB_OK) {
     cudaStreamDestroy(cs);
@@ -857,9 +867,8 @@ dsb_status dsb_step_graph_create(const dsb_model* model, int n_seq, int tokens_p
   }
   e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
   if (e == cudaSuccess) {
-    e = cudaMemcpyAsync(g->dev_meta, g->pinned, g->n_words * sizeof(int32_t), cudaMemcpyHostToDevice, cs);
-    dsb_status es = DSB_OK;
-    if (e == cudaSuccess) es = enqueue_step(model, g->dev_meta, n_seq, tokens_per_seq, max_items, logits, ws, sms, cs);
+    const dsb_status es = enqueue_step(model, g->dev_meta, n_seq, tokens_per_seq, max_items, logits, ws, sms, cs,
+                                       g->pinned_dev, g->n_words);
     cudaError_t e2 = cudaStreamEndCapture(cs, &g->graph);
     if (e == cudaSuccess && es != DSB_OK) {
       if (g->graph) cudaGraphDestroy(g->graph);

@@ -107,8 +107,11 @@ size_t attention_partial_bytes(int n_tok, int n_q_heads, int head_dim, int ctx);
 cudaError_t launch_rmsnorm_quant(const float* x, const float* w, int n_tok, int hidden, float eps, void* xq,
                                  cudaStream_t st);
 cudaError_t launch_silu_mul_quant(const float* gu, int n_tok, int ffn, void* xq, cudaStream_t st);
-cudaError_t launch_embed(const void* table, int hidden, const int32_t* tokens_dev, int n_tok, float* h,
-                         cudaStream_t st);
+// tokens: device-readable token ids.  meta_src non-NULL: the kernel also
+// copies n_words words from meta_src (device-readable, e.g. mapped pinned
+// host memory) to meta_dst.
+cudaError_t launch_embed(const void* table, int hidden, const int32_t* tokens, int n_tok, float* h,
+                         const int32_t* meta_src, int32_t* meta_dst, int n_words, cudaStream_t st);
 
 // Scratch of dsb_attention_decode_multi_noalloc (csrc/noalloc.cu): a static
 // device array, looked up once per device.

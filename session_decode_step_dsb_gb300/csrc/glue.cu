@@ -85,11 +85,19 @@ __global__ void __launch_bounds__(kGlueThreads) silu_mul_quant_kernel(const floa
 }
 
 // h[t][:] = dequantised q8_0 row token[t] of the embedding table.  One warp per block.
+// With meta_src set (the captured step reads its per-step metadata straight
+// from mapped pinned host memory), the CTAs also copy the n_words metadata
+// words to meta_dst for the kernels that follow; tokens then points into
+// meta_src too.
 __global__ void __launch_bounds__(kGlueThreads) embed_kernel(const uint8_t* __restrict__ table, int hidden,
                                                              const int32_t* __restrict__ tokens, long long n_blocks,
-                                                             float* __restrict__ h) {
+                                                             float* __restrict__ h, const int32_t* meta_src,
+                                                             int32_t* meta_dst, int n_words) {
   pdl_wait();
   pdl_trigger();
+  if (meta_src)
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_words; i += gridDim.x * blockDim.x)
+      meta_dst[i] = meta_src[i];
   const long long blk = (long long)blockIdx.x * (kGlueThreads / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (blk >= n_blocks) return;
@@ -120,13 +128,13 @@ cudaError_t launch_silu_mul_quant(const float* gu, int n_tok, int ffn, void* xq,
                        static_cast<uint8_t*>(xq));
 }
 
-cudaError_t launch_embed(const void* table, int hidden, const int32_t* tokens_dev, int n_tok, float* h,
-                         cudaStream_t st) {
+cudaError_t launch_embed(const void* table, int hidden, const int32_t* tokens, int n_tok, float* h,
+                         const int32_t* meta_src, int32_t* meta_dst, int n_words, cudaStream_t st) {
   const long long n_blocks = (long long)n_tok * (hidden / 32);
   if (n_blocks == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((n_blocks + 7) / 8);
   return launch_kernel(embed_kernel, dim3(grid), dim3(kGlueThreads), 0, st, static_cast<const uint8_t*>(table), hidden,
-                       tokens_dev, n_blocks, h);
+                       tokens, n_blocks, h, meta_src, meta_dst, n_words);
 }
 
 }  // namespace dsbk
