@@ -222,6 +222,52 @@ dsb_status dsb_attention_decode_multi_q8_0(const float* q, int n_q_heads, const 
                                            const int32_t* seq_lens, void* xq, dsb_workspace* ws,
                                            void* stream);
 
+/* ---- paged / ring KV geometry ([PTO] paged attention with a block table,
+ * pa_max_blocks; [DS4] multi-sequence decode attention commit: each sequence
+ * carries its own cache view and ring geometry). ----------------------------
+ *
+ * The cache is a pool of pages of DSB_KV_PAGE keys, K and V each
+ * [n_pages][n_kv_heads][DSB_KV_PAGE][head_dim] in the cache dtype.  Sequence s
+ * (host arrays): block_table[s * max_blocks + i] (page indices, the first
+ * n_blocks[s] used) and window[s].  The key at absolute position p is row
+ * p % DSB_KV_PAGE of page block_table[s][i] with i = p / DSB_KV_PAGE
+ * (window[s] == 0: a linear table, which must cover the sequence) or
+ * i = (p / DSB_KV_PAGE) % n_blocks[s] (window[s] > 0: a ring holding the newest
+ * n_blocks[s] * DSB_KV_PAGE positions, at least window[s] + T - 1).  Draft
+ * token j of T sits at pos = seq_lens[s] - T + j and sees keys
+ * max(0, pos - window + 1) .. pos (all keys 0 .. pos without a window).
+ * Sequences may share pages for reading.  Violations are DSB_ERR_INVALID_ARG
+ * before any launch. */
+#define DSB_KV_PAGE 128
+
+typedef struct {
+  void* k;          /* device page pool */
+  void* v;          /* device page pool */
+  dsb_dtype dtype;
+  int32_t n_pages;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+} dsb_kv_pages;
+
+/* KV write through the paged geometry: the k and v rows of token t
+ * (sequence t / T) at pos[t] (host int32[n_seq*T], >= 0), converted to the
+ * cache dtype (round to nearest even).  Two tokens of one call writing the same
+ * page row are rejected.  k, v: device float32 [n_tok][n_kv_heads][head_dim]. */
+dsb_status dsb_kv_scatter_paged(const dsb_kv_pages* kv, const int32_t* block_table, int max_blocks,
+                                const int32_t* n_blocks, const int32_t* window, int n_seq,
+                                int tokens_per_seq, const int32_t* pos, const float* k,
+                                const float* v, dsb_workspace* ws, void* stream);
+
+/* Multi-sequence GQA decode attention through the paged geometry; q, out and
+ * the result as dsb_attention_decode_multi.  The workspace must hold the
+ * split-K partials of the longest visited key range (a workspace made for a
+ * ctx of max_blocks * DSB_KV_PAGE does). */
+dsb_status dsb_attention_decode_paged(const float* q, int n_q_heads, const dsb_kv_pages* kv,
+                                      const int32_t* block_table, int max_blocks, const int32_t* n_blocks,
+                                      const int32_t* window, int n_seq, int tokens_per_seq,
+                                      const int32_t* seq_lens, float* out, dsb_workspace* ws,
+                                      void* stream);
+
 /* ---- step glue, one fused kernel per call ([DS4] "What": RoPE/norm around
  * the attention projections and the dense stages run once for all sessions;
  * each emits the pre-quantised q8_0 activations the next matmul reads). ---- */

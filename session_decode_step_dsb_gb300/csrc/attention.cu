@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
     int n_kv_heads,
     int ctx, const int32_t* __restrict__ batch_index, const int32_t* __restrict__ seq_lens,
     const int32_t* __restrict__ chunk_off, int n_seq, int tps, int max_chunks, float scale,
-    float* __restrict__ partials) {
+    float* __restrict__ partials, const PagedView pv) {
   constexpr int NPAIR = D / 2;
   constexpr int NPART = kThreads / NPAIR;
   constexpr int KPP = kCh / NPART;
@@ -105,23 +105,34 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
     else
       hi = mid - 1;
   }
-  const int s = lo, c = w - chunk_off[s];
-  const int slot = batch_index[s], L = seq_lens[s];
+  const int s = lo, c_rel = w - chunk_off[s];  // c_rel: this sequence's chunk, counted from its first
+  const int L = seq_lens[s];
+  // Paged view: chunk c lives in one page (128 keys), found through the
+  // block table (modulo the block count for a ring); a window hides keys
+  // older than pos - W + 1, so the first chunks of a long ring are skipped.
+  const int W = pv.block_table ? pv.window[s] : 0;
+  const int c = (W > 0 ? max(0, L - tps + 1 - W) / kCh : 0) + c_rel;
   const int key0 = c * kCh;
   const int nkeys = min(kCh, L - key0);
-
-  const size_t head_row0 = ((size_t)slot * n_kv_heads + g) * (size_t)ctx;  // cache row of key 0
+  size_t chunk_row0;  // cache row of key key0 (rows of a chunk are consecutive)
+  if (pv.block_table) {
+    const int nb = pv.n_blocks[s];
+    const int page = pv.block_table[(size_t)s * pv.max_blocks + (W > 0 ? c % nb : c)];
+    chunk_row0 = ((size_t)page * n_kv_heads + g) * kCh;
+  } else {
+    chunk_row0 = ((size_t)batch_index[s] * n_kv_heads + g) * (size_t)ctx + key0;
+  }
   __syncthreads();  // the previous item is done with every shared buffer
   if (tid == 0) {
     const uint32_t bytes = (uint32_t)nkeys * D * sizeof(T);
     mbar_arrive_expect_tx(bar, bytes);
-    bulk_g2s(Vs, vc + (head_row0 + key0) * D, bytes, bar);
+    bulk_g2s(Vs, vc + chunk_row0 * D, bytes, bar);
   }
   // Thread tid owns key key0 + tid: its K row goes into registers first, so
   // that the K loads and the q staging below are in flight together.
   uint4 kreg[D / 8];
   if (tid < nkeys) {
-    const uint4* kp = reinterpret_cast<const uint4*>(kc + (head_row0 + key0 + tid) * D);
+    const uint4* kp = reinterpret_cast<const uint4*>(kc + (chunk_row0 + tid) * D);
 #pragma unroll
     for (int cc = 0; cc < D / 8; ++cc) kreg[cc] = ld_v4(kp + cc);  // this step's rows were written by the previous kernel
   } else {
@@ -166,8 +177,10 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
       for (int r = 0; r < kRowGroup; ++r) {
         if (r0 + r < R) {
           const int j = (r0 + r) / G;
-          const int vis = L - tps + j + 1;
-          ps[(size_t)(r0 + r) * kCh + tid] = (key0 + tid < vis) ? __fmul_rn(dot[r], scale) : -INFINITY;
+          const int vis = L - tps + j + 1;          // keys before vis are visible to draft token j ...
+          const int vlo = W > 0 ? vis - W : 0;      // ... from vlo on under a window
+          const int key = key0 + tid;
+          ps[(size_t)(r0 + r) * kCh + tid] = (key < vis && key >= vlo) ? __fmul_rn(dot[r], scale) : -INFINITY;
         }
       }
     }
@@ -243,7 +256,7 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
           }
           const int j = (r0 + r) / G, gi = (r0 + r) - j * G;
           const int t = s * tps + j, h = g * G + gi;
-          float* dst = partials + (((size_t)t * n_q_heads + h) * max_chunks + c) * (D + 2);
+          float* dst = partials + (((size_t)t * n_q_heads + h) * max_chunks + c_rel) * (D + 2);
           dst[2 + 2 * pr] = x0;
           dst[3 + 2 * pr] = x1;
           if (pr == 0) {
@@ -265,7 +278,7 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
 // q8_0-quantised (D / 32 blocks per head) straight into xq.
 template <int D, bool QOUT>
 __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __restrict__ partials, int n_q_heads,
-                                                              int tps, const int32_t* __restrict__ seq_lens,
+                                                              int tps, const int32_t* __restrict__ chunk_off,
                                                               int max_chunks, int n_tok, float* __restrict__ out,
                                                               uint8_t* __restrict__ xq) {
   pdl_wait();
@@ -274,9 +287,10 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
   const int lane = threadIdx.x & 31;
   if (wg >= n_tok * n_q_heads) return;
   const int t = wg / n_q_heads, h = wg - t * n_q_heads;
-  const int s = t / tps, j = t - s * tps;
-  const int vis = seq_lens[s] - tps + j + 1;
-  const int nch = (vis + kCh - 1) / kCh;
+  const int s = t / tps;
+  // every chunk of the sequence; those that hide all of this row's keys hold
+  // max = -inf and add exactly nothing
+  const int nch = chunk_off[s + 1] - chunk_off[s];
   const float* base = partials + ((size_t)t * n_q_heads + h) * max_chunks * (D + 2);
   float M = -INFINITY;
   for (int c = lane; c < nch; c += 32) M = fmaxf(M, __ldcg(base + (size_t)c * (D + 2)));
@@ -290,7 +304,8 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
     float wl = 0.0f;
     if (c0 + lane < nch) {
       const float* pc = base + (size_t)(c0 + lane) * (D + 2);
-      wl = expf(__ldcg(pc) - M);
+      const float mc = __ldcg(pc);
+      wl = (mc == -INFINITY) ? 0.0f : expf(mc - M);
       lsum = __fmaf_rn(wl, __ldcg(pc + 1), lsum);
     }
     const int n = min(32, nch - c0);
@@ -326,7 +341,7 @@ template <int D, typename T, int kRowGroup>
 cudaError_t launch_rg(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc,
                          int n_kv_heads, int ctx,
                          MetaView meta, int n_seq, int tps, long long max_items, int max_chunks, float* partials,
-                         float* out, void* xq_out, cudaStream_t st) {
+                         float* out, void* xq_out, PagedView pv, cudaStream_t st) {
   const int R = (n_q_heads / n_kv_heads) * tps;
   const size_t smem = partial_smem<D, T, kRowGroup>(R);
   auto kern = attention_partial_kernel<D, T, kRowGroup>;
@@ -351,33 +366,33 @@ cudaError_t launch_rg(const float* q, long long q_stride, int n_q_heads, const v
   const unsigned grid = (unsigned)(items < resident ? (items > 0 ? items : 1) : resident);
   e = launch_kernel(kern, dim3(grid), dim3(kThreads), smem, st, q, q_stride, n_q_heads, static_cast<const T*>(kc),
                     static_cast<const T*>(vc), n_kv_heads, ctx, meta.batch_index, meta.seq_lens, meta.chunk_off,
-                    n_seq, tps, max_chunks, scale, partials);
+                    n_seq, tps, max_chunks, scale, partials, pv);
   if (e != cudaSuccess) return e;
   const int n_tok = n_seq * tps;
   const unsigned mgrid = (unsigned)((n_tok * n_q_heads + 3) / 4);
   if (xq_out)
     return launch_kernel(attention_merge_kernel<D, true>, dim3(mgrid), dim3(128), 0, st, partials, n_q_heads, tps,
-                         meta.seq_lens, max_chunks, n_tok, out, static_cast<uint8_t*>(xq_out));
+                         meta.chunk_off, max_chunks, n_tok, out, static_cast<uint8_t*>(xq_out));
   return launch_kernel(attention_merge_kernel<D, false>, dim3(mgrid), dim3(128), 0, st, partials, n_q_heads, tps,
-                       meta.seq_lens, max_chunks, n_tok, out, static_cast<uint8_t*>(nullptr));
+                       meta.chunk_off, max_chunks, n_tok, out, static_cast<uint8_t*>(nullptr));
 }
 
 template <int D, typename T>
 cudaError_t launch_typed(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc,
                          int n_kv_heads, int ctx, MetaView meta, int n_seq, int tps, long long max_items,
-                         int max_chunks, float* partials, float* out, void* xq_out, cudaStream_t st) {
+                         int max_chunks, float* partials, float* out, void* xq_out, PagedView pv, cudaStream_t st) {
   const int R = (n_q_heads / n_kv_heads) * tps;
   if (R <= 1)
     return launch_rg<D, T, 1>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tps, max_items,
-                              max_chunks, partials, out, xq_out, st);
+                              max_chunks, partials, out, xq_out, pv, st);
   if (R <= 2)
     return launch_rg<D, T, 2>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tps, max_items,
-                              max_chunks, partials, out, xq_out, st);
+                              max_chunks, partials, out, xq_out, pv, st);
   if (R <= 4)
     return launch_rg<D, T, 4>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tps, max_items,
-                              max_chunks, partials, out, xq_out, st);
+                              max_chunks, partials, out, xq_out, pv, st);
   return launch_rg<D, T, kMaxRowGroup>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tps,
-                                       max_items, max_chunks, partials, out, xq_out, st);
+                                       max_items, max_chunks, partials, out, xq_out, pv, st);
 }
 
 }  // namespace
@@ -391,21 +406,21 @@ cudaError_t launch_attention_decode_multi(const float* q, long long q_stride, in
                                           const void* vc, int dtype,
                                           int n_kv_heads, int ctx, int head_dim, MetaView meta, int n_seq,
                                           int tokens_per_seq, long long max_items, int max_chunks, float* partials,
-                                          float* out, void* xq_out, cudaStream_t st) {
+                                          float* out, void* xq_out, cudaStream_t st, PagedView pv) {
   if (n_seq == 0) return cudaSuccess;
   if (head_dim == 128) {
     if (dtype == 0)
       return launch_typed<128, __half>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
-                                       max_items, max_chunks, partials, out, xq_out, st);
+                                       max_items, max_chunks, partials, out, xq_out, pv, st);
     return launch_typed<128, __nv_bfloat16>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
-                                            max_items, max_chunks, partials, out, xq_out, st);
+                                            max_items, max_chunks, partials, out, xq_out, pv, st);
   }
   if (head_dim == 64) {
     if (dtype == 0)
       return launch_typed<64, __half>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
-                                      max_items, max_chunks, partials, out, xq_out, st);
+                                      max_items, max_chunks, partials, out, xq_out, pv, st);
     return launch_typed<64, __nv_bfloat16>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
-                                           max_items, max_chunks, partials, out, xq_out, st);
+                                           max_items, max_chunks, partials, out, xq_out, pv, st);
   }
   return cudaErrorInvalidValue;
 }

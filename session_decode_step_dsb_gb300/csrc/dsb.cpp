@@ -432,6 +432,165 @@ static dsb_status attention_common(const float* q, int n_q_heads, const dsb_kv_c
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "attention_decode_multi launch");
 }
 
+// ---- paged / ring KV geometry ----------------------------------------------
+
+static dsb_status check_pages(const dsb_kv_pages* kv) {
+  if (!kv) return fail(DSB_ERR_INVALID_ARG, "kv is NULL");
+  if (!kv->k || !kv->v) return fail(DSB_ERR_INVALID_ARG, "kv->k / kv->v is NULL");
+  if (!aligned16(kv->k) || !aligned16(kv->v)) return fail(DSB_ERR_INVALID_ARG, "page pools not 16-byte aligned");
+  if (kv->dtype != DSB_F16 && kv->dtype != DSB_BF16) return fail(DSB_ERR_INVALID_ARG, "dtype must be DSB_F16 or DSB_BF16");
+  if (kv->n_pages < 1 || kv->n_kv_heads < 1) return fail(DSB_ERR_INVALID_ARG, "n_pages / n_kv_heads < 1");
+  if (kv->head_dim < 8 || kv->head_dim % 8 || kv->head_dim > 1024)
+    return fail(DSB_ERR_INVALID_ARG, "head_dim=%d must be a multiple of 8 in [8, 1024]", kv->head_dim);
+  return DSB_OK;
+}
+
+// Block tables, block counts, windows and lengths of one call; lens: the KV
+// lengths after the step (NULL when only positions are known).
+static dsb_status check_paged_geometry(const dsb_kv_pages* kv, const int32_t* block_table, int max_blocks,
+                                       const int32_t* n_blocks, const int32_t* window, int n_seq, int tps,
+                                       const int32_t* lens) {
+  if (n_seq < 1 || n_seq > DSB_MAX_SEQS) return fail(DSB_ERR_INVALID_ARG, "n_seq=%d out of [1, %d]", n_seq, DSB_MAX_SEQS);
+  if (tps < 1 || (long long)n_seq * tps > DSB_MAX_TOKENS)
+    return fail(DSB_ERR_INVALID_ARG, "tokens_per_seq=%d out of range", tps);
+  if (max_blocks < 1) return fail(DSB_ERR_INVALID_ARG, "max_blocks=%d < 1", max_blocks);
+  if (!block_table || !n_blocks || !window) return fail(DSB_ERR_INVALID_ARG, "block_table / n_blocks / window is NULL");
+  for (int s = 0; s < n_seq; ++s) {
+    const int nb = n_blocks[s], w = window[s];
+    if (nb < 1 || nb > max_blocks) return fail(DSB_ERR_INVALID_ARG, "n_blocks[%d]=%d out of [1, %d]", s, nb, max_blocks);
+    if (w < 0) return fail(DSB_ERR_INVALID_ARG, "window[%d]=%d < 0", s, w);
+    for (int i = 0; i < nb; ++i) {
+      const int page = block_table[(size_t)s * max_blocks + i];
+      if (page < 0 || page >= kv->n_pages)
+        return fail(DSB_ERR_INVALID_ARG, "block_table[%d][%d]=%d out of [0, %d)", s, i, page, kv->n_pages);
+    }
+    if (w > 0 && (long long)nb * DSB_KV_PAGE < (long long)w + tps - 1)
+      return fail(DSB_ERR_INVALID_ARG, "sequence %d: a ring of %d pages cannot hold window %d + T - 1", s, nb, w);
+    if (lens) {
+      if (lens[s] < tps) return fail(DSB_ERR_INVALID_ARG, "seq_lens[%d]=%d < T=%d", s, lens[s], tps);
+      if (w == 0 && ((long long)lens[s] + DSB_KV_PAGE - 1) / DSB_KV_PAGE > nb)
+        return fail(DSB_ERR_INVALID_ARG, "sequence %d: %d blocks do not cover %d keys", s, nb, lens[s]);
+    }
+  }
+  return DSB_OK;
+}
+
+// Chunks of sequence s the attention visits: from the first one a window
+// leaves visible to the last.
+static int paged_first_chunk(int len, int tps, int w) {
+  return w > 0 ? std::max(0, len - tps + 1 - w) / DSB_ATTN_CHUNK : 0;
+}
+
+dsb_status dsb_kv_scatter_paged(const dsb_kv_pages* kv, const int32_t* block_table, int max_blocks,
+                                const int32_t* n_blocks, const int32_t* window, int n_seq, int tokens_per_seq,
+                                const int32_t* pos, const float* k, const float* v, dsb_workspace* ws, void* stream) {
+  dsb_status st = check_pages(kv);
+  if (st != DSB_OK) return st;
+  st = check_paged_geometry(kv, block_table, max_blocks, n_blocks, window, n_seq, tokens_per_seq, nullptr);
+  if (st != DSB_OK) return st;
+  if (!pos || !k || !v) return fail(DSB_ERR_INVALID_ARG, "pos / k / v is NULL");
+  if (!aligned16(k) || !aligned16(v)) return fail(DSB_ERR_INVALID_ARG, "k / v not 16-byte aligned");
+  if (!ws) return fail(DSB_ERR_WORKSPACE, "workspace is NULL");
+  const int n_tok = n_seq * tokens_per_seq;
+  std::vector<long long> rows;  // (page, row) of every write: two writes of one row would race
+  rows.reserve((size_t)n_tok);
+  for (int t = 0; t < n_tok; ++t) {
+    const int s = t / tokens_per_seq, p = pos[t];
+    if (p < 0) return fail(DSB_ERR_INVALID_ARG, "pos[%d]=%d < 0", t, p);
+    int i = p / DSB_KV_PAGE;
+    if (window[s] > 0) {
+      i %= n_blocks[s];
+    } else if (i >= n_blocks[s]) {
+      return fail(DSB_ERR_INVALID_ARG, "pos[%d]=%d beyond sequence %d's %d blocks", t, p, s, n_blocks[s]);
+    }
+    rows.push_back((long long)block_table[(size_t)s * max_blocks + i] * DSB_KV_PAGE + p % DSB_KV_PAGE);
+  }
+  std::vector<long long> sorted = rows;
+  std::sort(sorted.begin(), sorted.end());
+  if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end())
+    return fail(DSB_ERR_INVALID_ARG, "two tokens of the call write the same page row");
+  std::vector<int32_t> words;
+  words.reserve((size_t)n_seq * max_blocks + 2 * (size_t)n_seq + n_tok);
+  words.insert(words.end(), block_table, block_table + (size_t)n_seq * max_blocks);
+  words.insert(words.end(), n_blocks, n_blocks + n_seq);
+  words.insert(words.end(), window, window + n_seq);
+  words.insert(words.end(), pos, pos + n_tok);
+  if (words.size() > kMetaWords) return fail(DSB_ERR_UNSUPPORTED, "block tables exceed the staging slot");
+  const int32_t* dev = nullptr;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  st = stage(ws, words, cs, &dev);
+  if (st != DSB_OK) return st;
+  dsbk::PagedView pv;
+  pv.block_table = dev;
+  pv.max_blocks = max_blocks;
+  pv.n_blocks = dev + (size_t)n_seq * max_blocks;
+  pv.window = pv.n_blocks + n_seq;
+  cudaError_t e = dsbk::launch_kv_scatter_paged(kv->k, kv->v, kv->dtype, kv->n_kv_heads, kv->head_dim, pv,
+                                                tokens_per_seq, pv.window + n_seq, n_tok, k, v,
+                                                (long long)kv->n_kv_heads * kv->head_dim, cs);
+  return e == cudaSuccess ? DSB_OK : cuda_fail(e, "kv_scatter_paged launch");
+}
+
+dsb_status dsb_attention_decode_paged(const float* q, int n_q_heads, const dsb_kv_pages* kv,
+                                      const int32_t* block_table, int max_blocks, const int32_t* n_blocks,
+                                      const int32_t* window, int n_seq, int tokens_per_seq, const int32_t* seq_lens,
+                                      float* out, dsb_workspace* ws, void* stream) {
+  dsb_status st = check_pages(kv);
+  if (st != DSB_OK) return st;
+  if (kv->head_dim != 64 && kv->head_dim != 128)
+    return fail(DSB_ERR_UNSUPPORTED, "head_dim=%d: attention serves 64 and 128", kv->head_dim);
+  if (n_q_heads < 1 || n_q_heads % kv->n_kv_heads)
+    return fail(DSB_ERR_INVALID_ARG, "n_q_heads=%d is not a positive multiple of n_kv_heads=%d", n_q_heads,
+                kv->n_kv_heads);
+  if ((long long)(n_q_heads / kv->n_kv_heads) * tokens_per_seq > 64)
+    return fail(DSB_ERR_UNSUPPORTED, "query rows per kv head (G*T) exceed 64");
+  if (!seq_lens) return fail(DSB_ERR_INVALID_ARG, "seq_lens is NULL");
+  st = check_paged_geometry(kv, block_table, max_blocks, n_blocks, window, n_seq, tokens_per_seq, seq_lens);
+  if (st != DSB_OK) return st;
+  if (!q || !out) return fail(DSB_ERR_INVALID_ARG, "q / out is NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(DSB_ERR_INVALID_ARG, "q / out not 16-byte aligned");
+  if (!ws) return fail(DSB_ERR_WORKSPACE, "workspace is NULL");
+  const int n_tok = n_seq * tokens_per_seq;
+  std::vector<int32_t> words;
+  words.reserve(3 * (size_t)n_seq + 1 + (size_t)n_seq * max_blocks + 2 * (size_t)n_seq);
+  words.insert(words.end(), (size_t)n_seq, 0);  // batch_index: unused by the paged view
+  words.insert(words.end(), seq_lens, seq_lens + n_seq);
+  long long total = 0;
+  int max_chunks = 1;
+  words.push_back(0);
+  for (int s = 0; s < n_seq; ++s) {
+    const int c0 = paged_first_chunk(seq_lens[s], tokens_per_seq, window[s]);
+    const int n = (seq_lens[s] - 1) / DSB_ATTN_CHUNK - c0 + 1;
+    max_chunks = std::max(max_chunks, n);
+    total += n;
+    words.push_back((int32_t)total);
+  }
+  if (total * kv->n_kv_heads > INT_MAX) return fail(DSB_ERR_INVALID_ARG, "too many attention chunks");
+  words.insert(words.end(), block_table, block_table + (size_t)n_seq * max_blocks);
+  words.insert(words.end(), n_blocks, n_blocks + n_seq);
+  words.insert(words.end(), window, window + n_seq);
+  if (words.size() > kMetaWords) return fail(DSB_ERR_UNSUPPORTED, "block tables exceed the staging slot");
+  const size_t need = (size_t)n_tok * n_q_heads * max_chunks * (kv->head_dim + 2) * sizeof(float);
+  if (need > partial_capacity(ws))
+    return fail(DSB_ERR_WORKSPACE, "attention needs %zu workspace bytes for partials, have %zu", need,
+                partial_capacity(ws));
+  const int32_t* dev = nullptr;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  st = stage(ws, words, cs, &dev);
+  if (st != DSB_OK) return st;
+  dsbk::MetaView mv{dev, dev + n_seq, dev + 2 * n_seq, nullptr};
+  dsbk::PagedView pv;
+  pv.block_table = dev + 3 * (size_t)n_seq + 1;
+  pv.max_blocks = max_blocks;
+  pv.n_blocks = pv.block_table + (size_t)n_seq * max_blocks;
+  pv.window = pv.n_blocks + n_seq;
+  cudaError_t e = dsbk::launch_attention_decode_multi(
+      q, (long long)n_q_heads * kv->head_dim, n_q_heads, kv->k, kv->v, kv->dtype, kv->n_kv_heads, 0, kv->head_dim,
+      mv, n_seq, tokens_per_seq, total * kv->n_kv_heads, max_chunks, reinterpret_cast<float*>(partial_base(ws)), out,
+      nullptr, cs, pv);
+  return e == cudaSuccess ? DSB_OK : cuda_fail(e, "attention_decode_paged launch");
+}
+
 dsb_status dsb_attention_decode_multi(const float* q, int n_q_heads, const dsb_kv_cache* kv,
                                       const int32_t* batch_index, int n_seq, int tokens_per_seq,
                                       const int32_t* seq_lens, float* out, dsb_workspace* ws, void* stream) {

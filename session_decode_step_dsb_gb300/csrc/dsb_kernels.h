@@ -51,6 +51,19 @@ struct MetaView {
   const int32_t* pos;          // [n_tok]
 };
 
+// Paged KV geometry per sequence (device arrays): the cache is a pool of
+// 128-key pages [n_pages][Hkv][128][D]; sequence s finds key position p in
+// page block_table[s * max_blocks + i], row p % 128, with i = p / 128
+// (window[s] == 0) or i = (p / 128) % n_blocks[s] (a ring; window[s] > 0 also
+// hides keys older than pos - window + 1).  block_table == NULL: the
+// contiguous [F][Hkv][ctx][D] cache addressed through batch_index.
+struct PagedView {
+  const int32_t* block_table = nullptr;
+  int max_blocks = 0;
+  const int32_t* n_blocks = nullptr;
+  const int32_t* window = nullptr;
+};
+
 int matmul_split(int64_t rows, int64_t cols, int num_sms);
 size_t matmul_smem_bytes(int64_t rows, int64_t cols, int n_tok, int num_sms);
 // residual (may alias y, may be NULL): y = residual + W x.
@@ -96,11 +109,18 @@ cudaError_t launch_kv_scatter(void* kc, void* vc, int dtype, int n_kv_heads, int
 // partials: float [n_tok][n_q_heads][max_chunks][head_dim + 2].  With xq_out
 // non-NULL the merge writes q8_0 rows [n_tok][n_q_heads*head_dim/32 blocks]
 // instead of float32 out.
+// With pv.block_table set, kc / vc are page pools and ctx is unused; a
+// sequence's work items are its chunks from the first one a window leaves
+// visible (meta.chunk_off counts those).
 cudaError_t launch_attention_decode_multi(const float* q, long long q_stride, int n_q_heads, const void* kc,
                                           const void* vc, int dtype,
                                           int n_kv_heads, int ctx, int head_dim, MetaView meta, int n_seq,
                                           int tokens_per_seq, long long max_items, int max_chunks, float* partials,
-                                          float* out, void* xq_out, cudaStream_t st);
+                                          float* out, void* xq_out, cudaStream_t st, PagedView pv = PagedView{});
+// KV write through the paged view: token t of sequence t / T at pos[t].
+cudaError_t launch_kv_scatter_paged(void* kp, void* vp, int dtype, int n_kv_heads, int head_dim, PagedView pv,
+                                    int tokens_per_seq, const int32_t* pos_dev, int n_tok, const float* k,
+                                    const float* v, long long kv_stride, cudaStream_t st);
 
 size_t attention_partial_bytes(int n_tok, int n_q_heads, int head_dim, int ctx);
 

@@ -118,6 +118,28 @@ __global__ void kv_scatter_kernel(T* __restrict__ kc, T* __restrict__ vc, int n_
   }
 }
 
+// Paged KV write, grid (n_tok, n_kv_heads), one thread per element of a head row.
+template <typename T>
+__global__ void kv_scatter_paged_kernel(T* __restrict__ kp, T* __restrict__ vp, int n_kv_heads, int head_dim,
+                                        const PagedView pv, int tokens_per_seq, const int32_t* __restrict__ pos,
+                                        const float* __restrict__ k, const float* __restrict__ v,
+                                        long long kv_stride) {
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x, h = blockIdx.y;
+  const int s = t / tokens_per_seq;
+  const int p = pos[t];
+  int i = p >> 7;  // 128-key pages
+  if (pv.window[s] > 0) i %= pv.n_blocks[s];
+  const int page = pv.block_table[(size_t)s * pv.max_blocks + i];
+  const size_t dst = (((size_t)page * n_kv_heads + h) * 128 + (p & 127)) * head_dim;
+  const size_t src = (size_t)t * kv_stride + (size_t)h * head_dim;
+  for (int d = threadIdx.x; d < head_dim; d += blockDim.x) {
+    kp[dst + d] = cvt_rn<T>(__ldcg(k + src + d));
+    vp[dst + d] = cvt_rn<T>(__ldcg(v + src + d));
+  }
+}
+
 // The step's fused pass, grid (n_tok, ceil((Hq + Hkv) / kRopeHeads)), one
 // thread per pair.  Head slot hs < Hq rotates query head hs in place; slot
 // Hq + g rotates kv head g of k and writes it, and kv head g of v, into the
@@ -201,6 +223,20 @@ cudaError_t launch_kv_scatter(void* kc, void* vc, int dtype, int n_kv_heads, int
   return launch_kernel(kv_scatter_kernel<__nv_bfloat16>, grid, dim3(threads), 0, st, static_cast<__nv_bfloat16*>(kc),
                        static_cast<__nv_bfloat16*>(vc), n_kv_heads, ctx, head_dim, batch_index_dev, tokens_per_seq,
                        pos_dev, k, v, kv_stride);
+}
+
+cudaError_t launch_kv_scatter_paged(void* kp, void* vp, int dtype, int n_kv_heads, int head_dim, PagedView pv,
+                                    int tokens_per_seq, const int32_t* pos_dev, int n_tok, const float* k,
+                                    const float* v, long long kv_stride, cudaStream_t st) {
+  if (n_tok == 0) return cudaSuccess;
+  const dim3 grid((unsigned)n_tok, (unsigned)n_kv_heads);
+  const int threads = head_dim < 256 ? ((head_dim + 31) / 32) * 32 : 256;
+  if (dtype == 0)
+    return launch_kernel(kv_scatter_paged_kernel<__half>, grid, dim3(threads), 0, st, static_cast<__half*>(kp),
+                         static_cast<__half*>(vp), n_kv_heads, head_dim, pv, tokens_per_seq, pos_dev, k, v, kv_stride);
+  return launch_kernel(kv_scatter_paged_kernel<__nv_bfloat16>, grid, dim3(threads), 0, st,
+                       static_cast<__nv_bfloat16*>(kp), static_cast<__nv_bfloat16*>(vp), n_kv_heads, head_dim, pv,
+                       tokens_per_seq, pos_dev, k, v, kv_stride);
 }
 
 cudaError_t launch_rope_kv_write(float* qkv, long long stride, int n_q_heads, int n_kv_heads, int head_dim,

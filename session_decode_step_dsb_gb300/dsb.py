@@ -42,6 +42,13 @@ class KVCache(ctypes.Structure):
                 ("head_dim", ctypes.c_int32)]
 
 
+class KVPages(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("dtype", ctypes.c_int), ("n_pages", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+KV_PAGE = 128
+
 _lib = None
 
 _P = ctypes.c_void_p
@@ -70,6 +77,9 @@ SIGNATURES = {
     "dsb_attention_decode_multi_noalloc": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P]),
     "dsb_attention_decode_multi_q8_0": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P, _P]),
     "dsb_rmsnorm_q8_0": (_I, [_P, _P, _I, _I, _F, _P, _P]),
+    "dsb_kv_scatter_paged": (_I, [ctypes.POINTER(KVPages), _PI32, _I, _PI32, _PI32, _I, _I, _PI32, _P, _P, _P, _P]),
+    "dsb_attention_decode_paged": (_I, [_P, _I, ctypes.POINTER(KVPages), _PI32, _I, _PI32, _PI32, _I, _I, _PI32, _P,
+                                        _P, _P]),
     "dsb_silu_mul_q8_0": (_I, [_P, _I, _I, _P, _P]),
     "dsb_embed_q8_0": (_I, [_P, _I, _I, _PI32, _I, _P, _P, _P]),
     "dsb_rope_kv_write": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _F, _P, _P]),
@@ -289,6 +299,47 @@ def attention_decode_multi_q8_0(q, kv: KVCache, batch_index, tokens_per_seq: int
     _check(lib().dsb_attention_decode_multi_q8_0(_ptr(q), hq, ctypes.byref(kv), pbi, len(bi), tokens_per_seq, psl,
                                                  _ptr(xq), ws.handle, _stream(stream)))
     return xq
+
+
+def kv_pages(k_pool, v_pool, dtype: int) -> KVPages:
+    """Describe device page pools ``[n_pages, Hkv, 128, D]``; the returned struct
+    keeps the two tensors alive for as long as it lives."""
+    n_pages, hkv, page, d = k_pool.shape
+    if page != KV_PAGE:
+        raise ValueError("pages hold 128 keys")
+    kv = KVPages(_ptr(k_pool), _ptr(v_pool), dtype, n_pages, hkv, d)
+    kv._tensors = (k_pool, v_pool)
+    return kv
+
+
+def _geometry(block_table, n_blocks, window):
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    if bt.ndim != 2:
+        raise ValueError("block_table is [n_seq, max_blocks]")
+    nb, pnb = _i32(n_blocks)
+    win, pwin = _i32(window)
+    return bt, bt.ctypes.data_as(_PI32), nb, pnb, win, pwin
+
+
+def kv_scatter_paged(kv: KVPages, block_table, n_blocks, window, tokens_per_seq: int, pos, k, v, ws: Workspace,
+                     stream=None):
+    bt, pbt, nb, pnb, win, pwin = _geometry(block_table, n_blocks, window)
+    ps, pp = _i32(pos)
+    _check(lib().dsb_kv_scatter_paged(ctypes.byref(kv), pbt, bt.shape[1], pnb, pwin, bt.shape[0], tokens_per_seq, pp,
+                                      _ptr(k), _ptr(v), ws.handle, _stream(stream)))
+
+
+def attention_decode_paged(q, kv: KVPages, block_table, n_blocks, window, tokens_per_seq: int, seq_lens,
+                           ws: Workspace, out=None, stream=None):
+    import torch
+    n_tok, hq, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    bt, pbt, nb, pnb, win, pwin = _geometry(block_table, n_blocks, window)
+    sl, psl = _i32(seq_lens)
+    _check(lib().dsb_attention_decode_paged(_ptr(q), hq, ctypes.byref(kv), pbt, bt.shape[1], pnb, pwin, bt.shape[0],
+                                            tokens_per_seq, psl, _ptr(out), ws.handle, _stream(stream)))
+    return out
 
 
 def rmsnorm_q8_0(x, w, eps: float, stream=None):
