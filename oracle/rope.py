@@ -37,3 +37,16 @@ def rope_posvec(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
     half = d // 2
     x1, x2 = x[..., :half], x[..., half:]
     return np.concatenate([x1 * c - x2 * s, x1 * s + x2 * c], axis=-1)
+
+
+def head_rmsnorm_rope(x: np.ndarray, pos: np.ndarray, theta: float, w, eps: float) -> np.ndarray:
+    """Per-head RMS norm, then the pos-vector RoPE (the ds4 page's fused head
+    norm + RoPE tail and its position-vector twin, read as: every head vector
+    of ``x[n_tok, H, D]`` is scaled by ``1 / sqrt(mean(x^2) + eps)`` and by the
+    per-dimension weight ``w[D]``, then rotated as ``rope_posvec``).  ``w``
+    None: no norm.  float64 result."""
+    x = np.asarray(x, dtype=np.float64)
+    if w is not None:
+        ms = np.mean(x * x, axis=-1, keepdims=True)
+        x = x / np.sqrt(ms + eps) * np.asarray(w, dtype=np.float64)
+    return rope_posvec(x, pos, theta)

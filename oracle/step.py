@@ -57,6 +57,8 @@ def decode_step(shape: Shape, w: dict, k_caches: list, v_caches: list, cache_dty
                 token_ids, batch_index, tokens_per_seq: int, seq_lens):
     """Returns ``(logits float64 [n_tok, vocab], new k_caches, new v_caches)``.
 
+    ``w`` may also hold per-layer float32 ``q_norm[l], k_norm[l]`` (width
+    head_dim): a per-head RMS norm of q and k before their rotation.
     ``w`` holds q8_0 byte arrays ``embed, head`` and per layer ``wqkv[l],
     wo[l], wgu[l], wdown[l]`` plus float32 norm weights ``attn_norm[l],
     ffn_norm[l], final_norm``.  Caches are uint16 bit arrays ``[F, Hkv, C, D]``.
@@ -73,8 +75,12 @@ def decode_step(shape: Shape, w: dict, k_caches: list, v_caches: list, cache_dty
         q = qkv[:, :hq * d].reshape(n_tok, hq, d)
         k = qkv[:, hq * d:(hq + hkv) * d].reshape(n_tok, hkv, d)
         v = qkv[:, (hq + hkv) * d:].reshape(n_tok, hkv, d)
-        q = rope.rope_posvec(q, pos, sh.theta)
-        k = rope.rope_posvec(k, pos, sh.theta)
+        # optional per-head q / k RMS norm before the rotation (Qwen3-style
+        # q_norm / k_norm weights of width head_dim)
+        qn = w["q_norm"][layer] if "q_norm" in w else None
+        kn = w["k_norm"][layer] if "k_norm" in w else None
+        q = rope.head_rmsnorm_rope(q, pos, sh.theta, qn, sh.eps)
+        k = rope.head_rmsnorm_rope(k, pos, sh.theta, kn, sh.eps)
         kc, vc = kv.kv_scatter(k_caches[layer], v_caches[layer], batch_index, tokens_per_seq, pos,
                                k.astype(np.float32), v.astype(np.float32), cache_dtype)
         new_k.append(kc)

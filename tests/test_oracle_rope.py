@@ -66,3 +66,32 @@ def test_each_row_uses_its_own_position():
     y = rope.rope_posvec(x, pos, 10000.0)
     for t in range(4):
         assert np.array_equal(y[t], rope.rope_posvec(x[t:t + 1], pos[t:t + 1], 10000.0)[0])
+
+
+def test_head_norm_rope_golden():
+    """Hand-derived values (tests/golden/head_norm_rope.txt) pin the order:
+    norm, then weight, then rotation."""
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "head_norm_rope.txt")
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        pos, eps, w, x, want = (p.strip() for p in line.split("|"))
+        xv = np.array([float(v) for v in x.split()])[None, None, :]
+        wv = np.array([float(v) for v in w.split()])
+        got = rope.head_rmsnorm_rope(xv, np.array([int(pos)]), 10000.0, wv, float(eps))[0, 0]
+        assert np.allclose(got, [float(v) for v in want.split()], rtol=0, atol=1e-14)
+
+
+def test_head_norm_rope_unit_weights_give_unit_mean_square():
+    """With unit weights the normed head has mean square ms / (ms + eps), and
+    the rotation keeps it."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((3, 4, 64)) * 7.0
+    eps = 1e-6
+    y = rope.head_rmsnorm_rope(x, np.array([0, 5, 90000]), 10000.0, np.ones(64), eps)
+    ms = np.mean(x * x, axis=-1)
+    assert np.allclose(np.mean(y * y, axis=-1), ms / (ms + eps), rtol=1e-12)
+    assert np.array_equal(rope.head_rmsnorm_rope(x, np.array([1, 2, 3]), 10000.0, None, eps),
+                          rope.rope_posvec(x, np.array([1, 2, 3]), 10000.0))
