@@ -174,6 +174,9 @@ def _make_model(ms, seed: int):
     w["embed"] = q8(ms.vocab, ms.hidden)
     w["head"] = q8(ms.vocab, ms.hidden)
     w["final_norm"] = torch.ones(ms.hidden, device="cuda")
+    if ms.qk_norm:
+        w["q_norm"] = [torch.ones(ms.head_dim, device="cuda") for _ in range(ms.n_layers)]
+        w["k_norm"] = [torch.ones(ms.head_dim, device="cuda") for _ in range(ms.n_layers)]
     cdt = torch.float16 if ms.cache_dtype == "f16" else torch.bfloat16
     kc, vc = [], []
     for _ in range(ms.n_layers):
@@ -480,6 +483,9 @@ def _oracle_model(ms, seed):
     w["attn_norm"] = [np.ones(ms.hidden, np.float32)] * ms.n_layers
     w["ffn_norm"] = [np.ones(ms.hidden, np.float32)] * ms.n_layers
     w["final_norm"] = np.ones(ms.hidden, np.float32)
+    if ms.qk_norm:
+        w["q_norm"] = [np.ones(ms.head_dim, np.float32)] * ms.n_layers
+        w["k_norm"] = [np.ones(ms.head_dim, np.float32)] * ms.n_layers
     dims = (ms.full_batch_size, ms.n_kv_heads, ms.ctx, ms.head_dim)
     kc = [synth.cache_bits(seed, sid(synth.STREAM_KCACHE, l), dims, ms.cache_dtype) for l in range(ms.n_layers)]
     vc = [synth.cache_bits(seed, sid(synth.STREAM_VCACHE, l), dims, ms.cache_dtype) for l in range(ms.n_layers)]

@@ -185,6 +185,17 @@ dsb_status dsb_rope_posvec(float* q, int n_q_heads, float* k, int n_kv_heads, in
                            int n_tok, const int32_t* pos, float theta, dsb_workspace* ws,
                            void* stream);
 
+/* Per-head RMS norm, then the pos-vector RoPE ([DS4] the fused head norm +
+ * RoPE tail and its position-vector twin): every head vector x of q (and of k)
+ * becomes x / sqrt(mean(x^2) + eps) * w elementwise, w = q_norm (k_norm) a
+ * device float32 [head_dim] weight, and is then rotated as dsb_rope_posvec.
+ * Either weight may be NULL: those heads are only rotated.  Sum of squares,
+ * root and division in float32 (round to nearest).  Other arguments and errors
+ * as dsb_rope_posvec; eps must be finite and >= 0. */
+dsb_status dsb_head_rmsnorm_rope(float* q, int n_q_heads, float* k, int n_kv_heads, int head_dim, int n_tok,
+                                 const int32_t* pos, float theta, const float* q_norm, const float* k_norm,
+                                 float eps, dsb_workspace* ws, void* stream);
+
 /* KV write through batch_index ([QAIC] "Objective"; [DS4] batched-decode
  * encoder commit).  For s < n_seq, j < tokens_per_seq, t = s*T + j:
  *   K[batch_index[s]][h][pos[t]][:] = cvt(k[t][h][:]),  same for V,
@@ -296,10 +307,13 @@ dsb_status dsb_embed_q8_0(const void* table, int vocab, int hidden, const int32_
  * q heads are rotated in place (as dsb_rope_posvec); k rotated and v as is are
  * written, converted to the cache dtype, at K/V[batch_index[s]][h][pos[t]]
  * (as dsb_kv_scatter).  The k and v parts of qkv are left as they were.
- * Arguments and errors as those two calls. */
+ * q_norm / k_norm (device float32 [head_dim], each may be NULL): the per-head
+ * RMS norm of dsb_head_rmsnorm_rope, with eps, before the rotation.
+ * Arguments and errors as those calls. */
 dsb_status dsb_rope_kv_write(float* qkv, int n_q_heads, const dsb_kv_cache* kv, const int32_t* batch_index,
                              int n_seq, int tokens_per_seq, const int32_t* pos, float theta,
-                             dsb_workspace* ws, void* stream);
+                             const float* q_norm, const float* k_norm, float eps, dsb_workspace* ws,
+                             void* stream);
 
 /* Decode attention for callers that cannot allocate device memory: code
  * running inside an allocator hook or memory-pool callback, processes whose
@@ -332,7 +346,8 @@ dsb_status dsb_attention_decode_multi_noalloc(const float* q, int n_q_heads, con
  * then logits = Whead q8(rmsnorm(h)).  Token row t = s*T + j of sequence s
  * sits at position seq_lens[s] - T + j.  Embedding, head and every matrix are
  * q8_0; norms are float32 weights; the step's float32 activations live in the
- * workspace. */
+ * workspace.  A layer with q_norm / k_norm weights applies the per-head RMS
+ * norm of dsb_head_rmsnorm_rope (eps = rms_eps) to q / k before the rope. */
 typedef struct {
   int32_t hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, n_layers;
   float rms_eps;    /* e.g. 1e-6 */
@@ -347,6 +362,8 @@ typedef struct {
   const float* attn_norm; /* device [hidden] */
   const float* ffn_norm;  /* device [hidden] */
   dsb_kv_cache kv;        /* this layer's retained cache */
+  const float* q_norm;    /* device [head_dim] per-head q RMS-norm weight, or NULL (no norm) */
+  const float* k_norm;    /* device [head_dim] per-head k RMS-norm weight, or NULL (no norm) */
 } dsb_layer;
 
 typedef struct {

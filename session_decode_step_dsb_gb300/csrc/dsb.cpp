@@ -322,8 +322,11 @@ dsb_status dsb_matmul_q8_0_wide(const dsb_q8_0_mat* w, const void* xq, int n_tok
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "matmul_q8_0_wide launch");
 }
 
-dsb_status dsb_rope_posvec(float* q, int n_q_heads, float* k, int n_kv_heads, int head_dim, int n_tok,
-                           const int32_t* pos, float theta, dsb_workspace* ws, void* stream) {
+dsb_status dsb_head_rmsnorm_rope(float* q, int n_q_heads, float* k, int n_kv_heads, int head_dim, int n_tok,
+                                 const int32_t* pos, float theta, const float* q_norm, const float* k_norm, float eps,
+                                 dsb_workspace* ws, void* stream) {
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(DSB_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (k_norm && !k) return fail(DSB_ERR_INVALID_ARG, "k_norm given without k");
   if (n_tok < 0 || n_tok > DSB_MAX_TOKENS) return fail(DSB_ERR_INVALID_ARG, "n_tok=%d out of [0, %d]", n_tok, DSB_MAX_TOKENS);
   if (head_dim < 2 || head_dim % 2 || head_dim > 1024)
     return fail(DSB_ERR_INVALID_ARG, "head_dim=%d must be even in [2, 1024]", head_dim);
@@ -345,8 +348,15 @@ dsb_status dsb_rope_posvec(float* q, int n_q_heads, float* k, int n_kv_heads, in
   static thread_local dsbk::RopeFreqs freqs;
   dsbk::rope_freqs((double)theta, head_dim, &freqs);
   cudaError_t e = dsbk::launch_rope_posvec(q, (long long)n_q_heads * head_dim, n_q_heads, k,
-                                           (long long)n_kv_heads * head_dim, n_kv_heads, head_dim, n_tok, dev, freqs, st);
+                                           (long long)n_kv_heads * head_dim, n_kv_heads, head_dim, n_tok, dev, freqs, st,
+                                           q_norm, k_norm, eps);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "rope_posvec launch");
+}
+
+dsb_status dsb_rope_posvec(float* q, int n_q_heads, float* k, int n_kv_heads, int head_dim, int n_tok,
+                           const int32_t* pos, float theta, dsb_workspace* ws, void* stream) {
+  return dsb_head_rmsnorm_rope(q, n_q_heads, k, n_kv_heads, head_dim, n_tok, pos, theta, nullptr, nullptr, 0.0f, ws,
+                               stream);
 }
 
 dsb_status dsb_kv_scatter(const dsb_kv_cache* kv, const int32_t* batch_index, int n_seq, int tokens_per_seq,
@@ -652,8 +662,9 @@ dsb_status dsb_embed_q8_0(const void* table, int vocab, int hidden, const int32_
 }
 
 dsb_status dsb_rope_kv_write(float* qkv, int n_q_heads, const dsb_kv_cache* kv, const int32_t* batch_index,
-                             int n_seq, int tokens_per_seq, const int32_t* pos, float theta, dsb_workspace* ws,
-                             void* stream) {
+                             int n_seq, int tokens_per_seq, const int32_t* pos, float theta, const float* q_norm,
+                             const float* k_norm, float eps, dsb_workspace* ws, void* stream) {
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(DSB_ERR_INVALID_ARG, "eps must be finite and >= 0");
   dsb_status st = check_kv(kv);
   if (st != DSB_OK) return st;
   if (n_q_heads < 1 || n_q_heads % kv->n_kv_heads)
@@ -688,7 +699,8 @@ dsb_status dsb_rope_kv_write(float* qkv, int n_q_heads, const dsb_kv_cache* kv, 
   dsbk::rope_freqs((double)theta, kv->head_dim, &freqs);
   const long long stride = (long long)(n_q_heads + 2 * kv->n_kv_heads) * kv->head_dim;
   cudaError_t e = dsbk::launch_rope_kv_write(qkv, stride, n_q_heads, kv->n_kv_heads, kv->head_dim, dev + n_seq, dev,
-                                             tokens_per_seq, n_tok, kv->k, kv->v, kv->dtype, kv->ctx, freqs, cs);
+                                             tokens_per_seq, n_tok, kv->k, kv->v, kv->dtype, kv->ctx, freqs, cs, q_norm,
+                                             k_norm, eps);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "rope_kv_write launch");
 }
 
@@ -871,7 +883,8 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
     if ((e = dsbk::launch_rmsnorm_quant(h, Ly.attn_norm, n_tok, s.hidden, s.rms_eps, xq, st)) != cudaSuccess) break;
     if ((e = run_matmul(Ly.wqkv, xq, n_tok, qkv, nullptr, sms, pack, st)) != cudaSuccess) break;
     if ((e = dsbk::launch_rope_kv_write(qkv, qkv_stride, Hq, Hkv, D, pos_dev, bi_dev, tps, n_tok, Ly.kv.k, Ly.kv.v,
-                                        Ly.kv.dtype, Ly.kv.ctx, freqs, st)) != cudaSuccess)
+                                        Ly.kv.dtype, Ly.kv.ctx, freqs, st, Ly.q_norm, Ly.k_norm, s.rms_eps)) !=
+        cudaSuccess)
       break;
     if ((e = dsbk::launch_attention_decode_multi(qkv, qkv_stride, Hq, Ly.kv.k, Ly.kv.v, Ly.kv.dtype, Hkv, Ly.kv.ctx, D,
                                                  mv, n_seq, tps, max_items, max_chunks, partials, att, xq, st)) !=

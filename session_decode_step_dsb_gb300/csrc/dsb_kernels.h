@@ -93,12 +93,16 @@ void rope_freqs(double theta, int head_dim, RopeFreqs* out);
 // q_stride / k_stride: floats between consecutive token rows.
 cudaError_t launch_rope_posvec(float* q, long long q_stride, int n_q_heads, float* k, long long k_stride,
                                int n_kv_heads, int head_dim, int n_tok, const int32_t* pos_dev,
-                               const RopeFreqs& freqs, cudaStream_t st);
+                               const RopeFreqs& freqs, cudaStream_t st, const float* q_norm = nullptr,
+                               const float* k_norm = nullptr, float eps = 0.0f);
 // Step-fused RoPE + KV write on the [q | k | v] rows of qkv (row stride `stride`).
+// q_norm / k_norm (float32 [head_dim], may be NULL): per-head RMS norm of the
+// q / k heads before the rotation, with eps.
 cudaError_t launch_rope_kv_write(float* qkv, long long stride, int n_q_heads, int n_kv_heads, int head_dim,
                                  const int32_t* pos_dev, const int32_t* batch_index_dev, int tokens_per_seq,
                                  int n_tok, void* kc, void* vc, int dtype, int ctx, const RopeFreqs& freqs,
-                                 cudaStream_t st);
+                                 cudaStream_t st, const float* q_norm = nullptr, const float* k_norm = nullptr,
+                                 float eps = 0.0f);
 cudaError_t launch_kv_scatter(void* kc, void* vc, int dtype, int n_kv_heads, int ctx, int head_dim,
                               const int32_t* batch_index_dev, int tokens_per_seq, const int32_t* pos_dev, int n_tok,
                               const float* k, const float* v, long long kv_stride, cudaStream_t st);

@@ -49,20 +49,48 @@ __device__ __forceinline__ void rope_cs(int pos, double freq, float* c, float* s
 // Heads handled per thread in one pass: every load of a pass is issued before
 // any store, so the pass costs one memory round trip instead of one per head.
 constexpr int kRopeHeads = 8;
+constexpr int kRopeMaxWarps = 16;  // head_dim <= 1024: at most 512 pair threads
+
+// Optional per-head RMS norm before the rotation: for each of the block's
+// heads, inv[u] = 1 / sqrt(mean(x^2) + eps) over the head's head_dim values
+// (pair i of head u is (x1[u], x2[u]) in thread i; threads past the last
+// pair hold zeros).  Sums go through a fixed xor tree per warp and the warps
+// in order.  Every thread of the block must call it.
+__device__ __forceinline__ void head_inv_rms(const float (&x1)[kRopeHeads], const float (&x2)[kRopeHeads],
+                                             int head_dim, float eps, float (&inv)[kRopeHeads]) {
+  __shared__ float part[kRopeHeads][kRopeMaxWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n_warps = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int u = 0; u < kRopeHeads; ++u) {
+    float ss = __fmaf_rn(x2[u], x2[u], __fmul_rn(x1[u], x1[u]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+    if (lane == 0) part[u][warp] = ss;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < kRopeHeads; ++u) {
+    float tot = 0.0f;
+    for (int w = 0; w < n_warps; ++w) tot = __fadd_rn(tot, part[u][w]);
+    inv[u] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)head_dim), eps)));
+  }
+}
 
 // grid (n_tok, ceil((Hq + Hkv) / kRopeHeads)), one thread per pair.  Head slot
 // hs < Hq is query head hs, otherwise kv head hs - Hq of k.
 __global__ void rope_posvec_kernel(float* __restrict__ q, long long q_stride, int n_q_heads, float* __restrict__ k,
                                    long long k_stride, int n_kv_heads, int head_dim, const int32_t* __restrict__ pos,
-                                   const __grid_constant__ RopeFreqs freqs) {
+                                   const __grid_constant__ RopeFreqs freqs, const float* __restrict__ q_norm,
+                                   const float* __restrict__ k_norm, float eps) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x;
   const int half = head_dim >> 1;
   const int i = threadIdx.x;
-  if (i >= half) return;
-  float c, s;
-  rope_cs(pos[t], freqs.f[i], &c, &s);
+  const bool pair = i < half;
+  float c = 1.0f, s = 0.0f;
+  if (pair) rope_cs(pos[t], freqs.f[i], &c, &s);
   const int h0 = blockIdx.y * kRopeHeads;
   float* ptr[kRopeHeads];
   float x1[kRopeHeads], x2[kRopeHeads];
@@ -74,14 +102,27 @@ __global__ void rope_posvec_kernel(float* __restrict__ q, long long q_stride, in
       ptr[u] = q + (size_t)t * q_stride + (size_t)hs * head_dim;
     else if (k && hs < n_q_heads + n_kv_heads)
       ptr[u] = k + (size_t)t * k_stride + (size_t)(hs - n_q_heads) * head_dim;
-    if (ptr[u]) {
+    x1[u] = x2[u] = 0.0f;
+    if (ptr[u] && pair) {
       x1[u] = __ldcg(ptr[u] + i);
       x2[u] = __ldcg(ptr[u] + i + half);
     }
   }
+  if (q_norm || k_norm) {
+    float inv[kRopeHeads];
+    head_inv_rms(x1, x2, head_dim, eps, inv);
+#pragma unroll
+    for (int u = 0; u < kRopeHeads; ++u) {
+      const float* w = h0 + u < n_q_heads ? q_norm : k_norm;
+      if (w && pair) {
+        x1[u] = __fmul_rn(__fmul_rn(x1[u], inv[u]), w[i]);
+        x2[u] = __fmul_rn(__fmul_rn(x2[u], inv[u]), w[i + half]);
+      }
+    }
+  }
 #pragma unroll
   for (int u = 0; u < kRopeHeads; ++u) {
-    if (ptr[u]) {
+    if (ptr[u] && pair) {
       ptr[u][i] = __fmaf_rn(x1[u], c, __fmul_rn(-x2[u], s));
       ptr[u][i + half] = __fmaf_rn(x1[u], s, __fmul_rn(x2[u], c));
     }
@@ -148,16 +189,17 @@ template <typename T>
 __global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, int n_q_heads, int n_kv_heads,
                                      int head_dim, const int32_t* __restrict__ pos,
                                      const int32_t* __restrict__ batch_index, int tokens_per_seq, T* __restrict__ kc,
-                                     T* __restrict__ vc, int ctx, const __grid_constant__ RopeFreqs freqs) {
+                                     T* __restrict__ vc, int ctx, const __grid_constant__ RopeFreqs freqs,
+                                     const float* __restrict__ q_norm, const float* __restrict__ k_norm, float eps) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x;
   const int half = head_dim >> 1;
   const int i = threadIdx.x;
-  if (i >= half) return;
+  const bool pair = i < half;
   const int p = pos[t];
-  float c, s;
-  rope_cs(p, freqs.f[i], &c, &s);
+  float c = 1.0f, s = 0.0f;
+  if (pair) rope_cs(p, freqs.f[i], &c, &s);
   float* row = qkv + (size_t)t * stride;
   const int slot = batch_index[t / tokens_per_seq];
   const int h0 = blockIdx.y * kRopeHeads;
@@ -165,7 +207,8 @@ __global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, 
 #pragma unroll
   for (int u = 0; u < kRopeHeads; ++u) {
     const int hs = h0 + u;
-    if (hs < n_q_heads + n_kv_heads) {
+    x1[u] = x2[u] = v1[u] = v2[u] = 0.0f;
+    if (hs < n_q_heads + n_kv_heads && pair) {
       const float* src = row + (size_t)hs * head_dim;  // q heads, then k heads
       x1[u] = __ldcg(src + i);
       x2[u] = __ldcg(src + i + half);
@@ -176,10 +219,22 @@ __global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, 
       }
     }
   }
+  if (q_norm || k_norm) {
+    float inv[kRopeHeads];
+    head_inv_rms(x1, x2, head_dim, eps, inv);
+#pragma unroll
+    for (int u = 0; u < kRopeHeads; ++u) {
+      const float* w = h0 + u < n_q_heads ? q_norm : k_norm;
+      if (w && pair) {
+        x1[u] = __fmul_rn(__fmul_rn(x1[u], inv[u]), w[i]);
+        x2[u] = __fmul_rn(__fmul_rn(x2[u], inv[u]), w[i + half]);
+      }
+    }
+  }
 #pragma unroll
   for (int u = 0; u < kRopeHeads; ++u) {
     const int hs = h0 + u;
-    if (hs >= n_q_heads + n_kv_heads) continue;
+    if (hs >= n_q_heads + n_kv_heads || !pair) continue;
     const float y1 = __fmaf_rn(x1[u], c, __fmul_rn(-x2[u], s));
     const float y2 = __fmaf_rn(x1[u], s, __fmul_rn(x2[u], c));
     if (hs < n_q_heads) {
@@ -201,13 +256,14 @@ __global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, 
 
 cudaError_t launch_rope_posvec(float* q, long long q_stride, int n_q_heads, float* k, long long k_stride,
                                int n_kv_heads, int head_dim, int n_tok, const int32_t* pos_dev,
-                               const RopeFreqs& freqs, cudaStream_t st) {
+                               const RopeFreqs& freqs, cudaStream_t st, const float* q_norm, const float* k_norm,
+                               float eps) {
   if (n_tok == 0) return cudaSuccess;
   const int half = head_dim / 2;
   const int threads = ((half + 31) / 32) * 32;
   const int groups = (n_q_heads + (k ? n_kv_heads : 0) + kRopeHeads - 1) / kRopeHeads;
   return launch_kernel(rope_posvec_kernel, dim3(n_tok, groups), dim3(threads), 0, st, q, q_stride, n_q_heads, k,
-                       k_stride, n_kv_heads, head_dim, pos_dev, freqs);
+                       k_stride, n_kv_heads, head_dim, pos_dev, freqs, q_norm, k_norm, eps);
 }
 
 cudaError_t launch_kv_scatter(void* kc, void* vc, int dtype, int n_kv_heads, int ctx, int head_dim,
@@ -242,17 +298,18 @@ cudaError_t launch_kv_scatter_paged(void* kp, void* vp, int dtype, int n_kv_head
 cudaError_t launch_rope_kv_write(float* qkv, long long stride, int n_q_heads, int n_kv_heads, int head_dim,
                                  const int32_t* pos_dev, const int32_t* batch_index_dev, int tokens_per_seq,
                                  int n_tok, void* kc, void* vc, int dtype, int ctx, const RopeFreqs& freqs,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, const float* q_norm, const float* k_norm, float eps) {
   if (n_tok == 0) return cudaSuccess;
   const int threads = ((head_dim / 2 + 31) / 32) * 32;
   const dim3 grid((unsigned)n_tok, (unsigned)((n_q_heads + n_kv_heads + kRopeHeads - 1) / kRopeHeads));
   if (dtype == 0)
     return launch_kernel(rope_kv_write_kernel<__half>, grid, dim3(threads), 0, st, qkv, stride, n_q_heads,
                          n_kv_heads, head_dim, pos_dev, batch_index_dev, tokens_per_seq, static_cast<__half*>(kc),
-                         static_cast<__half*>(vc), ctx, freqs);
+                         static_cast<__half*>(vc), ctx, freqs, q_norm, k_norm, eps);
   return launch_kernel(rope_kv_write_kernel<__nv_bfloat16>, grid, dim3(threads), 0, st, qkv, stride, n_q_heads,
                        n_kv_heads, head_dim, pos_dev, batch_index_dev, tokens_per_seq,
-                       static_cast<__nv_bfloat16*>(kc), static_cast<__nv_bfloat16*>(vc), ctx, freqs);
+                       static_cast<__nv_bfloat16*>(kc), static_cast<__nv_bfloat16*>(vc), ctx, freqs, q_norm, k_norm,
+                       eps);
 }
 
 void rope_freqs(double theta, int head_dim, RopeFreqs* out) {

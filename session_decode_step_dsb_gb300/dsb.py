@@ -72,6 +72,7 @@ SIGNATURES = {
     "dsb_matmul_q8_0_wide_scratch_bytes": (ctypes.c_size_t, [_I, _I64]),
     "dsb_matmul_q8_0_wide": (_I, [ctypes.POINTER(Q8Mat), _P, _I, _P, _P, ctypes.c_size_t, _P]),
     "dsb_rope_posvec": (_I, [_P, _I, _P, _I, _I, _I, _PI32, _F, _P, _P]),
+    "dsb_head_rmsnorm_rope": (_I, [_P, _I, _P, _I, _I, _I, _PI32, _F, _P, _P, _F, _P, _P]),
     "dsb_kv_scatter": (_I, [ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P, _P, _P]),
     "dsb_attention_decode_multi": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P, _P]),
     "dsb_attention_decode_multi_noalloc": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P]),
@@ -82,7 +83,7 @@ SIGNATURES = {
                                         _P, _P]),
     "dsb_silu_mul_q8_0": (_I, [_P, _I, _I, _P, _P]),
     "dsb_embed_q8_0": (_I, [_P, _I, _I, _PI32, _I, _P, _P, _P]),
-    "dsb_rope_kv_write": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _F, _P, _P]),
+    "dsb_rope_kv_write": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _F, _P, _P, _F, _P, _P]),
 }
 
 
@@ -244,6 +245,16 @@ def rope_posvec(q, k, pos, theta: float, ws: Workspace, stream=None):
     _check(lib().dsb_rope_posvec(_ptr(q), hq, _ptr(k), hkv, d, n_tok, p, float(theta), ws.handle, _stream(stream)))
 
 
+def head_rmsnorm_rope(q, k, pos, theta: float, q_norm, k_norm, eps: float, ws: Workspace, stream=None):
+    """In place: per-head RMS norm (weights ``q_norm, k_norm`` float32 ``[D]``,
+    either may be None) then RoPE on ``q[n_tok, Hq, D]`` and ``k[n_tok, Hkv, D]``."""
+    n_tok, hq, d = q.shape
+    hkv = 0 if k is None else k.shape[1]
+    arr, p = _i32(pos)
+    _check(lib().dsb_head_rmsnorm_rope(_ptr(q), hq, _ptr(k), hkv, d, n_tok, p, float(theta), _ptr(q_norm),
+                                       _ptr(k_norm), float(eps), ws.handle, _stream(stream)))
+
+
 def attention_decode_multi_noalloc(q, kv: KVCache, batch_index, tokens_per_seq: int, seq_lens, out=None,
                                    stream=None):
     """Same as :func:`attention_decode_multi` without a workspace: for callers
@@ -371,12 +382,14 @@ def embed_q8_0(table, vocab: int, hidden: int, token_ids, ws: Workspace, stream=
 
 
 def rope_kv_write(qkv, n_q_heads: int, kv: KVCache, batch_index, tokens_per_seq: int, pos, theta: float,
-                  ws: Workspace, stream=None):
-    """Fused RoPE + KV write on ``qkv[n_tok, (Hq + 2 Hkv) * D]`` (q rotated in place)."""
+                  ws: Workspace, stream=None, q_norm=None, k_norm=None, eps: float = 0.0):
+    """Fused (optional per-head RMS norm +) RoPE + KV write on
+    ``qkv[n_tok, (Hq + 2 Hkv) * D]`` (q rotated in place)."""
     bi, pbi = _i32(batch_index)
     ps, pp = _i32(pos)
     _check(lib().dsb_rope_kv_write(_ptr(qkv), n_q_heads, ctypes.byref(kv), pbi, len(bi), tokens_per_seq, pp,
-                                   float(theta), ws.handle, _stream(stream)))
+                                   float(theta), _ptr(q_norm), _ptr(k_norm), float(eps), ws.handle,
+                                   _stream(stream)))
     return qkv
 
 
@@ -389,7 +402,8 @@ class ModelShapeC(ctypes.Structure):
 
 class LayerC(ctypes.Structure):
     _fields_ = [("wqkv", Q8Mat), ("wo", Q8Mat), ("wgu", Q8Mat), ("wdown", Q8Mat), ("attn_norm", ctypes.c_void_p),
-                ("ffn_norm", ctypes.c_void_p), ("kv", KVCache)]
+                ("ffn_norm", ctypes.c_void_p), ("kv", KVCache), ("q_norm", ctypes.c_void_p),
+                ("k_norm", ctypes.c_void_p)]
 
 
 class ModelC(ctypes.Structure):
@@ -484,8 +498,10 @@ class DecodeModel:
 
     ``weights`` maps names to *device* tensors: q8_0 byte matrices ``embed,
     head`` and per-layer lists ``wqkv, wo, wgu, wdown``; float32 ``final_norm``
-    and per-layer ``attn_norm, ffn_norm``.  ``k_caches / v_caches`` are per-layer
-    device tensors ``[F, Hkv, ctx, D]`` of a 16-bit dtype.
+    and per-layer ``attn_norm, ffn_norm`` (optionally per-layer ``q_norm,
+    k_norm`` of width D: the per-head RMS norm before the rope).
+    ``k_caches / v_caches`` are per-layer device tensors ``[F, Hkv, ctx, D]``
+    of a 16-bit dtype.
     """
 
     def __init__(self, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, n_layers, weights, k_caches, v_caches,
@@ -503,6 +519,10 @@ class DecodeModel:
             layers[l].attn_norm = _ptr(weights["attn_norm"][l])
             layers[l].ffn_norm = _ptr(weights["ffn_norm"][l])
             layers[l].kv = kv_cache(k_caches[l], v_caches[l], cache_dtype)
+            if "q_norm" in weights:
+                layers[l].q_norm = _ptr(weights["q_norm"][l])
+            if "k_norm" in weights:
+                layers[l].k_norm = _ptr(weights["k_norm"][l])
         self._layers = layers
         self.c = ModelC(self.shape, _ptr(weights["embed"]), layers, _ptr(weights["final_norm"]),
                         _mat(weights["head"], vocab, hidden))

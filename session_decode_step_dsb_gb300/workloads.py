@@ -27,6 +27,7 @@ class ModelShape:
     cache_dtype: str  # "f16" or "bf16"
     eps: float = 1e-6
     theta: float = 10000.0
+    qk_norm: bool = False  # per-head RMS norm of q and k before the rope (Qwen3 layers have one)
 
     @property
     def qkv_rows(self) -> int:
@@ -41,6 +42,6 @@ LLAMA68M_SPEC = ModelShape("llama-68m-shaped-spec", 768, 12, 12, 64, 3072, 32000
 # Qwen3-14B shapes: hidden 5120, 40 q heads, 8 kv heads, head_dim 128, FFN 17408,
 # vocab 151936; bf16 cache [16, 8, 4096, 128].  The page gives no layer count
 # for the measured step; the full model has 40 layers.
-QWEN3_14B = ModelShape("qwen3-14b-shaped", 5120, 40, 8, 128, 17408, 151936, 40, 16, 4096, "bf16")
+QWEN3_14B = ModelShape("qwen3-14b-shaped", 5120, 40, 8, 128, 17408, 151936, 40, 16, 4096, "bf16", qk_norm=True)
 
 WEIGHT_STD = 0.02

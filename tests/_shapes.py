@@ -14,14 +14,19 @@ from session_decode_step_dsb_gb300 import synth
 
 from session_decode_step_dsb_gb300.workloads import LLAMA68M, ModelShape  # noqa: F401
 
-QWEN3_14B_1L = ModelShape("qwen3-14b-shaped-1-layer", 5120, 40, 8, 128, 17408, 151936, 1, 16, 4096, "bf16")
+QWEN3_14B_1L = ModelShape("qwen3-14b-shaped-1-layer", 5120, 40, 8, 128, 17408, 151936, 1, 16, 4096, "bf16",
+                          qk_norm=True)
 # One Qwen3-14B-shaped layer (GQA 40/8, head_dim 128, FFN 17408, bf16 cache
 # [16, 8, 4096, 128]) under a 4096-row head: the layer is the workload's, the
 # head is cut to keep the oracle's weight draws to seconds (the full 151936-row
 # head is a plain matmul shape, checked by the matmul tests).
-QWEN3_14B_LAYER = ModelShape("qwen3-14b-shaped-layer", 5120, 40, 8, 128, 17408, 4096, 1, 16, 4096, "bf16")
+QWEN3_14B_LAYER = ModelShape("qwen3-14b-shaped-layer", 5120, 40, 8, 128, 17408, 4096, 1, 16, 4096, "bf16",
+                             qk_norm=True)
 TINY = ModelShape("tiny", 256, 4, 2, 64, 512, 1000, 2, 4, 96, "f16")
 TINY_BF16 = ModelShape("tiny-bf16", 512, 8, 2, 128, 768, 700, 1, 5, 300, "bf16")
+# tiny shapes with the per-head q / k RMS norm before the rope
+TINY_QKN = ModelShape("tiny-qknorm", 256, 4, 2, 64, 512, 1000, 2, 4, 96, "f16", qk_norm=True)
+TINY_BF16_QKN = ModelShape("tiny-bf16-qknorm", 512, 8, 2, 128, 768, 700, 1, 5, 300, "bf16", qk_norm=True)
 
 W_STD = 0.02
 
@@ -40,6 +45,10 @@ def weight_f32(seed: int, shape: ModelShape):
     out["attn_norm"] = [np.ones(shape.hidden, np.float32) for _ in range(shape.n_layers)]
     out["ffn_norm"] = [np.ones(shape.hidden, np.float32) for _ in range(shape.n_layers)]
     out["final_norm"] = np.ones(shape.hidden, np.float32)
+    if shape.qk_norm:   # weights around 1, as trained q / k norms are
+        for name, idx in (("q_norm", 4), ("k_norm", 5)):
+            out[name] = [(1.0 + synth.normal_rows(seed, sid(synth.STREAM_W, 10 * layer + idx), 1, shape.head_dim,
+                                                  0.1)[0]).astype(np.float32) for layer in range(shape.n_layers)]
     return out
 
 

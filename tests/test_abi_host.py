@@ -139,6 +139,15 @@ def test_rope_rejects_bad_arguments(lib):
     assert lib.dsb_rope_posvec(fake, 4, None, 2, 64, 2, ppos, ctypes.c_float(10000.0), fake, None) == 1
     assert lib.dsb_rope_posvec(fake, 4, fake, 2, 64, 2, ppos, ctypes.c_float(-1.0), fake, None) == 1
     assert lib.dsb_rope_posvec(fake, 4, fake, 2, 64, 2, ppos, ctypes.c_float(10000.0), None, None) == 3
+    th, eps = ctypes.c_float(10000.0), ctypes.c_float(1e-6)
+    assert lib.dsb_head_rmsnorm_rope(fake, 4, fake, 2, 64, 2, ppos, th, fake, fake, ctypes.c_float(-1.0), fake,
+                                     None) == 1
+    assert lib.dsb_head_rmsnorm_rope(fake, 4, fake, 2, 64, 2, ppos, th, fake, fake, ctypes.c_float(float("nan")),
+                                     fake, None) == 1
+    assert "eps" in _err(lib)
+    assert lib.dsb_head_rmsnorm_rope(fake, 4, None, 0, 64, 2, ppos, th, fake, fake, eps, fake, None) == 1
+    assert "k_norm" in _err(lib)
+    assert lib.dsb_head_rmsnorm_rope(fake, 4, fake, 2, 64, 2, ppos, th, fake, None, eps, None, None) == 3
 
 
 def test_workspace_sizes(lib):

@@ -1,7 +1,7 @@
 """GPU parity of the decode step's fused glue kernels, each called on its own
 through the C ABI and fed the oracle's own float32 inputs: RMS-norm + q8_0,
-SiLU(gate) * up + q8_0, the q8_0 embedding gather, the fused RoPE + KV write,
-and the attention with q8_0 output.
+SiLU(gate) * up + q8_0, the q8_0 embedding gather, the per-head RMS norm +
+RoPE, the fused (norm +) RoPE + KV write, and the attention with q8_0 output.
 
 Quantised outputs are compared with ``assert_q8_close`` (codes within one
 step, scales within one fp16 ulp, and only at rounding boundaries); float
@@ -77,9 +77,52 @@ def test_embed_q8_0_exact(cuda_device):
     assert e.value.status == 1
 
 
-@pytest.mark.parametrize("hq,hkv,d,dtype,T", [(12, 12, 64, "f16", 1), (40, 8, 128, "bf16", 1), (12, 12, 64, "f16", 8),
-                                              (8, 2, 128, "bf16", 4)])
-def test_rope_kv_write(cuda_device, hq, hkv, d, dtype, T):
+def _head_weights(seed, d, n):
+    return [(1.0 + synth.normal_rows(seed, synth.stream_id(synth.STREAM_W, 60 + i), 1, d, 0.1)[0]).astype(np.float32)
+            for i in range(n)]
+
+
+@pytest.mark.parametrize("hq,hkv,d,norms", [(12, 12, 64, "qk"), (40, 8, 128, "qk"), (8, 2, 128, "k"), (4, 0, 256, "q"),
+                                            (5, 3, 1024, "qk"), (3, 1, 2, "qk"), (6, 2, 64, "")])
+def test_head_rmsnorm_rope(cuda_device, hq, hkv, d, norms):
+    """Per-head RMS norm then RoPE against the oracle; heads of very different
+    scales (1e-3 .. 1e3) and an all-zero head, which stays zero."""
+    dd = _dsb()
+    n_tok = 7
+    pos = np.array([0, 1, 5, 127, 2047, 4095, 100000], np.int32)
+    q = synth.normal(8, synth.stream_id(synth.STREAM_Q, 32), (n_tok, hq, d))
+    q *= np.float32(10.0) ** np.linspace(-3, 3, hq, dtype=np.float32)[None, :, None]
+    q[2, 0] = 0.0
+    k = synth.normal(8, synth.stream_id(synth.STREAM_K, 32), (n_tok, hkv, d)) * np.float32(30.0) if hkv else None
+    qw, kw = _head_weights(8, d, 2)
+    qn = qw if "q" in norms else None
+    kn = kw if "k" in norms and hkv else None
+    eps = 1e-6
+    qd = to_dev(q)
+    kd = to_dev(k) if hkv else None
+    dd.head_rmsnorm_rope(qd, kd, pos, 10000.0, None if qn is None else to_dev(qn), None if kn is None else to_dev(kn),
+                         eps, dd.Workspace(n_tok, hq, d, 16))
+    got_q = to_host(qd)
+    _assert_heads_close(got_q, orope.head_rmsnorm_rope(q, pos, 10000.0, qn, eps), "q")
+    if qn is not None:
+        assert not got_q[2, 0].any()
+    if hkv:
+        _assert_heads_close(to_host(kd), orope.head_rmsnorm_rope(k, pos, 10000.0, kn, eps), "k")
+
+
+def _assert_heads_close(got, ref, what):
+    """Every element within ROPE_RTOL of its head vector's RMS (heads here span
+    six orders of magnitude; an all-zero head must come back exactly zero)."""
+    rms = np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True))
+    err = np.abs(got.astype(np.float64) - ref)
+    assert np.all(np.isfinite(got)), what
+    assert np.all(err <= ROPE_RTOL * rms), (what, float(np.max(err / np.maximum(rms, 1e-300))))
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype,T,norm", [(12, 12, 64, "f16", 1, False), (40, 8, 128, "bf16", 1, False),
+                                                   (12, 12, 64, "f16", 8, False), (8, 2, 128, "bf16", 4, False),
+                                                   (40, 8, 128, "bf16", 2, True), (12, 12, 64, "f16", 3, True)])
+def test_rope_kv_write(cuda_device, hq, hkv, d, dtype, T, norm):
     dd = _dsb()
     F, C = 6, 4096
     bi = np.array([5, 0, 2], np.int32)
@@ -93,14 +136,18 @@ def test_rope_kv_write(cuda_device, hq, hkv, d, dtype, T):
     kd, vd = _bits_dev(kc), _bits_dev(vc)
     kv = dd.kv_cache(kd, vd, DT[dtype])
     qkv_d = to_dev(qkv)
-    dd.rope_kv_write(qkv_d, hq, kv, bi, T, pos, 10000.0, dd.Workspace(n_tok, hq, d, C))
+    qw, kw = _head_weights(6, d, 2) if norm else (None, None)
+    eps = 1e-6
+    dd.rope_kv_write(qkv_d, hq, kv, bi, T, pos, 10000.0, dd.Workspace(n_tok, hq, d, C),
+                     q_norm=None if qw is None else to_dev(qw), k_norm=None if kw is None else to_dev(kw), eps=eps)
     got = to_host(qkv_d)
     q = qkv[:, :hq * d].reshape(n_tok, hq, d)
     k = qkv[:, hq * d:(hq + hkv) * d].reshape(n_tok, hkv, d)
     v = qkv[:, (hq + hkv) * d:].reshape(n_tok, hkv, d)
-    assert_close(got[:, :hq * d].reshape(n_tok, hq, d), orope.rope_posvec(q, pos, 10000.0), ROPE_RTOL, ROPE_ATOL, "q")
+    assert_close(got[:, :hq * d].reshape(n_tok, hq, d), orope.head_rmsnorm_rope(q, pos, 10000.0, qw, eps), ROPE_RTOL,
+                 ROPE_ATOL, "q")
     assert np.array_equal(got[:, hq * d:].view(np.uint32), qkv[:, hq * d:].view(np.uint32))  # k, v untouched
-    kr = orope.rope_posvec(k, pos, 10000.0).astype(np.float32)
+    kr = orope.head_rmsnorm_rope(k, pos, 10000.0, kw, eps).astype(np.float32)
     want_k, want_v = okv.kv_scatter(kc, vc, bi, T, pos, kr, v, dtype)
     gk, gv = to_host(kd).view(np.uint16), to_host(vd).view(np.uint16)
     assert np.array_equal(gv, want_v)                       # v: one conversion of the same float32 values

@@ -61,7 +61,9 @@ def _build(ms, seed=0):
         dev[k] = d.quantize_q8_0(to_dev(wf[k]))
         orc[k] = oq.quantize_rows(wf[k])
         assert to_host(dev[k]).tobytes() == orc[k].tobytes()
-    for k in ("attn_norm", "ffn_norm"):
+    for k in ("attn_norm", "ffn_norm", "q_norm", "k_norm"):
+        if k not in wf:
+            continue
         dev[k] = [to_dev(v) for v in wf[k]]
         orc[k] = wf[k]
     dev["final_norm"], orc["final_norm"] = to_dev(wf["final_norm"]), wf["final_norm"]
@@ -90,7 +92,9 @@ def _rms_err(got, ref):
 # Speculative decode on the llama shapes: T = K + 1 in {8, 32} puts n_tok = 32
 # and 64 tokens through every matmul (beyond the narrow kernel's 16), and the
 # causal mask inside the drafts through the attention.
-CASES = [(_shapes.TINY, 3, 1), (_shapes.TINY, 2, 4), (_shapes.TINY_BF16, 5, 1), (_shapes.LLAMA68M, 4, 1),
+# The qk-norm shapes add the per-head q / k RMS norm before the rope.
+CASES = [(_shapes.TINY, 3, 1), (_shapes.TINY, 2, 4), (_shapes.TINY_BF16, 5, 1), (_shapes.TINY_QKN, 3, 1),
+         (_shapes.TINY_QKN, 2, 4), (_shapes.TINY_BF16_QKN, 4, 2), (_shapes.LLAMA68M, 4, 1),
          (_shapes.LLAMA68M, 1, 1), (_shapes.LLAMA68M, 4, 8), (_shapes.LLAMA68M, 2, 32),
          pytest.param(_shapes.QWEN3_14B_LAYER, 3, 1, marks=pytest.mark.slow),
          pytest.param(_shapes.QWEN3_14B_LAYER, 16, 1, marks=pytest.mark.slow)]
