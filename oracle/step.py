@@ -41,6 +41,7 @@ class Shape:
     n_layers: int
     eps: float = 1e-6
     theta: float = 10000.0
+    yarn: object = None   # rope.Yarn, or None for the plain RoPE
 
 
 def quant(x: np.ndarray) -> np.ndarray:
@@ -79,8 +80,8 @@ def decode_step(shape: Shape, w: dict, k_caches: list, v_caches: list, cache_dty
         # q_norm / k_norm weights of width head_dim)
         qn = w["q_norm"][layer] if "q_norm" in w else None
         kn = w["k_norm"][layer] if "k_norm" in w else None
-        q = rope.head_rmsnorm_rope(q, pos, sh.theta, qn, sh.eps)
-        k = rope.head_rmsnorm_rope(k, pos, sh.theta, kn, sh.eps)
+        q = rope.head_rmsnorm_rope(q, pos, sh.theta, qn, sh.eps, sh.yarn)
+        k = rope.head_rmsnorm_rope(k, pos, sh.theta, kn, sh.eps, sh.yarn)
         kc, vc = kv.kv_scatter(k_caches[layer], v_caches[layer], batch_index, tokens_per_seq, pos,
                                k.astype(np.float32), v.astype(np.float32), cache_dtype)
         new_k.append(kc)
