@@ -185,15 +185,36 @@ dsb_status dsb_rope_posvec(float* q, int n_q_heads, float* k, int n_kv_heads, in
                            int n_tok, const int32_t* pos, float theta, dsb_workspace* ws,
                            void* stream);
 
+/* RoPE parameters.  yarn_factor <= 1 (e.g. a zeroed struct with theta set):
+ * the plain pos-vector RoPE of dsb_rope_posvec.  yarn_factor = s > 1: the
+ * YaRN variant ([DS4] pos-vector RoPE commit, "plain and YaRN paths"; read as
+ * published by Peng et al. 2023, "YaRN: Efficient Context Window Extension of
+ * Large Language Models", sections 3.2-3.3): with L = yarn_orig_ctx and
+ * corr(b) = D ln(L / (2 pi b)) / (2 ln theta), low = max(floor(corr(beta_fast)), 0),
+ * high = min(ceil(corr(beta_slow)), D - 1), pair i's frequency
+ * f_i = theta^(-2i/D) becomes f_i (1 - ramp_i) + (f_i / s) ramp_i with
+ * ramp_i = clamp((i - low) / max(high - low, 0.001), 0, 1), and every rotated
+ * value is multiplied by 0.1 ln s + 1 (float32).  Frequencies and the
+ * correction range in float64.  Requires theta > 0 finite; with yarn:
+ * yarn_orig_ctx >= 1 and 0 < beta_slow < beta_fast (typically 32 and 1). */
+typedef struct {
+  float theta;
+  float yarn_factor;
+  int32_t yarn_orig_ctx;
+  float yarn_beta_fast;
+  float yarn_beta_slow;
+} dsb_rope;
+
 /* Per-head RMS norm, then the pos-vector RoPE ([DS4] the fused head norm +
  * RoPE tail and its position-vector twin): every head vector x of q (and of k)
  * becomes x / sqrt(mean(x^2) + eps) * w elementwise, w = q_norm (k_norm) a
- * device float32 [head_dim] weight, and is then rotated as dsb_rope_posvec.
+ * device float32 [head_dim] weight, and is then rotated as dsb_rope_posvec
+ * with the parameters in rope (host struct, read during the call).
  * Either weight may be NULL: those heads are only rotated.  Sum of squares,
  * root and division in float32 (round to nearest).  Other arguments and errors
  * as dsb_rope_posvec; eps must be finite and >= 0. */
 dsb_status dsb_head_rmsnorm_rope(float* q, int n_q_heads, float* k, int n_kv_heads, int head_dim, int n_tok,
-                                 const int32_t* pos, float theta, const float* q_norm, const float* k_norm,
+                                 const int32_t* pos, const dsb_rope* rope, const float* q_norm, const float* k_norm,
                                  float eps, dsb_workspace* ws, void* stream);
 
 /* KV write through batch_index ([QAIC] "Objective"; [DS4] batched-decode
@@ -307,11 +328,12 @@ dsb_status dsb_embed_q8_0(const void* table, int vocab, int hidden, const int32_
  * q heads are rotated in place (as dsb_rope_posvec); k rotated and v as is are
  * written, converted to the cache dtype, at K/V[batch_index[s]][h][pos[t]]
  * (as dsb_kv_scatter).  The k and v parts of qkv are left as they were.
+ * rope: the RoPE parameters (plain or YaRN) as dsb_head_rmsnorm_rope.
  * q_norm / k_norm (device float32 [head_dim], each may be NULL): the per-head
  * RMS norm of dsb_head_rmsnorm_rope, with eps, before the rotation.
  * Arguments and errors as those calls. */
 dsb_status dsb_rope_kv_write(float* qkv, int n_q_heads, const dsb_kv_cache* kv, const int32_t* batch_index,
-                             int n_seq, int tokens_per_seq, const int32_t* pos, float theta,
+                             int n_seq, int tokens_per_seq, const int32_t* pos, const dsb_rope* rope,
                              const float* q_norm, const float* k_norm, float eps, dsb_workspace* ws,
                              void* stream);
 
@@ -350,8 +372,8 @@ dsb_status dsb_attention_decode_multi_noalloc(const float* q, int n_q_heads, con
  * norm of dsb_head_rmsnorm_rope (eps = rms_eps) to q / k before the rope. */
 typedef struct {
   int32_t hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, n_layers;
-  float rms_eps;    /* e.g. 1e-6 */
-  float rope_theta; /* e.g. 10000 */
+  float rms_eps; /* e.g. 1e-6 */
+  dsb_rope rope; /* theta e.g. 10000; plain RoPE or YaRN */
 } dsb_model_shape;
 
 typedef struct {

@@ -164,6 +164,27 @@ dsb_status check_batch(const dsb_kv_cache* kv, const int32_t* batch_index, int n
   return DSB_OK;
 }
 
+dsb_status check_rope(const dsb_rope* r) {
+  if (!r) return fail(DSB_ERR_INVALID_ARG, "rope is NULL");
+  if (!(r->theta > 0.0f) || !std::isfinite(r->theta)) return fail(DSB_ERR_INVALID_ARG, "theta must be finite and > 0");
+  if (std::isnan(r->yarn_factor) || std::isinf(r->yarn_factor))
+    return fail(DSB_ERR_INVALID_ARG, "yarn_factor must be finite");
+  if (r->yarn_factor > 1.0f) {
+    if (r->yarn_orig_ctx < 1) return fail(DSB_ERR_INVALID_ARG, "yarn_orig_ctx=%d < 1", r->yarn_orig_ctx);
+    if (!(r->yarn_beta_slow > 0.0f) || !(r->yarn_beta_fast > r->yarn_beta_slow) || !std::isfinite(r->yarn_beta_fast))
+      return fail(DSB_ERR_INVALID_ARG, "yarn betas must satisfy 0 < beta_slow < beta_fast, finite");
+  }
+  return DSB_OK;
+}
+
+void fill_rope_freqs(const dsb_rope& r, int head_dim, dsbk::RopeFreqs* out) {
+  if (r.yarn_factor > 1.0f)
+    dsbk::rope_freqs((double)r.theta, head_dim, out, (double)r.yarn_factor, r.yarn_orig_ctx, (double)r.yarn_beta_fast,
+                     (double)r.yarn_beta_slow);
+  else
+    dsbk::rope_freqs((double)r.theta, head_dim, out);
+}
+
 }  // namespace
 
 extern "C" {
@@ -323,7 +344,8 @@ dsb_status dsb_matmul_q8_0_wide(const dsb_q8_0_mat* w, const void* xq, int n_tok
 }
 
 dsb_status dsb_head_rmsnorm_rope(float* q, int n_q_heads, float* k, int n_kv_heads, int head_dim, int n_tok,
-                                 const int32_t* pos, float theta, const float* q_norm, const float* k_norm, float eps,
+                                 const int32_t* pos, const dsb_rope* rope, const float* q_norm, const float* k_norm,
+                                 float eps,
                                  dsb_workspace* ws, void* stream) {
   if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(DSB_ERR_INVALID_ARG, "eps must be finite and >= 0");
   if (k_norm && !k) return fail(DSB_ERR_INVALID_ARG, "k_norm given without k");
@@ -333,7 +355,7 @@ dsb_status dsb_head_rmsnorm_rope(float* q, int n_q_heads, float* k, int n_kv_hea
   if (n_q_heads < 1) return fail(DSB_ERR_INVALID_ARG, "n_q_heads=%d < 1", n_q_heads);
   if (n_kv_heads < 0 || (n_kv_heads == 0) != (k == nullptr))
     return fail(DSB_ERR_INVALID_ARG, "k must be NULL exactly when n_kv_heads == 0");
-  if (!(theta > 0.0f) || !std::isfinite(theta)) return fail(DSB_ERR_INVALID_ARG, "theta must be finite and > 0");
+  if (check_rope(rope) != DSB_OK) return DSB_ERR_INVALID_ARG;
   if (!ws) return fail(DSB_ERR_WORKSPACE, "workspace is NULL");
   if (n_tok == 0) return DSB_OK;
   if (!q || !pos) return fail(DSB_ERR_INVALID_ARG, "q / pos is NULL");
@@ -346,7 +368,7 @@ dsb_status dsb_head_rmsnorm_rope(float* q, int n_q_heads, float* k, int n_kv_hea
   dsb_status s = stage(ws, words, st, &dev);
   if (s != DSB_OK) return s;
   static thread_local dsbk::RopeFreqs freqs;
-  dsbk::rope_freqs((double)theta, head_dim, &freqs);
+  fill_rope_freqs(*rope, head_dim, &freqs);
   cudaError_t e = dsbk::launch_rope_posvec(q, (long long)n_q_heads * head_dim, n_q_heads, k,
                                            (long long)n_kv_heads * head_dim, n_kv_heads, head_dim, n_tok, dev, freqs, st,
                                            q_norm, k_norm, eps);
@@ -355,7 +377,8 @@ dsb_status dsb_head_rmsnorm_rope(float* q, int n_q_heads, float* k, int n_kv_hea
 
 dsb_status dsb_rope_posvec(float* q, int n_q_heads, float* k, int n_kv_heads, int head_dim, int n_tok,
                            const int32_t* pos, float theta, dsb_workspace* ws, void* stream) {
-  return dsb_head_rmsnorm_rope(q, n_q_heads, k, n_kv_heads, head_dim, n_tok, pos, theta, nullptr, nullptr, 0.0f, ws,
+  const dsb_rope rope{theta, 0.0f, 0, 0.0f, 0.0f};
+  return dsb_head_rmsnorm_rope(q, n_q_heads, k, n_kv_heads, head_dim, n_tok, pos, &rope, nullptr, nullptr, 0.0f, ws,
                                stream);
 }
 
@@ -662,7 +685,8 @@ dsb_status dsb_embed_q8_0(const void* table, int vocab, int hidden, const int32_
 }
 
 dsb_status dsb_rope_kv_write(float* qkv, int n_q_heads, const dsb_kv_cache* kv, const int32_t* batch_index,
-                             int n_seq, int tokens_per_seq, const int32_t* pos, float theta, const float* q_norm,
+                             int n_seq, int tokens_per_seq, const int32_t* pos, const dsb_rope* rope,
+                             const float* q_norm,
                              const float* k_norm, float eps, dsb_workspace* ws, void* stream) {
   if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(DSB_ERR_INVALID_ARG, "eps must be finite and >= 0");
   dsb_status st = check_kv(kv);
@@ -673,7 +697,7 @@ dsb_status dsb_rope_kv_write(float* qkv, int n_q_heads, const dsb_kv_cache* kv, 
   if (kv->head_dim % 2 || kv->head_dim > 1024) return fail(DSB_ERR_INVALID_ARG, "head_dim=%d must be even, <= 1024", kv->head_dim);
   st = check_batch(kv, batch_index, n_seq, tokens_per_seq);
   if (st != DSB_OK) return st;
-  if (!(theta > 0.0f) || !std::isfinite(theta)) return fail(DSB_ERR_INVALID_ARG, "theta must be finite and > 0");
+  if (check_rope(rope) != DSB_OK) return DSB_ERR_INVALID_ARG;
   if (!qkv || !pos) return fail(DSB_ERR_INVALID_ARG, "qkv / pos is NULL");
   if (!aligned16(qkv)) return fail(DSB_ERR_INVALID_ARG, "qkv not 16-byte aligned");
   if (!ws) return fail(DSB_ERR_WORKSPACE, "workspace is NULL");
@@ -696,7 +720,7 @@ dsb_status dsb_rope_kv_write(float* qkv, int n_q_heads, const dsb_kv_cache* kv, 
   st = stage(ws, words, cs, &dev);
   if (st != DSB_OK) return st;
   static thread_local dsbk::RopeFreqs freqs;
-  dsbk::rope_freqs((double)theta, kv->head_dim, &freqs);
+  fill_rope_freqs(*rope, kv->head_dim, &freqs);
   const long long stride = (long long)(n_q_heads + 2 * kv->n_kv_heads) * kv->head_dim;
   cudaError_t e = dsbk::launch_rope_kv_write(qkv, stride, n_q_heads, kv->n_kv_heads, kv->head_dim, dev + n_seq, dev,
                                              tokens_per_seq, n_tok, kv->k, kv->v, kv->dtype, kv->ctx, freqs, cs, q_norm,
@@ -765,7 +789,7 @@ dsb_status check_model(const dsb_model* m, const dsb_kv_cache** kv0) {
     return fail(DSB_ERR_UNSUPPORTED, "hidden, ffn and n_q_heads*head_dim must be multiples of 256");
   if (s.head_dim != 64 && s.head_dim != 128) return fail(DSB_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
   if (!(s.rms_eps > 0.0f) || !std::isfinite(s.rms_eps)) return fail(DSB_ERR_INVALID_ARG, "rms_eps must be > 0");
-  if (!(s.rope_theta > 0.0f) || !std::isfinite(s.rope_theta)) return fail(DSB_ERR_INVALID_ARG, "rope_theta must be > 0");
+  if (check_rope(&s.rope) != DSB_OK) return DSB_ERR_INVALID_ARG;
   if (!m->embed || !aligned16(m->embed)) return fail(DSB_ERR_INVALID_ARG, "embed is NULL or not 16-byte aligned");
   if (!m->final_norm) return fail(DSB_ERR_INVALID_ARG, "final_norm is NULL");
   if (!m->layers) return fail(DSB_ERR_INVALID_ARG, "layers is NULL");
@@ -872,7 +896,7 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
   const int max_chunks = (kv0.ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
   const dsbk::MetaView mv{bi_dev, sl_dev, co_dev, pos_dev};
   static thread_local dsbk::RopeFreqs freqs;
-  dsbk::rope_freqs((double)s.rope_theta, D, &freqs);
+  fill_rope_freqs(s.rope, D, &freqs);
   // The first kernel follows the metadata copy; every later kernel may be
   // scheduled while its predecessor finishes (programmatic dependent launch).
   cudaError_t e = dsbk::launch_embed(m->embed, s.hidden, meta_src ? meta_src : tokens_dev, n_tok, h, meta_src,

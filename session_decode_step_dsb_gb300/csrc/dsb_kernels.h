@@ -82,13 +82,18 @@ unsigned int read_clear_error_matmul_tc();
 
 cudaError_t launch_quantize_q8_0(const float* x, int64_t n_rows, int64_t cols, void* xq, cudaStream_t st);
 
-// Float64 frequencies theta^(-2i/D) of the rotate-half pairs (a model
-// constant), passed to the RoPE kernels by value.
+// Float64 frequencies of the rotate-half pairs (a model constant) and the
+// float32 factor every rotated value is multiplied by, passed to the RoPE
+// kernels by value.  Plain RoPE: f_i = theta^(-2i/D), mscale 1.  YaRN
+// (yarn_factor s > 1, original context yarn_orig_ctx): f_i blended between
+// f_i and f_i / s by a ramp over the pair index, mscale 0.1 ln s + 1.
 constexpr int kRopeMaxPairs = 512;
 struct RopeFreqs {
   double f[kRopeMaxPairs];
+  float mscale;
 };
-void rope_freqs(double theta, int head_dim, RopeFreqs* out);
+void rope_freqs(double theta, int head_dim, RopeFreqs* out, double yarn_factor = 0.0, int yarn_orig_ctx = 0,
+                double yarn_beta_fast = 32.0, double yarn_beta_slow = 1.0);
 
 // q_stride / k_stride: floats between consecutive token rows.
 cudaError_t launch_rope_posvec(float* q, long long q_stride, int n_q_heads, float* k, long long k_stride,

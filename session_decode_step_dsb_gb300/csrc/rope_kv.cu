@@ -90,7 +90,11 @@ __global__ void rope_posvec_kernel(float* __restrict__ q, long long q_stride, in
   const int i = threadIdx.x;
   const bool pair = i < half;
   float c = 1.0f, s = 0.0f;
-  if (pair) rope_cs(pos[t], freqs.f[i], &c, &s);
+  if (pair) {
+    rope_cs(pos[t], freqs.f[i], &c, &s);
+    c = __fmul_rn(c, freqs.mscale);
+    s = __fmul_rn(s, freqs.mscale);
+  }
   const int h0 = blockIdx.y * kRopeHeads;
   float* ptr[kRopeHeads];
   float x1[kRopeHeads], x2[kRopeHeads];
@@ -199,7 +203,11 @@ __global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, 
   const bool pair = i < half;
   const int p = pos[t];
   float c = 1.0f, s = 0.0f;
-  if (pair) rope_cs(p, freqs.f[i], &c, &s);
+  if (pair) {
+    rope_cs(p, freqs.f[i], &c, &s);
+    c = __fmul_rn(c, freqs.mscale);
+    s = __fmul_rn(s, freqs.mscale);
+  }
   float* row = qkv + (size_t)t * stride;
   const int slot = batch_index[t / tokens_per_seq];
   const int h0 = blockIdx.y * kRopeHeads;
@@ -312,8 +320,38 @@ cudaError_t launch_rope_kv_write(float* qkv, long long stride, int n_q_heads, in
                        eps);
 }
 
-void rope_freqs(double theta, int head_dim, RopeFreqs* out) {
-  for (int i = 0; i < head_dim / 2 && i < kRopeMaxPairs; ++i) out->f[i] = pow(theta, -2.0 * i / head_dim);
+// YaRN (Peng et al. 2023, "YaRN: Efficient Context Window Extension of Large
+// Language Models", sections 3.2 "NTK-by-parts" and 3.3): pair i turns
+// r_i = L f_i / (2 pi) times over the original context L.  Pairs that turn at
+// least beta_fast times keep f_i, pairs that turn at most beta_slow times take
+// f_i / s, and the pair indices in between blend the two linearly; the index
+// where r = b is D ln(L / (2 pi b)) / (2 ln theta), rounded outward.  The
+// attention temperature 0.1 ln s + 1 scales q and k through the rotation.
+void rope_freqs(double theta, int head_dim, RopeFreqs* out, double yarn_factor, int yarn_orig_ctx,
+                double yarn_beta_fast, double yarn_beta_slow) {
+  const int half = head_dim / 2 < kRopeMaxPairs ? head_dim / 2 : kRopeMaxPairs;
+  const bool yarn = yarn_factor > 1.0;
+  double low = 0.0, span = 1.0;
+  if (yarn) {
+    const double log_theta2 = 2.0 * log(theta);
+    const double two_pi = 6.283185307179586;
+    const double c_fast = head_dim * log(yarn_orig_ctx / (two_pi * yarn_beta_fast)) / log_theta2;
+    const double c_slow = head_dim * log(yarn_orig_ctx / (two_pi * yarn_beta_slow)) / log_theta2;
+    low = floor(c_fast) > 0.0 ? floor(c_fast) : 0.0;
+    const double high = ceil(c_slow) < head_dim - 1 ? ceil(c_slow) : (double)(head_dim - 1);
+    span = high - low > 0.001 ? high - low : 0.001;
+  }
+  for (int i = 0; i < half; ++i) {
+    const double f = pow(theta, -2.0 * i / head_dim);
+    if (!yarn) {
+      out->f[i] = f;
+      continue;
+    }
+    double ramp = (i - low) / span;
+    ramp = ramp < 0.0 ? 0.0 : (ramp > 1.0 ? 1.0 : ramp);
+    out->f[i] = f * (1.0 - ramp) + (f / yarn_factor) * ramp;
+  }
+  out->mscale = yarn ? (float)(0.1 * log(yarn_factor) + 1.0) : 1.0f;
 }
 
 }  // namespace dsbk

@@ -9,7 +9,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from typing import Optional, Sequence
+from typing import NamedTuple, Optional, Sequence
 
 import numpy as np
 
@@ -47,6 +47,28 @@ class KVPages(ctypes.Structure):
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
 
 
+class RopeC(ctypes.Structure):
+    _fields_ = [("theta", ctypes.c_float), ("yarn_factor", ctypes.c_float), ("yarn_orig_ctx", ctypes.c_int32),
+                ("yarn_beta_fast", ctypes.c_float), ("yarn_beta_slow", ctypes.c_float)]
+
+
+class Yarn(NamedTuple):
+    """YaRN RoPE parameters: scale ``factor`` > 1 over the original context
+    ``orig_ctx``, ramp bounds ``beta_fast`` / ``beta_slow`` (rotation counts)."""
+    factor: float
+    orig_ctx: int
+    beta_fast: float = 32.0
+    beta_slow: float = 1.0
+
+
+def rope_params(theta: float, yarn=None) -> RopeC:
+    """``dsb_rope`` for the plain RoPE (``yarn`` None) or YaRN (any object with
+    ``factor, orig_ctx, beta_fast, beta_slow``)."""
+    if yarn is None:
+        return RopeC(float(theta), 0.0, 0, 0.0, 0.0)
+    return RopeC(float(theta), float(yarn.factor), int(yarn.orig_ctx), float(yarn.beta_fast), float(yarn.beta_slow))
+
+
 KV_PAGE = 128
 
 _lib = None
@@ -72,7 +94,7 @@ SIGNATURES = {
     "dsb_matmul_q8_0_wide_scratch_bytes": (ctypes.c_size_t, [_I, _I64]),
     "dsb_matmul_q8_0_wide": (_I, [ctypes.POINTER(Q8Mat), _P, _I, _P, _P, ctypes.c_size_t, _P]),
     "dsb_rope_posvec": (_I, [_P, _I, _P, _I, _I, _I, _PI32, _F, _P, _P]),
-    "dsb_head_rmsnorm_rope": (_I, [_P, _I, _P, _I, _I, _I, _PI32, _F, _P, _P, _F, _P, _P]),
+    "dsb_head_rmsnorm_rope": (_I, [_P, _I, _P, _I, _I, _I, _PI32, _P, _P, _P, _F, _P, _P]),
     "dsb_kv_scatter": (_I, [ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P, _P, _P]),
     "dsb_attention_decode_multi": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P, _P]),
     "dsb_attention_decode_multi_noalloc": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P]),
@@ -83,7 +105,7 @@ SIGNATURES = {
                                         _P, _P]),
     "dsb_silu_mul_q8_0": (_I, [_P, _I, _I, _P, _P]),
     "dsb_embed_q8_0": (_I, [_P, _I, _I, _PI32, _I, _P, _P, _P]),
-    "dsb_rope_kv_write": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _F, _P, _P, _F, _P, _P]),
+    "dsb_rope_kv_write": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P, _P, _F, _P, _P]),
 }
 
 
@@ -245,13 +267,15 @@ def rope_posvec(q, k, pos, theta: float, ws: Workspace, stream=None):
     _check(lib().dsb_rope_posvec(_ptr(q), hq, _ptr(k), hkv, d, n_tok, p, float(theta), ws.handle, _stream(stream)))
 
 
-def head_rmsnorm_rope(q, k, pos, theta: float, q_norm, k_norm, eps: float, ws: Workspace, stream=None):
+def head_rmsnorm_rope(q, k, pos, theta: float, q_norm, k_norm, eps: float, ws: Workspace, stream=None, yarn=None):
     """In place: per-head RMS norm (weights ``q_norm, k_norm`` float32 ``[D]``,
-    either may be None) then RoPE on ``q[n_tok, Hq, D]`` and ``k[n_tok, Hkv, D]``."""
+    either may be None) then RoPE (plain, or YaRN with ``yarn``) on
+    ``q[n_tok, Hq, D]`` and ``k[n_tok, Hkv, D]``."""
     n_tok, hq, d = q.shape
     hkv = 0 if k is None else k.shape[1]
     arr, p = _i32(pos)
-    _check(lib().dsb_head_rmsnorm_rope(_ptr(q), hq, _ptr(k), hkv, d, n_tok, p, float(theta), _ptr(q_norm),
+    r = rope_params(theta, yarn)
+    _check(lib().dsb_head_rmsnorm_rope(_ptr(q), hq, _ptr(k), hkv, d, n_tok, p, ctypes.byref(r), _ptr(q_norm),
                                        _ptr(k_norm), float(eps), ws.handle, _stream(stream)))
 
 
@@ -382,13 +406,14 @@ def embed_q8_0(table, vocab: int, hidden: int, token_ids, ws: Workspace, stream=
 
 
 def rope_kv_write(qkv, n_q_heads: int, kv: KVCache, batch_index, tokens_per_seq: int, pos, theta: float,
-                  ws: Workspace, stream=None, q_norm=None, k_norm=None, eps: float = 0.0):
+                  ws: Workspace, stream=None, q_norm=None, k_norm=None, eps: float = 0.0, yarn=None):
     """Fused (optional per-head RMS norm +) RoPE + KV write on
     ``qkv[n_tok, (Hq + 2 Hkv) * D]`` (q rotated in place)."""
     bi, pbi = _i32(batch_index)
     ps, pp = _i32(pos)
+    r = rope_params(theta, yarn)
     _check(lib().dsb_rope_kv_write(_ptr(qkv), n_q_heads, ctypes.byref(kv), pbi, len(bi), tokens_per_seq, pp,
-                                   float(theta), _ptr(q_norm), _ptr(k_norm), float(eps), ws.handle,
+                                   ctypes.byref(r), _ptr(q_norm), _ptr(k_norm), float(eps), ws.handle,
                                    _stream(stream)))
     return qkv
 
@@ -397,7 +422,7 @@ def rope_kv_write(qkv, n_q_heads: int, kv: KVCache, batch_index, tokens_per_seq:
 class ModelShapeC(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("ffn", ctypes.c_int32), ("vocab", ctypes.c_int32),
-                ("n_layers", ctypes.c_int32), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)]
+                ("n_layers", ctypes.c_int32), ("rms_eps", ctypes.c_float), ("rope", RopeC)]
 
 
 class LayerC(ctypes.Structure):
@@ -505,8 +530,9 @@ class DecodeModel:
     """
 
     def __init__(self, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, n_layers, weights, k_caches, v_caches,
-                 cache_dtype: int, rms_eps=1e-6, rope_theta=10000.0):
-        self.shape = ModelShapeC(hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, n_layers, rms_eps, rope_theta)
+                 cache_dtype: int, rms_eps=1e-6, rope_theta=10000.0, yarn=None):
+        self.shape = ModelShapeC(hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, n_layers, rms_eps,
+                                 rope_params(rope_theta, yarn))
         self.w = weights
         self.k_caches, self.v_caches = k_caches, v_caches
         qkv_rows = (n_q_heads + 2 * n_kv_heads) * head_dim

@@ -28,6 +28,8 @@ class ModelShape:
     eps: float = 1e-6
     theta: float = 10000.0
     qk_norm: bool = False  # per-head RMS norm of q and k before the rope (Qwen3 layers have one)
+    yarn_factor: float = 0.0  # > 1: YaRN RoPE over the original context yarn_orig_ctx
+    yarn_orig_ctx: int = 0
 
     @property
     def qkv_rows(self) -> int:

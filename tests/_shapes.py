@@ -27,6 +27,11 @@ TINY_BF16 = ModelShape("tiny-bf16", 512, 8, 2, 128, 768, 700, 1, 5, 300, "bf16")
 # tiny shapes with the per-head q / k RMS norm before the rope
 TINY_QKN = ModelShape("tiny-qknorm", 256, 4, 2, 64, 512, 1000, 2, 4, 96, "f16", qk_norm=True)
 TINY_BF16_QKN = ModelShape("tiny-bf16-qknorm", 512, 8, 2, 128, 768, 700, 1, 5, 300, "bf16", qk_norm=True)
+# tiny shapes with the YaRN RoPE (context extended 4x over an original 64 / 128)
+TINY_YARN = ModelShape("tiny-yarn", 256, 4, 2, 64, 512, 1000, 2, 4, 256, "f16", qk_norm=True, yarn_factor=4.0,
+                       yarn_orig_ctx=64)
+TINY_BF16_YARN = ModelShape("tiny-bf16-yarn", 512, 8, 2, 128, 768, 700, 1, 5, 300, "bf16", yarn_factor=4.0,
+                            yarn_orig_ctx=128)
 
 W_STD = 0.02
 

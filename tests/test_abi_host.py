@@ -139,7 +139,8 @@ def test_rope_rejects_bad_arguments(lib):
     assert lib.dsb_rope_posvec(fake, 4, None, 2, 64, 2, ppos, ctypes.c_float(10000.0), fake, None) == 1
     assert lib.dsb_rope_posvec(fake, 4, fake, 2, 64, 2, ppos, ctypes.c_float(-1.0), fake, None) == 1
     assert lib.dsb_rope_posvec(fake, 4, fake, 2, 64, 2, ppos, ctypes.c_float(10000.0), None, None) == 3
-    th, eps = ctypes.c_float(10000.0), ctypes.c_float(1e-6)
+    from session_decode_step_dsb_gb300 import dsb
+    th, eps = ctypes.byref(dsb.rope_params(10000.0)), ctypes.c_float(1e-6)
     assert lib.dsb_head_rmsnorm_rope(fake, 4, fake, 2, 64, 2, ppos, th, fake, fake, ctypes.c_float(-1.0), fake,
                                      None) == 1
     assert lib.dsb_head_rmsnorm_rope(fake, 4, fake, 2, 64, 2, ppos, th, fake, fake, ctypes.c_float(float("nan")),
@@ -148,6 +149,13 @@ def test_rope_rejects_bad_arguments(lib):
     assert lib.dsb_head_rmsnorm_rope(fake, 4, None, 0, 64, 2, ppos, th, fake, fake, eps, fake, None) == 1
     assert "k_norm" in _err(lib)
     assert lib.dsb_head_rmsnorm_rope(fake, 4, fake, 2, 64, 2, ppos, th, fake, None, eps, None, None) == 3
+    assert lib.dsb_head_rmsnorm_rope(fake, 4, fake, 2, 64, 2, ppos, None, fake, None, eps, fake, None) == 1
+    for bad in (dsb.Yarn(4.0, 0), dsb.Yarn(4.0, 4096, 1.0, 32.0), dsb.Yarn(4.0, 4096, 32.0, 0.0),
+                dsb.Yarn(float("inf"), 4096)):
+        r = ctypes.byref(dsb.rope_params(10000.0, bad))
+        assert lib.dsb_head_rmsnorm_rope(fake, 4, fake, 2, 64, 2, ppos, r, fake, None, eps, fake, None) == 1, bad
+    ok = ctypes.byref(dsb.rope_params(10000.0, dsb.Yarn(4.0, 4096)))
+    assert lib.dsb_head_rmsnorm_rope(fake, 4, fake, 2, 64, 2, ppos, ok, fake, None, eps, None, None) == 3
 
 
 def test_workspace_sizes(lib):

@@ -82,12 +82,20 @@ def _head_weights(seed, d, n):
             for i in range(n)]
 
 
-@pytest.mark.parametrize("hq,hkv,d,norms", [(12, 12, 64, "qk"), (40, 8, 128, "qk"), (8, 2, 128, "k"), (4, 0, 256, "q"),
-                                            (5, 3, 1024, "qk"), (3, 1, 2, "qk"), (6, 2, 64, "")])
-def test_head_rmsnorm_rope(cuda_device, hq, hkv, d, norms):
-    """Per-head RMS norm then RoPE against the oracle; heads of very different
-    scales (1e-3 .. 1e3) and an all-zero head, which stays zero."""
+YARNS = {"": None, "y4": (4.0, 4096), "y16": (16.0, 2048), "y8": (8.0, 32768)}
+
+
+@pytest.mark.parametrize("hq,hkv,d,norms,yarn", [(12, 12, 64, "qk", ""), (40, 8, 128, "qk", ""), (8, 2, 128, "k", ""),
+                                                 (4, 0, 256, "q", ""), (5, 3, 1024, "qk", ""), (3, 1, 2, "qk", ""),
+                                                 (6, 2, 64, "", ""), (40, 8, 128, "qk", "y4"), (8, 2, 64, "", "y16"),
+                                                 (5, 3, 1024, "q", "y8")])
+def test_head_rmsnorm_rope(cuda_device, hq, hkv, d, norms, yarn):
+    """Per-head RMS norm then RoPE (plain or YaRN) against the oracle; heads of
+    very different scales (1e-3 .. 1e3) and an all-zero head, which stays
+    zero."""
     dd = _dsb()
+    oy = orope.Yarn(*YARNS[yarn]) if YARNS[yarn] else None
+    dy = dd.Yarn(*YARNS[yarn]) if YARNS[yarn] else None
     n_tok = 7
     pos = np.array([0, 1, 5, 127, 2047, 4095, 100000], np.int32)
     q = synth.normal(8, synth.stream_id(synth.STREAM_Q, 32), (n_tok, hq, d))
@@ -101,13 +109,13 @@ def test_head_rmsnorm_rope(cuda_device, hq, hkv, d, norms):
     qd = to_dev(q)
     kd = to_dev(k) if hkv else None
     dd.head_rmsnorm_rope(qd, kd, pos, 10000.0, None if qn is None else to_dev(qn), None if kn is None else to_dev(kn),
-                         eps, dd.Workspace(n_tok, hq, d, 16))
+                         eps, dd.Workspace(n_tok, hq, d, 16), yarn=dy)
     got_q = to_host(qd)
-    _assert_heads_close(got_q, orope.head_rmsnorm_rope(q, pos, 10000.0, qn, eps), "q")
+    _assert_heads_close(got_q, orope.head_rmsnorm_rope(q, pos, 10000.0, qn, eps, oy), "q")
     if qn is not None:
         assert not got_q[2, 0].any()
     if hkv:
-        _assert_heads_close(to_host(kd), orope.head_rmsnorm_rope(k, pos, 10000.0, kn, eps), "k")
+        _assert_heads_close(to_host(kd), orope.head_rmsnorm_rope(k, pos, 10000.0, kn, eps, oy), "k")
 
 
 def _assert_heads_close(got, ref, what):
@@ -119,11 +127,18 @@ def _assert_heads_close(got, ref, what):
     assert np.all(err <= ROPE_RTOL * rms), (what, float(np.max(err / np.maximum(rms, 1e-300))))
 
 
-@pytest.mark.parametrize("hq,hkv,d,dtype,T,norm", [(12, 12, 64, "f16", 1, False), (40, 8, 128, "bf16", 1, False),
-                                                   (12, 12, 64, "f16", 8, False), (8, 2, 128, "bf16", 4, False),
-                                                   (40, 8, 128, "bf16", 2, True), (12, 12, 64, "f16", 3, True)])
-def test_rope_kv_write(cuda_device, hq, hkv, d, dtype, T, norm):
+@pytest.mark.parametrize("hq,hkv,d,dtype,T,norm,yarn", [(12, 12, 64, "f16", 1, False, ""),
+                                                        (40, 8, 128, "bf16", 1, False, ""),
+                                                        (12, 12, 64, "f16", 8, False, ""),
+                                                        (8, 2, 128, "bf16", 4, False, ""),
+                                                        (40, 8, 128, "bf16", 2, True, ""),
+                                                        (12, 12, 64, "f16", 3, True, ""),
+                                                        (40, 8, 128, "bf16", 2, True, "y4"),
+                                                        (12, 12, 64, "f16", 1, False, "y16")])
+def test_rope_kv_write(cuda_device, hq, hkv, d, dtype, T, norm, yarn):
     dd = _dsb()
+    oy = orope.Yarn(*YARNS[yarn]) if YARNS[yarn] else None
+    dy = dd.Yarn(*YARNS[yarn]) if YARNS[yarn] else None
     F, C = 6, 4096
     bi = np.array([5, 0, 2], np.int32)
     lens = np.array([C, T, 1777], np.int32)
@@ -139,15 +154,16 @@ def test_rope_kv_write(cuda_device, hq, hkv, d, dtype, T, norm):
     qw, kw = _head_weights(6, d, 2) if norm else (None, None)
     eps = 1e-6
     dd.rope_kv_write(qkv_d, hq, kv, bi, T, pos, 10000.0, dd.Workspace(n_tok, hq, d, C),
-                     q_norm=None if qw is None else to_dev(qw), k_norm=None if kw is None else to_dev(kw), eps=eps)
+                     q_norm=None if qw is None else to_dev(qw), k_norm=None if kw is None else to_dev(kw), eps=eps,
+                     yarn=dy)
     got = to_host(qkv_d)
     q = qkv[:, :hq * d].reshape(n_tok, hq, d)
     k = qkv[:, hq * d:(hq + hkv) * d].reshape(n_tok, hkv, d)
     v = qkv[:, (hq + hkv) * d:].reshape(n_tok, hkv, d)
-    assert_close(got[:, :hq * d].reshape(n_tok, hq, d), orope.head_rmsnorm_rope(q, pos, 10000.0, qw, eps), ROPE_RTOL,
-                 ROPE_ATOL, "q")
+    assert_close(got[:, :hq * d].reshape(n_tok, hq, d), orope.head_rmsnorm_rope(q, pos, 10000.0, qw, eps, oy),
+                 ROPE_RTOL, ROPE_ATOL, "q")
     assert np.array_equal(got[:, hq * d:].view(np.uint32), qkv[:, hq * d:].view(np.uint32))  # k, v untouched
-    kr = orope.head_rmsnorm_rope(k, pos, 10000.0, kw, eps).astype(np.float32)
+    kr = orope.head_rmsnorm_rope(k, pos, 10000.0, kw, eps, oy).astype(np.float32)
     want_k, want_v = okv.kv_scatter(kc, vc, bi, T, pos, kr, v, dtype)
     gk, gv = to_host(kd).view(np.uint16), to_host(vd).view(np.uint16)
     assert np.array_equal(gv, want_v)                       # v: one conversion of the same float32 values

@@ -71,14 +71,17 @@ def _build(ms, seed=0):
     vc = [_shapes.cache_bits(seed, ms, l, "v") for l in range(ms.n_layers)]
     kd = [to_dev(c.view(np.int16)) for c in kc]
     vd = [to_dev(c.view(np.int16)) for c in vc]
+    yarn = d.Yarn(ms.yarn_factor, ms.yarn_orig_ctx) if ms.yarn_factor > 1 else None
     model = d.DecodeModel(ms.hidden, ms.n_q_heads, ms.n_kv_heads, ms.head_dim, ms.ffn, ms.vocab, ms.n_layers, dev,
-                          kd, vd, DT[ms.cache_dtype], ms.eps, ms.theta)
+                          kd, vd, DT[ms.cache_dtype], ms.eps, ms.theta, yarn)
     return model, orc, kc, vc
 
 
 def _oshape(ms):
+    from oracle import rope as orope
+    yarn = orope.Yarn(ms.yarn_factor, ms.yarn_orig_ctx) if ms.yarn_factor > 1 else None
     return ostep.Shape(ms.hidden, ms.n_q_heads, ms.n_kv_heads, ms.head_dim, ms.ffn, ms.vocab, ms.n_layers, ms.eps,
-                       ms.theta)
+                       ms.theta, yarn)
 
 
 def _rel_err(got, ref):
@@ -92,9 +95,11 @@ def _rms_err(got, ref):
 # Speculative decode on the llama shapes: T = K + 1 in {8, 32} puts n_tok = 32
 # and 64 tokens through every matmul (beyond the narrow kernel's 16), and the
 # causal mask inside the drafts through the attention.
-# The qk-norm shapes add the per-head q / k RMS norm before the rope.
+# The qk-norm shapes add the per-head q / k RMS norm before the rope; the
+# yarn shapes use the YaRN RoPE with sequences past the original context.
 CASES = [(_shapes.TINY, 3, 1), (_shapes.TINY, 2, 4), (_shapes.TINY_BF16, 5, 1), (_shapes.TINY_QKN, 3, 1),
-         (_shapes.TINY_QKN, 2, 4), (_shapes.TINY_BF16_QKN, 4, 2), (_shapes.LLAMA68M, 4, 1),
+         (_shapes.TINY_QKN, 2, 4), (_shapes.TINY_BF16_QKN, 4, 2), (_shapes.TINY_YARN, 3, 2),
+         (_shapes.TINY_BF16_YARN, 4, 1), (_shapes.LLAMA68M, 4, 1),
          (_shapes.LLAMA68M, 1, 1), (_shapes.LLAMA68M, 4, 8), (_shapes.LLAMA68M, 2, 32),
          pytest.param(_shapes.QWEN3_14B_LAYER, 3, 1, marks=pytest.mark.slow),
          pytest.param(_shapes.QWEN3_14B_LAYER, 16, 1, marks=pytest.mark.slow)]
