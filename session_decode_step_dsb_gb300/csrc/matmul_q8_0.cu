@@ -20,16 +20,22 @@
 //    16-byte shared loads (the 272-byte stride is an odd number of 16-byte
 //    bank groups) and unpacks the 34-byte blocks with funnel shifts.
 //  * Activation blocks of the CTA's k-range are unpacked once, at kernel start,
-//    into an aligned layout (32 code bytes + fp32 scale per block and token),
-//    so the inner loop reads them with warp-uniform (broadcast) 16-byte loads.
+//    into a word-major layout: for each block and each of its eight 4-code
+//    words, that word of every token side by side (then the fp32 scales), so
+//    the inner loop reads four tokens' words with one warp-uniform (broadcast)
+//    16-byte load.
 //  * Block dots are __dp4a chains started from the bit pattern of 1.5 * 2^23:
 //    |isum| <= 32*127*127 < 2^22, so the int32 result read as a float is
-//    1.5*2^23 + isum exactly and one FADD converts it (no I2F).
+//    1.5*2^23 + isum exactly and one FADD converts it (no I2F).  The chains
+//    of all n_tok tokens advance word by word together, so consecutive dp4a
+//    instructions never depend on each other.
 //  * When rows alone give too few CTAs, k is split over the CTAs of a thread
 //    block cluster (<= 8) and the partial sums are added through distributed
-//    shared memory in cluster-rank order.  No atomics; every reduction order
-//    depends only on (rows, cols) and the device's SM count, never on n_tok,
-//    so column t of an n_tok = k call is bitwise equal to the n_tok = 1 call.
+//    shared memory in cluster-rank order; every CTA of the cluster sums a
+//    slice of the tile, from double-buffered sums, one cluster barrier per
+//    tile.  No atomics; every reduction order depends only on (rows, cols) and
+//    the device, never on n_tok, so column t of an n_tok = k call is bitwise
+//    equal to the n_tok = 1 call.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -114,8 +120,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr int kTile = ROWS ? kWarps * kRowsPerCta : kRowsPerCta;
   constexpr int kRed = ROWS ? 0 : kWarps * NT * 32;          // warp partials (k-split mode)
   constexpr int kSum = (ROWS ? kWarps : 1) * NT * 32;        // one CTA sum buffer
-  constexpr int kSumBufs = ROWS ? 1 : 2;  // rows mode: one buffer, a second barrier per tile
   constexpr int NTP = NT + (NT & 1);      // scale row stride: even, so token pairs load as 8 bytes
+  constexpr int NTA = (NT + 3) & ~3;      // word row stride: four tokens per 16-byte load
   extern __shared__ __align__(128) uint8_t smem[];
   const int nks = nb >> 3;
   const int S = gridDim.y;
@@ -135,12 +141,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   // the CTA sums at the same offset -- the distributed-shared-memory reads of
   // rank 0 rely on that.
   const int kr_alloc = (nks + S - 1) / S;
-  uint32_t* act_q = reinterpret_cast<uint32_t*>(smem);                              // [kr*8][NT][8]
-  float* act_s = reinterpret_cast<float*>(act_q + (size_t)kr_alloc * 8 * NT * 8);  // [kr*8][NTP]
+  uint32_t* act_q = reinterpret_cast<uint32_t*>(smem);                               // [kr*8][8][NTA]
+  float* act_s = reinterpret_cast<float*>(act_q + (size_t)kr_alloc * 8 * 8 * NTA);  // [kr*8][NTP]
   uint8_t* stages = reinterpret_cast<uint8_t*>(act_s + (size_t)kr_alloc * 8 * NTP);  // [kWarps][kNStage][kStage]
   float* red = reinterpret_cast<float*>(stages + (size_t)kWarps * kNStage * kStage);  // [kWarps][NT][32]
   float* red_sum = red + kRed;                                                        // [kSumBufs][kSum]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red_sum + kSumBufs * kSum);           // [kWarps][kNStage]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red_sum + 2 * kSum);                  // [kWarps][kNStage]
   uint8_t* my_stages = stages + (size_t)warp * kNStage * kStage;
   uint64_t* my_bars = bars + warp * kNStage;
 
@@ -173,11 +179,18 @@ __global__ void __launch_bounds__(kThreads, 2)
   pdl_wait();  // the activations (and y / residual) may be the previous kernel's results
   pdl_trigger();
 
-  // Unpack the CTA's activation blocks [ks0*8, ks1*8) x NT into aligned form
-  // (unrolled so that several blocks' loads are in flight at once).
+  // Unpack the CTA's activation blocks [ks0*8, ks1*8) x NT into the
+  // word-major form (unrolled so that several blocks' loads are in flight at
+  // once); the pad tokens NT..NTA-1 hold zero words.
 #pragma unroll 4
-  for (int idx = threadIdx.x; idx < kr * 8 * NT; idx += kThreads) {
-    const int b = idx / NT, t = idx - b * NT;
+  for (int idx = threadIdx.x; idx < kr * 8 * NTA; idx += kThreads) {
+    const int b = idx / NTA, t = idx - b * NTA;
+    uint32_t* dq = act_q + (size_t)b * 8 * NTA + t;
+    if (t >= NT) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) dq[k * NTA] = 0u;
+      continue;
+    }
     const long long g = (long long)t * nb + (long long)ksr.ks0 * 8 + b;  // global block index
     const uint32_t* src = reinterpret_cast<const uint32_t*>(xq + ((34 * g) & ~3LL));
     uint32_t wv[9];
@@ -185,9 +198,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int k = 0; k < 9; ++k) wv[k] = ld_u32(src + k);  // written by the previous kernel
     const bool odd = (g & 1) != 0;  // odd blocks start 2 bytes into a word
     const uint32_t sh = odd ? 32u : 16u;
-    uint32_t* dq = act_q + ((size_t)b * NT + t) * 8;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) dq[k] = __funnelshift_rc(wv[k], wv[k + 1], sh);
+    for (int k = 0; k < 8; ++k) dq[k * NTA] = __funnelshift_rc(wv[k], wv[k + 1], sh);
     act_s[(size_t)b * NTP + t] = half_bits_to_float(odd ? (wv[0] >> 16) : wv[0]);
   }
   __syncthreads();
@@ -238,48 +250,39 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int k = 0; k < 8; ++k) q[k] = w[base + 1 + k];
           dw = half_bits_to_float(w[base] >> 16);
         }
-        const uint32_t* aq = act_q + ((size_t)(kl * 8 + b) * NT) * 8;
+        const uint32_t* aq = act_q + (size_t)(kl * 8 + b) * 8 * NTA;
         const float* as = act_s + (size_t)(kl * 8 + b) * NTP;  // 8-byte aligned row
-        const unsigned long long dw2 = dup_pair(dw);
+        // the NT block dots advance word by word together
+        int sd[NTA];
 #pragma unroll
-        for (int t = 0; t < NT; t += 2) {
-          // two tokens' dp4a chains interleaved
-          const uint4 a0 = *reinterpret_cast<const uint4*>(aq + t * 8);
-          const uint4 a1 = *reinterpret_cast<const uint4*>(aq + t * 8 + 4);
-          uint4 b0 = make_uint4(0, 0, 0, 0), b1 = make_uint4(0, 0, 0, 0);
-          if (t + 1 < NT) {
-            b0 = *reinterpret_cast<const uint4*>(aq + (t + 1) * 8);
-            b1 = *reinterpret_cast<const uint4*>(aq + (t + 1) * 8 + 4);
+        for (int t = 0; t < NTA; ++t) sd[t] = (int)kMagic;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+#pragma unroll
+          for (int t4 = 0; t4 < NTA; t4 += 4) {
+            const uint4 a = *reinterpret_cast<const uint4*>(aq + k * NTA + t4);
+            sd[t4 + 0] = __dp4a((int)q[k], (int)a.x, sd[t4 + 0]);
+            if (t4 + 1 < NT) sd[t4 + 1] = __dp4a((int)q[k], (int)a.y, sd[t4 + 1]);
+            if (t4 + 2 < NT) sd[t4 + 2] = __dp4a((int)q[k], (int)a.z, sd[t4 + 2]);
+            if (t4 + 3 < NT) sd[t4 + 3] = __dp4a((int)q[k], (int)a.w, sd[t4 + 3]);
           }
-          int sa = (int)kMagic, sb = (int)kMagic;
-          sa = __dp4a((int)q[0], (int)a0.x, sa);
-          sb = __dp4a((int)q[0], (int)b0.x, sb);
-          sa = __dp4a((int)q[1], (int)a0.y, sa);
-          sb = __dp4a((int)q[1], (int)b0.y, sb);
-          sa = __dp4a((int)q[2], (int)a0.z, sa);
-          sb = __dp4a((int)q[2], (int)b0.z, sb);
-          sa = __dp4a((int)q[3], (int)a0.w, sa);
-          sb = __dp4a((int)q[3], (int)b0.w, sb);
-          sa = __dp4a((int)q[4], (int)a1.x, sa);
-          sb = __dp4a((int)q[4], (int)b1.x, sb);
-          sa = __dp4a((int)q[5], (int)a1.y, sa);
-          sb = __dp4a((int)q[5], (int)b1.y, sb);
-          sa = __dp4a((int)q[6], (int)a1.z, sa);
-          sb = __dp4a((int)q[6], (int)b1.z, sb);
-          sa = __dp4a((int)q[7], (int)a1.w, sa);
-          sb = __dp4a((int)q[7], (int)b1.w, sb);
-          if constexpr (EMIT) {
-            if (row < rows) {
-              isum_out[((size_t)t * rows + row) * nb + (size_t)ks * 8 + b] = sa - (int)kMagic;
-              if (t + 1 < NT) isum_out[((size_t)(t + 1) * rows + row) * nb + (size_t)ks * 8 + b] = sb - (int)kMagic;
-            }
-          } else {
+        }
+        if constexpr (EMIT) {
+          if (row < rows) {
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+              isum_out[((size_t)t * rows + row) * nb + (size_t)ks * 8 + b] = sd[t] - (int)kMagic;
+          }
+        } else {
+          const unsigned long long dw2 = dup_pair(dw);
+#pragma unroll
+          for (int t = 0; t < NT; t += 2) {
             unsigned long long sx2;
             if (t + 1 < NT)
               sx2 = *reinterpret_cast<const unsigned long long*>(as + t);
             else
               sx2 = dup_pair(as[t]);
-            acc2[t / 2] = acc_pair(acc2[t / 2], sa, sb, mul_pair(dw2, sx2));
+            acc2[t / 2] = acc_pair(acc2[t / 2], sd[t], t + 1 < NT ? sd[t + 1] : (int)kMagic, mul_pair(dw2, sx2));
           }
         }
       }
@@ -304,13 +307,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       } else {
         // The CTA's sum for this tile (k-split mode: warp partials added in
-        // warp order), then rank 0 adds the cluster's CTA sums in rank order.
-        // k-split mode double-buffers the sums by tile parity, so one cluster
-        // barrier per tile suffices (a buffer is rewritten two tiles later,
-        // after the next barrier, which rank 0 reaches only once it has read
-        // this one); rows mode keeps one larger buffer and takes a second
-        // barrier after rank 0's reads.
-        float* rs = red_sum + (kSumBufs == 2 ? (m & 1) : 0) * kSum;
+        // warp order), then the cluster's CTA sums are added in rank order,
+        // each CTA taking a slice of the tile's outputs.  The sums are
+        // double-buffered by tile parity, so one cluster barrier per tile
+        // suffices: a buffer is rewritten two tiles later, after the next
+        // barrier, which no CTA reaches before it has read this one.
+        float* rs = red_sum + (m & 1) * kSum;
         if constexpr (ROWS) {
 #pragma unroll
           for (int t = 0; t < NT; ++t) rs[(warp * NT + t) * 32 + lane] = acc[t];
@@ -326,49 +328,95 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
         }
         cluster_sync();
-        if (rank == 0) {
-          for (int idx = threadIdx.x; idx < kSum; idx += kThreads) {
-            float v = rs[idx];
-            for (int r = 1; r < S; ++r) v = __fadd_rn(v, ld_dsmem_f32(&rs[idx], (uint32_t)r));
-            const int wq = ROWS ? idx / (NT * 32) : 0;
-            const int t = (idx / 32) % NT, rr = row0 + wq * kRowsPerCta + (idx & 31);
-            if (rr < rows) {
-              const size_t o = (size_t)t * rows + rr;
-              y[o] = residual ? __fadd_rn(__ldcg(residual + o), v) : v;  // residual may alias y
-            }
+        for (int idx = rank * kThreads + (int)threadIdx.x; idx < kSum; idx += S * kThreads) {
+          float part[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+            if (r < S) part[r] = ld_dsmem_f32(&rs[idx], (uint32_t)r);
+          float v = part[0];
+#pragma unroll
+          for (int r = 1; r < 8; ++r)
+            if (r < S) v = __fadd_rn(v, part[r]);
+          const int wq = ROWS ? idx / (NT * 32) : 0;
+          const int t = (idx / 32) % NT, rr = row0 + wq * kRowsPerCta + (idx & 31);
+          if (rr < rows) {
+            const size_t o = (size_t)t * rows + rr;
+            y[o] = residual ? __fadd_rn(__ldcg(residual + o), v) : v;  // residual may alias y
           }
         }
-        if constexpr (ROWS) cluster_sync();  // rank 0 is done with every CTA's buffer
       }
     }
   }
-  // keep this CTA's sums alive until rank 0 has read them
-  if (!EMIT && !ROWS) cluster_sync();
+  // keep this CTA's sums alive until every CTA of the cluster has read them
+  if (!EMIT && !(ROWS && S == 1)) cluster_sync();
 }
 
 size_t smem_bytes(int kr, int nt, bool rows_mode) {
   const size_t red = rows_mode ? 0 : (size_t)kWarps * nt * 32 * 4;
-  const size_t sums = rows_mode ? (size_t)kWarps * nt * 32 * 4 : 2 * (size_t)nt * 32 * 4;
+  const size_t sums = 2 * (rows_mode ? (size_t)kWarps : 1) * nt * 32 * 4;
   const size_t ntp = (size_t)nt + (nt & 1);
-  return (size_t)kr * 8 * (nt * 32 + ntp * 4) + (size_t)kWarps * kNStage * kStage + red + sums +
+  const size_t nta = ((size_t)nt + 3) & ~(size_t)3;
+  return (size_t)kr * 8 * (nta * 32 + ntp * 4) + (size_t)kWarps * kNStage * kStage + red + sums +
          (size_t)kWarps * kNStage * 8;
+}
+
+// Per-instantiation host caches (not thread-safe; one host thread drives a
+// device): the largest dynamic shared memory granted so far, and the number of
+// co-resident clusters for each (S, smem) seen.
+template <int NT, bool EMIT, bool ROWS>
+cudaError_t grant_smem(size_t smem) {
+  static size_t granted = 0;
+  if (smem <= granted) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(matmul_q8_0_narrow_kernel<NT, EMIT, ROWS>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess) granted = smem;
+  return e;
+}
+
+template <int NT, bool EMIT, bool ROWS>
+cudaError_t cluster_capacity(int S, size_t smem, int* clusters) {
+  struct Entry {
+    int S;
+    size_t smem;
+    int clusters;
+  };
+  static Entry cache[16];
+  static int n_cache = 0;
+  for (int i = 0; i < n_cache; ++i)
+    if (cache[i].S == S && cache[i].smem == smem) {
+      *clusters = cache[i].clusters;
+      return cudaSuccess;
+    }
+  cudaError_t e = grant_smem<NT, EMIT, ROWS>(smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)S;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.gridDim = dim3(1, (unsigned)S, 1);
+  int c = 0;
+  e = cudaOccupancyMaxActiveClusters(&c, matmul_q8_0_narrow_kernel<NT, EMIT, ROWS>, &cfg);
+  if (e != cudaSuccess) return e;
+  cache[n_cache < 16 ? n_cache++ : 15] = Entry{S, smem, c};
+  *clusters = c;
+  return cudaSuccess;
 }
 
 template <int NT, bool EMIT, bool ROWS>
 cudaError_t launch_nt(const uint8_t* W, int rows, int nb, const uint8_t* xq, float* y, const float* residual,
                       int32_t* isum, int S, size_t smem, cudaStream_t st) {
   auto kern = matmul_q8_0_narrow_kernel<NT, EMIT, ROWS>;
-  // Per-instantiation caches (not thread-safe; one host thread drives a
-  // device): the largest dynamic shared memory granted so far, and the number
-  // of co-resident clusters for each (S, smem) seen -- the persistent grid.
-  struct Entry {
-    int S;
-    size_t smem;
-    int clusters;
-  };
-  static Entry cache[8];
-  static int n_cache = 0;
-  static size_t granted = 0;
+  // The persistent grid: as many clusters as fit at once, up to one per tile.
+  int resident = 0;
+  cudaError_t e = cluster_capacity<NT, EMIT, ROWS>(S, smem, &resident);
+  if (e != cudaSuccess) return e;
+  if (resident < 1) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -378,25 +426,9 @@ cudaError_t launch_nt(const uint8_t* W, int rows, int nb, const uint8_t* xq, flo
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  if (smem > granted) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    granted = smem;
-  }
-  int resident = 0;
-  for (int i = 0; i < n_cache; ++i)
-    if (cache[i].S == S && cache[i].smem == smem) resident = cache[i].clusters;
-  if (resident == 0) {
-    cfg.gridDim = dim3(1, (unsigned)S, 1);
-    cudaError_t e = cudaOccupancyMaxActiveClusters(&resident, kern, &cfg);
-    if (e != cudaSuccess) return e;
-    if (resident < 1) return cudaErrorInvalidConfiguration;
-    cache[n_cache < 8 ? n_cache++ : 7] = Entry{S, smem, resident};
-  }
   const int tile = ROWS ? kWarps * kRowsPerCta : kRowsPerCta;
   const int tiles = (rows + tile - 1) / tile;
   const int n_clusters = tiles < resident ? tiles : resident;
@@ -426,30 +458,48 @@ struct Plan {
   int S;
 };
 
-// Depends on (rows, cols, SM count) only -- never on n_tok -- so that the
-// summation order of every output is the same for every n_tok.  Each CTA of
-// a cluster keeps the activations of its k-range in shared memory, which at
+// Depends on (rows, cols) and the device only -- never on n_tok -- so that
+// the summation order of every output is the same for every n_tok.  Each CTA
+// of a cluster keeps the activations of its k-range in shared memory, which at
 // n_tok = 16 allows at most 8 k-steps (36 KiB) next to the weight rings.
-// Rows mode (128-row tiles, no cross-warp sums) when there are at least as
-// many 128-row tiles per cluster slot as SMs; otherwise k-split mode on
-// 32-row tiles.  Among the admissible S the smallest estimated makespan (tiles
-// per cluster x k-steps per CTA, plus a per-tile reduction cost) wins,
-// assuming two resident CTAs per SM.
+// Rows mode: 128-row tiles, warps own 32 rows over the CTA's whole k-range;
+// k-split mode: 32-row tiles whose k-steps the 4 warps share.  Among the
+// admissible (mode, S) the smallest estimated makespan (tiles per cluster x
+// k-steps per warp, plus a per-tile reduction cost) wins, with the number of
+// clusters that fit on the device at once taken from the occupancy query of
+// the n_tok = 16 instance (the largest shared memory).
 Plan matmul_plan(int64_t rows, int64_t cols, int num_sms) {
+  struct Memo {
+    int64_t rows, cols;
+    Plan plan;
+  };
+  static Memo memo[64];
+  static int n_memo = 0;
+  for (int i = 0; i < n_memo; ++i)
+    if (memo[i].rows == rows && memo[i].cols == cols) return memo[i].plan;
   const int nks = (int)(cols / 256);
   int s_max = nks < 8 ? nks : 8;
   int s_min = (nks + 7) / 8;
   if (s_min > s_max) s_min = s_max;
   if (s_min < 1) s_min = 1;
-  const int P = 2 * num_sms;
   Plan best{false, s_min};
   double best_cost = 1e30;
+  bool queried = true;
   for (int mode = 0; mode < 2; ++mode) {
     const bool rm = mode == 1;
     const int tile = rm ? kWarps * kRowsPerCta : kRowsPerCta;
     const int tiles = (int)((rows + tile - 1) / tile);
     for (int S = s_min; S <= s_max; ++S) {
-      const int clusters = P / S > 0 ? P / S : 1;
+      const size_t smem = smem_bytes((nks + S - 1) / S, 16, rm);
+      int clusters = 0;
+      const cudaError_t e = rm ? cluster_capacity<16, false, true>(S, smem, &clusters)
+                               : cluster_capacity<16, false, false>(S, smem, &clusters);
+      if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        queried = false;
+        clusters = (2 * num_sms) / S;  // estimate: two CTAs per SM
+      }
+      if (clusters < 1) continue;
       const int per = (tiles + clusters - 1) / clusters;
       const int ksteps = (nks + S - 1) / S;
       // time ~ tiles per cluster x (k-steps each warp runs + per-tile sync cost)
@@ -462,6 +512,7 @@ Plan matmul_plan(int64_t rows, int64_t cols, int num_sms) {
       }
     }
   }
+  if (queried && n_memo < 64) memo[n_memo++] = Memo{rows, cols, best};
   return best;
 }
 
