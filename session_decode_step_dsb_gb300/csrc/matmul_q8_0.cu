@@ -48,7 +48,8 @@ namespace dsbk {
 
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kPairs = 4;             // row groups (or k-step lanes) of a CTA
+constexpr int kWarps = 2 * kPairs;     // two warps per row group: one per token half
 constexpr int kThreads = kWarps * 32;
 constexpr int kRowsPerCta = 32;
 constexpr int kChunkBytes = 272;  // 8 blocks of 34 bytes
@@ -105,22 +106,34 @@ __device__ __forceinline__ float2 unpack_pair(unsigned long long v) {
   return r;
 }
 
-// ROWS = false (few-row matrices): a CTA tile is 32 rows and its 4 warps
-//   take interleaved k-steps of the CTA's k-range; warp partials are added in
-//   warp order at each tile end.
-// ROWS = true (many-row matrices): a CTA tile is 128 rows, warp w owns rows
-//   32w..32w+31 over the whole k-range; no partials are exchanged between
-//   warps, and with S = 1 no barrier of any kind is taken after start-up.
-// In both modes the S CTAs of a cluster split k and rank 0 adds their sums in
-// rank order through distributed shared memory.
+// The 8 warps form 4 pairs; the two warps of a pair read the same weight
+// stages (one 2-stage ring per pair) and take the first and second half of the
+// tokens, so a weight byte crosses shared memory once per pair while twice as
+// many warps hide the latencies.  The first warp of a pair refills a stage once
+// both hold it in registers (a 64-thread named barrier per k-step; it let the
+// refill go out earlier than polled "empty" mbarriers did).
+// ROWS = false (few-row matrices): a CTA tile is 32 rows and its 4 pairs
+//   take interleaved k-steps of the CTA's k-range; pair partials are added in
+//   pair order at each tile end.
+// ROWS = true (many-row matrices): a CTA tile is 128 rows, pair p owns rows
+//   32p..32p+31 over the whole k-range; no partials are exchanged between
+//   pairs, and with S = 1 no CTA-wide barrier is taken after start-up.
+// In both modes the S CTAs of a cluster split k and their sums are added in
+// rank order through distributed shared memory.  Token t's arithmetic (block
+// order, k-step order, pair and rank order) does not depend on n_tok.
 template <int NT, bool EMIT, bool ROWS>
 __global__ void __launch_bounds__(kThreads, 2)
     matmul_q8_0_narrow_kernel(const uint8_t* __restrict__ W, int rows, int nb, const uint8_t* xq,
                               float* y, const float* residual, int32_t* __restrict__ isum_out) {
-  constexpr int kTile = ROWS ? kWarps * kRowsPerCta : kRowsPerCta;
-  constexpr int kRed = ROWS ? 0 : kWarps * NT * 32;          // warp partials (k-split mode)
-  constexpr int kSum = (ROWS ? kWarps : 1) * NT * 32;        // one CTA sum buffer
-  constexpr int NTP = NT + (NT & 1);      // scale row stride: even, so token pairs load as 8 bytes
+  constexpr int kTile = ROWS ? kPairs * kRowsPerCta : kRowsPerCta;
+  constexpr int kRed = ROWS ? 0 : kPairs * NT * 32;          // pair partials (k-split mode)
+  constexpr int kSum = (ROWS ? kPairs : 1) * NT * 32;        // one CTA sum buffer
+  // Token halves: the first warp of a pair takes NTH0 tokens, the second the
+  // rest.  NTH is even, so both halves start on an even token and their word
+  // and scale pairs load as aligned 8-byte words; n_tok <= 2 is not split.
+  constexpr int NTH = ((NT + 1) / 2 + 1) & ~1;
+  constexpr int NTH0 = NTH < NT ? NTH : NT;
+  constexpr int NTP = 2 * NTH;            // scale row stride: both halves' pairs within the row
   constexpr int NTA = (NT + 3) & ~3;      // word row stride: four tokens per 16-byte load
   extern __shared__ __align__(128) uint8_t smem[];
   const int nks = nb >> 3;
@@ -130,10 +143,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   const Split ksr = kstep_range(nks, S, rank);
   const int kr = ksr.ks1 - ksr.ks0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = warp & (kPairs - 1), half = warp / kPairs;
+  const int t0 = half ? NTH0 : 0;                  // this warp's first token
+  const int nt_mine = half ? NT - NTH0 : NTH0;     // and its token count (0 for the second half at n_tok <= 2)
   const size_t row_bytes = (size_t)nb * 34;
   const int tiles = (rows + kTile - 1) / kTile;
   const int n_tiles = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / n_clusters + 1 : 0;
-  const int warp_row = ROWS ? warp * kRowsPerCta : 0;
+  const int warp_row = ROWS ? pair * kRowsPerCta : 0;
 
   // Shared layout: act codes | act scales | stage rings | warp partials |
   // CTA sums (double-buffered) | barriers.  The act region is sized for the
@@ -143,24 +159,25 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int kr_alloc = (nks + S - 1) / S;
   uint32_t* act_q = reinterpret_cast<uint32_t*>(smem);                               // [kr*8][8][NTA]
   float* act_s = reinterpret_cast<float*>(act_q + (size_t)kr_alloc * 8 * 8 * NTA);  // [kr*8][NTP]
-  uint8_t* stages = reinterpret_cast<uint8_t*>(act_s + (size_t)kr_alloc * 8 * NTP);  // [kWarps][kNStage][kStage]
-  float* red = reinterpret_cast<float*>(stages + (size_t)kWarps * kNStage * kStage);  // [kWarps][NT][32]
-  float* red_sum = red + kRed;                                                        // [kSumBufs][kSum]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red_sum + 2 * kSum);                  // [kWarps][kNStage]
-  uint8_t* my_stages = stages + (size_t)warp * kNStage * kStage;
-  uint64_t* my_bars = bars + warp * kNStage;
+  uint8_t* stages = reinterpret_cast<uint8_t*>(act_s + (size_t)kr_alloc * 8 * NTP);  // [kPairs][kNStage][kStage]
+  float* red = reinterpret_cast<float*>(stages + (size_t)kPairs * kNStage * kStage);  // [kPairs][NT][32]
+  float* red_sum = red + kRed;                                                        // [2][kSum]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red_sum + 2 * kSum);                  // [kPairs][kNStage]
+  uint8_t* my_stages = stages + (size_t)pair * kNStage * kStage;
+  uint64_t* my_bars = bars + pair * kNStage;
+  constexpr int kReaders = NT > NTH0 ? 2 : 1;       // warps of a pair with tokens
 
-  if (lane == 0) {
+  if (half == 0 && lane == 0) {
     for (int s = 0; s < kNStage; ++s) mbar_init(&my_bars[s], 1);
     fence_mbar_init();
   }
   __syncwarp();
 
-  // This warp's units: for each of the CTA's tiles m, its k-steps (all of the
-  // k-range in ROWS mode, every kWarps-th otherwise).  Unit u = m*n_mine + i.
-  const int n_mine = ROWS ? kr : (kr > warp ? (kr - warp + kWarps - 1) / kWarps : 0);
+  // This pair's units: for each of the CTA's tiles m, its k-steps (all of the
+  // k-range in ROWS mode, every kPairs-th otherwise).  Unit u = m*n_mine + i.
+  const int n_mine = ROWS ? kr : (kr > pair ? (kr - pair + kPairs - 1) / kPairs : 0);
   const int n_units = n_tiles * n_mine;
-  auto kstep = [&](int i) { return ROWS ? ksr.ks0 + i : ksr.ks0 + warp + kWarps * i; };
+  auto kstep = [&](int i) { return ROWS ? ksr.ks0 + i : ksr.ks0 + pair + kPairs * i; };
   auto issue = [&](int u) {
     const int m = u / n_mine, i = u - m * n_mine;
     const int row0 = ((int)blockIdx.x + m * n_clusters) * kTile + warp_row;
@@ -175,7 +192,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (row < rows)
       bulk_g2s(dst + lane * kChunkBytes, W + (size_t)row * row_bytes + (size_t)ks * kChunkBytes, kChunkBytes, bar);
   };
-  for (int u = 0; u < kNStage && u < n_units; ++u) issue(u);  // weights do not depend on the previous kernel
+  if (half == 0)
+    for (int u = 0; u < kNStage && u < n_units; ++u) issue(u);  // weights do not depend on the previous kernel
   pdl_wait();  // the activations (and y / residual) may be the previous kernel's results
   pdl_trigger();
 
@@ -189,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (t >= NT) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) dq[k * NTA] = 0u;
+      for (int tp = t; tp < NTP; tp += NTA) act_s[(size_t)b * NTP + tp] = 0.0f;
       continue;
     }
     const long long g = (long long)t * nb + (long long)ksr.ks0 * 8 + b;  // global block index
@@ -209,11 +228,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (int m = 0; m < n_tiles; ++m) {
     const int row0 = ((int)blockIdx.x + m * n_clusters) * kTile;
     const int row = row0 + warp_row + lane;
-    unsigned long long acc2[(NT + 1) / 2];
+    unsigned long long acc2[(NTH + 1) / 2];
 #pragma unroll
-    for (int p = 0; p < (NT + 1) / 2; ++p) acc2[p] = 0ull;
+    for (int p = 0; p < (NTH + 1) / 2; ++p) acc2[p] = 0ull;
 
     for (int i = 0; i < n_mine; ++i, ++u) {
+      if (nt_mine == 0) continue;  // the second warp of a pair at n_tok <= 2
       const int ks = kstep(i);
       const int kl = ks - ksr.ks0;
       uint64_t* bar = &my_bars[u % kNStage];
@@ -232,8 +252,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         w[4 * c + 2] = v.z;
         w[4 * c + 3] = v.w;
       }
-      __syncwarp();  // every lane has read the stage: it may be refilled
-      if (!dead && u + kNStage < n_units) issue(u + kNStage);
+      // every reader of the pair holds the stage: it may be refilled
+      if constexpr (kReaders == 2)
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");
+      else
+        __syncwarp();
+      if (half == 0 && !dead && u + kNStage < n_units) issue(u + kNStage);
 
 #pragma unroll
       for (int b = 0; b < 8; ++b) {
@@ -250,64 +274,70 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int k = 0; k < 8; ++k) q[k] = w[base + 1 + k];
           dw = half_bits_to_float(w[base] >> 16);
         }
-        const uint32_t* aq = act_q + (size_t)(kl * 8 + b) * 8 * NTA;
-        const float* as = act_s + (size_t)(kl * 8 + b) * NTP;  // 8-byte aligned row
-        // the NT block dots advance word by word together
-        int sd[NTA];
+        const uint32_t* aq = act_q + (size_t)(kl * 8 + b) * 8 * NTA + t0;
+        const float* as = act_s + (size_t)(kl * 8 + b) * NTP + t0;
+        // this warp's block dots advance word by word together (two words per
+        // 8-byte load; t0 is even)
+        int sd[NTH];
 #pragma unroll
-        for (int t = 0; t < NTA; ++t) sd[t] = (int)kMagic;
+        for (int t = 0; t < NTH; ++t) sd[t] = (int)kMagic;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
 #pragma unroll
-          for (int t4 = 0; t4 < NTA; t4 += 4) {
-            const uint4 a = *reinterpret_cast<const uint4*>(aq + k * NTA + t4);
-            sd[t4 + 0] = __dp4a((int)q[k], (int)a.x, sd[t4 + 0]);
-            if (t4 + 1 < NT) sd[t4 + 1] = __dp4a((int)q[k], (int)a.y, sd[t4 + 1]);
-            if (t4 + 2 < NT) sd[t4 + 2] = __dp4a((int)q[k], (int)a.z, sd[t4 + 2]);
-            if (t4 + 3 < NT) sd[t4 + 3] = __dp4a((int)q[k], (int)a.w, sd[t4 + 3]);
+          for (int t2 = 0; t2 < NTH; t2 += 2) {
+            if (t2 + 1 < NTH) {
+              const uint2 a = *reinterpret_cast<const uint2*>(aq + k * NTA + t2);
+              if (t2 < nt_mine) sd[t2] = __dp4a((int)q[k], (int)a.x, sd[t2]);
+              if (t2 + 1 < nt_mine) sd[t2 + 1] = __dp4a((int)q[k], (int)a.y, sd[t2 + 1]);
+            } else if (t2 < nt_mine) {
+              sd[t2] = __dp4a((int)q[k], (int)aq[k * NTA + t2], sd[t2]);
+            }
           }
         }
         if constexpr (EMIT) {
           if (row < rows) {
 #pragma unroll
-            for (int t = 0; t < NT; ++t)
-              isum_out[((size_t)t * rows + row) * nb + (size_t)ks * 8 + b] = sd[t] - (int)kMagic;
+            for (int t = 0; t < NTH; ++t)
+              if (t < nt_mine)
+                isum_out[((size_t)(t0 + t) * rows + row) * nb + (size_t)ks * 8 + b] = sd[t] - (int)kMagic;
           }
         } else {
           const unsigned long long dw2 = dup_pair(dw);
 #pragma unroll
-          for (int t = 0; t < NT; t += 2) {
+          for (int t = 0; t < NTH; t += 2) {
             unsigned long long sx2;
-            if (t + 1 < NT)
+            if (t + 1 < NTH)
               sx2 = *reinterpret_cast<const unsigned long long*>(as + t);
             else
               sx2 = dup_pair(as[t]);
-            acc2[t / 2] = acc_pair(acc2[t / 2], sd[t], t + 1 < NT ? sd[t + 1] : (int)kMagic, mul_pair(dw2, sx2));
+            acc2[t / 2] = acc_pair(acc2[t / 2], sd[t], t + 1 < NTH ? sd[t + 1] : (int)kMagic, mul_pair(dw2, sx2));
           }
         }
       }
     }
 
     if constexpr (!EMIT) {
-      float acc[NT];
+      float acc[NTH];
 #pragma unroll
-      for (int p = 0; p < (NT + 1) / 2; ++p) {
+      for (int p = 0; p < (NTH + 1) / 2; ++p) {
         const float2 v = unpack_pair(acc2[p]);
         acc[2 * p] = v.x;
-        if (2 * p + 1 < NT) acc[2 * p + 1] = v.y;
+        if (2 * p + 1 < NTH) acc[2 * p + 1] = v.y;
       }
       if (ROWS && S == 1) {
-        // One warp owns these rows over the whole k: write them directly.
+        // One pair owns these rows over the whole k: write them directly.
         if (row < rows) {
 #pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            const size_t o = (size_t)t * rows + row;
-            y[o] = residual ? __fadd_rn(__ldcg(residual + o), acc[t]) : acc[t];  // residual may alias y
+          for (int t = 0; t < NTH; ++t) {
+            if (t < nt_mine) {
+              const size_t o = (size_t)(t0 + t) * rows + row;
+              y[o] = residual ? __fadd_rn(__ldcg(residual + o), acc[t]) : acc[t];  // residual may alias y
+            }
           }
         }
       } else {
-        // The CTA's sum for this tile (k-split mode: warp partials added in
-        // warp order), then the cluster's CTA sums are added in rank order,
+        // The CTA's sum for this tile (k-split mode: pair partials added in
+        // pair order), then the cluster's CTA sums are added in rank order,
         // each CTA taking a slice of the tile's outputs.  The sums are
         // double-buffered by tile parity, so one cluster barrier per tile
         // suffices: a buffer is rewritten two tiles later, after the next
@@ -315,15 +345,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         float* rs = red_sum + (m & 1) * kSum;
         if constexpr (ROWS) {
 #pragma unroll
-          for (int t = 0; t < NT; ++t) rs[(warp * NT + t) * 32 + lane] = acc[t];
+          for (int t = 0; t < NTH; ++t)
+            if (t < nt_mine) rs[(pair * NT + t0 + t) * 32 + lane] = acc[t];
         } else {
 #pragma unroll
-          for (int t = 0; t < NT; ++t) red[(warp * NT + t) * 32 + lane] = acc[t];
+          for (int t = 0; t < NTH; ++t)
+            if (t < nt_mine) red[(pair * NT + t0 + t) * 32 + lane] = acc[t];
           __syncthreads();
           for (int idx = threadIdx.x; idx < NT * 32; idx += kThreads) {
             float v = red[idx];
 #pragma unroll
-            for (int w2 = 1; w2 < kWarps; ++w2) v = __fadd_rn(v, red[w2 * NT * 32 + idx]);
+            for (int p2 = 1; p2 < kPairs; ++p2) v = __fadd_rn(v, red[p2 * NT * 32 + idx]);
             rs[idx] = v;
           }
         }
@@ -337,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int r = 1; r < 8; ++r)
             if (r < S) v = __fadd_rn(v, part[r]);
-          const int wq = ROWS ? idx / (NT * 32) : 0;
+          const int wq = ROWS ? idx / (NT * 32) : 0;  // the pair (row group) of this output
           const int t = (idx / 32) % NT, rr = row0 + wq * kRowsPerCta + (idx & 31);
           if (rr < rows) {
             const size_t o = (size_t)t * rows + rr;
@@ -352,12 +384,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 size_t smem_bytes(int kr, int nt, bool rows_mode) {
-  const size_t red = rows_mode ? 0 : (size_t)kWarps * nt * 32 * 4;
-  const size_t sums = 2 * (rows_mode ? (size_t)kWarps : 1) * nt * 32 * 4;
-  const size_t ntp = (size_t)nt + (nt & 1);
+  const size_t red = rows_mode ? 0 : (size_t)kPairs * nt * 32 * 4;
+  const size_t sums = 2 * (rows_mode ? (size_t)kPairs : 1) * nt * 32 * 4;
+  const size_t ntp = 2 * ((((size_t)nt + 1) / 2 + 1) & ~(size_t)1);  // the kernel's NTP
   const size_t nta = ((size_t)nt + 3) & ~(size_t)3;
-  return (size_t)kr * 8 * (nta * 32 + ntp * 4) + (size_t)kWarps * kNStage * kStage + red + sums +
-         (size_t)kWarps * kNStage * 8;
+  return (size_t)kr * 8 * (nta * 32 + ntp * 4) + (size_t)kPairs * kNStage * kStage + red + sums +
+         (size_t)kPairs * kNStage * 8;
 }
 
 // Per-instantiation host caches (not thread-safe; one host thread drives a
@@ -429,7 +461,7 @@ cudaError_t launch_nt(const uint8_t* W, int rows, int nb, const uint8_t* xq, flo
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  const int tile = ROWS ? kWarps * kRowsPerCta : kRowsPerCta;
+  const int tile = ROWS ? kPairs * kRowsPerCta : kRowsPerCta;
   const int tiles = (rows + tile - 1) / tile;
   const int n_clusters = tiles < resident ? tiles : resident;
   cfg.gridDim = dim3((unsigned)n_clusters, (unsigned)S, 1);
@@ -487,7 +519,7 @@ Plan matmul_plan(int64_t rows, int64_t cols, int num_sms) {
   bool queried = true;
   for (int mode = 0; mode < 2; ++mode) {
     const bool rm = mode == 1;
-    const int tile = rm ? kWarps * kRowsPerCta : kRowsPerCta;
+    const int tile = rm ? kPairs * kRowsPerCta : kRowsPerCta;
     const int tiles = (int)((rows + tile - 1) / tile);
     for (int S = s_min; S <= s_max; ++S) {
       const size_t smem = smem_bytes((nks + S - 1) / S, 16, rm);
@@ -504,7 +536,7 @@ Plan matmul_plan(int64_t rows, int64_t cols, int num_sms) {
       const int ksteps = (nks + S - 1) / S;
       // time ~ tiles per cluster x (k-steps each warp runs + per-tile sync cost)
       const double sync = (rm && S == 1) ? 0.0 : 0.5;
-      const double warp_steps = rm ? (double)ksteps : (double)((ksteps + kWarps - 1) / kWarps);
+      const double warp_steps = rm ? (double)ksteps : (double)((ksteps + kPairs - 1) / kPairs);
       const double c = per * (warp_steps + sync);
       if (c < best_cost - 1e-9) {
         best_cost = c;
