@@ -79,6 +79,15 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
+// Split halves of the cluster barrier (every thread of every CTA of the
+// cluster; an arrive must be followed by its wait before the next arrive).
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

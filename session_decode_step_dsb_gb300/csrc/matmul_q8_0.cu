@@ -30,7 +30,7 @@
 //    of all n_tok tokens advance word by word together, so consecutive dp4a
 //    instructions never depend on each other.
 //  * When rows alone give too few CTAs, k is split over the CTAs of a thread
-//    block cluster (<= 8) and the partial sums are added through distributed
+//    block cluster (<= 16 CTAs) and the partial sums are added through distributed
 //    shared memory in cluster-rank order; every CTA of the cluster sums a
 //    slice of the tile, from double-buffered sums, one cluster barrier per
 //    tile.  No atomics; every reduction order depends only on (rows, cols) and
@@ -40,6 +40,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "dsb_kernels.h"
 #include "dsb_ptx.cuh"
@@ -55,9 +56,9 @@ constexpr int kRowsPerCta = 32;
 constexpr int kChunkBytes = 272;  // 8 blocks of 34 bytes
 constexpr int kStage = kRowsPerCta * kChunkBytes;
 constexpr int kNStage = 2;
+constexpr int kMaxCluster = 16;  // k-split CTAs per cluster (above 8: a non-portable cluster size)
 constexpr uint32_t kMagic = 0x4B400000u;  // bits of 12582912.0f = 1.5 * 2^23
 constexpr unsigned long long kMagic2 = 0x4B4000004B400000ull;
-constexpr float kMagicF = 12582912.0f;
 
 __device__ unsigned int g_err_matmul = 0;
 
@@ -145,7 +146,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int pair = warp & (kPairs - 1), half = warp / kPairs;
   const int t0 = half ? NTH0 : 0;                  // this warp's first token
-  const int nt_mine = half ? NT - NTH0 : NTH0;     // and its token count (0 for the second half at n_tok <= 2)
   const size_t row_bytes = (size_t)nb * 34;
   const int tiles = (rows + kTile - 1) / kTile;
   const int n_tiles = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / n_clusters + 1 : 0;
@@ -223,164 +223,188 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
 
+  // Cross-CTA sums: the CTA sum of tile m goes to buffer m & 1 and the CTA
+  // arrives on the cluster barrier; it waits, and adds the cluster's sums of
+  // tile m (its slice, ranks in order), only after computing tile m + 1.  A
+  // buffer is rewritten two tiles later, after the next wait, which no CTA
+  // passes before every CTA has read it.
+  constexpr bool kCluster = !EMIT;  // ROWS && S == 1 writes directly instead (runtime)
+  const bool cluster_sums = kCluster && !(ROWS && S == 1);
+  auto reduce_tile = [&](int m) {
+    const float* rs = red_sum + (m & 1) * kSum;
+    const int row0 = ((int)blockIdx.x + m * n_clusters) * kTile;
+    for (int idx = rank * kThreads + (int)threadIdx.x; idx < kSum; idx += S * kThreads) {
+      float part[kMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < S) part[r] = ld_dsmem_f32(&rs[idx], (uint32_t)r);
+      float v = part[0];
+#pragma unroll
+      for (int r = 1; r < kMaxCluster; ++r)
+        if (r < S) v = __fadd_rn(v, part[r]);
+      const int wq = ROWS ? idx / (NT * 32) : 0;  // the pair (row group) of this output
+      const int t = (idx / 32) % NT, rr = row0 + wq * kRowsPerCta + (idx & 31);
+      if (rr < rows) {
+        const size_t o = (size_t)t * rows + rr;
+        y[o] = residual ? __fadd_rn(__ldcg(residual + o), v) : v;  // residual may alias y
+      }
+    }
+  };
+
   bool dead = false;
   int u = 0;
-  for (int m = 0; m < n_tiles; ++m) {
-    const int row0 = ((int)blockIdx.x + m * n_clusters) * kTile;
-    const int row = row0 + warp_row + lane;
-    unsigned long long acc2[(NTH + 1) / 2];
+  // The tile loop, specialised on this warp's token count NTM (compile time):
+  // the two halves of a pair run their own instance.
+  auto run = [&](auto ntm_c) {
+    constexpr int NTM = decltype(ntm_c)::value;
+    constexpr int NTMA = NTM > 0 ? NTM : 1;  // array extents
+    for (int m = 0; m < n_tiles; ++m) {
+      const int row0 = ((int)blockIdx.x + m * n_clusters) * kTile;
+      const int row = row0 + warp_row + lane;
+      unsigned long long acc2[(NTMA + 1) / 2];
 #pragma unroll
-    for (int p = 0; p < (NTH + 1) / 2; ++p) acc2[p] = 0ull;
+      for (int p = 0; p < (NTMA + 1) / 2; ++p) acc2[p] = 0ull;
 
-    for (int i = 0; i < n_mine; ++i, ++u) {
-      if (nt_mine == 0) continue;  // the second warp of a pair at n_tok <= 2
-      const int ks = kstep(i);
-      const int kl = ks - ksr.ks0;
-      uint64_t* bar = &my_bars[u % kNStage];
-      if (!dead) {
-        const bool ok = mbar_wait(bar, (uint32_t)((u / kNStage) & 1));
-        dead = __any_sync(0xffffffffu, !ok);  // warp-uniform
-        if (dead && lane == 0) g_err_matmul = 1u;
-      }
-      const uint4* src = reinterpret_cast<const uint4*>(my_stages + (size_t)(u % kNStage) * kStage + lane * kChunkBytes);
-      uint32_t w[68];
+      if constexpr (NTM > 0) {
+        for (int i = 0; i < n_mine; ++i, ++u) {
+          const int ks = kstep(i);
+          const int kl = ks - ksr.ks0;
+          uint64_t* bar = &my_bars[u % kNStage];
+          if (!dead) {
+            const bool ok = mbar_wait(bar, (uint32_t)((u / kNStage) & 1));
+            dead = __any_sync(0xffffffffu, !ok);  // warp-uniform
+            if (dead && lane == 0) g_err_matmul = 1u;
+          }
+          const uint4* src =
+              reinterpret_cast<const uint4*>(my_stages + (size_t)(u % kNStage) * kStage + lane * kChunkBytes);
+          uint32_t w[68];
 #pragma unroll
-      for (int c = 0; c < 17; ++c) {
-        const uint4 v = src[c];
-        w[4 * c + 0] = v.x;
-        w[4 * c + 1] = v.y;
-        w[4 * c + 2] = v.z;
-        w[4 * c + 3] = v.w;
-      }
-      // every reader of the pair holds the stage: it may be refilled
-      if constexpr (kReaders == 2)
-        asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");
-      else
-        __syncwarp();
-      if (half == 0 && !dead && u + kNStage < n_units) issue(u + kNStage);
+          for (int c = 0; c < 17; ++c) {
+            const uint4 v = src[c];
+            w[4 * c + 0] = v.x;
+            w[4 * c + 1] = v.y;
+            w[4 * c + 2] = v.z;
+            w[4 * c + 3] = v.w;
+          }
+          // every reader of the pair holds the stage: it may be refilled
+          if constexpr (kReaders == 2)
+            asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");
+          else
+            __syncwarp();
+          if (half == 0 && !dead && u + kNStage < n_units) issue(u + kNStage);
 
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        uint32_t q[8];
-        float dw;
-        if ((b & 1) == 0) {
-          const int base = (17 * b) / 2;
+          for (int b = 0; b < 8; ++b) {
+            uint32_t q[8];
+            float dw;
+            if ((b & 1) == 0) {
+              const int base = (17 * b) / 2;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) q[k] = __funnelshift_r(w[base + k], w[base + k + 1], 16);
-          dw = half_bits_to_float(w[base]);
-        } else {
-          const int base = (17 * b - 1) / 2;
+              for (int k = 0; k < 8; ++k) q[k] = __funnelshift_r(w[base + k], w[base + k + 1], 16);
+              dw = half_bits_to_float(w[base]);
+            } else {
+              const int base = (17 * b - 1) / 2;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) q[k] = w[base + 1 + k];
-          dw = half_bits_to_float(w[base] >> 16);
-        }
-        const uint32_t* aq = act_q + (size_t)(kl * 8 + b) * 8 * NTA + t0;
-        const float* as = act_s + (size_t)(kl * 8 + b) * NTP + t0;
-        // this warp's block dots advance word by word together (two words per
-        // 8-byte load; t0 is even)
-        int sd[NTH];
+              for (int k = 0; k < 8; ++k) q[k] = w[base + 1 + k];
+              dw = half_bits_to_float(w[base] >> 16);
+            }
+            const uint32_t* aq = act_q + (size_t)(kl * 8 + b) * 8 * NTA + t0;
+            // this warp's block dots advance word by word together (two
+            // words per 8-byte load; t0 is even)
+            int sd[NTM];
 #pragma unroll
-        for (int t = 0; t < NTH; ++t) sd[t] = (int)kMagic;
+            for (int t = 0; t < NTM; ++t) sd[t] = (int)kMagic;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < 8; ++k) {
 #pragma unroll
-          for (int t2 = 0; t2 < NTH; t2 += 2) {
-            if (t2 + 1 < NTH) {
-              const uint2 a = *reinterpret_cast<const uint2*>(aq + k * NTA + t2);
-              if (t2 < nt_mine) sd[t2] = __dp4a((int)q[k], (int)a.x, sd[t2]);
-              if (t2 + 1 < nt_mine) sd[t2 + 1] = __dp4a((int)q[k], (int)a.y, sd[t2 + 1]);
-            } else if (t2 < nt_mine) {
-              sd[t2] = __dp4a((int)q[k], (int)aq[k * NTA + t2], sd[t2]);
+              for (int t2 = 0; t2 < NTM; t2 += 2) {
+                if (t2 + 1 < NTM) {
+                  const uint2 a = *reinterpret_cast<const uint2*>(aq + k * NTA + t2);
+                  sd[t2] = __dp4a((int)q[k], (int)a.x, sd[t2]);
+                  sd[t2 + 1] = __dp4a((int)q[k], (int)a.y, sd[t2 + 1]);
+                } else {
+                  sd[t2] = __dp4a((int)q[k], (int)aq[k * NTA + t2], sd[t2]);
+                }
+              }
+            }
+            if constexpr (EMIT) {
+              if (row < rows) {
+#pragma unroll
+                for (int t = 0; t < NTM; ++t)
+                  isum_out[((size_t)(t0 + t) * rows + row) * nb + (size_t)ks * 8 + b] = sd[t] - (int)kMagic;
+              }
+            } else {
+              const float* as = act_s + (size_t)(kl * 8 + b) * NTP + t0;
+              const unsigned long long dw2 = dup_pair(dw);
+#pragma unroll
+              for (int t = 0; t < NTM; t += 2) {
+                unsigned long long sx2;
+                if (t + 1 < NTM)
+                  sx2 = *reinterpret_cast<const unsigned long long*>(as + t);
+                else
+                  sx2 = dup_pair(as[t]);
+                acc2[t / 2] =
+                    acc_pair(acc2[t / 2], sd[t], t + 1 < NTM ? sd[t + 1] : (int)kMagic, mul_pair(dw2, sx2));
+              }
             }
           }
         }
-        if constexpr (EMIT) {
+      }
+
+      if constexpr (!EMIT) {
+        float acc[NTMA];
+#pragma unroll
+        for (int p = 0; p < (NTMA + 1) / 2; ++p) {
+          const float2 v = unpack_pair(acc2[p]);
+          acc[2 * p] = v.x;
+          if (2 * p + 1 < NTMA) acc[2 * p + 1] = v.y;
+        }
+        if (!cluster_sums) {
+          // One pair owns these rows over the whole k: write them directly.
           if (row < rows) {
 #pragma unroll
-            for (int t = 0; t < NTH; ++t)
-              if (t < nt_mine)
-                isum_out[((size_t)(t0 + t) * rows + row) * nb + (size_t)ks * 8 + b] = sd[t] - (int)kMagic;
-          }
-        } else {
-          const unsigned long long dw2 = dup_pair(dw);
-#pragma unroll
-          for (int t = 0; t < NTH; t += 2) {
-            unsigned long long sx2;
-            if (t + 1 < NTH)
-              sx2 = *reinterpret_cast<const unsigned long long*>(as + t);
-            else
-              sx2 = dup_pair(as[t]);
-            acc2[t / 2] = acc_pair(acc2[t / 2], sd[t], t + 1 < NTH ? sd[t + 1] : (int)kMagic, mul_pair(dw2, sx2));
-          }
-        }
-      }
-    }
-
-    if constexpr (!EMIT) {
-      float acc[NTH];
-#pragma unroll
-      for (int p = 0; p < (NTH + 1) / 2; ++p) {
-        const float2 v = unpack_pair(acc2[p]);
-        acc[2 * p] = v.x;
-        if (2 * p + 1 < NTH) acc[2 * p + 1] = v.y;
-      }
-      if (ROWS && S == 1) {
-        // One pair owns these rows over the whole k: write them directly.
-        if (row < rows) {
-#pragma unroll
-          for (int t = 0; t < NTH; ++t) {
-            if (t < nt_mine) {
+            for (int t = 0; t < NTM; ++t) {
               const size_t o = (size_t)(t0 + t) * rows + row;
               y[o] = residual ? __fadd_rn(__ldcg(residual + o), acc[t]) : acc[t];  // residual may alias y
             }
           }
-        }
-      } else {
-        // The CTA's sum for this tile (k-split mode: pair partials added in
-        // pair order), then the cluster's CTA sums are added in rank order,
-        // each CTA taking a slice of the tile's outputs.  The sums are
-        // double-buffered by tile parity, so one cluster barrier per tile
-        // suffices: a buffer is rewritten two tiles later, after the next
-        // barrier, which no CTA reaches before it has read this one.
-        float* rs = red_sum + (m & 1) * kSum;
-        if constexpr (ROWS) {
-#pragma unroll
-          for (int t = 0; t < NTH; ++t)
-            if (t < nt_mine) rs[(pair * NT + t0 + t) * 32 + lane] = acc[t];
         } else {
-#pragma unroll
-          for (int t = 0; t < NTH; ++t)
-            if (t < nt_mine) red[(pair * NT + t0 + t) * 32 + lane] = acc[t];
-          __syncthreads();
-          for (int idx = threadIdx.x; idx < NT * 32; idx += kThreads) {
-            float v = red[idx];
-#pragma unroll
-            for (int p2 = 1; p2 < kPairs; ++p2) v = __fadd_rn(v, red[p2 * NT * 32 + idx]);
-            rs[idx] = v;
+          // the previous tile's cluster sums, now that this tile is computed
+          if (m > 0) {
+            cluster_wait();
+            reduce_tile(m - 1);
           }
-        }
-        cluster_sync();
-        for (int idx = rank * kThreads + (int)threadIdx.x; idx < kSum; idx += S * kThreads) {
-          float part[8];
+          // this tile's CTA sum (k-split mode: pair partials in pair order)
+          float* rs = red_sum + (m & 1) * kSum;
+          if constexpr (ROWS) {
 #pragma unroll
-          for (int r = 0; r < 8; ++r)
-            if (r < S) part[r] = ld_dsmem_f32(&rs[idx], (uint32_t)r);
-          float v = part[0];
+            for (int t = 0; t < NTM; ++t) rs[(pair * NT + t0 + t) * 32 + lane] = acc[t];
+          } else {
 #pragma unroll
-          for (int r = 1; r < 8; ++r)
-            if (r < S) v = __fadd_rn(v, part[r]);
-          const int wq = ROWS ? idx / (NT * 32) : 0;  // the pair (row group) of this output
-          const int t = (idx / 32) % NT, rr = row0 + wq * kRowsPerCta + (idx & 31);
-          if (rr < rows) {
-            const size_t o = (size_t)t * rows + rr;
-            y[o] = residual ? __fadd_rn(__ldcg(residual + o), v) : v;  // residual may alias y
+            for (int t = 0; t < NTM; ++t) red[(pair * NT + t0 + t) * 32 + lane] = acc[t];
+            __syncthreads();
+            for (int idx = threadIdx.x; idx < NT * 32; idx += kThreads) {
+              float v = red[idx];
+#pragma unroll
+              for (int p2 = 1; p2 < kPairs; ++p2) v = __fadd_rn(v, red[p2 * NT * 32 + idx]);
+              rs[idx] = v;
+            }
           }
+          cluster_arrive();
         }
       }
     }
-  }
-  // keep this CTA's sums alive until every CTA of the cluster has read them
-  if (!EMIT && !(ROWS && S == 1)) cluster_sync();
+    if (cluster_sums && n_tiles > 0) {
+      cluster_wait();
+      reduce_tile(n_tiles - 1);
+      // keep this CTA's sums alive until every CTA of the cluster has read them
+      cluster_sync();
+    }
+  };
+  if (half == 0)
+    run(std::integral_constant<int, NTH0>{});
+  else
+    run(std::integral_constant<int, NT - NTH0>{});
 }
 
 size_t smem_bytes(int kr, int nt, bool rows_mode) {
@@ -398,6 +422,13 @@ size_t smem_bytes(int kr, int nt, bool rows_mode) {
 template <int NT, bool EMIT, bool ROWS>
 cudaError_t grant_smem(size_t smem) {
   static size_t granted = 0;
+  static bool non_portable = false;
+  if (!non_portable) {
+    cudaError_t e = cudaFuncSetAttribute(matmul_q8_0_narrow_kernel<NT, EMIT, ROWS>,
+                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    non_portable = true;
+  }
   if (smem <= granted) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(matmul_q8_0_narrow_kernel<NT, EMIT, ROWS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -510,7 +541,7 @@ Plan matmul_plan(int64_t rows, int64_t cols, int num_sms) {
   for (int i = 0; i < n_memo; ++i)
     if (memo[i].rows == rows && memo[i].cols == cols) return memo[i].plan;
   const int nks = (int)(cols / 256);
-  int s_max = nks < 8 ? nks : 8;
+  int s_max = nks < kMaxCluster ? nks : kMaxCluster;
   int s_min = (nks + 7) / 8;
   if (s_min > s_max) s_min = s_max;
   if (s_min < 1) s_min = 1;
