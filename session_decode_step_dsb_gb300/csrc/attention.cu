@@ -15,18 +15,25 @@
 // shared buffer and gives up past ~31k compressed rows ("Known limitation");
 // here the keys of each (sequence, kv head) are cut into DSB_ATTN_CHUNK = 128
 // key chunks, so long contexts and b = 1 both fill the 152 SMs:
-//  * partial kernel, one CTA per (sequence, chunk, kv head): the V chunk is
-//    brought into shared memory by one 1-D TMA bulk copy (contiguous in the
-//    [F][Hkv][C][D] cache) while the CTA computes scores; thread k owns key k,
-//    holds its K row in registers (16-byte read-only loads) and dots it against
-//    the G*T query rows of the GQA group, which are read from shared memory by
-//    broadcast.  Every K/V byte is read once for all G*T query rows.  Per row
-//    it writes (max, sum of exp, sum of exp * V) for the chunk.
+//  * partial kernel, a persistent CTA loop over work items (sequence, chunk,
+//    kv head).  The chunk's K and V rows (contiguous in the cache) come in by
+//    TMA tensor copies with the 128-byte swizzle, in 64-key boxes, so thread k
+//    reads key k's row 16 bytes at a time without bank conflicts while the
+//    query rows are read by broadcast; the next item's K and V are requested
+//    as soon as this item is done with the buffers.  Thread k dots key k
+//    against the G*T query rows of the GQA group (packed f32x2 FMAs); the
+//    chunk's per-row max and sum of exp are block reductions in a fixed
+//    order; for P.V warp w takes keys 32w..32w+31 and each lane 4 (or 2)
+//    dimensions, reading the probabilities key-major (four rows per load),
+//    and the four warps' sums are added in warp order.  Every K/V byte is read
+//    once for all G*T query rows.  Per row it writes (max, sum of exp,
+//    sum of exp * V) for the chunk.
 //  * merge kernel, one warp per (token row, head): rescales the chunk partials
 //    by exp(m_c - max_c m_c) and adds them in chunk order.
 // No atomics and no inter-CTA waits; the chunking depends only on each
 // sequence's own length, so a sequence's rows are bitwise equal whether it runs
 // alone or inside a batch.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -43,60 +50,82 @@ namespace {
 
 constexpr int kCh = 128;  // keys per chunk (DSB_ATTN_CHUNK)
 constexpr int kThreads = 128;
+constexpr int kWarps = kThreads / 32;
 // Query rows handled together in the score and P.V loops: the widest row
 // group is 8, and each launch takes the narrowest power of two >= G*T, so a
 // one-row item (MHA, T = 1) issues no predicated-off work for absent rows.
 constexpr int kMaxRowGroup = 8;
+constexpr int kBoxCols = 64;                   // elements per swizzled 128-byte row
+constexpr int kBoxKeys = 64;                   // keys per TMA box
+constexpr int kBoxBytes = kBoxKeys * 128;      // 8 KiB
+constexpr int kColBoxBytes = kCh * 128;        // one 64-column slab of a chunk: 16 KiB
 
 __device__ unsigned int g_err_attention = 0;
+
+// Byte offset of 16-byte piece j (elements 8j..8j+7) of key k's row in a
+// chunk tile [D/64][128 keys][128 bytes] written by TMA with the 128-byte
+// swizzle: the piece index within a 128-byte row is XORed with k mod 8.
+__device__ __forceinline__ uint32_t swz(int k, int j) {
+  return (uint32_t)((j >> 3) * kColBoxBytes + k * 128 + (((j & 7) ^ (k & 7)) << 4));
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ unsigned long long pack2(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(unsigned long long v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ unsigned long long fma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
 
 template <typename T>
 struct Cvt;
 template <>
 struct Cvt<__half> {
   static __device__ __forceinline__ float2 two(uint32_t w) { return __half22float2(*reinterpret_cast<__half2*>(&w)); }
+  static __device__ __forceinline__ unsigned long long two_packed(uint32_t w) {
+    const float2 f = two(w);
+    return pack2(f.x, f.y);
+  }
 };
 template <>
 struct Cvt<__nv_bfloat16> {
   static __device__ __forceinline__ float2 two(uint32_t w) {
     return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w));
   }
+  // bf16 -> f32 is exact: the bf16 bits are the float's top half
+  static __device__ __forceinline__ unsigned long long two_packed(uint32_t w) {
+    return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  }
 };
 
-template <int D, typename T, int kRowGroup>
-__global__ void __launch_bounds__(kThreads) attention_partial_kernel(
-    const float* __restrict__ q, long long q_stride, int n_q_heads, const T* kc, const T* __restrict__ vc,
-    int n_kv_heads,
-    int ctx, const int32_t* __restrict__ batch_index, const int32_t* __restrict__ seq_lens,
-    const int32_t* __restrict__ chunk_off, int n_seq, int tps, int max_chunks, float scale,
-    float* __restrict__ partials, const PagedView pv) {
-  constexpr int NPAIR = D / 2;
-  constexpr int NPART = kThreads / NPAIR;
-  constexpr int KPP = kCh / NPART;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int G = n_q_heads / n_kv_heads, R = G * tps;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_wait();  // q and the cache rows of this step come from the previous kernels
-  pdl_trigger();
+// Work item -> (sequence, relative chunk, kv head), its first key, key count
+// and first cache row (contiguous cache or paged pool).
+struct Item {
+  int s, c_rel, g, key0, nkeys, L, W;
+  long long row0;
+};
 
-  T* Vs = reinterpret_cast<T*>(smem);                                        // [kCh][D]
-  float* qs = reinterpret_cast<float*>(smem + (size_t)kCh * D * sizeof(T));  // [R][D]
-  float* ps = qs + (size_t)R * D;                                            // [R][kCh]
-  float* ms = ps + (size_t)R * kCh;                                          // [R]
-  float* ls = ms + R;                                                        // [R]
-  float* red = ls + R;                                                       // [NPART-1][kRowGroup][D]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(red + (NPART - 1) * kRowGroup * D);
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
-
-  // Persistent loop over work items (chunk, kv head); the item count comes
-  // from the device metadata, so a captured launch serves any seq_lens.
-  const int total_items = chunk_off[n_seq] * n_kv_heads;
-  uint32_t phase = 0;
-  for (int item = blockIdx.x; item < total_items; item += gridDim.x, phase ^= 1u) {
-  const int w = item / n_kv_heads, g = item - w * n_kv_heads;
+__device__ __forceinline__ Item decode_item(int item, int n_kv_heads, int ctx, const int32_t* batch_index,
+                                            const int32_t* seq_lens, const int32_t* chunk_off, int n_seq, int tps,
+                                            const PagedView& pv) {
+  Item it;
+  const int w = item / n_kv_heads;
+  it.g = item - w * n_kv_heads;
   int lo = 0, hi = n_seq - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -105,169 +134,245 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
     else
       hi = mid - 1;
   }
-  const int s = lo, c_rel = w - chunk_off[s];  // c_rel: this sequence's chunk, counted from its first
-  const int L = seq_lens[s];
+  it.s = lo;
+  it.c_rel = w - chunk_off[lo];  // this sequence's chunk, counted from its first
+  it.L = seq_lens[lo];
   // Paged view: chunk c lives in one page (128 keys), found through the
   // block table (modulo the block count for a ring); a window hides keys
   // older than pos - W + 1, so the first chunks of a long ring are skipped.
-  const int W = pv.block_table ? pv.window[s] : 0;
-  const int c = (W > 0 ? max(0, L - tps + 1 - W) / kCh : 0) + c_rel;
-  const int key0 = c * kCh;
-  const int nkeys = min(kCh, L - key0);
-  size_t chunk_row0;  // cache row of key key0 (rows of a chunk are consecutive)
+  it.W = pv.block_table ? pv.window[lo] : 0;
+  const int c = (it.W > 0 ? max(0, it.L - tps + 1 - it.W) / kCh : 0) + it.c_rel;
+  it.key0 = c * kCh;
+  it.nkeys = min(kCh, it.L - it.key0);
   if (pv.block_table) {
-    const int nb = pv.n_blocks[s];
-    const int page = pv.block_table[(size_t)s * pv.max_blocks + (W > 0 ? c % nb : c)];
-    chunk_row0 = ((size_t)page * n_kv_heads + g) * kCh;
+    const int nb = pv.n_blocks[lo];
+    const int page = pv.block_table[(size_t)lo * pv.max_blocks + (it.W > 0 ? c % nb : c)];
+    it.row0 = ((long long)page * n_kv_heads + it.g) * kCh;
   } else {
-    chunk_row0 = ((size_t)batch_index[s] * n_kv_heads + g) * (size_t)ctx + key0;
+    it.row0 = ((long long)batch_index[lo] * n_kv_heads + it.g) * (long long)ctx + it.key0;
   }
-  __syncthreads();  // the previous item is done with every shared buffer
+  return it;
+}
+
+// One thread issues the chunk's K and V boxes (64-key boxes, only as many as
+// hold its keys) on the two barriers.
+template <int D>
+__device__ __forceinline__ void issue_chunk(const Item& it, const CUtensorMap* tmk, const CUtensorMap* tmv, uint8_t* Ks,
+                                            uint8_t* Vs, uint64_t* bar_k, uint64_t* bar_v) {
+  const int halves = it.nkeys > kBoxKeys ? 2 : 1;
+  const uint32_t bytes = (uint32_t)((D / kBoxCols) * halves * kBoxBytes);
+  mbar_arrive_expect_tx(bar_k, bytes);
+  mbar_arrive_expect_tx(bar_v, bytes);
+#pragma unroll
+  for (int cb = 0; cb < D / kBoxCols; ++cb)
+    for (int h = 0; h < halves; ++h)
+      tma_load_2d(Ks + cb * kColBoxBytes + h * kBoxBytes, tmk, cb * kBoxCols, (int)(it.row0 + h * kBoxKeys), bar_k);
+#pragma unroll
+  for (int cb = 0; cb < D / kBoxCols; ++cb)
+    for (int h = 0; h < halves; ++h)
+      tma_load_2d(Vs + cb * kColBoxBytes + h * kBoxBytes, tmv, cb * kBoxCols, (int)(it.row0 + h * kBoxKeys), bar_v);
+}
+
+template <int D, typename T, int kRowGroup>
+__global__ void __launch_bounds__(kThreads) attention_partial_kernel(
+    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const float* __restrict__ q,
+    long long q_stride, int n_q_heads, int n_kv_heads, int ctx, const int32_t* __restrict__ batch_index,
+    const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ chunk_off, int n_seq, int tps, int max_chunks,
+    float scale, float* __restrict__ partials, const PagedView pv) {
+  constexpr int NJ = D / 8;  // 16-byte pieces of a key row
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int G = n_q_heads / n_kv_heads, R = G * tps;
+  const int RP = (R + 3) & ~3;  // key-major probability row stride
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // Shared layout (the swizzled tiles need 1024-byte alignment):
+  // Ks | Vs [D/64][128][128 B] | qs [R][D] | ps [128][RP] | wstat [2][warps][8] |
+  // ms, ls [R] | barriers.  After the scores Ks holds the P.V warp sums.
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Ks = smem;
+  uint8_t* Vs = Ks + (size_t)D * kCh * sizeof(T);
+  float* qs = reinterpret_cast<float*>(Vs + (size_t)D * kCh * sizeof(T));
+  float* ps = qs + (size_t)R * D;
+  float* wstat = ps + (size_t)kCh * RP;
+  float* ms = wstat + 2 * kWarps * kRowGroup;
+  float* ls = ms + R;
+  uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(ls + R) + 7) & ~uintptr_t(7));
+  float* red = reinterpret_cast<float*>(Ks);  // [warps][kRowGroup][D], reused after the scores
   if (tid == 0) {
-    const uint32_t bytes = (uint32_t)nkeys * D * sizeof(T);
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_g2s(Vs, vc + chunk_row0 * D, bytes, bar);
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
   }
-  // Thread tid owns key key0 + tid: its K row goes into registers first, so
-  // that the K loads and the q staging below are in flight together.
-  uint4 kreg[D / 8];
-  if (tid < nkeys) {
-    const uint4* kp = reinterpret_cast<const uint4*>(kc + (chunk_row0 + tid) * D);
-#pragma unroll
-    for (int cc = 0; cc < D / 8; ++cc) kreg[cc] = ld_v4(kp + cc);  // this step's rows were written by the previous kernel
-  } else {
-#pragma unroll
-    for (int cc = 0; cc < D / 8; ++cc) kreg[cc] = make_uint4(0, 0, 0, 0);
-  }
-  for (int idx = tid; idx < R * D; idx += kThreads) {
-    const int r = idx / D, d = idx - r * D;
-    const int j = r / G, gi = r - j * G;
-    qs[idx] = __ldcg(q + (size_t)(s * tps + j) * q_stride + (size_t)(g * G + gi) * D + d);
-  }
-  __syncthreads();
+  pdl_wait();  // q and the cache rows of this step come from the previous kernels
+  pdl_trigger();
 
-  // ---- scores
-  {
-    for (int r0 = 0; r0 < R; r0 += kRowGroup) {
-      float dot[kRowGroup];
-#pragma unroll
-      for (int r = 0; r < kRowGroup; ++r) dot[r] = 0.0f;
-#pragma unroll
-      for (int cc = 0; cc < D / 8; ++cc) {
-        float kf[8];
-        const float2 k01 = Cvt<T>::two(kreg[cc].x), k23 = Cvt<T>::two(kreg[cc].y);
-        const float2 k45 = Cvt<T>::two(kreg[cc].z), k67 = Cvt<T>::two(kreg[cc].w);
-        kf[0] = k01.x; kf[1] = k01.y; kf[2] = k23.x; kf[3] = k23.y;
-        kf[4] = k45.x; kf[5] = k45.y; kf[6] = k67.x; kf[7] = k67.y;
-#pragma unroll
-        for (int r = 0; r < kRowGroup; ++r) {
-          if (r0 + r < R) {
-            const float4 qa = *reinterpret_cast<const float4*>(qs + (size_t)(r0 + r) * D + cc * 8);
-            const float4 qb = *reinterpret_cast<const float4*>(qs + (size_t)(r0 + r) * D + cc * 8 + 4);
-            float a = dot[r];
-            a = __fmaf_rn(qa.x, kf[0], a); a = __fmaf_rn(qa.y, kf[1], a);
-            a = __fmaf_rn(qa.z, kf[2], a); a = __fmaf_rn(qa.w, kf[3], a);
-            a = __fmaf_rn(qb.x, kf[4], a); a = __fmaf_rn(qb.y, kf[5], a);
-            a = __fmaf_rn(qb.z, kf[6], a); a = __fmaf_rn(qb.w, kf[7], a);
-            dot[r] = a;
-          }
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < kRowGroup; ++r) {
-        if (r0 + r < R) {
-          const int j = (r0 + r) / G;
-          const int vis = L - tps + j + 1;          // keys before vis are visible to draft token j ...
-          const int vlo = W > 0 ? vis - W : 0;      // ... from vlo on under a window
-          const int key = key0 + tid;
-          ps[(size_t)(r0 + r) * kCh + tid] = (key < vis && key >= vlo) ? __fmul_rn(dot[r], scale) : -INFINITY;
-        }
-      }
-    }
-  }
-  __syncthreads();
-
-  // ---- chunk softmax statistics, one warp per row
-  for (int r = warp; r < R; r += kThreads / 32) {
-    float v[kCh / 32];
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kCh / 32; ++i) {
-      v[i] = ps[(size_t)r * kCh + lane + 32 * i];
-      m = fmaxf(m, v[i]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float l = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kCh / 32; ++i) {
-      const float p = (m == -INFINITY) ? 0.0f : expf(v[i] - m);
-      ps[(size_t)r * kCh + lane + 32 * i] = p;
-      l = __fadd_rn(l, p);
-    }
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, o));
-    if (lane == 0) {
-      ms[r] = m;
-      ls[r] = l;
-    }
-  }
-  const bool ok = mbar_wait(bar, phase);
-  if (!ok) g_err_attention = 1u;
-  __syncthreads();
-
-  // ---- P V: thread = (pair of dims, key part); parts added in order
-  const int pr = tid % NPAIR, part = tid / NPAIR;
-  for (int r0 = 0; r0 < R; r0 += kRowGroup) {
-    float a0[kRowGroup], a1[kRowGroup];
-#pragma unroll
-    for (int r = 0; r < kRowGroup; ++r) a0[r] = a1[r] = 0.0f;
-    for (int kk = 0; kk < KPP; ++kk) {
-      const int key = part * KPP + kk;
-      if (key < nkeys) {
-        const float2 vf = Cvt<T>::two(*reinterpret_cast<const uint32_t*>(Vs + (size_t)key * D + 2 * pr));
-#pragma unroll
-        for (int r = 0; r < kRowGroup; ++r) {
-          if (r0 + r < R) {
-            const float p = ps[(size_t)(r0 + r) * kCh + key];
-            a0[r] = __fmaf_rn(p, vf.x, a0[r]);
-            a1[r] = __fmaf_rn(p, vf.y, a1[r]);
-          }
-        }
-      }
-    }
-    if (part > 0) {
-#pragma unroll
-      for (int r = 0; r < kRowGroup; ++r) {
-        red[((part - 1) * kRowGroup + r) * D + 2 * pr] = a0[r];
-        red[((part - 1) * kRowGroup + r) * D + 2 * pr + 1] = a1[r];
-      }
+  // Persistent loop over work items (chunk, kv head); the item count comes
+  // from the device metadata, so a captured launch serves any seq_lens.
+  const int total_items = chunk_off[n_seq] * n_kv_heads;
+  if (tid == 0 && (int)blockIdx.x < total_items)
+    issue_chunk<D>(decode_item(blockIdx.x, n_kv_heads, ctx, batch_index, seq_lens, chunk_off, n_seq, tps, pv), &tmk,
+                   &tmv, Ks, Vs, &bars[0], &bars[1]);
+  uint32_t phase = 0;
+  for (int item = blockIdx.x; item < total_items; item += gridDim.x, phase ^= 1u) {
+    const Item it = decode_item(item, n_kv_heads, ctx, batch_index, seq_lens, chunk_off, n_seq, tps, pv);
+    for (int idx = tid; idx < R * D; idx += kThreads) {
+      const int r = idx / D, d = idx - r * D;
+      const int j = r / G, gi = r - j * G;
+      qs[idx] = __ldcg(q + (size_t)(it.s * tps + j) * q_stride + (size_t)(it.g * G + gi) * D + d);
     }
     __syncthreads();
-    if (part == 0) {
+    if (!mbar_wait(&bars[0], phase)) g_err_attention = 1u;
+
+    // ---- scores and the chunk's softmax statistics, row group by row group
+    const int k = tid;
+    for (int r0 = 0; r0 < R; r0 += kRowGroup) {
+      unsigned long long dot2[kRowGroup];
+#pragma unroll
+      for (int r = 0; r < kRowGroup; ++r) dot2[r] = 0ull;
+#pragma unroll
+      for (int jj = 0; jj < NJ; ++jj) {
+        const uint4 kw = *reinterpret_cast<const uint4*>(Ks + swz(k, jj));
+        const unsigned long long k01 = Cvt<T>::two_packed(kw.x), k23 = Cvt<T>::two_packed(kw.y);
+        const unsigned long long k45 = Cvt<T>::two_packed(kw.z), k67 = Cvt<T>::two_packed(kw.w);
+#pragma unroll
+        for (int r = 0; r < kRowGroup; ++r) {
+          if (r0 + r < R) {
+            const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(qs + (size_t)(r0 + r) * D + jj * 8);
+            const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(qs + (size_t)(r0 + r) * D + jj * 8 + 4);
+            unsigned long long a = dot2[r];
+            a = fma2(qa.x, k01, a);
+            a = fma2(qa.y, k23, a);
+            a = fma2(qb.x, k45, a);
+            a = fma2(qb.y, k67, a);
+            dot2[r] = a;
+          }
+        }
+      }
+      float sc[kRowGroup];
 #pragma unroll
       for (int r = 0; r < kRowGroup; ++r) {
-        if (r0 + r < R) {
-          float x0 = a0[r], x1 = a1[r];
+        const float2 d2 = unpack2(dot2[r]);
+        const int j = (r0 + r) / G;
+        const int vis = it.L - tps + j + 1;          // keys before vis are visible to draft token j ...
+        const int vlo = it.W > 0 ? vis - it.W : 0;   // ... from vlo on under a window
+        const int key = it.key0 + k;
+        const bool ok = r0 + r < R && k < it.nkeys && key < vis && key >= vlo;
+        sc[r] = ok ? __fmul_rn(__fadd_rn(d2.x, d2.y), scale) : -INFINITY;
+      }
+      // row max over the chunk: xor tree in each warp, then the warps in order
 #pragma unroll
-          for (int pp = 1; pp < NPART; ++pp) {
-            x0 = __fadd_rn(x0, red[((pp - 1) * kRowGroup + r) * D + 2 * pr]);
-            x1 = __fadd_rn(x1, red[((pp - 1) * kRowGroup + r) * D + 2 * pr + 1]);
+      for (int r = 0; r < kRowGroup; ++r) {
+        float m = sc[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) wstat[warp * kRowGroup + r] = m;
+      }
+      __syncthreads();
+      float p[kRowGroup];
+#pragma unroll
+      for (int r = 0; r < kRowGroup; ++r) {
+        float M = wstat[r];
+#pragma unroll
+        for (int w2 = 1; w2 < kWarps; ++w2) M = fmaxf(M, wstat[w2 * kRowGroup + r]);
+        p[r] = (M == -INFINITY) ? 0.0f : expf(sc[r] - M);
+        if (tid == 0 && r0 + r < R) ms[r0 + r] = M;
+        float l = p[r];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, o));
+        if (lane == 0) wstat[kWarps * kRowGroup + warp * kRowGroup + r] = l;
+        if (r0 + r < R) ps[(size_t)k * RP + r0 + r] = p[r];
+      }
+      __syncthreads();
+      if (tid < kRowGroup && r0 + tid < R) {
+        float l = wstat[kWarps * kRowGroup + tid];
+#pragma unroll
+        for (int w2 = 1; w2 < kWarps; ++w2) l = __fadd_rn(l, wstat[kWarps * kRowGroup + w2 * kRowGroup + tid]);
+        ls[r0 + tid] = l;
+      }
+    }
+    if (!mbar_wait(&bars[1], phase)) g_err_attention = 1u;
+
+    // ---- P V: warp w takes keys 32w.., lane 4 (D = 128) or 2 (D = 64) dims
+    constexpr int DPL = D / 32;  // dimensions per lane
+    const int kb = warp * 32, ke = min(kb + 32, it.nkeys);
+    int vj, vsub;  // this lane's 16-byte piece of a V row and the byte within it
+    if constexpr (DPL == 4) {
+      vj = lane >> 1;          // 16-byte piece (0..15)
+      vsub = (lane & 1) * 8;   // byte within it
+    } else {
+      vj = lane >> 2;          // 0..7
+      vsub = (lane & 3) * 4;
+    }
+    for (int r0 = 0; r0 < R; r0 += kRowGroup) {
+      unsigned long long acc[kRowGroup][DPL / 2];
+#pragma unroll
+      for (int r = 0; r < kRowGroup; ++r)
+#pragma unroll
+        for (int e = 0; e < DPL / 2; ++e) acc[r][e] = 0ull;
+      for (int kk = kb; kk < ke; ++kk) {
+        const uint8_t* vp = Vs + swz(kk, vj) + vsub;
+        unsigned long long v2[DPL / 2];
+        if constexpr (DPL == 4) {
+          const uint2 vw = *reinterpret_cast<const uint2*>(vp);
+          v2[0] = Cvt<T>::two_packed(vw.x);
+          v2[1] = Cvt<T>::two_packed(vw.y);
+        } else {
+          v2[0] = Cvt<T>::two_packed(*reinterpret_cast<const uint32_t*>(vp));
+        }
+        const float* pk = ps + (size_t)kk * RP + r0;
+#pragma unroll
+        for (int r4 = 0; r4 < kRowGroup; r4 += 4) {
+          if (r0 + r4 < R) {
+            const float4 p4 = *reinterpret_cast<const float4*>(pk + r4);
+            const float pr[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+            for (int i = 0; i < 4 && r4 + i < kRowGroup; ++i) {
+              const unsigned long long pp = pack2(pr[i], pr[i]);
+#pragma unroll
+              for (int e = 0; e < DPL / 2; ++e) acc[r4 + i][e] = fma2(pp, v2[e], acc[r4 + i][e]);
+            }
           }
+        }
+      }
+      // the warps' sums, added in warp order (red overlays Ks: every thread is
+      // past the scores)
+#pragma unroll
+      for (int r = 0; r < kRowGroup; ++r) {
+        float* dst = red + ((size_t)warp * kRowGroup + r) * D + lane * DPL;
+        if constexpr (DPL == 4) {
+          const float2 a = unpack2(acc[r][0]), b = unpack2(acc[r][1]);
+          *reinterpret_cast<float4*>(dst) = make_float4(a.x, a.y, b.x, b.y);
+        } else {
+          *reinterpret_cast<float2*>(dst) = unpack2(acc[r][0]);
+        }
+      }
+      __syncthreads();
+      for (int idx = tid; idx < kRowGroup * D; idx += kThreads) {
+        const int r = idx / D, d = idx - r * D;
+        if (r0 + r < R) {
+          float x = red[idx];
+#pragma unroll
+          for (int w2 = 1; w2 < kWarps; ++w2) x = __fadd_rn(x, red[(size_t)w2 * kRowGroup * D + idx]);
           const int j = (r0 + r) / G, gi = (r0 + r) - j * G;
-          const int t = s * tps + j, h = g * G + gi;
-          float* dst = partials + (((size_t)t * n_q_heads + h) * max_chunks + c_rel) * (D + 2);
-          dst[2 + 2 * pr] = x0;
-          dst[3 + 2 * pr] = x1;
-          if (pr == 0) {
+          const int t = it.s * tps + j, h = it.g * G + gi;
+          float* dst = partials + (((size_t)t * n_q_heads + h) * max_chunks + it.c_rel) * (D + 2);
+          dst[2 + d] = x;
+          if (d == 0) {
             dst[0] = ms[r0 + r];
             dst[1] = ls[r0 + r];
           }
         }
       }
+      fence_proxy_async_smem();  // these generic accesses of Ks / Vs precede the next TMA writes
+      __syncthreads();
     }
-    __syncthreads();
-  }
+    // both buffers are free: request the next item's K and V
+    const int next = item + gridDim.x;
+    if (tid == 0 && next < total_items)
+      issue_chunk<D>(decode_item(next, n_kv_heads, ctx, batch_index, seq_lens, chunk_off, n_seq, tps, pv), &tmk, &tmv,
+                     Ks, Vs, &bars[0], &bars[1]);
   }  // work items
 }
 
@@ -332,21 +437,70 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
 
 template <int D, typename T, int kRowGroup>
 size_t partial_smem(int R) {
-  constexpr int NPART = kThreads / (D / 2);
-  return (size_t)kCh * D * sizeof(T) + (size_t)R * D * 4 + (size_t)R * kCh * 4 + (size_t)2 * R * 4 +
-         (size_t)(NPART - 1) * kRowGroup * D * 4 + 16;
+  const int RP = (R + 3) & ~3;
+  return 1024 + 2 * (size_t)kCh * D * sizeof(T) + (size_t)R * D * 4 + (size_t)kCh * RP * 4 +
+         (size_t)2 * kWarps * kRowGroup * 4 + (size_t)2 * R * 4 + 8 + 2 * 8;
+}
+
+// Tensor maps of the K and V caches viewed as [rows][D] 16-bit elements, with
+// 64-column x 64-key boxes and the 128-byte swizzle.  Encoded on the host
+// (no device work) and cached by address and shape.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+cudaError_t kv_tensor_map(const void* base, long long rows, int D, int dtype, CUtensorMap* out) {
+  struct Entry {
+    const void* base;
+    long long rows;
+    int D, dtype;
+    CUtensorMap map;
+  };
+  static Entry cache[16];
+  static int n_cache = 0, next_slot = 0;
+  static EncodeTiledFn encode = nullptr;
+  for (int i = 0; i < n_cache; ++i)
+    if (cache[i].base == base && cache[i].rows == rows && cache[i].D == D && cache[i].dtype == dtype) {
+      *out = cache[i].map;
+      return cudaSuccess;
+    }
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBoxCols, (cuuint32_t)kBoxKeys};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  const CUresult r = encode(&m, dtype == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const int slot = n_cache < 16 ? n_cache++ : (next_slot++ & 15);
+  cache[slot] = Entry{base, rows, D, dtype, m};
+  *out = m;
+  return cudaSuccess;
 }
 
 template <int D, typename T, int kRowGroup>
-cudaError_t launch_rg(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc,
-                         int n_kv_heads, int ctx,
-                         MetaView meta, int n_seq, int tps, long long max_items, int max_chunks, float* partials,
-                         float* out, void* xq_out, PagedView pv, cudaStream_t st) {
+cudaError_t launch_rg(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc, int dtype,
+                      int n_kv_heads, int ctx, long long kv_rows, MetaView meta, int n_seq, int tps,
+                      long long max_items, int max_chunks, float* partials, float* out, void* xq_out, PagedView pv,
+                      cudaStream_t st) {
   const int R = (n_q_heads / n_kv_heads) * tps;
   const size_t smem = partial_smem<D, T, kRowGroup>(R);
   auto kern = attention_partial_kernel<D, T, kRowGroup>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  CUtensorMap tmk, tmv;
+  if ((e = kv_tensor_map(kc, kv_rows, D, dtype, &tmk)) != cudaSuccess) return e;
+  if ((e = kv_tensor_map(vc, kv_rows, D, dtype, &tmv)) != cudaSuccess) return e;
   const float scale = (float)(1.0 / sqrt((double)D));
   // Persistent grid: as many CTAs as fit at once, capped by the item count.
   static int resident = 0;
@@ -364,9 +518,8 @@ cudaError_t launch_rg(const float* q, long long q_stride, int n_q_heads, const v
   }
   const long long items = (long long)max_items;
   const unsigned grid = (unsigned)(items < resident ? (items > 0 ? items : 1) : resident);
-  e = launch_kernel(kern, dim3(grid), dim3(kThreads), smem, st, q, q_stride, n_q_heads, static_cast<const T*>(kc),
-                    static_cast<const T*>(vc), n_kv_heads, ctx, meta.batch_index, meta.seq_lens, meta.chunk_off,
-                    n_seq, tps, max_chunks, scale, partials, pv);
+  e = launch_kernel(kern, dim3(grid), dim3(kThreads), smem, st, tmk, tmv, q, q_stride, n_q_heads, n_kv_heads, ctx,
+                    meta.batch_index, meta.seq_lens, meta.chunk_off, n_seq, tps, max_chunks, scale, partials, pv);
   if (e != cudaSuccess) return e;
   const int n_tok = n_seq * tps;
   const unsigned mgrid = (unsigned)((n_tok * n_q_heads + 3) / 4);
@@ -378,21 +531,22 @@ cudaError_t launch_rg(const float* q, long long q_stride, int n_q_heads, const v
 }
 
 template <int D, typename T>
-cudaError_t launch_typed(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc,
-                         int n_kv_heads, int ctx, MetaView meta, int n_seq, int tps, long long max_items,
-                         int max_chunks, float* partials, float* out, void* xq_out, PagedView pv, cudaStream_t st) {
+cudaError_t launch_typed(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc, int dtype,
+                         int n_kv_heads, int ctx, long long kv_rows, MetaView meta, int n_seq, int tps,
+                         long long max_items, int max_chunks, float* partials, float* out, void* xq_out, PagedView pv,
+                         cudaStream_t st) {
   const int R = (n_q_heads / n_kv_heads) * tps;
   if (R <= 1)
-    return launch_rg<D, T, 1>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tps, max_items,
-                              max_chunks, partials, out, xq_out, pv, st);
+    return launch_rg<D, T, 1>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
+                              max_items, max_chunks, partials, out, xq_out, pv, st);
   if (R <= 2)
-    return launch_rg<D, T, 2>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tps, max_items,
-                              max_chunks, partials, out, xq_out, pv, st);
+    return launch_rg<D, T, 2>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
+                              max_items, max_chunks, partials, out, xq_out, pv, st);
   if (R <= 4)
-    return launch_rg<D, T, 4>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tps, max_items,
-                              max_chunks, partials, out, xq_out, pv, st);
-  return launch_rg<D, T, kMaxRowGroup>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tps,
-                                       max_items, max_chunks, partials, out, xq_out, pv, st);
+    return launch_rg<D, T, 4>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
+                              max_items, max_chunks, partials, out, xq_out, pv, st);
+  return launch_rg<D, T, kMaxRowGroup>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq,
+                                       tps, max_items, max_chunks, partials, out, xq_out, pv, st);
 }
 
 }  // namespace
@@ -403,24 +557,26 @@ size_t attention_partial_bytes(int n_tok, int n_q_heads, int head_dim, int ctx) 
 }
 
 cudaError_t launch_attention_decode_multi(const float* q, long long q_stride, int n_q_heads, const void* kc,
-                                          const void* vc, int dtype,
-                                          int n_kv_heads, int ctx, int head_dim, MetaView meta, int n_seq,
-                                          int tokens_per_seq, long long max_items, int max_chunks, float* partials,
-                                          float* out, void* xq_out, cudaStream_t st, PagedView pv) {
+                                          const void* vc, int dtype, int n_kv_heads, int ctx, int head_dim,
+                                          long long kv_rows, MetaView meta, int n_seq, int tokens_per_seq,
+                                          long long max_items, int max_chunks, float* partials, float* out,
+                                          void* xq_out, cudaStream_t st, PagedView pv) {
   if (n_seq == 0) return cudaSuccess;
   if (head_dim == 128) {
     if (dtype == 0)
-      return launch_typed<128, __half>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
-                                       max_items, max_chunks, partials, out, xq_out, pv, st);
-    return launch_typed<128, __nv_bfloat16>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
-                                            max_items, max_chunks, partials, out, xq_out, pv, st);
+      return launch_typed<128, __half>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq,
+                                       tokens_per_seq, max_items, max_chunks, partials, out, xq_out, pv, st);
+    return launch_typed<128, __nv_bfloat16>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta,
+                                            n_seq, tokens_per_seq, max_items, max_chunks, partials, out, xq_out, pv,
+                                            st);
   }
   if (head_dim == 64) {
     if (dtype == 0)
-      return launch_typed<64, __half>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
-                                      max_items, max_chunks, partials, out, xq_out, pv, st);
-    return launch_typed<64, __nv_bfloat16>(q, q_stride, n_q_heads, kc, vc, n_kv_heads, ctx, meta, n_seq, tokens_per_seq,
-                                           max_items, max_chunks, partials, out, xq_out, pv, st);
+      return launch_typed<64, __half>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq,
+                                      tokens_per_seq, max_items, max_chunks, partials, out, xq_out, pv, st);
+    return launch_typed<64, __nv_bfloat16>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta,
+                                           n_seq, tokens_per_seq, max_items, max_chunks, partials, out, xq_out, pv,
+                                           st);
   }
   return cudaErrorInvalidValue;
 }

@@ -460,7 +460,8 @@ static dsb_status attention_common(const float* q, int n_q_heads, const dsb_kv_c
   dsbk::MetaView mv{dev, dev + n_seq, dev + 2 * n_seq, nullptr};
   const int max_chunks = (kv->ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
   cudaError_t e = dsbk::launch_attention_decode_multi(
-      q, (long long)n_q_heads * kv->head_dim, n_q_heads, kv->k, kv->v, kv->dtype, kv->n_kv_heads, kv->ctx, kv->head_dim, mv, n_seq, tokens_per_seq,
+      q, (long long)n_q_heads * kv->head_dim, n_q_heads, kv->k, kv->v, kv->dtype, kv->n_kv_heads, kv->ctx, kv->head_dim,
+      (long long)kv->full_batch_size * kv->n_kv_heads * kv->ctx, mv, n_seq, tokens_per_seq,
       total * kv->n_kv_heads, max_chunks, reinterpret_cast<float*>(partial_base(ws)), out, xq, cs);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "attention_decode_multi launch");
 }
@@ -619,7 +620,7 @@ dsb_status dsb_attention_decode_paged(const float* q, int n_q_heads, const dsb_k
   pv.window = pv.n_blocks + n_seq;
   cudaError_t e = dsbk::launch_attention_decode_multi(
       q, (long long)n_q_heads * kv->head_dim, n_q_heads, kv->k, kv->v, kv->dtype, kv->n_kv_heads, 0, kv->head_dim,
-      mv, n_seq, tokens_per_seq, total * kv->n_kv_heads, max_chunks, reinterpret_cast<float*>(partial_base(ws)), out,
+      (long long)kv->n_pages * kv->n_kv_heads * DSB_KV_PAGE, mv, n_seq, tokens_per_seq, total * kv->n_kv_heads, max_chunks, reinterpret_cast<float*>(partial_base(ws)), out,
       nullptr, cs, pv);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "attention_decode_paged launch");
 }
@@ -911,6 +912,7 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
         cudaSuccess)
       break;
     if ((e = dsbk::launch_attention_decode_multi(qkv, qkv_stride, Hq, Ly.kv.k, Ly.kv.v, Ly.kv.dtype, Hkv, Ly.kv.ctx, D,
+                                                 (long long)Ly.kv.full_batch_size * Hkv * Ly.kv.ctx,
                                                  mv, n_seq, tps, max_items, max_chunks, partials, att, xq, st)) !=
         cudaSuccess)
       break;
@@ -1193,7 +1195,9 @@ extern "C" dsb_status dsb_attention_decode_multi_noalloc(const float* q, int n_q
   float* partials = reinterpret_cast<float*>(static_cast<char*>(scratch) + dsbk::kNoAllocTableBytes);
   const int max_chunks = (kv->ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
   e = dsbk::launch_attention_decode_multi(q, (long long)n_q_heads * kv->head_dim, n_q_heads, kv->k, kv->v, kv->dtype,
-                                          kv->n_kv_heads, kv->ctx, kv->head_dim, mv, n_seq, tokens_per_seq,
-                                          total * kv->n_kv_heads, max_chunks, partials, out, nullptr, cs);
+                                          kv->n_kv_heads, kv->ctx, kv->head_dim,
+                                          (long long)kv->full_batch_size * kv->n_kv_heads * kv->ctx, mv, n_seq,
+                                          tokens_per_seq, total * kv->n_kv_heads, max_chunks, partials, out, nullptr,
+                                          cs);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "attention_decode_multi_noalloc launch");
 }

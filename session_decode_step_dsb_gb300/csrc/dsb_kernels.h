@@ -121,11 +121,14 @@ cudaError_t launch_kv_scatter(void* kc, void* vc, int dtype, int n_kv_heads, int
 // With pv.block_table set, kc / vc are page pools and ctx is unused; a
 // sequence's work items are its chunks from the first one a window leaves
 // visible (meta.chunk_off counts those).
+// kv_rows: rows of the K / V tensors viewed as [kv_rows][head_dim] (F*Hkv*ctx
+// for a contiguous cache, n_pages*Hkv*128 for a page pool); the kernels read
+// them through TMA tensor maps of exactly that extent.
 cudaError_t launch_attention_decode_multi(const float* q, long long q_stride, int n_q_heads, const void* kc,
-                                          const void* vc, int dtype,
-                                          int n_kv_heads, int ctx, int head_dim, MetaView meta, int n_seq,
-                                          int tokens_per_seq, long long max_items, int max_chunks, float* partials,
-                                          float* out, void* xq_out, cudaStream_t st, PagedView pv = PagedView{});
+                                          const void* vc, int dtype, int n_kv_heads, int ctx, int head_dim,
+                                          long long kv_rows, MetaView meta, int n_seq, int tokens_per_seq,
+                                          long long max_items, int max_chunks, float* partials, float* out,
+                                          void* xq_out, cudaStream_t st, PagedView pv = PagedView{});
 // KV write through the paged view: token t of sequence t / T at pos[t].
 cudaError_t launch_kv_scatter_paged(void* kp, void* vp, int dtype, int n_kv_heads, int head_dim, PagedView pv,
                                     int tokens_per_seq, const int32_t* pos_dev, int n_tok, const float* k,
