@@ -27,7 +27,9 @@
 //    dimensions, reading the probabilities key-major (four rows per load),
 //    and the four warps' sums are added in warp order.  Every K/V byte is read
 //    once for all G*T query rows.  Per row it writes (max, sum of exp,
-//    sum of exp * V) for the chunk.
+//    sum of exp * V) for the chunk.  While an item is being computed, one
+//    thread decodes the next item and the query rows of the next item are
+//    loaded into registers, so an item starts with no dependent global reads.
 //  * merge kernel, one warp per (token row, head): rescales the chunk partials
 //    by exp(m_c - max_c m_c) and adds them in chunk order.
 // No atomics and no inter-CTA waits; the chunking depends only on each
@@ -197,6 +199,7 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
   float* ms = wstat + 2 * kWarps * kRowGroup;
   float* ls = ms + R;
   uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(ls + R) + 7) & ~uintptr_t(7));
+  Item* nx = reinterpret_cast<Item*>(bars + 2);  // the next item, decoded ahead by thread 0
   float* red = reinterpret_cast<float*>(Ks);  // [warps][kRowGroup][D], reused after the scores
   if (tid == 0) {
     mbar_init(&bars[0], 1);
@@ -211,18 +214,36 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
   // Persistent loop over work items (chunk, kv head); the item count comes
   // from the device metadata, so a captured launch serves any seq_lens.
   const int total_items = chunk_off[n_seq] * n_kv_heads;
-  if (tid == 0 && (int)blockIdx.x < total_items)
-    issue_chunk<D>(decode_item(blockIdx.x, n_kv_heads, ctx, batch_index, seq_lens, chunk_off, n_seq, tps, pv), &tmk,
-                   &tmv, Ks, Vs, &bars[0], &bars[1]);
+  // Query element idx of the item's [R][D] block, read from q.
+  auto q_elem = [&](const Item& x, int idx) {
+    const int r = idx / D, d = idx - r * D;
+    const int j = r / G, gi = r - j * G;
+    return __ldcg(q + (size_t)(x.s * tps + j) * q_stride + (size_t)(x.g * G + gi) * D + d);
+  };
+  constexpr int kQPre = 8;  // query elements per thread carried over from the previous item
+  float qpre[kQPre];
+  if ((int)blockIdx.x < total_items) {
+    const Item first = decode_item(blockIdx.x, n_kv_heads, ctx, batch_index, seq_lens, chunk_off, n_seq, tps, pv);
+    if (tid == 0) {
+      *nx = first;
+      issue_chunk<D>(first, &tmk, &tmv, Ks, Vs, &bars[0], &bars[1]);
+    }
+#pragma unroll
+    for (int i = 0; i < kQPre; ++i)
+      if (tid + i * kThreads < R * D) qpre[i] = q_elem(first, tid + i * kThreads);
+  }
+  __syncthreads();
   uint32_t phase = 0;
   for (int item = blockIdx.x; item < total_items; item += gridDim.x, phase ^= 1u) {
-    const Item it = decode_item(item, n_kv_heads, ctx, batch_index, seq_lens, chunk_off, n_seq, tps, pv);
-    for (int idx = tid; idx < R * D; idx += kThreads) {
-      const int r = idx / D, d = idx - r * D;
-      const int j = r / G, gi = r - j * G;
-      qs[idx] = __ldcg(q + (size_t)(it.s * tps + j) * q_stride + (size_t)(it.g * G + gi) * D + d);
-    }
+    const Item it = *nx;
+#pragma unroll
+    for (int i = 0; i < kQPre; ++i)
+      if (tid + i * kThreads < R * D) qs[tid + i * kThreads] = qpre[i];
+    for (int idx = tid + kQPre * kThreads; idx < R * D; idx += kThreads) qs[idx] = q_elem(it, idx);
     __syncthreads();
+    const int next = item + gridDim.x;
+    if (tid == 0 && next < total_items)
+      *nx = decode_item(next, n_kv_heads, ctx, batch_index, seq_lens, chunk_off, n_seq, tps, pv);
     if (!mbar_wait(&bars[0], phase)) g_err_attention = 1u;
 
     // ---- scores and the chunk's softmax statistics, row group by row group
@@ -291,6 +312,13 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
         for (int w2 = 1; w2 < kWarps; ++w2) l = __fadd_rn(l, wstat[kWarps * kRowGroup + w2 * kRowGroup + tid]);
         ls[r0 + tid] = l;
       }
+    }
+    // the next item's query rows (thread 0 decoded it before the barriers above)
+    if (next < total_items) {
+      const Item nxt = *nx;
+#pragma unroll
+      for (int i = 0; i < kQPre; ++i)
+        if (tid + i * kThreads < R * D) qpre[i] = q_elem(nxt, tid + i * kThreads);
     }
     if (!mbar_wait(&bars[1], phase)) g_err_attention = 1u;
 
@@ -369,10 +397,7 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
       __syncthreads();
     }
     // both buffers are free: request the next item's K and V
-    const int next = item + gridDim.x;
-    if (tid == 0 && next < total_items)
-      issue_chunk<D>(decode_item(next, n_kv_heads, ctx, batch_index, seq_lens, chunk_off, n_seq, tps, pv), &tmk, &tmv,
-                     Ks, Vs, &bars[0], &bars[1]);
+    if (tid == 0 && next < total_items) issue_chunk<D>(*nx, &tmk, &tmv, Ks, Vs, &bars[0], &bars[1]);
   }  // work items
 }
 
@@ -414,12 +439,25 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
       lsum = __fmaf_rn(wl, __ldcg(pc + 1), lsum);
     }
     const int n = min(32, nch - c0);
-#pragma unroll 4
-    for (int cc = 0; cc < n; ++cc) {
-      const float wc = __shfl_sync(0xffffffffu, wl, cc);
-      const float* pc = base + (size_t)(c0 + cc) * (D + 2) + 2;
+    // eight chunks' loads in flight, then their terms added in chunk order
+    for (int cb = 0; cb < n; cb += 8) {
+      float v[8][D / 32];
 #pragma unroll
-      for (int e = 0; e < D / 32; ++e) acc[e] = __fmaf_rn(wc, __ldcg(pc + lane + 32 * e), acc[e]);
+      for (int i = 0; i < 8; ++i) {
+        if (cb + i < n) {
+          const float* pc = base + (size_t)(c0 + cb + i) * (D + 2) + 2;
+#pragma unroll
+          for (int e = 0; e < D / 32; ++e) v[i][e] = __ldcg(pc + lane + 32 * e);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float wc = __shfl_sync(0xffffffffu, wl, (cb + i) & 31);
+        if (cb + i < n) {
+#pragma unroll
+          for (int e = 0; e < D / 32; ++e) acc[e] = __fmaf_rn(wc, v[i][e], acc[e]);
+        }
+      }
     }
   }
 #pragma unroll
@@ -439,7 +477,7 @@ template <int D, typename T, int kRowGroup>
 size_t partial_smem(int R) {
   const int RP = (R + 3) & ~3;
   return 1024 + 2 * (size_t)kCh * D * sizeof(T) + (size_t)R * D * 4 + (size_t)kCh * RP * 4 +
-         (size_t)2 * kWarps * kRowGroup * 4 + (size_t)2 * R * 4 + 8 + 2 * 8;
+         (size_t)2 * kWarps * kRowGroup * 4 + (size_t)2 * R * 4 + 8 + 2 * 8 + sizeof(Item);
 }
 
 // Tensor maps of the K and V caches viewed as [rows][D] 16-bit elements, with
