@@ -875,7 +875,8 @@ cudaError_t run_matmul(const dsb_q8_0_mat& w, const void* xq, int n_tok, float* 
 // copies to meta_dev (n_meta_words words) while it reads the token ids.
 dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, int tps, long long max_items,
                         float* logits, dsb_workspace* ws, int sms, cudaStream_t st, const int32_t* meta_src = nullptr,
-                        size_t n_meta_words = 0) {
+                        size_t n_meta_words = 0, const int32_t* meta_words = nullptr,
+                        dsbk::EmbedParamNode* embed_node = nullptr) {
   const dsb_model_shape& s = m->shape;
   const dsb_kv_cache& kv0 = m->layers[0].kv;
   const int n_tok = n_seq * tps;
@@ -900,8 +901,13 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
   fill_rope_freqs(s.rope, D, &freqs);
   // The first kernel follows the metadata copy; every later kernel may be
   // scheduled while its predecessor finishes (programmatic dependent launch).
-  cudaError_t e = dsbk::launch_embed(m->embed, s.hidden, meta_src ? meta_src : tokens_dev, n_tok, h, meta_src,
-                                     const_cast<int32_t*>(meta_dev), (int)n_meta_words, st);
+  // meta_words: host words passed in the first kernel's parameters (the
+  // captured step rewrites them per replay); meta_src: mapped host memory
+  // the first kernel reads; neither: the metadata is already at meta_dev.
+  cudaError_t e = meta_words ? dsbk::launch_embed_params(m->embed, s.hidden, n_tok, h, meta_words, (int)n_meta_words,
+                                                         const_cast<int32_t*>(meta_dev), st, embed_node)
+                             : dsbk::launch_embed(m->embed, s.hidden, meta_src ? meta_src : tokens_dev, n_tok, h,
+                                                  meta_src, const_cast<int32_t*>(meta_dev), (int)n_meta_words, st);
   dsbk::set_pdl(true);
   for (int l = 0; l < s.n_layers && e == cudaSuccess; ++l) {
     const dsb_layer& Ly = m->layers[l];
@@ -970,7 +976,34 @@ struct dsb_step_graph {
   cudaGraphExec_t exec = nullptr;
   cudaEvent_t done = nullptr;
   bool launched = false;
+  // Parameter-block mode (n_words <= kEmbedParamMaxWords): the metadata rides
+  // in the first kernel's parameters, rewritten per replay with
+  // cudaGraphExecKernelNodeSetParams; the GPU never reads host memory.
+  bool param_mode = false;
+  cudaGraphNode_t embed_node = nullptr;
+  dsbk::EmbedParamNode embed{};
+  const void* a_table = nullptr;
+  int a_hidden = 0;
+  long long a_n_blocks = 0;
+  float* a_h = nullptr;
+  int32_t* a_meta_dst = nullptr;
+  int a_n_words = 0;
+  std::vector<int32_t> a_words;  // capacity words: the parameter block
 };
+
+// The parameters of the graph's embedding node for the current words.
+static cudaError_t set_embed_node(dsb_step_graph* g) {
+  void* args[7] = {&g->a_table, &g->a_hidden, &g->a_n_blocks, &g->a_h, g->a_words.data(), &g->a_meta_dst,
+                   &g->a_n_words};
+  cudaKernelNodeParams p{};
+  p.func = const_cast<void*>(g->embed.func);
+  p.gridDim = dim3(g->embed.grid);
+  p.blockDim = dim3(g->embed.block);
+  p.sharedMemBytes = 0;
+  p.kernelParams = args;
+  p.extra = nullptr;
+  return cudaGraphExecKernelNodeSetParams(g->exec, g->embed_node, &p);
+}
 
 extern "C" {
 
@@ -1049,12 +1082,15 @@ dsb_status dsb_step_graph_create(const dsb_model* model, int n_seq, int tokens_p
   // Placeholder metadata for the capture: one chunk per sequence; the real
   // values are written before every launch.
   std::memset(g->pinned, 0, g->n_words * sizeof(int32_t));
+  g->param_mode = g->n_words <= (size_t)dsbk::kEmbedParamMaxWords;
+  std::vector<int32_t> zeros(g->n_words, 0);
+  const int32_t* words_arg = g->param_mode ? zeros.data() : nullptr;
   const long long max_items =
       (long long)n_seq * ((kv0->ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK) * model->shape.n_kv_heads;
   // Warm every launcher's one-time set-up outside the capture.
   dsbk::set_dry_run(true);
   dsb_status dry = enqueue_step(model, g->dev_meta, n_seq, tokens_per_seq, max_items, logits, ws, sms, cs,
-                                g->pinned_dev, g->n_words);
+                                g->pinned_dev, g->n_words, words_arg);
   dsbk::set_dry_run(false);
   if (dry != DSB_OK) {
     cudaStreamDestroy(cs);
@@ -1066,7 +1102,7 @@ dsb_status dsb_step_graph_create(const dsb_model* model, int n_seq, int tokens_p
   e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
   if (e == cudaSuccess) {
     const dsb_status es = enqueue_step(model, g->dev_meta, n_seq, tokens_per_seq, max_items, logits, ws, sms, cs,
-                                       g->pinned_dev, g->n_words);
+                                       g->pinned_dev, g->n_words, words_arg, &g->embed);
     cudaError_t e2 = cudaStreamEndCapture(cs, &g->graph);
     if (e == cudaSuccess && es != DSB_OK) {
       if (g->graph) cudaGraphDestroy(g->graph);
@@ -1080,7 +1116,27 @@ dsb_status dsb_step_graph_create(const dsb_model* model, int n_seq, int tokens_p
   }
   cudaStreamDestroy(cs);
   if (e == cudaSuccess) e = cudaGraphInstantiate(&g->exec, g->graph, 0);
+  if (e == cudaSuccess && g->param_mode) {
+    // the embedding kernel is the graph's single root node
+    size_t n_roots = 1;
+    cudaGraphNode_t root = nullptr;
+    e = cudaGraphGetRootNodes(g->graph, &root, &n_roots);
+    cudaGraphNodeType type = cudaGraphNodeTypeEmpty;
+    if (e == cudaSuccess && n_roots == 1) e = cudaGraphNodeGetType(root, &type);
+    if (e == cudaSuccess && (n_roots != 1 || type != cudaGraphNodeTypeKernel)) e = cudaErrorInvalidValue;
+    if (e == cudaSuccess) {
+      g->embed_node = root;
+      g->a_table = model->embed;
+      g->a_hidden = model->shape.hidden;
+      g->a_n_blocks = g->embed.n_blocks;
+      g->a_h = reinterpret_cast<float*>(ws->dev + L.h);
+      g->a_meta_dst = g->dev_meta;
+      g->a_n_words = (int)g->n_words;
+      g->a_words.assign((size_t)g->embed.capacity, 0);
+    }
+  }
   if (e != cudaSuccess) {
+    if (g->exec) cudaGraphExecDestroy(g->exec);
     if (g->graph) cudaGraphDestroy(g->graph);
     cudaEventDestroy(g->done);
     cudaFreeHost(g->pinned);
@@ -1101,7 +1157,15 @@ dsb_status dsb_step_graph_launch(dsb_step_graph* g, const int32_t* token_ids, co
   long long total = 0;
   std::vector<int32_t> words = step_words(token_ids, batch_index, g->n_seq, g->tps, seq_lens, &total);
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (words != g->last) {
+  if (g->param_mode) {
+    // the node's parameters are copied when set: no wait for the previous replay
+    if (words != g->last) {
+      std::copy(words.begin(), words.end(), g->a_words.begin());
+      cudaError_t e = set_embed_node(g);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGraphExecKernelNodeSetParams(step)");
+      g->last.swap(words);
+    }
+  } else if (words != g->last) {
     if (g->launched) {  // the previous replay may still be reading the pinned copy
       const auto t0 = std::chrono::steady_clock::now();
       for (;;) {

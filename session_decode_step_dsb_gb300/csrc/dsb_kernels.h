@@ -142,6 +142,25 @@ cudaError_t launch_silu_mul_quant(const float* gu, int n_tok, int ffn, void* xq,
 // tokens: device-readable token ids.  meta_src non-NULL: the kernel also
 // copies n_words words from meta_src (device-readable, e.g. mapped pinned
 // host memory) to meta_dst.
+// The step's metadata words as a kernel parameter block (N words).
+template <int N>
+struct StepMetaWords {
+  int32_t w[N];
+};
+constexpr int kEmbedParamMaxWords = 4096;  // 16 KiB of kernel parameters
+// What a captured launch of the parameter-block embedding needs to rebuild
+// its node parameters: the kernel, its launch shape and the block capacity.
+struct EmbedParamNode {
+  const void* func = nullptr;
+  unsigned grid = 0, block = 0;
+  long long n_blocks = 0;
+  int capacity = 0;
+};
+// Embedding gather with the step's n_words metadata words (tokens first)
+// passed by value in the kernel's parameters (n_words <= kEmbedParamMaxWords)
+// and copied to meta_dst; `node`, if given, receives the launch description.
+cudaError_t launch_embed_params(const void* table, int hidden, int n_tok, float* h, const int32_t* words, int n_words,
+                                int32_t* meta_dst, cudaStream_t st, EmbedParamNode* node = nullptr);
 cudaError_t launch_embed(const void* table, int hidden, const int32_t* tokens, int n_tok, float* h,
                          const int32_t* meta_src, int32_t* meta_dst, int n_words, cudaStream_t st);
 

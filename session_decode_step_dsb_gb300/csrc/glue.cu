@@ -111,7 +111,61 @@ __global__ void __launch_bounds__(kGlueThreads) embed_kernel(const uint8_t* __re
   h[(size_t)t * hidden + b * 32 + lane] = __fmul_rn(d, (float)q);
 }
 
+// The same gather with the step's metadata words carried in the kernel's own
+// parameter block (a captured step rewrites them per replay), so no kernel
+// reads host memory: the CTAs copy the n_words words to meta_dst for the
+// kernels that follow, and the token ids are its first n_tok words.
+template <int N>
+__global__ void __launch_bounds__(kGlueThreads) embed_param_kernel(const uint8_t* __restrict__ table, int hidden,
+                                                                   long long n_blocks, float* __restrict__ h,
+                                                                   const __grid_constant__ StepMetaWords<N> meta,
+                                                                   int32_t* meta_dst, int n_words) {
+  pdl_wait();
+  pdl_trigger();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_words; i += gridDim.x * blockDim.x) meta_dst[i] = meta.w[i];
+  const long long blk = (long long)blockIdx.x * (kGlueThreads / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (blk >= n_blocks) return;
+  const int per_row = hidden / 32;
+  const long long t = blk / per_row;
+  const int b = (int)(blk - t * per_row);
+  const uint8_t* src = table + ((size_t)meta.w[t] * per_row + b) * 34;
+  const unsigned short sbits = (unsigned short)(src[0] | (src[1] << 8));
+  const float d = __half2float(__ushort_as_half(sbits));
+  const int8_t q = (int8_t)src[2 + lane];
+  h[(size_t)t * hidden + b * 32 + lane] = __fmul_rn(d, (float)q);
+}
+
+template <int N>
+cudaError_t launch_embed_param_n(const uint8_t* table, int hidden, int n_tok, float* h, const int32_t* words,
+                                 int n_words, int32_t* meta_dst, cudaStream_t st, EmbedParamNode* node) {
+  const long long n_blocks = (long long)n_tok * (hidden / 32);
+  const unsigned grid = (unsigned)((n_blocks + 7) / 8);
+  if (node) {
+    node->func = reinterpret_cast<const void*>(embed_param_kernel<N>);
+    node->grid = grid;
+    node->block = kGlueThreads;
+    node->n_blocks = n_blocks;
+    node->capacity = N;
+  }
+  StepMetaWords<N> m;
+  for (int i = 0; i < N; ++i) m.w[i] = i < n_words ? words[i] : 0;
+  return launch_kernel(embed_param_kernel<N>, dim3(grid), dim3(kGlueThreads), 0, st, table, hidden, n_blocks, h, m,
+                       meta_dst, n_words);
+}
+
 }  // namespace
+
+cudaError_t launch_embed_params(const void* table, int hidden, int n_tok, float* h, const int32_t* words, int n_words,
+                                int32_t* meta_dst, cudaStream_t st, EmbedParamNode* node) {
+  if (n_tok == 0) return cudaSuccess;
+  const uint8_t* t8 = static_cast<const uint8_t*>(table);
+  if (n_words <= 256) return launch_embed_param_n<256>(t8, hidden, n_tok, h, words, n_words, meta_dst, st, node);
+  if (n_words <= 1024) return launch_embed_param_n<1024>(t8, hidden, n_tok, h, words, n_words, meta_dst, st, node);
+  if (n_words <= kEmbedParamMaxWords)
+    return launch_embed_param_n<kEmbedParamMaxWords>(t8, hidden, n_tok, h, words, n_words, meta_dst, st, node);
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_rmsnorm_quant(const float* x, const float* w, int n_tok, int hidden, float eps, void* xq,
                                  cudaStream_t st) {
