@@ -559,6 +559,52 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+PROBE_ATTENTION = {  # F, Hq, Hkv, ctx, D, cache dtype, b, T, shortest seq_len
+    "qwen3-14b": (16, 40, 8, 4096, 128, 1, 16, 1, 1),
+    "llama-68m": (8, 12, 12, 2048, 64, 0, 8, 1, 128),
+}
+
+
+def run_probe(spec: str):
+    """A few launches of one kernel at one shape, for a profiler to capture
+    (no timing, no JSON line): ``matmul:ROWS:COLS:NTOK[,NTOK...]`` runs the
+    narrow matmul three times per n_tok on N(0, 0.02) weights;
+    ``attention:WORKLOAD`` runs the decode attention four times on that
+    workload's cache shape (b sequences, seq_lens uniform)."""
+    import torch
+    from session_decode_step_dsb_gb300 import dsb
+    kind, *rest = spec.split(":")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4321)
+    if kind == "matmul":
+        rows, cols, nts = int(rest[0]), int(rest[1]), [int(v) for v in rest[2].split(",")]
+        w = dsb.quantize_q8_0(torch.randn((rows, cols), generator=g, device="cuda") * 0.02)
+        x = dsb.quantize_q8_0(torch.randn((16, cols), generator=g, device="cuda"))
+        for nt in nts:
+            xs = x[:nt].contiguous()
+            for _ in range(3):
+                dsb.matmul_q8_0_narrow(w, rows, cols, xs, nt)
+    elif kind == "attention":
+        F, hq, hkv, C, D, dt, b, T, lo = PROBE_ATTENTION[rest[0]]
+        cdt = torch.float16 if dt == 0 else torch.bfloat16
+        kc = torch.randn((F, hkv, C, D), generator=g, device="cuda").to(cdt).view(torch.int16)
+        vc = torch.randn((F, hkv, C, D), generator=g, device="cuda").to(cdt).view(torch.int16)
+        kv = dsb.kv_cache(kc, vc, dt)
+        rng = np.random.default_rng(3)
+        bi = rng.permutation(F)[:b].astype(np.int32)
+        lens = rng.integers(max(lo, T), C + 1, b).astype(np.int32)
+        q = torch.randn((b * T, hq, D), generator=g, device="cuda")
+        ws = dsb.Workspace(b * T, hq, D, C)
+        out = torch.empty_like(q)
+        for _ in range(4):
+            dsb.attention_decode_multi(q, kv, bi, T, lens, ws, out=out)
+    else:
+        raise SystemExit(f"unknown probe {spec!r}")
+    torch.cuda.synchronize()
+    dsb.device_error()
+    print("probe ok", spec)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -573,7 +619,13 @@ def main(argv=None):
     ap.add_argument("--no-matmul-sweep", action="store_true")
     ap.add_argument("--attn-sweep", action="store_true",
                     help="also time the split-K attention at ctx 32768/65536 (allocates ~70 GB)")
+    ap.add_argument("--probe", default=None,
+                    help="run one kernel a few times for a profiler and exit: matmul:ROWS:COLS:NTOK[,..] or "
+                         "attention:WORKLOAD")
     args = ap.parse_args(argv)
+    if args.probe:
+        run_probe(args.probe)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
