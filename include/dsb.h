@@ -316,6 +316,22 @@ dsb_status dsb_rmsnorm_q8_0(const float* x, const float* w, int n_tok, int hidde
  * xq: device q8_0 [n_tok][ffn/32]; ffn % 32 == 0. */
 dsb_status dsb_silu_mul_q8_0(const float* gu, int n_tok, int ffn, void* xq, void* stream);
 
+/* The narrow matmul with its activation quantisation in the same kernel: each
+ * CTA quantises the activation blocks of its own k-range from float rows, so
+ * no q8_0 activation array round-trips through memory and one launch replaces
+ * two.  Outputs are bitwise those of the two-call sequence.
+ *   dsb_rmsnorm_matmul_q8_0: y = W q8(rmsnorm(x) * norm_w) as
+ *     dsb_rmsnorm_q8_0(x, norm_w, n_tok, w->cols, eps) then
+ *     dsb_matmul_q8_0_narrow; x: device float32 [n_tok][w->cols].
+ *   dsb_silu_matmul_q8_0: y = W q8(silu(g) * u) as dsb_silu_mul_q8_0(gu,
+ *     n_tok, w->cols) then dsb_matmul_q8_0_narrow; gu: device float32
+ *     [n_tok][2 * w->cols] = [gate | up].
+ * y: device float32 [n_tok][w->rows].  n_tok in [1, 16]; w->cols a multiple of
+ * 256 (and <= 8192 for the RMSNorm); errors as those calls. */
+dsb_status dsb_rmsnorm_matmul_q8_0(const dsb_q8_0_mat* w, const float* x, const float* norm_w, float eps, int n_tok,
+                                   float* y, void* stream);
+dsb_status dsb_silu_matmul_q8_0(const dsb_q8_0_mat* w, const float* gu, int n_tok, float* y, void* stream);
+
 /* h[t] = the dequantised q8_0 row token_ids[t] of the embedding table
  * (device q8_0 [vocab][hidden/32]); exact in float32.  token_ids: host int32
  * [n_tok], each in [0, vocab) (DSB_ERR_INVALID_ARG otherwise); staged through

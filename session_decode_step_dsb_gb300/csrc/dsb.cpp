@@ -249,7 +249,7 @@ dsb_status dsb_device_error(void) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
   const unsigned int m = dsbk::read_clear_error_matmul();
-  const unsigned int mt = dsbk::read_clear_error_matmul_tc();
+  const unsigned int mt = dsbk::read_clear_error_matmul_tc() | dsbk::read_clear_error_matmul_fused();
   const unsigned int a = dsbk::read_clear_error_attention();
   if (m || mt || a)
     return fail(DSB_ERR_DEVICE, "a kernel's bounded wait ran out (matmul=%u matmul_tc=%u attention=%u)", m, mt, a);
@@ -662,6 +662,41 @@ dsb_status dsb_silu_mul_q8_0(const float* gu, int n_tok, int ffn, void* xq, void
   if (!aligned16(gu) || !aligned16(xq)) return fail(DSB_ERR_INVALID_ARG, "gu / xq not 16-byte aligned");
   cudaError_t e = dsbk::launch_silu_mul_quant(gu, n_tok, ffn, xq, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "silu_mul_q8_0 launch");
+}
+
+static dsb_status fused_matmul_common(int pro, const dsb_q8_0_mat* w, const float* xf, const float* norm_w,
+                                      float eps, int n_tok, float* y, void* stream) {
+  dsb_status st = check_mat(w);
+  if (st != DSB_OK) return st;
+  if (n_tok < 1 || n_tok > DSB_NARROW_MAX)
+    return fail(DSB_ERR_INVALID_ARG, "n_tok=%d out of [1, %d]", n_tok, DSB_NARROW_MAX);
+  if (pro == 1) {
+    if (w->cols > 8192) return fail(DSB_ERR_UNSUPPORTED, "cols=%lld: RMSNorm serves up to 8192", (long long)w->cols);
+    if (!(eps > 0.0f) || !std::isfinite(eps)) return fail(DSB_ERR_INVALID_ARG, "eps must be finite and > 0");
+    if (!norm_w) return fail(DSB_ERR_INVALID_ARG, "norm_w is NULL");
+    if (!aligned16(norm_w)) return fail(DSB_ERR_INVALID_ARG, "norm_w not 16-byte aligned");
+  }
+  if (!xf || !y) return fail(DSB_ERR_INVALID_ARG, "input / y is NULL");
+  if (!aligned16(xf) || !aligned16(y)) return fail(DSB_ERR_INVALID_ARG, "input / y not 16-byte aligned");
+  DeviceInfo di;
+  st = device_info(&di);
+  if (st != DSB_OK) return st;
+  if (dsbk::matmul_fused_smem_bytes(w->rows, w->cols, n_tok, pro, di.sms) > (size_t)di.max_smem_optin)
+    return fail(DSB_ERR_UNSUPPORTED, "matmul %lldx%lld exceeds the shared memory", (long long)w->rows,
+                (long long)w->cols);
+  const int stride = pro == 1 ? (int)w->cols : 2 * (int)w->cols;
+  cudaError_t e = dsbk::launch_matmul_q8_0_fused(pro, w->blocks, w->rows, w->cols, xf, stride, norm_w, eps, n_tok, y,
+                                                 nullptr, di.sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSB_OK : cuda_fail(e, "fused matmul launch");
+}
+
+dsb_status dsb_rmsnorm_matmul_q8_0(const dsb_q8_0_mat* w, const float* x, const float* norm_w, float eps, int n_tok,
+                                   float* y, void* stream) {
+  return fused_matmul_common(1, w, x, norm_w, eps, n_tok, y, stream);
+}
+
+dsb_status dsb_silu_matmul_q8_0(const dsb_q8_0_mat* w, const float* gu, int n_tok, float* y, void* stream) {
+  return fused_matmul_common(2, w, gu, nullptr, 0.0f, n_tok, y, stream);
 }
 
 dsb_status dsb_embed_q8_0(const void* table, int vocab, int hidden, const int32_t* token_ids, int n_tok, float* h,

@@ -65,6 +65,18 @@ struct PagedView {
 };
 
 int matmul_split(int64_t rows, int64_t cols, int num_sms);
+// The (tiling, cluster split) plan of a matrix: returns S, sets rows_mode.
+int matmul_plan_of(int64_t rows, int64_t cols, int num_sms, bool* rows_mode);
+// Narrow matmul (n_tok <= 16) whose activations are float rows quantised in
+// the kernel: pro 1 = RMSNorm (norm_w, eps) of xf[n_tok][xf_stride] over cols
+// values then q8_0; pro 2 = silu(gate) * up of xf = [gate | up] (stride
+// xf_stride, up at column cols + c) then q8_0.  Outputs bitwise those of the
+// standalone quantising kernel followed by launch_matmul_q8_0_narrow.
+size_t matmul_fused_smem_bytes(int64_t rows, int64_t cols, int n_tok, int pro, int num_sms);
+cudaError_t launch_matmul_q8_0_fused(int pro, const void* W, int64_t rows, int64_t cols, const float* xf,
+                                     int xf_stride, const float* norm_w, float eps, int n_tok, float* y,
+                                     const float* residual, int num_sms, cudaStream_t st);
+unsigned int read_clear_error_matmul_fused();
 size_t matmul_smem_bytes(int64_t rows, int64_t cols, int n_tok, int num_sms);
 // residual (may alias y, may be NULL): y = residual + W x.
 cudaError_t launch_matmul_q8_0_narrow(const void* W, int64_t rows, int64_t cols, const void* xq, int n_tok, float* y,

@@ -95,6 +95,8 @@ SIGNATURES = {
     "dsb_matmul_q8_0_wide": (_I, [ctypes.POINTER(Q8Mat), _P, _I, _P, _P, ctypes.c_size_t, _P]),
     "dsb_rope_posvec": (_I, [_P, _I, _P, _I, _I, _I, _PI32, _F, _P, _P]),
     "dsb_head_rmsnorm_rope": (_I, [_P, _I, _P, _I, _I, _I, _PI32, _P, _P, _P, _F, _P, _P]),
+    "dsb_rmsnorm_matmul_q8_0": (_I, [ctypes.POINTER(Q8Mat), _P, _P, _F, _I, _P, _P]),
+    "dsb_silu_matmul_q8_0": (_I, [ctypes.POINTER(Q8Mat), _P, _I, _P, _P]),
     "dsb_kv_scatter": (_I, [ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P, _P, _P]),
     "dsb_attention_decode_multi": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P, _P]),
     "dsb_attention_decode_multi_noalloc": (_I, [_P, _I, ctypes.POINTER(KVCache), _PI32, _I, _I, _PI32, _P, _P]),
@@ -256,6 +258,29 @@ def matmul_q8_0_wide(w_blocks, rows: int, cols: int, xq, n_tok: int, y=None, scr
     m = _mat(w_blocks, rows, cols)
     _check(lib().dsb_matmul_q8_0_wide(ctypes.byref(m), _ptr(xq), n_tok, _ptr(y), _ptr(scratch), scratch.numel(),
                                       _stream(stream)))
+    return y
+
+
+def rmsnorm_matmul_q8_0(w_blocks, rows: int, cols: int, x, norm_w, eps: float, y=None, stream=None):
+    """``y[n_tok, rows] = W q8(rmsnorm(x) * norm_w)`` in one kernel (x float32 ``[n_tok, cols]``)."""
+    import torch
+    n_tok = x.shape[0]
+    if y is None:
+        y = torch.empty((n_tok, rows), dtype=torch.float32, device=x.device)
+    m = _mat(w_blocks, rows, cols)
+    _check(lib().dsb_rmsnorm_matmul_q8_0(ctypes.byref(m), _ptr(x), _ptr(norm_w), float(eps), n_tok, _ptr(y),
+                                         _stream(stream)))
+    return y
+
+
+def silu_matmul_q8_0(w_blocks, rows: int, cols: int, gu, y=None, stream=None):
+    """``y[n_tok, rows] = W q8(silu(gate) * up)`` in one kernel (gu float32 ``[n_tok, 2 cols]``)."""
+    import torch
+    n_tok = gu.shape[0]
+    if y is None:
+        y = torch.empty((n_tok, rows), dtype=torch.float32, device=gu.device)
+    m = _mat(w_blocks, rows, cols)
+    _check(lib().dsb_silu_matmul_q8_0(ctypes.byref(m), _ptr(gu), n_tok, _ptr(y), _stream(stream)))
     return y
 
 
