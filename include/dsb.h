@@ -49,7 +49,7 @@ extern "C" {
 typedef enum {
   DSB_OK = 0,
   DSB_ERR_INVALID_ARG = 1, /* bad pointer, size, index or combination     */
-  DSB_ERR_UNSUPPORTED = 2, /* valid but not served by this build          */
+  DSB_ERR_UNSUPPORTED = 2, /* valid but not served by this library        */
   DSB_ERR_WORKSPACE = 3,   /* workspace missing or too small              */
   DSB_ERR_CUDA = 4,        /* a CUDA runtime call failed (see last_error) */
   DSB_ERR_TIMEOUT = 5,     /* a bounded host wait ran out                 */
