@@ -432,13 +432,15 @@ def run_dsb(args):
             "metric": "decode-step tokens/s and q8_0 narrow-matmul HBM GB/s (% of peak), n_tok=1..16",
             "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int8xint8->int32 dot (q8_0), f32 accumulate; f16 KV",
+            "vs_baseline": None, "dtype": f"int8xint8->int32 dot (q8_0), f32 accumulate; {ms.cache_dtype} KV",
             "data": "synthetic (seeded random weights/caches of the workload's shapes; no trained weights)",
             "config": {"workload": ms.name, "b": b, "tokens_per_seq": T, "n_tok": n_tok,
                        "full_batch_size": ms.full_batch_size, "ctx": ms.ctx, "seq_lens": [int(v) for v in lens],
                        "layers": ms.n_layers, "hidden": ms.hidden, "vocab": ms.vocab,
                        "l2": "flushed (512 MiB write) before every timed step", "parallelism": f"replicas x{world}",
                        "step_bytes": total_bytes, "weight_bytes": wbytes, "kv_bytes": kvbytes},
+            "step_ms": {"p50": round(float(np.percentile(ts, 50)), 5), "p90": round(float(np.percentile(ts, 90)), 5),
+                        "p95": round(float(np.percentile(ts, 95)), 5), "mean": round(float(mean), 5)},
             "step_roofline": {"bytes": total_bytes, "achieved_gbs": round(total_bytes / (ms_step * 1e-3) / 1e9, 1),
                               "peak_gbs": peak, "frac": round(total_bytes / (ms_step * 1e-3) / 1e9 / peak, 4)},
             "roofline": {"kernel": "matmul_q8_0_narrow_kernel", "bound": "hbm", "achieved": round(achieved, 1),
