@@ -571,6 +571,7 @@ def run_probe(spec: str):
     """A few launches of one kernel at one shape, for a profiler to capture
     (no timing, no JSON line): ``matmul:ROWS:COLS:NTOK[,NTOK...]`` runs the
     narrow matmul three times per n_tok on N(0, 0.02) weights;
+    ``wide:ROWS:COLS:NTOK`` the tensor-core matmul three times;
     ``attention:WORKLOAD`` runs the decode attention four times on that
     workload's cache shape (b sequences, seq_lens uniform)."""
     import torch
@@ -586,6 +587,12 @@ def run_probe(spec: str):
             xs = x[:nt].contiguous()
             for _ in range(3):
                 dsb.matmul_q8_0_narrow(w, rows, cols, xs, nt)
+    elif kind == "wide":
+        rows, cols, nt = int(rest[0]), int(rest[1]), int(rest[2])
+        w = dsb.quantize_q8_0(torch.randn((rows, cols), generator=g, device="cuda") * 0.02)
+        x = dsb.quantize_q8_0(torch.randn((nt, cols), generator=g, device="cuda"))
+        for _ in range(3):
+            dsb.matmul_q8_0_wide(w, rows, cols, x, nt)
     elif kind == "attention":
         F, hq, hkv, C, D, dt, b, T, lo = PROBE_ATTENTION[rest[0]]
         cdt = torch.float16 if dt == 0 else torch.bfloat16
@@ -622,8 +629,8 @@ def main(argv=None):
     ap.add_argument("--attn-sweep", action="store_true",
                     help="also time the split-K attention at ctx 32768/65536 (allocates ~70 GB)")
     ap.add_argument("--probe", default=None,
-                    help="run one kernel a few times for a profiler and exit: matmul:ROWS:COLS:NTOK[,..] or "
-                         "attention:WORKLOAD")
+                    help="run one kernel a few times for a profiler and exit: matmul:ROWS:COLS:NTOK[,..], "
+                         "wide:ROWS:COLS:NTOK or attention:WORKLOAD")
     args = ap.parse_args(argv)
     if args.probe:
         run_probe(args.probe)
