@@ -353,7 +353,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---------------------------------------------------------------- workers
     const int r0 = warp * kTcRowsPerWarp;
     const int my_rows = max(0, min(kTcRowsPerWarp, rows_valid - r0));
-    const int r_sub = lane >> 2, g = lane & 3;
+    // lane = 8 g + r_sub: the 8 lanes of a quarter-warp write one 16-byte
+    // piece each of 8 different rows of one core matrix, 8 different bank
+    // groups, so the operand stores are conflict-free
+    const int r_sub = lane & 7, g = lane >> 3;
     int raw_issued = 0;
     const int n_chunks = nbl / kTcChunk;
     int drained = 0;
