@@ -30,6 +30,10 @@ TINY_BF16_QKN = ModelShape("tiny-bf16-qknorm", 512, 8, 2, 128, 768, 700, 1, 5, 3
 # tiny shapes with the YaRN RoPE (context extended 4x over an original 64 / 128)
 TINY_YARN = ModelShape("tiny-yarn", 256, 4, 2, 64, 512, 1000, 2, 4, 256, "f16", qk_norm=True, yarn_factor=4.0,
                        yarn_orig_ctx=64)
+# many sessions x long drafts: n_tok = 64 * 32 = 2048 token rows, so a captured
+# step's metadata (2 n_tok + 3 b + 1 words) outgrows the first kernel's
+# parameter block and is read from mapped pinned memory instead
+TINY_WIDE = ModelShape("tiny-wide", 256, 4, 2, 64, 512, 1000, 1, 80, 64, "f16")
 TINY_BF16_YARN = ModelShape("tiny-bf16-yarn", 512, 8, 2, 128, 768, 700, 1, 5, 300, "bf16", yarn_factor=4.0,
                             yarn_orig_ctx=128)
 

@@ -154,6 +154,26 @@ def test_batched_step_rows_equal_single_sequence_steps(cuda_device, ms, b, T):
         assert np.array_equal(one.view(np.uint32), batched[s * T:(s + 1) * T].view(np.uint32)), s
 
 
+def test_graph_replay_mapped_metadata_equals_eager_step(cuda_device):
+    """A step whose metadata exceeds the parameter block (n_tok = 2048): the
+    graph reads it from mapped pinned memory; replays with new metadata equal
+    the eager step bitwise."""
+    import torch
+    ms = _shapes.TINY_WIDE
+    b, T = 64, 32
+    model, _, _, _ = _build(ms)
+    ws = model.workspace(b * T)
+    logits = torch.empty((b * T, ms.vocab), dtype=torch.float32, device="cuda")
+    g = model.graph(b, T, logits, ws)
+    for seed in (6, 7):
+        bi, lens, toks = _shapes.step_meta(seed, ms, b, T)
+        eager = to_host(model.step(toks, bi, T, lens, ws))
+        replay = to_host(g.launch(toks, bi, lens))
+        assert np.array_equal(eager.view(np.uint32), replay.view(np.uint32)), seed
+    g.close()
+    _dsb().device_error()
+
+
 @pytest.mark.parametrize("b,T", [(4, 1), (2, 32)])
 def test_graph_replay_equals_eager_step(cuda_device, b, T):
     import torch
