@@ -62,6 +62,30 @@ def test_matmul_rejects_bad_arguments(lib):
     assert lib.dsb_matmul_q8_0_block_dots(ctypes.byref(m), fake, 1, None, None) == 1
 
 
+def test_fused_matmul_rejects_bad_arguments(lib):
+    """The norm / SiLU-gate + matmul entry points validate on the host before
+    any device work."""
+    from session_decode_step_dsb_gb300 import dsb
+    fake = ctypes.c_void_p(1 << 20)
+    m = dsb.Q8Mat(fake, 64, 256)
+    eps = ctypes.c_float(1e-6)
+    assert lib.dsb_rmsnorm_matmul_q8_0(ctypes.byref(m), fake, fake, eps, 0, fake, None) == 1
+    assert "n_tok" in _err(lib)
+    assert lib.dsb_rmsnorm_matmul_q8_0(ctypes.byref(m), fake, fake, eps, 17, fake, None) == 1
+    assert lib.dsb_rmsnorm_matmul_q8_0(ctypes.byref(m), fake, fake, ctypes.c_float(0.0), 2, fake, None) == 1
+    assert "eps" in _err(lib)
+    assert lib.dsb_rmsnorm_matmul_q8_0(ctypes.byref(m), fake, None, eps, 2, fake, None) == 1
+    assert lib.dsb_rmsnorm_matmul_q8_0(ctypes.byref(m), None, fake, eps, 2, fake, None) == 1
+    assert lib.dsb_rmsnorm_matmul_q8_0(ctypes.byref(m), ctypes.c_void_p((1 << 20) + 4), fake, eps, 2, fake,
+                                       None) == 1
+    wide = dsb.Q8Mat(fake, 64, 8448)
+    assert lib.dsb_rmsnorm_matmul_q8_0(ctypes.byref(wide), fake, fake, eps, 2, fake, None) == 2
+    assert lib.dsb_silu_matmul_q8_0(ctypes.byref(m), fake, 17, fake, None) == 1
+    assert lib.dsb_silu_matmul_q8_0(ctypes.byref(m), fake, 2, None, None) == 1
+    m96 = dsb.Q8Mat(fake, 64, 96)
+    assert lib.dsb_silu_matmul_q8_0(ctypes.byref(m96), fake, 2, fake, None) == 2  # cols % 256
+
+
 def test_quantize_rejects_bad_arguments(lib):
     fake = ctypes.c_void_p(1 << 20)
     assert lib.dsb_quantize_q8_0(fake, 4, 33, fake, None) == 1
