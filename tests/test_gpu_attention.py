@@ -98,6 +98,10 @@ ATTN_CASES = [
     (128, 12, 12, 2048, 64, "f16", [100, 3], [300, 2048], 8),               # speculative drafts (K=7)
     (8, 4, 4, 700, 128, "f16", [1], [700], 16),                             # ragged ctx, T=16
     (5, 8, 2, 384, 128, "bf16", [0, 1, 2, 3, 4], [1, 127, 128, 129, 384], 1),  # chunk edges
+    # 64-key copy-box edges; slot 5 is the last of the cache tensor and C = 200
+    # is not a multiple of 64, so its last box reaches past the tensor's end
+    (6, 8, 2, 200, 64, "f16", [5, 0, 3, 1, 2, 4], [200, 63, 64, 65, 191, 192], 1),
+    (6, 10, 2, 200, 128, "bf16", [5, 2], [200, 65], 2),                    # G*T = 10: two query row groups
 ]
 
 
