@@ -427,16 +427,22 @@ dsb_status dsb_decode_step(const dsb_model* model, const int32_t* token_ids, con
                            void* stream);
 
 /* The same step captured once into a CUDA graph for a fixed (n_seq, T) and
- * replayed.  The graph owns a pinned copy of the step metadata that its first
- * node copies to the device, so a replay serves new token ids, slots and
- * seq_lens without re-capture; the attention kernel reads its work count on the
- * device.  The model, logits and workspace must stay valid for the graph's
- * lifetime; one graph per workspace at a time. */
+ * replayed.  The step's metadata (token ids, slots, seq_lens and what follows
+ * from them) reaches the graph's first kernel, which copies it to the
+ * workspace for the others: in that kernel's parameters, rewritten on the host
+ * for each replay with new metadata, when it fits 4096 int32 words (2*n_seq*T
+ * + 3*n_seq + 1); otherwise from a mapped pinned host copy the graph owns.  So
+ * a replay serves new token ids, slots and seq_lens without re-capture; the
+ * attention kernel reads its work count on the device.  The model, logits and
+ * workspace must stay valid for the graph's lifetime; one graph per workspace
+ * at a time. */
 typedef struct dsb_step_graph dsb_step_graph;
 dsb_status dsb_step_graph_create(const dsb_model* model, int n_seq, int tokens_per_seq, float* logits,
                                  dsb_workspace* ws, void* stream, dsb_step_graph** out);
-/* Validates and stages the metadata (waiting, bounded, for the previous
- * replay's metadata copy when it changes), then launches the graph. */
+/* Validates and stages the metadata, then launches the graph.  When the
+ * metadata changes: parameter form, the first kernel's parameters are
+ * rewritten (no wait); mapped form, the host waits (bounded) until the previous
+ * replay has read the pinned copy before rewriting it. */
 dsb_status dsb_step_graph_launch(dsb_step_graph* g, const int32_t* token_ids, const int32_t* batch_index,
                                  const int32_t* seq_lens, void* stream);
 dsb_status dsb_step_graph_destroy(dsb_step_graph* g);
