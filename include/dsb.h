@@ -30,8 +30,10 @@
  *     status of the calling thread.
  *   - Work is enqueued on the given stream (a cudaStream_t; NULL = legacy
  *     default stream) and runs asynchronously.  Device pointers must be 16-byte
- *     aligned.  Kernels never spin on other CTAs; the mbarrier waits inside a
- *     CTA are bounded and, if exceeded, set a device error word reported by
+ *     aligned.  Kernels never spin on flags other CTAs set: CTAs of one
+ *     launch meet only at the hardware barrier of their thread-block cluster
+ *     (co-scheduled by construction), and the mbarrier waits inside a CTA are
+ *     bounded and, if exceeded, set a device error word reported by
  *     dsb_device_error().
  *   - A workspace serves one stream at a time (the engine-owned scratch shared
  *     by the sessions one thread drives, [DS4] session-split commit).
