@@ -37,6 +37,11 @@
  *     dsb_device_error().
  *   - A workspace serves one stream at a time (the engine-owned scratch shared
  *     by the sessions one thread drives, [DS4] session-split commit).
+ *   - Host threads may call concurrently when each passes its own workspace
+ *     (and model, step graph, batch former): the library's own host state --
+ *     launch plans, tensor maps, occupancy and device queries -- is memoised
+ *     behind locks.  The one exception is the shared scratch of
+ *     dsb_attention_decode_multi_noalloc, described there.
  */
 #ifndef DSB_H
 #define DSB_H

@@ -41,6 +41,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "dsb_kernels.h"
 #include "dsb_ptx.cuh"
@@ -494,9 +495,11 @@ cudaError_t kv_tensor_map(const void* base, long long rows, int D, int dtype, CU
     int D, dtype;
     CUtensorMap map;
   };
+  static std::mutex mu;
   static Entry cache[16];
   static int n_cache = 0, next_slot = 0;
   static EncodeTiledFn encode = nullptr;
+  std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n_cache; ++i)
     if (cache[i].base == base && cache[i].rows == rows && cache[i].D == D && cache[i].dtype == dtype) {
       *out = cache[i].map;
@@ -541,18 +544,26 @@ cudaError_t launch_rg(const float* q, long long q_stride, int n_q_heads, const v
   if ((e = kv_tensor_map(vc, kv_rows, D, dtype, &tmv)) != cudaSuccess) return e;
   const float scale = (float)(1.0 / sqrt((double)D));
   // Persistent grid: as many CTAs as fit at once, capped by the item count.
-  static int resident = 0;
-  static size_t resident_smem = 0;
-  if (resident == 0 || resident_smem != smem) {
-    int per_sm = 0, dev = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
-    if (e != cudaSuccess) return e;
+  int resident = 0;
+  {
+    static std::mutex mu;
+    static int cached = 0, cached_dev = -1;
+    static size_t cached_smem = 0;
+    int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    resident = (per_sm > 0 ? per_sm : 1) * sms;
-    resident_smem = smem;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached == 0 || cached_smem != smem || cached_dev != dev) {
+      int per_sm = 0, sms = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+      if (e != cudaSuccess) return e;
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      cached = (per_sm > 0 ? per_sm : 1) * sms;
+      cached_smem = smem;
+      cached_dev = dev;
+    }
+    resident = cached;
   }
   const long long items = (long long)max_items;
   const unsigned grid = (unsigned)(items < resident ? (items > 0 ? items : 1) : resident);

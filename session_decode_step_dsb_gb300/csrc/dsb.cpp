@@ -15,6 +15,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 #include <thread>
@@ -59,17 +60,24 @@ dsb_status device_info(DeviceInfo* out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  static std::mutex mu;
   static DeviceInfo cache[64];
-  if (dev >= 0 && dev < 64 && cache[dev].sms > 0) {
-    *out = cache[dev];
-    return DSB_OK;
+  if (dev >= 0 && dev < 64) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev].sms > 0) {
+      *out = cache[dev];
+      return DSB_OK;
+    }
   }
   DeviceInfo d;
   e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
   e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(shared memory)");
-  if (dev >= 0 && dev < 64) cache[dev] = d;
+  if (dev >= 0 && dev < 64) {
+    std::lock_guard<std::mutex> lock(mu);
+    cache[dev] = d;
+  }
   *out = d;
   return DSB_OK;
 }

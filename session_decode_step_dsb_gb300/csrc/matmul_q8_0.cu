@@ -60,12 +60,15 @@ struct Plan {
 Plan matmul_plan(int64_t rows, int64_t cols, int num_sms) {
   struct Memo {
     int64_t rows, cols;
+    int num_sms;
     Plan plan;
   };
+  static std::mutex mu;
   static Memo memo[64];
   static int n_memo = 0;
+  std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n_memo; ++i)
-    if (memo[i].rows == rows && memo[i].cols == cols) return memo[i].plan;
+    if (memo[i].rows == rows && memo[i].cols == cols && memo[i].num_sms == num_sms) return memo[i].plan;
   const int nks = (int)(cols / 256);
   int s_max = nks < kMaxCluster ? nks : kMaxCluster;
   int s_min = (nks + 7) / 8;
@@ -101,7 +104,7 @@ Plan matmul_plan(int64_t rows, int64_t cols, int num_sms) {
       }
     }
   }
-  if (queried && n_memo < 64) memo[n_memo++] = Memo{rows, cols, best};
+  if (queried && n_memo < 64) memo[n_memo++] = Memo{rows, cols, num_sms, best};
   return best;
 }
 

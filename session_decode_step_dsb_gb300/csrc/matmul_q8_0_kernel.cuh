@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 #include <type_traits>
 
 #include "dsb_kernels.h"
@@ -500,13 +501,16 @@ size_t smem_bytes(int kr, int nt, bool rows_mode, int pro = 0) {
          (size_t)kPairs * kNStage * 8 + (pro == 1 ? (size_t)nt * 9 * 4 : 0);
 }
 
-// Per-instantiation host caches (not thread-safe; one host thread drives a
-// device): the largest dynamic shared memory granted so far, and the number of
-// co-resident clusters for each (S, smem) seen.
+// Per-instantiation host caches, each behind its own lock: the largest
+// dynamic shared memory granted so far, and the number of co-resident clusters
+// for each (S, smem) seen.  The attributes are per function, the same for every
+// device of one architecture.
 template <int NT, bool EMIT, bool ROWS, int PRO>
 cudaError_t grant_smem(size_t smem) {
+  static std::mutex mu;
   static size_t granted = 0;
   static bool non_portable = false;
+  std::lock_guard<std::mutex> lock(mu);
   if (!non_portable) {
     cudaError_t e = cudaFuncSetAttribute(matmul_q8_0_narrow_kernel<NT, EMIT, ROWS, PRO>,
                                          cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -527,8 +531,10 @@ cudaError_t cluster_capacity(int S, size_t smem, int* clusters) {
     size_t smem;
     int clusters;
   };
+  static std::mutex mu;
   static Entry cache[16];
   static int n_cache = 0;
+  std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n_cache; ++i)
     if (cache[i].S == S && cache[i].smem == smem) {
       *clusters = cache[i].clusters;
