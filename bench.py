@@ -423,6 +423,9 @@ def run_dsb(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "llama-68m":
         cpu = cpu_baseline(ms, b, T, budget_s=args.cpu_budget)
+        cpu["cpu"] = _cpu_model()
+        if args.cpu_all_core_budget > 0:
+            cpu["all_cores"] = cpu_all_cores(args.workload, b, T, budget_s=args.cpu_all_core_budget)
 
     graph.close()
     total_bytes, wbytes, kvbytes = step_bytes(ms, b, T, lens)
@@ -516,6 +519,90 @@ def cpu_baseline(ms, b, T, budget_s=20.0):
     return {"value": round(n * T / dt, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"{n} single-sequence steps (1 of the {b} sessions each, {T} token(s)) of the {ms.name} "
                       f"workload, float64 numpy, {dt:.1f} s"}
+
+
+def _cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (x86: model name; Arm: the
+    implementer / part codes), with the machine type."""
+    import platform
+    name = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model", "CPU part"):
+            for line in info.splitlines():
+                if line.startswith(key):
+                    name = line.split(":", 1)[1].strip()
+                    break
+            if name:
+                if key == "CPU part":
+                    name = "Arm CPU part " + name
+                break
+    except OSError:
+        pass
+    return f"{name or 'unknown'} ({platform.machine()})"
+
+
+def _oracle_worker(workload, b, T, budget_s, worker, start, ready, results):
+    """One process of the all-core oracle run: builds the oracle model, reports
+    ready, waits for the common start, then runs single-sequence oracle steps
+    (sessions taken in turn from worker onwards) for budget_s seconds."""
+    from oracle import step as ostep
+    ms = _shape(workload)
+    w, kc, vc = _oracle_model(ms, seed=0)
+    bi, lens, toks = _meta(ms, b, T, seed=7)
+    shape = ostep.Shape(ms.hidden, ms.n_q_heads, ms.n_kv_heads, ms.head_dim, ms.ffn, ms.vocab, ms.n_layers, ms.eps,
+                        ms.theta)
+    ready.put(worker)
+    start.wait(600)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        s = (worker + n) % b
+        ostep.decode_step(shape, w, kc, vc, ms.cache_dtype, toks[s * T:(s + 1) * T], bi[s:s + 1], T, lens[s:s + 1])
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    results.put((n, time.perf_counter() - t0))
+
+
+def cpu_all_cores(workload, b, T, budget_s=8.0, max_workers=16):
+    """The same oracle step on every host core at once: one spawned process
+    per core (BLAS threads 1 each), all starting together after building
+    their model; throughput = all steps' tokens / the longest process time."""
+    import multiprocessing as mp
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    n = max(1, min(cores, max_workers))
+    ctx = mp.get_context("spawn")
+    start, ready, results = ctx.Event(), ctx.Queue(), ctx.Queue()
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS")}
+    os.environ["OMP_NUM_THREADS"] = os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    procs = [ctx.Process(target=_oracle_worker, args=(workload, b, T, budget_s, i, start, ready, results))
+             for i in range(n)]
+    try:
+        for p in procs:
+            p.start()
+        for _ in procs:
+            ready.get(timeout=600)
+        start.set()
+        res = [results.get(timeout=budget_s + 600) for _ in procs]
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+        for p in procs:
+            p.join(timeout=60)
+            if p.is_alive():
+                p.kill()
+    steps = sum(r[0] for r in res)
+    dt = max(r[1] for r in res)
+    return {"value": round(steps * T / dt, 3), "unit": "tokens/s", "cores": n, "host_cores": cores,
+            "sample": f"{steps} single-sequence oracle steps over {n} processes in {dt:.1f} s"}
 
 
 def run_reference(args):
@@ -625,6 +712,8 @@ def main(argv=None):
     ap.add_argument("--T", type=int, default=1)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-all-core-budget", type=float, default=8.0,
+                    help="seconds of the all-core oracle run beside the single-core one (0: skip)")
     ap.add_argument("--no-matmul-sweep", action="store_true")
     ap.add_argument("--attn-sweep", action="store_true",
                     help="also time the split-K attention at ctx 32768/65536 (allocates ~70 GB)")

@@ -31,3 +31,13 @@ def test_step_bytes_qwen_gqa_reads_each_kv_head_once():
 def test_warmup_below_three_is_rejected():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_cpu_all_cores_runs_every_process():
+    """The all-core oracle run starts its spawned processes together and
+    counts every process's steps (bounded: two processes, half a second)."""
+    r = bench.cpu_all_cores("llama-68m", 2, 1, budget_s=0.5, max_workers=2)
+    assert r["cores"] == min(2, r["host_cores"])
+    assert r["value"] > 0 and r["unit"] == "tokens/s"
+    assert "oracle steps over" in r["sample"]
+    assert bench._cpu_model().endswith(")")
