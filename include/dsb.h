@@ -85,7 +85,11 @@ typedef struct {
 } dsb_q8_0_mat;
 
 /* A retained KV cache on the device ([QAIC] "Objective"): K and V each
- * [full_batch_size][n_kv_heads][ctx][head_dim] in dtype, row-major. */
+ * [full_batch_size][n_kv_heads][ctx][head_dim] in dtype, row-major.  The
+ * attention names a row (slot, kv head, position) by a 32-bit tensor
+ * coordinate: full_batch_size * n_kv_heads * ctx above 2^31 - 129 is
+ * DSB_ERR_UNSUPPORTED (no such cache fits in one GPU's memory at
+ * head_dim >= 64). */
 typedef struct {
   void* k;
   void* v;
@@ -283,7 +287,7 @@ typedef struct {
   void* k;          /* device page pool */
   void* v;          /* device page pool */
   dsb_dtype dtype;
-  int32_t n_pages;
+  int32_t n_pages;  /* n_pages * n_kv_heads * DSB_KV_PAGE <= 2^31 - 129 */
   int32_t n_kv_heads;
   int32_t head_dim;
 } dsb_kv_pages;

@@ -150,6 +150,11 @@ dsb_status check_kv(const dsb_kv_cache* kv) {
   if (kv->ctx < 1) return fail(DSB_ERR_INVALID_ARG, "kv->ctx=%d", kv->ctx);
   if (kv->head_dim < 2 || kv->head_dim % 2 || kv->head_dim > 1024)
     return fail(DSB_ERR_INVALID_ARG, "kv->head_dim=%d must be even in [2, 1024]", kv->head_dim);
+  // the attention addresses cache rows (slot, kv head, position) by a 32-bit
+  // tensor coordinate
+  if ((long long)kv->full_batch_size * kv->n_kv_heads * kv->ctx > (long long)INT_MAX - 128)
+    return fail(DSB_ERR_UNSUPPORTED, "cache of %lld rows (full_batch_size*n_kv_heads*ctx) exceeds 2^31 - 129",
+                (long long)kv->full_batch_size * kv->n_kv_heads * kv->ctx);
   return DSB_OK;
 }
 
@@ -484,6 +489,9 @@ static dsb_status check_pages(const dsb_kv_pages* kv) {
   if (kv->n_pages < 1 || kv->n_kv_heads < 1) return fail(DSB_ERR_INVALID_ARG, "n_pages / n_kv_heads < 1");
   if (kv->head_dim < 8 || kv->head_dim % 8 || kv->head_dim > 1024)
     return fail(DSB_ERR_INVALID_ARG, "head_dim=%d must be a multiple of 8 in [8, 1024]", kv->head_dim);
+  if ((long long)kv->n_pages * kv->n_kv_heads * DSB_KV_PAGE > (long long)INT_MAX - 128)
+    return fail(DSB_ERR_UNSUPPORTED, "page pools of %lld rows (n_pages*n_kv_heads*%d) exceed 2^31 - 129",
+                (long long)kv->n_pages * kv->n_kv_heads * DSB_KV_PAGE, DSB_KV_PAGE);
   return DSB_OK;
 }
 

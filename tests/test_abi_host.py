@@ -152,6 +152,24 @@ def test_attention_rejects_bad_metadata(lib):
     assert lib.dsb_attention_decode_multi(fake, 8, ctypes.byref(kv96), pbi, 2, 1, plens, fake, fake, None) == 2
     assert lib.dsb_attention_decode_multi(fake, 2 * 40, ctypes.byref(kv), pbi, 2, 2, plens, fake, fake, None) == 2
     assert lib.dsb_attention_decode_multi(fake, 8, ctypes.byref(kv), pbi, 2, 1, plens, fake, None, None) == 3
+    # full_batch_size * n_kv_heads * ctx beyond the 32-bit row coordinate
+    huge = _kv(fake, full_batch_size=256, n_kv_heads=128, ctx=65536)
+    assert lib.dsb_attention_decode_multi(fake, 128, ctypes.byref(huge), pbi, 2, 1, plens, fake, fake, None) == 2
+    assert "2^31" in _err(lib)
+    assert lib.dsb_kv_scatter(ctypes.byref(huge), pbi, 2, 1, plens, fake, fake, fake, None) == 2
+
+
+def test_paged_rejects_pools_beyond_the_row_coordinate(lib):
+    from session_decode_step_dsb_gb300 import dsb
+    fake = ctypes.c_void_p(1 << 20)
+    pages = dsb.KVPages(fake, fake, 0, 1 << 20, 16, 64)   # 2^20 pages x 16 heads x 128 rows = 2^31 rows
+    bt, pbt = _i32([[0, 1]])
+    nb, pnb = _i32([2])
+    win, pwin = _i32([0])
+    lens, plens = _i32([200])
+    assert lib.dsb_attention_decode_paged(fake, 16, ctypes.byref(pages), pbt, 2, pnb, pwin, 1, 1, plens, fake,
+                                          fake, None) == 2
+    assert "2^31" in _err(lib)
 
 
 def test_rope_rejects_bad_arguments(lib):
