@@ -78,3 +78,56 @@ def test_form_matches_step_contract(dsb):
         bf.commit(bi)
         for s in bi:
             assert bf.length(int(s)) == before[int(s)] + T
+
+
+def test_random_ops_match_a_dictionary_model(dsb):
+    """Random join / leave / submit / form / commit sequences against a plain
+    model: lowest free slot on join, lengths advanced by T on commit, and
+    form() listing exactly the queued sessions in slot order with their
+    tokens; rejected calls change nothing."""
+    rng = np.random.default_rng(5)
+    F, C, T = 6, 40, 2
+    bf = dsb.BatchFormer(F, C, T)
+    length, queued = {}, {}
+    for _ in range(400):
+        op = int(rng.integers(0, 4))
+        if op == 0:
+            pre = int(rng.integers(0, C))
+            if len(length) == F:
+                with pytest.raises(dsb.DsbError):
+                    bf.join(pre)
+            else:
+                s = bf.join(pre)
+                assert s == min(set(range(F)) - set(length))
+                length[s] = pre
+        elif op == 1:
+            s = int(rng.integers(0, F))
+            if s in length:
+                bf.leave(s)
+                del length[s]
+                queued.pop(s, None)
+            else:
+                with pytest.raises(dsb.DsbError):
+                    bf.leave(s)
+        elif op == 2 and length:
+            s = int(rng.choice(sorted(length)))
+            toks = rng.integers(0, 50000, T).astype(np.int32)
+            if length[s] + T > C:
+                with pytest.raises(dsb.DsbError):
+                    bf.submit(s, toks)
+            else:
+                bf.submit(s, toks)
+                queued[s] = toks
+        else:
+            bi, sl, tk = bf.form()
+            want = sorted(queued)
+            assert list(bi) == want
+            assert list(sl) == [length[s] + T for s in want]
+            assert np.array_equal(tk, np.concatenate([queued[s] for s in want]) if want else np.zeros(0, np.int32))
+            if want and rng.random() < 0.8:
+                bf.commit(bi)
+                for s in want:
+                    length[s] += T
+                queued.clear()
+        for s in range(F):
+            assert bf.length(s) == length.get(s, -1)
