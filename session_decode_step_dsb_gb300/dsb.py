@@ -1,9 +1,12 @@
 """ctypes binding of libdsb.so (C ABI in include/dsb.h).
 
 Argument marshalling only: tensors become device pointers, host index arrays
-become int32 buffers, the current torch stream becomes the cudaStream_t.  Every
-step of the computation runs in the library's CUDA kernels; if the library has
-not been built the first call raises instead of falling back to anything.
+become int32 buffers, the current torch stream becomes the cudaStream_t.  Since
+the C ABI sees bare pointers, the binding first checks that every tensor holds
+the bytes and element type the call will touch and that every host array has
+the call's length (ValueError otherwise).  Every step of the computation runs
+in the library's CUDA kernels; if the library has not been built the first call
+raises instead of falling back to anything.
 """
 from __future__ import annotations
 
@@ -151,9 +154,35 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _i32(a: Sequence[int]):
-    arr = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+def _i32(a: Sequence[int], n: Optional[int] = None, name: str = "array"):
+    arr = np.ascontiguousarray(np.asarray(a, dtype=np.int32)).reshape(-1)
+    if n is not None and arr.size != n:
+        raise ValueError(f"{name} has {arr.size} entries, needs {n}")
     return arr, arr.ctypes.data_as(_PI32)
+
+
+def _need(t, nbytes: int, name: str, kind: Optional[str] = None):
+    """Checks, before any pointer reaches the library, that tensor ``t`` holds
+    at least ``nbytes`` bytes of the expected kind ("f32", "u8" or "16": any
+    16-bit type): the C ABI sees bare pointers, so a short buffer would be read
+    or written past its end on the device."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if kind == "f32" and t.dtype != torch.float32:
+        raise ValueError(f"{name} must be float32, got {t.dtype}")
+    if kind == "u8" and t.dtype != torch.uint8:
+        raise ValueError(f"{name} must be uint8 (q8_0 bytes), got {t.dtype}")
+    if kind == "16" and t.element_size() != 2:
+        raise ValueError(f"{name} must have a 16-bit element type, got {t.dtype}")
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{name} holds {have} bytes, needs {nbytes}")
+
+
+def _need_opt(t, nbytes: int, name: str, kind: Optional[str] = None):
+    if t is not None:
+        _need(t, nbytes, name, kind)
 
 
 def version() -> str:
@@ -200,14 +229,22 @@ def quantize_q8_0(x, xq=None, stream=None):
     """q8_0 bytes ``[n_rows, cols/32*34]`` (uint8, device) of float32 rows ``x``."""
     import torch
     n_rows, cols = x.shape
+    _need(x, 4 * n_rows * cols, "x", "f32")
     if xq is None:
         xq = torch.empty((n_rows, q8_rows_bytes(cols)), dtype=torch.uint8, device=x.device)
+    _need(xq, n_rows * q8_rows_bytes(cols), "xq", "u8")
     _check(lib().dsb_quantize_q8_0(_ptr(x), n_rows, cols, _ptr(xq), _stream(stream)))
     return xq
 
 
-def _mat(w_blocks, rows: int, cols: int) -> Q8Mat:
+def _mat(w_blocks, rows: int, cols: int, name: str = "w_blocks") -> Q8Mat:
+    _need(w_blocks, rows * q8_rows_bytes(cols), name, "u8")
     return Q8Mat(_ptr(w_blocks), rows, cols)
+
+
+def _mm_io(rows: int, cols: int, xq, n_tok: int, y):
+    _need(xq, n_tok * q8_rows_bytes(cols), "xq", "u8")
+    _need(y, 4 * n_tok * rows, "y", "f32")
 
 
 def matmul_q8_0_narrow(w_blocks, rows: int, cols: int, xq, n_tok: int, y=None, stream=None):
@@ -215,6 +252,7 @@ def matmul_q8_0_narrow(w_blocks, rows: int, cols: int, xq, n_tok: int, y=None, s
     import torch
     if y is None:
         y = torch.empty((n_tok, rows), dtype=torch.float32, device=w_blocks.device)
+    _mm_io(rows, cols, xq, n_tok, y)
     m = _mat(w_blocks, rows, cols)
     _check(lib().dsb_matmul_q8_0_narrow(ctypes.byref(m), _ptr(xq), n_tok, _ptr(y), _stream(stream)))
     return y
@@ -225,6 +263,7 @@ def matmul_q8_0(w_blocks, rows: int, cols: int, xq, n_tok: int, y=None, stream=N
     import torch
     if y is None:
         y = torch.empty((n_tok, rows), dtype=torch.float32, device=w_blocks.device)
+    _mm_io(rows, cols, xq, n_tok, y)
     m = _mat(w_blocks, rows, cols)
     _check(lib().dsb_matmul_q8_0(ctypes.byref(m), _ptr(xq), n_tok, _ptr(y), _stream(stream)))
     return y
@@ -234,6 +273,7 @@ def matmul_q8_0_block_dots(w_blocks, rows: int, cols: int, xq, n_tok: int, strea
     """int32 ``isum[n_tok, rows, cols/32]`` through the narrow kernel's dp4a chain."""
     import torch
     isum = torch.empty((n_tok, rows, cols // 32), dtype=torch.int32, device=w_blocks.device)
+    _need(xq, n_tok * q8_rows_bytes(cols), "xq", "u8")
     m = _mat(w_blocks, rows, cols)
     _check(lib().dsb_matmul_q8_0_block_dots(ctypes.byref(m), _ptr(xq), n_tok, _ptr(isum), _stream(stream)))
     return isum
@@ -255,6 +295,8 @@ def matmul_q8_0_wide(w_blocks, rows: int, cols: int, xq, n_tok: int, y=None, scr
         y = torch.empty((n_tok, rows), dtype=torch.float32, device=w_blocks.device)
     if scratch is None:
         scratch, _ = _wide_scratch(n_tok, cols, w_blocks.device)
+    _mm_io(rows, cols, xq, n_tok, y)
+    _need(scratch, 0, "scratch", "u8")
     m = _mat(w_blocks, rows, cols)
     _check(lib().dsb_matmul_q8_0_wide(ctypes.byref(m), _ptr(xq), n_tok, _ptr(y), _ptr(scratch), scratch.numel(),
                                       _stream(stream)))
@@ -267,6 +309,9 @@ def rmsnorm_matmul_q8_0(w_blocks, rows: int, cols: int, x, norm_w, eps: float, y
     n_tok = x.shape[0]
     if y is None:
         y = torch.empty((n_tok, rows), dtype=torch.float32, device=x.device)
+    _need(x, 4 * n_tok * cols, "x", "f32")
+    _need_opt(norm_w, 4 * cols, "norm_w", "f32")
+    _need(y, 4 * n_tok * rows, "y", "f32")
     m = _mat(w_blocks, rows, cols)
     _check(lib().dsb_rmsnorm_matmul_q8_0(ctypes.byref(m), _ptr(x), _ptr(norm_w), float(eps), n_tok, _ptr(y),
                                          _stream(stream)))
@@ -279,6 +324,8 @@ def silu_matmul_q8_0(w_blocks, rows: int, cols: int, gu, y=None, stream=None):
     n_tok = gu.shape[0]
     if y is None:
         y = torch.empty((n_tok, rows), dtype=torch.float32, device=gu.device)
+    _need(gu, 8 * n_tok * cols, "gu", "f32")
+    _need(y, 4 * n_tok * rows, "y", "f32")
     m = _mat(w_blocks, rows, cols)
     _check(lib().dsb_silu_matmul_q8_0(ctypes.byref(m), _ptr(gu), n_tok, _ptr(y), _stream(stream)))
     return y
@@ -288,7 +335,9 @@ def rope_posvec(q, k, pos, theta: float, ws: Workspace, stream=None):
     """In-place RoPE on ``q[n_tok, Hq, D]`` and ``k[n_tok, Hkv, D]`` (k may be None)."""
     n_tok, hq, d = q.shape
     hkv = 0 if k is None else k.shape[1]
-    arr, p = _i32(pos)
+    _need(q, 4 * n_tok * hq * d, "q", "f32")
+    _need_opt(k, 4 * n_tok * hkv * d, "k", "f32")
+    arr, p = _i32(pos, n_tok, "pos")
     _check(lib().dsb_rope_posvec(_ptr(q), hq, _ptr(k), hkv, d, n_tok, p, float(theta), ws.handle, _stream(stream)))
 
 
@@ -298,7 +347,11 @@ def head_rmsnorm_rope(q, k, pos, theta: float, q_norm, k_norm, eps: float, ws: W
     ``q[n_tok, Hq, D]`` and ``k[n_tok, Hkv, D]``."""
     n_tok, hq, d = q.shape
     hkv = 0 if k is None else k.shape[1]
-    arr, p = _i32(pos)
+    _need(q, 4 * n_tok * hq * d, "q", "f32")
+    _need_opt(k, 4 * n_tok * hkv * d, "k", "f32")
+    _need_opt(q_norm, 4 * d, "q_norm", "f32")
+    _need_opt(k_norm, 4 * d, "k_norm", "f32")
+    arr, p = _i32(pos, n_tok, "pos")
     r = rope_params(theta, yarn)
     _check(lib().dsb_head_rmsnorm_rope(_ptr(q), hq, _ptr(k), hkv, d, n_tok, p, ctypes.byref(r), _ptr(q_norm),
                                        _ptr(k_norm), float(eps), ws.handle, _stream(stream)))
@@ -313,7 +366,8 @@ def attention_decode_multi_noalloc(q, kv: KVCache, batch_index, tokens_per_seq: 
     if out is None:
         out = torch.empty_like(q)
     bi, pbi = _i32(batch_index)
-    sl, psl = _i32(seq_lens)
+    sl, psl = _i32(seq_lens, bi.size, "seq_lens")
+    _attn_io(q, kv.head_dim, bi.size * tokens_per_seq, out)
     _check(lib().dsb_attention_decode_multi_noalloc(_ptr(q), q.shape[1], ctypes.byref(kv), pbi, len(bi),
                                                     tokens_per_seq, psl, _ptr(out), _stream(stream)))
     return out
@@ -323,14 +377,30 @@ def kv_cache(k_cache, v_cache, dtype: int) -> KVCache:
     """Describe device caches ``[F, Hkv, ctx, D]``; the returned struct keeps
     the two tensors alive for as long as it lives."""
     f, hkv, ctx, d = k_cache.shape
+    if tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache shapes differ")
+    _need(k_cache, 2 * f * hkv * ctx * d, "k_cache", "16")
+    _need(v_cache, 2 * f * hkv * ctx * d, "v_cache", "16")
     kv = KVCache(_ptr(k_cache), _ptr(v_cache), dtype, f, hkv, ctx, d)
     kv._tensors = (k_cache, v_cache)
     return kv
 
 
+def _attn_io(q, head_dim: int, n_tok: int, out, out_kind: str = "f32"):
+    """q float32 [n_tok, Hq, head_dim]; out the same size."""
+    if q.dim() != 3 or q.shape[0] != n_tok or q.shape[2] != head_dim:
+        raise ValueError(f"q must be [n_seq*T={n_tok}, Hq, head_dim={head_dim}], got {tuple(q.shape)}")
+    _need(q, 4 * q.numel(), "q", "f32")
+    if out_kind == "f32":
+        _need(out, 4 * q.numel(), "out", "f32")
+
+
 def kv_scatter(kv: KVCache, batch_index, tokens_per_seq: int, pos, k, v, ws: Workspace, stream=None):
     bi, pbi = _i32(batch_index)
-    ps, pp = _i32(pos)
+    n_tok = bi.size * tokens_per_seq
+    ps, pp = _i32(pos, n_tok, "pos")
+    _need(k, 4 * n_tok * kv.n_kv_heads * kv.head_dim, "k", "f32")
+    _need(v, 4 * n_tok * kv.n_kv_heads * kv.head_dim, "v", "f32")
     _check(lib().dsb_kv_scatter(ctypes.byref(kv), pbi, len(bi), tokens_per_seq, pp, _ptr(k), _ptr(v), ws.handle,
                                 _stream(stream)))
 
@@ -342,7 +412,8 @@ def attention_decode_multi(q, kv: KVCache, batch_index, tokens_per_seq: int, seq
     if out is None:
         out = torch.empty_like(q)
     bi, pbi = _i32(batch_index)
-    sl, psl = _i32(seq_lens)
+    sl, psl = _i32(seq_lens, bi.size, "seq_lens")
+    _attn_io(q, kv.head_dim, bi.size * tokens_per_seq, out)
     _check(lib().dsb_attention_decode_multi(_ptr(q), hq, ctypes.byref(kv), pbi, len(bi), tokens_per_seq, psl,
                                             _ptr(out), ws.handle, _stream(stream)))
     return out
@@ -355,7 +426,8 @@ def attention_decode_multi_q8_0(q, kv: KVCache, batch_index, tokens_per_seq: int
     n_tok, hq, d = q.shape
     xq = torch.empty((n_tok, hq * d // 32 * 34), dtype=torch.uint8, device=q.device)
     bi, pbi = _i32(batch_index)
-    sl, psl = _i32(seq_lens)
+    sl, psl = _i32(seq_lens, bi.size, "seq_lens")
+    _attn_io(q, kv.head_dim, bi.size * tokens_per_seq, None, out_kind="none")
     _check(lib().dsb_attention_decode_multi_q8_0(_ptr(q), hq, ctypes.byref(kv), pbi, len(bi), tokens_per_seq, psl,
                                                  _ptr(xq), ws.handle, _stream(stream)))
     return xq
@@ -367,6 +439,10 @@ def kv_pages(k_pool, v_pool, dtype: int) -> KVPages:
     n_pages, hkv, page, d = k_pool.shape
     if page != KV_PAGE:
         raise ValueError("pages hold 128 keys")
+    if tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise ValueError("k_pool and v_pool shapes differ")
+    _need(k_pool, 2 * k_pool.numel(), "k_pool", "16")
+    _need(v_pool, 2 * v_pool.numel(), "v_pool", "16")
     kv = KVPages(_ptr(k_pool), _ptr(v_pool), dtype, n_pages, hkv, d)
     kv._tensors = (k_pool, v_pool)
     return kv
@@ -376,15 +452,18 @@ def _geometry(block_table, n_blocks, window):
     bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
     if bt.ndim != 2:
         raise ValueError("block_table is [n_seq, max_blocks]")
-    nb, pnb = _i32(n_blocks)
-    win, pwin = _i32(window)
+    nb, pnb = _i32(n_blocks, bt.shape[0], "n_blocks")
+    win, pwin = _i32(window, bt.shape[0], "window")
     return bt, bt.ctypes.data_as(_PI32), nb, pnb, win, pwin
 
 
 def kv_scatter_paged(kv: KVPages, block_table, n_blocks, window, tokens_per_seq: int, pos, k, v, ws: Workspace,
                      stream=None):
     bt, pbt, nb, pnb, win, pwin = _geometry(block_table, n_blocks, window)
-    ps, pp = _i32(pos)
+    n_tok = bt.shape[0] * tokens_per_seq
+    ps, pp = _i32(pos, n_tok, "pos")
+    _need(k, 4 * n_tok * kv.n_kv_heads * kv.head_dim, "k", "f32")
+    _need(v, 4 * n_tok * kv.n_kv_heads * kv.head_dim, "v", "f32")
     _check(lib().dsb_kv_scatter_paged(ctypes.byref(kv), pbt, bt.shape[1], pnb, pwin, bt.shape[0], tokens_per_seq, pp,
                                       _ptr(k), _ptr(v), ws.handle, _stream(stream)))
 
@@ -396,7 +475,8 @@ def attention_decode_paged(q, kv: KVPages, block_table, n_blocks, window, tokens
     if out is None:
         out = torch.empty_like(q)
     bt, pbt, nb, pnb, win, pwin = _geometry(block_table, n_blocks, window)
-    sl, psl = _i32(seq_lens)
+    sl, psl = _i32(seq_lens, bt.shape[0], "seq_lens")
+    _attn_io(q, kv.head_dim, bt.shape[0] * tokens_per_seq, out)
     _check(lib().dsb_attention_decode_paged(_ptr(q), hq, ctypes.byref(kv), pbt, bt.shape[1], pnb, pwin, bt.shape[0],
                                             tokens_per_seq, psl, _ptr(out), ws.handle, _stream(stream)))
     return out
@@ -406,6 +486,8 @@ def rmsnorm_q8_0(x, w, eps: float, stream=None):
     """q8_0 ``[n_tok, hidden/32*34]`` of the RMS-normed rows of ``x``."""
     import torch
     n_tok, hidden = x.shape
+    _need(x, 4 * n_tok * hidden, "x", "f32")
+    _need(w, 4 * hidden, "w", "f32")
     xq = torch.empty((n_tok, hidden // 32 * 34), dtype=torch.uint8, device=x.device)
     _check(lib().dsb_rmsnorm_q8_0(_ptr(x), _ptr(w), n_tok, hidden, float(eps), _ptr(xq), _stream(stream)))
     return xq
@@ -416,6 +498,7 @@ def silu_mul_q8_0(gu, stream=None):
     import torch
     n_tok, two_ffn = gu.shape
     ffn = two_ffn // 2
+    _need(gu, 4 * gu.numel(), "gu", "f32")
     xq = torch.empty((n_tok, ffn // 32 * 34), dtype=torch.uint8, device=gu.device)
     _check(lib().dsb_silu_mul_q8_0(_ptr(gu), n_tok, ffn, _ptr(xq), _stream(stream)))
     return xq
@@ -425,6 +508,7 @@ def embed_q8_0(table, vocab: int, hidden: int, token_ids, ws: Workspace, stream=
     """float32 ``[n_tok, hidden]``: dequantised embedding rows of the tokens."""
     import torch
     tk, ptk = _i32(token_ids)
+    _need(table, vocab * q8_rows_bytes(hidden), "table", "u8")
     h = torch.empty((len(tk), hidden), dtype=torch.float32, device=table.device)
     _check(lib().dsb_embed_q8_0(_ptr(table), vocab, hidden, ptk, len(tk), _ptr(h), ws.handle, _stream(stream)))
     return h
@@ -435,7 +519,11 @@ def rope_kv_write(qkv, n_q_heads: int, kv: KVCache, batch_index, tokens_per_seq:
     """Fused (optional per-head RMS norm +) RoPE + KV write on
     ``qkv[n_tok, (Hq + 2 Hkv) * D]`` (q rotated in place)."""
     bi, pbi = _i32(batch_index)
-    ps, pp = _i32(pos)
+    n_tok = bi.size * tokens_per_seq
+    ps, pp = _i32(pos, n_tok, "pos")
+    _need(qkv, 4 * n_tok * (n_q_heads + 2 * kv.n_kv_heads) * kv.head_dim, "qkv", "f32")
+    _need_opt(q_norm, 4 * kv.head_dim, "q_norm", "f32")
+    _need_opt(k_norm, 4 * kv.head_dim, "k_norm", "f32")
     r = rope_params(theta, yarn)
     _check(lib().dsb_rope_kv_write(_ptr(qkv), n_q_heads, ctypes.byref(kv), pbi, len(bi), tokens_per_seq, pp,
                                    ctypes.byref(r), _ptr(q_norm), _ptr(k_norm), float(eps), ws.handle,
@@ -563,20 +651,29 @@ class DecodeModel:
         qkv_rows = (n_q_heads + 2 * n_kv_heads) * head_dim
         layers = (LayerC * n_layers)()
         for l in range(n_layers):
-            layers[l].wqkv = _mat(weights["wqkv"][l], qkv_rows, hidden)
-            layers[l].wo = _mat(weights["wo"][l], hidden, n_q_heads * head_dim)
-            layers[l].wgu = _mat(weights["wgu"][l], 2 * ffn, hidden)
-            layers[l].wdown = _mat(weights["wdown"][l], hidden, ffn)
+            layers[l].wqkv = _mat(weights["wqkv"][l], qkv_rows, hidden, f"wqkv[{l}]")
+            layers[l].wo = _mat(weights["wo"][l], hidden, n_q_heads * head_dim, f"wo[{l}]")
+            layers[l].wgu = _mat(weights["wgu"][l], 2 * ffn, hidden, f"wgu[{l}]")
+            layers[l].wdown = _mat(weights["wdown"][l], hidden, ffn, f"wdown[{l}]")
+            _need(weights["attn_norm"][l], 4 * hidden, f"attn_norm[{l}]", "f32")
+            _need(weights["ffn_norm"][l], 4 * hidden, f"ffn_norm[{l}]", "f32")
+            if tuple(k_caches[l].shape[1:]) != (k_caches[0].shape[1], k_caches[0].shape[2], head_dim) or \
+                    k_caches[l].shape[1] != n_kv_heads:
+                raise ValueError(f"k_caches[{l}] must be [F, n_kv_heads={n_kv_heads}, ctx, head_dim={head_dim}]")
             layers[l].attn_norm = _ptr(weights["attn_norm"][l])
             layers[l].ffn_norm = _ptr(weights["ffn_norm"][l])
             layers[l].kv = kv_cache(k_caches[l], v_caches[l], cache_dtype)
             if "q_norm" in weights:
+                _need(weights["q_norm"][l], 4 * head_dim, f"q_norm[{l}]", "f32")
                 layers[l].q_norm = _ptr(weights["q_norm"][l])
             if "k_norm" in weights:
+                _need(weights["k_norm"][l], 4 * head_dim, f"k_norm[{l}]", "f32")
                 layers[l].k_norm = _ptr(weights["k_norm"][l])
         self._layers = layers
+        _need(weights["embed"], vocab * q8_rows_bytes(hidden), "embed", "u8")
+        _need(weights["final_norm"], 4 * hidden, "final_norm", "f32")
         self.c = ModelC(self.shape, _ptr(weights["embed"]), layers, _ptr(weights["final_norm"]),
-                        _mat(weights["head"], vocab, hidden))
+                        _mat(weights["head"], vocab, hidden, "head"))
         self.vocab = vocab
         self.ctx = k_caches[0].shape[2]
         self.full_batch_size = k_caches[0].shape[0]
@@ -589,9 +686,10 @@ class DecodeModel:
         n_seq = len(batch_index)
         if logits is None:
             logits = torch.empty((n_seq * tokens_per_seq, self.vocab), dtype=torch.float32, device="cuda")
-        tk, ptk = _i32(token_ids)
+        _need(logits, 4 * n_seq * tokens_per_seq * self.vocab, "logits", "f32")
+        tk, ptk = _i32(token_ids, n_seq * tokens_per_seq, "token_ids")
         bi, pbi = _i32(batch_index)
-        sl, psl = _i32(seq_lens)
+        sl, psl = _i32(seq_lens, n_seq, "seq_lens")
         _check(lib().dsb_decode_step(ctypes.byref(self.c), ptk, pbi, n_seq, tokens_per_seq, psl, _ptr(logits),
                                      ws.handle, _stream(stream)))
         return logits
@@ -605,15 +703,17 @@ class StepGraph:
 
     def __init__(self, model: DecodeModel, n_seq: int, tokens_per_seq: int, logits, ws: Workspace, stream=None):
         self.model, self.logits, self.ws = model, logits, ws
+        self.n_seq, self.T = n_seq, tokens_per_seq
+        _need(logits, 4 * n_seq * tokens_per_seq * model.vocab, "logits", "f32")
         handle = _P()
         _check(lib().dsb_step_graph_create(ctypes.byref(model.c), n_seq, tokens_per_seq, _ptr(logits), ws.handle,
                                            _stream(stream), ctypes.byref(handle)))
         self.handle = handle
 
     def launch(self, token_ids, batch_index, seq_lens, stream=None):
-        tk, ptk = _i32(token_ids)
-        bi, pbi = _i32(batch_index)
-        sl, psl = _i32(seq_lens)
+        tk, ptk = _i32(token_ids, self.n_seq * self.T, "token_ids")
+        bi, pbi = _i32(batch_index, self.n_seq, "batch_index")
+        sl, psl = _i32(seq_lens, self.n_seq, "seq_lens")
         _check(lib().dsb_step_graph_launch(self.handle, ptk, pbi, psl, _stream(stream)))
         return self.logits
 
