@@ -85,30 +85,40 @@ def _max_over_ranks(dist, value: float, device) -> float:
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    """nvidia-smi samples of SM clock and throttle reasons every 100 ms; the
+    summary keeps the samples stamped inside the region (between __enter__
+    returning and __exit__), or all of them if the region was too short to
+    catch one (``in_region`` says which)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 100
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t_start = self.t_end = None
 
     def __enter__(self):
+        import datetime
         fd, self.path = tempfile.mkstemp(prefix="dsb_clocks_", suffix=".csv")
         os.close(fd)
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
-        time.sleep(0.3)
+        time.sleep(0.2)
+        self.t_start = datetime.datetime.now()
         return self
 
     def __exit__(self, *exc):
+        import datetime
+        self.t_end = datetime.datetime.now()
+        time.sleep(2.0 * self.INTERVAL_MS / 1000.0)   # let a sample stamped before t_end reach the file
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -116,12 +126,22 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
+    @staticmethod
+    def _stamp(text):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text, fmt)
+            except ValueError:
+                pass
+        return None
+
     def summary(self):
         rows = []
         try:
             for line in open(self.path):
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                if len(parts) >= 10 and parts[2].replace(".", "").isdigit():
                     rows.append(parts)
         except Exception:
             pass
@@ -131,12 +151,15 @@ class ClockSampler:
             except Exception:
                 pass
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        sm = [float(r[1]) for r in rows]
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0, "in_region": False}
+        inside = [r for r in rows if self.t_start is not None and self.t_end is not None and
+                  (lambda t: t is not None and self.t_start <= t <= self.t_end)(self._stamp(r[0]))]
+        use = inside or rows
+        sm = [float(r[2]) for r in use]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
-                "samples": len(rows)}
+        reasons = sorted({names[i] for r in use for i in range(4) if r[6 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(use[0][3]), "reasons": reasons,
+                "samples": len(use), "in_region": bool(inside)}
 
 
 # ----------------------------------------------------------------- workloads

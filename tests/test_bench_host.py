@@ -41,3 +41,32 @@ def test_cpu_all_cores_runs_every_process():
     assert r["value"] > 0 and r["unit"] == "tokens/s"
     assert "oracle steps over" in r["sample"]
     assert bench._cpu_model().endswith(")")
+
+
+def test_clock_summary_keeps_the_samples_inside_the_region(tmp_path):
+    """Samples stamped before or after the timed region are left out; a
+    throttle reason seen only outside it does not count."""
+    import datetime
+    c = bench.ClockSampler(0)
+    c.path = str(tmp_path / "clocks.csv")
+    c.t_start = datetime.datetime(2026, 1, 2, 10, 0, 0, 100000)
+    c.t_end = datetime.datetime(2026, 1, 2, 10, 0, 0, 200000)
+    rows = [("10:00:00.050", 1400, "Active"), ("10:00:00.120", 2070, "Not Active"),
+            ("10:00:00.140", 2060, "Not Active"), ("10:00:00.260", 1000, "Active")]
+    with open(c.path, "w") as f:
+        for t, mhz, hw in rows:
+            f.write(f"2026/01/02 {t}, 0, {mhz}, 2070, 800.5, 0x0, {hw}, Not Active, Not Active, Not Active\n")
+    s = c.summary()
+    assert s["samples"] == 2 and s["in_region"] and s["sm_mhz"] == 2065 and s["reasons"] == []
+
+
+def test_clock_summary_falls_back_to_every_sample(tmp_path):
+    import datetime
+    c = bench.ClockSampler(0)
+    c.path = str(tmp_path / "clocks.csv")
+    c.t_start = datetime.datetime(2026, 1, 2, 10, 0, 1)
+    c.t_end = datetime.datetime(2026, 1, 2, 10, 0, 1, 5000)
+    with open(c.path, "w") as f:
+        f.write("2026/01/02 10:00:00.900, 0, 2070, 2070, 700, 0x0, Not Active, Not Active, Not Active, Active\n")
+    s = c.summary()
+    assert s["samples"] == 1 and not s["in_region"] and s["reasons"] == ["sw_power_cap"]
