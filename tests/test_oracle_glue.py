@@ -40,3 +40,20 @@ def test_embedding_is_dequantised_row():
     q, d = q8_0.unpack(table[3])
     want = (q.astype(np.float64) * d.astype(np.float64)[:, None]).reshape(64)
     assert np.array_equal(e[0], want) and np.array_equal(e[1], want)
+
+
+def test_silu_odd_part_is_the_identity():
+    """x*sigmoid(x) - (-x)*sigmoid(-x) = x*(sigmoid(x) + sigmoid(-x)) = x; a
+    sign slip in the exponent breaks it."""
+    x = np.linspace(-30.0, 30.0, 121)
+    one = np.ones_like(x)
+    assert np.allclose(glue.silu_mul(x, one) - glue.silu_mul(-x, one), x, rtol=1e-14, atol=1e-14)
+
+
+def test_rmsnorm_rows_are_independent():
+    x = np.random.default_rng(2).standard_normal((4, 32)) * np.array([[1e-3], [1.0], [1e3], [0.0]])
+    w = np.linspace(0.1, 2.0, 32)
+    full = glue.rmsnorm(x, w, 1e-6)
+    for t in range(4):
+        assert np.array_equal(full[t], glue.rmsnorm(x[t:t + 1], w, 1e-6)[0])
+    assert not full[3].any()   # an all-zero row stays zero
