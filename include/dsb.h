@@ -373,13 +373,19 @@ dsb_status dsb_rope_kv_write(float* qkv, int n_q_heads, const dsb_kv_cache* kv, 
  * no workspace: the split-K partials and the sequence table live in one static
  * 16 MiB device array that every device holds while the library is loaded.
  *   - The first call on a device looks up that array's address (with the
- *     device current); make that first call before any stream capture.
+ *     device current) and may load the library's kernels onto the device,
+ *     which the driver backs with device memory (lazy module loading): make
+ *     that first call outside the no-allocation context (e.g. at start-up)
+ *     and before any stream capture.  Later calls allocate nothing.
+ *   - The address is kept for the life of the process: resetting the device
+ *     (cudaDeviceReset) after the first call on it is not supported.
  *   - Limits: n_seq <= 256, and n_tok * n_q_heads * ceil(ctx/128) *
  *     (head_dim + 2) * 4 bytes of partials must fit in 16 MiB - 4 KiB;
  *     larger calls return DSB_ERR_UNSUPPORTED with a message.
  *   - All calls share the array: calls that overlap on the GPU (other streams,
  *     other threads) race; serialise them.  Nothing in it needs zeroing.
- *   - Calls no cudaMalloc, cudaFree or other allocating routine. */
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine, and uses no
+ *     heap memory per call: the sequence table is built on the stack. */
 dsb_status dsb_attention_decode_multi_noalloc(const float* q, int n_q_heads, const dsb_kv_cache* kv,
                                               const int32_t* batch_index, int n_seq, int tokens_per_seq,
                                               const int32_t* seq_lens, float* out, void* stream);
@@ -436,6 +442,36 @@ size_t dsb_step_workspace_bytes(const dsb_model_shape* shape, int max_tokens, in
 dsb_status dsb_decode_step(const dsb_model* model, const int32_t* token_ids, const int32_t* batch_index, int n_seq,
                            int tokens_per_seq, const int32_t* seq_lens, float* logits, dsb_workspace* ws,
                            void* stream);
+
+/* Stage trace of the step, for parity checking.  dsb_decode_step_trace runs
+ * the kernels of dsb_decode_step, in the same order and with the same launch
+ * plans, and after each stage copies that stage's result (on the same stream)
+ * into the caller's device buffers below; a NULL pointer skips that copy.  The
+ * copies change no value the step computes, so a test can hold every stage of
+ * every layer to its own operation's tolerance, fed the GPU's own inputs to
+ * that stage ([DS4] "Correctness": the batched step must agree with its
+ * parts).  Sizes with n_tok = n_seq*T; q8_0 rows are cols/32 blocks of 34 B. */
+typedef struct {
+  void* x_attn;    /* q8_0 [n_tok][hidden/32]: q8(rmsnorm(h_in, attn_norm)) */
+  float* qkv;      /* [n_tok][(Hq + 2 Hkv) D]: Wqkv x_attn, before the rope */
+  float* qkv_rope; /* the same after the rope + KV write kernel: q heads rotated (and normed) */
+  void* att_q8;    /* q8_0 [n_tok][Hq D/32]: q8(attention) */
+  float* h_attn;   /* [n_tok][hidden]: h_in + Wo att_q8 */
+  void* x_ffn;     /* q8_0 [n_tok][hidden/32]: q8(rmsnorm(h_attn, ffn_norm)) */
+  float* gu;       /* [n_tok][2 ffn]: Wgu x_ffn (gate columns, then up) */
+  void* act_q8;    /* q8_0 [n_tok][ffn/32]: q8(silu(gate) * up) */
+  float* h_out;    /* [n_tok][hidden]: h_attn + Wdown act_q8, the next layer's h_in */
+} dsb_layer_trace;
+
+typedef struct {
+  float* h_embed;                /* [n_tok][hidden]: the embedded tokens */
+  const dsb_layer_trace* layers; /* HOST array [n_layers], or NULL */
+  void* x_final;                 /* q8_0 [n_tok][hidden/32]: q8(rmsnorm(h_out, final_norm)) */
+} dsb_step_trace;
+
+dsb_status dsb_decode_step_trace(const dsb_model* model, const int32_t* token_ids, const int32_t* batch_index,
+                                 int n_seq, int tokens_per_seq, const int32_t* seq_lens, float* logits,
+                                 dsb_workspace* ws, const dsb_step_trace* trace, void* stream);
 
 /* The same step captured once into a CUDA graph for a fixed (n_seq, T) and
  * replayed.  The step's metadata (token ids, slots, seq_lens and what follows

@@ -927,7 +927,7 @@ cudaError_t run_matmul(const dsb_q8_0_mat& w, const void* xq, int n_tok, float* 
 dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, int tps, long long max_items,
                         float* logits, dsb_workspace* ws, int sms, cudaStream_t st, const int32_t* meta_src = nullptr,
                         size_t n_meta_words = 0, const int32_t* meta_words = nullptr,
-                        dsbk::EmbedParamNode* embed_node = nullptr) {
+                        dsbk::EmbedParamNode* embed_node = nullptr, const dsb_step_trace* trace = nullptr) {
   const dsb_model_shape& s = m->shape;
   const dsb_kv_cache& kv0 = m->layers[0].kv;
   const int n_tok = n_seq * tps;
@@ -959,27 +959,47 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
                                                          const_cast<int32_t*>(meta_dev), st, embed_node)
                              : dsbk::launch_embed(m->embed, s.hidden, meta_src ? meta_src : tokens_dev, n_tok, h,
                                                   meta_src, const_cast<int32_t*>(meta_dev), (int)n_meta_words, st);
+  // Stage trace (parity checking only): a copy of a stage's result after its
+  // kernel, on the same stream; nothing when the pointer is NULL.
+  const size_t ntz = (size_t)n_tok;
+  auto copy_out = [&](void* dst, const void* src, size_t bytes) {
+    if (e == cudaSuccess && dst) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st);
+    return e == cudaSuccess;
+  };
+  const size_t h_bytes = ntz * s.hidden * 4, xh_bytes = ntz * (s.hidden / 32) * 34;
+  if (trace) copy_out(trace->h_embed, h, h_bytes);
   dsbk::set_pdl(true);
   for (int l = 0; l < s.n_layers && e == cudaSuccess; ++l) {
     const dsb_layer& Ly = m->layers[l];
+    const dsb_layer_trace* tr = trace && trace->layers ? &trace->layers[l] : nullptr;
     if ((e = dsbk::launch_rmsnorm_quant(h, Ly.attn_norm, n_tok, s.hidden, s.rms_eps, xq, st)) != cudaSuccess) break;
+    if (tr && !copy_out(tr->x_attn, xq, xh_bytes)) break;
     if ((e = run_matmul(Ly.wqkv, xq, n_tok, qkv, nullptr, sms, pack, st)) != cudaSuccess) break;
+    if (tr && !copy_out(tr->qkv, qkv, ntz * qkv_stride * 4)) break;
     if ((e = dsbk::launch_rope_kv_write(qkv, qkv_stride, Hq, Hkv, D, pos_dev, bi_dev, tps, n_tok, Ly.kv.k, Ly.kv.v,
                                         Ly.kv.dtype, Ly.kv.ctx, freqs, st, Ly.q_norm, Ly.k_norm, s.rms_eps)) !=
         cudaSuccess)
       break;
+    if (tr && !copy_out(tr->qkv_rope, qkv, ntz * qkv_stride * 4)) break;
     if ((e = dsbk::launch_attention_decode_multi(qkv, qkv_stride, Hq, Ly.kv.k, Ly.kv.v, Ly.kv.dtype, Hkv, Ly.kv.ctx, D,
                                                  (long long)Ly.kv.full_batch_size * Hkv * Ly.kv.ctx,
                                                  mv, n_seq, tps, max_items, max_chunks, partials, att, xq, st)) !=
         cudaSuccess)
       break;
+    if (tr && !copy_out(tr->att_q8, xq, ntz * ((size_t)Hq * D / 32) * 34)) break;
     if ((e = run_matmul(Ly.wo, xq, n_tok, h, h, sms, pack, st)) != cudaSuccess) break;
+    if (tr && !copy_out(tr->h_attn, h, h_bytes)) break;
     if ((e = dsbk::launch_rmsnorm_quant(h, Ly.ffn_norm, n_tok, s.hidden, s.rms_eps, xq, st)) != cudaSuccess) break;
+    if (tr && !copy_out(tr->x_ffn, xq, xh_bytes)) break;
     if ((e = run_matmul(Ly.wgu, xq, n_tok, gu, nullptr, sms, pack, st)) != cudaSuccess) break;
+    if (tr && !copy_out(tr->gu, gu, ntz * 2 * (size_t)s.ffn * 4)) break;
     if ((e = dsbk::launch_silu_mul_quant(gu, n_tok, s.ffn, xq, st)) != cudaSuccess) break;
+    if (tr && !copy_out(tr->act_q8, xq, ntz * ((size_t)s.ffn / 32) * 34)) break;
     if ((e = run_matmul(Ly.wdown, xq, n_tok, h, h, sms, pack, st)) != cudaSuccess) break;
+    if (tr && !copy_out(tr->h_out, h, h_bytes)) break;
   }
   if (e == cudaSuccess) e = dsbk::launch_rmsnorm_quant(h, m->final_norm, n_tok, s.hidden, s.rms_eps, xq, st);
+  if (trace) copy_out(trace->x_final, xq, xh_bytes);
   if (e == cudaSuccess) e = run_matmul(m->head, xq, n_tok, logits, nullptr, sms, pack, st);
   dsbk::set_pdl(false);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "decode step launch");
@@ -1068,6 +1088,13 @@ size_t dsb_step_workspace_bytes(const dsb_model_shape* shape, int max_tokens, in
 dsb_status dsb_decode_step(const dsb_model* model, const int32_t* token_ids, const int32_t* batch_index, int n_seq,
                            int tokens_per_seq, const int32_t* seq_lens, float* logits, dsb_workspace* ws,
                            void* stream) {
+  return dsb_decode_step_trace(model, token_ids, batch_index, n_seq, tokens_per_seq, seq_lens, logits, ws, nullptr,
+                               stream);
+}
+
+dsb_status dsb_decode_step_trace(const dsb_model* model, const int32_t* token_ids, const int32_t* batch_index,
+                                 int n_seq, int tokens_per_seq, const int32_t* seq_lens, float* logits,
+                                 dsb_workspace* ws, const dsb_step_trace* trace, void* stream) {
   const dsb_kv_cache* kv0 = nullptr;
   dsb_status st = check_model(model, &kv0);
   if (st != DSB_OK) return st;
@@ -1084,7 +1111,8 @@ dsb_status dsb_decode_step(const dsb_model* model, const int32_t* token_ids, con
   const int32_t* dev = nullptr;
   st = stage(ws, words, cs, &dev);
   if (st != DSB_OK) return st;
-  return enqueue_step(model, dev, n_seq, tokens_per_seq, total * model->shape.n_kv_heads, logits, ws, sms, cs);
+  return enqueue_step(model, dev, n_seq, tokens_per_seq, total * model->shape.n_kv_heads, logits, ws, sms, cs,
+                      nullptr, 0, nullptr, nullptr, trace);
 }
 
 dsb_status dsb_step_graph_create(const dsb_model* model, int n_seq, int tokens_per_seq, float* logits,
@@ -1293,17 +1321,12 @@ extern "C" dsb_status dsb_attention_decode_multi_noalloc(const float* q, int n_q
                 "attention needs %zu bytes of partials; the no-allocation scratch holds %zu (use "
                 "dsb_attention_decode_multi with a workspace)",
                 need, dsbk::kNoAllocScratchBytes - dsbk::kNoAllocTableBytes);
-  std::vector<int32_t> chunk_off((size_t)n_seq + 1, 0);
-  long long total = 0;
-  for (int s = 0; s < n_seq; ++s) {
-    total += (seq_lens[s] + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
-    chunk_off[(size_t)s + 1] = (int32_t)total;
-  }
   void* scratch = nullptr;
   cudaError_t e = dsbk::noalloc_scratch(&scratch);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-allocation scratch)");
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  e = dsbk::launch_noalloc_table(batch_index, seq_lens, chunk_off.data(), n_seq, scratch, cs);
+  long long total = 0;
+  e = dsbk::launch_noalloc_table(batch_index, seq_lens, n_seq, scratch, &total, cs);
   if (e != cudaSuccess) return cuda_fail(e, "no-allocation sequence table");
   const int32_t* table = static_cast<const int32_t*>(scratch);
   dsbk::MetaView mv{table, table + n_seq, table + 2 * n_seq, nullptr};

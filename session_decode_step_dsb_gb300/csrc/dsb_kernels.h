@@ -182,8 +182,8 @@ constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
 constexpr int kNoAllocMaxSeqs = 256;
 constexpr size_t kNoAllocTableBytes = 4096;  // the sequence table at the start of the array
 cudaError_t noalloc_scratch(void** out);
-cudaError_t launch_noalloc_table(const int32_t* batch_index, const int32_t* seq_lens, const int32_t* chunk_off,
-                                 int n_seq, void* scratch, cudaStream_t st);
+cudaError_t launch_noalloc_table(const int32_t* batch_index, const int32_t* seq_lens, int n_seq, void* scratch,
+                                 long long* total_chunks, cudaStream_t st);
 
 unsigned int read_clear_error_matmul();
 unsigned int read_clear_error_attention();

@@ -11,7 +11,12 @@
 //
 // Rules of the shared array:
 //  * its device address is looked up once per device (cudaGetSymbolAddress,
-//    with that device current) on the first call made on that device;
+//    with that device current) on the first call made on that device.  That
+//    first call may also load this library's kernels onto the device (lazy
+//    module loading, the CUDA default), which the driver backs with device
+//    memory: make it outside the no-allocation context, e.g. at start-up;
+//  * the address is kept for the life of the process, so a device reset
+//    (cudaDeviceReset) after the first call on that device is not supported;
 //  * every call on a device uses the same array, so calls whose work overlaps
 //    on the GPU (e.g. on two streams at once) race -- serialise them;
 //  * nothing in it has to start at zero: each call writes its sequence table
@@ -21,6 +26,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "dsb.h"
 #include "dsb_kernels.h"
 
 namespace dsbk {
@@ -69,15 +75,19 @@ cudaError_t noalloc_scratch(void** out) {
   return cudaSuccess;
 }
 
-cudaError_t launch_noalloc_table(const int32_t* batch_index, const int32_t* seq_lens, const int32_t* chunk_off,
-                                 int n_seq, void* scratch, cudaStream_t st) {
+// The table is built on this thread's stack (no heap use per call); chunk_off
+// is the running count of 128-key chunks.  *total_chunks = chunk_off[n_seq].
+cudaError_t launch_noalloc_table(const int32_t* batch_index, const int32_t* seq_lens, int n_seq, void* scratch,
+                                 long long* total_chunks, cudaStream_t st) {
   NoAllocTable tab;
   tab.n_seq = n_seq;
+  tab.chunk_off[0] = 0;
   for (int i = 0; i < n_seq; ++i) {
     tab.batch_index[i] = batch_index[i];
     tab.seq_lens[i] = seq_lens[i];
+    tab.chunk_off[i + 1] = tab.chunk_off[i] + (seq_lens[i] + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
   }
-  for (int i = 0; i <= n_seq; ++i) tab.chunk_off[i] = chunk_off[i];
+  *total_chunks = tab.chunk_off[n_seq];
   noalloc_table_kernel<<<1, 256, 0, st>>>(tab, static_cast<int32_t*>(scratch));
   return cudaGetLastError();
 }

@@ -549,9 +549,21 @@ class ModelC(ctypes.Structure):
                 ("final_norm", ctypes.c_void_p), ("head", Q8Mat)]
 
 
+class LayerTraceC(ctypes.Structure):
+    _fields_ = [("x_attn", ctypes.c_void_p), ("qkv", ctypes.c_void_p), ("qkv_rope", ctypes.c_void_p),
+                ("att_q8", ctypes.c_void_p), ("h_attn", ctypes.c_void_p), ("x_ffn", ctypes.c_void_p),
+                ("gu", ctypes.c_void_p), ("act_q8", ctypes.c_void_p), ("h_out", ctypes.c_void_p)]
+
+
+class StepTraceC(ctypes.Structure):
+    _fields_ = [("h_embed", ctypes.c_void_p), ("layers", ctypes.POINTER(LayerTraceC)), ("x_final", ctypes.c_void_p)]
+
+
 SIGNATURES.update({
     "dsb_step_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(ModelShapeC), _I, _I]),
     "dsb_decode_step": (_I, [ctypes.POINTER(ModelC), _PI32, _PI32, _I, _I, _PI32, _P, _P, _P]),
+    "dsb_decode_step_trace": (_I, [ctypes.POINTER(ModelC), _PI32, _PI32, _I, _I, _PI32, _P, _P,
+                                   ctypes.POINTER(StepTraceC), _P]),
     "dsb_step_graph_create": (_I, [ctypes.POINTER(ModelC), _I, _I, _P, _P, _P, ctypes.POINTER(_P)]),
     "dsb_step_graph_launch": (_I, [_P, _PI32, _PI32, _PI32, _P]),
     "dsb_step_graph_destroy": (_I, [_P]),
@@ -693,6 +705,44 @@ class DecodeModel:
         _check(lib().dsb_decode_step(ctypes.byref(self.c), ptk, pbi, n_seq, tokens_per_seq, psl, _ptr(logits),
                                      ws.handle, _stream(stream)))
         return logits
+
+    def step_trace(self, token_ids, batch_index, tokens_per_seq: int, seq_lens, ws: Workspace, stream=None):
+        """The step with every stage's result copied out (dsb_decode_step_trace).
+
+        Returns ``(logits, trace)``: ``trace`` maps ``"h_embed"`` and
+        ``"x_final"`` to device tensors and ``"layers"`` to one dict per layer
+        (``x_attn, qkv, qkv_rope, att_q8, h_attn, x_ffn, gu, act_q8, h_out``);
+        q8_0 stages are uint8 ``[n_tok, cols/32*34]``, the others float32."""
+        import torch
+        n_seq = len(batch_index)
+        n_tok = n_seq * tokens_per_seq
+        sh = self.shape
+        hid, hq, hkv, d, ffn = sh.hidden, sh.n_q_heads, sh.n_kv_heads, sh.head_dim, sh.ffn
+
+        def f32(cols):
+            return torch.empty((n_tok, cols), dtype=torch.float32, device="cuda")
+
+        def q8(cols):
+            return torch.empty((n_tok, q8_rows_bytes(cols)), dtype=torch.uint8, device="cuda")
+
+        layers = []
+        arr = (LayerTraceC * sh.n_layers)()
+        for l in range(sh.n_layers):
+            t = {"x_attn": q8(hid), "qkv": f32((hq + 2 * hkv) * d), "qkv_rope": f32((hq + 2 * hkv) * d),
+                 "att_q8": q8(hq * d), "h_attn": f32(hid), "x_ffn": q8(hid), "gu": f32(2 * ffn), "act_q8": q8(ffn),
+                 "h_out": f32(hid)}
+            for k, v in t.items():
+                setattr(arr[l], k, _ptr(v))
+            layers.append(t)
+        trace = {"h_embed": f32(hid), "x_final": q8(hid), "layers": layers}
+        c = StepTraceC(_ptr(trace["h_embed"]), arr, _ptr(trace["x_final"]))
+        logits = torch.empty((n_tok, self.vocab), dtype=torch.float32, device="cuda")
+        tk, ptk = _i32(token_ids, n_tok, "token_ids")
+        bi, pbi = _i32(batch_index)
+        sl, psl = _i32(seq_lens, n_seq, "seq_lens")
+        _check(lib().dsb_decode_step_trace(ctypes.byref(self.c), ptk, pbi, n_seq, tokens_per_seq, psl, _ptr(logits),
+                                           ws.handle, ctypes.byref(c), _stream(stream)))
+        return logits, trace
 
     def graph(self, n_seq: int, tokens_per_seq: int, logits, ws: Workspace, stream=None) -> "StepGraph":
         return StepGraph(self, n_seq, tokens_per_seq, logits, ws, stream)

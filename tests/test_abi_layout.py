@@ -20,6 +20,8 @@ STRUCTS = {  # C type -> binding class name
     "dsb_model_shape": "ModelShapeC",
     "dsb_layer": "LayerC",
     "dsb_model": "ModelC",
+    "dsb_layer_trace": "LayerTraceC",
+    "dsb_step_trace": "StepTraceC",
 }
 MACROS = {"DSB_MAX_SEQS": "MAX_SEQS", "DSB_MAX_TOKENS": "MAX_TOKENS", "DSB_NARROW_MAX": "NARROW_MAX",
           "DSB_ATTN_CHUNK": "ATTN_CHUNK", "DSB_KV_PAGE": "KV_PAGE", "DSB_F16": "DSB_F16", "DSB_BF16": "DSB_BF16",

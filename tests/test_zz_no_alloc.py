@@ -60,6 +60,44 @@ def test_no_alloc_matches_workspace_entry_on_two_calls(cuda_device):
     d.device_error()
 
 
+@pytest.mark.gpu
+def test_no_alloc_at_its_limits_and_allocates_nothing(cuda_device):
+    """The largest sequence table (256 sequences) and partials that fill the
+    scratch exactly, each against the workspace entry and the oracle; after a
+    first call (which may load kernels), a second call leaves the device's free
+    memory unchanged."""
+    import torch
+    d = _dsb()
+    rng = np.random.default_rng(7)
+    n_max = 256
+    lens256 = rng.integers(1, 257, n_max).astype(np.int32)
+    # 18 tokens x 56 heads x 32 chunks x (128 + 2) x 4 bytes = 16 MiB - 4 KiB
+    cap_lens = rng.integers(1, 4097, 18).astype(np.int32)
+    cases = [
+        (n_max, 8, 2, 256, 64, "f16", rng.permutation(n_max).astype(np.int32), lens256, 1),
+        (18, 56, 8, 4096, 128, "bf16", rng.permutation(18).astype(np.int32), cap_lens, 1),
+    ]
+    for n, (F, hq, hkv, C, D, dtype, bi, lens, T) in enumerate(cases):
+        kc, vc, q, kv = _case(10 + n, F, hq, hkv, C, D, dtype, bi, lens, T)
+        qd = to_dev(q)
+        ws = d.Workspace(len(bi) * T, hq, D, C)
+        ref = to_host(d.attention_decode_multi(qd, kv, bi, T, lens, ws))
+        out = torch.empty_like(qd)
+        d.attention_decode_multi_noalloc(qd, kv, bi, T, lens, out=out)
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
+        out.zero_()
+        d.attention_decode_multi_noalloc(qd, kv, bi, T, lens, out=out)
+        torch.cuda.synchronize()
+        free1 = torch.cuda.mem_get_info()[0]
+        assert free1 == free0, f"case {n}: free device memory moved by {free0 - free1} bytes across a call"
+        got = to_host(out)
+        assert_close(got, ref, ATTN_RTOL, ATTN_ATOL, f"no-alloc limit case {n} vs workspace entry")
+        oracle = oatt.attention_decode_multi(q, okv.bits_to_f64(kc, dtype), okv.bits_to_f64(vc, dtype), bi, T, lens)
+        assert_close(got, oracle, ATTN_RTOL, ATTN_ATOL, f"no-alloc limit case {n} vs oracle")
+    d.device_error()
+
+
 def test_no_alloc_rejects_sizes_beyond_its_scratch():
     from session_decode_step_dsb_gb300 import build, dsb
     import os
