@@ -786,7 +786,8 @@ def run_probe(spec: str):
     narrow matmul three times per n_tok on N(0, 0.02) weights;
     ``wide:ROWS:COLS:NTOK`` the tensor-core matmul three times;
     ``attention:WORKLOAD`` runs the decode attention four times on that
-    workload's cache shape (b sequences, seq_lens uniform)."""
+    workload's cache shape (b sequences, seq_lens uniform); ``dp4a`` measures
+    the dp4a issue rate and latency (one JSON line)."""
     import torch
     from session_decode_step_dsb_gb300 import dsb
     kind, *rest = spec.split(":")
@@ -820,6 +821,40 @@ def run_probe(spec: str):
         out = torch.empty_like(q)
         for _ in range(4):
             dsb.attention_decode_multi(q, kv, bi, T, lens, ws, out=out)
+    elif kind == "dp4a":
+        # the dp4a issue rate (many warps, independent chains) and latency
+        # (one dependent chain), from which the narrow matmul's arithmetic
+        # ceiling follows: 8 dp4a per q8_0 block and token
+        props = torch.cuda.get_device_properties(0)
+        sms = props.multi_processor_count
+        out = torch.zeros(4, dtype=torch.int32, device="cuda")
+        res = {}
+        for blocks in (sms * 8, sms * 32):
+            iters = 4096
+            for _ in range(2):
+                dsb.probe_dp4a(0, blocks, iters, out)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            dsb.probe_dp4a(0, blocks, iters, out)
+            e1.record()
+            e1.synchronize()
+            sec = e0.elapsed_time(e1) * 1e-3
+            ops = blocks * 256 * 8 * iters
+            res[f"rate_{blocks // sms}_ctas_per_sm"] = {"dp4a_per_s": ops / sec, "seconds": sec}
+        dsb.probe_dp4a(1, 1, 1 << 16, out)
+        torch.cuda.synchronize()
+        cyc, it = int(out[1].item()) & 0xFFFFFFFF, int(out[2].item())
+        res["latency_cycles"] = cyc / it
+        with ClockSampler(0) as clk:
+            dsb.probe_dp4a(0, sms * 32, 1 << 15, out)
+            torch.cuda.synchronize()
+        clocks = clk.summary()
+        res["clocks"] = clocks
+        mhz = clocks.get("sm_mhz") or 2070.0
+        best = max(v["dp4a_per_s"] for k, v in res.items() if k.startswith("rate_"))
+        res["dp4a_per_clk_per_sm"] = best / (sms * mhz * 1e6)
+        res["sms"] = sms
+        print(json.dumps({"probe": "dp4a", **res}))
     else:
         raise SystemExit(f"unknown probe {spec!r}")
     torch.cuda.synchronize()
@@ -847,7 +882,7 @@ def main(argv=None):
                     help="skip the llama-68m-shaped step and the b x K speculative grid")
     ap.add_argument("--probe", default=None,
                     help="run one kernel a few times for a profiler and exit: matmul:ROWS:COLS:NTOK[,..], "
-                         "wide:ROWS:COLS:NTOK or attention:WORKLOAD")
+                         "wide:ROWS:COLS:NTOK, attention:WORKLOAD, or dp4a (the dp4a rate / latency probe)")
     args = ap.parse_args(argv)
     if args.probe:
         run_probe(args.probe)

@@ -390,6 +390,19 @@ dsb_status dsb_attention_decode_multi_noalloc(const float* q, int n_q_heads, con
                                               const int32_t* batch_index, int n_seq, int tokens_per_seq,
                                               const int32_t* seq_lens, float* out, void* stream);
 
+/* ---- measurement probe -------------------------------------------------------
+ * The issue rate and latency of the four-way int8 dot product (__dp4a) the
+ * narrow q8_0 matmul is built on, so that its arithmetic ceiling comes from a
+ * measurement of committed code.  Not part of the decode step.
+ *   mode 0: `blocks` CTAs of 256 threads, each thread 8 independent chains of
+ *           `iters` dp4a (8 * iters * 256 * blocks in total); time the call
+ *           with events on `stream`.
+ *   mode 1: one thread runs one dependent chain of `iters` dp4a; out[1] = SM
+ *           clock cycles it took, out[2] = iters.
+ * out: device uint32[3].  DSB_ERR_INVALID_ARG for another mode or sizes out of
+ * range; DSB_ERR_CUDA if the launch fails. */
+dsb_status dsb_probe_dp4a(int mode, int blocks, int iters, uint32_t* out, void* stream);
+
 /* ---- the whole decode step -------------------------------------------------
  * A llama-style pre-norm decoder driven through the kernels above, one pass
  * for all live sessions ([DS4] "What" and "Design note": dense stages batched

@@ -65,8 +65,9 @@ struct PagedView {
 };
 
 int matmul_split(int64_t rows, int64_t cols, int num_sms);
-// The (tiling, cluster split) plan of a matrix: returns S, sets rows_mode.
-int matmul_plan_of(int64_t rows, int64_t cols, int num_sms, bool* rows_mode);
+// The (tiling, cluster split) plan of a matrix: returns S (CTAs per cluster
+// along k), sets *G (row groups of 32 rows per CTA tile).
+int matmul_plan_of(int64_t rows, int64_t cols, int num_sms, int* G);
 // Narrow matmul (n_tok <= 16) whose activations are float rows quantised in
 // the kernel: pro 1 = RMSNorm (norm_w, eps) of xf[n_tok][xf_stride] over cols
 // values then q8_0; pro 2 = silu(gate) * up of xf = [gate | up] (stride

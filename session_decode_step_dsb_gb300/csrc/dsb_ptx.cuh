@@ -102,6 +102,23 @@ __device__ __forceinline__ float ld_dsmem_f32(const float* p, uint32_t rank) {
   return v;
 }
 
+// The address, in the cluster's shared window, of the variable at `p` (this
+// CTA's shared window) in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(p)), "r"(rank));
+  return remote;
+}
+
+// A float from a cluster shared-window address (cluster_map).  Volatile, so it
+// stays after the cluster barrier that publishes the value, but without a
+// memory clobber, so independent loads of neighbouring outputs overlap.
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
 // Programmatic dependent launch.  pdl_wait() blocks until the grid this one
 // depends on has completed and its writes are visible (a no-op when the launch
 // carries no programmatic dependency); pdl_trigger() lets the dependent grid be
@@ -120,6 +137,24 @@ __device__ __forceinline__ uint4 ld_v4(const void* p) {
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p)
                : "memory");
+  return r;
+}
+
+// The same, for data written by the previous kernel of a programmatic chain
+// and read after pdl_wait(): volatile (not hoisted above the wait) but without
+// a memory clobber, so a thread's loads of several blocks stay in flight
+// together instead of waiting for each other's shared-memory stores.
+__device__ __forceinline__ uint32_t ld_u32_after_wait(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint4 ld_v4_after_wait(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
   return r;
 }
 

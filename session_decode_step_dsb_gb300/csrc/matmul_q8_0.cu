@@ -9,16 +9,15 @@
 // weight block must cross HBM once and serve every token.
 //
 // GB300 design (differs from the page's one-warp-per-row kernel):
-//  * A CTA owns 32 weight rows (lane = row) and a contiguous range of 8-block
-//    k-steps; its 4 warps take interleaved k-steps.  A k-step of one row is
-//    8 blocks = 272 bytes = 17 x 16 bytes, so every row chunk is 16-byte
-//    aligned whenever cols % 256 == 0.
+//  * One persistent CTA per SM, 8 warps.  A warp owns 32 weight rows (lane =
+//    row) and every token; k-steps of 8 blocks = 272 bytes = 17 x 16 bytes,
+//    so every row chunk is 16-byte aligned whenever cols % 256 == 0.
 //  * Each warp streams its 32 row chunks with 1-D TMA bulk copies
-//    (cp.async.bulk, one 272-byte copy per lane) into a private NSTAGE-deep
-//    shared-memory ring guarded by mbarriers; no thread spends instructions on
-//    global loads of weights.  A lane reads its chunk back with 17 conflict-free
-//    16-byte shared loads (the 272-byte stride is an odd number of 16-byte
-//    bank groups) and unpacks the 34-byte blocks with funnel shifts.
+//    (cp.async.bulk, one 272-byte copy per lane) into its own 2-stage
+//    shared-memory ring guarded by mbarriers; it reads a stage back into
+//    registers (17 conflict-free 16-byte shared loads per lane), hands the
+//    stage to the copy two units ahead and computes from registers, so two
+//    copies stay in flight per warp and no warp waits on another in the k loop.
 //  * Activation blocks of the CTA's k-range are unpacked once, at kernel start,
 //    into a word-major layout: for each block and each of its eight 4-code
 //    words, that word of every token side by side (then the fp32 scales), so
@@ -26,16 +25,16 @@
 //    16-byte load.
 //  * Block dots are __dp4a chains started from the bit pattern of 1.5 * 2^23:
 //    |isum| <= 32*127*127 < 2^22, so the int32 result read as a float is
-//    1.5*2^23 + isum exactly and one FADD converts it (no I2F).  The chains
-//    of all n_tok tokens advance word by word together, so consecutive dp4a
-//    instructions never depend on each other.
-//  * When rows alone give too few CTAs, k is split over the CTAs of a thread
-//    block cluster (<= 16 CTAs) and the partial sums are added through distributed
-//    shared memory in cluster-rank order; every CTA of the cluster sums a
-//    slice of the tile, from double-buffered sums, one cluster barrier per
-//    tile.  No atomics; every reduction order depends only on (rows, cols) and
-//    the device, never on n_tok, so column t of an n_tok = k call is bitwise
-//    equal to the n_tok = 1 call.
+//    1.5*2^23 + isum exactly and one FADD converts it (no I2F).  Four tokens'
+//    chains advance word by word together, so consecutive dp4a instructions
+//    never depend on each other.
+//  * A CTA tile is G row groups; the 8 / G warps of a group take interleaved
+//    k-steps, and k is further split over the CTAs of a thread block cluster
+//    (<= 16 CTAs).  Partial sums are added in warp order in shared memory and
+//    in cluster-rank order through distributed shared memory, one cluster
+//    barrier per tile (double-buffered sums).  No atomics; every reduction
+//    order depends only on (rows, cols) and the device, never on n_tok, so
+//    column t of an n_tok = k call is bitwise equal to the n_tok = 1 call.
 #include "matmul_q8_0_kernel.cuh"
 
 namespace dsbk {
@@ -43,20 +42,35 @@ namespace dsbk {
 namespace {
 
 struct Plan {
-  bool rows_mode;
-  int S;
+  int G;  // row groups (of 32 rows) per CTA tile; 8 / G warps per group
+  int S;  // CTAs per cluster along k
 };
+
+int max_smem_optin() {
+  static std::mutex mu;
+  static int dev_cached = -1, value = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev != dev_cached) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+    value = v;
+    dev_cached = dev;
+  }
+  return value;
+}
 
 // Depends on (rows, cols) and the device only -- never on n_tok -- so that
 // the summation order of every output is the same for every n_tok.  Each CTA
-// of a cluster keeps the activations of its k-range in shared memory, which at
-// n_tok = 16 allows at most 8 k-steps (36 KiB) next to the weight rings.
-// Rows mode: 128-row tiles, warps own 32 rows over the CTA's whole k-range;
-// k-split mode: 32-row tiles whose k-steps the 4 warps share.  Among the
-// admissible (mode, S) the smallest estimated makespan (tiles per cluster x
-// k-steps per warp, plus a per-tile reduction cost) wins, with the number of
-// clusters that fit on the device at once taken from the occupancy query of
-// the n_tok = 16 instance (the largest shared memory).
+// keeps the activations of its k-range in shared memory, so at n_tok = 16 the
+// k-range of one CTA is bounded (about 12 k-steps next to the weight rings);
+// longer rows are split over a cluster.  Among the admissible (G, S) the
+// smallest estimated makespan wins: rounds of tiles over the clusters that fit
+// on the device at once (occupancy query of the n_tok = 16 instance, the
+// largest shared memory) x the k-steps of one warp per tile plus the tile's
+// reduction costs, stretched when too few SMs are busy to draw the HBM
+// bandwidth (each SM keeps ~140 KB of weights in flight).
 Plan matmul_plan(int64_t rows, int64_t cols, int num_sms) {
   struct Memo {
     int64_t rows, cols;
@@ -70,37 +84,34 @@ Plan matmul_plan(int64_t rows, int64_t cols, int num_sms) {
   for (int i = 0; i < n_memo; ++i)
     if (memo[i].rows == rows && memo[i].cols == cols && memo[i].num_sms == num_sms) return memo[i].plan;
   const int nks = (int)(cols / 256);
-  int s_max = nks < kMaxCluster ? nks : kMaxCluster;
-  int s_min = (nks + 7) / 8;
-  if (s_min > s_max) s_min = s_max;
-  if (s_min < 1) s_min = 1;
-  Plan best{false, s_min};
+  const int s_max = nks < kMaxCluster ? nks : kMaxCluster;
+  const size_t cap = (size_t)max_smem_optin();
+  Plan best{kWarps, s_max};
   double best_cost = 1e30;
-  bool queried = true;
-  for (int mode = 0; mode < 2; ++mode) {
-    const bool rm = mode == 1;
-    const int tile = rm ? kPairs * kRowsPerCta : kRowsPerCta;
-    const int tiles = (int)((rows + tile - 1) / tile);
-    for (int S = s_min; S <= s_max; ++S) {
-      const size_t smem = smem_bytes((nks + S - 1) / S, 16, rm);
+  bool queried = cap > 0;
+  for (int G = kWarps; G >= 1; G /= 2) {
+    const int KW = kWarps / G;
+    const long long tiles = (rows + 32LL * G - 1) / (32LL * G);
+    for (int S = 1; S <= s_max; ++S) {
+      const int kr = (nks + S - 1) / S;
+      const size_t smem = smem_bytes(kr, 16, G, S);
+      if (cap > 0 && smem > cap) continue;
       int clusters = 0;
-      const cudaError_t e = rm ? cluster_capacity<16, false, true, 0>(S, smem, &clusters)
-                               : cluster_capacity<16, false, false, 0>(S, smem, &clusters);
+      const cudaError_t e = cluster_capacity<16, false, 0>(S, smem, &clusters);
       if (e != cudaSuccess) {
         (void)cudaGetLastError();
         queried = false;
-        clusters = (2 * num_sms) / S;  // estimate: two CTAs per SM
+        clusters = num_sms / S;  // estimate: one CTA per SM
       }
       if (clusters < 1) continue;
-      const int per = (tiles + clusters - 1) / clusters;
-      const int ksteps = (nks + S - 1) / S;
-      // time ~ tiles per cluster x (k-steps each warp runs + per-tile sync cost)
-      const double sync = (rm && S == 1) ? 0.0 : 0.5;
-      const double warp_steps = rm ? (double)ksteps : (double)((ksteps + kPairs - 1) / kPairs);
-      const double c = per * (warp_steps + sync);
+      const long long rounds = (tiles + clusters - 1) / clusters;
+      const double per_tile = (double)((kr + KW - 1) / KW) + (KW > 1 ? 0.3 : 0.0) + (S > 1 ? 0.4 : 0.0);
+      const long long busy = (tiles < clusters ? tiles : clusters) * S;
+      const double stretch = busy >= 96 ? 1.0 : 96.0 / (double)busy;
+      const double c = (double)rounds * per_tile * stretch;
       if (c < best_cost - 1e-9) {
         best_cost = c;
-        best = Plan{rm, S};
+        best = Plan{G, S};
       }
     }
   }
@@ -112,9 +123,9 @@ Plan matmul_plan(int64_t rows, int64_t cols, int num_sms) {
 
 int matmul_split(int64_t rows, int64_t cols, int num_sms) { return matmul_plan(rows, cols, num_sms).S; }
 
-int matmul_plan_of(int64_t rows, int64_t cols, int num_sms, bool* rows_mode) {
+int matmul_plan_of(int64_t rows, int64_t cols, int num_sms, int* G) {
   const Plan pl = matmul_plan(rows, cols, num_sms);
-  *rows_mode = pl.rows_mode;
+  *G = pl.G;
   return pl.S;
 }
 
@@ -122,7 +133,7 @@ size_t matmul_smem_bytes(int64_t rows, int64_t cols, int n_tok, int num_sms) {
   const Plan pl = matmul_plan(rows, cols, num_sms);
   const int nks = (int)(cols / 256);
   const int kr_max = (nks + pl.S - 1) / pl.S;
-  return smem_bytes(kr_max, n_tok, pl.rows_mode);
+  return smem_bytes(kr_max, n_tok, pl.G, pl.S);
 }
 
 cudaError_t launch_matmul_q8_0_narrow(const void* W, int64_t rows, int64_t cols, const void* xq, int n_tok,
@@ -133,11 +144,8 @@ cudaError_t launch_matmul_q8_0_narrow(const void* W, int64_t rows, int64_t cols,
   const uint8_t* w8 = static_cast<const uint8_t*>(W);
   ActSrc src;
   src.xq = static_cast<const uint8_t*>(xq);
-  if (isum)
-    return pl.rows_mode ? dispatch<true, true, 0>(n_tok, w8, (int)rows, nb, src, y, residual, isum, pl.S, smem, st)
-                        : dispatch<true, false, 0>(n_tok, w8, (int)rows, nb, src, y, residual, isum, pl.S, smem, st);
-  return pl.rows_mode ? dispatch<false, true, 0>(n_tok, w8, (int)rows, nb, src, y, residual, isum, pl.S, smem, st)
-                      : dispatch<false, false, 0>(n_tok, w8, (int)rows, nb, src, y, residual, isum, pl.S, smem, st);
+  if (isum) return dispatch<true, 0>(n_tok, w8, (int)rows, nb, src, y, residual, isum, pl.G, pl.S, smem, st);
+  return dispatch<false, 0>(n_tok, w8, (int)rows, nb, src, y, residual, isum, pl.G, pl.S, smem, st);
 }
 
 namespace {

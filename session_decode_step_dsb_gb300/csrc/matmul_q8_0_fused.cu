@@ -12,17 +12,17 @@
 namespace dsbk {
 
 size_t matmul_fused_smem_bytes(int64_t rows, int64_t cols, int n_tok, int pro, int num_sms) {
-  bool rows_mode = false;
-  const int S = matmul_plan_of(rows, cols, num_sms, &rows_mode);
+  int G = 0;
+  const int S = matmul_plan_of(rows, cols, num_sms, &G);
   const int nks = (int)(cols / 256);
-  return smem_bytes((nks + S - 1) / S, n_tok, rows_mode, pro);
+  return smem_bytes((nks + S - 1) / S, n_tok, G, S, pro);
 }
 
 cudaError_t launch_matmul_q8_0_fused(int pro, const void* W, int64_t rows, int64_t cols, const float* xf,
                                      int xf_stride, const float* norm_w, float eps, int n_tok, float* y,
                                      const float* residual, int num_sms, cudaStream_t st) {
-  bool rows_mode = false;
-  const int S = matmul_plan_of(rows, cols, num_sms, &rows_mode);
+  int G = 0;
+  const int S = matmul_plan_of(rows, cols, num_sms, &G);
   const size_t smem = matmul_fused_smem_bytes(rows, cols, n_tok, pro, num_sms);
   const int nb = (int)(cols / 32);
   const uint8_t* w8 = static_cast<const uint8_t*>(W);
@@ -31,12 +31,8 @@ cudaError_t launch_matmul_q8_0_fused(int pro, const void* W, int64_t rows, int64
   src.norm_w = norm_w;
   src.eps = eps;
   src.xf_stride = xf_stride;
-  if (pro == 1)
-    return rows_mode ? dispatch<false, true, 1>(n_tok, w8, (int)rows, nb, src, y, residual, nullptr, S, smem, st)
-                     : dispatch<false, false, 1>(n_tok, w8, (int)rows, nb, src, y, residual, nullptr, S, smem, st);
-  if (pro == 2)
-    return rows_mode ? dispatch<false, true, 2>(n_tok, w8, (int)rows, nb, src, y, residual, nullptr, S, smem, st)
-                     : dispatch<false, false, 2>(n_tok, w8, (int)rows, nb, src, y, residual, nullptr, S, smem, st);
+  if (pro == 1) return dispatch<false, 1>(n_tok, w8, (int)rows, nb, src, y, residual, nullptr, G, S, smem, st);
+  if (pro == 2) return dispatch<false, 2>(n_tok, w8, (int)rows, nb, src, y, residual, nullptr, G, S, smem, st);
   return cudaErrorInvalidValue;
 }
 

@@ -4,6 +4,7 @@
 // parallel).  Everything here has internal linkage: each unit holds its own
 // instances, host caches and device error flag.
 #pragma once
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -18,18 +19,26 @@ namespace dsbk {
 
 namespace {
 
-constexpr int kPairs = 4;             // row groups (or k-step lanes) of a CTA
-constexpr int kWarps = 2 * kPairs;     // two warps per row group: one per token half
+constexpr int kWarps = 8;              // warps of a CTA; one CTA per SM
 constexpr int kThreads = kWarps * 32;
-constexpr int kRowsPerCta = 32;
-constexpr int kChunkBytes = 272;  // 8 blocks of 34 bytes
-constexpr int kStage = kRowsPerCta * kChunkBytes;
-constexpr int kNStage = 2;
-constexpr int kMaxCluster = 16;  // k-split CTAs per cluster (above 8: a non-portable cluster size)
+constexpr int kRowsPerWarp = 32;        // lane = weight row
+constexpr int kChunkBytes = 272;        // one k-step of a row: 8 blocks of 34 bytes
+constexpr int kStage = kRowsPerWarp * kChunkBytes;
+constexpr int kNStage = 2;              // weight stages per warp
+constexpr int kMaxCluster = 16;         // k-split CTAs per cluster (above 8: a non-portable cluster size)
 constexpr uint32_t kMagic = 0x4B400000u;  // bits of 12582912.0f = 1.5 * 2^23
 constexpr unsigned long long kMagic2 = 0x4B4000004B400000ull;
 
 __device__ unsigned int g_err_matmul = 0;
+
+// One 2-D tensor copy of a weight stage: 32 rows x 272 bytes (x in 16-bit
+// elements: the k-step times 136; y: the first row), counted on `bar`.
+__device__ __forceinline__ void tma_stage_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
 
 __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));
@@ -70,27 +79,34 @@ __device__ __forceinline__ unsigned long long dup_pair(float x) {
   return r;
 }
 
+__device__ __forceinline__ unsigned long long make_pair(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+
 __device__ __forceinline__ float2 unpack_pair(unsigned long long v) {
   float2 r;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
   return r;
 }
 
-// The 8 warps form 4 pairs; the two warps of a pair read the same weight
-// stages (one 2-stage ring per pair) and take the first and second half of the
-// tokens, so a weight byte crosses shared memory once per pair while twice as
-// many warps hide the latencies.  The first warp of a pair refills a stage once
-// both hold it in registers (a 64-thread named barrier per k-step; it let the
-// refill go out earlier than polled "empty" mbarriers did).
-// ROWS = false (few-row matrices): a CTA tile is 32 rows and its 4 pairs
-//   take interleaved k-steps of the CTA's k-range; pair partials are added in
-//   pair order at each tile end.
-// ROWS = true (many-row matrices): a CTA tile is 128 rows, pair p owns rows
-//   32p..32p+31 over the whole k-range; no partials are exchanged between
-//   pairs, and with S = 1 no CTA-wide barrier is taken after start-up.
-// In both modes the S CTAs of a cluster split k and their sums are added in
-// rank order through distributed shared memory.  Token t's arithmetic (block
-// order, k-step order, pair and rank order) does not depend on n_tok.
+// The kernel.  A CTA (one per SM, 8 warps) works through tiles of G row
+// groups of 32 rows (lane = row); the KW = 8 / G warps of a row group take
+// interleaved k-steps of the CTA's k-range, and the S CTAs of a cluster split
+// the k-range of the matrix.  Every warp handles all n_tok tokens of its rows
+// and owns a 2-stage ring of weight stages (32 rows x 272 bytes, one 1-D bulk
+// copy per lane): it loads a stage into registers (17 conflict-free 16-byte
+// shared loads per lane; the 272-byte stride is an odd number of 16-byte bank
+// groups), releases it to the copy two units ahead, and computes from
+// registers while both stages are in flight.  No warp waits on another warp
+// inside the k loop.
+//
+// Sums per token: each warp adds its blocks in k order; the KW warps of a row
+// group are added in warp order (shared memory), then the S CTAs of a cluster
+// in rank order (distributed shared memory).  None of this depends on n_tok,
+// so column t of an n_tok = k call is bitwise the n_tok = 1 call.
+//
 // Activation source of a launch.  PRO 0: q8_0 rows xq.  PRO 1: float rows xf
 // (row stride xf_stride) that the kernel RMS-normalises (weight norm_w, eps)
 // and quantises itself; PRO 2: float rows [gate | up] (gate at column c, up at
@@ -106,21 +122,46 @@ struct ActSrc {
   int xf_stride = 0;
 };
 
-template <int NT, bool EMIT, bool ROWS, int PRO>
-__global__ void __launch_bounds__(kThreads, 2)
-    matmul_q8_0_narrow_kernel(const uint8_t* __restrict__ W, int rows, int nb, const ActSrc src,
-                              float* y, const float* residual, int32_t* __restrict__ isum_out) {
-  const uint8_t* xq = src.xq;
-  constexpr int kTile = ROWS ? kPairs * kRowsPerCta : kRowsPerCta;
-  constexpr int kRed = ROWS ? 0 : kPairs * NT * 32;          // pair partials (k-split mode)
-  constexpr int kSum = (ROWS ? kPairs : 1) * NT * 32;        // one CTA sum buffer
-  // Token halves: the first warp of a pair takes NTH0 tokens, the second the
-  // rest.  NTH is even, so both halves start on an even token and their word
-  // and scale pairs load as aligned 8-byte words; n_tok <= 2 is not split.
-  constexpr int NTH = ((NT + 1) / 2 + 1) & ~1;
-  constexpr int NTH0 = NTH < NT ? NTH : NT;
-  constexpr int NTP = 2 * NTH;            // scale row stride: both halves' pairs within the row
-  constexpr int NTA = (NT + 3) & ~3;      // word row stride: four tokens per 16-byte load
+// Activation row strides: NTA token slots per (block, word) and per block's
+// scales, rounded up to 4 so that four tokens load as one 16-byte word.
+__host__ __device__ constexpr int act_nta(int nt) { return (nt + 3) & ~3; }
+
+// Shared-memory layout (bytes), identical in every CTA of a cluster (the
+// distributed-shared-memory reads rely on the sums sitting at one offset):
+//   act codes [kr_alloc*8][8][NTA] u32 | act scales [kr_alloc*8][NTA] f32 |
+//   stages [8 warps][2][8704] | warp partials [8][NT][32] f32 (G < 8) |
+//   CTA sums [2][G][NT][32] f32 (S > 1) | mbarriers [8][2] | prologue scratch
+struct SmemLayout {
+  size_t act_s, stages, red, red_sum, bars, pro, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int kr_alloc, int nt, int G, int S, int pro) {
+  SmemLayout L;
+  const size_t nta = (size_t)act_nta(nt);
+  size_t off = (size_t)kr_alloc * 8 * 8 * nta * 4;
+  L.act_s = off;
+  off += (size_t)kr_alloc * 8 * nta * 4;
+  off = (off + 127) & ~(size_t)127;
+  L.stages = off;
+  off += (size_t)kWarps * kNStage * kStage;
+  L.red = off;
+  if (G < kWarps) off += (size_t)kWarps * nt * 32 * 4;
+  L.red_sum = off;
+  if (S > 1) off += (size_t)2 * G * nt * 32 * 4;
+  L.bars = off;
+  off += (size_t)kWarps * kNStage * 8;
+  L.pro = off;
+  if (pro == 1) off += (size_t)nt * (kWarps + 1) * 4;
+  L.total = off;
+  return L;
+}
+
+template <int NT, bool EMIT, int PRO>
+__global__ void __launch_bounds__(kThreads, 1)
+    matmul_q8_0_narrow_kernel(const __grid_constant__ CUtensorMap tmw, int rows, int nb, const ActSrc src, float* y,
+                              const float* residual, int32_t* __restrict__ isum_out, int G) {
+  constexpr int NTA = act_nta(NT);
+  constexpr int NP = (NT + 1) / 2;  // token pairs
   extern __shared__ __align__(128) uint8_t smem[];
   const int nks = nb >> 3;
   const int S = gridDim.y;
@@ -129,93 +170,107 @@ __global__ void __launch_bounds__(kThreads, 2)
   const Split ksr = kstep_range(nks, S, rank);
   const int kr = ksr.ks1 - ksr.ks0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pair = warp & (kPairs - 1), half = warp / kPairs;
-  const int t0 = half ? NTH0 : 0;                  // this warp's first token
-  const size_t row_bytes = (size_t)nb * 34;
-  const int tiles = (rows + kTile - 1) / kTile;
+  const int KW = kWarps / G;
+  const int grp = warp % G, kph = warp / G;
+  const int tile_rows = G * kRowsPerWarp;
+  const int tiles = (rows + tile_rows - 1) / tile_rows;
   const int n_tiles = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / n_clusters + 1 : 0;
-  const int warp_row = ROWS ? pair * kRowsPerCta : 0;
-
-  // Shared layout: act codes | act scales | stage rings | warp partials |
-  // CTA sums (double-buffered) | barriers.  The act region is sized for the
-  // largest k-range of the cluster in every CTA, so all CTAs of a cluster put
-  // the CTA sums at the same offset -- the distributed-shared-memory reads of
-  // rank 0 rely on that.
   const int kr_alloc = (nks + S - 1) / S;
-  uint32_t* act_q = reinterpret_cast<uint32_t*>(smem);                               // [kr*8][8][NTA]
-  float* act_s = reinterpret_cast<float*>(act_q + (size_t)kr_alloc * 8 * 8 * NTA);  // [kr*8][NTP]
-  uint8_t* stages = reinterpret_cast<uint8_t*>(act_s + (size_t)kr_alloc * 8 * NTP);  // [kPairs][kNStage][kStage]
-  float* red = reinterpret_cast<float*>(stages + (size_t)kPairs * kNStage * kStage);  // [kPairs][NT][32]
-  float* red_sum = red + kRed;                                                        // [2][kSum]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red_sum + 2 * kSum);                  // [kPairs][kNStage]
-  uint8_t* my_stages = stages + (size_t)pair * kNStage * kStage;
-  uint64_t* my_bars = bars + pair * kNStage;
-  constexpr int kReaders = NT > NTH0 ? 2 : 1;       // warps of a pair with tokens
+  const SmemLayout L = smem_layout(kr_alloc, NT, G, S, PRO);
+  uint32_t* act_q = reinterpret_cast<uint32_t*>(smem);
+  float* act_s = reinterpret_cast<float*>(smem + L.act_s);
+  uint8_t* my_stages = smem + L.stages + (size_t)warp * kNStage * kStage;
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  float* red_sum = reinterpret_cast<float*>(smem + L.red_sum);
+  uint64_t* my_bars = reinterpret_cast<uint64_t*>(smem + L.bars) + warp * kNStage;
+  const int kSum = G * NT * 32;  // one CTA sum buffer (floats)
 
-  if (half == 0 && lane == 0) {
+  if (lane == 0) {
     for (int s = 0; s < kNStage; ++s) mbar_init(&my_bars[s], 1);
     fence_mbar_init();
   }
   __syncwarp();
 
-  // This pair's units: for each of the CTA's tiles m, its k-steps (all of the
-  // k-range in ROWS mode, every kPairs-th otherwise).  Unit u = m*n_mine + i.
-  const int n_mine = ROWS ? kr : (kr > pair ? (kr - pair + kPairs - 1) / kPairs : 0);
+  // This warp's units: for each of the CTA's tiles m, the k-steps
+  // ks0 + kph, ks0 + kph + KW, ... of the CTA's k-range.  Unit u = m*n_mine + i.
+  const int n_mine = kr > kph ? (kr - kph + KW - 1) / KW : 0;
   const int n_units = n_tiles * n_mine;
-  auto kstep = [&](int i) { return ROWS ? ksr.ks0 + i : ksr.ks0 + pair + kPairs * i; };
+  // Lane 0 requests unit u's stage with one 2-D tensor copy (rows past the
+  // matrix read as zeros and are never stored); a row group wholly past the
+  // end only arrives.
   auto issue = [&](int u) {
+    if (lane != 0) return;
     const int m = u / n_mine, i = u - m * n_mine;
-    const int row0 = ((int)blockIdx.x + m * n_clusters) * kTile + warp_row;
-    const int row = row0 + lane;
-    const int ks = kstep(i);
+    const int row0 = ((int)blockIdx.x + m * n_clusters) * tile_rows + grp * kRowsPerWarp;
+    const int ks = ksr.ks0 + kph + KW * i;
     uint64_t* bar = &my_bars[u % kNStage];
-    uint8_t* dst = my_stages + (size_t)(u % kNStage) * kStage;
-    const int live = rows - row0 < kRowsPerCta ? rows - row0 : kRowsPerCta;
-    if (lane == 0 && live > 0) mbar_arrive_expect_tx(bar, (uint32_t)(live * kChunkBytes));
-    if (lane == 0 && live <= 0) mbar_arrive_expect_tx(bar, 0u);
-    __syncwarp();
-    if (row < rows)
-      bulk_g2s(dst + lane * kChunkBytes, W + (size_t)row * row_bytes + (size_t)ks * kChunkBytes, kChunkBytes, bar);
+    if (row0 < rows) {
+      mbar_arrive_expect_tx(bar, (uint32_t)kStage);
+      tma_stage_2d(my_stages + (size_t)(u % kNStage) * kStage, &tmw, ks * (kChunkBytes / 2), row0, bar);
+    } else {
+      mbar_arrive_expect_tx(bar, 0u);
+    }
   };
-  if (half == 0)
-    for (int u = 0; u < kNStage && u < n_units; ++u) issue(u);  // weights do not depend on the previous kernel
+  int issued = 0;  // units whose copies were requested
+  for (; issued < kNStage && issued < n_units; ++issued) issue(issued);  // weights do not depend on the previous kernel
   pdl_wait();  // the activations (and y / residual) may be the previous kernel's results
   pdl_trigger();
 
   if constexpr (PRO == 0) {
     // Unpack the CTA's activation blocks [ks0*8, ks1*8) x NT into the
-    // word-major form (unrolled so that several blocks' loads are in flight at
-    // once); the pad tokens NT..NTA-1 hold zero words.
-  #pragma unroll 4
-    for (int idx = threadIdx.x; idx < kr * 8 * NTA; idx += kThreads) {
-      const int b = idx / NTA, t = idx - b * NTA;
-      uint32_t* dq = act_q + (size_t)b * 8 * NTA + t;
-      if (t >= NT) {
-  #pragma unroll
-        for (int k = 0; k < 8; ++k) dq[k * NTA] = 0u;
-        for (int tp = t; tp < NTP; tp += NTA) act_s[(size_t)b * NTP + tp] = 0.0f;
-        continue;
+    // word-major form.  Item (k-step j, token t), tokens fastest: the 272
+    // contiguous bytes of token t's row for k-step ks0 + j (8 blocks), read
+    // with 17 16-byte loads (the row offset and the k-step are multiples of
+    // 16 bytes), split into codes and scales as the weight chunks are, and
+    // stored word-major (consecutive threads write consecutive tokens).
+    for (int it = threadIdx.x; it < kr * NT; it += kThreads) {
+      const int j = it / NT, t = it - j * NT;
+      const uint8_t* rowp = src.xq + (size_t)t * nb * 34 + (size_t)(ksr.ks0 + j) * kChunkBytes;
+      uint32_t wv[68];
+#pragma unroll
+      for (int c = 0; c < 17; ++c) {
+        const uint4 v = ld_v4_after_wait(rowp + 16 * c);  // written by the previous kernel
+        wv[4 * c + 0] = v.x;
+        wv[4 * c + 1] = v.y;
+        wv[4 * c + 2] = v.z;
+        wv[4 * c + 3] = v.w;
       }
-      const long long g = (long long)t * nb + (long long)ksr.ks0 * 8 + b;  // global block index
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(xq + ((34 * g) & ~3LL));
-      uint32_t wv[9];
-  #pragma unroll
-      for (int k = 0; k < 9; ++k) wv[k] = ld_u32(src + k);  // written by the previous kernel
-      const bool odd = (g & 1) != 0;  // odd blocks start 2 bytes into a word
-      const uint32_t sh = odd ? 32u : 16u;
-  #pragma unroll
-      for (int k = 0; k < 8; ++k) dq[k * NTA] = __funnelshift_rc(wv[k], wv[k + 1], sh);
-      act_s[(size_t)b * NTP + t] = half_bits_to_float(odd ? (wv[0] >> 16) : wv[0]);
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        uint32_t* dq = act_q + (size_t)(j * 8 + b) * 8 * NTA + t;
+        if ((b & 1) == 0) {
+          const int base = (17 * b) / 2;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) dq[k * NTA] = __funnelshift_r(wv[base + k], wv[base + k + 1], 16);
+          act_s[(size_t)(j * 8 + b) * NTA + t] = half_bits_to_float(wv[base]);
+        } else {
+          const int base = (17 * b - 1) / 2;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) dq[k * NTA] = wv[base + 1 + k];
+          act_s[(size_t)(j * 8 + b) * NTA + t] = half_bits_to_float(wv[base] >> 16);
+        }
+      }
+    }
+    if constexpr (NTA > NT) {
+      // the pad tokens NT..NTA-1 hold zero words and scales
+      for (int idx = threadIdx.x; idx < kr * 8 * 9 * (NTA - NT); idx += kThreads) {
+        const int bw = idx / (NTA - NT), t = NT + idx - bw * (NTA - NT);  // bw: (block, word 0..7 | scale 8)
+        const int b = bw / 9, k = bw - b * 9;
+        if (k < 8)
+          act_q[(size_t)b * 8 * NTA + k * NTA + t] = 0u;
+        else
+          act_s[(size_t)b * NTA + t] = 0.0f;
+      }
     }
   } else {
     // The pad tokens NT..NTA-1 hold zero words and scales.
     for (int idx = threadIdx.x; idx < kr * 8 * 8; idx += kThreads)
       for (int t = NT; t < NTA; ++t) act_q[(size_t)idx * NTA + t] = 0u;
     for (int idx = threadIdx.x; idx < kr * 8; idx += kThreads)
-      for (int t = NT; t < NTP; ++t) act_s[(size_t)idx * NTP + t] = 0.0f;
+      for (int t = NT; t < NTA; ++t) act_s[(size_t)idx * NTA + t] = 0.0f;
     const int cols = nb * 32;
-    float* inv_s = reinterpret_cast<float*>(bars + kPairs * kNStage);  // [NT]
-    float* part_s = inv_s + NT;                                         // [NT][8]
+    float* inv_s = reinterpret_cast<float*>(smem + L.pro);  // [NT]
+    float* part_s = inv_s + NT;                              // [NT][8]
     if constexpr (PRO == 1) {
       // each token row's 1 / sqrt(mean(x^2) + eps): thread j sums elements
       // j, j + 256, ... (fused multiply-adds in that order), an xor tree in
@@ -282,8 +337,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           const float uu[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const float g = v[4 * i + j];
-            v[4 * i + j] = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), uu[j]);
+            const float gg = v[4 * i + j];
+            v[4 * i + j] = __fmul_rn(__fdiv_rn(gg, __fadd_rn(1.0f, expf(-gg))), uu[j]);
           }
         }
       }
@@ -303,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         dq[k * NTA] = word;
       }
-      act_s[(size_t)b * NTP + t] = __half2float(__float2half_rn(d));
+      act_s[(size_t)b * NTA + t] = __half2float(__float2half_rn(d));
     }
   }
   __syncthreads();
@@ -313,218 +368,304 @@ __global__ void __launch_bounds__(kThreads, 2)
   // tile m (its slice, ranks in order), only after computing tile m + 1.  A
   // buffer is rewritten two tiles later, after the next wait, which no CTA
   // passes before every CTA has read it.
-  constexpr bool kCluster = !EMIT;  // ROWS && S == 1 writes directly instead (runtime)
-  const bool cluster_sums = kCluster && !(ROWS && S == 1);
-  auto reduce_tile = [&](int m) {
+  const bool cluster_sums = !EMIT && S > 1;
+  // A tile's cluster sums are finished in two halves: gather_tile reads the
+  // S ranks' sums of this CTA's slice over distributed shared memory and adds
+  // them in rank order into registers (before this CTA's next arrive, which
+  // releases the buffer); finish_tile adds the residual and stores y after
+  // that arrive, so the arrive never waits for global stores.  A slice holds
+  // at most G*NT*32 / (2*256) <= 8 outputs per thread.
+  constexpr int kMaxOut = 8;
+  float vsum[kMaxOut];
+  auto gather_tile = [&](int m) {
     const float* rs = red_sum + (m & 1) * kSum;
-    const int row0 = ((int)blockIdx.x + m * n_clusters) * kTile;
-    for (int idx = rank * kThreads + (int)threadIdx.x; idx < kSum; idx += S * kThreads) {
-      float part[kMaxCluster];
+    uint32_t base[kMaxCluster];  // this buffer in each rank's shared window
 #pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r)
-        if (r < S) part[r] = ld_dsmem_f32(&rs[idx], (uint32_t)r);
-      float v = part[0];
+    for (int r = 0; r < kMaxCluster; ++r)
+      if (r < S) base[r] = cluster_map(rs, (uint32_t)r);
 #pragma unroll
-      for (int r = 1; r < kMaxCluster; ++r)
-        if (r < S) v = __fadd_rn(v, part[r]);
-      const int wq = ROWS ? idx / (NT * 32) : 0;  // the pair (row group) of this output
-      const int t = (idx / 32) % NT, rr = row0 + wq * kRowsPerCta + (idx & 31);
-      if (rr < rows) {
-        const size_t o = (size_t)t * rows + rr;
-        y[o] = residual ? __fadd_rn(__ldcg(residual + o), v) : v;  // residual may alias y
+    for (int jo = 0; jo < kMaxOut; ++jo) {
+      const int idx = rank * kThreads + (int)threadIdx.x + jo * S * kThreads;
+      if (idx < kSum) {
+        float part[kMaxCluster];
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r)
+          if (r < S) part[r] = ld_cluster_f32(base[r] + 4u * (uint32_t)idx);
+        float v = part[0];
+#pragma unroll
+        for (int r = 1; r < kMaxCluster; ++r)
+          if (r < S) v = __fadd_rn(v, part[r]);
+        vsum[jo] = v;
+      }
+    }
+  };
+  auto finish_tile = [&](int m) {
+    const int row0 = ((int)blockIdx.x + m * n_clusters) * tile_rows;
+#pragma unroll
+    for (int jo = 0; jo < kMaxOut; ++jo) {
+      const int idx = rank * kThreads + (int)threadIdx.x + jo * S * kThreads;
+      if (idx < kSum) {
+        const int gq = idx / (NT * 32);  // row group of this output
+        const int t = (idx / 32) % NT, rr = row0 + gq * kRowsPerWarp + (idx & 31);
+        if (rr < rows) {
+          const size_t o = (size_t)t * rows + rr;
+          y[o] = residual ? __fadd_rn(__ldcg(residual + o), vsum[jo]) : vsum[jo];  // residual may alias y
+        }
       }
     }
   };
 
   bool dead = false;
-  int u = 0;
-  // The tile loop, specialised on this warp's token count NTM (compile time):
-  // the two halves of a pair run their own instance.
-  auto run = [&](auto ntm_c) {
-    constexpr int NTM = decltype(ntm_c)::value;
-    constexpr int NTMA = NTM > 0 ? NTM : 1;  // array extents
-    for (int m = 0; m < n_tiles; ++m) {
-      const int row0 = ((int)blockIdx.x + m * n_clusters) * kTile;
-      const int row = row0 + warp_row + lane;
-      unsigned long long acc2[(NTMA + 1) / 2];
+  int u = 0, landed = 0;  // landed: units whose stage wait succeeded
+  for (int m = 0; m < n_tiles; ++m) {
+    const int row0 = ((int)blockIdx.x + m * n_clusters) * tile_rows;
+    const int row = row0 + grp * kRowsPerWarp + lane;
+    unsigned long long acc2[NP];
 #pragma unroll
-      for (int p = 0; p < (NTMA + 1) / 2; ++p) acc2[p] = 0ull;
+    for (int p = 0; p < NP; ++p) acc2[p] = 0ull;
 
-      if constexpr (NTM > 0) {
-        for (int i = 0; i < n_mine; ++i, ++u) {
-          const int ks = kstep(i);
-          const int kl = ks - ksr.ks0;
-          uint64_t* bar = &my_bars[u % kNStage];
-          if (!dead) {
-            const bool ok = mbar_wait(bar, (uint32_t)((u / kNStage) & 1));
-            dead = __any_sync(0xffffffffu, !ok);  // warp-uniform
-            if (dead && lane == 0) g_err_matmul = 1u;
-          }
-          const uint4* src =
-              reinterpret_cast<const uint4*>(my_stages + (size_t)(u % kNStage) * kStage + lane * kChunkBytes);
-          uint32_t w[68];
+    for (int i = 0; i < n_mine; ++i, ++u) {
+      const int ks = ksr.ks0 + kph + KW * i;
+      const int kl = ks - ksr.ks0;
+      uint64_t* bar = &my_bars[u % kNStage];
+      if (!dead) {
+        const bool ok = mbar_wait(bar, (uint32_t)((u / kNStage) & 1));
+        dead = __any_sync(0xffffffffu, !ok);  // warp-uniform
+        if (dead && lane == 0) g_err_matmul = 1u;
+        if (!dead) landed = u + 1;
+      }
+      const uint4* stg =
+          reinterpret_cast<const uint4*>(my_stages + (size_t)(u % kNStage) * kStage + lane * kChunkBytes);
+      uint32_t w[68];
 #pragma unroll
-          for (int c = 0; c < 17; ++c) {
-            const uint4 v = src[c];
-            w[4 * c + 0] = v.x;
-            w[4 * c + 1] = v.y;
-            w[4 * c + 2] = v.z;
-            w[4 * c + 3] = v.w;
-          }
-          // every reader of the pair holds the stage: it may be refilled
-          if constexpr (kReaders == 2)
-            asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");
-          else
-            __syncwarp();
-          if (half == 0 && !dead && u + kNStage < n_units) issue(u + kNStage);
-
-#pragma unroll
-          for (int b = 0; b < 8; ++b) {
-            uint32_t q[8];
-            float dw;
-            if ((b & 1) == 0) {
-              const int base = (17 * b) / 2;
-#pragma unroll
-              for (int k = 0; k < 8; ++k) q[k] = __funnelshift_r(w[base + k], w[base + k + 1], 16);
-              dw = half_bits_to_float(w[base]);
-            } else {
-              const int base = (17 * b - 1) / 2;
-#pragma unroll
-              for (int k = 0; k < 8; ++k) q[k] = w[base + 1 + k];
-              dw = half_bits_to_float(w[base] >> 16);
-            }
-            const uint32_t* aq = act_q + (size_t)(kl * 8 + b) * 8 * NTA + t0;
-            // this warp's block dots advance word by word together (two
-            // words per 8-byte load; t0 is even)
-            int sd[NTM];
-#pragma unroll
-            for (int t = 0; t < NTM; ++t) sd[t] = (int)kMagic;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-#pragma unroll
-              for (int t2 = 0; t2 < NTM; t2 += 2) {
-                if (t2 + 1 < NTM) {
-                  const uint2 a = *reinterpret_cast<const uint2*>(aq + k * NTA + t2);
-                  sd[t2] = __dp4a((int)q[k], (int)a.x, sd[t2]);
-                  sd[t2 + 1] = __dp4a((int)q[k], (int)a.y, sd[t2 + 1]);
-                } else {
-                  sd[t2] = __dp4a((int)q[k], (int)aq[k * NTA + t2], sd[t2]);
-                }
-              }
-            }
-            if constexpr (EMIT) {
-              if (row < rows) {
-#pragma unroll
-                for (int t = 0; t < NTM; ++t)
-                  isum_out[((size_t)(t0 + t) * rows + row) * nb + (size_t)ks * 8 + b] = sd[t] - (int)kMagic;
-              }
-            } else {
-              const float* as = act_s + (size_t)(kl * 8 + b) * NTP + t0;
-              const unsigned long long dw2 = dup_pair(dw);
-#pragma unroll
-              for (int t = 0; t < NTM; t += 2) {
-                unsigned long long sx2;
-                if (t + 1 < NTM)
-                  sx2 = *reinterpret_cast<const unsigned long long*>(as + t);
-                else
-                  sx2 = dup_pair(as[t]);
-                acc2[t / 2] =
-                    acc_pair(acc2[t / 2], sd[t], t + 1 < NTM ? sd[t + 1] : (int)kMagic, mul_pair(dw2, sx2));
-              }
-            }
-          }
-        }
+      for (int c = 0; c < 17; ++c) {
+        const uint4 v = stg[c];
+        w[4 * c + 0] = v.x;
+        w[4 * c + 1] = v.y;
+        w[4 * c + 2] = v.z;
+        w[4 * c + 3] = v.w;
+      }
+      // Every lane's reads of the stage are ordered before the copy that
+      // overwrites it (the copy writes through the async proxy).
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (!dead && u + kNStage < n_units) {
+        issue(u + kNStage);
+        issued = u + kNStage + 1;
       }
 
-      if constexpr (!EMIT) {
-        float acc[NTMA];
 #pragma unroll
-        for (int p = 0; p < (NTMA + 1) / 2; ++p) {
-          const float2 v = unpack_pair(acc2[p]);
-          acc[2 * p] = v.x;
-          if (2 * p + 1 < NTMA) acc[2 * p + 1] = v.y;
+      for (int b = 0; b < 8; ++b) {
+        uint32_t q[8];
+        float dw;
+        if ((b & 1) == 0) {
+          const int base = (17 * b) / 2;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) q[k] = __funnelshift_r(w[base + k], w[base + k + 1], 16);
+          dw = half_bits_to_float(w[base]);
+        } else {
+          const int base = (17 * b - 1) / 2;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) q[k] = w[base + 1 + k];
+          dw = half_bits_to_float(w[base] >> 16);
         }
-        if (!cluster_sums) {
-          // One pair owns these rows over the whole k: write them directly.
+        const uint32_t* aq = act_q + (size_t)(kl * 8 + b) * 8 * NTA;
+        const float* as = act_s + (size_t)(kl * 8 + b) * NTA;
+        const unsigned long long dw2 = dup_pair(dw);
+        // every token's chain advances word by word together (NT independent
+        // dp4a chains); one broadcast 16-byte load gives word k of four tokens
+        int sd[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) sd[t] = (int)kMagic;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+#pragma unroll
+          for (int t4 = 0; t4 < NT; t4 += 4) {
+            const int cnt = NT - t4 < 4 ? NT - t4 : 4;
+            if (cnt >= 3) {
+              const uint4 a = *reinterpret_cast<const uint4*>(aq + k * NTA + t4);
+              sd[t4] = __dp4a((int)q[k], (int)a.x, sd[t4]);
+              sd[t4 + 1] = __dp4a((int)q[k], (int)a.y, sd[t4 + 1]);
+              sd[t4 + 2] = __dp4a((int)q[k], (int)a.z, sd[t4 + 2]);
+              if (cnt == 4) sd[t4 + 3] = __dp4a((int)q[k], (int)a.w, sd[t4 + 3]);
+            } else if (cnt == 2) {
+              const uint2 a = *reinterpret_cast<const uint2*>(aq + k * NTA + t4);
+              sd[t4] = __dp4a((int)q[k], (int)a.x, sd[t4]);
+              sd[t4 + 1] = __dp4a((int)q[k], (int)a.y, sd[t4 + 1]);
+            } else {
+              sd[t4] = __dp4a((int)q[k], (int)aq[k * NTA + t4], sd[t4]);
+            }
+          }
+        }
+        if constexpr (EMIT) {
           if (row < rows) {
 #pragma unroll
-            for (int t = 0; t < NTM; ++t) {
-              const size_t o = (size_t)(t0 + t) * rows + row;
-              y[o] = residual ? __fadd_rn(__ldcg(residual + o), acc[t]) : acc[t];  // residual may alias y
-            }
+            for (int t = 0; t < NT; ++t)
+              isum_out[((size_t)t * rows + row) * nb + (size_t)ks * 8 + b] = sd[t] - (int)kMagic;
           }
         } else {
-          // the previous tile's cluster sums, now that this tile is computed
-          if (m > 0) {
-            cluster_wait();
-            reduce_tile(m - 1);
-          }
-          // this tile's CTA sum (k-split mode: pair partials in pair order)
-          float* rs = red_sum + (m & 1) * kSum;
-          if constexpr (ROWS) {
 #pragma unroll
-            for (int t = 0; t < NTM; ++t) rs[(pair * NT + t0 + t) * 32 + lane] = acc[t];
-          } else {
-#pragma unroll
-            for (int t = 0; t < NTM; ++t) red[(pair * NT + t0 + t) * 32 + lane] = acc[t];
-            __syncthreads();
-            for (int idx = threadIdx.x; idx < NT * 32; idx += kThreads) {
-              float v = red[idx];
-#pragma unroll
-              for (int p2 = 1; p2 < kPairs; ++p2) v = __fadd_rn(v, red[p2 * NT * 32 + idx]);
-              rs[idx] = v;
+          for (int t4 = 0; t4 < NT; t4 += 4) {
+            const int cnt = NT - t4 < 4 ? NT - t4 : 4;
+            if (cnt >= 3) {
+              const float4 sx = *reinterpret_cast<const float4*>(as + t4);
+              acc2[t4 / 2] = acc_pair(acc2[t4 / 2], sd[t4], sd[t4 + 1], mul_pair(dw2, make_pair(sx.x, sx.y)));
+              acc2[t4 / 2 + 1] = acc_pair(acc2[t4 / 2 + 1], sd[t4 + 2], cnt == 4 ? sd[t4 + 3] : (int)kMagic,
+                                          mul_pair(dw2, make_pair(sx.z, sx.w)));
+            } else if (cnt == 2) {
+              const float2 sx = *reinterpret_cast<const float2*>(as + t4);
+              acc2[t4 / 2] = acc_pair(acc2[t4 / 2], sd[t4], sd[t4 + 1], mul_pair(dw2, make_pair(sx.x, sx.y)));
+            } else {
+              acc2[t4 / 2] = acc_pair(acc2[t4 / 2], sd[t4], (int)kMagic, mul_pair(dw2, dup_pair(as[t4])));
             }
           }
-          cluster_arrive();
         }
       }
     }
-    if (cluster_sums && n_tiles > 0) {
-      cluster_wait();
-      reduce_tile(n_tiles - 1);
-      // keep this CTA's sums alive until every CTA of the cluster has read them
-      cluster_sync();
+
+    if constexpr (!EMIT) {
+      float acc[NT];
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        const float2 v = unpack_pair(acc2[p]);
+        acc[2 * p] = v.x;
+        if (2 * p + 1 < NT) acc[2 * p + 1] = v.y;
+      }
+      if (KW == 1 && S == 1) {
+        // One warp owns these rows over the whole k: write them directly.
+        if (row < rows) {
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const size_t o = (size_t)t * rows + row;
+            y[o] = residual ? __fadd_rn(__ldcg(residual + o), acc[t]) : acc[t];  // residual may alias y
+          }
+        }
+      } else {
+        // the previous tile's cluster sums, now that this tile is computed
+        if (cluster_sums && m > 0) {
+          cluster_wait();
+          gather_tile(m - 1);
+        }
+        float* rs = red_sum + (m & 1) * kSum;
+        if (KW == 1) {
+#pragma unroll
+          for (int t = 0; t < NT; ++t) rs[(grp * NT + t) * 32 + lane] = acc[t];
+        } else {
+          // the KW warps of each row group, added in warp (k-phase) order
+#pragma unroll
+          for (int t = 0; t < NT; ++t) red[(warp * NT + t) * 32 + lane] = acc[t];
+          __syncthreads();
+          for (int idx = threadIdx.x; idx < kSum; idx += kThreads) {
+            const int gq = idx / (NT * 32), rest = idx - gq * NT * 32;
+            float v = red[gq * NT * 32 + rest];
+            for (int p2 = 1; p2 < KW; ++p2) v = __fadd_rn(v, red[(p2 * G + gq) * NT * 32 + rest]);
+            if (cluster_sums) {
+              rs[idx] = v;
+            } else {
+              const int t = rest / 32, rr = row0 + gq * kRowsPerWarp + (rest & 31);
+              if (rr < rows) {
+                const size_t o = (size_t)t * rows + rr;
+                y[o] = residual ? __fadd_rn(__ldcg(residual + o), v) : v;
+              }
+            }
+          }
+          __syncthreads();  // every partial read before the next tile rewrites them
+        }
+        if (cluster_sums) {
+          cluster_arrive();
+          if (m > 0) finish_tile(m - 1);
+        }
+      }
     }
-  };
-  if (half == 0)
-    run(std::integral_constant<int, NTH0>{});
-  else
-    run(std::integral_constant<int, NT - NTH0>{});
+  }
+  if (cluster_sums && n_tiles > 0) {
+    cluster_wait();
+    gather_tile(n_tiles - 1);
+    // keep this CTA's sums alive until every CTA of the cluster has read them
+    cluster_arrive();
+    finish_tile(n_tiles - 1);
+    cluster_wait();
+  }
+  if (dead) {
+    // A wait ran out: give the copies still in flight (units landed ..
+    // issued - 1) a bounded chance to land before the CTA's shared memory is
+    // released.
+    for (int v = landed; v < issued; ++v) (void)mbar_wait(&my_bars[v % kNStage], (uint32_t)((v / kNStage) & 1));
+  }
 }
 
-size_t smem_bytes(int kr, int nt, bool rows_mode, int pro = 0) {
-  const size_t red = rows_mode ? 0 : (size_t)kPairs * nt * 32 * 4;
-  const size_t sums = 2 * (rows_mode ? (size_t)kPairs : 1) * nt * 32 * 4;
-  const size_t ntp = 2 * ((((size_t)nt + 1) / 2 + 1) & ~(size_t)1);  // the kernel's NTP
-  const size_t nta = ((size_t)nt + 3) & ~(size_t)3;
-  return (size_t)kr * 8 * (nta * 32 + ntp * 4) + (size_t)kPairs * kNStage * kStage + red + sums +
-         (size_t)kPairs * kNStage * 8 + (pro == 1 ? (size_t)nt * 9 * 4 : 0);
+size_t smem_bytes(int kr, int nt, int G, int S, int pro = 0) { return smem_layout(kr, nt, G, S, pro).total; }
+
+// The weight matrix as a 2-D tensor of 16-bit elements, [rows][cols/32*17],
+// read in boxes of 136 x 32 (one k-step of 32 rows, 8704 bytes, no swizzle).
+// Encoded on the host and cached by (address, shape).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+cudaError_t weight_tensor_map(const void* W, int rows, int nb, CUtensorMap* out) {
+  struct Entry {
+    const void* base;
+    int rows, nb;
+    CUtensorMap map;
+  };
+  static std::mutex mu;
+  static Entry cache[64];
+  static int n_cache = 0, next_slot = 0;
+  static EncodeTiledFn encode = nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_cache; ++i)
+    if (cache[i].base == W && cache[i].rows == rows && cache[i].nb == nb) {
+      *out = cache[i].map;
+      return cudaSuccess;
+    }
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)nb * 17, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)nb * 34};
+  const cuuint32_t box[2] = {(cuuint32_t)(kChunkBytes / 2), (cuuint32_t)kRowsPerWarp};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMap m;
+  const CUresult r = encode(&m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(W), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const int slot = n_cache < 64 ? n_cache++ : (next_slot++ & 63);
+  cache[slot] = Entry{W, rows, nb, m};
+  *out = m;
+  return cudaSuccess;
 }
 
 // Per-instantiation host caches, each behind its own lock: the largest
 // dynamic shared memory granted so far, and the number of co-resident clusters
 // for each (S, smem) seen.  The attributes are per function, the same for every
 // device of one architecture.
-template <int NT, bool EMIT, bool ROWS, int PRO>
+template <int NT, bool EMIT, int PRO>
 cudaError_t grant_smem(size_t smem) {
   static std::mutex mu;
   static size_t granted = 0;
   static bool non_portable = false;
   std::lock_guard<std::mutex> lock(mu);
   if (!non_portable) {
-    cudaError_t e = cudaFuncSetAttribute(matmul_q8_0_narrow_kernel<NT, EMIT, ROWS, PRO>,
+    cudaError_t e = cudaFuncSetAttribute(matmul_q8_0_narrow_kernel<NT, EMIT, PRO>,
                                          cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     non_portable = true;
   }
   if (smem <= granted) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(matmul_q8_0_narrow_kernel<NT, EMIT, ROWS, PRO>,
+  cudaError_t e = cudaFuncSetAttribute(matmul_q8_0_narrow_kernel<NT, EMIT, PRO>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess) granted = smem;
   return e;
 }
 
-template <int NT, bool EMIT, bool ROWS, int PRO>
+template <int NT, bool EMIT, int PRO>
 cudaError_t cluster_capacity(int S, size_t smem, int* clusters) {
   struct Entry {
     int S;
@@ -532,7 +673,7 @@ cudaError_t cluster_capacity(int S, size_t smem, int* clusters) {
     int clusters;
   };
   static std::mutex mu;
-  static Entry cache[16];
+  static Entry cache[32];
   static int n_cache = 0;
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n_cache; ++i)
@@ -540,7 +681,7 @@ cudaError_t cluster_capacity(int S, size_t smem, int* clusters) {
       *clusters = cache[i].clusters;
       return cudaSuccess;
     }
-  cudaError_t e = grant_smem<NT, EMIT, ROWS, PRO>(smem);
+  cudaError_t e = grant_smem<NT, EMIT, PRO>(smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -554,22 +695,24 @@ cudaError_t cluster_capacity(int S, size_t smem, int* clusters) {
   cfg.dynamicSmemBytes = smem;
   cfg.gridDim = dim3(1, (unsigned)S, 1);
   int c = 0;
-  e = cudaOccupancyMaxActiveClusters(&c, matmul_q8_0_narrow_kernel<NT, EMIT, ROWS, PRO>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&c, matmul_q8_0_narrow_kernel<NT, EMIT, PRO>, &cfg);
   if (e != cudaSuccess) return e;
-  cache[n_cache < 16 ? n_cache++ : 15] = Entry{S, smem, c};
+  cache[n_cache < 32 ? n_cache++ : 31] = Entry{S, smem, c};
   *clusters = c;
   return cudaSuccess;
 }
 
-template <int NT, bool EMIT, bool ROWS, int PRO>
+template <int NT, bool EMIT, int PRO>
 cudaError_t launch_nt(const uint8_t* W, int rows, int nb, const ActSrc& src, float* y, const float* residual,
-                      int32_t* isum, int S, size_t smem, cudaStream_t st) {
-  auto kern = matmul_q8_0_narrow_kernel<NT, EMIT, ROWS, PRO>;
+                      int32_t* isum, int G, int S, size_t smem, cudaStream_t st) {
+  auto kern = matmul_q8_0_narrow_kernel<NT, EMIT, PRO>;
   // The persistent grid: as many clusters as fit at once, up to one per tile.
   int resident = 0;
-  cudaError_t e = cluster_capacity<NT, EMIT, ROWS, PRO>(S, smem, &resident);
+  cudaError_t e = cluster_capacity<NT, EMIT, PRO>(S, smem, &resident);
   if (e != cudaSuccess) return e;
   if (resident < 1) return cudaErrorInvalidConfiguration;
+  CUtensorMap tmw;
+  if ((e = weight_tensor_map(W, rows, nb, &tmw)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -582,22 +725,22 @@ cudaError_t launch_nt(const uint8_t* W, int rows, int nb, const ActSrc& src, flo
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  const int tile = ROWS ? kPairs * kRowsPerCta : kRowsPerCta;
+  const int tile = G * kRowsPerWarp;
   const int tiles = (rows + tile - 1) / tile;
   const int n_clusters = tiles < resident ? tiles : resident;
   cfg.gridDim = dim3((unsigned)n_clusters, (unsigned)S, 1);
   cfg.numAttrs = pdl() ? 2 : 1;
   if (dry_run()) return cudaSuccess;
-  return cudaLaunchKernelEx(&cfg, kern, W, rows, nb, src, y, residual, isum);
+  return cudaLaunchKernelEx(&cfg, kern, tmw, rows, nb, src, y, residual, isum, G);
 }
 
-template <bool EMIT, bool ROWS, int PRO>
+template <bool EMIT, int PRO>
 cudaError_t dispatch(int nt, const uint8_t* W, int rows, int nb, const ActSrc& src, float* y, const float* residual,
-                     int32_t* isum, int S, size_t smem, cudaStream_t st) {
+                     int32_t* isum, int G, int S, size_t smem, cudaStream_t st) {
   switch (nt) {
 #define DSB_CASE(N) \
   case N:           \
-    return launch_nt<N, EMIT, ROWS, PRO>(W, rows, nb, src, y, residual, isum, S, smem, st);
+    return launch_nt<N, EMIT, PRO>(W, rows, nb, src, y, residual, isum, G, S, smem, st);
     DSB_CASE(1) DSB_CASE(2) DSB_CASE(3) DSB_CASE(4) DSB_CASE(5) DSB_CASE(6) DSB_CASE(7) DSB_CASE(8)
     DSB_CASE(9) DSB_CASE(10) DSB_CASE(11) DSB_CASE(12) DSB_CASE(13) DSB_CASE(14) DSB_CASE(15) DSB_CASE(16)
 #undef DSB_CASE

@@ -560,6 +560,7 @@ class StepTraceC(ctypes.Structure):
 
 
 SIGNATURES.update({
+    "dsb_probe_dp4a": (_I, [_I, _I, _I, _P, _P]),
     "dsb_step_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(ModelShapeC), _I, _I]),
     "dsb_decode_step": (_I, [ctypes.POINTER(ModelC), _PI32, _PI32, _I, _I, _PI32, _P, _P, _P]),
     "dsb_decode_step_trace": (_I, [ctypes.POINTER(ModelC), _PI32, _PI32, _I, _I, _PI32, _P, _P,
@@ -576,6 +577,13 @@ SIGNATURES.update({
     "dsb_batch_commit": (_I, [_P, _PI32, _I]),
     "dsb_batch_length": (_I, [_P, _I]),
 })
+
+
+def probe_dp4a(mode: int, blocks: int, iters: int, out, stream=None):
+    """The dp4a rate (mode 0) / latency (mode 1) probe; ``out`` device uint32[3]."""
+    _need(out, 12, "out")
+    _check(lib().dsb_probe_dp4a(mode, blocks, iters, _ptr(out), _stream(stream)))
+    return out
 
 
 class BatchFormer:
