@@ -119,6 +119,12 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+
 // Programmatic dependent launch.  pdl_wait() blocks until the grid this one
 // depends on has completed and its writes are visible (a no-op when the launch
 // carries no programmatic dependency); pdl_trigger() lets the dependent grid be

@@ -129,8 +129,8 @@ __host__ __device__ constexpr int act_nta(int nt) { return (nt + 3) & ~3; }
 // Shared-memory layout (bytes), identical in every CTA of a cluster (the
 // distributed-shared-memory reads rely on the sums sitting at one offset):
 //   act codes [kr_alloc*8][8][NTA] u32 | act scales [kr_alloc*8][NTA] f32 |
-//   stages [8 warps][2][8704] | warp partials [8][NT][32] f32 (G < 8) |
-//   CTA sums [2][G][NT][32] f32 (S > 1) | mbarriers [8][2] | prologue scratch
+//   stages [2][8 warps][8704] | warp partials [8][NT][32] f32 (G < 8) |
+//   CTA sums [2][G][NT][32] f32 (S > 1) | mbarriers [8][2] + 1 | prologue scratch
 struct SmemLayout {
   size_t act_s, stages, red, red_sum, bars, pro, total;
 };
@@ -149,7 +149,7 @@ __host__ __device__ inline SmemLayout smem_layout(int kr_alloc, int nt, int G, i
   L.red_sum = off;
   if (S > 1) off += (size_t)2 * G * nt * 32 * 4;
   L.bars = off;
-  off += (size_t)kWarps * kNStage * 8;
+  off += (size_t)(kWarps * kNStage + 1) * 8;
   L.pro = off;
   if (pro == 1) off += (size_t)nt * (kWarps + 1) * 4;
   L.total = off;
@@ -179,17 +179,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const SmemLayout L = smem_layout(kr_alloc, NT, G, S, PRO);
   uint32_t* act_q = reinterpret_cast<uint32_t*>(smem);
   float* act_s = reinterpret_cast<float*>(smem + L.act_s);
-  uint8_t* my_stages = smem + L.stages + (size_t)warp * kNStage * kStage;
+  // stage s of this warp at stages + (s * 8 + warp) * 8704: the second stages
+  // of all warps are contiguous, and hold the raw activations at start-up
+  auto stage_ptr = [&](int s) { return smem + L.stages + ((size_t)s * kWarps + warp) * kStage; };
   float* red = reinterpret_cast<float*>(smem + L.red);
   float* red_sum = reinterpret_cast<float*>(smem + L.red_sum);
   uint64_t* my_bars = reinterpret_cast<uint64_t*>(smem + L.bars) + warp * kNStage;
+  uint64_t* act_bar = reinterpret_cast<uint64_t*>(smem + L.bars) + kWarps * kNStage;
   const int kSum = G * NT * 32;  // one CTA sum buffer (floats)
 
   if (lane == 0) {
     for (int s = 0; s < kNStage; ++s) mbar_init(&my_bars[s], 1);
+    if (warp == 0) mbar_init(act_bar, 1);
     fence_mbar_init();
   }
-  __syncwarp();
+  __syncthreads();
 
   // This warp's units: for each of the CTA's tiles m, the k-steps
   // ks0 + kph, ks0 + kph + KW, ... of the CTA's k-range.  Unit u = m*n_mine + i.
@@ -206,34 +210,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bar = &my_bars[u % kNStage];
     if (row0 < rows) {
       mbar_arrive_expect_tx(bar, (uint32_t)kStage);
-      tma_stage_2d(my_stages + (size_t)(u % kNStage) * kStage, &tmw, ks * (kChunkBytes / 2), row0, bar);
+      tma_stage_2d(stage_ptr(u % kNStage), &tmw, ks * (kChunkBytes / 2), row0, bar);
     } else {
       mbar_arrive_expect_tx(bar, 0u);
     }
   };
   int issued = 0;  // units whose copies were requested
-  for (; issued < kNStage && issued < n_units; ++issued) issue(issued);  // weights do not depend on the previous kernel
+  if (n_units > 0) issue(issued++);  // weights do not depend on the previous kernel
   pdl_wait();  // the activations (and y / residual) may be the previous kernel's results
   pdl_trigger();
+  bool dead = false;
 
   if constexpr (PRO == 0) {
     // Unpack the CTA's activation blocks [ks0*8, ks1*8) x NT into the
     // word-major form.  Item (k-step j, token t), tokens fastest: the 272
-    // contiguous bytes of token t's row for k-step ks0 + j (8 blocks), read
-    // with 17 16-byte loads (the row offset and the k-step are multiples of
-    // 16 bytes), split into codes and scales as the weight chunks are, and
-    // stored word-major (consecutive threads write consecutive tokens).
+    // contiguous bytes of token t's row for k-step ks0 + j (8 blocks), split
+    // into codes and scales as the weight chunks are, and stored word-major
+    // (consecutive threads write consecutive tokens).  The rows arrive by one
+    // 1-D bulk copy per token (kr * 272 bytes, 16-byte aligned) into the
+    // second weight stages, which no copy uses yet; if they do not fit there,
+    // each item is read from global memory with 17 16-byte loads.
+    const uint32_t raw_bytes = (uint32_t)(NT * kr * kChunkBytes);
+    const bool via_tma = raw_bytes <= (uint32_t)(kWarps * kStage);
+    const uint8_t* raw = smem + L.stages + (size_t)kWarps * kStage;
+    if (via_tma) {
+      if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(act_bar, raw_bytes);
+        for (int t = 0; t < NT; ++t)
+          bulk_g2s(const_cast<uint8_t*>(raw) + (size_t)t * kr * kChunkBytes,
+                   src.xq + (size_t)t * nb * 34 + (size_t)ksr.ks0 * kChunkBytes, (uint32_t)(kr * kChunkBytes), act_bar);
+      }
+      const bool ok = mbar_wait(act_bar, 0u);
+      dead = __syncthreads_or(!ok) != 0;
+      if (dead && threadIdx.x == 0) g_err_matmul = 1u;
+    }
     for (int it = threadIdx.x; it < kr * NT; it += kThreads) {
       const int j = it / NT, t = it - j * NT;
-      const uint8_t* rowp = src.xq + (size_t)t * nb * 34 + (size_t)(ksr.ks0 + j) * kChunkBytes;
       uint32_t wv[68];
+      if (via_tma) {
+        const uint4* rp = reinterpret_cast<const uint4*>(raw + ((size_t)t * kr + j) * kChunkBytes);
 #pragma unroll
-      for (int c = 0; c < 17; ++c) {
-        const uint4 v = ld_v4_after_wait(rowp + 16 * c);  // written by the previous kernel
-        wv[4 * c + 0] = v.x;
-        wv[4 * c + 1] = v.y;
-        wv[4 * c + 2] = v.z;
-        wv[4 * c + 3] = v.w;
+        for (int c = 0; c < 17; ++c) {
+          const uint4 v = rp[c];
+          wv[4 * c + 0] = v.x;
+          wv[4 * c + 1] = v.y;
+          wv[4 * c + 2] = v.z;
+          wv[4 * c + 3] = v.w;
+        }
+      } else {
+        const uint8_t* rowp = src.xq + (size_t)t * nb * 34 + (size_t)(ksr.ks0 + j) * kChunkBytes;
+#pragma unroll
+        for (int c = 0; c < 17; ++c) {
+          const uint4 v = ld_v4_after_wait(rowp + 16 * c);  // written by the previous kernel
+          wv[4 * c + 0] = v.x;
+          wv[4 * c + 1] = v.y;
+          wv[4 * c + 2] = v.z;
+          wv[4 * c + 3] = v.w;
+        }
       }
 #pragma unroll
       for (int b = 0; b < 8; ++b) {
@@ -361,7 +394,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       act_s[(size_t)b * NTA + t] = __half2float(__float2half_rn(d));
     }
   }
+  // every thread's reads of the raw rows precede the copies into those stages
+  fence_proxy_async_smem();
   __syncthreads();
+  if (!dead && issued < n_units) issue(issued++);
 
   // Cross-CTA sums: the CTA sum of tile m goes to buffer m & 1 and the CTA
   // arrives on the cluster barrier; it waits, and adds the cluster's sums of
@@ -375,8 +411,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // releases the buffer); finish_tile adds the residual and stores y after
   // that arrive, so the arrive never waits for global stores.  A slice holds
   // at most G*NT*32 / (2*256) <= 8 outputs per thread.
-  constexpr int kMaxOut = 8;
-  float vsum[kMaxOut];
+  // A slice holds at most G*NT*32 / (2*256) <= 8 outputs per thread, read as
+  // 16-byte quads (4 consecutive rows of one token).
+  constexpr int kMaxQuad = 2;
+  float4 vsum[kMaxQuad];
   auto gather_tile = [&](int m) {
     const float* rs = red_sum + (m & 1) * kSum;
     uint32_t base[kMaxCluster];  // this buffer in each rank's shared window
@@ -384,38 +422,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; r < kMaxCluster; ++r)
       if (r < S) base[r] = cluster_map(rs, (uint32_t)r);
 #pragma unroll
-    for (int jo = 0; jo < kMaxOut; ++jo) {
-      const int idx = rank * kThreads + (int)threadIdx.x + jo * S * kThreads;
-      if (idx < kSum) {
-        float part[kMaxCluster];
+    for (int jq = 0; jq < kMaxQuad; ++jq) {
+      const int qd = rank * kThreads + (int)threadIdx.x + jq * S * kThreads;
+      if (qd < kSum / 4) {
+        float4 part[kMaxCluster];  // every rank's load in flight before the adds
 #pragma unroll
         for (int r = 0; r < kMaxCluster; ++r)
-          if (r < S) part[r] = ld_cluster_f32(base[r] + 4u * (uint32_t)idx);
-        float v = part[0];
+          if (r < S) part[r] = ld_cluster_v4(base[r] + 16u * (uint32_t)qd);
+        float4 v = part[0];
 #pragma unroll
         for (int r = 1; r < kMaxCluster; ++r)
-          if (r < S) v = __fadd_rn(v, part[r]);
-        vsum[jo] = v;
+          if (r < S) {
+            v.x = __fadd_rn(v.x, part[r].x);
+            v.y = __fadd_rn(v.y, part[r].y);
+            v.z = __fadd_rn(v.z, part[r].z);
+            v.w = __fadd_rn(v.w, part[r].w);
+          }
+        vsum[jq] = v;
       }
     }
   };
   auto finish_tile = [&](int m) {
     const int row0 = ((int)blockIdx.x + m * n_clusters) * tile_rows;
 #pragma unroll
-    for (int jo = 0; jo < kMaxOut; ++jo) {
-      const int idx = rank * kThreads + (int)threadIdx.x + jo * S * kThreads;
-      if (idx < kSum) {
+    for (int jq = 0; jq < kMaxQuad; ++jq) {
+      const int qd = rank * kThreads + (int)threadIdx.x + jq * S * kThreads;
+      if (qd < kSum / 4) {
+        const int idx = 4 * qd;
         const int gq = idx / (NT * 32);  // row group of this output
-        const int t = (idx / 32) % NT, rr = row0 + gq * kRowsPerWarp + (idx & 31);
-        if (rr < rows) {
-          const size_t o = (size_t)t * rows + rr;
-          y[o] = residual ? __fadd_rn(__ldcg(residual + o), vsum[jo]) : vsum[jo];  // residual may alias y
+        const int t = (idx / 32) % NT, r0 = row0 + gq * kRowsPerWarp + (idx & 31);
+        const float vv[4] = {vsum[jq].x, vsum[jq].y, vsum[jq].z, vsum[jq].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (r0 + e < rows) {
+            const size_t o = (size_t)t * rows + r0 + e;
+            y[o] = residual ? __fadd_rn(__ldcg(residual + o), vv[e]) : vv[e];  // residual may alias y
+          }
         }
       }
     }
   };
 
-  bool dead = false;
   int u = 0, landed = 0;  // landed: units whose stage wait succeeded
   for (int m = 0; m < n_tiles; ++m) {
     const int row0 = ((int)blockIdx.x + m * n_clusters) * tile_rows;
@@ -435,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!dead) landed = u + 1;
       }
       const uint4* stg =
-          reinterpret_cast<const uint4*>(my_stages + (size_t)(u % kNStage) * kStage + lane * kChunkBytes);
+          reinterpret_cast<const uint4*>(stage_ptr(u % kNStage) + lane * kChunkBytes);
       uint32_t w[68];
 #pragma unroll
       for (int c = 0; c < 17; ++c) {
