@@ -787,7 +787,8 @@ def run_probe(spec: str):
     ``wide:ROWS:COLS:NTOK`` the tensor-core matmul three times;
     ``attention:WORKLOAD`` runs the decode attention four times on that
     workload's cache shape (b sequences, seq_lens uniform); ``dp4a`` measures
-    the dp4a issue rate and latency (one JSON line)."""
+    the dp4a issue rate and latency (one JSON line); ``step:WORKLOAD[:B]``
+    replays the workload's captured decode step four times."""
     import torch
     from session_decode_step_dsb_gb300 import dsb
     kind, *rest = spec.split(":")
@@ -821,6 +822,23 @@ def run_probe(spec: str):
         out = torch.empty_like(q)
         for _ in range(4):
             dsb.attention_decode_multi(q, kv, bi, T, lens, ws, out=out)
+    elif kind == "step":
+        # the captured decode step of a workload (default live batch), replayed
+        # three times after a warm-up replay: 1 + 10 * layers + 2 kernels each
+        ms = _shape(rest[0])
+        b = int(rest[1]) if len(rest) > 1 else DEFAULT_B[rest[0]]
+        model = _make_model(ms, seed=1000)
+        bi, lens, toks = _meta(ms, b, 1, seed=7)
+        ws = model.workspace(b)
+        logits = torch.empty((b, ms.vocab), dtype=torch.float32, device="cuda")
+        graph = model.graph(b, 1, logits, ws)
+        torch.cuda.synchronize()
+        for _ in range(4):
+            graph.launch(toks, bi, lens)
+        torch.cuda.synchronize()
+        graph.close()
+        print(json.dumps({"probe": "step", "workload": ms.name, "b": b,
+                          "kernels_per_step": launches_per_step(ms)}))
     elif kind == "dp4a":
         # the dp4a issue rate (many warps, independent chains) and latency
         # (one dependent chain), from which the narrow matmul's arithmetic

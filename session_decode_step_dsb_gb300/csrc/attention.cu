@@ -594,6 +594,11 @@ cudaError_t launch_typed(const float* q, long long q_stride, int n_q_heads, cons
   if (R <= 4)
     return launch_rg<D, T, 4>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
                               max_items, max_chunks, partials, out, xq_out, pv, st);
+  // five query rows per kv head: GQA 5:1 at one token per sequence (the
+  // Qwen3-14B shape), where a group of eight would carry three idle rows
+  if (R == 5)
+    return launch_rg<D, T, 5>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
+                              max_items, max_chunks, partials, out, xq_out, pv, st);
   return launch_rg<D, T, kMaxRowGroup>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq,
                                        tps, max_items, max_chunks, partials, out, xq_out, pv, st);
 }

@@ -26,10 +26,13 @@ constexpr int kGlueThreads = 256;
 
 constexpr int kMaxPerThread = 32;  // hidden <= 8192
 
-// One CTA per token row.  Thread j holds elements j, j + 256, ... in registers
-// (one memory round trip); the sum of squares goes through a fixed tree; then
-// warp w quantises blocks w, w + 8, ... -- element 32b + lane of block b is
-// exactly the value thread 32w + lane already holds.
+// A grid of (token row, split) CTAs.  Thread j holds elements j, j + 256, ...
+// of the row in registers (one memory round trip); the sum of squares goes
+// through a fixed tree, identical in every CTA of the row; then warp w
+// quantises blocks w + 8k for the CTA's share of k (blockIdx.y-th of
+// gridDim.y) -- element 32b + lane of block b is exactly the value thread
+// 32w + lane already holds.  Splitting the blocks over CTAs keeps a 16-token
+// step's norm from running on 16 SMs.
 __global__ void __launch_bounds__(kGlueThreads) rmsnorm_quant_kernel(const float* __restrict__ x,
                                                                      const float* __restrict__ w, int hidden,
                                                                      float eps, uint8_t* __restrict__ xq) {
@@ -57,9 +60,11 @@ __global__ void __launch_bounds__(kGlueThreads) rmsnorm_quant_kernel(const float
   for (int i = 0; i < kGlueThreads / 32; ++i) tot = __fadd_rn(tot, part[i]);
   const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)hidden), eps)));
   uint8_t* out = xq + (size_t)t * (hidden / 32) * 34;
+  const int kper = (n + (int)gridDim.y - 1) / (int)gridDim.y;
+  const int k0 = (int)blockIdx.y * kper, k1 = k0 + kper;
 #pragma unroll
   for (int k = 0; k < kMaxPerThread; ++k) {
-    if (k < n) {
+    if (k < n && k >= k0 && k < k1) {
       const int e = threadIdx.x + k * kGlueThreads;
       const int b = e >> 5;
       q8_block_store(__fmul_rn(__fmul_rn(v[k], inv), w[e]), out + (size_t)b * 34, lane);
@@ -170,7 +175,12 @@ cudaError_t launch_embed_params(const void* table, int hidden, int n_tok, float*
 cudaError_t launch_rmsnorm_quant(const float* x, const float* w, int n_tok, int hidden, float eps, void* xq,
                                  cudaStream_t st) {
   if (n_tok == 0) return cudaSuccess;
-  return launch_kernel(rmsnorm_quant_kernel, dim3(n_tok), dim3(kGlueThreads), 0, st, x, w, hidden, eps,
+  // about two blocks per warp: hidden / 32 blocks over 8 warps per CTA
+  const int n = hidden / kGlueThreads;
+  int split = (hidden / 32 + 15) / 16;
+  if (split > n) split = n;
+  if (split < 1) split = 1;
+  return launch_kernel(rmsnorm_quant_kernel, dim3(n_tok, split), dim3(kGlueThreads), 0, st, x, w, hidden, eps,
                        static_cast<uint8_t*>(xq));
 }
 
