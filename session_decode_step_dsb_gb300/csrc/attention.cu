@@ -176,7 +176,9 @@ __device__ __forceinline__ void issue_chunk(const Item& it, const CUtensorMap* t
       tma_load_2d(Vs + cb * kColBoxBytes + h * kBoxBytes, tmv, cb * kBoxCols, (int)(it.row0 + h * kBoxKeys), bar_v);
 }
 
-template <int D, typename T, int kRowGroup>
+// kFull: R is a multiple of kRowGroup, so every row of every group is live and
+// the per-row guards fold away at compile time.
+template <int D, typename T, int kRowGroup, bool kFull>
 __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
     const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const float* __restrict__ q,
     long long q_stride, int n_q_heads, int n_kv_heads, int ctx, const int32_t* __restrict__ batch_index,
@@ -260,7 +262,7 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
         const unsigned long long k45 = Cvt<T>::two_packed(kw.z), k67 = Cvt<T>::two_packed(kw.w);
 #pragma unroll
         for (int r = 0; r < kRowGroup; ++r) {
-          if (r0 + r < R) {
+          if ((kFull || r0 + r < R)) {
             const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(qs + (size_t)(r0 + r) * D + jj * 8);
             const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(qs + (size_t)(r0 + r) * D + jj * 8 + 4);
             unsigned long long a = dot2[r];
@@ -280,7 +282,7 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
         const int vis = it.L - tps + j + 1;          // keys before vis are visible to draft token j ...
         const int vlo = it.W > 0 ? vis - it.W : 0;   // ... from vlo on under a window
         const int key = it.key0 + k;
-        const bool ok = r0 + r < R && k < it.nkeys && key < vis && key >= vlo;
+        const bool ok = (kFull || r0 + r < R) && k < it.nkeys && key < vis && key >= vlo;
         sc[r] = ok ? __fmul_rn(__fadd_rn(d2.x, d2.y), scale) : -INFINITY;
       }
       // row max over the chunk: xor tree in each warp, then the warps in order
@@ -299,15 +301,15 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
 #pragma unroll
         for (int w2 = 1; w2 < kWarps; ++w2) M = fmaxf(M, wstat[w2 * kRowGroup + r]);
         p[r] = (M == -INFINITY) ? 0.0f : expf(sc[r] - M);
-        if (tid == 0 && r0 + r < R) ms[r0 + r] = M;
+        if (tid == 0 && (kFull || r0 + r < R)) ms[r0 + r] = M;
         float l = p[r];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, o));
         if (lane == 0) wstat[kWarps * kRowGroup + warp * kRowGroup + r] = l;
-        if (r0 + r < R) ps[(size_t)k * RP + r0 + r] = p[r];
+        if ((kFull || r0 + r < R)) ps[(size_t)k * RP + r0 + r] = p[r];
       }
       __syncthreads();
-      if (tid < kRowGroup && r0 + tid < R) {
+      if (tid < kRowGroup && (kFull || r0 + tid < R)) {
         float l = wstat[kWarps * kRowGroup + tid];
 #pragma unroll
         for (int w2 = 1; w2 < kWarps; ++w2) l = __fadd_rn(l, wstat[kWarps * kRowGroup + w2 * kRowGroup + tid]);
@@ -353,7 +355,7 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
         const float* pk = ps + (size_t)kk * RP + r0;
 #pragma unroll
         for (int r4 = 0; r4 < kRowGroup; r4 += 4) {
-          if (r0 + r4 < R) {
+          if ((kFull || r0 + r4 < R)) {
             const float4 p4 = *reinterpret_cast<const float4*>(pk + r4);
             const float pr[4] = {p4.x, p4.y, p4.z, p4.w};
 #pragma unroll
@@ -380,7 +382,7 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
       __syncthreads();
       for (int idx = tid; idx < kRowGroup * D; idx += kThreads) {
         const int r = idx / D, d = idx - r * D;
-        if (r0 + r < R) {
+        if ((kFull || r0 + r < R)) {
           float x = red[idx];
 #pragma unroll
           for (int w2 = 1; w2 < kWarps; ++w2) x = __fadd_rn(x, red[(size_t)w2 * kRowGroup * D + idx]);
@@ -529,14 +531,14 @@ cudaError_t kv_tensor_map(const void* base, long long rows, int D, int dtype, CU
   return cudaSuccess;
 }
 
-template <int D, typename T, int kRowGroup>
-cudaError_t launch_rg(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc, int dtype,
-                      int n_kv_heads, int ctx, long long kv_rows, MetaView meta, int n_seq, int tps,
-                      long long max_items, int max_chunks, float* partials, float* out, void* xq_out, PagedView pv,
-                      cudaStream_t st) {
+template <int D, typename T, int kRowGroup, bool kFull>
+cudaError_t launch_rg_full(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc, int dtype,
+                           int n_kv_heads, int ctx, long long kv_rows, MetaView meta, int n_seq, int tps,
+                           long long max_items, int max_chunks, float* partials, float* out, void* xq_out,
+                           PagedView pv, cudaStream_t st) {
   const int R = (n_q_heads / n_kv_heads) * tps;
   const size_t smem = partial_smem<D, T, kRowGroup>(R);
-  auto kern = attention_partial_kernel<D, T, kRowGroup>;
+  auto kern = attention_partial_kernel<D, T, kRowGroup, kFull>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   CUtensorMap tmk, tmv;
@@ -577,6 +579,24 @@ cudaError_t launch_rg(const float* q, long long q_stride, int n_q_heads, const v
                          meta.chunk_off, max_chunks, n_tok, out, static_cast<uint8_t*>(xq_out));
   return launch_kernel(attention_merge_kernel<D, false>, dim3(mgrid), dim3(128), 0, st, partials, n_q_heads, tps,
                        meta.chunk_off, max_chunks, n_tok, out, static_cast<uint8_t*>(nullptr));
+}
+
+// Row groups of 1, 2 and 5 serve R = 1, 2 and 5 only (always full); 4 and 8
+// also serve R = 3 and R = 6, 7, 9.. (a partial last group).
+template <int D, typename T, int kRowGroup>
+cudaError_t launch_rg(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc, int dtype,
+                      int n_kv_heads, int ctx, long long kv_rows, MetaView meta, int n_seq, int tps,
+                      long long max_items, int max_chunks, float* partials, float* out, void* xq_out, PagedView pv,
+                      cudaStream_t st) {
+  const int R = (n_q_heads / n_kv_heads) * tps;
+  if (kRowGroup == 4 || kRowGroup == kMaxRowGroup) {
+    if (R % kRowGroup != 0)
+      return launch_rg_full<D, T, kRowGroup, false>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows,
+                                                    meta, n_seq, tps, max_items, max_chunks, partials, out, xq_out, pv,
+                                                    st);
+  }
+  return launch_rg_full<D, T, kRowGroup, true>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta,
+                                               n_seq, tps, max_items, max_chunks, partials, out, xq_out, pv, st);
 }
 
 template <int D, typename T>
