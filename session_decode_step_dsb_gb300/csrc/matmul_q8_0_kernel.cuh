@@ -223,32 +223,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if constexpr (PRO == 0) {
     // Unpack the CTA's activation blocks [ks0*8, ks1*8) x NT into the
-    // word-major form.  Item (k-step j, token t), tokens fastest: the 272
-    // contiguous bytes of token t's row for k-step ks0 + j (8 blocks), split
-    // into codes and scales as the weight chunks are, and stored word-major
-    // (consecutive threads write consecutive tokens).  The rows arrive by one
-    // 1-D bulk copy per token (kr * 272 bytes, 16-byte aligned) into the
-    // second weight stages, which no copy uses yet; if they do not fit there,
-    // each item is read from global memory with 17 16-byte loads.
-    const uint32_t raw_bytes = (uint32_t)(NT * kr * kChunkBytes);
-    const bool via_tma = raw_bytes <= (uint32_t)(kWarps * kStage);
-    const uint8_t* raw = smem + L.stages + (size_t)kWarps * kStage;
-    if (via_tma) {
-      if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(act_bar, raw_bytes);
-        for (int t = 0; t < NT; ++t)
-          bulk_g2s(const_cast<uint8_t*>(raw) + (size_t)t * kr * kChunkBytes,
-                   src.xq + (size_t)t * nb * 34 + (size_t)ksr.ks0 * kChunkBytes, (uint32_t)(kr * kChunkBytes), act_bar);
+    // word-major form.  The rows arrive by one 1-D bulk copy per token (kr *
+    // 272 bytes, 16-byte aligned) into the second weight stages, which no copy
+    // uses yet, in as many rounds of tokens as that region needs.  Item
+    // (k-step j, token t), tokens fastest: the 272 bytes of token t's row for
+    // k-step ks0 + j (8 blocks), split into codes and scales as the weight
+    // chunks are, and stored word-major (consecutive threads write consecutive
+    // tokens).
+    uint8_t* raw = smem + L.stages + (size_t)kWarps * kStage;
+    const int row_raw = kr * kChunkBytes;
+    int per_round = (kWarps * kStage) / row_raw;
+    if (per_round > NT) per_round = NT;
+    for (int t0 = 0, rd = 0; t0 < NT && !dead; t0 += per_round, ++rd) {
+      const int tn = NT - t0 < per_round ? NT - t0 : per_round;
+      if (rd > 0) {
+        // the previous round's reads of the raw rows precede the next copies
+        fence_proxy_async_smem();
+        __syncthreads();
       }
-      const bool ok = mbar_wait(act_bar, 0u);
+      if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(act_bar, (uint32_t)(tn * row_raw));
+        for (int t = 0; t < tn; ++t)
+          bulk_g2s(raw + (size_t)t * row_raw, src.xq + (size_t)(t0 + t) * nb * 34 + (size_t)ksr.ks0 * kChunkBytes,
+                   (uint32_t)row_raw, act_bar);
+      }
+      const bool ok = mbar_wait(act_bar, (uint32_t)(rd & 1));
       dead = __syncthreads_or(!ok) != 0;
-      if (dead && threadIdx.x == 0) g_err_matmul = 1u;
-    }
-    for (int it = threadIdx.x; it < kr * NT; it += kThreads) {
-      const int j = it / NT, t = it - j * NT;
-      uint32_t wv[68];
-      if (via_tma) {
-        const uint4* rp = reinterpret_cast<const uint4*>(raw + ((size_t)t * kr + j) * kChunkBytes);
+      if (dead) {
+        if (threadIdx.x == 0) g_err_matmul = 1u;
+        break;
+      }
+      for (int it = threadIdx.x; it < kr * tn; it += kThreads) {
+        const int j = it / tn, tl = it - j * tn, t = t0 + tl;
+        const uint4* rp = reinterpret_cast<const uint4*>(raw + (size_t)tl * row_raw + (size_t)j * kChunkBytes);
+        uint32_t wv[68];
 #pragma unroll
         for (int c = 0; c < 17; ++c) {
           const uint4 v = rp[c];
@@ -257,30 +265,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           wv[4 * c + 2] = v.z;
           wv[4 * c + 3] = v.w;
         }
-      } else {
-        const uint8_t* rowp = src.xq + (size_t)t * nb * 34 + (size_t)(ksr.ks0 + j) * kChunkBytes;
 #pragma unroll
-        for (int c = 0; c < 17; ++c) {
-          const uint4 v = ld_v4_after_wait(rowp + 16 * c);  // written by the previous kernel
-          wv[4 * c + 0] = v.x;
-          wv[4 * c + 1] = v.y;
-          wv[4 * c + 2] = v.z;
-          wv[4 * c + 3] = v.w;
-        }
-      }
+        for (int b = 0; b < 8; ++b) {
+          uint32_t* dq = act_q + (size_t)(j * 8 + b) * 8 * NTA + t;
+          if ((b & 1) == 0) {
+            const int base = (17 * b) / 2;
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        uint32_t* dq = act_q + (size_t)(j * 8 + b) * 8 * NTA + t;
-        if ((b & 1) == 0) {
-          const int base = (17 * b) / 2;
+            for (int k = 0; k < 8; ++k) dq[k * NTA] = __funnelshift_r(wv[base + k], wv[base + k + 1], 16);
+            act_s[(size_t)(j * 8 + b) * NTA + t] = half_bits_to_float(wv[base]);
+          } else {
+            const int base = (17 * b - 1) / 2;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) dq[k * NTA] = __funnelshift_r(wv[base + k], wv[base + k + 1], 16);
-          act_s[(size_t)(j * 8 + b) * NTA + t] = half_bits_to_float(wv[base]);
-        } else {
-          const int base = (17 * b - 1) / 2;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) dq[k * NTA] = wv[base + 1 + k];
-          act_s[(size_t)(j * 8 + b) * NTA + t] = half_bits_to_float(wv[base] >> 16);
+            for (int k = 0; k < 8; ++k) dq[k * NTA] = wv[base + 1 + k];
+            act_s[(size_t)(j * 8 + b) * NTA + t] = half_bits_to_float(wv[base] >> 16);
+          }
         }
       }
     }
