@@ -808,7 +808,8 @@ def run_probe(spec: str):
     ``wide:ROWS:COLS:NTOK`` the tensor-core matmul three times;
     ``attention:WORKLOAD`` runs the decode attention four times on that
     workload's cache shape (b sequences, seq_lens uniform); ``dp4a`` measures
-    the dp4a issue rate and latency (one JSON line); ``step:WORKLOAD[:B]``
+    the dp4a issue rate and latency (one JSON line); ``mma`` the mma.sync
+    f16 and s8 product rates (one JSON line); ``step:WORKLOAD[:B]``
     replays the workload's captured decode step four times."""
     import torch
     from session_decode_step_dsb_gb300 import dsb
@@ -894,6 +895,35 @@ def run_probe(spec: str):
         res["dp4a_per_clk_per_sm"] = best / (sms * mhz * 1e6)
         res["sms"] = sms
         print(json.dumps({"probe": "dp4a", **res}))
+    elif kind == "mma":
+        # warp-level tensor-core products (mma.sync): m16n8k16 f16 -> f32 and
+        # m16n8k32 s8 -> s32, 8 independent tiles per warp
+        props = torch.cuda.get_device_properties(0)
+        sms = props.multi_processor_count
+        out = torch.zeros(4, dtype=torch.int32, device="cuda")
+        res = {"sms": sms}
+        with ClockSampler(0) as clk:
+            for mode, name, ops_per in ((2, "f16_m16n8k16", 2 * 16 * 8 * 16), (3, "s8_m16n8k32", 2 * 16 * 8 * 32)):
+                best = 0.0
+                for blocks in (sms, sms * 2, sms * 4):
+                    iters = 2048
+                    dsb.probe_mma(mode, blocks, iters, out)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    dsb.probe_mma(mode, blocks, iters, out)
+                    e1.record()
+                    e1.synchronize()
+                    sec = e0.elapsed_time(e1) * 1e-3
+                    n = blocks * 8 * 8 * iters
+                    res[f"{name}_{blocks // sms}_ctas_per_sm"] = {"tops": n * ops_per / sec / 1e12, "seconds": sec}
+                    best = max(best, n / sec)
+                res[f"{name}_per_clk_per_sm"] = best
+        clocks = clk.summary()
+        mhz = clocks.get("sm_mhz") or 2070.0
+        for name in ("f16_m16n8k16", "s8_m16n8k32"):
+            res[f"{name}_per_clk_per_sm"] = res[f"{name}_per_clk_per_sm"] / (sms * mhz * 1e6)
+        res["clocks"] = clocks
+        print(json.dumps({"probe": "mma", **res}))
     else:
         raise SystemExit(f"unknown probe {spec!r}")
     torch.cuda.synchronize()
@@ -921,7 +951,8 @@ def main(argv=None):
                     help="skip the llama-68m-shaped step and the b x K speculative grid")
     ap.add_argument("--probe", default=None,
                     help="run one kernel a few times for a profiler and exit: matmul:ROWS:COLS:NTOK[,..], "
-                         "wide:ROWS:COLS:NTOK, attention:WORKLOAD, or dp4a (the dp4a rate / latency probe)")
+                         "wide:ROWS:COLS:NTOK, attention:WORKLOAD, dp4a (the dp4a rate / latency probe) "
+                         "or mma (the mma.sync rate probe)")
     args = ap.parse_args(argv)
     if args.probe:
         run_probe(args.probe)

@@ -403,6 +403,17 @@ dsb_status dsb_attention_decode_multi_noalloc(const float* q, int n_q_heads, con
  * range; DSB_ERR_CUDA if the launch fails. */
 dsb_status dsb_probe_dp4a(int mode, int blocks, int iters, uint32_t* out, void* stream);
 
+/* The issue rate of the warp-level tensor-core products a narrow q8_0 matmul
+ * can use in place of dp4a.  `blocks` CTAs of 256 threads; every warp runs 8
+ * independent accumulator tiles for `iters` iterations, i.e. 64 * iters *
+ * blocks products in total:
+ *   mode 2: mma.sync m16n8k16, f16 x f16 -> f32 (4096 flops each);
+ *   mode 3: mma.sync m16n8k32, s8 x s8 -> s32 (8192 ops each).
+ * Time the call with events on `stream`.  out: device uint32[1] (written only
+ * to keep the results live).  DSB_ERR_INVALID_ARG for another mode or sizes
+ * out of range; DSB_ERR_CUDA if the launch fails. */
+dsb_status dsb_probe_mma(int mode, int blocks, int iters, uint32_t* out, void* stream);
+
 /* ---- the whole decode step -------------------------------------------------
  * A llama-style pre-norm decoder driven through the kernels above, one pass
  * for all live sessions ([DS4] "What" and "Design note": dense stages batched

@@ -561,6 +561,7 @@ class StepTraceC(ctypes.Structure):
 
 SIGNATURES.update({
     "dsb_probe_dp4a": (_I, [_I, _I, _I, _P, _P]),
+    "dsb_probe_mma": (_I, [_I, _I, _I, _P, _P]),
     "dsb_step_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(ModelShapeC), _I, _I]),
     "dsb_decode_step": (_I, [ctypes.POINTER(ModelC), _PI32, _PI32, _I, _I, _PI32, _P, _P, _P]),
     "dsb_decode_step_trace": (_I, [ctypes.POINTER(ModelC), _PI32, _PI32, _I, _I, _PI32, _P, _P,
@@ -583,6 +584,14 @@ def probe_dp4a(mode: int, blocks: int, iters: int, out, stream=None):
     """The dp4a rate (mode 0) / latency (mode 1) probe; ``out`` device uint32[3]."""
     _need(out, 12, "out")
     _check(lib().dsb_probe_dp4a(mode, blocks, iters, _ptr(out), _stream(stream)))
+    return out
+
+
+def probe_mma(mode: int, blocks: int, iters: int, out, stream=None):
+    """The mma.sync rate probe (mode 2: m16n8k16 f16, mode 3: m16n8k32 s8);
+    ``out`` device uint32[1]."""
+    _need(out, 4, "out")
+    _check(lib().dsb_probe_mma(mode, blocks, iters, _ptr(out), _stream(stream)))
     return out
 
 
