@@ -12,22 +12,36 @@
 //  * One persistent CTA per SM, 8 warps.  A warp owns 32 weight rows (lane =
 //    row) and every token; k-steps of 8 blocks = 272 bytes = 17 x 16 bytes,
 //    so every row chunk is 16-byte aligned whenever cols % 256 == 0.
-//  * Each warp streams its 32 row chunks with 1-D TMA bulk copies
-//    (cp.async.bulk, one 272-byte copy per lane) into its own 2-stage
-//    shared-memory ring guarded by mbarriers; it reads a stage back into
+//  * Each warp streams its 32 row chunks with one 2-D TMA tensor copy per
+//    stage (cp.async.bulk.tensor over the matrix viewed as rows x (cols/32 *
+//    17) 16-bit elements, box 136 x 32, so one copy moves 32 rows x 272
+//    bytes) into its own 2-stage shared-memory ring guarded by mbarriers
+//    (one copy per stage rather than one per row: the copy engine's issue
+//    rate, not HBM, bounded the per-row form); it reads a stage back into
 //    registers (17 conflict-free 16-byte shared loads per lane), hands the
 //    stage to the copy two units ahead and computes from registers, so two
 //    copies stay in flight per warp and no warp waits on another in the k loop.
-//  * Activation blocks of the CTA's k-range are unpacked once, at kernel start,
-//    into a word-major layout: for each block and each of its eight 4-code
+//  * Activation blocks of the CTA's k-range arrive by one bulk copy per token
+//    and are unpacked once, at kernel start, into a word-major layout: for each block and each of its eight 4-code
 //    words, that word of every token side by side (then the fp32 scales), so
 //    the inner loop reads four tokens' words with one warp-uniform (broadcast)
 //    16-byte load.
-//  * Block dots are __dp4a chains started from the bit pattern of 1.5 * 2^23:
-//    |isum| <= 32*127*127 < 2^22, so the int32 result read as a float is
-//    1.5*2^23 + isum exactly and one FADD converts it (no I2F).  Four tokens'
-//    chains advance word by word together, so consecutive dp4a instructions
-//    never depend on each other.
+//  * Up to 7 tokens, block dots are __dp4a chains started from the bit pattern
+//    of 1.5 * 2^23: |isum| <= 32*127*127 < 2^22, so the int32 result read as a
+//    float is 1.5*2^23 + isum exactly and one FADD converts it (no I2F).  Four
+//    tokens' chains advance word by word together, so consecutive dp4a
+//    instructions never depend on each other.
+//  * From 8 tokens on, the block dots run on the tensor cores: a warp's 32
+//    rows x 8-token tiles x one q8_0 block are two mma.sync m16n8k16 (f16 in,
+//    f32 accumulate).  Weight codes enter as the exact f16 values 1152 + q
+//    (one xor and two byte permutes per four codes), activation codes as f16
+//    q, and the accumulator starts at -1152 * (the block's activation code
+//    sum), so the product is the exact integer block dot.  dp4a's issue rate
+//    (64 per clock per SM, measured) and the shared-memory broadcasts that feed
+//    it bound the dp4a form at 16 tokens; the tensor-core form reads each
+//    activation word once per warp and fragment.  Both forms scale and add the
+//    block dots with the same float operations in the same order, so their
+//    outputs are bitwise equal.
 //  * A CTA tile is G row groups; the 8 / G warps of a group take interleaved
 //    k-steps, and k is further split over the CTAs of a thread block cluster
 //    (<= 16 CTAs).  Partial sums are added in warp order in shared memory and

@@ -95,8 +95,8 @@ __device__ __forceinline__ float2 unpack_pair(unsigned long long v) {
 // groups of 32 rows (lane = row); the KW = 8 / G warps of a row group take
 // interleaved k-steps of the CTA's k-range, and the S CTAs of a cluster split
 // the k-range of the matrix.  Every warp handles all n_tok tokens of its rows
-// and owns a 2-stage ring of weight stages (32 rows x 272 bytes, one 1-D bulk
-// copy per lane): it loads a stage into registers (17 conflict-free 16-byte
+// and owns a 2-stage ring of weight stages (32 rows x 272 bytes, one 2-D
+// tensor copy per stage): it loads a stage into registers (17 conflict-free 16-byte
 // shared loads per lane; the 272-byte stride is an odd number of 16-byte bank
 // groups), releases it to the copy two units ahead, and computes from
 // registers while both stages are in flight.  No warp waits on another warp
@@ -122,13 +122,65 @@ struct ActSrc {
   int xf_stride = 0;
 };
 
+// From this many tokens on, the k loop runs on the tensor cores (warp-level
+// mma.sync m16n8k16, f16 x f16 -> f32) instead of dp4a chains.  A q8_0 block
+// is K = 32, two products: the weight codes enter as the f16 values 1152 + q
+// (exact: integers below 2048), the activation codes as f16 q, and the
+// accumulator starts at -1152 * sum(q_x) of the block, so the result is the
+// exact integer block dot (every partial sum is an integer below 2^24).  The
+// scaling that follows is the dp4a path's, operation for operation, so both
+// paths give bitwise the same outputs.
+constexpr int kMmaMinNt = 8;
+__host__ __device__ constexpr bool use_mma(int nt) { return nt >= kMmaMinNt; }
+
 // Activation row strides: NTA token slots per (block, word) and per block's
-// scales, rounded up to 4 so that four tokens load as one 16-byte word.
-__host__ __device__ constexpr int act_nta(int nt) { return (nt + 3) & ~3; }
+// scales, rounded up to 4 so that four tokens load as one 16-byte word (dp4a
+// path), or to 8, the tensor-core tile width (mma path).
+__host__ __device__ constexpr int act_nta(int nt) { return use_mma(nt) ? (nt + 7) & ~7 : (nt + 3) & ~3; }
+
+// Slot of token t in the row of activation word k.  In the mma layout with 16
+// slots the two 8-token halves trade places in words 2, 3, 6 and 7, so that a
+// warp's fragment loads (word 4h + c of token 8n + g for lane 4g + c) hit 32
+// distinct banks.
+__device__ __forceinline__ int act_pos(int nta, bool mma, int k, int t) {
+  return (mma && nta == 16) ? (t ^ (((k >> 1) & 1) << 3)) : t;
+}
+
+// d = a * b + c for f32 pairs.
+__device__ __forceinline__ unsigned long long fma_pair(unsigned long long a, unsigned long long b,
+                                                       unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// Four signed codes (bytes of x ^ 0x80808080) as two f16 pairs of 1152 + q:
+// bytes 0, 1 -> lo, bytes 2, 3 -> hi.
+__device__ __forceinline__ void codes_to_f16_offset(uint32_t xu, uint32_t& lo, uint32_t& hi) {
+  lo = __byte_perm(xu, 0x64646464u, 0x4140);
+  hi = __byte_perm(xu, 0x64646464u, 0x4342);
+}
+
+// The same, minus 1152: the codes themselves as f16 pairs (exact).
+__device__ __forceinline__ void codes_to_f16(uint32_t xu, uint32_t& lo, uint32_t& hi) {
+  codes_to_f16_offset(xu, lo, hi);
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(0x64806480u));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(0x64806480u));
+}
+
+// D += A * B, one m16n8k16 tile (A row-major 16 x 16, B column-major 16 x 8).
+__device__ __forceinline__ void mma_16816(float& d0, float& d1, float& d2, float& d3, uint32_t a0, uint32_t a1,
+                                          uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
 // Shared-memory layout (bytes), identical in every CTA of a cluster (the
 // distributed-shared-memory reads rely on the sums sitting at one offset):
-//   act codes [kr_alloc*8][8][NTA] u32 | act scales [kr_alloc*8][NTA] f32 |
+//   act codes [kr_alloc*8][8][NTA] u32 | act scales [kr_alloc*8][NTA] f32
+//   (mma path: u32 = fp16 scale bits | int16 code sum << 16) |
 //   stages [2][8 warps][8704] | warp partials [8][NT][32] f32 (G < 8) |
 //   CTA sums [2][G][NT][32] f32 (S > 1) | mbarriers [8][2] + 1 | prologue scratch
 struct SmemLayout {
@@ -162,6 +214,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                               const float* residual, int32_t* __restrict__ isum_out, int G) {
   constexpr int NTA = act_nta(NT);
   constexpr int NP = (NT + 1) / 2;  // token pairs
+  constexpr bool kMma = use_mma(NT);
+  constexpr int NTN = NTA / 8;                               // mma path: 8-token tiles
+  constexpr uint32_t kActXor = kMma ? 0x80808080u : 0u;  // mma path stores codes + 128 per byte
   extern __shared__ __align__(128) uint8_t smem[];
   const int nks = nb >> 3;
   const int S = gridDim.y;
@@ -179,6 +234,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const SmemLayout L = smem_layout(kr_alloc, NT, G, S, PRO);
   uint32_t* act_q = reinterpret_cast<uint32_t*>(smem);
   float* act_s = reinterpret_cast<float*>(smem + L.act_s);
+  uint32_t* act_su = reinterpret_cast<uint32_t*>(smem + L.act_s);  // mma path view
+  // the fp16 scale (bits) of activation block idx = blk * NTA + t: as a float
+  // (dp4a path) or kept as bits, next to the block's code sum (mma path)
+  auto store_scale = [&](size_t idx, uint32_t bits16) {
+    if constexpr (kMma)
+      act_su[idx] = bits16 & 0xFFFFu;
+    else
+      act_s[idx] = half_bits_to_float(bits16);
+  };
+  // activation word k of block blk (CTA-local) for token t
+  auto act_word = [&](int blk, int k, int t) -> uint32_t& {
+    return act_q[(size_t)(blk * 8 + k) * NTA + act_pos(NTA, kMma, k, t)];
+  };
   // stage s of this warp at stages + (s * 8 + warp) * 8704: the second stages
   // of all warps are contiguous, and hold the raw activations at start-up
   auto stage_ptr = [&](int s) { return smem + L.stages + ((size_t)s * kWarps + warp) * kStage; };
@@ -267,17 +335,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
-          uint32_t* dq = act_q + (size_t)(j * 8 + b) * 8 * NTA + t;
           if ((b & 1) == 0) {
             const int base = (17 * b) / 2;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) dq[k * NTA] = __funnelshift_r(wv[base + k], wv[base + k + 1], 16);
-            act_s[(size_t)(j * 8 + b) * NTA + t] = half_bits_to_float(wv[base]);
+            for (int k = 0; k < 8; ++k)
+              act_word(j * 8 + b, k, t) = __funnelshift_r(wv[base + k], wv[base + k + 1], 16) ^ kActXor;
+            store_scale((size_t)(j * 8 + b) * NTA + t, wv[base]);
           } else {
             const int base = (17 * b - 1) / 2;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) dq[k * NTA] = wv[base + 1 + k];
-            act_s[(size_t)(j * 8 + b) * NTA + t] = half_bits_to_float(wv[base] >> 16);
+            for (int k = 0; k < 8; ++k) act_word(j * 8 + b, k, t) = wv[base + 1 + k] ^ kActXor;
+            store_scale((size_t)(j * 8 + b) * NTA + t, wv[base] >> 16);
           }
         }
       }
@@ -288,17 +356,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bw = idx / (NTA - NT), t = NT + idx - bw * (NTA - NT);  // bw: (block, word 0..7 | scale 8)
         const int b = bw / 9, k = bw - b * 9;
         if (k < 8)
-          act_q[(size_t)b * 8 * NTA + k * NTA + t] = 0u;
+          act_word(b, k, t) = kActXor;
         else
-          act_s[(size_t)b * NTA + t] = 0.0f;
+          act_su[(size_t)b * NTA + t] = 0u;  // 0.0f in either form
       }
     }
   } else {
     // The pad tokens NT..NTA-1 hold zero words and scales.
     for (int idx = threadIdx.x; idx < kr * 8 * 8; idx += kThreads)
-      for (int t = NT; t < NTA; ++t) act_q[(size_t)idx * NTA + t] = 0u;
+      for (int t = NT; t < NTA; ++t) act_word(idx >> 3, idx & 7, t) = kActXor;
     for (int idx = threadIdx.x; idx < kr * 8; idx += kThreads)
-      for (int t = NT; t < NTA; ++t) act_s[(size_t)idx * NTA + t] = 0.0f;
+      for (int t = NT; t < NTA; ++t) act_su[(size_t)idx * NTA + t] = 0u;  // 0.0f in either form
     const int cols = nb * 32;
     float* inv_s = reinterpret_cast<float*>(smem + L.pro);  // [NT]
     float* part_s = inv_s + NT;                              // [NT][8]
@@ -377,7 +445,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 32; ++j) a = fmaxf(a, fabsf(v[j]));
       const float d = __fdiv_rn(a, 127.0f);
-      uint32_t* dq = act_q + (size_t)b * 8 * NTA + t;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         uint32_t word = 0;
@@ -387,9 +454,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (d != 0.0f) q = (int)fminf(fmaxf(roundf(__fdiv_rn(v[4 * k + j], d)), -127.0f), 127.0f);
           word |= ((uint32_t)q & 0xFFu) << (8 * j);
         }
-        dq[k * NTA] = word;
+        act_word(b, k, t) = word ^ kActXor;
       }
-      act_s[(size_t)b * NTA + t] = __half2float(__float2half_rn(d));
+      store_scale((size_t)b * NTA + t, __half_as_ushort(__float2half_rn(d)));
+    }
+  }
+  if constexpr (kMma) {
+    // the sum of the 32 codes of every (block, token), |sum| <= 4064, as int16
+    // in the high half of the scale word: -1152 * sum starts the block's
+    // tensor-core accumulator.  The stored bytes are codes + 128.
+    __syncthreads();
+    if (!dead) {
+      for (int idx = threadIdx.x; idx < kr * 8 * NT; idx += kThreads) {
+        const int blk = idx / NT, t = idx - blk * NT;
+        unsigned int su = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) su = __dp4a(act_word(blk, k, t), 0x01010101u, su);
+        act_su[(size_t)blk * NTA + t] |= ((uint32_t)((int)su - 32 * 128) & 0xFFFFu) << 16;
+      }
     }
   }
   // every thread's reads of the raw rows precede the copies into those stages
@@ -465,9 +547,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int m = 0; m < n_tiles; ++m) {
     const int row0 = ((int)blockIdx.x + m * n_clusters) * tile_rows;
     const int row = row0 + grp * kRowsPerWarp + lane;
-    unsigned long long acc2[NP];
+    unsigned long long acc2[kMma ? 1 : NP];
+    unsigned long long accm[kMma ? 4 : 1][kMma ? NTN : 1];
+    if constexpr (kMma) {
 #pragma unroll
-    for (int p = 0; p < NP; ++p) acc2[p] = 0ull;
+      for (int ri = 0; ri < 4; ++ri)
+#pragma unroll
+        for (int n = 0; n < NTN; ++n) accm[ri][n] = 0ull;
+    } else {
+#pragma unroll
+      for (int p = 0; p < NP; ++p) acc2[p] = 0ull;
+    }
 
     for (int i = 0; i < n_mine; ++i, ++u) {
       const int ks = ksr.ks0 + kph + KW * i;
@@ -479,89 +569,169 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (dead && lane == 0) g_err_matmul = 1u;
         if (!dead) landed = u + 1;
       }
-      const uint4* stg =
-          reinterpret_cast<const uint4*>(stage_ptr(u % kNStage) + lane * kChunkBytes);
-      uint32_t w[68];
-#pragma unroll
-      for (int c = 0; c < 17; ++c) {
-        const uint4 v = stg[c];
-        w[4 * c + 0] = v.x;
-        w[4 * c + 1] = v.y;
-        w[4 * c + 2] = v.z;
-        w[4 * c + 3] = v.w;
-      }
       // Every lane's reads of the stage are ordered before the copy that
       // overwrites it (the copy writes through the async proxy).
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (!dead && u + kNStage < n_units) {
-        issue(u + kNStage);
-        issued = u + kNStage + 1;
-      }
+      auto release = [&]() {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (!dead && u + kNStage < n_units) {
+          issue(u + kNStage);
+          issued = u + kNStage + 1;
+        }
+      };
+      if constexpr (kMma) {
+        // Lane 4g + c holds, for rows 8ri + g (ri = 0..3: the two 16-row
+        // tiles' upper and lower halves), code words c and 4 + c of every
+        // block of the k-step (the K order inside a block is permuted the same
+        // way for weights and activations), plus the rows' scales.  Block b
+        // starts at byte 34b of a row: an even block's codes start 2 bytes
+        // past a word boundary (two words per code word, byte_perm), an odd
+        // block's on one.  Row r's words start at bank 4r, so every load hits
+        // 32 distinct banks.
+        const int g = lane >> 2, c = lane & 3;
+        const uint32_t* st = reinterpret_cast<const uint32_t*>(stage_ptr(u % kNStage));
+        uint32_t wq[4][8][2];
+        uint32_t wsc[4][4];  // scales of blocks 2j (low half) and 2j + 1 (high half)
+#pragma unroll
+        for (int ri = 0; ri < 4; ++ri) {
+          const uint32_t* rp = st + (8 * ri + g) * (kChunkBytes / 4);
+#pragma unroll
+          for (int b = 0; b < 8; b += 2) {
+            const int w0 = (34 * b) / 4;            // even block: scale in the low half of word w0
+            const int w1 = (34 * (b + 1) + 2) / 4;  // odd block: codes from word w1, scale in the high half of w1 - 1
+            const uint32_t v0 = rp[w0 + c], v1 = rp[w0 + c + 1], v4 = rp[w0 + c + 4], v5 = rp[w0 + c + 5];
+            wq[ri][b][0] = __byte_perm(v0, v1, 0x5432);
+            wq[ri][b][1] = __byte_perm(v4, v5, 0x5432);
+            wq[ri][b + 1][0] = rp[w1 + c];
+            wq[ri][b + 1][1] = rp[w1 + c + 4];
+            wsc[ri][b / 2] = __byte_perm(rp[w0], rp[w1 - 1], 0x7610);
+          }
+        }
+        release();
+        __syncwarp();  // the warp-wide tensor-core products below run converged
 
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        uint32_t q[8];
-        float dw;
-        if ((b & 1) == 0) {
-          const int base = (17 * b) / 2;
+        for (int b = 0; b < 8; ++b) {
+          const int kb = kl * 8 + b;
+          uint32_t af[4][2][2];  // [row ri][half h][slots 2c, 2c+1 | 2c+8, 2c+9]
+          float dw[4];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) q[k] = __funnelshift_r(w[base + k], w[base + k + 1], 16);
-          dw = half_bits_to_float(w[base]);
-        } else {
-          const int base = (17 * b - 1) / 2;
+          for (int ri = 0; ri < 4; ++ri) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) q[k] = w[base + 1 + k];
-          dw = half_bits_to_float(w[base] >> 16);
-        }
-        const uint32_t* aq = act_q + (size_t)(kl * 8 + b) * 8 * NTA;
-        const float* as = act_s + (size_t)(kl * 8 + b) * NTA;
-        const unsigned long long dw2 = dup_pair(dw);
-        // every token's chain advances word by word together (NT independent
-        // dp4a chains); one broadcast 16-byte load gives word k of four tokens
-        int sd[NT];
+            for (int h = 0; h < 2; ++h) codes_to_f16_offset(wq[ri][b][h] ^ 0x80808080u, af[ri][h][0], af[ri][h][1]);
+            dw[ri] = half_bits_to_float((b & 1) ? (wsc[ri][b / 2] >> 16) : wsc[ri][b / 2]);
+          }
 #pragma unroll
-        for (int t = 0; t < NT; ++t) sd[t] = (int)kMagic;
+          for (int n = 0; n < NTN; ++n) {
+            const int tb = 8 * n;
+            uint32_t bf[2][2];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+            for (int h = 0; h < 2; ++h) codes_to_f16(act_word(kb, 4 * h + c, tb + g), bf[h][0], bf[h][1]);
+            // tokens tb + 2c, tb + 2c + 1: scales and -1152 * code sums
+            const uint2 sc = *reinterpret_cast<const uint2*>(act_su + (size_t)kb * NTA + tb + 2 * c);
+            const unsigned long long sx2 = make_pair(half_bits_to_float(sc.x), half_bits_to_float(sc.y));
+            const float cx0 = -1152.0f * (float)((int)sc.x >> 16), cx1 = -1152.0f * (float)((int)sc.y >> 16);
 #pragma unroll
-          for (int t4 = 0; t4 < NT; t4 += 4) {
-            const int cnt = NT - t4 < 4 ? NT - t4 : 4;
-            if (cnt >= 3) {
-              const uint4 a = *reinterpret_cast<const uint4*>(aq + k * NTA + t4);
-              sd[t4] = __dp4a((int)q[k], (int)a.x, sd[t4]);
-              sd[t4 + 1] = __dp4a((int)q[k], (int)a.y, sd[t4 + 1]);
-              sd[t4 + 2] = __dp4a((int)q[k], (int)a.z, sd[t4 + 2]);
-              if (cnt == 4) sd[t4 + 3] = __dp4a((int)q[k], (int)a.w, sd[t4 + 3]);
-            } else if (cnt == 2) {
-              const uint2 a = *reinterpret_cast<const uint2*>(aq + k * NTA + t4);
-              sd[t4] = __dp4a((int)q[k], (int)a.x, sd[t4]);
-              sd[t4 + 1] = __dp4a((int)q[k], (int)a.y, sd[t4 + 1]);
-            } else {
-              sd[t4] = __dp4a((int)q[k], (int)aq[k * NTA + t4], sd[t4]);
+            for (int mt = 0; mt < 2; ++mt) {
+              float d0 = cx0, d1 = cx1, d2 = cx0, d3 = cx1;
+              mma_16816(d0, d1, d2, d3, af[2 * mt][0][0], af[2 * mt + 1][0][0], af[2 * mt][0][1],
+                        af[2 * mt + 1][0][1], bf[0][0], bf[0][1]);
+              mma_16816(d0, d1, d2, d3, af[2 * mt][1][0], af[2 * mt + 1][1][0], af[2 * mt][1][1],
+                        af[2 * mt + 1][1][1], bf[1][0], bf[1][1]);
+              if constexpr (EMIT) {
+                const float dd[4] = {d0, d1, d2, d3};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int r = row0 + grp * kRowsPerWarp + 16 * mt + 8 * (e >> 1) + g, t = tb + 2 * c + (e & 1);
+                  if (r < rows && t < NT)
+                    isum_out[((size_t)t * rows + r) * nb + (size_t)ks * 8 + b] = __float2int_rn(dd[e]);
+                }
+              } else {
+                accm[2 * mt][n] = fma_pair(make_pair(d0, d1), mul_pair(dup_pair(dw[2 * mt]), sx2), accm[2 * mt][n]);
+                accm[2 * mt + 1][n] =
+                    fma_pair(make_pair(d2, d3), mul_pair(dup_pair(dw[2 * mt + 1]), sx2), accm[2 * mt + 1][n]);
+              }
             }
           }
         }
-        if constexpr (EMIT) {
-          if (row < rows) {
+      } else {
+        const uint4* stg =
+            reinterpret_cast<const uint4*>(stage_ptr(u % kNStage) + lane * kChunkBytes);
+        uint32_t w[68];
 #pragma unroll
-            for (int t = 0; t < NT; ++t)
-              isum_out[((size_t)t * rows + row) * nb + (size_t)ks * 8 + b] = sd[t] - (int)kMagic;
+        for (int c = 0; c < 17; ++c) {
+          const uint4 v = stg[c];
+          w[4 * c + 0] = v.x;
+          w[4 * c + 1] = v.y;
+          w[4 * c + 2] = v.z;
+          w[4 * c + 3] = v.w;
+        }
+        release();
+
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          uint32_t q[8];
+          float dw;
+          if ((b & 1) == 0) {
+            const int base = (17 * b) / 2;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) q[k] = __funnelshift_r(w[base + k], w[base + k + 1], 16);
+            dw = half_bits_to_float(w[base]);
+          } else {
+            const int base = (17 * b - 1) / 2;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) q[k] = w[base + 1 + k];
+            dw = half_bits_to_float(w[base] >> 16);
           }
-        } else {
+          const uint32_t* aq = act_q + (size_t)(kl * 8 + b) * 8 * NTA;
+          const float* as = act_s + (size_t)(kl * 8 + b) * NTA;
+          const unsigned long long dw2 = dup_pair(dw);
+          // every token's chain advances word by word together (NT independent
+          // dp4a chains); one broadcast 16-byte load gives word k of four tokens
+          int sd[NT];
 #pragma unroll
-          for (int t4 = 0; t4 < NT; t4 += 4) {
-            const int cnt = NT - t4 < 4 ? NT - t4 : 4;
-            if (cnt >= 3) {
-              const float4 sx = *reinterpret_cast<const float4*>(as + t4);
-              acc2[t4 / 2] = acc_pair(acc2[t4 / 2], sd[t4], sd[t4 + 1], mul_pair(dw2, make_pair(sx.x, sx.y)));
-              acc2[t4 / 2 + 1] = acc_pair(acc2[t4 / 2 + 1], sd[t4 + 2], cnt == 4 ? sd[t4 + 3] : (int)kMagic,
-                                          mul_pair(dw2, make_pair(sx.z, sx.w)));
-            } else if (cnt == 2) {
-              const float2 sx = *reinterpret_cast<const float2*>(as + t4);
-              acc2[t4 / 2] = acc_pair(acc2[t4 / 2], sd[t4], sd[t4 + 1], mul_pair(dw2, make_pair(sx.x, sx.y)));
-            } else {
-              acc2[t4 / 2] = acc_pair(acc2[t4 / 2], sd[t4], (int)kMagic, mul_pair(dw2, dup_pair(as[t4])));
+          for (int t = 0; t < NT; ++t) sd[t] = (int)kMagic;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+#pragma unroll
+            for (int t4 = 0; t4 < NT; t4 += 4) {
+              const int cnt = NT - t4 < 4 ? NT - t4 : 4;
+              if (cnt >= 3) {
+                const uint4 a = *reinterpret_cast<const uint4*>(aq + k * NTA + t4);
+                sd[t4] = __dp4a((int)q[k], (int)a.x, sd[t4]);
+                sd[t4 + 1] = __dp4a((int)q[k], (int)a.y, sd[t4 + 1]);
+                sd[t4 + 2] = __dp4a((int)q[k], (int)a.z, sd[t4 + 2]);
+                if (cnt == 4) sd[t4 + 3] = __dp4a((int)q[k], (int)a.w, sd[t4 + 3]);
+              } else if (cnt == 2) {
+                const uint2 a = *reinterpret_cast<const uint2*>(aq + k * NTA + t4);
+                sd[t4] = __dp4a((int)q[k], (int)a.x, sd[t4]);
+                sd[t4 + 1] = __dp4a((int)q[k], (int)a.y, sd[t4 + 1]);
+              } else {
+                sd[t4] = __dp4a((int)q[k], (int)aq[k * NTA + t4], sd[t4]);
+              }
+            }
+          }
+          if constexpr (EMIT) {
+            if (row < rows) {
+#pragma unroll
+              for (int t = 0; t < NT; ++t)
+                isum_out[((size_t)t * rows + row) * nb + (size_t)ks * 8 + b] = sd[t] - (int)kMagic;
+            }
+          } else {
+#pragma unroll
+            for (int t4 = 0; t4 < NT; t4 += 4) {
+              const int cnt = NT - t4 < 4 ? NT - t4 : 4;
+              if (cnt >= 3) {
+                const float4 sx = *reinterpret_cast<const float4*>(as + t4);
+                acc2[t4 / 2] = acc_pair(acc2[t4 / 2], sd[t4], sd[t4 + 1], mul_pair(dw2, make_pair(sx.x, sx.y)));
+                acc2[t4 / 2 + 1] = acc_pair(acc2[t4 / 2 + 1], sd[t4 + 2], cnt == 4 ? sd[t4 + 3] : (int)kMagic,
+                                            mul_pair(dw2, make_pair(sx.z, sx.w)));
+              } else if (cnt == 2) {
+                const float2 sx = *reinterpret_cast<const float2*>(as + t4);
+                acc2[t4 / 2] = acc_pair(acc2[t4 / 2], sd[t4], sd[t4 + 1], mul_pair(dw2, make_pair(sx.x, sx.y)));
+              } else {
+                acc2[t4 / 2] = acc_pair(acc2[t4 / 2], sd[t4], (int)kMagic, mul_pair(dw2, dup_pair(as[t4])));
+              }
             }
           }
         }
@@ -569,22 +739,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if constexpr (!EMIT) {
-      float acc[NT];
+      // this thread's outputs as (row within the warp's 32, token, value)
+      float acc[kMma ? 1 : NT];
+      if constexpr (!kMma) {
 #pragma unroll
-      for (int p = 0; p < NP; ++p) {
-        const float2 v = unpack_pair(acc2[p]);
-        acc[2 * p] = v.x;
-        if (2 * p + 1 < NT) acc[2 * p + 1] = v.y;
+        for (int p = 0; p < NP; ++p) {
+          const float2 v = unpack_pair(acc2[p]);
+          acc[2 * p] = v.x;
+          if (2 * p + 1 < NT) acc[2 * p + 1] = v.y;
+        }
       }
+      auto for_outputs = [&](auto&& f) {
+        if constexpr (kMma) {
+          const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+          for (int ri = 0; ri < 4; ++ri)
+#pragma unroll
+            for (int n = 0; n < NTN; ++n) {
+              const float2 v = unpack_pair(accm[ri][n]);
+              const int t = 8 * n + 2 * c;
+              if (t < NT) f(8 * ri + g, t, v.x);
+              if (t + 1 < NT) f(8 * ri + g, t + 1, v.y);
+            }
+        } else {
+#pragma unroll
+          for (int t = 0; t < NT; ++t) f(lane, t, acc[t]);
+        }
+      };
       if (KW == 1 && S == 1) {
         // One warp owns these rows over the whole k: write them directly.
-        if (row < rows) {
-#pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            const size_t o = (size_t)t * rows + row;
-            y[o] = residual ? __fadd_rn(__ldcg(residual + o), acc[t]) : acc[t];  // residual may alias y
+        for_outputs([&](int rl, int t, float v) {
+          const int r = row0 + grp * kRowsPerWarp + rl;
+          if (r < rows) {
+            const size_t o = (size_t)t * rows + r;
+            y[o] = residual ? __fadd_rn(__ldcg(residual + o), v) : v;  // residual may alias y
           }
-        }
+        });
       } else {
         // the previous tile's cluster sums, now that this tile is computed
         if (cluster_sums && m > 0) {
@@ -593,12 +783,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float* rs = red_sum + (m & 1) * kSum;
         if (KW == 1) {
-#pragma unroll
-          for (int t = 0; t < NT; ++t) rs[(grp * NT + t) * 32 + lane] = acc[t];
+          for_outputs([&](int rl, int t, float v) { rs[(grp * NT + t) * 32 + rl] = v; });
         } else {
           // the KW warps of each row group, added in warp (k-phase) order
-#pragma unroll
-          for (int t = 0; t < NT; ++t) red[(warp * NT + t) * 32 + lane] = acc[t];
+          for_outputs([&](int rl, int t, float v) { red[(warp * NT + t) * 32 + rl] = v; });
           __syncthreads();
           for (int idx = threadIdx.x; idx < kSum; idx += kThreads) {
             const int gq = idx / (NT * 32), rest = idx - gq * NT * 32;
