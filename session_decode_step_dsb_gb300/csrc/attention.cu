@@ -30,6 +30,10 @@
 //    sum of exp * V) for the chunk.  While an item is being computed, one
 //    thread decodes the next item and the query rows of the next item are
 //    loaded into registers, so an item starts with no dependent global reads.
+//  * up to 32 query rows per kv head, the same partial kernel runs its two
+//    contractions on the tensor cores (attention_partial_tc_kernel below):
+//    the per-key CUDA-core dot products and the broadcast query reads they
+//    need were the kernel's cost at decode sizes.
 //  * merge kernel, one warp per (token row, head): rescales the chunk partials
 //    by exp(m_c - max_c m_c) and adds them in chunk order.
 // No atomics and no inter-CTA waits; the chunking depends only on each
@@ -157,23 +161,33 @@ __device__ __forceinline__ Item decode_item(int item, int n_kv_heads, int ctx, c
   return it;
 }
 
-// One thread issues the chunk's K and V boxes (64-key boxes, only as many as
-// hold its keys) on the two barriers.
+// One thread issues the chunk's K (or V) boxes (64-key boxes, only as many as
+// hold its keys) on one barrier.
+template <int D>
+__device__ __forceinline__ uint32_t tile_bytes(const Item& it) {
+  return (uint32_t)((D / kBoxCols) * (it.nkeys > kBoxKeys ? 2 : 1) * kBoxBytes);
+}
+
+template <int D>
+__device__ __forceinline__ void issue_boxes(const Item& it, const CUtensorMap* tm, uint8_t* dst, uint64_t* bar) {
+  const int halves = it.nkeys > kBoxKeys ? 2 : 1;
+#pragma unroll
+  for (int cb = 0; cb < D / kBoxCols; ++cb)
+    for (int h = 0; h < halves; ++h)
+      tma_load_2d(dst + cb * kColBoxBytes + h * kBoxBytes, tm, cb * kBoxCols, (int)(it.row0 + h * kBoxKeys), bar);
+}
+
+template <int D>
+__device__ __forceinline__ void issue_tile(const Item& it, const CUtensorMap* tm, uint8_t* dst, uint64_t* bar) {
+  mbar_arrive_expect_tx(bar, tile_bytes<D>(it));
+  issue_boxes<D>(it, tm, dst, bar);
+}
+
 template <int D>
 __device__ __forceinline__ void issue_chunk(const Item& it, const CUtensorMap* tmk, const CUtensorMap* tmv, uint8_t* Ks,
                                             uint8_t* Vs, uint64_t* bar_k, uint64_t* bar_v) {
-  const int halves = it.nkeys > kBoxKeys ? 2 : 1;
-  const uint32_t bytes = (uint32_t)((D / kBoxCols) * halves * kBoxBytes);
-  mbar_arrive_expect_tx(bar_k, bytes);
-  mbar_arrive_expect_tx(bar_v, bytes);
-#pragma unroll
-  for (int cb = 0; cb < D / kBoxCols; ++cb)
-    for (int h = 0; h < halves; ++h)
-      tma_load_2d(Ks + cb * kColBoxBytes + h * kBoxBytes, tmk, cb * kBoxCols, (int)(it.row0 + h * kBoxKeys), bar_k);
-#pragma unroll
-  for (int cb = 0; cb < D / kBoxCols; ++cb)
-    for (int h = 0; h < halves; ++h)
-      tma_load_2d(Vs + cb * kColBoxBytes + h * kBoxBytes, tmv, cb * kBoxCols, (int)(it.row0 + h * kBoxKeys), bar_v);
+  issue_tile<D>(it, tmk, Ks, bar_k);
+  issue_tile<D>(it, tmv, Vs, bar_v);
 }
 
 // kFull: R is a multiple of kRowGroup, so every row of every group is live and
@@ -404,6 +418,346 @@ __global__ void __launch_bounds__(kThreads) attention_partial_kernel(
   }  // work items
 }
 
+// ---- the tensor-core partial kernel ----------------------------------------
+//
+// Same items, same partial records, same masks as the kernel above; the two
+// contractions of an item run on the tensor cores (warp-level mma.sync
+// m16n8k16 in the cache's 16-bit type, f32 accumulate):
+//   S^T = K . Q^T   keys x query rows: warp w takes keys 32w..32w+31 (two
+//                   16-key tiles), all rows (8-row tiles), K = D;
+//   O^T = V^T . P^T dims x query rows: warp w takes dims D/4 * w.. (one or
+//                   two 16-dim tiles), all rows, K = the chunk's keys.
+// K and V fragments come straight from the swizzled TMA tiles by ldmatrix
+// (V transposed on the way).  The float query rows and probabilities enter
+// as hi + lo pairs of the 16-bit type (x = hi + lo to 2^-16 relative, 2^-22
+// for f16), each product being two MMAs, so the scores and sums keep float
+// accuracy; the cache values are exact in that type.  The query rows arrive
+// by bulk copies issued just before the item's K boxes and on the same
+// barrier (plain loads issued after the CTAs' K and V copies waited behind
+// all of that traffic).  K's buffer is handed to the next item's query and K
+// copies as soon as the scores are done, V's after P.V.
+template <typename T>
+struct Tc;
+template <>
+struct Tc<__half> {
+  static __device__ __forceinline__ void split(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __floats2half2_rn(x0, x1);
+    const float2 f = __half22float2(h);
+    const __half2 l = __floats2half2_rn(x0 - f.x, x1 - f.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+  }
+  static __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+};
+template <>
+struct Tc<__nv_bfloat16> {
+  static __device__ __forceinline__ void split(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 f = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - f.x, x1 - f.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+  }
+  static __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// Shared memory of the tensor-core kernel (bytes past the 1024-byte aligned
+// base): Ks | Vs [D/64][128][128 B] | Qf [R8][D] f32 (the query rows as
+// copied) | Qh | Ql [R8][D + 8] | Ph | Pl [R8][136] (16-bit; the 16-byte row
+// padding puts the 8 rows of an ldmatrix in distinct banks) | per-warp row
+// max and sum [2][4][R8] f32 | 2 barriers | next item.
+template <int D, int NRT>
+__host__ __device__ constexpr size_t tc_smem_bytes() {
+  return 1024 + 4 * (size_t)kCh * D + (size_t)(8 * NRT) * D * 4 + 2 * (size_t)(8 * NRT) * (D + 8) * 2 +
+         2 * (size_t)(8 * NRT) * (kCh + 8) * 2 + 2 * (size_t)kWarps * (8 * NRT) * 4 + 2 * 8 + sizeof(Item) + 8;
+}
+
+template <int D, typename T, int NRT>
+__global__ void __launch_bounds__(kThreads) attention_partial_tc_kernel(
+    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const float* __restrict__ q,
+    long long q_stride, int n_q_heads, int n_kv_heads, int ctx, const int32_t* __restrict__ batch_index,
+    const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ chunk_off, int n_seq, int tps, int max_chunks,
+    float scale, float* __restrict__ partials, const PagedView pv) {
+  constexpr int R8 = 8 * NRT;        // query rows, padded to whole 8-row tiles
+  constexpr int QS = D + 8;          // row strides (16-bit elements)
+  constexpr int PS = kCh + 8;
+  constexpr int MTV = D / kWarps / 16;  // 16-dim tiles of P.V per warp
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int G = n_q_heads / n_kv_heads, R = G * tps;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Ks = smem;
+  uint8_t* Vs = Ks + (size_t)D * kCh * 2;
+  float* Qf = reinterpret_cast<float*>(Vs + (size_t)D * kCh * 2);
+  uint16_t* Qh = reinterpret_cast<uint16_t*>(Qf + R8 * D);
+  uint16_t* Ql = Qh + R8 * QS;
+  uint16_t* Ph = Ql + R8 * QS;
+  uint16_t* Pl = Ph + R8 * PS;
+  float* wmax = reinterpret_cast<float*>(Pl + R8 * PS);  // [warp][R8]
+  float* wsum = wmax + kWarps * R8;
+  uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(wsum + kWarps * R8) + 7) & ~uintptr_t(7));
+  Item* nx = reinterpret_cast<Item*>(bars + 2);
+  const uint32_t ks_addr = smem_addr(Ks), vs_addr = smem_addr(Vs);
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+  }
+  // the padding query rows R..R8-1 stay zero
+  for (int idx = tid; idx < (R8 - R) * QS; idx += kThreads) {
+    Qh[R * QS + idx] = 0;
+    Ql[R * QS + idx] = 0;
+  }
+  pdl_wait();  // q and the cache rows of this step come from the previous kernels
+  pdl_trigger();
+
+  const int total_items = chunk_off[n_seq] * n_kv_heads;
+  // Thread 0 requests an item's query rows (one bulk copy of G*D floats per
+  // draft token) and then its K boxes, all on bars[0]: the query rows are
+  // first in line behind no K or V traffic of this CTA.
+  auto issue_qk = [&](const Item& x) {
+    const uint32_t qb = (uint32_t)(G * D * 4);
+    mbar_arrive_expect_tx(&bars[0], (uint32_t)tps * qb + tile_bytes<D>(x));
+    for (int j = 0; j < tps; ++j)
+      bulk_g2s(Qf + (size_t)j * G * D, q + (size_t)(x.s * tps + j) * q_stride + (size_t)x.g * G * D, qb, &bars[0]);
+    issue_boxes<D>(x, &tmk, Ks, &bars[0]);
+  };
+  if ((int)blockIdx.x < total_items && tid == 0) {
+    const Item first = decode_item(blockIdx.x, n_kv_heads, ctx, batch_index, seq_lens, chunk_off, n_seq, tps, pv);
+    *nx = first;
+    issue_qk(first);
+    issue_tile<D>(first, &tmv, Vs, &bars[1]);
+  }
+  __syncthreads();
+  uint32_t phase = 0;
+  for (int item = blockIdx.x; item < total_items; item += gridDim.x, phase ^= 1u) {
+    const Item it = *nx;
+    if (!mbar_wait(&bars[0], phase)) g_err_attention = 1u;  // query rows and K
+    __syncwarp();  // ldmatrix and mma.sync below run warp-converged
+    for (int i2 = tid; i2 < R * D / 2; i2 += kThreads) {
+      const float2 v = *reinterpret_cast<const float2*>(Qf + 2 * i2);
+      const int e = 2 * i2, r = e / D, d = e - r * D;
+      uint32_t hi, lo;
+      Tc<T>::split(v.x, v.y, hi, lo);
+      *reinterpret_cast<uint32_t*>(Qh + r * QS + d) = hi;
+      *reinterpret_cast<uint32_t*>(Ql + r * QS + d) = lo;
+    }
+    __syncthreads();
+    const int next = item + gridDim.x;
+    if (tid == 0 && next < total_items)
+      *nx = decode_item(next, n_kv_heads, ctx, batch_index, seq_lens, chunk_off, n_seq, tps, pv);
+
+    // ---- S^T = K . Q^T: this warp's 32 keys x R8 rows
+    float sacc[2][NRT][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NRT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.0f;
+    {
+      const int mi = lane >> 3;  // the ldmatrix sub-matrix this lane addresses
+#pragma unroll
+      for (int kq = 0; kq < D / 16; ++kq) {
+        uint32_t a[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+          ldsm_x4(a[mt], ks_addr + swz(32 * warp + 16 * mt + (lane & 7) + 8 * (mi & 1), 2 * kq + (mi >> 1)));
+#pragma unroll
+        for (int nt = 0; nt < NRT; ++nt) {
+          uint32_t b[4];  // Qh dims +0, +8, Ql dims +0, +8 of rows 8nt..8nt+7
+          ldsm_x4(b, smem_addr((mi >> 1 ? Ql : Qh) + (8 * nt + (lane & 7)) * QS + 16 * kq + 8 * (mi & 1)));
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            Tc<T>::mma(sacc[mt][nt], a[mt], b[0], b[1]);
+            Tc<T>::mma(sacc[mt][nt], a[mt], b[2], b[3]);
+          }
+        }
+      }
+    }
+    // scale and mask: element e of tile (mt, nt) is key 32w + 16mt + g + 8(e >> 1),
+    // row 8nt + 2c + (e & 1); then the chunk's row maxima
+    float mx[NRT][2];
+#pragma unroll
+    for (int nt = 0; nt < NRT; ++nt) mx[nt][0] = mx[nt][1] = -INFINITY;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NRT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int kl = 32 * warp + 16 * mt + g + 8 * (e >> 1), row = 8 * nt + 2 * c + (e & 1);
+          const int j = row / G;
+          const int vis = it.L - tps + j + 1;         // keys before vis are visible to draft token j ...
+          const int vlo = it.W > 0 ? vis - it.W : 0;  // ... from vlo on under a window
+          const int key = it.key0 + kl;
+          const bool ok = row < R && kl < it.nkeys && key < vis && key >= vlo;
+          const float v = ok ? __fmul_rn(sacc[mt][nt][e], scale) : -INFINITY;
+          sacc[mt][nt][e] = v;
+          mx[nt][e & 1] = fmaxf(mx[nt][e & 1], v);
+        }
+#pragma unroll
+    for (int nt = 0; nt < NRT; ++nt)
+#pragma unroll
+      for (int j2 = 0; j2 < 2; ++j2) {
+        float m = mx[nt][j2];
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (g == 0) wmax[warp * R8 + 8 * nt + 2 * c + j2] = m;
+      }
+    fence_proxy_async_smem();  // the K and query reads precede the next item's copies
+    __syncthreads();
+    if (tid == 0 && next < total_items) issue_qk(*nx);
+
+    // ---- probabilities (hi + lo into Ph / Pl) and the per-warp row sums
+    float sm[NRT][2];
+#pragma unroll
+    for (int nt = 0; nt < NRT; ++nt)
+#pragma unroll
+      for (int j2 = 0; j2 < 2; ++j2) {
+        const int row = 8 * nt + 2 * c + j2;
+        float M = wmax[row];
+#pragma unroll
+        for (int w2 = 1; w2 < kWarps; ++w2) M = fmaxf(M, wmax[w2 * R8 + row]);
+        mx[nt][j2] = M;
+        sm[nt][j2] = 0.0f;
+      }
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NRT; ++nt)
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {  // keys g and g + 8 of the tile, rows 2c and 2c + 1
+          const float M0 = mx[nt][0], M1 = mx[nt][1];
+          const float p0 = (M0 == -INFINITY) ? 0.0f : expf(sacc[mt][nt][2 * e2] - M0);
+          const float p1 = (M1 == -INFINITY) ? 0.0f : expf(sacc[mt][nt][2 * e2 + 1] - M1);
+          sm[nt][0] = __fadd_rn(sm[nt][0], p0);
+          sm[nt][1] = __fadd_rn(sm[nt][1], p1);
+          const int kl = 32 * warp + 16 * mt + g + 8 * e2, row = 8 * nt + 2 * c;
+          uint32_t hi, lo;
+          Tc<T>::split(p0, p1, hi, lo);
+          Ph[row * PS + kl] = (uint16_t)(hi & 0xFFFFu);
+          Ph[(row + 1) * PS + kl] = (uint16_t)(hi >> 16);
+          Pl[row * PS + kl] = (uint16_t)(lo & 0xFFFFu);
+          Pl[(row + 1) * PS + kl] = (uint16_t)(lo >> 16);
+        }
+#pragma unroll
+    for (int nt = 0; nt < NRT; ++nt)
+#pragma unroll
+      for (int j2 = 0; j2 < 2; ++j2) {
+        float l = sm[nt][j2];
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, o));
+        if (g == 0) wsum[warp * R8 + 8 * nt + 2 * c + j2] = l;
+      }
+    __syncthreads();
+    // row statistics of the chunk: (max, sum of exp), warps added in order
+    if (tid < R) {
+      float M = wmax[tid], l = wsum[tid];
+#pragma unroll
+      for (int w2 = 1; w2 < kWarps; ++w2) {
+        M = fmaxf(M, wmax[w2 * R8 + tid]);
+        l = __fadd_rn(l, wsum[w2 * R8 + tid]);
+      }
+      const int j = tid / G, gi = tid - j * G;
+      float* dst = partials + (((size_t)(it.s * tps + j) * n_q_heads + it.g * G + gi) * max_chunks + it.c_rel) * (D + 2);
+      dst[0] = M;
+      dst[1] = l;
+    }
+    if (!mbar_wait(&bars[1], phase)) g_err_attention = 1u;
+    __syncwarp();
+
+    // ---- O^T = V^T . P^T: this warp's dims x R8 rows over the chunk's keys
+    float oacc[MTV][NRT][4];
+#pragma unroll
+    for (int mv = 0; mv < MTV; ++mv)
+#pragma unroll
+      for (int nt = 0; nt < NRT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oacc[mv][nt][e] = 0.0f;
+    {
+      const int mi = lane >> 3;
+      const int nkk = (it.nkeys + 15) >> 4;
+      for (int kk = 0; kk < nkk; ++kk) {
+        uint32_t a[MTV][4];
+#pragma unroll
+        for (int mv = 0; mv < MTV; ++mv)
+          ldsm_x4_trans(a[mv], vs_addr + swz(16 * kk + (lane & 7) + 8 * (mi >> 1), (D / kWarps / 8) * warp + 2 * mv +
+                                                                                      (mi & 1)));
+        if (16 * kk + 16 > it.nkeys) {
+          // keys past the chunk's end: their rows may hold anything (the
+          // probabilities there are zero, but 0 * inf is not), so zero them
+          const int k0 = 16 * kk + 2 * c, k8 = k0 + 8;
+          const uint32_t m0 = (k0 < it.nkeys ? 0xFFFFu : 0u) | (k0 + 1 < it.nkeys ? 0xFFFF0000u : 0u);
+          const uint32_t m8 = (k8 < it.nkeys ? 0xFFFFu : 0u) | (k8 + 1 < it.nkeys ? 0xFFFF0000u : 0u);
+#pragma unroll
+          for (int mv = 0; mv < MTV; ++mv) {
+            a[mv][0] &= m0;
+            a[mv][1] &= m0;
+            a[mv][2] &= m8;
+            a[mv][3] &= m8;
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NRT; ++nt) {
+          uint32_t b[4];  // Ph keys +0, +8, Pl keys +0, +8 of rows 8nt..8nt+7
+          ldsm_x4(b, smem_addr((mi >> 1 ? Pl : Ph) + (8 * nt + (lane & 7)) * PS + 16 * kk + 8 * (mi & 1)));
+#pragma unroll
+          for (int mv = 0; mv < MTV; ++mv) {
+            Tc<T>::mma(oacc[mv][nt], a[mv], b[0], b[1]);
+            Tc<T>::mma(oacc[mv][nt], a[mv], b[2], b[3]);
+          }
+        }
+      }
+    }
+    // element e of tile (mv, nt): dim D/4 * w + 16mv + g + 8(e >> 1), row 8nt + 2c + (e & 1)
+#pragma unroll
+    for (int nt = 0; nt < NRT; ++nt)
+#pragma unroll
+      for (int j2 = 0; j2 < 2; ++j2) {
+        const int row = 8 * nt + 2 * c + j2;
+        if (row < R) {
+          const int j = row / G, gi = row - j * G;
+          float* dst = partials +
+                       (((size_t)(it.s * tps + j) * n_q_heads + it.g * G + gi) * max_chunks + it.c_rel) * (D + 2) + 2;
+#pragma unroll
+          for (int mv = 0; mv < MTV; ++mv) {
+            const int d0 = (D / kWarps) * warp + 16 * mv + g;
+            dst[d0] = oacc[mv][nt][j2];
+            dst[d0 + 8] = oacc[mv][nt][2 + j2];
+          }
+        }
+      }
+    fence_proxy_async_smem();  // the V reads precede the next item's copy into Vs
+    __syncthreads();
+    if (tid == 0 && next < total_items) issue_tile<D>(*nx, &tmv, Vs, &bars[1]);
+  }  // work items
+}
+
 // One warp per (token row, query head).  Lanes first take the chunks 32 at a
 // time (max of m_c, then w_c = exp(m_c - M) and the partial sum of w_c l_c);
 // the sums over lanes use a fixed xor tree; then the warp walks the chunks in
@@ -531,41 +885,45 @@ cudaError_t kv_tensor_map(const void* base, long long rows, int D, int dtype, CU
   return cudaSuccess;
 }
 
-template <int D, typename T, int kRowGroup, bool kFull>
-cudaError_t launch_rg_full(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc, int dtype,
-                           int n_kv_heads, int ctx, long long kv_rows, MetaView meta, int n_seq, int tps,
-                           long long max_items, int max_chunks, float* partials, float* out, void* xq_out,
-                           PagedView pv, cudaStream_t st) {
-  const int R = (n_q_heads / n_kv_heads) * tps;
-  const size_t smem = partial_smem<D, T, kRowGroup>(R);
-  auto kern = attention_partial_kernel<D, T, kRowGroup, kFull>;
+// Launch a partial kernel as a persistent grid (as many CTAs as fit at once,
+// capped by the item count), then the merge.
+template <int D, typename Kern>
+cudaError_t launch_partial_merge(Kern kern, size_t smem, const float* q, long long q_stride, int n_q_heads,
+                                 const void* kc, const void* vc, int dtype, int n_kv_heads, int ctx, long long kv_rows,
+                                 MetaView meta, int n_seq, int tps, long long max_items, int max_chunks,
+                                 float* partials, float* out, void* xq_out, PagedView pv, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   CUtensorMap tmk, tmv;
   if ((e = kv_tensor_map(kc, kv_rows, D, dtype, &tmk)) != cudaSuccess) return e;
   if ((e = kv_tensor_map(vc, kv_rows, D, dtype, &tmv)) != cudaSuccess) return e;
   const float scale = (float)(1.0 / sqrt((double)D));
-  // Persistent grid: as many CTAs as fit at once, capped by the item count.
   int resident = 0;
   {
+    struct Entry {
+      const void* kern;
+      size_t smem;
+      int dev, ctas;
+    };
     static std::mutex mu;
-    static int cached = 0, cached_dev = -1;
-    static size_t cached_smem = 0;
+    static Entry cache[32];
+    static int n_cache = 0;
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(mu);
-    if (cached == 0 || cached_smem != smem || cached_dev != dev) {
+    for (int i = 0; i < n_cache; ++i)
+      if (cache[i].kern == reinterpret_cast<const void*>(kern) && cache[i].smem == smem && cache[i].dev == dev)
+        resident = cache[i].ctas;
+    if (resident == 0) {
       int per_sm = 0, sms = 0;
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
       if (e != cudaSuccess) return e;
       e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
       if (e != cudaSuccess) return e;
-      cached = (per_sm > 0 ? per_sm : 1) * sms;
-      cached_smem = smem;
-      cached_dev = dev;
+      resident = (per_sm > 0 ? per_sm : 1) * sms;
+      if (n_cache < 32) cache[n_cache++] = Entry{reinterpret_cast<const void*>(kern), smem, dev, resident};
     }
-    resident = cached;
   }
   const long long items = (long long)max_items;
   const unsigned grid = (unsigned)(items < resident ? (items > 0 ? items : 1) : resident);
@@ -579,6 +937,27 @@ cudaError_t launch_rg_full(const float* q, long long q_stride, int n_q_heads, co
                          meta.chunk_off, max_chunks, n_tok, out, static_cast<uint8_t*>(xq_out));
   return launch_kernel(attention_merge_kernel<D, false>, dim3(mgrid), dim3(128), 0, st, partials, n_q_heads, tps,
                        meta.chunk_off, max_chunks, n_tok, out, static_cast<uint8_t*>(nullptr));
+}
+
+template <int D, typename T, int kRowGroup, bool kFull>
+cudaError_t launch_rg_full(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc, int dtype,
+                           int n_kv_heads, int ctx, long long kv_rows, MetaView meta, int n_seq, int tps,
+                           long long max_items, int max_chunks, float* partials, float* out, void* xq_out,
+                           PagedView pv, cudaStream_t st) {
+  const int R = (n_q_heads / n_kv_heads) * tps;
+  return launch_partial_merge<D>(attention_partial_kernel<D, T, kRowGroup, kFull>, partial_smem<D, T, kRowGroup>(R), q,
+                                 q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
+                                 max_items, max_chunks, partials, out, xq_out, pv, st);
+}
+
+template <int D, typename T, int NRT>
+cudaError_t launch_tc(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc, int dtype,
+                      int n_kv_heads, int ctx, long long kv_rows, MetaView meta, int n_seq, int tps,
+                      long long max_items, int max_chunks, float* partials, float* out, void* xq_out, PagedView pv,
+                      cudaStream_t st) {
+  return launch_partial_merge<D>(attention_partial_tc_kernel<D, T, NRT>, tc_smem_bytes<D, NRT>(), q, q_stride,
+                                 n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps, max_items,
+                                 max_chunks, partials, out, xq_out, pv, st);
 }
 
 // Row groups of 1, 2 and 5 serve R = 1, 2 and 5 only (always full); 4 and 8
@@ -605,6 +984,19 @@ cudaError_t launch_typed(const float* q, long long q_stride, int n_q_heads, cons
                          long long max_items, int max_chunks, float* partials, float* out, void* xq_out, PagedView pv,
                          cudaStream_t st) {
   const int R = (n_q_heads / n_kv_heads) * tps;
+  // up to 32 query rows per kv head: the tensor-core kernel (1, 2 or 4
+  // eight-row tiles), which copies the query rows in bulk (16-byte aligned
+  // rows); wider groups or unaligned query rows: the row-group kernel
+  const bool tc_ok = (reinterpret_cast<uintptr_t>(q) & 15) == 0 && (q_stride & 3) == 0;
+  if (tc_ok && R <= 8)
+    return launch_tc<D, T, 1>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
+                              max_items, max_chunks, partials, out, xq_out, pv, st);
+  if (tc_ok && R <= 16)
+    return launch_tc<D, T, 2>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
+                              max_items, max_chunks, partials, out, xq_out, pv, st);
+  if (tc_ok && R <= 32)
+    return launch_tc<D, T, 4>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
+                              max_items, max_chunks, partials, out, xq_out, pv, st);
   if (R <= 1)
     return launch_rg<D, T, 1>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
                               max_items, max_chunks, partials, out, xq_out, pv, st);

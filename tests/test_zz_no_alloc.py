@@ -83,6 +83,10 @@ def test_no_alloc_at_its_limits_and_allocates_nothing(cuda_device):
         ws = d.Workspace(len(bi) * T, hq, D, C)
         ref = to_host(d.attention_decode_multi(qd, kv, bi, T, lens, ws))
         out = torch.empty_like(qd)
+        # torch's own fill kernel runs inside the measured window below; with
+        # lazy module loading its first launch loads it into device memory,
+        # so it runs once here first
+        out.zero_()
         d.attention_decode_multi_noalloc(qd, kv, bi, T, lens, out=out)
         torch.cuda.synchronize()
         free0 = torch.cuda.mem_get_info()[0]
