@@ -236,10 +236,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* act_s = reinterpret_cast<float*>(smem + L.act_s);
   uint32_t* act_su = reinterpret_cast<uint32_t*>(smem + L.act_s);  // mma path view
   // the fp16 scale (bits) of activation block idx = blk * NTA + t: as a float
-  // (dp4a path) or kept as bits, next to the block's code sum (mma path)
-  auto store_scale = [&](size_t idx, uint32_t bits16) {
+  // (dp4a path), or kept as bits with the block's code sum (|sum| <= 4064) as
+  // int16 in the high half (mma path: -1152 * sum starts the block's
+  // tensor-core accumulator)
+  auto store_scale = [&](size_t idx, uint32_t bits16, int code_sum) {
     if constexpr (kMma)
-      act_su[idx] = bits16 & 0xFFFFu;
+      act_su[idx] = (bits16 & 0xFFFFu) | ((uint32_t)code_sum << 16);
     else
       act_s[idx] = half_bits_to_float(bits16);
   };
@@ -335,17 +337,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
+          int sx = 0;  // the block's code sum (mma path)
           if ((b & 1) == 0) {
             const int base = (17 * b) / 2;
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              act_word(j * 8 + b, k, t) = __funnelshift_r(wv[base + k], wv[base + k + 1], 16) ^ kActXor;
-            store_scale((size_t)(j * 8 + b) * NTA + t, wv[base]);
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t x = __funnelshift_r(wv[base + k], wv[base + k + 1], 16);
+              if constexpr (kMma) sx = __dp4a((int)x, 0x01010101, sx);
+              act_word(j * 8 + b, k, t) = x ^ kActXor;
+            }
+            store_scale((size_t)(j * 8 + b) * NTA + t, wv[base], sx);
           } else {
             const int base = (17 * b - 1) / 2;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) act_word(j * 8 + b, k, t) = wv[base + 1 + k] ^ kActXor;
-            store_scale((size_t)(j * 8 + b) * NTA + t, wv[base] >> 16);
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t x = wv[base + 1 + k];
+              if constexpr (kMma) sx = __dp4a((int)x, 0x01010101, sx);
+              act_word(j * 8 + b, k, t) = x ^ kActXor;
+            }
+            store_scale((size_t)(j * 8 + b) * NTA + t, wv[base] >> 16, sx);
           }
         }
       }
@@ -445,6 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 32; ++j) a = fmaxf(a, fabsf(v[j]));
       const float d = __fdiv_rn(a, 127.0f);
+      int sx = 0;  // the block's code sum (mma path)
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         uint32_t word = 0;
@@ -454,24 +465,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (d != 0.0f) q = (int)fminf(fmaxf(roundf(__fdiv_rn(v[4 * k + j], d)), -127.0f), 127.0f);
           word |= ((uint32_t)q & 0xFFu) << (8 * j);
         }
+        if constexpr (kMma) sx = __dp4a((int)word, 0x01010101, sx);
         act_word(b, k, t) = word ^ kActXor;
       }
-      store_scale((size_t)b * NTA + t, __half_as_ushort(__float2half_rn(d)));
-    }
-  }
-  if constexpr (kMma) {
-    // the sum of the 32 codes of every (block, token), |sum| <= 4064, as int16
-    // in the high half of the scale word: -1152 * sum starts the block's
-    // tensor-core accumulator.  The stored bytes are codes + 128.
-    __syncthreads();
-    if (!dead) {
-      for (int idx = threadIdx.x; idx < kr * 8 * NT; idx += kThreads) {
-        const int blk = idx / NT, t = idx - blk * NT;
-        unsigned int su = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) su = __dp4a(act_word(blk, k, t), 0x01010101u, su);
-        act_su[(size_t)blk * NTA + t] |= ((uint32_t)((int)su - 32 * 128) & 0xFFFFu) << 16;
-      }
+      store_scale((size_t)b * NTA + t, __half_as_ushort(__float2half_rn(d)), sx);
     }
   }
   // every thread's reads of the raw rows precede the copies into those stages
