@@ -47,6 +47,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "dsb_actlayout.cuh"
 #include "dsb_kernels.h"
 #include "dsb_ptx.cuh"
 #include "dsb_q8.cuh"
@@ -767,7 +768,8 @@ template <int D, bool QOUT>
 __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __restrict__ partials, int n_q_heads,
                                                               int tps, const int32_t* __restrict__ chunk_off,
                                                               int max_chunks, int n_tok, float* __restrict__ out,
-                                                              uint8_t* __restrict__ xq) {
+                                                              uint8_t* __restrict__ xq,
+                                                              uint32_t* __restrict__ xq_staged) {
   pdl_wait();
   pdl_trigger();
   const int wg = blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -822,7 +824,13 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
   if constexpr (QOUT) {
     uint8_t* dst = xq + ((size_t)t * n_q_heads + h) * (D / 32) * 34;
 #pragma unroll
-    for (int e = 0; e < D / 32; ++e) q8_block_store(__fdiv_rn(acc[e], lsum), dst + (size_t)e * 34, lane);
+    for (int e = 0; e < D / 32; ++e) {
+      if (xq_staged)
+        q8_block_store_staged(__fdiv_rn(acc[e], lsum), dst + (size_t)e * 34, xq_staged,
+                              (long long)n_q_heads * (D / 32), h * (D / 32) + e, t, n_tok, lane);
+      else
+        q8_block_store(__fdiv_rn(acc[e], lsum), dst + (size_t)e * 34, lane);
+    }
   } else {
     float* o = out + ((size_t)t * n_q_heads + h) * D;
 #pragma unroll
@@ -891,7 +899,7 @@ template <int D, typename Kern>
 cudaError_t launch_partial_merge(Kern kern, size_t smem, const float* q, long long q_stride, int n_q_heads,
                                  const void* kc, const void* vc, int dtype, int n_kv_heads, int ctx, long long kv_rows,
                                  MetaView meta, int n_seq, int tps, long long max_items, int max_chunks,
-                                 float* partials, float* out, void* xq_out, PagedView pv, cudaStream_t st) {
+                                 float* partials, float* out, void* xq_out, void* xq_staged, PagedView pv, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   CUtensorMap tmk, tmv;
@@ -934,30 +942,32 @@ cudaError_t launch_partial_merge(Kern kern, size_t smem, const float* q, long lo
   const unsigned mgrid = (unsigned)((n_tok * n_q_heads + 3) / 4);
   if (xq_out)
     return launch_kernel(attention_merge_kernel<D, true>, dim3(mgrid), dim3(128), 0, st, partials, n_q_heads, tps,
-                         meta.chunk_off, max_chunks, n_tok, out, static_cast<uint8_t*>(xq_out));
+                         meta.chunk_off, max_chunks, n_tok, out, static_cast<uint8_t*>(xq_out),
+                         static_cast<uint32_t*>(xq_staged));
   return launch_kernel(attention_merge_kernel<D, false>, dim3(mgrid), dim3(128), 0, st, partials, n_q_heads, tps,
-                       meta.chunk_off, max_chunks, n_tok, out, static_cast<uint8_t*>(nullptr));
+                       meta.chunk_off, max_chunks, n_tok, out, static_cast<uint8_t*>(nullptr),
+                       static_cast<uint32_t*>(nullptr));
 }
 
 template <int D, typename T, int kRowGroup, bool kFull>
 cudaError_t launch_rg_full(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc, int dtype,
                            int n_kv_heads, int ctx, long long kv_rows, MetaView meta, int n_seq, int tps,
-                           long long max_items, int max_chunks, float* partials, float* out, void* xq_out,
+                           long long max_items, int max_chunks, float* partials, float* out, void* xq_out, void* xq_staged,
                            PagedView pv, cudaStream_t st) {
   const int R = (n_q_heads / n_kv_heads) * tps;
   return launch_partial_merge<D>(attention_partial_kernel<D, T, kRowGroup, kFull>, partial_smem<D, T, kRowGroup>(R), q,
                                  q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
-                                 max_items, max_chunks, partials, out, xq_out, pv, st);
+                                 max_items, max_chunks, partials, out, xq_out, xq_staged, pv, st);
 }
 
 template <int D, typename T, int NRT>
 cudaError_t launch_tc(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc, int dtype,
                       int n_kv_heads, int ctx, long long kv_rows, MetaView meta, int n_seq, int tps,
-                      long long max_items, int max_chunks, float* partials, float* out, void* xq_out, PagedView pv,
+                      long long max_items, int max_chunks, float* partials, float* out, void* xq_out, void* xq_staged, PagedView pv,
                       cudaStream_t st) {
   return launch_partial_merge<D>(attention_partial_tc_kernel<D, T, NRT>, tc_smem_bytes<D, NRT>(), q, q_stride,
                                  n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps, max_items,
-                                 max_chunks, partials, out, xq_out, pv, st);
+                                 max_chunks, partials, out, xq_out, xq_staged, pv, st);
 }
 
 // Row groups of 1, 2 and 5 serve R = 1, 2 and 5 only (always full); 4 and 8
@@ -965,23 +975,23 @@ cudaError_t launch_tc(const float* q, long long q_stride, int n_q_heads, const v
 template <int D, typename T, int kRowGroup>
 cudaError_t launch_rg(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc, int dtype,
                       int n_kv_heads, int ctx, long long kv_rows, MetaView meta, int n_seq, int tps,
-                      long long max_items, int max_chunks, float* partials, float* out, void* xq_out, PagedView pv,
+                      long long max_items, int max_chunks, float* partials, float* out, void* xq_out, void* xq_staged, PagedView pv,
                       cudaStream_t st) {
   const int R = (n_q_heads / n_kv_heads) * tps;
   if (kRowGroup == 4 || kRowGroup == kMaxRowGroup) {
     if (R % kRowGroup != 0)
       return launch_rg_full<D, T, kRowGroup, false>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows,
-                                                    meta, n_seq, tps, max_items, max_chunks, partials, out, xq_out, pv,
+                                                    meta, n_seq, tps, max_items, max_chunks, partials, out, xq_out, xq_staged, pv,
                                                     st);
   }
   return launch_rg_full<D, T, kRowGroup, true>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta,
-                                               n_seq, tps, max_items, max_chunks, partials, out, xq_out, pv, st);
+                                               n_seq, tps, max_items, max_chunks, partials, out, xq_out, xq_staged, pv, st);
 }
 
 template <int D, typename T>
 cudaError_t launch_typed(const float* q, long long q_stride, int n_q_heads, const void* kc, const void* vc, int dtype,
                          int n_kv_heads, int ctx, long long kv_rows, MetaView meta, int n_seq, int tps,
-                         long long max_items, int max_chunks, float* partials, float* out, void* xq_out, PagedView pv,
+                         long long max_items, int max_chunks, float* partials, float* out, void* xq_out, void* xq_staged, PagedView pv,
                          cudaStream_t st) {
   const int R = (n_q_heads / n_kv_heads) * tps;
   // up to 32 query rows per kv head: the tensor-core kernel (1, 2 or 4
@@ -990,29 +1000,29 @@ cudaError_t launch_typed(const float* q, long long q_stride, int n_q_heads, cons
   const bool tc_ok = (reinterpret_cast<uintptr_t>(q) & 15) == 0 && (q_stride & 3) == 0;
   if (tc_ok && R <= 8)
     return launch_tc<D, T, 1>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
-                              max_items, max_chunks, partials, out, xq_out, pv, st);
+                              max_items, max_chunks, partials, out, xq_out, xq_staged, pv, st);
   if (tc_ok && R <= 16)
     return launch_tc<D, T, 2>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
-                              max_items, max_chunks, partials, out, xq_out, pv, st);
+                              max_items, max_chunks, partials, out, xq_out, xq_staged, pv, st);
   if (tc_ok && R <= 32)
     return launch_tc<D, T, 4>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
-                              max_items, max_chunks, partials, out, xq_out, pv, st);
+                              max_items, max_chunks, partials, out, xq_out, xq_staged, pv, st);
   if (R <= 1)
     return launch_rg<D, T, 1>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
-                              max_items, max_chunks, partials, out, xq_out, pv, st);
+                              max_items, max_chunks, partials, out, xq_out, xq_staged, pv, st);
   if (R <= 2)
     return launch_rg<D, T, 2>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
-                              max_items, max_chunks, partials, out, xq_out, pv, st);
+                              max_items, max_chunks, partials, out, xq_out, xq_staged, pv, st);
   if (R <= 4)
     return launch_rg<D, T, 4>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
-                              max_items, max_chunks, partials, out, xq_out, pv, st);
+                              max_items, max_chunks, partials, out, xq_out, xq_staged, pv, st);
   // five query rows per kv head: GQA 5:1 at one token per sequence (the
   // Qwen3-14B shape), where a group of eight would carry three idle rows
   if (R == 5)
     return launch_rg<D, T, 5>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq, tps,
-                              max_items, max_chunks, partials, out, xq_out, pv, st);
+                              max_items, max_chunks, partials, out, xq_out, xq_staged, pv, st);
   return launch_rg<D, T, kMaxRowGroup>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq,
-                                       tps, max_items, max_chunks, partials, out, xq_out, pv, st);
+                                       tps, max_items, max_chunks, partials, out, xq_out, xq_staged, pv, st);
 }
 
 }  // namespace
@@ -1026,22 +1036,22 @@ cudaError_t launch_attention_decode_multi(const float* q, long long q_stride, in
                                           const void* vc, int dtype, int n_kv_heads, int ctx, int head_dim,
                                           long long kv_rows, MetaView meta, int n_seq, int tokens_per_seq,
                                           long long max_items, int max_chunks, float* partials, float* out,
-                                          void* xq_out, cudaStream_t st, PagedView pv) {
+                                          void* xq_out, cudaStream_t st, PagedView pv, void* xq_staged) {
   if (n_seq == 0) return cudaSuccess;
   if (head_dim == 128) {
     if (dtype == 0)
       return launch_typed<128, __half>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq,
-                                       tokens_per_seq, max_items, max_chunks, partials, out, xq_out, pv, st);
+                                       tokens_per_seq, max_items, max_chunks, partials, out, xq_out, xq_staged, pv, st);
     return launch_typed<128, __nv_bfloat16>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta,
-                                            n_seq, tokens_per_seq, max_items, max_chunks, partials, out, xq_out, pv,
+                                            n_seq, tokens_per_seq, max_items, max_chunks, partials, out, xq_out, xq_staged, pv,
                                             st);
   }
   if (head_dim == 64) {
     if (dtype == 0)
       return launch_typed<64, __half>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta, n_seq,
-                                      tokens_per_seq, max_items, max_chunks, partials, out, xq_out, pv, st);
+                                      tokens_per_seq, max_items, max_chunks, partials, out, xq_out, xq_staged, pv, st);
     return launch_typed<64, __nv_bfloat16>(q, q_stride, n_q_heads, kc, vc, dtype, n_kv_heads, ctx, kv_rows, meta,
-                                           n_seq, tokens_per_seq, max_items, max_chunks, partials, out, xq_out, pv,
+                                           n_seq, tokens_per_seq, max_items, max_chunks, partials, out, xq_out, xq_staged, pv,
                                            st);
   }
   return cudaErrorInvalidValue;

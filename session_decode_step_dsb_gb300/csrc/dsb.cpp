@@ -262,7 +262,8 @@ dsb_status dsb_device_error(void) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
   const unsigned int m = dsbk::read_clear_error_matmul();
-  const unsigned int mt = dsbk::read_clear_error_matmul_tc() | dsbk::read_clear_error_matmul_fused();
+  const unsigned int mt = dsbk::read_clear_error_matmul_tc() | dsbk::read_clear_error_matmul_fused() |
+                           dsbk::read_clear_error_matmul_staged();
   const unsigned int a = dsbk::read_clear_error_attention();
   if (m || mt || a)
     return fail(DSB_ERR_DEVICE, "a kernel's bounded wait ran out (matmul=%u matmul_tc=%u attention=%u)", m, mt, a);
@@ -788,7 +789,7 @@ dsb_status dsb_rope_kv_write(float* qkv, int n_q_heads, const dsb_kv_cache* kv, 
 namespace {
 
 struct StepLayout {
-  size_t h = 0, qkv = 0, att = 0, gu = 0, xq = 0, graph_meta = 0, partials = 0, pack = 0, total = 0;
+  size_t h = 0, qkv = 0, att = 0, gu = 0, xq = 0, staged = 0, graph_meta = 0, partials = 0, pack = 0, total = 0;
 };
 
 StepLayout step_layout(const dsb_model_shape& sh, int n_tok, int ctx) {
@@ -810,6 +811,9 @@ StepLayout step_layout(const dsb_model_shape& sh, int n_tok, int ctx) {
   L.att = take(nt * att_cols * 4);
   L.gu = take(nt * 2 * (size_t)sh.ffn * 4);
   L.xq = take(nt * (max_cols / 32) * 34);
+  // the narrow matmul's staged activation layout, written by the q8_0-emitting
+  // kernels next to the q8_0 rows (n_tok <= DSB_NARROW_MAX)
+  L.staged = take(n_tok <= DSB_NARROW_MAX ? dsbk::matmul_staged_bytes(n_tok, (int64_t)max_cols) : 0);
   L.graph_meta = take(kMetaSlotBytes);
   L.partials = take(dsbk::attention_partial_bytes(n_tok, sh.n_q_heads, sh.head_dim, ctx));
   // packed token operands of the tensor-core matmul (n_tok > DSB_NARROW_MAX)
@@ -944,6 +948,12 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
   void* xq = ws->dev + L.xq;
   float* partials = reinterpret_cast<float*>(ws->dev + L.partials);
   void* pack = ws->dev + L.pack;
+  // staged activations for the narrow matmuls (nullptr past DSB_NARROW_MAX tokens)
+  void* stg = n_tok <= DSB_NARROW_MAX ? static_cast<void*>(ws->dev + L.staged) : nullptr;
+  auto mm = [&](const dsb_q8_0_mat& w, float* y, const float* residual) {
+    if (stg) return dsbk::launch_matmul_q8_0_staged(w.blocks, w.rows, w.cols, stg, n_tok, y, residual, sms, st);
+    return run_matmul(w, xq, n_tok, y, residual, sms, pack, st);
+  };
   const int D = s.head_dim, Hq = s.n_q_heads, Hkv = s.n_kv_heads;
   const long long qkv_stride = (long long)(Hq + 2 * Hkv) * D;
   const int max_chunks = (kv0.ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
@@ -972,9 +982,10 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
   for (int l = 0; l < s.n_layers && e == cudaSuccess; ++l) {
     const dsb_layer& Ly = m->layers[l];
     const dsb_layer_trace* tr = trace && trace->layers ? &trace->layers[l] : nullptr;
-    if ((e = dsbk::launch_rmsnorm_quant(h, Ly.attn_norm, n_tok, s.hidden, s.rms_eps, xq, st)) != cudaSuccess) break;
+    if ((e = dsbk::launch_rmsnorm_quant(h, Ly.attn_norm, n_tok, s.hidden, s.rms_eps, xq, st, stg)) != cudaSuccess)
+      break;
     if (tr && !copy_out(tr->x_attn, xq, xh_bytes)) break;
-    if ((e = run_matmul(Ly.wqkv, xq, n_tok, qkv, nullptr, sms, pack, st)) != cudaSuccess) break;
+    if ((e = mm(Ly.wqkv, qkv, nullptr)) != cudaSuccess) break;
     if (tr && !copy_out(tr->qkv, qkv, ntz * qkv_stride * 4)) break;
     if ((e = dsbk::launch_rope_kv_write(qkv, qkv_stride, Hq, Hkv, D, pos_dev, bi_dev, tps, n_tok, Ly.kv.k, Ly.kv.v,
                                         Ly.kv.dtype, Ly.kv.ctx, freqs, st, Ly.q_norm, Ly.k_norm, s.rms_eps)) !=
@@ -983,24 +994,25 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
     if (tr && !copy_out(tr->qkv_rope, qkv, ntz * qkv_stride * 4)) break;
     if ((e = dsbk::launch_attention_decode_multi(qkv, qkv_stride, Hq, Ly.kv.k, Ly.kv.v, Ly.kv.dtype, Hkv, Ly.kv.ctx, D,
                                                  (long long)Ly.kv.full_batch_size * Hkv * Ly.kv.ctx,
-                                                 mv, n_seq, tps, max_items, max_chunks, partials, att, xq, st)) !=
-        cudaSuccess)
+                                                 mv, n_seq, tps, max_items, max_chunks, partials, att, xq, st,
+                                                 dsbk::PagedView{}, stg)) != cudaSuccess)
       break;
     if (tr && !copy_out(tr->att_q8, xq, ntz * ((size_t)Hq * D / 32) * 34)) break;
-    if ((e = run_matmul(Ly.wo, xq, n_tok, h, h, sms, pack, st)) != cudaSuccess) break;
+    if ((e = mm(Ly.wo, h, h)) != cudaSuccess) break;
     if (tr && !copy_out(tr->h_attn, h, h_bytes)) break;
-    if ((e = dsbk::launch_rmsnorm_quant(h, Ly.ffn_norm, n_tok, s.hidden, s.rms_eps, xq, st)) != cudaSuccess) break;
+    if ((e = dsbk::launch_rmsnorm_quant(h, Ly.ffn_norm, n_tok, s.hidden, s.rms_eps, xq, st, stg)) != cudaSuccess)
+      break;
     if (tr && !copy_out(tr->x_ffn, xq, xh_bytes)) break;
-    if ((e = run_matmul(Ly.wgu, xq, n_tok, gu, nullptr, sms, pack, st)) != cudaSuccess) break;
+    if ((e = mm(Ly.wgu, gu, nullptr)) != cudaSuccess) break;
     if (tr && !copy_out(tr->gu, gu, ntz * 2 * (size_t)s.ffn * 4)) break;
-    if ((e = dsbk::launch_silu_mul_quant(gu, n_tok, s.ffn, xq, st)) != cudaSuccess) break;
+    if ((e = dsbk::launch_silu_mul_quant(gu, n_tok, s.ffn, xq, st, stg)) != cudaSuccess) break;
     if (tr && !copy_out(tr->act_q8, xq, ntz * ((size_t)s.ffn / 32) * 34)) break;
-    if ((e = run_matmul(Ly.wdown, xq, n_tok, h, h, sms, pack, st)) != cudaSuccess) break;
+    if ((e = mm(Ly.wdown, h, h)) != cudaSuccess) break;
     if (tr && !copy_out(tr->h_out, h, h_bytes)) break;
   }
-  if (e == cudaSuccess) e = dsbk::launch_rmsnorm_quant(h, m->final_norm, n_tok, s.hidden, s.rms_eps, xq, st);
+  if (e == cudaSuccess) e = dsbk::launch_rmsnorm_quant(h, m->final_norm, n_tok, s.hidden, s.rms_eps, xq, st, stg);
   if (trace) copy_out(trace->x_final, xq, xh_bytes);
-  if (e == cudaSuccess) e = run_matmul(m->head, xq, n_tok, logits, nullptr, sms, pack, st);
+  if (e == cudaSuccess) e = mm(m->head, logits, nullptr);
   dsbk::set_pdl(false);
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "decode step launch");
 }

@@ -79,6 +79,14 @@ cudaError_t launch_matmul_q8_0_fused(int pro, const void* W, int64_t rows, int64
                                      const float* residual, int num_sms, cudaStream_t st);
 unsigned int read_clear_error_matmul_fused();
 size_t matmul_smem_bytes(int64_t rows, int64_t cols, int n_tok, int num_sms);
+// Narrow matmul (n_tok <= 16) whose activations are already in the staged
+// layout of dsb_actlayout.cuh (staged_act_bytes(n_tok, cols / 32) bytes,
+// 256-byte aligned), as the step's q8_0-emitting kernels write it; outputs
+// bitwise those of launch_matmul_q8_0_narrow on the same activations.
+cudaError_t launch_matmul_q8_0_staged(const void* W, int64_t rows, int64_t cols, const void* staged, int n_tok,
+                                      float* y, const float* residual, int num_sms, cudaStream_t st);
+size_t matmul_staged_bytes(int n_tok, int64_t cols);  // staged_act_bytes(n_tok, cols / 32)
+unsigned int read_clear_error_matmul_staged();
 // residual (may alias y, may be NULL): y = residual + W x.
 cudaError_t launch_matmul_q8_0_narrow(const void* W, int64_t rows, int64_t cols, const void* xq, int n_tok, float* y,
                                       const float* residual, int32_t* isum, int num_sms, cudaStream_t st);
@@ -141,7 +149,8 @@ cudaError_t launch_attention_decode_multi(const float* q, long long q_stride, in
                                           const void* vc, int dtype, int n_kv_heads, int ctx, int head_dim,
                                           long long kv_rows, MetaView meta, int n_seq, int tokens_per_seq,
                                           long long max_items, int max_chunks, float* partials, float* out,
-                                          void* xq_out, cudaStream_t st, PagedView pv = PagedView{});
+                                          void* xq_out, cudaStream_t st, PagedView pv = PagedView{},
+                                          void* xq_staged = nullptr);
 // KV write through the paged view: token t of sequence t / T at pos[t].
 cudaError_t launch_kv_scatter_paged(void* kp, void* vp, int dtype, int n_kv_heads, int head_dim, PagedView pv,
                                     int tokens_per_seq, const int32_t* pos_dev, int n_tok, const float* k,
@@ -149,9 +158,11 @@ cudaError_t launch_kv_scatter_paged(void* kp, void* vp, int dtype, int n_kv_head
 
 size_t attention_partial_bytes(int n_tok, int n_q_heads, int head_dim, int ctx);
 
+// staged (optional): also write the narrow matmul's staged layout of the rows.
 cudaError_t launch_rmsnorm_quant(const float* x, const float* w, int n_tok, int hidden, float eps, void* xq,
-                                 cudaStream_t st);
-cudaError_t launch_silu_mul_quant(const float* gu, int n_tok, int ffn, void* xq, cudaStream_t st);
+                                 cudaStream_t st, void* staged = nullptr);
+cudaError_t launch_silu_mul_quant(const float* gu, int n_tok, int ffn, void* xq, cudaStream_t st,
+                                  void* staged = nullptr);
 // tokens: device-readable token ids.  meta_src non-NULL: the kernel also
 // copies n_words words from meta_src (device-readable, e.g. mapped pinned
 // host memory) to meta_dst.

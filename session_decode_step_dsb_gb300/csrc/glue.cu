@@ -14,6 +14,7 @@
 
 #include <cstdint>
 
+#include "dsb_actlayout.cuh"
 #include "dsb_kernels.h"
 #include "dsb_ptx.cuh"
 #include "dsb_q8.cuh"
@@ -25,6 +26,7 @@ namespace {
 constexpr int kGlueThreads = 256;
 
 constexpr int kMaxPerThread = 32;  // hidden <= 8192
+constexpr int kMaxShare = 4;       // values per thread a RMSNorm CTA quantises
 
 // A grid of (token row, split) CTAs.  Thread j holds elements j, j + 256, ...
 // of the row in registers (one memory round trip); the sum of squares goes
@@ -33,9 +35,12 @@ constexpr int kMaxPerThread = 32;  // hidden <= 8192
 // gridDim.y) -- element 32b + lane of block b is exactly the value thread
 // 32w + lane already holds.  Splitting the blocks over CTAs keeps a 16-token
 // step's norm from running on 16 SMs.
+// With staged set, the rows also go to the narrow matmul's staged layout
+// (n_tok = gridDim.x tokens, hidden / 32 blocks).
 __global__ void __launch_bounds__(kGlueThreads) rmsnorm_quant_kernel(const float* __restrict__ x,
                                                                      const float* __restrict__ w, int hidden,
-                                                                     float eps, uint8_t* __restrict__ xq) {
+                                                                     float eps, uint8_t* __restrict__ xq,
+                                                                     uint32_t* __restrict__ staged) {
   __shared__ float part[kGlueThreads / 32];
   pdl_wait();
   pdl_trigger();
@@ -60,21 +65,40 @@ __global__ void __launch_bounds__(kGlueThreads) rmsnorm_quant_kernel(const float
   for (int i = 0; i < kGlueThreads / 32; ++i) tot = __fadd_rn(tot, part[i]);
   const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)hidden), eps)));
   uint8_t* out = xq + (size_t)t * (hidden / 32) * 34;
+  // this CTA's share k0 .. k0 + kper - 1 of the thread's values (kper <=
+  // kMaxShare, as the launch sizes the split): picked out of the register
+  // array by compile-time indices, so the quantise-and-store code below exists
+  // kMaxShare times, not kMaxPerThread times
   const int kper = (n + (int)gridDim.y - 1) / (int)gridDim.y;
-  const int k0 = (int)blockIdx.y * kper, k1 = k0 + kper;
+  const int k0 = (int)blockIdx.y * kper;
+  float mine[kMaxShare];
 #pragma unroll
-  for (int k = 0; k < kMaxPerThread; ++k) {
-    if (k < n && k >= k0 && k < k1) {
+  for (int j = 0; j < kMaxShare; ++j) mine[j] = 0.0f;
+#pragma unroll
+  for (int k = 0; k < kMaxPerThread; ++k)
+#pragma unroll
+    for (int j = 0; j < kMaxShare; ++j)
+      if (k == k0 + j) mine[j] = v[k];
+#pragma unroll
+  for (int j = 0; j < kMaxShare; ++j) {
+    const int k = k0 + j;
+    if (j < kper && k < n) {
       const int e = threadIdx.x + k * kGlueThreads;
       const int b = e >> 5;
-      q8_block_store(__fmul_rn(__fmul_rn(v[k], inv), w[e]), out + (size_t)b * 34, lane);
+      const float y = __fmul_rn(__fmul_rn(mine[j], inv), w[e]);
+      if (staged)
+        q8_block_store_staged(y, out + (size_t)b * 34, staged, hidden / 32, b, t, (int)gridDim.x, lane);
+      else
+        q8_block_store(y, out + (size_t)b * 34, lane);
     }
   }
 }
 
 // gu: [n_tok][2*ffn] = [gate | up]; out: q8_0 [n_tok][ffn].  One warp per block.
+// With staged set, the rows also go to the narrow matmul's staged layout.
 __global__ void __launch_bounds__(kGlueThreads) silu_mul_quant_kernel(const float* __restrict__ gu, int ffn,
-                                                                      long long n_blocks, uint8_t* __restrict__ xq) {
+                                                                      long long n_blocks, uint8_t* __restrict__ xq,
+                                                                      uint32_t* __restrict__ staged, int n_tok) {
   pdl_wait();
   pdl_trigger();
   const long long blk = (long long)blockIdx.x * (kGlueThreads / 32) + (threadIdx.x >> 5);
@@ -86,7 +110,11 @@ __global__ void __launch_bounds__(kGlueThreads) silu_mul_quant_kernel(const floa
   const float g = __ldcg(gu + (size_t)t * 2 * ffn + i);
   const float u = __ldcg(gu + (size_t)t * 2 * ffn + ffn + i);
   const float s = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
-  q8_block_store(__fmul_rn(s, u), xq + (size_t)blk * 34, lane);
+  if (staged)
+    q8_block_store_staged(__fmul_rn(s, u), xq + (size_t)blk * 34, staged, per_row, (int)(blk - t * per_row), (int)t,
+                          n_tok, lane);
+  else
+    q8_block_store(__fmul_rn(s, u), xq + (size_t)blk * 34, lane);
 }
 
 // h[t][:] = dequantised q8_0 row token[t] of the embedding table.  One warp per block.
@@ -173,23 +201,24 @@ cudaError_t launch_embed_params(const void* table, int hidden, int n_tok, float*
 }
 
 cudaError_t launch_rmsnorm_quant(const float* x, const float* w, int n_tok, int hidden, float eps, void* xq,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, void* staged) {
   if (n_tok == 0) return cudaSuccess;
   // about two blocks per warp: hidden / 32 blocks over 8 warps per CTA
   const int n = hidden / kGlueThreads;
   int split = (hidden / 32 + 15) / 16;
   if (split > n) split = n;
+  if (split < (n + kMaxShare - 1) / kMaxShare) split = (n + kMaxShare - 1) / kMaxShare;
   if (split < 1) split = 1;
   return launch_kernel(rmsnorm_quant_kernel, dim3(n_tok, split), dim3(kGlueThreads), 0, st, x, w, hidden, eps,
-                       static_cast<uint8_t*>(xq));
+                       static_cast<uint8_t*>(xq), static_cast<uint32_t*>(staged));
 }
 
-cudaError_t launch_silu_mul_quant(const float* gu, int n_tok, int ffn, void* xq, cudaStream_t st) {
+cudaError_t launch_silu_mul_quant(const float* gu, int n_tok, int ffn, void* xq, cudaStream_t st, void* staged) {
   const long long n_blocks = (long long)n_tok * (ffn / 32);
   if (n_blocks == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((n_blocks + 7) / 8);
   return launch_kernel(silu_mul_quant_kernel, dim3(grid), dim3(kGlueThreads), 0, st, gu, ffn, n_blocks,
-                       static_cast<uint8_t*>(xq));
+                       static_cast<uint8_t*>(xq), static_cast<uint32_t*>(staged), n_tok);
 }
 
 cudaError_t launch_embed(const void* table, int hidden, const int32_t* tokens, int n_tok, float* h,

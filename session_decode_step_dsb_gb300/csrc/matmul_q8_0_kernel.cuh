@@ -12,6 +12,7 @@
 #include <mutex>
 #include <type_traits>
 
+#include "dsb_actlayout.cuh"
 #include "dsb_kernels.h"
 #include "dsb_ptx.cuh"
 
@@ -107,7 +108,9 @@ __device__ __forceinline__ float2 unpack_pair(unsigned long long v) {
 // in rank order (distributed shared memory).  None of this depends on n_tok,
 // so column t of an n_tok = k call is bitwise the n_tok = 1 call.
 //
-// Activation source of a launch.  PRO 0: q8_0 rows xq.  PRO 1: float rows xf
+// Activation source of a launch.  PRO 0: q8_0 rows xq.  PRO 3: the same
+// activations already in the staged layout (written by the kernel that
+// produced them), copied in as they are.  PRO 1: float rows xf
 // (row stride xf_stride) that the kernel RMS-normalises (weight norm_w, eps)
 // and quantises itself; PRO 2: float rows [gate | up] (gate at column c, up at
 // column c + cols) that it turns into silu(gate) * up and quantises.  The
@@ -115,6 +118,7 @@ __device__ __forceinline__ float2 unpack_pair(unsigned long long v) {
 // kernels step by step (the same sum-of-squares order, the same codec), so
 // their codes and scales are bitwise those kernels' output.
 struct ActSrc {
+  const uint32_t* staged = nullptr;  // PRO 3: the activations already in the staged layout
   const uint8_t* xq = nullptr;
   const float* xf = nullptr;
   const float* norm_w = nullptr;
@@ -122,29 +126,15 @@ struct ActSrc {
   int xf_stride = 0;
 };
 
-// From this many tokens on, the k loop runs on the tensor cores (warp-level
+// From kMmaMinNt tokens on, the k loop runs on the tensor cores (warp-level
 // mma.sync m16n8k16, f16 x f16 -> f32) instead of dp4a chains.  A q8_0 block
 // is K = 32, two products: the weight codes enter as the f16 values 1152 + q
 // (exact: integers below 2048), the activation codes as f16 q, and the
 // accumulator starts at -1152 * sum(q_x) of the block, so the result is the
 // exact integer block dot (every partial sum is an integer below 2^24).  The
 // scaling that follows is the dp4a path's, operation for operation, so both
-// paths give bitwise the same outputs.
-constexpr int kMmaMinNt = 8;
-__host__ __device__ constexpr bool use_mma(int nt) { return nt >= kMmaMinNt; }
-
-// Activation row strides: NTA token slots per (block, word) and per block's
-// scales, rounded up to 4 so that four tokens load as one 16-byte word (dp4a
-// path), or to 8, the tensor-core tile width (mma path).
-__host__ __device__ constexpr int act_nta(int nt) { return use_mma(nt) ? (nt + 7) & ~7 : (nt + 3) & ~3; }
-
-// Slot of token t in the row of activation word k.  In the mma layout with 16
-// slots the two 8-token halves trade places in words 2, 3, 6 and 7, so that a
-// warp's fragment loads (word 4h + c of token 8n + g for lane 4g + c) hit 32
-// distinct banks.
-__device__ __forceinline__ int act_pos(int nta, bool mma, int k, int t) {
-  return (mma && nta == 16) ? (t ^ (((k >> 1) & 1) << 3)) : t;
-}
+// paths give bitwise the same outputs.  The activation layout both paths read
+// (use_mma, act_nta, act_pos) is in dsb_actlayout.cuh.
 
 // d = a * b + c for f32 pairs.
 __device__ __forceinline__ unsigned long long fma_pair(unsigned long long a, unsigned long long b,
@@ -286,12 +276,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   int issued = 0;  // units whose copies were requested
-  if (n_units > 0) issue(issued++);  // weights do not depend on the previous kernel
+  // Weights do not depend on the previous kernel.  The second stages hold the
+  // raw activation rows during start-up except when they arrive staged.
+  for (int i = 0; i < (PRO == 3 ? kNStage : 1); ++i)
+    if (issued < n_units) issue(issued++);
   pdl_wait();  // the activations (and y / residual) may be the previous kernel's results
   pdl_trigger();
   bool dead = false;
 
-  if constexpr (PRO == 0) {
+  if constexpr (PRO == 3) {
+    // The CTA's k-range of the staged layout: codes [ks0*8, ks1*8) x 8 x NTA
+    // and their scale words, two bulk copies (sizes multiples of 128 bytes).
+    if (threadIdx.x == 0) {
+      const uint32_t cb = (uint32_t)kr * 8 * 8 * NTA * 4, sb = (uint32_t)kr * 8 * NTA * 4;
+      mbar_arrive_expect_tx(act_bar, cb + sb);
+      bulk_g2s(act_q, src.staged + (size_t)ksr.ks0 * 8 * 8 * NTA, cb, act_bar);
+      bulk_g2s(act_su, src.staged + (size_t)nb * 8 * NTA + (size_t)ksr.ks0 * 8 * NTA, sb, act_bar);
+    }
+    const bool ok = mbar_wait(act_bar, 0u);
+    dead = __syncthreads_or(!ok) != 0;
+    if (dead && threadIdx.x == 0) g_err_matmul = 1u;
+  } else if constexpr (PRO == 0) {
     // Unpack the CTA's activation blocks [ks0*8, ks1*8) x NT into the
     // word-major form.  The rows arrive by one 1-D bulk copy per token (kr *
     // 272 bytes, 16-byte aligned) into the second weight stages, which no copy
@@ -474,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // every thread's reads of the raw rows precede the copies into those stages
   fence_proxy_async_smem();
   __syncthreads();
-  if (!dead && issued < n_units) issue(issued++);
+  while (!dead && issued < n_units && issued < kNStage) issue(issued++);
 
   // Cross-CTA sums: the CTA sum of tile m goes to buffer m & 1 and the CTA
   // arrives on the cluster barrier; it waits, and adds the cluster's sums of
