@@ -484,14 +484,15 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
 }
 
 // Shared memory of the tensor-core kernel (bytes past the 1024-byte aligned
-// base): Ks | Vs [D/64][128][128 B] | Qf [R8][D] f32 (the query rows as
-// copied) | Qh | Ql [R8][D + 8] | Ph | Pl [R8][136] (16-bit; the 16-byte row
-// padding puts the 8 rows of an ldmatrix in distinct banks) | per-warp row
-// max and sum [2][4][R8] f32 | 2 barriers | next item.
+// base): Ks | Vs [D/64][128][128 B] | Qf [R8][D + 8] f32 (the query rows as
+// copied, one bulk copy per row) | Ph | Pl [R8][136] (16-bit) -- the row
+// padding spreads a fragment load's 8 rows over the banks | per-warp row max
+// and sum [2][4][R8] f32 | 2 barriers | two next-item slots.  About 74 KB at
+// D = 128 and 8 rows: three CTAs per SM.
 template <int D, int NRT>
 __host__ __device__ constexpr size_t tc_smem_bytes() {
-  return 1024 + 4 * (size_t)kCh * D + (size_t)(8 * NRT) * D * 4 + 2 * (size_t)(8 * NRT) * (D + 8) * 2 +
-         2 * (size_t)(8 * NRT) * (kCh + 8) * 2 + 2 * (size_t)kWarps * (8 * NRT) * 4 + 2 * 8 + sizeof(Item) + 8;
+  return 1024 + 4 * (size_t)kCh * D + (size_t)(8 * NRT) * (D + 8) * 4 + 2 * (size_t)(8 * NRT) * (kCh + 8) * 2 +
+         2 * (size_t)kWarps * (8 * NRT) * 4 + 2 * 8 + 2 * sizeof(Item) + 8;
 }
 
 template <int D, typename T, int NRT>
@@ -501,8 +502,8 @@ __global__ void __launch_bounds__(kThreads) attention_partial_tc_kernel(
     const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ chunk_off, int n_seq, int tps, int max_chunks,
     float scale, float* __restrict__ partials, const PagedView pv) {
   constexpr int R8 = 8 * NRT;        // query rows, padded to whole 8-row tiles
-  constexpr int QS = D + 8;          // row strides (16-bit elements)
-  constexpr int PS = kCh + 8;
+  constexpr int QF = D + 8;          // query row stride (floats)
+  constexpr int PS = kCh + 8;        // probability row stride (16-bit elements)
   constexpr int MTV = D / kWarps / 16;  // 16-dim tiles of P.V per warp
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int G = n_q_heads / n_kv_heads, R = G * tps;
@@ -512,14 +513,12 @@ __global__ void __launch_bounds__(kThreads) attention_partial_tc_kernel(
   uint8_t* Ks = smem;
   uint8_t* Vs = Ks + (size_t)D * kCh * 2;
   float* Qf = reinterpret_cast<float*>(Vs + (size_t)D * kCh * 2);
-  uint16_t* Qh = reinterpret_cast<uint16_t*>(Qf + R8 * D);
-  uint16_t* Ql = Qh + R8 * QS;
-  uint16_t* Ph = Ql + R8 * QS;
+  uint16_t* Ph = reinterpret_cast<uint16_t*>(Qf + R8 * QF);
   uint16_t* Pl = Ph + R8 * PS;
   float* wmax = reinterpret_cast<float*>(Pl + R8 * PS);  // [warp][R8]
   float* wsum = wmax + kWarps * R8;
   uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(wsum + kWarps * R8) + 7) & ~uintptr_t(7));
-  Item* nx = reinterpret_cast<Item*>(bars + 2);
+  Item* nx2 = reinterpret_cast<Item*>(bars + 2);  // items alternate between two slots
   const uint32_t ks_addr = smem_addr(Ks), vs_addr = smem_addr(Vs);
   if (tid == 0) {
     mbar_init(&bars[0], 1);
@@ -528,49 +527,41 @@ __global__ void __launch_bounds__(kThreads) attention_partial_tc_kernel(
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
   }
-  // the padding query rows R..R8-1 stay zero
-  for (int idx = tid; idx < (R8 - R) * QS; idx += kThreads) {
-    Qh[R * QS + idx] = 0;
-    Ql[R * QS + idx] = 0;
-  }
+  // the padding query rows R..R8-1 stay zero (no copy writes them)
+  for (int idx = tid; idx < (R8 - R) * QF; idx += kThreads) Qf[R * QF + idx] = 0.0f;
   pdl_wait();  // q and the cache rows of this step come from the previous kernels
   pdl_trigger();
 
   const int total_items = chunk_off[n_seq] * n_kv_heads;
-  // Thread 0 requests an item's query rows (one bulk copy of G*D floats per
-  // draft token) and then its K boxes, all on bars[0]: the query rows are
-  // first in line behind no K or V traffic of this CTA.
+  // Thread 0 requests an item's query rows (one bulk copy of D floats per
+  // row, into the padded rows of Qf) and then its K boxes, all on bars[0]:
+  // the query rows are first in line behind no K or V traffic of this CTA.
   auto issue_qk = [&](const Item& x) {
-    const uint32_t qb = (uint32_t)(G * D * 4);
-    mbar_arrive_expect_tx(&bars[0], (uint32_t)tps * qb + tile_bytes<D>(x));
-    for (int j = 0; j < tps; ++j)
-      bulk_g2s(Qf + (size_t)j * G * D, q + (size_t)(x.s * tps + j) * q_stride + (size_t)x.g * G * D, qb, &bars[0]);
+    const uint32_t qb = (uint32_t)(D * 4);
+    mbar_arrive_expect_tx(&bars[0], (uint32_t)R * qb + tile_bytes<D>(x));
+    for (int r = 0; r < R; ++r) {
+      const int j = r / G, gi = r - j * G;
+      bulk_g2s(Qf + (size_t)r * QF, q + (size_t)(x.s * tps + j) * q_stride + (size_t)(x.g * G + gi) * D, qb,
+               &bars[0]);
+    }
     issue_boxes<D>(x, &tmk, Ks, &bars[0]);
   };
   if ((int)blockIdx.x < total_items && tid == 0) {
     const Item first = decode_item(blockIdx.x, n_kv_heads, ctx, batch_index, seq_lens, chunk_off, n_seq, tps, pv);
-    *nx = first;
+    nx2[0] = first;
     issue_qk(first);
     issue_tile<D>(first, &tmv, Vs, &bars[1]);
   }
   __syncthreads();
   uint32_t phase = 0;
-  for (int item = blockIdx.x; item < total_items; item += gridDim.x, phase ^= 1u) {
-    const Item it = *nx;
-    if (!mbar_wait(&bars[0], phase)) g_err_attention = 1u;  // query rows and K
-    __syncwarp();  // ldmatrix and mma.sync below run warp-converged
-    for (int i2 = tid; i2 < R * D / 2; i2 += kThreads) {
-      const float2 v = *reinterpret_cast<const float2*>(Qf + 2 * i2);
-      const int e = 2 * i2, r = e / D, d = e - r * D;
-      uint32_t hi, lo;
-      Tc<T>::split(v.x, v.y, hi, lo);
-      *reinterpret_cast<uint32_t*>(Qh + r * QS + d) = hi;
-      *reinterpret_cast<uint32_t*>(Ql + r * QS + d) = lo;
-    }
-    __syncthreads();
+  for (int item = blockIdx.x, slot = 0; item < total_items; item += gridDim.x, phase ^= 1u, slot ^= 1) {
+    const Item it = nx2[slot];
+    Item* nx = &nx2[slot ^ 1];  // the next item's slot, last read an item ago
     const int next = item + gridDim.x;
     if (tid == 0 && next < total_items)
       *nx = decode_item(next, n_kv_heads, ctx, batch_index, seq_lens, chunk_off, n_seq, tps, pv);
+    if (!mbar_wait(&bars[0], phase)) g_err_attention = 1u;  // query rows and K
+    __syncwarp();  // ldmatrix and mma.sync below run warp-converged
 
     // ---- S^T = K . Q^T: this warp's 32 keys x R8 rows
     float sacc[2][NRT][4];
@@ -590,12 +581,16 @@ __global__ void __launch_bounds__(kThreads) attention_partial_tc_kernel(
           ldsm_x4(a[mt], ks_addr + swz(32 * warp + 16 * mt + (lane & 7) + 8 * (mi & 1), 2 * kq + (mi >> 1)));
 #pragma unroll
         for (int nt = 0; nt < NRT; ++nt) {
-          uint32_t b[4];  // Qh dims +0, +8, Ql dims +0, +8 of rows 8nt..8nt+7
-          ldsm_x4(b, smem_addr((mi >> 1 ? Ql : Qh) + (8 * nt + (lane & 7)) * QS + 16 * kq + 8 * (mi & 1)));
+          // row 8nt + g, dims 16kq + 2c, +1 and 16kq + 8 + 2c, +1: hi and lo parts
+          const float* qr = Qf + (8 * nt + g) * QF + 16 * kq + 2 * c;
+          const float2 q0 = *reinterpret_cast<const float2*>(qr), q1 = *reinterpret_cast<const float2*>(qr + 8);
+          uint32_t h0, l0, h1, l1;
+          Tc<T>::split(q0.x, q0.y, h0, l0);
+          Tc<T>::split(q1.x, q1.y, h1, l1);
 #pragma unroll
           for (int mt = 0; mt < 2; ++mt) {
-            Tc<T>::mma(sacc[mt][nt], a[mt], b[0], b[1]);
-            Tc<T>::mma(sacc[mt][nt], a[mt], b[2], b[3]);
+            Tc<T>::mma(sacc[mt][nt], a[mt], h0, h1);
+            Tc<T>::mma(sacc[mt][nt], a[mt], l0, l1);
           }
         }
       }
@@ -781,8 +776,26 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
   // max = -inf and add exactly nothing
   const int nch = chunk_off[s + 1] - chunk_off[s];
   const float* base = partials + ((size_t)t * n_q_heads + h) * max_chunks * (D + 2);
-  float M = -INFINITY;
-  for (int c = lane; c < nch; c += 32) M = fmaxf(M, __ldcg(base + (size_t)c * (D + 2)));
+  // The first 32 chunks' (m, l) and the first kB chunks' sums are requested
+  // together, before anything depends on them: at decode contexts (<= 32
+  // chunks) the merge then waits for two rounds of loads, not six.
+  constexpr int kB = 16;  // chunks per batch of sum loads
+  float v[kB][D / 32];
+  float m0 = -INFINITY, l0 = 0.0f;
+  if (lane < nch) {
+    const float* pc = base + (size_t)lane * (D + 2);
+    m0 = __ldcg(pc);
+    l0 = __ldcg(pc + 1);
+  }
+#pragma unroll
+  for (int i = 0; i < kB; ++i)
+    if (i < nch) {
+      const float* pc = base + (size_t)i * (D + 2) + 2;
+#pragma unroll
+      for (int e = 0; e < D / 32; ++e) v[i][e] = __ldcg(pc + lane + 32 * e);
+    }
+  float M = m0;
+  for (int c = lane + 32; c < nch; c += 32) M = fmaxf(M, __ldcg(base + (size_t)c * (D + 2)));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float lsum = 0.0f;
@@ -792,25 +805,30 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
   for (int c0 = 0; c0 < nch; c0 += 32) {
     float wl = 0.0f;
     if (c0 + lane < nch) {
-      const float* pc = base + (size_t)(c0 + lane) * (D + 2);
-      const float mc = __ldcg(pc);
+      float mc = m0, lc = l0;
+      if (c0 > 0) {
+        const float* pc = base + (size_t)(c0 + lane) * (D + 2);
+        mc = __ldcg(pc);
+        lc = __ldcg(pc + 1);
+      }
       wl = (mc == -INFINITY) ? 0.0f : expf(mc - M);
-      lsum = __fmaf_rn(wl, __ldcg(pc + 1), lsum);
+      lsum = __fmaf_rn(wl, lc, lsum);
     }
     const int n = min(32, nch - c0);
-    // eight chunks' loads in flight, then their terms added in chunk order
-    for (int cb = 0; cb < n; cb += 8) {
-      float v[8][D / 32];
+    // kB chunks' loads in flight, then their terms added in chunk order
+    for (int cb = 0; cb < n; cb += kB) {
+      if (c0 + cb > 0) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (cb + i < n) {
-          const float* pc = base + (size_t)(c0 + cb + i) * (D + 2) + 2;
+        for (int i = 0; i < kB; ++i) {
+          if (cb + i < n) {
+            const float* pc = base + (size_t)(c0 + cb + i) * (D + 2) + 2;
 #pragma unroll
-          for (int e = 0; e < D / 32; ++e) v[i][e] = __ldcg(pc + lane + 32 * e);
+            for (int e = 0; e < D / 32; ++e) v[i][e] = __ldcg(pc + lane + 32 * e);
+          }
         }
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < kB; ++i) {
         const float wc = __shfl_sync(0xffffffffu, wl, (cb + i) & 31);
         if (cb + i < n) {
 #pragma unroll
