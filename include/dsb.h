@@ -497,6 +497,29 @@ dsb_status dsb_decode_step_trace(const dsb_model* model, const int32_t* token_id
                                  int n_seq, int tokens_per_seq, const int32_t* seq_lens, float* logits,
                                  dsb_workspace* ws, const dsb_step_trace* trace, void* stream);
 
+/* The same step on paged and ring KV ([DS4] the multi-sequence decode
+ * attention commit: per-sequence cache views with ring geometry; [PTO] the
+ * paged attention it serves): layer l's K/V live in the page pool pages[l]
+ * (HOST array [n_layers]; every pool of one n_pages, dtype, n_kv_heads =
+ * shape.n_kv_heads and head_dim = shape.head_dim; the layers' contiguous kv
+ * fields are ignored), addressed through one block geometry for all layers
+ * as in dsb_attention_decode_paged: sequence s's key p sits in page
+ * block_table[s][p / 128] (ring, window[s] > 0: block (p / 128) mod
+ * n_blocks[s]), row p mod 128, and a window W shows draft token j only the
+ * keys (pos_j - W, pos_j].  block_table: host int32[n_seq][max_blocks];
+ * n_blocks, window: host int32[n_seq]; seq_lens as dsb_decode_step (the ring
+ * must hold W + T - 1 keys, a linear table must cover seq_lens[s]).  Two
+ * tokens of the step writing the same page row are rejected.  The workspace
+ * must hold the partials of 128 x (the most chunks a sequence visits) keys
+ * (dsb_step_workspace_bytes with ctx = 128 * (max_blocks + 1) always does).
+ * Same kernels and results as dsb_decode_step on a cache holding the same
+ * keys; DSB_ERR_UNSUPPORTED when the block tables do not fit the staging
+ * slot. */
+dsb_status dsb_decode_step_paged(const dsb_model* model, const dsb_kv_pages* pages, const int32_t* token_ids,
+                                 int n_seq, int tokens_per_seq, const int32_t* seq_lens, const int32_t* block_table,
+                                 int max_blocks, const int32_t* n_blocks, const int32_t* window, float* logits,
+                                 dsb_workspace* ws, void* stream);
+
 /* The same step captured once into a CUDA graph for a fixed (n_seq, T) and
  * replayed.  The step's metadata (token ids, slots, seq_lens and what follows
  * from them) reaches the graph's first kernel, which copies it to the

@@ -31,7 +31,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
-from . import attention, glue, kv, matmul, q8_0, rope
+from . import attention, glue, kv, matmul, paged, q8_0, rope
 
 
 @dataclass(frozen=True)
@@ -59,7 +59,7 @@ def positions(seq_lens, tokens_per_seq: int) -> np.ndarray:
 
 
 def decode_step(shape: Shape, w: dict, k_caches: list, v_caches: list, cache_dtype: str,
-                token_ids, batch_index, tokens_per_seq: int, seq_lens):
+                token_ids, batch_index, tokens_per_seq: int, seq_lens, geometry=None):
     """Returns ``(logits float64 [n_tok, vocab], new k_caches, new v_caches)``.
 
     ``w`` may also hold per-layer float32 ``q_norm[l], k_norm[l]`` (width
@@ -67,6 +67,10 @@ def decode_step(shape: Shape, w: dict, k_caches: list, v_caches: list, cache_dty
     ``w`` holds q8_0 byte arrays ``embed, head`` and per layer ``wqkv[l],
     wo[l], wgu[l], wdown[l]`` plus float32 norm weights ``attn_norm[l],
     ffn_norm[l], final_norm``.  Caches are uint16 bit arrays ``[F, Hkv, C, D]``.
+
+    ``geometry = (block_table, n_blocks, window)``: the caches are page pools
+    ``[n_pages, Hkv, 128, D]`` in the paged / ring geometry of ``paged``
+    (``batch_index`` unused), and the KV write and the attention go through it.
     """
     sh = shape
     pos = positions(seq_lens, tokens_per_seq)
@@ -86,13 +90,20 @@ def decode_step(shape: Shape, w: dict, k_caches: list, v_caches: list, cache_dty
         kn = w["k_norm"][layer] if "k_norm" in w else None
         q = rope.head_rmsnorm_rope(q, pos, sh.theta, qn, sh.eps, sh.yarn)
         k = rope.head_rmsnorm_rope(k, pos, sh.theta, kn, sh.eps, sh.yarn)
-        kc, vc = kv.kv_scatter(k_caches[layer], v_caches[layer], batch_index, tokens_per_seq, pos,
-                               k.astype(np.float32), v.astype(np.float32), cache_dtype)
+        if geometry is None:
+            kc, vc = kv.kv_scatter(k_caches[layer], v_caches[layer], batch_index, tokens_per_seq, pos,
+                                   k.astype(np.float32), v.astype(np.float32), cache_dtype)
+            a = attention.attention_decode_multi(q, kv.bits_to_f64(kc, cache_dtype),
+                                                 kv.bits_to_f64(vc, cache_dtype),
+                                                 batch_index, tokens_per_seq, seq_lens)
+        else:
+            bt, nbk, win = geometry
+            kc, vc = paged.scatter(k_caches[layer], v_caches[layer], bt, nbk, win, tokens_per_seq, pos,
+                                   k.astype(np.float32), v.astype(np.float32), cache_dtype)
+            a = paged.attention_paged(q, kv.bits_to_f64(kc, cache_dtype), kv.bits_to_f64(vc, cache_dtype),
+                                      bt, nbk, win, tokens_per_seq, seq_lens)
         new_k.append(kc)
         new_v.append(vc)
-        a = attention.attention_decode_multi(q, kv.bits_to_f64(kc, cache_dtype),
-                                             kv.bits_to_f64(vc, cache_dtype),
-                                             batch_index, tokens_per_seq, seq_lens)
         h = glue.residual_add(h, matmul.matmul_q8_0(w["wo"][layer], quant(a.reshape(n_tok, hq * d))))
         x = glue.rmsnorm(h, w["ffn_norm"][layer], sh.eps)
         gu = matmul.matmul_q8_0(w["wgu"][layer], quant(x))

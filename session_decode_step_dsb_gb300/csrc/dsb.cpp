@@ -833,7 +833,9 @@ dsb_status check_mat_shape(const dsb_q8_0_mat& m, long long rows, long long cols
 
 // Validates the model description; on success *kv0 is layer 0's cache (all
 // layers share its geometry).
-dsb_status check_model(const dsb_model* m, const dsb_kv_cache** kv0) {
+// need_kv: the layers' contiguous caches are checked (false: the step runs on
+// page pools given apart from the model, and kv0 is left NULL).
+dsb_status check_model(const dsb_model* m, const dsb_kv_cache** kv0, bool need_kv = true) {
   if (!m) return fail(DSB_ERR_INVALID_ARG, "model is NULL");
   const dsb_model_shape& s = m->shape;
   if (s.hidden < 256 || s.n_q_heads < 1 || s.n_kv_heads < 1 || s.head_dim < 2 || s.ffn < 256 || s.vocab < 1 ||
@@ -858,6 +860,7 @@ dsb_status check_model(const dsb_model* m, const dsb_kv_cache** kv0) {
     if ((st = check_mat_shape(L.wgu, 2LL * s.ffn, s.hidden, "wgu", l)) != DSB_OK) return st;
     if ((st = check_mat_shape(L.wdown, s.hidden, s.ffn, "wdown", l)) != DSB_OK) return st;
     if (!L.attn_norm || !L.ffn_norm) return fail(DSB_ERR_INVALID_ARG, "layer %d norm weights are NULL", l);
+    if (!need_kv) continue;
     if ((st = check_kv(&L.kv)) != DSB_OK) return fail(st, "layer %d kv: %s", l, dsb_last_error());
     if (L.kv.n_kv_heads != s.n_kv_heads || L.kv.head_dim != s.head_dim)
       return fail(DSB_ERR_INVALID_ARG, "layer %d kv heads/head_dim do not match the shape", l);
@@ -867,7 +870,7 @@ dsb_status check_model(const dsb_model* m, const dsb_kv_cache** kv0) {
   }
   dsb_status st = check_mat_shape(m->head, s.vocab, s.hidden, "head", -1);
   if (st != DSB_OK) return st;
-  *kv0 = &m->layers[0].kv;
+  *kv0 = need_kv ? &m->layers[0].kv : nullptr;
   return DSB_OK;
 }
 
@@ -928,14 +931,23 @@ cudaError_t run_matmul(const dsb_q8_0_mat& w, const void* xq, int n_tok, float* 
 // meta_src: NULL when the metadata already sits at meta_dev; otherwise a
 // device-readable copy (mapped pinned host memory) that the first kernel
 // copies to meta_dev (n_meta_words words) while it reads the token ids.
+// Page pools of a paged step: every layer's pool (host array) and the block
+// geometry, staged after the positions in the metadata block.
+struct StepPages {
+  const dsb_kv_pages* pages = nullptr;
+  int max_blocks = 0;
+  int max_chunks = 0;  // the most chunks a sequence's attention visits
+};
+
 dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, int tps, long long max_items,
                         float* logits, dsb_workspace* ws, int sms, cudaStream_t st, const int32_t* meta_src = nullptr,
                         size_t n_meta_words = 0, const int32_t* meta_words = nullptr,
-                        dsbk::EmbedParamNode* embed_node = nullptr, const dsb_step_trace* trace = nullptr) {
+                        dsbk::EmbedParamNode* embed_node = nullptr, const dsb_step_trace* trace = nullptr,
+                        const StepPages* pg = nullptr) {
   const dsb_model_shape& s = m->shape;
-  const dsb_kv_cache& kv0 = m->layers[0].kv;
   const int n_tok = n_seq * tps;
-  const StepLayout L = step_layout(s, n_tok, kv0.ctx);
+  const int ctx_cover = pg ? pg->max_chunks * DSB_ATTN_CHUNK : m->layers[0].kv.ctx;
+  const StepLayout L = step_layout(s, n_tok, ctx_cover);
   const int32_t* tokens_dev = meta_dev;
   const int32_t* bi_dev = tokens_dev + n_tok;
   const int32_t* sl_dev = bi_dev + n_seq;
@@ -956,8 +968,15 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
   };
   const int D = s.head_dim, Hq = s.n_q_heads, Hkv = s.n_kv_heads;
   const long long qkv_stride = (long long)(Hq + 2 * Hkv) * D;
-  const int max_chunks = (kv0.ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
+  const int max_chunks = (ctx_cover + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK;
   const dsbk::MetaView mv{bi_dev, sl_dev, co_dev, pos_dev};
+  dsbk::PagedView pv;
+  if (pg) {
+    pv.block_table = pos_dev + n_tok;
+    pv.max_blocks = pg->max_blocks;
+    pv.n_blocks = pv.block_table + (size_t)n_seq * pg->max_blocks;
+    pv.window = pv.n_blocks + n_seq;
+  }
   static thread_local dsbk::RopeFreqs freqs;
   fill_rope_freqs(s.rope, D, &freqs);
   // The first kernel follows the metadata copy; every later kernel may be
@@ -987,15 +1006,20 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
     if (tr && !copy_out(tr->x_attn, xq, xh_bytes)) break;
     if ((e = mm(Ly.wqkv, qkv, nullptr)) != cudaSuccess) break;
     if (tr && !copy_out(tr->qkv, qkv, ntz * qkv_stride * 4)) break;
-    if ((e = dsbk::launch_rope_kv_write(qkv, qkv_stride, Hq, Hkv, D, pos_dev, bi_dev, tps, n_tok, Ly.kv.k, Ly.kv.v,
-                                        Ly.kv.dtype, Ly.kv.ctx, freqs, st, Ly.q_norm, Ly.k_norm, s.rms_eps)) !=
-        cudaSuccess)
+    // this layer's cache: its contiguous cache, or its page pool
+    void* kc = pg ? pg->pages[l].k : Ly.kv.k;
+    void* vc = pg ? pg->pages[l].v : Ly.kv.v;
+    const int kv_dtype = pg ? (int)pg->pages[l].dtype : (int)Ly.kv.dtype;
+    const int kv_ctx = pg ? 0 : Ly.kv.ctx;
+    const long long kv_rows = pg ? (long long)pg->pages[l].n_pages * Hkv * DSB_KV_PAGE
+                                 : (long long)Ly.kv.full_batch_size * Hkv * Ly.kv.ctx;
+    if ((e = dsbk::launch_rope_kv_write(qkv, qkv_stride, Hq, Hkv, D, pos_dev, bi_dev, tps, n_tok, kc, vc, kv_dtype,
+                                        kv_ctx, freqs, st, Ly.q_norm, Ly.k_norm, s.rms_eps, pv)) != cudaSuccess)
       break;
     if (tr && !copy_out(tr->qkv_rope, qkv, ntz * qkv_stride * 4)) break;
-    if ((e = dsbk::launch_attention_decode_multi(qkv, qkv_stride, Hq, Ly.kv.k, Ly.kv.v, Ly.kv.dtype, Hkv, Ly.kv.ctx, D,
-                                                 (long long)Ly.kv.full_batch_size * Hkv * Ly.kv.ctx,
-                                                 mv, n_seq, tps, max_items, max_chunks, partials, att, xq, st,
-                                                 dsbk::PagedView{}, stg)) != cudaSuccess)
+    if ((e = dsbk::launch_attention_decode_multi(qkv, qkv_stride, Hq, kc, vc, kv_dtype, Hkv, kv_ctx, D, kv_rows, mv,
+                                                 n_seq, tps, max_items, max_chunks, partials, att, xq, st, pv, stg)) !=
+        cudaSuccess)
       break;
     if (tr && !copy_out(tr->att_q8, xq, ntz * ((size_t)Hq * D / 32) * 34)) break;
     if ((e = mm(Ly.wo, h, h)) != cudaSuccess) break;
@@ -1017,10 +1041,13 @@ dsb_status enqueue_step(const dsb_model* m, const int32_t* meta_dev, int n_seq, 
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "decode step launch");
 }
 
-dsb_status check_step_resources(const dsb_model* m, int n_tok, float* logits, dsb_workspace* ws, int* sms) {
+// ctx: the cache length the workspace's attention partials must cover (the
+// contiguous caches' ctx; for page pools, 128 x the most chunks a sequence visits).
+dsb_status check_step_resources(const dsb_model* m, int n_tok, float* logits, dsb_workspace* ws, int* sms,
+                                int ctx = -1) {
   if (!logits || !aligned16(logits)) return fail(DSB_ERR_INVALID_ARG, "logits is NULL or not 16-byte aligned");
   if (!ws) return fail(DSB_ERR_WORKSPACE, "workspace is NULL");
-  const StepLayout L = step_layout(m->shape, n_tok, m->layers[0].kv.ctx);
+  const StepLayout L = step_layout(m->shape, n_tok, ctx >= 0 ? ctx : m->layers[0].kv.ctx);
   if (L.total > ws->dev_bytes)
     return fail(DSB_ERR_WORKSPACE, "decode step needs %zu workspace bytes, have %zu", L.total, ws->dev_bytes);
   DeviceInfo di;
@@ -1125,6 +1152,80 @@ dsb_status dsb_decode_step_trace(const dsb_model* model, const int32_t* token_id
   if (st != DSB_OK) return st;
   return enqueue_step(model, dev, n_seq, tokens_per_seq, total * model->shape.n_kv_heads, logits, ws, sms, cs,
                       nullptr, 0, nullptr, nullptr, trace);
+}
+
+dsb_status dsb_decode_step_paged(const dsb_model* model, const dsb_kv_pages* pages, const int32_t* token_ids,
+                                 int n_seq, int tokens_per_seq, const int32_t* seq_lens, const int32_t* block_table,
+                                 int max_blocks, const int32_t* n_blocks, const int32_t* window, float* logits,
+                                 dsb_workspace* ws, void* stream) {
+  const dsb_kv_cache* unused = nullptr;
+  dsb_status st = check_model(model, &unused, false);
+  if (st != DSB_OK) return st;
+  const dsb_model_shape& sh = model->shape;
+  if (!pages) return fail(DSB_ERR_INVALID_ARG, "pages is NULL");
+  for (int l = 0; l < sh.n_layers; ++l) {
+    if ((st = check_pages(&pages[l])) != DSB_OK) return fail(st, "layer %d pages: %s", l, dsb_last_error());
+    if (pages[l].n_kv_heads != sh.n_kv_heads || pages[l].head_dim != sh.head_dim)
+      return fail(DSB_ERR_INVALID_ARG, "layer %d page pool heads/head_dim do not match the shape", l);
+    if (pages[l].n_pages != pages[0].n_pages || pages[l].dtype != pages[0].dtype)
+      return fail(DSB_ERR_INVALID_ARG, "layer %d page pool geometry differs from layer 0", l);
+  }
+  if ((long long)(sh.n_q_heads / sh.n_kv_heads) * tokens_per_seq > 64)
+    return fail(DSB_ERR_UNSUPPORTED, "query rows per kv head (G*T) exceed 64");
+  if (!seq_lens || !token_ids) return fail(DSB_ERR_INVALID_ARG, "token_ids / seq_lens is NULL");
+  st = check_paged_geometry(&pages[0], block_table, max_blocks, n_blocks, window, n_seq, tokens_per_seq, seq_lens);
+  if (st != DSB_OK) return st;
+  const int n_tok = n_seq * tokens_per_seq;
+  for (int t = 0; t < n_tok; ++t)
+    if (token_ids[t] < 0 || token_ids[t] >= sh.vocab)
+      return fail(DSB_ERR_INVALID_ARG, "token_ids[%d]=%d out of [0, vocab=%d)", t, token_ids[t], sh.vocab);
+  // every (page, row) the step writes, once: sequences may share pages
+  std::vector<long long> rows;
+  rows.reserve((size_t)n_tok);
+  for (int s = 0; s < n_seq; ++s)
+    for (int j = 0; j < tokens_per_seq; ++j) {
+      const int p = seq_lens[s] - tokens_per_seq + j;
+      int i = p / DSB_KV_PAGE;
+      if (window[s] > 0) i %= n_blocks[s];
+      rows.push_back((long long)block_table[(size_t)s * max_blocks + i] * DSB_KV_PAGE + p % DSB_KV_PAGE);
+    }
+  std::sort(rows.begin(), rows.end());
+  if (std::adjacent_find(rows.begin(), rows.end()) != rows.end())
+    return fail(DSB_ERR_INVALID_ARG, "two tokens of the step write the same page row");
+  // tokens | batch_index (unused: zeros) | seq_lens | chunk_off | pos | block_table | n_blocks | window
+  std::vector<int32_t> words(token_ids, token_ids + n_tok);
+  words.insert(words.end(), (size_t)n_seq, 0);
+  words.insert(words.end(), seq_lens, seq_lens + n_seq);
+  long long total = 0;
+  int max_chunks = 1;
+  words.push_back(0);
+  for (int s = 0; s < n_seq; ++s) {
+    const int c0 = paged_first_chunk(seq_lens[s], tokens_per_seq, window[s]);
+    const int n = (seq_lens[s] - 1) / DSB_ATTN_CHUNK - c0 + 1;
+    max_chunks = std::max(max_chunks, n);
+    total += n;
+    words.push_back((int32_t)total);
+  }
+  if (total * sh.n_kv_heads > INT_MAX) return fail(DSB_ERR_INVALID_ARG, "too many attention chunks");
+  for (int s = 0; s < n_seq; ++s)
+    for (int j = 0; j < tokens_per_seq; ++j) words.push_back(seq_lens[s] - tokens_per_seq + j);
+  words.insert(words.end(), block_table, block_table + (size_t)n_seq * max_blocks);
+  words.insert(words.end(), n_blocks, n_blocks + n_seq);
+  words.insert(words.end(), window, window + n_seq);
+  if (words.size() > kMetaWords) return fail(DSB_ERR_UNSUPPORTED, "step metadata with block tables exceeds the staging slot");
+  int sms = 0;
+  st = check_step_resources(model, n_tok, logits, ws, &sms, max_chunks * DSB_ATTN_CHUNK);
+  if (st != DSB_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const int32_t* dev = nullptr;
+  st = stage(ws, words, cs, &dev);
+  if (st != DSB_OK) return st;
+  StepPages pg;
+  pg.pages = pages;
+  pg.max_blocks = max_blocks;
+  pg.max_chunks = max_chunks;
+  return enqueue_step(model, dev, n_seq, tokens_per_seq, total * sh.n_kv_heads, logits, ws, sms, cs, nullptr, 0,
+                      nullptr, nullptr, nullptr, &pg);
 }
 
 dsb_status dsb_step_graph_create(const dsb_model* model, int n_seq, int tokens_per_seq, float* logits,

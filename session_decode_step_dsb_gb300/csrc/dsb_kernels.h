@@ -128,7 +128,7 @@ cudaError_t launch_rope_kv_write(float* qkv, long long stride, int n_q_heads, in
                                  const int32_t* pos_dev, const int32_t* batch_index_dev, int tokens_per_seq,
                                  int n_tok, void* kc, void* vc, int dtype, int ctx, const RopeFreqs& freqs,
                                  cudaStream_t st, const float* q_norm = nullptr, const float* k_norm = nullptr,
-                                 float eps = 0.0f);
+                                 float eps = 0.0f, PagedView pv = PagedView{});
 cudaError_t launch_kv_scatter(void* kc, void* vc, int dtype, int n_kv_heads, int ctx, int head_dim,
                               const int32_t* batch_index_dev, int tokens_per_seq, const int32_t* pos_dev, int n_tok,
                               const float* k, const float* v, long long kv_stride, cudaStream_t st);

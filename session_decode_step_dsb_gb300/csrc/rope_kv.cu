@@ -194,7 +194,8 @@ __global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, 
                                      int head_dim, const int32_t* __restrict__ pos,
                                      const int32_t* __restrict__ batch_index, int tokens_per_seq, T* __restrict__ kc,
                                      T* __restrict__ vc, int ctx, const __grid_constant__ RopeFreqs freqs,
-                                     const float* __restrict__ q_norm, const float* __restrict__ k_norm, float eps) {
+                                     const float* __restrict__ q_norm, const float* __restrict__ k_norm, float eps,
+                                     const PagedView pv) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x;
@@ -209,7 +210,21 @@ __global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, 
     s = __fmul_rn(s, freqs.mscale);
   }
   float* row = qkv + (size_t)t * stride;
-  const int slot = batch_index[t / tokens_per_seq];
+  // the cache row of (token t, kv head g) is kv_row + g * kv_head_stride: the
+  // token's slot at position p, or (paged view) row p mod 128 of the page its
+  // block table names (the block index modulo the block count for a ring)
+  const int sq = t / tokens_per_seq;
+  size_t kv_row, kv_head_stride;
+  if (pv.block_table) {
+    int bi = p >> 7;
+    if (pv.window[sq] > 0) bi %= pv.n_blocks[sq];
+    const int page = pv.block_table[(size_t)sq * pv.max_blocks + bi];
+    kv_row = ((size_t)page * n_kv_heads * 128 + (p & 127)) * head_dim;
+    kv_head_stride = (size_t)128 * head_dim;
+  } else {
+    kv_row = ((size_t)batch_index[sq] * n_kv_heads * ctx + p) * head_dim;
+    kv_head_stride = (size_t)ctx * head_dim;
+  }
   const int h0 = blockIdx.y * kRopeHeads;
   float x1[kRopeHeads], x2[kRopeHeads], v1[kRopeHeads], v2[kRopeHeads];
 #pragma unroll
@@ -251,7 +266,7 @@ __global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, 
       dst[i + half] = y2;
     } else {
       const int g = hs - n_q_heads;
-      const size_t dst = (((size_t)slot * n_kv_heads + g) * ctx + p) * head_dim;
+      const size_t dst = kv_row + (size_t)g * kv_head_stride;
       kc[dst + i] = cvt_rn<T>(y1);
       kc[dst + i + half] = cvt_rn<T>(y2);
       vc[dst + i] = cvt_rn<T>(v1[u]);
@@ -306,18 +321,19 @@ cudaError_t launch_kv_scatter_paged(void* kp, void* vp, int dtype, int n_kv_head
 cudaError_t launch_rope_kv_write(float* qkv, long long stride, int n_q_heads, int n_kv_heads, int head_dim,
                                  const int32_t* pos_dev, const int32_t* batch_index_dev, int tokens_per_seq,
                                  int n_tok, void* kc, void* vc, int dtype, int ctx, const RopeFreqs& freqs,
-                                 cudaStream_t st, const float* q_norm, const float* k_norm, float eps) {
+                                 cudaStream_t st, const float* q_norm, const float* k_norm, float eps,
+                                 PagedView pv) {
   if (n_tok == 0) return cudaSuccess;
   const int threads = ((head_dim / 2 + 31) / 32) * 32;
   const dim3 grid((unsigned)n_tok, (unsigned)((n_q_heads + n_kv_heads + kRopeHeads - 1) / kRopeHeads));
   if (dtype == 0)
     return launch_kernel(rope_kv_write_kernel<__half>, grid, dim3(threads), 0, st, qkv, stride, n_q_heads,
                          n_kv_heads, head_dim, pos_dev, batch_index_dev, tokens_per_seq, static_cast<__half*>(kc),
-                         static_cast<__half*>(vc), ctx, freqs, q_norm, k_norm, eps);
+                         static_cast<__half*>(vc), ctx, freqs, q_norm, k_norm, eps, pv);
   return launch_kernel(rope_kv_write_kernel<__nv_bfloat16>, grid, dim3(threads), 0, st, qkv, stride, n_q_heads,
                        n_kv_heads, head_dim, pos_dev, batch_index_dev, tokens_per_seq,
                        static_cast<__nv_bfloat16*>(kc), static_cast<__nv_bfloat16*>(vc), ctx, freqs, q_norm, k_norm,
-                       eps);
+                       eps, pv);
 }
 
 // YaRN (Peng et al. 2023, "YaRN: Efficient Context Window Extension of Large

@@ -564,6 +564,8 @@ SIGNATURES.update({
     "dsb_probe_mma": (_I, [_I, _I, _I, _P, _P]),
     "dsb_step_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(ModelShapeC), _I, _I]),
     "dsb_decode_step": (_I, [ctypes.POINTER(ModelC), _PI32, _PI32, _I, _I, _PI32, _P, _P, _P]),
+    "dsb_decode_step_paged": (_I, [ctypes.POINTER(ModelC), ctypes.POINTER(KVPages), _PI32, _I, _I, _PI32, _PI32, _I,
+                                   _PI32, _PI32, _P, _P, _P]),
     "dsb_decode_step_trace": (_I, [ctypes.POINTER(ModelC), _PI32, _PI32, _I, _I, _PI32, _P, _P,
                                    ctypes.POINTER(StepTraceC), _P]),
     "dsb_step_graph_create": (_I, [ctypes.POINTER(ModelC), _I, _I, _P, _P, _P, ctypes.POINTER(_P)]),
@@ -721,6 +723,27 @@ class DecodeModel:
         sl, psl = _i32(seq_lens, n_seq, "seq_lens")
         _check(lib().dsb_decode_step(ctypes.byref(self.c), ptk, pbi, n_seq, tokens_per_seq, psl, _ptr(logits),
                                      ws.handle, _stream(stream)))
+        return logits
+
+    def step_paged(self, pages, token_ids, tokens_per_seq: int, seq_lens, block_table, n_blocks, window,
+                   ws: Workspace, logits=None, stream=None):
+        """The step on page pools (dsb_decode_step_paged): ``pages`` is one
+        ``KVPages`` per layer (see ``kv_pages``); the block geometry is
+        ``block_table [n_seq][max_blocks]``, ``n_blocks`` and ``window``
+        (host int32, as ``attention_decode_paged``)."""
+        import torch
+        if len(pages) != self.shape.n_layers:
+            raise ValueError(f"pages: one pool per layer ({self.shape.n_layers}), got {len(pages)}")
+        bt, pbt, nb, pnb, win, pwin = _geometry(block_table, n_blocks, window)
+        n_seq = bt.shape[0]
+        if logits is None:
+            logits = torch.empty((n_seq * tokens_per_seq, self.vocab), dtype=torch.float32, device="cuda")
+        _need(logits, 4 * n_seq * tokens_per_seq * self.vocab, "logits", "f32")
+        tk, ptk = _i32(token_ids, n_seq * tokens_per_seq, "token_ids")
+        sl, psl = _i32(seq_lens, n_seq, "seq_lens")
+        arr = (KVPages * len(pages))(*pages)
+        _check(lib().dsb_decode_step_paged(ctypes.byref(self.c), arr, ptk, n_seq, tokens_per_seq, psl, pbt,
+                                           bt.shape[1], pnb, pwin, _ptr(logits), ws.handle, _stream(stream)))
         return logits
 
     def step_trace(self, token_ids, batch_index, tokens_per_seq: int, seq_lens, ws: Workspace, stream=None):

@@ -1,12 +1,15 @@
 """Checks of the oracle's composed decode step (CPU only).
 
-The composition is "parity unpinned" beyond its pinned parts (no printed
-end-to-end value exists); these tests check the invariants the pages state for
-a batched step: each sequence's result is what an independent single-sequence
-run gives (ds4 PR #530, "Correctness"; the two-sessions smoke test in the
-session-split commit), cache slots not named in batch_index are untouched (the
-per-slot frontier guard commit), a T-token draft step equals T one-token steps,
-and only visible history reaches the logits.
+No page prints an end-to-end value, so the composition is pinned by closed
+forms: with some of a layer's matrices zero, whole stages vanish and the step
+reduces to a short formula of the separately pinned pieces (residual
+placement, each stage's norm, the gate / up order, the V slice, the
+write-before-attend order).  The tests also check the invariants the pages
+state for a batched step: each sequence's result is what an independent
+single-sequence run gives (ds4 PR #530, "Correctness"; the two-sessions smoke
+test in the session-split commit), cache slots not named in batch_index are
+untouched (the per-slot frontier guard commit), a T-token draft step equals T
+one-token steps, and only visible history reaches the logits.
 """
 import numpy as np
 
