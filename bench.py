@@ -269,7 +269,8 @@ MATMUL_NTOK = [1, 2, 3, 4, 8, 16]
 def matmul_sweep(flush, stream, peak, iters=5):
     """Narrow q8_0 matmul GB/s on the DeepSeek-class dense-stage shapes at
     every n_tok the method targets (algorithmic bytes: weights once + q8_0
-    activations + float32 outputs)."""
+    activations + float32 outputs): from q8_0 rows (dsb_matmul_q8_0_narrow)
+    and from the staged layout the step's kernels write (staged_*)."""
     import torch
     from session_decode_step_dsb_gb300 import dsb
     out = []
@@ -290,8 +291,14 @@ def matmul_sweep(flush, stream, peak, iters=5):
             med, mean, _ = _time_device(lambda: dsb.matmul_q8_0_narrow(w, rows, cols, xs, nt, y), iters, flush, stream)
             byts = 34 * rows * (cols // 32) + 34 * nt * (cols // 32) + 4 * nt * rows
             gbs = byts / (med * 1e-3) / 1e9
+            # the step's path: the same product from the staged layout
+            stg = dsb.stage_q8_0(w, rows, cols, xs, nt)
+            dsb.matmul_q8_0_staged(w, rows, cols, stg, nt, y)
+            med_s, _, _ = _time_device(lambda: dsb.matmul_q8_0_staged(w, rows, cols, stg, nt, y), iters, flush, stream)
+            gbs_s = byts / (med_s * 1e-3) / 1e9
             out.append({"rows": rows, "cols": cols, "n_tok": nt, "us": round(med * 1e3, 2), "gbs": round(gbs, 1),
-                        "frac": round(gbs / peak, 4)})
+                        "frac": round(gbs / peak, 4), "staged_us": round(med_s * 1e3, 2),
+                        "staged_frac": round(gbs_s / peak, 4)})
         del w, x
     return out
 
@@ -459,14 +466,16 @@ def run_dsb(args):
         seq += [(ms.qkv_rows, ms.hidden, model.w["wqkv"][l]), (ms.hidden, ms.n_q_heads * ms.head_dim, model.w["wo"][l]),
                 (2 * ms.ffn, ms.hidden, model.w["wgu"][l]), (ms.hidden, ms.ffn, model.w["wdown"][l])]
     seq.append((ms.vocab, ms.hidden, model.w["head"]))
+    # the step's matmul path: activations in the staged layout the producing
+    # kernels write (staged once here, outside the timed graph)
     acts = {}
-    for rows, cols, _ in seq:
+    for rows, cols, wmat in seq:
         if (rows, cols) not in acts:
-            acts[(rows, cols)] = (dsb.quantize_q8_0(torch.randn((nt, cols), device=dev)),
-                                  torch.empty((nt, rows), device=dev))
+            xq_ = dsb.quantize_q8_0(torch.randn((nt, cols), device=dev))
+            acts[(rows, cols)] = (dsb.stage_q8_0(wmat, rows, cols, xq_, nt), torch.empty((nt, rows), device=dev))
     for rows, cols, wmat in seq:   # warm every launch's host caches before capture
         x, y = acts[(rows, cols)]
-        dsb.matmul_q8_0_narrow(wmat, rows, cols, x, nt, y)
+        dsb.matmul_q8_0_staged(wmat, rows, cols, x, nt, y)
     torch.cuda.synchronize()
     mm_graph = torch.cuda.CUDAGraph()
     cap_stream = torch.cuda.Stream()
@@ -475,7 +484,7 @@ def run_dsb(args):
         with torch.cuda.graph(mm_graph, stream=cap_stream):
             for rows, cols, wmat in seq:
                 x, y = acts[(rows, cols)]
-                dsb.matmul_q8_0_narrow(wmat, rows, cols, x, nt, y)
+                dsb.matmul_q8_0_staged(wmat, rows, cols, x, nt, y)
     stream.wait_stream(cap_stream)
     torch.cuda.synchronize()
     for _ in range(2):
@@ -487,7 +496,7 @@ def run_dsb(args):
     per_kernel = []
     for rows, cols, wmat in seq[:4] + seq[-1:]:
         x, y = acts[(rows, cols)]
-        m_, mean_, _ = _time_device(lambda: dsb.matmul_q8_0_narrow(wmat, rows, cols, x, nt, y), 10, flush, stream)
+        m_, mean_, _ = _time_device(lambda: dsb.matmul_q8_0_staged(wmat, rows, cols, x, nt, y), 10, flush, stream)
         byts = rows * nbk(cols) + nt * nbk(cols) + 4 * nt * rows
         per_kernel.append({"rows": rows, "cols": cols, "n_tok": nt, "us_alone": round(mean_ * 1e3, 2),
                            "gbs_alone": round(byts / (mean_ * 1e-3) / 1e9, 1)})
@@ -559,7 +568,8 @@ def run_dsb(args):
             "roofline": {"kernel": "matmul_q8_0_narrow_kernel", "bound": "hbm", "achieved": round(achieved, 1),
                          "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "per": f"one step's {len(seq)} matmul launches in step order ({ms.n_layers} layers x 4 + "
-                                f"head, n_tok {nt}), graph-replayed after an L2 flush",
+                                f"head, n_tok {nt}, activations staged as the step's kernels write them), "
+                                f"graph-replayed after an L2 flush",
                          "ms_per_sequence": round(mm_mean, 4), "algorithmic_bytes": int(tot_bytes),
                          "peak_kind": f"{peak_kind} hbm_gbs", "launches_alone": per_kernel},
             "b_sweep": sweep,
@@ -805,6 +815,8 @@ def run_probe(spec: str):
     """A few launches of one kernel at one shape, for a profiler to capture
     (no timing, no JSON line): ``matmul:ROWS:COLS:NTOK[,NTOK...]`` runs the
     narrow matmul three times per n_tok on N(0, 0.02) weights;
+    ``staged:ROWS:COLS:NTOK[,NTOK...]`` the same from the staged layout (the
+    step's matmul path);
     ``wide:ROWS:COLS:NTOK`` the tensor-core matmul three times;
     ``attention:WORKLOAD`` runs the decode attention four times on that
     workload's cache shape (b sequences, seq_lens uniform); ``dp4a`` measures
@@ -824,6 +836,14 @@ def run_probe(spec: str):
             xs = x[:nt].contiguous()
             for _ in range(3):
                 dsb.matmul_q8_0_narrow(w, rows, cols, xs, nt)
+    elif kind == "staged":
+        rows, cols, nts = int(rest[0]), int(rest[1]), [int(v) for v in rest[2].split(",")]
+        w = dsb.quantize_q8_0(torch.randn((rows, cols), generator=g, device="cuda") * 0.02)
+        x = dsb.quantize_q8_0(torch.randn((16, cols), generator=g, device="cuda"))
+        for nt in nts:
+            stg = dsb.stage_q8_0(w, rows, cols, x[:nt].contiguous(), nt)
+            for _ in range(3):
+                dsb.matmul_q8_0_staged(w, rows, cols, stg, nt)
     elif kind == "wide":
         rows, cols, nt = int(rest[0]), int(rest[1]), int(rest[2])
         w = dsb.quantize_q8_0(torch.randn((rows, cols), generator=g, device="cuda") * 0.02)
@@ -951,7 +971,7 @@ def main(argv=None):
                     help="skip the llama-68m-shaped step and the b x K speculative grid")
     ap.add_argument("--probe", default=None,
                     help="run one kernel a few times for a profiler and exit: matmul:ROWS:COLS:NTOK[,..], "
-                         "wide:ROWS:COLS:NTOK, attention:WORKLOAD, dp4a (the dp4a rate / latency probe) "
+                         "staged:ROWS:COLS:NTOKS, wide:ROWS:COLS:NTOK, attention:WORKLOAD, dp4a (the dp4a rate / latency probe) "
                          "or mma (the mma.sync rate probe)")
     args = ap.parse_args(argv)
     if args.probe:

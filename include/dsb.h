@@ -163,6 +163,28 @@ dsb_status dsb_matmul_q8_0(const dsb_q8_0_mat* w, const void* xq, int n_tok, flo
 dsb_status dsb_matmul_q8_0_block_dots(const dsb_q8_0_mat* w, const void* xq, int n_tok,
                                       int32_t* isum, void* stream);
 
+/* The narrow product from activations already in a staged layout: the path
+ * the decode step takes, where the kernel that produces the q8_0 activations
+ * writes this layout too ([DS4] "Why it's worth it -- the narrow-batch
+ * matmul": each weight block crosses HBM once for every token).
+ * dsb_stage_q8_0 writes the staged layout of xq (device q8_0 [n_tok][cols/32])
+ * that the narrow kernel reads at n_tok tokens: per block and 4-code word the
+ * words of every token side by side, then the scales (with the blocks' code
+ * sums from 8 tokens on); dsb_matmul_q8_0_staged computes y (device float32
+ * [n_tok][rows], 16-byte aligned) from it, bitwise equal to
+ * dsb_matmul_q8_0_narrow on xq.
+ * staged: device, 16-byte aligned, at least dsb_matmul_q8_0_staged_bytes(
+ * n_tok, cols) bytes, owned by the caller; its contents are only meaningful
+ * to the staged matmul at the same cols and n_tok.  n_tok in [1, 16]
+ * (DSB_ERR_INVALID_ARG otherwise); a short or unaligned staged buffer is
+ * DSB_ERR_WORKSPACE; cols % 256 != 0 is DSB_ERR_UNSUPPORTED.
+ * dsb_matmul_q8_0_staged_bytes is 0 for arguments out of range. */
+size_t dsb_matmul_q8_0_staged_bytes(int n_tok, int64_t cols);
+dsb_status dsb_stage_q8_0(const dsb_q8_0_mat* w, const void* xq, int n_tok, void* staged, size_t staged_bytes,
+                          void* stream);
+dsb_status dsb_matmul_q8_0_staged(const dsb_q8_0_mat* w, const void* staged, size_t staged_bytes, int n_tok, float* y,
+                                  void* stream);
+
 /* Scratch bytes dsb_matmul_q8_0_wide needs: the token operands packed for the
  * tensor cores, ceil(n_tok/128) * cols/32 * 16384 bytes.  0 if n_tok is out
  * of [1, DSB_MAX_TOKENS] or cols is not a positive multiple of 256. */

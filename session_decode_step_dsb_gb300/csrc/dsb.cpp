@@ -329,6 +329,50 @@ dsb_status dsb_matmul_q8_0_block_dots(const dsb_q8_0_mat* w, const void* xq, int
   return matmul_common(w, xq, n_tok, nullptr, isum, stream, true);
 }
 
+size_t dsb_matmul_q8_0_staged_bytes(int n_tok, int64_t cols) {
+  if (n_tok < 1 || n_tok > DSB_NARROW_MAX || cols < 256 || cols % 256) return 0;
+  return dsbk::matmul_staged_bytes(n_tok, cols);
+}
+
+static dsb_status staged_common(const dsb_q8_0_mat* w, int n_tok, const void* staged, size_t staged_bytes,
+                                DeviceInfo* di) {
+  dsb_status st = check_mat(w);
+  if (st != DSB_OK) return st;
+  if (n_tok < 1 || n_tok > DSB_NARROW_MAX)
+    return fail(DSB_ERR_INVALID_ARG, "n_tok=%d out of [1, %d]", n_tok, DSB_NARROW_MAX);
+  const size_t need = dsbk::matmul_staged_bytes(n_tok, w->cols);
+  if (!staged || !aligned16(staged)) return fail(DSB_ERR_WORKSPACE, "staged is NULL or not 16-byte aligned");
+  if (staged_bytes < need) return fail(DSB_ERR_WORKSPACE, "staged has %zu bytes, needs %zu", staged_bytes, need);
+  st = device_info(di);
+  if (st != DSB_OK) return st;
+  const size_t smem = dsbk::matmul_smem_bytes(w->rows, w->cols, n_tok, di->sms);
+  if (smem > (size_t)di->max_smem_optin)
+    return fail(DSB_ERR_UNSUPPORTED, "matmul %lldx%lld needs %zu bytes of shared memory (max %d)", (long long)w->rows,
+                (long long)w->cols, smem, di->max_smem_optin);
+  return DSB_OK;
+}
+
+dsb_status dsb_stage_q8_0(const dsb_q8_0_mat* w, const void* xq, int n_tok, void* staged, size_t staged_bytes,
+                          void* stream) {
+  DeviceInfo di;
+  dsb_status st = staged_common(w, n_tok, staged, staged_bytes, &di);
+  if (st != DSB_OK) return st;
+  if (!xq || !aligned16(xq)) return fail(DSB_ERR_INVALID_ARG, "xq is NULL or not 16-byte aligned");
+  cudaError_t e = dsbk::launch_stage_q8_0(xq, n_tok, w->cols, staged, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSB_OK : cuda_fail(e, "stage_q8_0 launch");
+}
+
+dsb_status dsb_matmul_q8_0_staged(const dsb_q8_0_mat* w, const void* staged, size_t staged_bytes, int n_tok, float* y,
+                                  void* stream) {
+  DeviceInfo di;
+  dsb_status st = staged_common(w, n_tok, staged, staged_bytes, &di);
+  if (st != DSB_OK) return st;
+  if (!y || !aligned16(y)) return fail(DSB_ERR_INVALID_ARG, "y is NULL or not 16-byte aligned");
+  cudaError_t e = dsbk::launch_matmul_q8_0_staged(w->blocks, w->rows, w->cols, staged, n_tok, y, nullptr, di.sms,
+                                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? DSB_OK : cuda_fail(e, "matmul_q8_0_staged launch");
+}
+
 size_t dsb_matmul_q8_0_wide_scratch_bytes(int n_tok, int64_t cols) {
   if (n_tok < 1 || n_tok > DSB_MAX_TOKENS || cols < 256 || cols % 256) return 0;
   return dsbk::matmul_tc_scratch_bytes(n_tok, cols);

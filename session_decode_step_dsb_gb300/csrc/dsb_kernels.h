@@ -80,12 +80,14 @@ cudaError_t launch_matmul_q8_0_fused(int pro, const void* W, int64_t rows, int64
 unsigned int read_clear_error_matmul_fused();
 size_t matmul_smem_bytes(int64_t rows, int64_t cols, int n_tok, int num_sms);
 // Narrow matmul (n_tok <= 16) whose activations are already in the staged
-// layout of dsb_actlayout.cuh (staged_act_bytes(n_tok, cols / 32) bytes,
+// layout of dsb_actlayout.cuh (matmul_staged_bytes(n_tok, cols) bytes,
 // 256-byte aligned), as the step's q8_0-emitting kernels write it; outputs
 // bitwise those of launch_matmul_q8_0_narrow on the same activations.
 cudaError_t launch_matmul_q8_0_staged(const void* W, int64_t rows, int64_t cols, const void* staged, int n_tok,
                                       float* y, const float* residual, int num_sms, cudaStream_t st);
 size_t matmul_staged_bytes(int n_tok, int64_t cols);  // staged_act_bytes(n_tok, cols / 32)
+// q8_0 rows xq [n_tok][cols/32] into the staged layout.
+cudaError_t launch_stage_q8_0(const void* xq, int n_tok, int64_t cols, void* staged, cudaStream_t st);
 unsigned int read_clear_error_matmul_staged();
 // residual (may alias y, may be NULL): y = residual + W x.
 cudaError_t launch_matmul_q8_0_narrow(const void* W, int64_t rows, int64_t cols, const void* xq, int n_tok, float* y,

@@ -19,6 +19,7 @@ import numpy as np
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libdsb.so")
 
 DSB_OK = 0
+DSB_ERR_INVALID_ARG = 1
 DSB_ERR_UNSUPPORTED = 2
 STATUS_NAMES = {0: "DSB_OK", 1: "DSB_ERR_INVALID_ARG", 2: "DSB_ERR_UNSUPPORTED", 3: "DSB_ERR_WORKSPACE",
                 4: "DSB_ERR_CUDA", 5: "DSB_ERR_TIMEOUT", 6: "DSB_ERR_DEVICE"}
@@ -94,6 +95,9 @@ SIGNATURES = {
     "dsb_matmul_q8_0_narrow": (_I, [ctypes.POINTER(Q8Mat), _P, _I, _P, _P]),
     "dsb_matmul_q8_0": (_I, [ctypes.POINTER(Q8Mat), _P, _I, _P, _P]),
     "dsb_matmul_q8_0_block_dots": (_I, [ctypes.POINTER(Q8Mat), _P, _I, _P, _P]),
+    "dsb_matmul_q8_0_staged_bytes": (ctypes.c_size_t, [_I, _I64]),
+    "dsb_stage_q8_0": (_I, [ctypes.POINTER(Q8Mat), _P, _I, _P, ctypes.c_size_t, _P]),
+    "dsb_matmul_q8_0_staged": (_I, [ctypes.POINTER(Q8Mat), _P, ctypes.c_size_t, _I, _P, _P]),
     "dsb_matmul_q8_0_wide_scratch_bytes": (ctypes.c_size_t, [_I, _I64]),
     "dsb_matmul_q8_0_wide": (_I, [ctypes.POINTER(Q8Mat), _P, _I, _P, _P, ctypes.c_size_t, _P]),
     "dsb_rope_posvec": (_I, [_P, _I, _P, _I, _I, _I, _PI32, _F, _P, _P]),
@@ -277,6 +281,36 @@ def matmul_q8_0_block_dots(w_blocks, rows: int, cols: int, xq, n_tok: int, strea
     m = _mat(w_blocks, rows, cols)
     _check(lib().dsb_matmul_q8_0_block_dots(ctypes.byref(m), _ptr(xq), n_tok, _ptr(isum), _stream(stream)))
     return isum
+
+
+def stage_q8_0(w_blocks, rows: int, cols: int, xq, n_tok: int, staged=None, stream=None):
+    """The staged activation layout of ``xq`` that the narrow kernel reads at
+    ``n_tok`` tokens (uint8 device tensor, allocated when not given)."""
+    import torch
+    nbytes = lib().dsb_matmul_q8_0_staged_bytes(n_tok, cols)
+    if nbytes == 0:
+        raise DsbError(DSB_ERR_INVALID_ARG, f"no staged layout for n_tok={n_tok}, cols={cols}")
+    if staged is None:
+        staged = torch.empty(nbytes, dtype=torch.uint8, device=w_blocks.device)
+    _need(xq, n_tok * q8_rows_bytes(cols), "xq", "u8")
+    _need(staged, nbytes, "staged", "u8")
+    m = _mat(w_blocks, rows, cols)
+    _check(lib().dsb_stage_q8_0(ctypes.byref(m), _ptr(xq), n_tok, _ptr(staged), staged.numel(), _stream(stream)))
+    return staged
+
+
+def matmul_q8_0_staged(w_blocks, rows: int, cols: int, staged, n_tok: int, y=None, stream=None):
+    """``y[n_tok, rows]`` from activations staged by :func:`stage_q8_0` (the
+    decode step's matmul path); bitwise :func:`matmul_q8_0_narrow`."""
+    import torch
+    if y is None:
+        y = torch.empty((n_tok, rows), dtype=torch.float32, device=w_blocks.device)
+    _need(y, 4 * n_tok * rows, "y", "f32")
+    _need(staged, 0, "staged", "u8")
+    m = _mat(w_blocks, rows, cols)
+    _check(lib().dsb_matmul_q8_0_staged(ctypes.byref(m), _ptr(staged), staged.numel(), n_tok, _ptr(y),
+                                        _stream(stream)))
+    return y
 
 
 def _wide_scratch(n_tok: int, cols: int, device):
