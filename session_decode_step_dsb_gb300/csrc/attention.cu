@@ -778,8 +778,8 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
   const float* base = partials + ((size_t)t * n_q_heads + h) * max_chunks * (D + 2);
   // The first 32 chunks' (m, l) and the first kB chunks' sums are requested
   // together, before anything depends on them: at decode contexts (<= 32
-  // chunks) the merge then waits for two rounds of loads, not six.
-  constexpr int kB = 16;  // chunks per batch of sum loads
+  // chunks, 4096 keys) the merge then waits for one round of loads.
+  constexpr int kB = 32;  // chunks per batch of sum loads
   float v[kB][D / 32];
   float m0 = -INFINITY, l0 = 0.0f;
   if (lane < nch) {
