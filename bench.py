@@ -266,11 +266,13 @@ MATMUL_SHAPES = [(7168, 7168), (18432, 7168), (129280, 7168)]
 MATMUL_NTOK = [1, 2, 3, 4, 8, 16]
 
 
-def matmul_sweep(flush, stream, peak, iters=5):
+def matmul_sweep(flush, stream, peak, iters=15):
     """Narrow q8_0 matmul GB/s on the DeepSeek-class dense-stage shapes at
     every n_tok the method targets (algorithmic bytes: weights once + q8_0
     activations + float32 outputs): from q8_0 rows (dsb_matmul_q8_0_narrow)
-    and from the staged layout the step's kernels write (staged_*)."""
+    and from the staged layout the step's kernels write (staged_*).  Mean of
+    the launches: the event clock here ticks in 2.048 us steps, and the mean
+    over launches that start at random phases of it resolves below a tick."""
     import torch
     from session_decode_step_dsb_gb300 import dsb
     out = []
@@ -288,16 +290,16 @@ def matmul_sweep(flush, stream, peak, iters=5):
             y = torch.empty((nt, rows), device="cuda")
             for _ in range(2):
                 dsb.matmul_q8_0_narrow(w, rows, cols, xs, nt, y)
-            med, mean, _ = _time_device(lambda: dsb.matmul_q8_0_narrow(w, rows, cols, xs, nt, y), iters, flush, stream)
+            _, t_row, _ = _time_device(lambda: dsb.matmul_q8_0_narrow(w, rows, cols, xs, nt, y), iters, flush, stream)
             byts = 34 * rows * (cols // 32) + 34 * nt * (cols // 32) + 4 * nt * rows
-            gbs = byts / (med * 1e-3) / 1e9
+            gbs = byts / (t_row * 1e-3) / 1e9
             # the step's path: the same product from the staged layout
             stg = dsb.stage_q8_0(w, rows, cols, xs, nt)
             dsb.matmul_q8_0_staged(w, rows, cols, stg, nt, y)
-            med_s, _, _ = _time_device(lambda: dsb.matmul_q8_0_staged(w, rows, cols, stg, nt, y), iters, flush, stream)
-            gbs_s = byts / (med_s * 1e-3) / 1e9
-            out.append({"rows": rows, "cols": cols, "n_tok": nt, "us": round(med * 1e3, 2), "gbs": round(gbs, 1),
-                        "frac": round(gbs / peak, 4), "staged_us": round(med_s * 1e3, 2),
+            _, t_stg, _ = _time_device(lambda: dsb.matmul_q8_0_staged(w, rows, cols, stg, nt, y), iters, flush, stream)
+            gbs_s = byts / (t_stg * 1e-3) / 1e9
+            out.append({"rows": rows, "cols": cols, "n_tok": nt, "us": round(t_row * 1e3, 2), "gbs": round(gbs, 1),
+                        "frac": round(gbs / peak, 4), "staged_us": round(t_stg * 1e3, 2),
                         "staged_frac": round(gbs_s / peak, 4)})
         del w, x
     return out
