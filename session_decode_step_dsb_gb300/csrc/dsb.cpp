@@ -354,20 +354,20 @@ static dsb_status staged_common(const dsb_q8_0_mat* w, int n_tok, const void* st
 
 dsb_status dsb_stage_q8_0(const dsb_q8_0_mat* w, const void* xq, int n_tok, void* staged, size_t staged_bytes,
                           void* stream) {
+  if (!xq || !aligned16(xq)) return fail(DSB_ERR_INVALID_ARG, "xq is NULL or not 16-byte aligned");
   DeviceInfo di;
   dsb_status st = staged_common(w, n_tok, staged, staged_bytes, &di);
   if (st != DSB_OK) return st;
-  if (!xq || !aligned16(xq)) return fail(DSB_ERR_INVALID_ARG, "xq is NULL or not 16-byte aligned");
   cudaError_t e = dsbk::launch_stage_q8_0(xq, n_tok, w->cols, staged, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "stage_q8_0 launch");
 }
 
 dsb_status dsb_matmul_q8_0_staged(const dsb_q8_0_mat* w, const void* staged, size_t staged_bytes, int n_tok, float* y,
                                   void* stream) {
+  if (!y || !aligned16(y)) return fail(DSB_ERR_INVALID_ARG, "y is NULL or not 16-byte aligned");
   DeviceInfo di;
   dsb_status st = staged_common(w, n_tok, staged, staged_bytes, &di);
   if (st != DSB_OK) return st;
-  if (!y || !aligned16(y)) return fail(DSB_ERR_INVALID_ARG, "y is NULL or not 16-byte aligned");
   cudaError_t e = dsbk::launch_matmul_q8_0_staged(w->blocks, w->rows, w->cols, staged, n_tok, y, nullptr, di.sms,
                                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DSB_OK : cuda_fail(e, "matmul_q8_0_staged launch");

@@ -86,6 +86,34 @@ def test_fused_matmul_rejects_bad_arguments(lib):
     assert lib.dsb_silu_matmul_q8_0(ctypes.byref(m96), fake, 2, fake, None) == 2  # cols % 256
 
 
+def test_staged_matmul_rejects_bad_arguments(lib):
+    """The staged-layout entry points (the step's matmul path as an op) check
+    the matrix, the token count and the staged buffer's size and alignment on
+    the host before any device work."""
+    from session_decode_step_dsb_gb300 import dsb
+    fake = ctypes.c_void_p(1 << 20)
+    m = dsb.Q8Mat(fake, 64, 1024)
+    need = lib.dsb_matmul_q8_0_staged_bytes(16, 1024)
+    assert need == 1024 // 32 * 36 * 16  # 32 blocks x (8 code words + 1 scale word) x 16 token slots
+    assert lib.dsb_matmul_q8_0_staged_bytes(3, 1024) == 1024 // 32 * 36 * 4
+    assert lib.dsb_matmul_q8_0_staged_bytes(9, 1024) == 1024 // 32 * 36 * 16
+    for nt, cols in [(0, 1024), (17, 1024), (16, 100), (16, 0)]:
+        assert lib.dsb_matmul_q8_0_staged_bytes(nt, cols) == 0
+    assert lib.dsb_stage_q8_0(ctypes.byref(m), fake, 0, fake, need, None) == 1
+    assert "n_tok" in _err(lib)
+    assert lib.dsb_stage_q8_0(ctypes.byref(m), fake, 17, fake, need, None) == 1
+    assert lib.dsb_stage_q8_0(ctypes.byref(m), None, 16, fake, need, None) == 1
+    assert lib.dsb_stage_q8_0(ctypes.byref(m), fake, 16, None, need, None) == 3
+    assert lib.dsb_stage_q8_0(ctypes.byref(m), fake, 16, fake, need - 16, None) == 3
+    assert "staged" in _err(lib)
+    assert lib.dsb_stage_q8_0(ctypes.byref(m), fake, 16, ctypes.c_void_p((1 << 20) + 8), need, None) == 3
+    assert lib.dsb_matmul_q8_0_staged(ctypes.byref(m), fake, need, 16, None, None) == 1
+    assert lib.dsb_matmul_q8_0_staged(ctypes.byref(m), fake, need - 16, 16, fake, None) == 3
+    assert lib.dsb_matmul_q8_0_staged(ctypes.byref(m), fake, need, 0, fake, None) == 1
+    m96 = dsb.Q8Mat(fake, 64, 96)
+    assert lib.dsb_matmul_q8_0_staged(ctypes.byref(m96), fake, need, 16, fake, None) == 2  # cols % 256
+
+
 def test_quantize_rejects_bad_arguments(lib):
     fake = ctypes.c_void_p(1 << 20)
     assert lib.dsb_quantize_q8_0(fake, 4, 33, fake, None) == 1
