@@ -754,21 +754,22 @@ __global__ void __launch_bounds__(kThreads) attention_partial_tc_kernel(
   }  // work items
 }
 
-// One warp per (token row, query head).  Lanes first take the chunks 32 at a
-// time (max of m_c, then w_c = exp(m_c - M) and the partial sum of w_c l_c);
-// the sums over lanes use a fixed xor tree; then the warp walks the chunks in
-// order, lane d accumulating w_c * acc_c[d].  With QOUT the normalised row is
-// q8_0-quantised (D / 32 blocks per head) straight into xq.
+// One CTA per (token row, query head), one warp per 32 dimensions of the head
+// (warp q owns dims 32q .. 32q + 31, one q8_0 block).  Every warp first takes
+// the chunks' (m, l) 32 at a time (max of m_c, then w_c = exp(m_c - M) and
+// the partial sum of w_c l_c; the sums over lanes use a fixed xor tree), then
+// walks the chunks in order, lane d accumulating w_c * acc_c[32q + d].  With
+// QOUT the normalised block is q8_0-quantised straight into xq.
 template <int D, bool QOUT>
-__global__ void __launch_bounds__(128) attention_merge_kernel(const float* __restrict__ partials, int n_q_heads,
-                                                              int tps, const int32_t* __restrict__ chunk_off,
-                                                              int max_chunks, int n_tok, float* __restrict__ out,
-                                                              uint8_t* __restrict__ xq,
-                                                              uint32_t* __restrict__ xq_staged) {
+__global__ void __launch_bounds__(D) attention_merge_kernel(const float* __restrict__ partials, int n_q_heads,
+                                                            int tps, const int32_t* __restrict__ chunk_off,
+                                                            int max_chunks, int n_tok, float* __restrict__ out,
+                                                            uint8_t* __restrict__ xq,
+                                                            uint32_t* __restrict__ xq_staged) {
   pdl_wait();
   pdl_trigger();
-  const int wg = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  const int wg = blockIdx.x;
+  const int qd = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (wg >= n_tok * n_q_heads) return;
   const int t = wg / n_q_heads, h = wg - t * n_q_heads;
   const int s = t / tps;
@@ -776,11 +777,12 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
   // max = -inf and add exactly nothing
   const int nch = chunk_off[s + 1] - chunk_off[s];
   const float* base = partials + ((size_t)t * n_q_heads + h) * max_chunks * (D + 2);
-  // The first 32 chunks' (m, l) and the first kB chunks' sums are requested
-  // together, before anything depends on them: at decode contexts (<= 32
-  // chunks, 4096 keys) the merge then waits for one round of loads.
+  const int dim = 32 * qd + lane;
+  // The first 32 chunks' (m, l) and their sums are requested together,
+  // before anything depends on them: at decode contexts (<= 32 chunks, 4096
+  // keys) the merge waits for one round of loads.
   constexpr int kB = 32;  // chunks per batch of sum loads
-  float v[kB][D / 32];
+  float v[kB];
   float m0 = -INFINITY, l0 = 0.0f;
   if (lane < nch) {
     const float* pc = base + (size_t)lane * (D + 2);
@@ -789,19 +791,12 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
   }
 #pragma unroll
   for (int i = 0; i < kB; ++i)
-    if (i < nch) {
-      const float* pc = base + (size_t)i * (D + 2) + 2;
-#pragma unroll
-      for (int e = 0; e < D / 32; ++e) v[i][e] = __ldcg(pc + lane + 32 * e);
-    }
+    if (i < nch) v[i] = __ldcg(base + (size_t)i * (D + 2) + 2 + dim);
   float M = m0;
   for (int c = lane + 32; c < nch; c += 32) M = fmaxf(M, __ldcg(base + (size_t)c * (D + 2)));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float lsum = 0.0f;
-  float acc[D / 32];
-#pragma unroll
-  for (int e = 0; e < D / 32; ++e) acc[e] = 0.0f;
+  float lsum = 0.0f, acc = 0.0f;
   for (int c0 = 0; c0 < nch; c0 += 32) {
     float wl = 0.0f;
     if (c0 + lane < nch) {
@@ -819,40 +814,27 @@ __global__ void __launch_bounds__(128) attention_merge_kernel(const float* __res
     for (int cb = 0; cb < n; cb += kB) {
       if (c0 + cb > 0) {
 #pragma unroll
-        for (int i = 0; i < kB; ++i) {
-          if (cb + i < n) {
-            const float* pc = base + (size_t)(c0 + cb + i) * (D + 2) + 2;
-#pragma unroll
-            for (int e = 0; e < D / 32; ++e) v[i][e] = __ldcg(pc + lane + 32 * e);
-          }
-        }
+        for (int i = 0; i < kB; ++i)
+          if (cb + i < n) v[i] = __ldcg(base + (size_t)(c0 + cb + i) * (D + 2) + 2 + dim);
       }
 #pragma unroll
       for (int i = 0; i < kB; ++i) {
         const float wc = __shfl_sync(0xffffffffu, wl, (cb + i) & 31);
-        if (cb + i < n) {
-#pragma unroll
-          for (int e = 0; e < D / 32; ++e) acc[e] = __fmaf_rn(wc, v[i][e], acc[e]);
-        }
+        if (cb + i < n) acc = __fmaf_rn(wc, v[i], acc);
       }
     }
   }
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) lsum = __fadd_rn(lsum, __shfl_xor_sync(0xffffffffu, lsum, o));
   if constexpr (QOUT) {
-    uint8_t* dst = xq + ((size_t)t * n_q_heads + h) * (D / 32) * 34;
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e) {
-      if (xq_staged)
-        q8_block_store_staged(__fdiv_rn(acc[e], lsum), dst + (size_t)e * 34, xq_staged,
-                              (long long)n_q_heads * (D / 32), h * (D / 32) + e, t, n_tok, lane);
-      else
-        q8_block_store(__fdiv_rn(acc[e], lsum), dst + (size_t)e * 34, lane);
-    }
+    uint8_t* dst = xq + (((size_t)t * n_q_heads + h) * (D / 32) + qd) * 34;
+    if (xq_staged)
+      q8_block_store_staged(__fdiv_rn(acc, lsum), dst, xq_staged, (long long)n_q_heads * (D / 32),
+                            h * (D / 32) + qd, t, n_tok, lane);
+    else
+      q8_block_store(__fdiv_rn(acc, lsum), dst, lane);
   } else {
-    float* o = out + ((size_t)t * n_q_heads + h) * D;
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e) o[lane + 32 * e] = __fdiv_rn(acc[e], lsum);
+    out[((size_t)t * n_q_heads + h) * D + dim] = __fdiv_rn(acc, lsum);
   }
 }
 
@@ -957,12 +939,12 @@ cudaError_t launch_partial_merge(Kern kern, size_t smem, const float* q, long lo
                     meta.batch_index, meta.seq_lens, meta.chunk_off, n_seq, tps, max_chunks, scale, partials, pv);
   if (e != cudaSuccess) return e;
   const int n_tok = n_seq * tps;
-  const unsigned mgrid = (unsigned)((n_tok * n_q_heads + 3) / 4);
+  const unsigned mgrid = (unsigned)(n_tok * n_q_heads);
   if (xq_out)
-    return launch_kernel(attention_merge_kernel<D, true>, dim3(mgrid), dim3(128), 0, st, partials, n_q_heads, tps,
+    return launch_kernel(attention_merge_kernel<D, true>, dim3(mgrid), dim3(D), 0, st, partials, n_q_heads, tps,
                          meta.chunk_off, max_chunks, n_tok, out, static_cast<uint8_t*>(xq_out),
                          static_cast<uint32_t*>(xq_staged));
-  return launch_kernel(attention_merge_kernel<D, false>, dim3(mgrid), dim3(128), 0, st, partials, n_q_heads, tps,
+  return launch_kernel(attention_merge_kernel<D, false>, dim3(mgrid), dim3(D), 0, st, partials, n_q_heads, tps,
                        meta.chunk_off, max_chunks, n_tok, out, static_cast<uint8_t*>(nullptr),
                        static_cast<uint32_t*>(nullptr));
 }
