@@ -203,9 +203,10 @@ cudaError_t launch_embed_params(const void* table, int hidden, int n_tok, float*
 cudaError_t launch_rmsnorm_quant(const float* x, const float* w, int n_tok, int hidden, float eps, void* xq,
                                  cudaStream_t st, void* staged) {
   if (n_tok == 0) return cudaSuccess;
-  // about two blocks per warp: hidden / 32 blocks over 8 warps per CTA
+  // about two blocks per warp (one block per warp up to 8 tokens, where
+  // there are few rows to spread): hidden / 32 blocks over 8 warps per CTA
   const int n = hidden / kGlueThreads;
-  int split = (hidden / 32 + 15) / 16;
+  int split = n_tok <= 8 ? (hidden / 32 + 7) / 8 : (hidden / 32 + 15) / 16;
   if (split > n) split = n;
   if (split < (n + kMaxShare - 1) / kMaxShare) split = (n + kMaxShare - 1) / kMaxShare;
   if (split < 1) split = 1;

@@ -49,6 +49,7 @@ __device__ __forceinline__ void rope_cs(int pos, double freq, float* c, float* s
 // Heads handled per thread in one pass: every load of a pass is issued before
 // any store, so the pass costs one memory round trip instead of one per head.
 constexpr int kRopeHeads = 8;
+constexpr int kRopeHeadsFew = 4;  // the step's RoPE + KV write up to 8 tokens: more, smaller CTAs
 constexpr int kRopeMaxWarps = 16;  // head_dim <= 1024: at most 512 pair threads
 
 // Optional per-head RMS norm before the rotation: for each of the block's
@@ -56,13 +57,14 @@ constexpr int kRopeMaxWarps = 16;  // head_dim <= 1024: at most 512 pair threads
 // (pair i of head u is (x1[u], x2[u]) in thread i; threads past the last
 // pair hold zeros).  Sums go through a fixed xor tree per warp and the warps
 // in order.  Every thread of the block must call it.
-__device__ __forceinline__ void head_inv_rms(const float (&x1)[kRopeHeads], const float (&x2)[kRopeHeads],
-                                             int head_dim, float eps, float (&inv)[kRopeHeads]) {
-  __shared__ float part[kRopeHeads][kRopeMaxWarps];
+template <int HG = kRopeHeads>
+__device__ __forceinline__ void head_inv_rms(const float (&x1)[HG], const float (&x2)[HG], int head_dim, float eps,
+                                             float (&inv)[HG]) {
+  __shared__ float part[HG][kRopeMaxWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n_warps = (blockDim.x + 31) >> 5;
 #pragma unroll
-  for (int u = 0; u < kRopeHeads; ++u) {
+  for (int u = 0; u < HG; ++u) {
     float ss = __fmaf_rn(x2[u], x2[u], __fmul_rn(x1[u], x1[u]));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
@@ -70,7 +72,7 @@ __device__ __forceinline__ void head_inv_rms(const float (&x1)[kRopeHeads], cons
   }
   __syncthreads();
 #pragma unroll
-  for (int u = 0; u < kRopeHeads; ++u) {
+  for (int u = 0; u < HG; ++u) {
     float tot = 0.0f;
     for (int w = 0; w < n_warps; ++w) tot = __fadd_rn(tot, part[u][w]);
     inv[u] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)head_dim), eps)));
@@ -185,11 +187,11 @@ __global__ void kv_scatter_paged_kernel(T* __restrict__ kp, T* __restrict__ vp, 
   }
 }
 
-// The step's fused pass, grid (n_tok, ceil((Hq + Hkv) / kRopeHeads)), one
+// The step's fused pass, grid (n_tok, ceil((Hq + Hkv) / HG)), one
 // thread per pair.  Head slot hs < Hq rotates query head hs in place; slot
 // Hq + g rotates kv head g of k and writes it, and kv head g of v, into the
 // cache slot of the token's sequence.  Loads of a pass precede its stores.
-template <typename T>
+template <typename T, int HG>
 __global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, int n_q_heads, int n_kv_heads,
                                      int head_dim, const int32_t* __restrict__ pos,
                                      const int32_t* __restrict__ batch_index, int tokens_per_seq, T* __restrict__ kc,
@@ -225,10 +227,10 @@ __global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, 
     kv_row = ((size_t)batch_index[sq] * n_kv_heads * ctx + p) * head_dim;
     kv_head_stride = (size_t)ctx * head_dim;
   }
-  const int h0 = blockIdx.y * kRopeHeads;
-  float x1[kRopeHeads], x2[kRopeHeads], v1[kRopeHeads], v2[kRopeHeads];
+  const int h0 = blockIdx.y * HG;
+  float x1[HG], x2[HG], v1[HG], v2[HG];
 #pragma unroll
-  for (int u = 0; u < kRopeHeads; ++u) {
+  for (int u = 0; u < HG; ++u) {
     const int hs = h0 + u;
     x1[u] = x2[u] = v1[u] = v2[u] = 0.0f;
     if (hs < n_q_heads + n_kv_heads && pair) {
@@ -243,10 +245,10 @@ __global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, 
     }
   }
   if (q_norm || k_norm) {
-    float inv[kRopeHeads];
-    head_inv_rms(x1, x2, head_dim, eps, inv);
+    float inv[HG];
+    head_inv_rms<HG>(x1, x2, head_dim, eps, inv);
 #pragma unroll
-    for (int u = 0; u < kRopeHeads; ++u) {
+    for (int u = 0; u < HG; ++u) {
       const float* w = h0 + u < n_q_heads ? q_norm : k_norm;
       if (w && pair) {
         x1[u] = __fmul_rn(__fmul_rn(x1[u], inv[u]), w[i]);
@@ -255,7 +257,7 @@ __global__ void rope_kv_write_kernel(float* __restrict__ qkv, long long stride, 
     }
   }
 #pragma unroll
-  for (int u = 0; u < kRopeHeads; ++u) {
+  for (int u = 0; u < HG; ++u) {
     const int hs = h0 + u;
     if (hs >= n_q_heads + n_kv_heads || !pair) continue;
     const float y1 = __fmaf_rn(x1[u], c, __fmul_rn(-x2[u], s));
@@ -325,15 +327,20 @@ cudaError_t launch_rope_kv_write(float* qkv, long long stride, int n_q_heads, in
                                  PagedView pv) {
   if (n_tok == 0) return cudaSuccess;
   const int threads = ((head_dim / 2 + 31) / 32) * 32;
-  const dim3 grid((unsigned)n_tok, (unsigned)((n_q_heads + n_kv_heads + kRopeHeads - 1) / kRopeHeads));
+  // up to 8 tokens, groups of 4 heads (more CTAs for the few tokens); else 8
+  const bool few = n_tok <= 8;
+  const int hg = few ? kRopeHeadsFew : kRopeHeads;
+  const dim3 grid((unsigned)n_tok, (unsigned)((n_q_heads + n_kv_heads + hg - 1) / hg));
   if (dtype == 0)
-    return launch_kernel(rope_kv_write_kernel<__half>, grid, dim3(threads), 0, st, qkv, stride, n_q_heads,
-                         n_kv_heads, head_dim, pos_dev, batch_index_dev, tokens_per_seq, static_cast<__half*>(kc),
-                         static_cast<__half*>(vc), ctx, freqs, q_norm, k_norm, eps, pv);
-  return launch_kernel(rope_kv_write_kernel<__nv_bfloat16>, grid, dim3(threads), 0, st, qkv, stride, n_q_heads,
-                       n_kv_heads, head_dim, pos_dev, batch_index_dev, tokens_per_seq,
-                       static_cast<__nv_bfloat16*>(kc), static_cast<__nv_bfloat16*>(vc), ctx, freqs, q_norm, k_norm,
-                       eps, pv);
+    return launch_kernel(few ? rope_kv_write_kernel<__half, kRopeHeadsFew> : rope_kv_write_kernel<__half, kRopeHeads>,
+                         grid, dim3(threads), 0, st, qkv, stride, n_q_heads, n_kv_heads, head_dim, pos_dev,
+                         batch_index_dev, tokens_per_seq, static_cast<__half*>(kc), static_cast<__half*>(vc), ctx,
+                         freqs, q_norm, k_norm, eps, pv);
+  return launch_kernel(
+      few ? rope_kv_write_kernel<__nv_bfloat16, kRopeHeadsFew> : rope_kv_write_kernel<__nv_bfloat16, kRopeHeads>,
+      grid, dim3(threads), 0, st, qkv, stride, n_q_heads, n_kv_heads, head_dim, pos_dev, batch_index_dev,
+      tokens_per_seq, static_cast<__nv_bfloat16*>(kc), static_cast<__nv_bfloat16*>(vc), ctx, freqs, q_norm, k_norm,
+      eps, pv);
 }
 
 // YaRN (Peng et al. 2023, "YaRN: Efficient Context Window Extension of Large
