@@ -146,7 +146,11 @@ def test_step_matches_oracle(cuda_device, ms, b, T):
             assert np.array_equal(kg[slot][:, keep], kc[l][slot][:, keep])
 
 
-@pytest.mark.parametrize("ms,b,T", [(_shapes.TINY, 3, 2), (_shapes.LLAMA68M, 4, 1)], ids=["tiny", "llama"])
+# (8 sequences x 2 tokens: the batched step's matmuls take 16 tokens on the
+# tensor-core block dots and its glue the wide launch shapes, each single
+# sequence's 2 tokens the dp4a block dots and the narrow shapes)
+@pytest.mark.parametrize("ms,b,T", [(_shapes.TINY, 3, 2), (_shapes.LLAMA68M, 4, 1), (_shapes.LLAMA68M, 8, 2)],
+                         ids=["tiny", "llama", "llama-16-tokens"])
 def test_batched_step_rows_equal_single_sequence_steps(cuda_device, ms, b, T):
     model, _, _, _ = _build(ms)
     bi, lens, toks = _shapes.step_meta(2, ms, b, T)
