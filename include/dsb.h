@@ -561,6 +561,27 @@ dsb_status dsb_step_graph_create(const dsb_model* model, int n_seq, int tokens_p
  * replay has read the pinned copy before rewriting it. */
 dsb_status dsb_step_graph_launch(dsb_step_graph* g, const int32_t* token_ids, const int32_t* batch_index,
                                  const int32_t* seq_lens, void* stream);
+/* The paged step (dsb_decode_step_paged) captured the same way, for a fixed
+ * (n_seq, T) and block-table width max_blocks: the pools' device memory is
+ * bound at capture (pages: host array [n_layers], read during the call only;
+ * the pools must outlive the graph), while every replay takes new token ids,
+ * seq_lens, block tables, block counts and windows in its metadata (mapped
+ * form once the block tables pass 4096 words).  The attention is captured for
+ * max_blocks + 1 chunks per sequence, the most any geometry of that width
+ * visits, and reads the actual count on the device; the workspace must hold
+ * dsb_step_workspace_bytes(shape, n_seq*T, 128 * (max_blocks + 1)).
+ * DSB_ERR_UNSUPPORTED when 2*n_seq*T + 3*n_seq + 1 + n_seq*(max_blocks + 2)
+ * words exceed the staging slot. */
+dsb_status dsb_step_graph_create_paged(const dsb_model* model, const dsb_kv_pages* pages, int max_blocks, int n_seq,
+                                       int tokens_per_seq, float* logits, dsb_workspace* ws, void* stream,
+                                       dsb_step_graph** out);
+/* Validates the step's geometry as dsb_decode_step_paged does (against the
+ * pools bound at capture) and launches the graph; the metadata handling is
+ * that of dsb_step_graph_launch.  Each launch function rejects a graph of the
+ * other kind with DSB_ERR_INVALID_ARG. */
+dsb_status dsb_step_graph_launch_paged(dsb_step_graph* g, const int32_t* token_ids, const int32_t* seq_lens,
+                                       const int32_t* block_table, const int32_t* n_blocks, const int32_t* window,
+                                       void* stream);
 dsb_status dsb_step_graph_destroy(dsb_step_graph* g);
 
 /* ---- live-batch former (host only) -----------------------------------------

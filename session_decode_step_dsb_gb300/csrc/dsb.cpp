@@ -1143,6 +1143,11 @@ struct dsb_step_graph {
   int32_t* a_meta_dst = nullptr;
   int a_n_words = 0;
   std::vector<int32_t> a_words;  // capacity words: the parameter block
+  // A step on page pools: layer 0's pool (for the geometry checks) and the
+  // block-table width the graph was captured for.
+  bool paged = false;
+  dsb_kv_pages pages0{};
+  int max_blocks = 0;
 };
 
 // The parameters of the graph's embedding node for the current words.
@@ -1198,15 +1203,15 @@ dsb_status dsb_decode_step_trace(const dsb_model* model, const int32_t* token_id
                       nullptr, 0, nullptr, nullptr, trace);
 }
 
-dsb_status dsb_decode_step_paged(const dsb_model* model, const dsb_kv_pages* pages, const int32_t* token_ids,
-                                 int n_seq, int tokens_per_seq, const int32_t* seq_lens, const int32_t* block_table,
-                                 int max_blocks, const int32_t* n_blocks, const int32_t* window, float* logits,
-                                 dsb_workspace* ws, void* stream) {
-  const dsb_kv_cache* unused = nullptr;
-  dsb_status st = check_model(model, &unused, false);
-  if (st != DSB_OK) return st;
-  const dsb_model_shape& sh = model->shape;
+// The metadata words of a step on page pools -- tokens | batch_index (unused:
+// zeros) | seq_lens | chunk_off | pos | block_table | n_blocks | window --
+// after every check of the call: tokens in range, the block geometry, and no
+// two tokens of the step writing one page row.  total: the step's attention
+// chunks; max_chunks: the most chunks one sequence visits.
+// One page pool per layer, all of the shape's heads and one geometry.
+static dsb_status check_pools(const dsb_model_shape& sh, const dsb_kv_pages* pages) {
   if (!pages) return fail(DSB_ERR_INVALID_ARG, "pages is NULL");
+  dsb_status st = DSB_OK;
   for (int l = 0; l < sh.n_layers; ++l) {
     if ((st = check_pages(&pages[l])) != DSB_OK) return fail(st, "layer %d pages: %s", l, dsb_last_error());
     if (pages[l].n_kv_heads != sh.n_kv_heads || pages[l].head_dim != sh.head_dim)
@@ -1214,10 +1219,18 @@ dsb_status dsb_decode_step_paged(const dsb_model* model, const dsb_kv_pages* pag
     if (pages[l].n_pages != pages[0].n_pages || pages[l].dtype != pages[0].dtype)
       return fail(DSB_ERR_INVALID_ARG, "layer %d page pool geometry differs from layer 0", l);
   }
+  return DSB_OK;
+}
+
+static dsb_status paged_step_words(const dsb_model_shape& sh, const dsb_kv_pages* pages0, const int32_t* token_ids,
+                                   int n_seq, int tokens_per_seq, const int32_t* seq_lens, const int32_t* block_table,
+                                   int max_blocks, const int32_t* n_blocks, const int32_t* window,
+                                   std::vector<int32_t>* out, long long* total_out, int* max_chunks_out) {
+  dsb_status st = DSB_OK;
   if ((long long)(sh.n_q_heads / sh.n_kv_heads) * tokens_per_seq > 64)
     return fail(DSB_ERR_UNSUPPORTED, "query rows per kv head (G*T) exceed 64");
   if (!seq_lens || !token_ids) return fail(DSB_ERR_INVALID_ARG, "token_ids / seq_lens is NULL");
-  st = check_paged_geometry(&pages[0], block_table, max_blocks, n_blocks, window, n_seq, tokens_per_seq, seq_lens);
+  st = check_paged_geometry(pages0, block_table, max_blocks, n_blocks, window, n_seq, tokens_per_seq, seq_lens);
   if (st != DSB_OK) return st;
   const int n_tok = n_seq * tokens_per_seq;
   for (int t = 0; t < n_tok; ++t)
@@ -1237,7 +1250,8 @@ dsb_status dsb_decode_step_paged(const dsb_model* model, const dsb_kv_pages* pag
   if (std::adjacent_find(rows.begin(), rows.end()) != rows.end())
     return fail(DSB_ERR_INVALID_ARG, "two tokens of the step write the same page row");
   // tokens | batch_index (unused: zeros) | seq_lens | chunk_off | pos | block_table | n_blocks | window
-  std::vector<int32_t> words(token_ids, token_ids + n_tok);
+  std::vector<int32_t>& words = *out;
+  words.assign(token_ids, token_ids + n_tok);
   words.insert(words.end(), (size_t)n_seq, 0);
   words.insert(words.end(), seq_lens, seq_lens + n_seq);
   long long total = 0;
@@ -1257,6 +1271,27 @@ dsb_status dsb_decode_step_paged(const dsb_model* model, const dsb_kv_pages* pag
   words.insert(words.end(), n_blocks, n_blocks + n_seq);
   words.insert(words.end(), window, window + n_seq);
   if (words.size() > kMetaWords) return fail(DSB_ERR_UNSUPPORTED, "step metadata with block tables exceeds the staging slot");
+  *total_out = total;
+  *max_chunks_out = max_chunks;
+  return DSB_OK;
+}
+
+dsb_status dsb_decode_step_paged(const dsb_model* model, const dsb_kv_pages* pages, const int32_t* token_ids,
+                                 int n_seq, int tokens_per_seq, const int32_t* seq_lens, const int32_t* block_table,
+                                 int max_blocks, const int32_t* n_blocks, const int32_t* window, float* logits,
+                                 dsb_workspace* ws, void* stream) {
+  const dsb_kv_cache* unused = nullptr;
+  dsb_status st = check_model(model, &unused, false);
+  if (st != DSB_OK) return st;
+  const dsb_model_shape& sh = model->shape;
+  if ((st = check_pools(sh, pages)) != DSB_OK) return st;
+  std::vector<int32_t> words;
+  long long total = 0;
+  int max_chunks = 1;
+  st = paged_step_words(sh, &pages[0], token_ids, n_seq, tokens_per_seq, seq_lens, block_table, max_blocks, n_blocks,
+                        window, &words, &total, &max_chunks);
+  if (st != DSB_OK) return st;
+  const int n_tok = n_seq * tokens_per_seq;
   int sms = 0;
   st = check_step_resources(model, n_tok, logits, ws, &sms, max_chunks * DSB_ATTN_CHUNK);
   if (st != DSB_OK) return st;
@@ -1272,33 +1307,15 @@ dsb_status dsb_decode_step_paged(const dsb_model* model, const dsb_kv_pages* pag
                       nullptr, nullptr, nullptr, &pg);
 }
 
-dsb_status dsb_step_graph_create(const dsb_model* model, int n_seq, int tokens_per_seq, float* logits,
-                                 dsb_workspace* ws, void* stream, dsb_step_graph** out) {
-  if (!out) return fail(DSB_ERR_INVALID_ARG, "out is NULL");
-  *out = nullptr;
-  const dsb_kv_cache* kv0 = nullptr;
-  dsb_status st = check_model(model, &kv0);
-  if (st != DSB_OK) return st;
-  if (n_seq < 1 || n_seq > kv0->full_batch_size || n_seq > DSB_MAX_SEQS || tokens_per_seq < 1 ||
-      (long long)n_seq * tokens_per_seq > DSB_MAX_TOKENS)
-    return fail(DSB_ERR_INVALID_ARG, "n_seq=%d / tokens_per_seq=%d out of range", n_seq, tokens_per_seq);
-  if ((long long)(model->shape.n_q_heads / model->shape.n_kv_heads) * tokens_per_seq > 64)
-    return fail(DSB_ERR_UNSUPPORTED, "query rows per kv head (G*T) exceed 64");
-  int sms = 0;
-  const int n_tok = n_seq * tokens_per_seq;
-  st = check_step_resources(model, n_tok, logits, ws, &sms);
-  if (st != DSB_OK) return st;
-  dsb_step_graph* g = new (std::nothrow) dsb_step_graph();
-  if (!g) return fail(DSB_ERR_INVALID_ARG, "out of host memory");
-  g->shape = model->shape;
-  g->kv0 = *kv0;
-  g->n_seq = n_seq;
-  g->tps = tokens_per_seq;
-  g->ws = ws;
-  g->n_words = (size_t)2 * n_tok + 3 * (size_t)n_seq + 1;
-  const StepLayout L = step_layout(model->shape, n_tok, kv0->ctx);
+// Captures the step into g (n_seq, tps, ws and n_words already set): the
+// contiguous caches, or the page pools of pg; ctx_cover: the cache length the
+// attention partials cover; max_items: a bound on the attention's work items.
+static dsb_status capture_step(dsb_step_graph* g, const dsb_model* model, float* logits, int sms, int ctx_cover,
+                               long long max_items, const StepPages* pg) {
+  const int n_tok = g->n_seq * g->tps;
+  dsb_workspace* ws = g->ws;
+  const StepLayout L = step_layout(model->shape, n_tok, ctx_cover);
   g->dev_meta = reinterpret_cast<int32_t*>(ws->dev + L.graph_meta);
-  (void)stream;  // the graph is captured on a private stream and replayed on the caller's
   cudaStream_t cs = nullptr;
   // The step's metadata is read by the first kernel straight from mapped
   // pinned host memory (no copy node at the head of the graph).
@@ -1310,45 +1327,35 @@ dsb_status dsb_step_graph_create(const dsb_model* model, int n_seq, int tokens_p
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
   if (e != cudaSuccess) {
     if (cs) cudaStreamDestroy(cs);
-    if (g->done) cudaEventDestroy(g->done);
-    if (g->pinned) cudaFreeHost(g->pinned);
-    delete g;
     return cuda_fail(e, "dsb_step_graph_create");
   }
-  // Placeholder metadata for the capture: one chunk per sequence; the real
-  // values are written before every launch.
+  // Placeholder metadata for the capture; the real values are written before
+  // every launch.
   std::memset(g->pinned, 0, g->n_words * sizeof(int32_t));
   g->param_mode = g->n_words <= (size_t)dsbk::kEmbedParamMaxWords;
   std::vector<int32_t> zeros(g->n_words, 0);
   const int32_t* words_arg = g->param_mode ? zeros.data() : nullptr;
-  const long long max_items =
-      (long long)n_seq * ((kv0->ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK) * model->shape.n_kv_heads;
   // Warm every launcher's one-time set-up outside the capture.
   dsbk::set_dry_run(true);
-  dsb_status dry = enqueue_step(model, g->dev_meta, n_seq, tokens_per_seq, max_items, logits, ws, sms, cs,
-                                g->pinned_dev, g->n_words, words_arg);
+  dsb_status dry = enqueue_step(model, g->dev_meta, g->n_seq, g->tps, max_items, logits, ws, sms, cs, g->pinned_dev,
+                                g->n_words, words_arg, nullptr, nullptr, pg);
   dsbk::set_dry_run(false);
   if (dry != DSB_OK) {
     cudaStreamDestroy(cs);
-    cudaEventDestroy(g->done);
-    cudaFreeHost(g->pinned);
-    delete g;
     return dry;
   }
   e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
   if (e == cudaSuccess) {
-    const dsb_status es = enqueue_step(model, g->dev_meta, n_seq, tokens_per_seq, max_items, logits, ws, sms, cs,
-                                       g->pinned_dev, g->n_words, words_arg, &g->embed);
+    const dsb_status es = enqueue_step(model, g->dev_meta, g->n_seq, g->tps, max_items, logits, ws, sms, cs,
+                                       g->pinned_dev, g->n_words, words_arg, &g->embed, nullptr, pg);
     cudaError_t e2 = cudaStreamEndCapture(cs, &g->graph);
-    if (e == cudaSuccess && es != DSB_OK) {
+    if (es != DSB_OK) {
       if (g->graph) cudaGraphDestroy(g->graph);
+      g->graph = nullptr;
       cudaStreamDestroy(cs);
-      cudaEventDestroy(g->done);
-      cudaFreeHost(g->pinned);
-      delete g;
       return es;
     }
-    if (e == cudaSuccess) e = e2;
+    e = e2;
   }
   cudaStreamDestroy(cs);
   if (e == cudaSuccess) e = cudaGraphInstantiate(&g->exec, g->graph, 0);
@@ -1371,28 +1378,23 @@ dsb_status dsb_step_graph_create(const dsb_model* model, int n_seq, int tokens_p
       g->a_words.assign((size_t)g->embed.capacity, 0);
     }
   }
-  if (e != cudaSuccess) {
-    if (g->exec) cudaGraphExecDestroy(g->exec);
-    if (g->graph) cudaGraphDestroy(g->graph);
-    cudaEventDestroy(g->done);
-    cudaFreeHost(g->pinned);
-    delete g;
-    return cuda_fail(e, "step graph capture");
-  }
-  *out = g;
-  return DSB_OK;
+  return e == cudaSuccess ? DSB_OK : cuda_fail(e, "step graph capture");
 }
 
-dsb_status dsb_step_graph_launch(dsb_step_graph* g, const int32_t* token_ids, const int32_t* batch_index,
-                                 const int32_t* seq_lens, void* stream) {
-  if (!g) return fail(DSB_ERR_INVALID_ARG, "graph is NULL");
-  dsb_model fake{};
-  fake.shape = g->shape;
-  dsb_status st = check_step_meta(&fake, &g->kv0, token_ids, batch_index, g->n_seq, g->tps, seq_lens);
-  if (st != DSB_OK) return st;
-  long long total = 0;
-  std::vector<int32_t> words = step_words(token_ids, batch_index, g->n_seq, g->tps, seq_lens, &total);
+// Frees whatever a (possibly half-built) graph holds.
+static void free_graph(dsb_step_graph* g) {
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  if (g->done) cudaEventDestroy(g->done);
+  if (g->pinned) cudaFreeHost(g->pinned);
+  delete g;
+}
+
+// Writes the step's metadata words for the next replay and launches it.
+static dsb_status launch_words(dsb_step_graph* g, std::vector<int32_t>& words, void* stream) {
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (words.size() != g->n_words) return fail(DSB_ERR_INVALID_ARG, "step metadata of %zu words, the graph holds %zu",
+                                              words.size(), g->n_words);
   if (g->param_mode) {
     // the node's parameters are copied when set: no wait for the previous replay
     if (words != g->last) {
@@ -1423,6 +1425,118 @@ dsb_status dsb_step_graph_launch(dsb_step_graph* g, const int32_t* token_ids, co
   return DSB_OK;
 }
 
+dsb_status dsb_step_graph_create(const dsb_model* model, int n_seq, int tokens_per_seq, float* logits,
+                                 dsb_workspace* ws, void* stream, dsb_step_graph** out) {
+  if (!out) return fail(DSB_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  const dsb_kv_cache* kv0 = nullptr;
+  dsb_status st = check_model(model, &kv0);
+  if (st != DSB_OK) return st;
+  if (n_seq < 1 || n_seq > kv0->full_batch_size || n_seq > DSB_MAX_SEQS || tokens_per_seq < 1 ||
+      (long long)n_seq * tokens_per_seq > DSB_MAX_TOKENS)
+    return fail(DSB_ERR_INVALID_ARG, "n_seq=%d / tokens_per_seq=%d out of range", n_seq, tokens_per_seq);
+  if ((long long)(model->shape.n_q_heads / model->shape.n_kv_heads) * tokens_per_seq > 64)
+    return fail(DSB_ERR_UNSUPPORTED, "query rows per kv head (G*T) exceed 64");
+  int sms = 0;
+  const int n_tok = n_seq * tokens_per_seq;
+  st = check_step_resources(model, n_tok, logits, ws, &sms);
+  if (st != DSB_OK) return st;
+  dsb_step_graph* g = new (std::nothrow) dsb_step_graph();
+  if (!g) return fail(DSB_ERR_INVALID_ARG, "out of host memory");
+  g->shape = model->shape;
+  g->kv0 = *kv0;
+  g->n_seq = n_seq;
+  g->tps = tokens_per_seq;
+  g->ws = ws;
+  g->n_words = (size_t)2 * n_tok + 3 * (size_t)n_seq + 1;
+  (void)stream;  // the graph is captured on a private stream and replayed on the caller's
+  const long long max_items =
+      (long long)n_seq * ((kv0->ctx + DSB_ATTN_CHUNK - 1) / DSB_ATTN_CHUNK) * model->shape.n_kv_heads;
+  st = capture_step(g, model, logits, sms, kv0->ctx, max_items, nullptr);
+  if (st != DSB_OK) {
+    free_graph(g);
+    return st;
+  }
+  *out = g;
+  return DSB_OK;
+}
+
+dsb_status dsb_step_graph_launch(dsb_step_graph* g, const int32_t* token_ids, const int32_t* batch_index,
+                                 const int32_t* seq_lens, void* stream) {
+  if (!g) return fail(DSB_ERR_INVALID_ARG, "graph is NULL");
+  if (g->paged) return fail(DSB_ERR_INVALID_ARG, "a graph on page pools launches with dsb_step_graph_launch_paged");
+  dsb_model fake{};
+  fake.shape = g->shape;
+  dsb_status st = check_step_meta(&fake, &g->kv0, token_ids, batch_index, g->n_seq, g->tps, seq_lens);
+  if (st != DSB_OK) return st;
+  long long total = 0;
+  std::vector<int32_t> words = step_words(token_ids, batch_index, g->n_seq, g->tps, seq_lens, &total);
+  return launch_words(g, words, stream);
+}
+
+dsb_status dsb_step_graph_create_paged(const dsb_model* model, const dsb_kv_pages* pages, int max_blocks, int n_seq,
+                                       int tokens_per_seq, float* logits, dsb_workspace* ws, void* stream,
+                                       dsb_step_graph** out) {
+  if (!out) return fail(DSB_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  const dsb_kv_cache* unused = nullptr;
+  dsb_status st = check_model(model, &unused, false);
+  if (st != DSB_OK) return st;
+  if ((st = check_pools(model->shape, pages)) != DSB_OK) return st;
+  if (n_seq < 1 || n_seq > DSB_MAX_SEQS || tokens_per_seq < 1 || (long long)n_seq * tokens_per_seq > DSB_MAX_TOKENS)
+    return fail(DSB_ERR_INVALID_ARG, "n_seq=%d / tokens_per_seq=%d out of range", n_seq, tokens_per_seq);
+  if (max_blocks < 1) return fail(DSB_ERR_INVALID_ARG, "max_blocks=%d < 1", max_blocks);
+  if ((long long)(model->shape.n_q_heads / model->shape.n_kv_heads) * tokens_per_seq > 64)
+    return fail(DSB_ERR_UNSUPPORTED, "query rows per kv head (G*T) exceed 64");
+  const int n_tok = n_seq * tokens_per_seq;
+  // tokens | batch_index | seq_lens | chunk_off | pos | block_table | n_blocks | window
+  const size_t n_words = (size_t)2 * n_tok + 3 * (size_t)n_seq + 1 + (size_t)n_seq * max_blocks + 2 * (size_t)n_seq;
+  if (n_words > kMetaWords) return fail(DSB_ERR_UNSUPPORTED, "step metadata with block tables exceeds the staging slot");
+  // a sequence visits at most max_blocks + 1 chunks: its blocks, and under a
+  // window the partly hidden chunk at the ring's start
+  const int max_chunks = max_blocks + 1;
+  int sms = 0;
+  st = check_step_resources(model, n_tok, logits, ws, &sms, max_chunks * DSB_ATTN_CHUNK);
+  if (st != DSB_OK) return st;
+  dsb_step_graph* g = new (std::nothrow) dsb_step_graph();
+  if (!g) return fail(DSB_ERR_INVALID_ARG, "out of host memory");
+  g->shape = model->shape;
+  g->n_seq = n_seq;
+  g->tps = tokens_per_seq;
+  g->ws = ws;
+  g->n_words = n_words;
+  g->paged = true;
+  g->pages0 = pages[0];
+  g->max_blocks = max_blocks;
+  (void)stream;
+  StepPages pg;
+  pg.pages = pages;
+  pg.max_blocks = max_blocks;
+  pg.max_chunks = max_chunks;
+  st = capture_step(g, model, logits, sms, max_chunks * DSB_ATTN_CHUNK,
+                    (long long)n_seq * max_chunks * model->shape.n_kv_heads, &pg);
+  if (st != DSB_OK) {
+    free_graph(g);
+    return st;
+  }
+  *out = g;
+  return DSB_OK;
+}
+
+dsb_status dsb_step_graph_launch_paged(dsb_step_graph* g, const int32_t* token_ids, const int32_t* seq_lens,
+                                       const int32_t* block_table, const int32_t* n_blocks, const int32_t* window,
+                                       void* stream) {
+  if (!g) return fail(DSB_ERR_INVALID_ARG, "graph is NULL");
+  if (!g->paged) return fail(DSB_ERR_INVALID_ARG, "a graph on contiguous caches launches with dsb_step_graph_launch");
+  std::vector<int32_t> words;
+  long long total = 0;
+  int max_chunks = 1;
+  dsb_status st = paged_step_words(g->shape, &g->pages0, token_ids, g->n_seq, g->tps, seq_lens, block_table,
+                                   g->max_blocks, n_blocks, window, &words, &total, &max_chunks);
+  if (st != DSB_OK) return st;
+  return launch_words(g, words, stream);
+}
+
 dsb_status dsb_step_graph_destroy(dsb_step_graph* g) {
   if (!g) return DSB_OK;
   dsb_status st = DSB_OK;
@@ -1436,11 +1550,7 @@ dsb_status dsb_step_graph_destroy(dsb_step_graph* g) {
       std::this_thread::yield();
     }
   }
-  if (g->exec) cudaGraphExecDestroy(g->exec);
-  if (g->graph) cudaGraphDestroy(g->graph);
-  if (g->done) cudaEventDestroy(g->done);
-  if (g->pinned) cudaFreeHost(g->pinned);
-  delete g;
+  free_graph(g);
   return st;
 }
 

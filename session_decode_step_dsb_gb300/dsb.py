@@ -604,6 +604,9 @@ SIGNATURES.update({
                                    ctypes.POINTER(StepTraceC), _P]),
     "dsb_step_graph_create": (_I, [ctypes.POINTER(ModelC), _I, _I, _P, _P, _P, ctypes.POINTER(_P)]),
     "dsb_step_graph_launch": (_I, [_P, _PI32, _PI32, _PI32, _P]),
+    "dsb_step_graph_create_paged": (_I, [ctypes.POINTER(ModelC), ctypes.POINTER(KVPages), _I, _I, _I, _P, _P, _P,
+                                         ctypes.POINTER(_P)]),
+    "dsb_step_graph_launch_paged": (_I, [_P, _PI32, _PI32, _PI32, _PI32, _PI32, _P]),
     "dsb_step_graph_destroy": (_I, [_P]),
     "dsb_batch_former_create": (_I, [_I, _I, _I, ctypes.POINTER(_P)]),
     "dsb_batch_former_destroy": (None, [_P]),
@@ -821,17 +824,32 @@ class DecodeModel:
     def graph(self, n_seq: int, tokens_per_seq: int, logits, ws: Workspace, stream=None) -> "StepGraph":
         return StepGraph(self, n_seq, tokens_per_seq, logits, ws, stream)
 
+    def graph_paged(self, pages, max_blocks: int, n_seq: int, tokens_per_seq: int, logits, ws: Workspace,
+                    stream=None) -> "StepGraph":
+        """The paged step captured for block tables ``max_blocks`` wide
+        (dsb_step_graph_create_paged); replay with ``launch_paged``."""
+        return StepGraph(self, n_seq, tokens_per_seq, logits, ws, stream, pages=pages, max_blocks=max_blocks)
+
 
 class StepGraph:
     """A decode step captured once for a fixed (n_seq, T) and replayed."""
 
-    def __init__(self, model: DecodeModel, n_seq: int, tokens_per_seq: int, logits, ws: Workspace, stream=None):
+    def __init__(self, model: DecodeModel, n_seq: int, tokens_per_seq: int, logits, ws: Workspace, stream=None,
+                 pages=None, max_blocks: int = 0):
         self.model, self.logits, self.ws = model, logits, ws
         self.n_seq, self.T = n_seq, tokens_per_seq
+        self.pages, self.max_blocks = pages, max_blocks
         _need(logits, 4 * n_seq * tokens_per_seq * model.vocab, "logits", "f32")
         handle = _P()
-        _check(lib().dsb_step_graph_create(ctypes.byref(model.c), n_seq, tokens_per_seq, _ptr(logits), ws.handle,
-                                           _stream(stream), ctypes.byref(handle)))
+        if pages is None:
+            _check(lib().dsb_step_graph_create(ctypes.byref(model.c), n_seq, tokens_per_seq, _ptr(logits), ws.handle,
+                                               _stream(stream), ctypes.byref(handle)))
+        else:
+            if len(pages) != model.shape.n_layers:
+                raise ValueError(f"pages: one pool per layer ({model.shape.n_layers}), got {len(pages)}")
+            arr = (KVPages * len(pages))(*pages)
+            _check(lib().dsb_step_graph_create_paged(ctypes.byref(model.c), arr, max_blocks, n_seq, tokens_per_seq,
+                                                     _ptr(logits), ws.handle, _stream(stream), ctypes.byref(handle)))
         self.handle = handle
 
     def launch(self, token_ids, batch_index, seq_lens, stream=None):
@@ -839,6 +857,17 @@ class StepGraph:
         bi, pbi = _i32(batch_index, self.n_seq, "batch_index")
         sl, psl = _i32(seq_lens, self.n_seq, "seq_lens")
         _check(lib().dsb_step_graph_launch(self.handle, ptk, pbi, psl, _stream(stream)))
+        return self.logits
+
+    def launch_paged(self, token_ids, seq_lens, block_table, n_blocks, window, stream=None):
+        """Replay of a graph on page pools with this step's geometry
+        (``block_table [n_seq][max_blocks]`` as captured)."""
+        bt, pbt, nb, pnb, win, pwin = _geometry(block_table, n_blocks, window)
+        if bt.shape != (self.n_seq, self.max_blocks):
+            raise ValueError(f"block_table: shape ({self.n_seq}, {self.max_blocks}) expected, got {bt.shape}")
+        tk, ptk = _i32(token_ids, self.n_seq * self.T, "token_ids")
+        sl, psl = _i32(seq_lens, self.n_seq, "seq_lens")
+        _check(lib().dsb_step_graph_launch_paged(self.handle, ptk, psl, pbt, pnb, pwin, _stream(stream)))
         return self.logits
 
     def close(self):

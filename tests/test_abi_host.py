@@ -239,3 +239,18 @@ def test_workspace_sizes(lib):
     assert lib.dsb_workspace_create(None, 1 << 20, ctypes.byref(out)) == 1
     assert lib.dsb_workspace_create(ctypes.c_void_p((1 << 20) + 8), 1 << 20, ctypes.byref(out)) == 1
     assert lib.dsb_workspace_create(ctypes.c_void_p(1 << 20), 100, ctypes.byref(out)) == 3
+
+
+def test_step_graph_entry_points_reject_null_handles(lib):
+    """The captured-step entry points, both kinds, refuse missing handles on
+    the host before any CUDA call."""
+    out = ctypes.c_void_p()
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.dsb_step_graph_create_paged(None, None, 2, 1, 1, fake, fake, None, ctypes.byref(out)) == 1
+    assert lib.dsb_step_graph_create_paged(None, None, 2, 1, 1, fake, fake, None, None) == 1
+    assert "out" in _err(lib)
+    assert lib.dsb_step_graph_launch_paged(None, None, None, None, None, None, None) == 1
+    assert "graph" in _err(lib)
+    assert lib.dsb_step_graph_launch(None, None, None, None, None) == 1
+    assert lib.dsb_step_graph_create(None, 1, 1, fake, fake, None, ctypes.byref(out)) == 1
+    assert not out.value

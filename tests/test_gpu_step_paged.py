@@ -135,3 +135,89 @@ def test_paged_step_rejects_bad_geometry(cuda_device):
         model.step_paged(pages, toks, T, lens_same, same, np.full(b, nb), np.zeros(b), ws)
     with pytest.raises(ValueError):
         model.step_paged(pages[:-1] if ms.n_layers > 1 else [], toks, T, lens, bt, np.full(b, nb), np.zeros(b), ws)
+
+
+def _geometry_steps(ms, b, T, max_blocks, seed):
+    """Three steps' metadata for one captured graph: linear tables with no
+    window; the next positions under a window W = 200 (each sequence's nb
+    blocks used as a ring, which the longer sequences wrap); then the first
+    step's lengths again with the sequences' page rows handed round (another
+    block table).  Tables are max_blocks wide, the columns past nb padding."""
+    bi, lens, toks = _shapes.step_meta(seed, ms, b, T)
+    nb = ms.ctx // P
+    perm = np.random.default_rng(seed).permutation(ms.full_batch_size * nb)
+    bt = np.zeros((b, max_blocks), np.int32)
+    for s, f in enumerate(bi):
+        bt[s, :nb] = [perm[int(f) * nb + i] for i in range(nb)]
+    rng = np.random.default_rng(seed + 1)
+    toks2 = rng.integers(0, ms.vocab, size=b * T).astype(np.int32)
+    toks3 = rng.integers(0, ms.vocab, size=b * T).astype(np.int32)
+    zero, full = np.zeros(b, np.int32), np.full(b, nb, np.int32)
+    return perm, [(toks, lens, bt, full, zero),
+                  (toks2, lens + T, bt, full, np.full(b, 200, np.int32)),
+                  (toks3, lens, np.roll(bt, 1, axis=0), full, zero)]
+
+
+@pytest.mark.parametrize("ms,b,T,wide", [(SHAPES[0], 3, 2, False), (SHAPES[1], 2, 3, False), (SHAPES[0], 4, 2, True)],
+                         ids=["f16-b3-T2-params", "bf16-qkn-b2-T3-params", "f16-b4-T2-mapped"])
+def test_paged_graph_replay_equals_the_eager_paged_step(cuda_device, ms, b, T, wide):
+    """The paged step captured once (dsb_step_graph_create_paged) and replayed
+    with a new geometry each time is bitwise the eager paged step on a second
+    copy of the pools: logits of every replay and the pools afterwards.  With
+    1100-wide tables the metadata passes the first kernel's parameter block
+    and the graph reads it from mapped memory."""
+    import torch
+    d = _dsb()
+    model, orc, kc, vc = _build(ms, seed=24)
+    nb = ms.ctx // P
+    max_blocks = 1100 if wide else nb
+    perm, steps = _geometry_steps(ms, b, T, max_blocks, seed=24 + b)
+    kp, vp = _pools(kc, perm, ms), _pools(vc, perm, ms)
+    for_graph, for_eager = _dev_pages(kp, vp, ms), _dev_pages(kp, vp, ms)
+    ws = d.StepWorkspace(model.shape, b * T, P * (max_blocks + 1))
+    logits = torch.empty((b * T, ms.vocab), dtype=torch.float32, device="cuda")
+    g = model.graph_paged(for_graph, max_blocks, b, T, logits, ws)
+    for i, (toks, lens, bt, nbk, win) in enumerate(steps):
+        eager = to_host(model.step_paged(for_eager, toks, T, lens, bt, nbk, win, ws))
+        replay = to_host(g.launch_paged(toks, lens, bt, nbk, win))
+        assert np.array_equal(eager.view(np.uint32), replay.view(np.uint32)), i
+    for l in range(ms.n_layers):
+        for j in range(2):
+            assert np.array_equal(to_host(for_graph[l]._tensors[j]).view(np.uint16),
+                                  to_host(for_eager[l]._tensors[j]).view(np.uint16)), (l, j)
+    g.close()
+    d.device_error()
+
+
+def test_paged_graph_rejects_the_other_kind_and_bad_geometry(cuda_device):
+    import torch
+    d = _dsb()
+    ms = SHAPES[0]
+    model, orc, kc, vc = _build(ms, seed=25)
+    b, T = 2, 1
+    nb = ms.ctx // P
+    perm, steps = _geometry_steps(ms, b, T, nb, seed=25)
+    pages = _dev_pages(_pools(kc, perm, ms), _pools(vc, perm, ms), ms)
+    ws = d.StepWorkspace(model.shape, b * T, P * (nb + 1))
+    logits = torch.empty((b * T, ms.vocab), dtype=torch.float32, device="cuda")
+    toks, lens, bt, nbk, win = steps[0]
+    g = model.graph_paged(pages, nb, b, T, logits, ws)
+    bi = np.arange(b, dtype=np.int32)
+    with pytest.raises(d.DsbError):   # a paged graph takes no contiguous launch
+        g.launch(toks, bi, lens)
+    bad = bt.copy()
+    bad[0, 0] = len(perm)             # page out of range
+    with pytest.raises(d.DsbError):
+        g.launch_paged(toks, lens, bad, nbk, win)
+    with pytest.raises(ValueError):   # a table of another width
+        g.launch_paged(toks, lens, bt[:, :1], nbk, win)
+    g.launch_paged(toks, lens, bt, nbk, win)
+    torch.cuda.synchronize()
+    g.close()
+    c = model.graph(b, T, logits, model.workspace(b * T))
+    st = d.lib().dsb_step_graph_launch_paged(c.handle, *[None] * 6)
+    assert st == d.DSB_ERR_INVALID_ARG   # a contiguous graph takes no paged launch
+    c.close()
+    with pytest.raises(d.DsbError):   # block tables beyond the staging slot
+        model.graph_paged(pages, 6000, b, T, logits, ws)
+    d.device_error()
