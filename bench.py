@@ -16,7 +16,8 @@ kernel.
 One "step" is one replay of the captured decode-step graph (every kernel of
 the hot path: embedding, RMSNorm+q8_0, narrow q8_0 matmuls, per-head norm +
 pos-vector RoPE + KV write through batch_index, split-K attention + merge,
-SiLU-gate, head).  L2 is flushed (a 512 MiB write) before every timed step and
+SiLU-gate, head).  L2 is flushed (a 512 MiB write, then half of it read back,
+so no dirty line stays) before every timed step and
 each step is timed on its stream with CUDA events.  Prints ONE JSON line on
 rank 0; besides the headline it carries the b sweep, the narrow-matmul GB/s
 sweep, the long-context attention GB/s, the llama-68m-shaped step and the
@@ -245,12 +246,23 @@ def step_bytes(ms, b, T, lens):
 HOST_SLACK_CYCLES = 200_000
 
 
+def _flush_l2(flush):
+    """Evict L2 before a timed call: write the 512 MiB buffer, then read its
+    first half back.  The write alone would leave L2 full of the buffer's dirty
+    lines, and the timed call would pay for writing them back to HBM as its own
+    reads evict them (129 MB: about 19 us of HBM time, a fifth of a small step);
+    after the read, every line L2 holds is clean and none is the timed call's."""
+    import torch
+    flush.zero_()
+    torch.count_nonzero(flush[: flush.numel() // 2])
+
+
 def _time_device(fn, iters, flush, stream):
     """Median and mean device time (ms) of fn(), L2 flushed before each call."""
     import torch
     ts = []
     for _ in range(iters):
-        flush.zero_()
+        _flush_l2(flush)
         torch.cuda._sleep(HOST_SLACK_CYCLES)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -561,7 +573,7 @@ def run_dsb(args):
             "config": {"workload": ms.name, "b": b, "tokens_per_seq": T, "n_tok": n_tok,
                        "full_batch_size": ms.full_batch_size, "ctx": ms.ctx, "seq_lens": [int(v) for v in lens],
                        "layers": ms.n_layers, "hidden": ms.hidden, "vocab": ms.vocab,
-                       "l2": "flushed (512 MiB write) before every timed step", "parallelism": f"replicas x{world}",
+                       "l2": "flushed before every timed step: 512 MiB written, then 256 MiB of it read back (clean cold L2)", "parallelism": f"replicas x{world}",
                        "step_bytes": total_bytes, "weight_bytes": wbytes, "kv_bytes": kvbytes},
             "step_ms": {"p50": round(float(np.percentile(ts, 50)), 5), "p90": round(float(np.percentile(ts, 90)), 5),
                         "p95": round(float(np.percentile(ts, 95)), 5), "mean": round(float(mean), 5)},

@@ -34,7 +34,8 @@ cudaError_t launch_matmul_q8_0_staged(const void* W, int64_t rows, int64_t cols,
                                       float* y, const float* residual, int num_sms, cudaStream_t st) {
   int G = 0;
   const int S = matmul_plan_of(rows, cols, num_sms, &G);
-  const size_t smem = matmul_smem_bytes(rows, cols, n_tok, num_sms);
+  const int nks = (int)(cols / 256);
+  const size_t smem = smem_bytes((nks + S - 1) / S, n_tok, G, S, 3);
   ActSrc src;
   src.staged = static_cast<const uint32_t*>(staged);
   return dispatch<false, 3>(n_tok, static_cast<const uint8_t*>(W), (int)rows, (int)(cols / 32), src, y, residual,
