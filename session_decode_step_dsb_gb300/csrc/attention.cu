@@ -128,36 +128,41 @@ struct Item {
   long long row0;
 };
 
+// kL2: the metadata is read through L2 (the tensor-core kernel decodes its
+// first item before it waits for its predecessor); the items after it read
+// it through L1, where the binary search's loads hit.
+template <bool kL2 = false>
 __device__ __forceinline__ Item decode_item(int item, int n_kv_heads, int ctx, const int32_t* batch_index,
                                             const int32_t* seq_lens, const int32_t* chunk_off, int n_seq, int tps,
                                             const PagedView& pv) {
+  auto ld = [](const int32_t* p) { return kL2 ? __ldcg(p) : *p; };
   Item it;
   const int w = item / n_kv_heads;
   it.g = item - w * n_kv_heads;
   int lo = 0, hi = n_seq - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (chunk_off[mid] <= w)
+    if (ld(chunk_off + mid) <= w)
       lo = mid;
     else
       hi = mid - 1;
   }
   it.s = lo;
-  it.c_rel = w - chunk_off[lo];  // this sequence's chunk, counted from its first
-  it.L = seq_lens[lo];
+  it.c_rel = w - ld(chunk_off + lo);  // this sequence's chunk, counted from its first
+  it.L = ld(seq_lens + lo);
   // Paged view: chunk c lives in one page (128 keys), found through the
   // block table (modulo the block count for a ring); a window hides keys
   // older than pos - W + 1, so the first chunks of a long ring are skipped.
-  it.W = pv.block_table ? pv.window[lo] : 0;
+  it.W = pv.block_table ? ld(pv.window + lo) : 0;
   const int c = (it.W > 0 ? max(0, it.L - tps + 1 - it.W) / kCh : 0) + it.c_rel;
   it.key0 = c * kCh;
   it.nkeys = min(kCh, it.L - it.key0);
   if (pv.block_table) {
-    const int nb = pv.n_blocks[lo];
-    const int page = pv.block_table[(size_t)lo * pv.max_blocks + (it.W > 0 ? c % nb : c)];
+    const int nb = ld(pv.n_blocks + lo);
+    const int page = ld(pv.block_table + (size_t)lo * pv.max_blocks + (it.W > 0 ? c % nb : c));
     it.row0 = ((long long)page * n_kv_heads + it.g) * kCh;
   } else {
-    it.row0 = ((long long)batch_index[lo] * n_kv_heads + it.g) * (long long)ctx + it.key0;
+    it.row0 = ((long long)ld(batch_index + lo) * n_kv_heads + it.g) * (long long)ctx + it.key0;
   }
   return it;
 }
@@ -529,28 +534,60 @@ __global__ void __launch_bounds__(kThreads) attention_partial_tc_kernel(
   }
   // the padding query rows R..R8-1 stay zero (no copy writes them)
   for (int idx = tid; idx < (R8 - R) * QF; idx += kThreads) Qf[R * QF + idx] = 0.0f;
-  pdl_wait();  // q and the cache rows of this step come from the previous kernels
-  pdl_trigger();
 
-  const int total_items = chunk_off[n_seq] * n_kv_heads;
   // Thread 0 requests an item's query rows (one bulk copy of D floats per
   // row, into the padded rows of Qf) and then its K boxes, all on bars[0]:
   // the query rows are first in line behind no K or V traffic of this CTA.
-  auto issue_qk = [&](const Item& x) {
-    const uint32_t qb = (uint32_t)(D * 4);
-    mbar_arrive_expect_tx(&bars[0], (uint32_t)R * qb + tile_bytes<D>(x));
+  const uint32_t qb = (uint32_t)(D * 4);
+  auto issue_q = [&](const Item& x) {
     for (int r = 0; r < R; ++r) {
       const int j = r / G, gi = r - j * G;
       bulk_g2s(Qf + (size_t)r * QF, q + (size_t)(x.s * tps + j) * q_stride + (size_t)(x.g * G + gi) * D, qb,
                &bars[0]);
     }
+  };
+  auto issue_qk = [&](const Item& x) {
+    mbar_arrive_expect_tx(&bars[0], (uint32_t)R * qb + tile_bytes<D>(x));
+    issue_q(x);
     issue_boxes<D>(x, &tmk, Ks, &bars[0]);
   };
+  // With at most two items per CTA the start-up is a large part of a CTA's
+  // time, so it moves ahead of the wait for the previous kernel.  The step's
+  // metadata (lengths, slots, chunk offsets) is written by its first kernel,
+  // which has completed before the previous kernel starts its own work (every
+  // kernel waits for its predecessor before it lets the next one launch): the
+  // first item is decoded before the wait, reading through L2.  So are its K
+  // and V requested, when the cache is contiguous and none of the rows the
+  // tile covers is one the previous kernel writes (the step's new rows
+  // L - T .. L - 1 of this slot; slots are distinct).  The query rows always
+  // follow the wait.  With more items per CTA the early start measured no
+  // faster (the Qwen3-14B-shaped step at 16 sequences, 5 items per CTA).
+  const int total_items = __ldcg(chunk_off + n_seq) * n_kv_heads;
+  const bool start_early = total_items <= 2 * (int)gridDim.x;
+  Item first{};
+  bool early = false;
+  if (start_early && (int)blockIdx.x < total_items && tid == 0) {
+    first = decode_item<true>(blockIdx.x, n_kv_heads, ctx, batch_index, seq_lens, chunk_off, n_seq, tps, pv);
+    const int tile_rows = (first.nkeys > kBoxKeys ? 2 : 1) * kBoxKeys;
+    early = pv.block_table == nullptr && first.key0 + tile_rows <= first.L - tps;
+    if (early) {
+      mbar_arrive_expect_tx(&bars[0], (uint32_t)R * qb + tile_bytes<D>(first));
+      issue_boxes<D>(first, &tmk, Ks, &bars[0]);
+      issue_tile<D>(first, &tmv, Vs, &bars[1]);
+    }
+  }
+  pdl_wait();  // q and the cache rows of this step come from the previous kernels
+  pdl_trigger();
   if ((int)blockIdx.x < total_items && tid == 0) {
-    const Item first = decode_item(blockIdx.x, n_kv_heads, ctx, batch_index, seq_lens, chunk_off, n_seq, tps, pv);
+    if (!start_early)
+      first = decode_item(blockIdx.x, n_kv_heads, ctx, batch_index, seq_lens, chunk_off, n_seq, tps, pv);
     nx2[0] = first;
-    issue_qk(first);
-    issue_tile<D>(first, &tmv, Vs, &bars[1]);
+    if (early) {
+      issue_q(first);
+    } else {
+      issue_qk(first);
+      issue_tile<D>(first, &tmv, Vs, &bars[1]);
+    }
   }
   __syncthreads();
   uint32_t phase = 0;
