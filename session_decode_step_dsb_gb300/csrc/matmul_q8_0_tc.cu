@@ -29,19 +29,26 @@
 // that the grid fills the SMs; rank 0 then adds the other ranks' float32
 // partial tiles through distributed shared memory in rank order (no atomics,
 // the same order on every run).  Warp roles (10 warps):
-//   0..7  workers.  During the K loop worker w owns weight rows 16w..16w+15:
-//         it stages their raw q8_0 bytes by 1-D bulk copies (8 blocks = 272 B
-//         per row, 16-byte aligned when cols % 256 == 0) into its own part of
-//         a two-stage ring, refilling a stage as soon as it has converted it,
-//         and writes their hi and lo operands, one q8_0 block per slot.  It
-//         also drains the chunk accumulators for TMEM lanes 32*(w%4).. and
-//         columns 64*(w/4).. into registers, a few blocks behind the MMAs, and
-//         at the end stores y (+ residual).  Warp 0 also allocates and frees
-//         the TMEM.
+//   0..7  workers.  Warps w and w + 4 own TMEM lane quarter w % 4 (weight
+//         rows 32(w%4) .. +31, lane = row) and convert its rows for the
+//         q8_0 blocks of even and odd index respectively: the odd warp stages
+//         the quarter's raw q8_0 bytes by 1-D bulk copies (8 blocks = 272 B per
+//         row, 16-byte aligned when cols % 256 == 0) into a two-stage ring
+//         that both read, refilling a stage once both are done with it; each
+//         lane splits its row's 32 values into hi and lo and stores them into
+//         the block's weight operand slot in tensor memory (tcgen05.st, 16
+//         columns each), so the MMAs read only the token operand from shared
+//         memory.  Every worker also drains the chunk accumulators for its
+//         lane quarter and columns 64*(w/4).. into registers, a few blocks
+//         behind the MMAs, and at the end stores y (+ residual).  Warp 0 also
+//         allocates and frees the TMEM.
 //   8     producer: bulk copies of the token operands (hi and lo), which a
 //         pack kernel laid out once per call.
-//   9     MMA issuer (one thread).
-// Operand layout (no swizzle, K-major): element (m, k) of a 128 x 32 f16
+//   9     MMA issuer (one thread); A from tensor memory, B from shared memory.
+// Tensor memory (512 columns): the two chunk accumulators (columns 0..255),
+// then eight weight operand slots of 32 columns (hi, then lo; a 128 x 16 f16
+// operand is 8 columns of two f16 values per lane).
+// Token operand layout (no swizzle, K-major): element (m, k) of a 128 x 32 f16
 // operand at byte (m/8)*512 + (k/8)*128 + (m%8)*16 + (k%8)*2, i.e. 8x8 core
 // matrices of 128 contiguous bytes, 128 B apart along K (LBO) and 512 B apart
 // along M/N (SBO).
@@ -68,15 +75,19 @@ constexpr int kTcM = 128;            // weight rows per CTA
 constexpr int kTcN = 128;            // token rows per CTA
 constexpr int kTcStageBlocks = 8;    // q8_0 blocks per raw weight stage
 constexpr int kTcRawStages = 2;
-constexpr int kTcSlots = 4;          // operand slots, one q8_0 block each
+constexpr int kTcSlots = 8;          // operand slots, one q8_0 block each
 constexpr int kTcWorkWarps = 8;
-constexpr int kTcRowsPerWarp = kTcM / kTcWorkWarps;           // 16
 constexpr int kTcProducerWarp = kTcWorkWarps;                 // 8
 constexpr int kTcMmaWarp = kTcProducerWarp + 1;               // 9
 constexpr int kTcThreads = (kTcMmaWarp + 1) * 32;             // 320
 constexpr int kTcChunk = 8;                                   // blocks per TMEM accumulation chunk
 constexpr int kTcAccRegions = 2;
-constexpr int kTcTmemCols = kTcAccRegions * kTcN;             // 256
+constexpr int kTcQuarters = kTcM / 32;                        // TMEM lane quarters (32 rows each)
+constexpr int kTcACol0 = kTcAccRegions * kTcN;                // 256: first column of the weight operand slots
+constexpr int kTcASlotCols = 32;                              // one slot: hi (16 columns), then lo (16)
+constexpr int kTcTmemCols = 512;                              // accumulators + operand slots, a power of two
+static_assert(kTcACol0 + kTcSlots * kTcASlotCols <= kTcTmemCols, "tensor memory holds the operand slots");
+static_assert(kTcSlots % 2 == 0, "a slot always holds blocks of one parity");
 constexpr int kOpBytes = kTcM * 32 * 2;                       // 8192: one 128 x 32 f16 operand
 constexpr int kRawRowBytes = kTcStageBlocks * 34;             // 272
 constexpr int kRawStageBytes = kTcM * kRawRowBytes;           // 34816
@@ -86,17 +97,16 @@ constexpr uint32_t kSuspendHintNs = 100000;                   // per try_wait
 static_assert(kTcN == kTcM, "token operands share the weight operands' geometry");
 
 struct __align__(1024) TcSmem {
-  uint8_t a[kTcSlots][2][kOpBytes];            // weight hi, lo (written by the workers)
   uint8_t b[kTcSlots][2][kOpBytes];            // token hi, lo (bulk-copied from the pack)
-  uint8_t raw[kTcRawStages][kRawStageBytes];   // raw q8_0 weight rows
-  uint64_t raw_full[kTcRawStages][kTcWorkWarps];
+  uint8_t raw[kTcRawStages][kRawStageBytes];   // raw q8_0 weight rows, 32 rows per lane quarter
+  uint64_t raw_full[kTcRawStages][kTcQuarters], raw_empty[kTcRawStages][kTcQuarters];
   uint64_t slot_full[kTcSlots], slot_empty[kTcSlots];
   uint64_t acc_full[kTcAccRegions], acc_empty[kTcAccRegions];
   uint32_t tmem_base;
   int abort_flag;
   int cta_ok;
 };
-static_assert(sizeof(((TcSmem*)nullptr)->a) >= (size_t)kTcM * kTcN * 4, "the partial tile reuses the weight slots");
+static_assert(sizeof(((TcSmem*)nullptr)->b) >= (size_t)kTcM * kTcN * 4, "the partial tile reuses the token slots");
 
 __device__ unsigned int g_err_matmul_tc = 0;
 
@@ -166,13 +176,26 @@ __device__ __forceinline__ uint32_t idesc_f16(int m, int n) {
   return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// D (tensor memory) (+)= A (tensor memory) x B (shared-memory descriptor).
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
           d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
+
+// 16 consecutive TMEM columns of this warp's 32 lanes, one 32-bit word each.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
@@ -267,9 +290,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kTcRawStages; ++i)
-      for (int c = 0; c < kTcWorkWarps; ++c) mbar_init(&s.raw_full[i][c], 1);
+      for (int c = 0; c < kTcQuarters; ++c) {
+        mbar_init(&s.raw_full[i][c], 1);
+        mbar_init(&s.raw_empty[i][c], 2);  // both warps of the quarter are done with the stage
+      }
     for (int i = 0; i < kTcSlots; ++i) {
-      mbar_init(&s.slot_full[i], kTcWorkWarps + 1);
+      mbar_init(&s.slot_full[i], kTcWorkWarps / 2 + 1);  // the four warps of the block's parity + the producer
       mbar_init(&s.slot_empty[i], 1);
     }
     for (int i = 0; i < kTcAccRegions; ++i) {
@@ -331,15 +357,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(ac * kTcN);
-        const uint64_t a_hi = smem_desc(s.a[sl][0]), a_lo = smem_desc(s.a[sl][1]);
+        const uint32_t a_hi = tmem + (uint32_t)(kTcACol0 + sl * kTcASlotCols), a_lo = a_hi + 16u;
         const uint64_t b_hi = smem_desc(s.b[sl][0]), b_lo = smem_desc(s.b[sl][1]);
 #pragma unroll
         for (int kh = 0; kh < 2; ++kh) {
-          // k = 16*kh .. +15: core matrices 2kh, 2kh+1 along K, 2 * LBO = 256 bytes per half
+          // k = 16*kh .. +15: the operands' TMEM columns 8kh .. 8kh + 7 (two
+          // f16 per column), core matrices 2kh, 2kh+1 of the token operand
+          // (2 * LBO = 256 bytes per half)
           const uint64_t dk = (uint64_t)(kh * (256u >> 4));
-          mma_f16(d, a_hi + dk, b_hi + dk, idesc, (jc > 0 || kh > 0) ? 1u : 0u);
-          mma_f16(d, a_hi + dk, b_lo + dk, idesc, 1u);
-          mma_f16(d, a_lo + dk, b_hi + dk, idesc, 1u);
+          const uint32_t ak = (uint32_t)(8 * kh);
+          mma_f16_ta(d, a_hi + ak, b_hi + dk, idesc, (jc > 0 || kh > 0) ? 1u : 0u);
+          mma_f16_ta(d, a_hi + ak, b_lo + dk, idesc, 1u);
+          mma_f16_ta(d, a_lo + ak, b_hi + dk, idesc, 1u);
         }
         mma_commit(&s.slot_empty[sl]);
         if (jc == kTcChunk - 1 || i == nbl - 1) mma_commit(&s.acc_full[ac]);
@@ -351,12 +380,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     ok = __shfl_sync(0xffffffffu, ok, 0);
   } else {
     // ---------------------------------------------------------------- workers
-    const int r0 = warp * kTcRowsPerWarp;
-    const int my_rows = max(0, min(kTcRowsPerWarp, rows_valid - r0));
-    // lane = 8 g + r_sub: the 8 lanes of a quarter-warp write one 16-byte
-    // piece each of 8 different rows of one core matrix, 8 different bank
-    // groups, so the operand stores are conflict-free
-    const int r_sub = lane & 7, g = lane >> 3;
+    // Warp w converts the rows of TMEM lane quarter qw = w % 4 (rows 32qw ..
+    // 32qw + 31, lane = row) for the blocks of parity w / 4; the two warps of a
+    // quarter share its raw stages, which the odd one refills once both are
+    // done with them.
+    const int qw = warp & 3, par = warp >> 2;
+    const int my_row = qw * 32 + lane;
+    const int quarter_rows = max(0, min(32, rows_valid - qw * 32));
+    const uint32_t lane_base = (uint32_t)(qw * 32) << 16;
     int raw_issued = 0;
     const int n_chunks = nbl / kTcChunk;
     int drained = 0;
@@ -382,77 +413,91 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) mbar_arrive(&s.acc_empty[ac]);
       return true;
     };
-    auto issue_raw = [&](int st) {  // this warp's rows of raw stage st
-      uint64_t* bar = &s.raw_full[st & 1][warp];
-      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(my_rows * kRawRowBytes));
+    // this quarter's rows of raw stage st, one row per lane (the odd warp)
+    auto issue_raw = [&](int st) {
+      uint64_t* bar = &s.raw_full[st & 1][qw];
+      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(quarter_rows * kRawRowBytes));
       __syncwarp();
-      if (lane < my_rows)
-        bulk_g2s(s.raw[st & 1] + (r0 + lane) * kRawRowBytes,
-                 W + (size_t)(row0 + r0 + lane) * row_bytes + (size_t)(c_lo + st) * kRawRowBytes, kRawRowBytes, bar);
+      if (lane < quarter_rows)
+        bulk_g2s(s.raw[st & 1] + (qw * 32 + lane) * kRawRowBytes,
+                 W + (size_t)(row0 + qw * 32 + lane) * row_bytes + (size_t)(c_lo + st) * kRawRowBytes, kRawRowBytes,
+                 bar);
     };
     // the weights do not depend on the previous kernel: start them first
-    for (; raw_issued < kTcRawStages && raw_issued < n_stages; ++raw_issued) issue_raw(raw_issued);
+    if (par == 1)
+      for (; raw_issued < kTcRawStages && raw_issued < n_stages; ++raw_issued) issue_raw(raw_issued);
     bool range_ok = true;
-    for (int i = 0; i < nbl; ++i) {
-      const int st = i / kTcStageBlocks, jb = i % kTcStageBlocks, rb = st & 1, sl = i % kTcSlots;
-      if (jb == 0) ok = tc_wait(s, &s.raw_full[rb][warp], (uint32_t)((st >> 1) & 1));
-      if (ok && i >= kTcSlots) ok = tc_wait(s, &s.slot_empty[sl], (uint32_t)((i / kTcSlots - 1) & 1));
-      ok = __all_sync(0xffffffffu, ok);
+    // Stage by stage; this warp's four blocks of a stage are jb = 2jj + par.
+    // Block jb's 34 bytes start at byte 34jb = 68jj + 34par of the row's
+    // stage chunk, i.e. 2par bytes into word jj of the three 16-byte pieces
+    // from byte 64jj + 32par on (16-byte loads at the 272-byte row stride
+    // touch eight distinct bank groups per quarter-warp).
+    for (int st = 0; st < n_stages && ok; ++st) {
+      const int rb = st & 1;
+      ok = __all_sync(0xffffffffu, tc_wait(s, &s.raw_full[rb][qw], (uint32_t)((st >> 1) & 1)));
       if (!ok) break;
-      const uint8_t* raw = s.raw[rb];
-      // load both of this lane's items first, then convert and store
-      uint32_t wv[2][2], dv[2];
+      const uint8_t* row_raw = s.raw[rb] + my_row * kRawRowBytes + 32 * par;
 #pragma unroll
-      for (int it = 0; it < 2; ++it) {
-        const int r = r0 + it * 8 + r_sub;
-        wv[it][0] = wv[it][1] = 0u;
-        dv[it] = 0u;
-        if (r < rows_valid) {
-          const int off = r * kRawRowBytes + jb * 34 + 2 + 8 * g;  // first of this lane's 8 codes
-          if (jb & 1) {  // codes start on a word boundary
-            wv[it][0] = *reinterpret_cast<const uint32_t*>(raw + off);
-            wv[it][1] = *reinterpret_cast<const uint32_t*>(raw + off + 4);
-          } else {       // two bytes into a word
-            const uint32_t a = *reinterpret_cast<const uint32_t*>(raw + off - 2);
-            const uint32_t b = *reinterpret_cast<const uint32_t*>(raw + off + 2);
-            const uint32_t c = *reinterpret_cast<const uint32_t*>(raw + off + 6);
-            wv[it][0] = __funnelshift_r(a, b, 16);
-            wv[it][1] = __funnelshift_r(b, c, 16);
+      for (int jj = 0; jj < kTcStageBlocks / 2; ++jj) {
+        const int i = st * kTcStageBlocks + 2 * jj + par, sl = i % kTcSlots;
+        if (i >= kTcSlots) ok = tc_wait(s, &s.slot_empty[sl], (uint32_t)((i / kTcSlots - 1) & 1));
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();  // the slot's previous MMAs have read its operands
+        uint32_t hi[16], lo[16];
+        uint32_t dbits = 0u;
+        if (lane < quarter_rows) {
+          const uint4* src = reinterpret_cast<const uint4*>(row_raw + 64 * jj);
+          const uint4 p0 = src[0], p1 = src[1], p2 = src[2];
+          const uint32_t wd[12] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w, p2.x, p2.y, p2.z, p2.w};
+          uint32_t bw[9];  // the block's bytes 4k .. 4k + 3
+#pragma unroll
+          for (int k = 0; k < 9; ++k) bw[k] = __funnelshift_r(wd[jj + k], wd[jj + k + 1 < 12 ? jj + k + 1 : 11], 16 * par);
+          dbits = bw[0] & 0xFFFFu;
+          const uint32_t d2 = dbits | (dbits << 16);
+          // codes 4k .. 4k + 3 are bytes 2 + 4k .. 5 + 4k of the block
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            uint32_t c01, c23;
+            codes_to_f16(__funnelshift_r(bw[k], bw[k + 1], 16), c01, c23);
+            split_pair(d2, c01, hi[2 * k], lo[2 * k]);
+            split_pair(d2, c23, hi[2 * k + 1], lo[2 * k + 1]);
           }
-          dv[it] = *reinterpret_cast<const uint16_t*>(raw + r * kRawRowBytes + jb * 34);
-        }
-      }
+        } else {
 #pragma unroll
-      for (int it = 0; it < 2; ++it) {
-        const int r = r0 + it * 8 + r_sub;
-        range_ok &= half_bits_to_float_tc(dv[it]) <= kMaxScale;
-        uint4 hi, lo;
-        split8(wv[it][0], wv[it][1], dv[it] | (dv[it] << 16), hi, lo);
-        const int o = (r >> 3) * 512 + g * 128 + (r & 7) * 16;
-        *reinterpret_cast<uint4*>(s.a[sl][0] + o) = hi;
-        *reinterpret_cast<uint4*>(s.a[sl][1] + o) = lo;
+          for (int k = 0; k < 16; ++k) hi[k] = lo[k] = 0u;
+        }
+        range_ok &= half_bits_to_float_tc(dbits) <= kMaxScale;
+        const uint32_t acol = tmem + lane_base + (uint32_t)(kTcACol0 + sl * kTcASlotCols);
+        tmem_st16(acol, hi);
+        tmem_st16(acol + 16u, lo);
+        tmem_st_wait();
+        tc_fence_before();  // the operand stores precede the MMAs the barrier releases
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.slot_full[sl]);
       }
-      fence_proxy_async_smem();  // the generic-proxy writes above feed the tensor core (async proxy)
+      if (!ok) break;
+      // both warps of the quarter are done with the stage: the odd one refills it
+      fence_proxy_async_smem();  // this warp's reads of the stage precede the refill's writes
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.slot_full[sl]);
-      // this warp alone reads its rows of the stage: refill it at once
-      if (jb == kTcStageBlocks - 1 && raw_issued < n_stages) {
-        fence_proxy_async_smem();
+      if (lane == 0) mbar_arrive(&s.raw_empty[rb][qw]);
+      if (par == 1 && raw_issued < n_stages) {
+        ok = __all_sync(0xffffffffu, tc_wait(s, &s.raw_empty[rb][qw], (uint32_t)((st >> 1) & 1)));
+        if (!ok) break;
         issue_raw(raw_issued);
         ++raw_issued;
       }
-      // the previous chunk's MMAs trail the conversions by at most the slot depth
-      if (i % kTcChunk == kTcSlots - 1 && i >= kTcChunk) {
+      // the chunk before this stage: its MMAs trail the conversions by at most the slot depth
+      if (st >= 1) {
         ok = drain(drained);
         ++drained;
-        if (!ok) break;
       }
     }
     if (!range_ok) atomicOr(&g_err_matmul_tc, 2u);
     // on the way out: every raw copy issued has landed
-    if (lane == 0)
+    if (lane == 0 && par == 1)
       for (int st = raw_issued - kTcRawStages; st < raw_issued; ++st)
-        if (st >= 0) tc_drain(&s.raw_full[st & 1][warp], (uint32_t)((st >> 1) & 1));
+        if (st >= 0) tc_drain(&s.raw_full[st & 1][qw], (uint32_t)((st >> 1) & 1));
     __syncwarp();
 
     while (ok && drained < n_chunks) {
@@ -485,7 +530,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (S == 1) {
     if (worker && cta_ok) store(acc);
   } else {
-    float* part = reinterpret_cast<float*>(&s.a[0][0][0]);  // [kTcN][kTcM], free once the MMAs are done
+    float* part = reinterpret_cast<float*>(&s.b[0][0][0]);  // [kTcN][kTcM], free once the MMAs are done
     if (worker && rank > 0) {
 #pragma unroll
       for (int j = 0; j < 64; ++j) part[(c0 + j) * kTcM + row_l] = acc[j];
