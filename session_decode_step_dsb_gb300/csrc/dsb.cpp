@@ -955,9 +955,23 @@ std::vector<int32_t> step_words(const int32_t* tokens, const int32_t* bi, int n_
 
 // n_tok <= DSB_NARROW_MAX: the narrow dp4a kernel; more: the tensor-core
 // kernel, with its token operands packed into `pack`.
+// Whether the step's matmul of n_tok > 16 token rows runs as narrow launches
+// of 16 tokens (the weights read once per 16 tokens) rather than on the
+// tensor cores (once per 128): estimated times from this GPU's measurements,
+// a 16-token narrow launch about 10 us + 0.234 us per MB of weights, the
+// tensor-core kernel about 30 us + 0.65 us per MB per 128 token rows (its
+// fixed cost dominates on small matrices: 2304 x 768 at 32 tokens took 30 us
+// there, against about 10 us per narrow launch).
+bool narrow_chunks_cheaper(int64_t rows, int64_t cols, int n_tok) {
+  const double mb = (double)rows * (double)(cols / 32) * 34.0 / 1e6;
+  const double narrow = (double)((n_tok + DSB_NARROW_MAX - 1) / DSB_NARROW_MAX) * (10.0 + 0.234 * mb);
+  const double tc = 30.0 + (double)((n_tok + 127) / 128) * 0.65 * mb;
+  return narrow < tc;
+}
+
 cudaError_t run_matmul(const dsb_q8_0_mat& w, const void* xq, int n_tok, float* y, const float* residual, int sms,
                        void* pack, cudaStream_t st) {
-  if (n_tok > DSB_NARROW_MAX)
+  if (n_tok > DSB_NARROW_MAX && !narrow_chunks_cheaper(w.rows, w.cols, n_tok))
     return dsbk::launch_matmul_q8_0_tc(w.blocks, w.rows, w.cols, xq, n_tok, y, residual, pack, st);
   const size_t blk_row = (size_t)(w.cols / 32) * 34;
   for (int t0 = 0; t0 < n_tok; t0 += DSB_NARROW_MAX) {
@@ -1102,14 +1116,12 @@ dsb_status check_step_resources(const dsb_model* m, int n_tok, float* logits, ds
                                 {s.hidden, (long long)s.n_q_heads * s.head_dim},
                                 {2LL * s.ffn, s.hidden},
                                 {s.hidden, s.ffn}};
-  if (n_tok > DSB_NARROW_MAX) {
-    if (dsbk::matmul_tc_smem_bytes() > (size_t)di.max_smem_optin)
-      return fail(DSB_ERR_UNSUPPORTED, "the tensor-core matmul exceeds shared memory");
-  } else {
-    for (auto& mm : mats)
-      if (dsbk::matmul_smem_bytes(mm[0], mm[1], n_tok, di.sms) > (size_t)di.max_smem_optin)
-        return fail(DSB_ERR_UNSUPPORTED, "a %lldx%lld matmul exceeds shared memory", mm[0], mm[1]);
-  }
+  // past 16 tokens a matmul runs on the tensor cores or as 16-token narrow launches
+  if (n_tok > DSB_NARROW_MAX && dsbk::matmul_tc_smem_bytes() > (size_t)di.max_smem_optin)
+    return fail(DSB_ERR_UNSUPPORTED, "the tensor-core matmul exceeds shared memory");
+  for (auto& mm : mats)
+    if (dsbk::matmul_smem_bytes(mm[0], mm[1], std::min(n_tok, DSB_NARROW_MAX), di.sms) > (size_t)di.max_smem_optin)
+      return fail(DSB_ERR_UNSUPPORTED, "a %lldx%lld matmul exceeds shared memory", mm[0], mm[1]);
   *sms = di.sms;
   return DSB_OK;
 }

@@ -95,15 +95,16 @@ def _rms_err(got, ref):
     return float(np.sqrt(np.mean((got - ref) ** 2)) / np.sqrt(np.mean(ref * ref)))
 
 
-# Speculative decode on the llama shapes: T = K + 1 in {8, 32} puts n_tok = 32
-# and 64 tokens through every matmul (beyond the narrow kernel's 16), and the
-# causal mask inside the drafts through the attention.
+# Speculative decode on the llama shapes: T = K + 1 in {8, 32} puts n_tok = 24,
+# 32 and 64 tokens through every matmul (beyond the narrow kernel's 16: up to
+# 32 as 16-token narrow launches, the last one ragged at 24; 64 on the tensor
+# cores), and the causal mask inside the drafts through the attention.
 # The qk-norm shapes add the per-head q / k RMS norm before the rope; the
 # yarn shapes use the YaRN RoPE with sequences past the original context.
 CASES = [(_shapes.TINY, 3, 1), (_shapes.TINY, 2, 4), (_shapes.TINY_BF16, 5, 1), (_shapes.TINY_QKN, 3, 1),
          (_shapes.TINY_QKN, 2, 4), (_shapes.TINY_BF16_QKN, 4, 2), (_shapes.TINY_YARN, 3, 2),
          (_shapes.TINY_BF16_YARN, 4, 1), (_shapes.LLAMA68M, 4, 1),
-         (_shapes.LLAMA68M, 1, 1), (_shapes.LLAMA68M, 4, 8), (_shapes.LLAMA68M, 2, 32),
+         (_shapes.LLAMA68M, 1, 1), (_shapes.LLAMA68M, 3, 8), (_shapes.LLAMA68M, 4, 8), (_shapes.LLAMA68M, 2, 32),
          pytest.param(_shapes.QWEN3_14B_LAYER, 3, 1, marks=pytest.mark.slow),
          pytest.param(_shapes.QWEN3_14B_LAYER, 16, 1, marks=pytest.mark.slow)]
 
