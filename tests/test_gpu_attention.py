@@ -180,27 +180,39 @@ def test_untouched_slots_after_scatter_and_attention(cuda_device):
 def test_long_context_sampled_heads(cuda_device, C):
     """MHA-shaped long-context attention (128 heads, D 128, fp16 cache of
     full_batch_size 8) past the ~31k rows where the ds4 page's multi-sequence
-    kernel stops; sampled (sequence, head) pairs are given synthetic cache rows
-    and checked against the oracle, the rest of the cache is zero."""
+    kernel stops.  Every head of every sequence's slot holds its own rows: head
+    h is synthetic block h mod 4 rotated by 37 h rows, so no two heads of a
+    slot agree and a head or slot read from the wrong place changes the
+    output.  Five heads (neighbours included) are checked against the oracle
+    on the same rows."""
     import torch
     F, H, D = 8, 128, 128
-    b = 4
+    b, P = 4, 4
     bi = synth.distinct_slots(8, 1, b, F)
     lens = synth.uniform_int(8, 2, 16384, C, b)
     lens[0] = C
+    pools = {}
+    for name, stream in (("k", synth.STREAM_KCACHE), ("v", synth.STREAM_VCACHE)):
+        pools[name] = [synth.cache_bits_rows(8, synth.stream_id(stream, 300 + p), (C, D), "f16", 0, C) for p in range(P)]
+
+    def rows(name, h):
+        return np.roll(pools[name][h % P], 37 * h, axis=0)
+
     kd = torch.zeros((F, H, C, D), dtype=torch.float16, device="cuda")
     vd = torch.zeros((F, H, C, D), dtype=torch.float16, device="cuda")
-    heads = [0, 77, 127]
+    for name, dst in (("k", kd), ("v", vd)):
+        dev_pools = [to_dev(x.view(np.int16)).view(torch.float16) for x in pools[name]]
+        for s in range(b):
+            for h in range(H):
+                dst[int(bi[s]), h, :lens[s]] = torch.roll(dev_pools[h % P], 37 * h, dims=0)[:lens[s]]
+        del dev_pools
+    heads = [0, 1, 64, 77, 127]
     kc_small = np.zeros((b, len(heads), C, D), np.uint16)   # oracle copy, one slot per sequence
     vc_small = np.zeros((b, len(heads), C, D), np.uint16)
     for s in range(b):
         for hi, h in enumerate(heads):
-            rows_k = synth.cache_bits_rows(8, synth.stream_id(synth.STREAM_KCACHE, 100 + s * H + h), (C, D), "f16", 0, int(lens[s]))
-            rows_v = synth.cache_bits_rows(8, synth.stream_id(synth.STREAM_VCACHE, 100 + s * H + h), (C, D), "f16", 0, int(lens[s]))
-            kc_small[s, hi, :lens[s]] = rows_k
-            vc_small[s, hi, :lens[s]] = rows_v
-            kd[int(bi[s]), h, :lens[s]] = to_dev(rows_k.view(np.int16)).view(torch.float16)
-            vd[int(bi[s]), h, :lens[s]] = to_dev(rows_v.view(np.int16)).view(torch.float16)
+            kc_small[s, hi, :lens[s]] = rows("k", h)[:lens[s]]
+            vc_small[s, hi, :lens[s]] = rows("v", h)[:lens[s]]
     q = synth.normal(8, synth.stream_id(synth.STREAM_Q, 4), (b, H, D))
     kv = _dsb().kv_cache(kd, vd, 0)
     out = to_host(_dsb().attention_decode_multi(to_dev(q), kv, bi, 1, lens, _ws(b, H, D, C)))
