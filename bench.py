@@ -317,6 +317,39 @@ def matmul_sweep(flush, stream, peak, iters=15):
     return out
 
 
+WIDE_CASES = [(18432, 7168, 32), (18432, 7168, 128), (18432, 7168, 256), (34816, 5120, 128)]
+
+
+def wide_sweep(flush, stream, iters=15):
+    """The wide q8_0 matmul on the tensor cores (dsb_matmul_q8_0_wide, the
+    step's path past 32 token rows) on the DeepSeek-class 18432 x 7168 stage
+    and the Qwen3-14B-shaped gate|up matrix: device time per call (mean of the
+    launches, L2 flushed before each) and its useful q8_0 work as TOPS-eq
+    (2 rows cols n_tok / time)."""
+    import torch
+    from session_decode_step_dsb_gb300 import dsb
+    out = []
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4321)
+    for rows, cols, nt in WIDE_CASES:
+        w = torch.empty((rows, cols // 32 * 34), dtype=torch.uint8, device="cuda")
+        step = max(1, (1 << 26) // cols)
+        for r0 in range(0, rows, step):
+            r1 = min(rows, r0 + step)
+            dsb.quantize_q8_0(torch.randn((r1 - r0, cols), generator=g, device="cuda") * 0.02, w[r0:r1])
+        x = dsb.quantize_q8_0(torch.randn((nt, cols), generator=g, device="cuda"))
+        y = torch.empty((nt, rows), device="cuda")
+        scratch, _ = dsb._wide_scratch(nt, cols, w.device)
+        for _ in range(2):
+            dsb.matmul_q8_0_wide(w, rows, cols, x, nt, y=y, scratch=scratch)
+        _, mean, _ = _time_device(lambda: dsb.matmul_q8_0_wide(w, rows, cols, x, nt, y=y, scratch=scratch), iters,
+                                  flush, stream)
+        out.append({"rows": rows, "cols": cols, "n_tok": nt, "us": round(mean * 1e3, 2),
+                    "tops_eq": round(2.0 * rows * cols * nt / (mean * 1e-3) / 1e12, 1)})
+        del w, x, y, scratch
+    return out
+
+
 ATTN_CTX = [32768, 65536]
 
 
@@ -523,6 +556,7 @@ def run_dsb(args):
 
     sweep_mm = matmul_sweep(flush, stream, peak) if (world == 1 and not args.no_matmul_sweep) else []
     sweep_attn = attention_sweep(flush, stream, peak) if (world == 1 and not args.no_attn_sweep) else []
+    sweep_wide = wide_sweep(flush, stream) if (world == 1 and not args.no_wide_sweep) else []
 
     # ---- end to end through the C ABI with host buffers: token ids, slots
     # and lengths from host arrays (staged by the library), logits copied back
@@ -589,6 +623,7 @@ def run_dsb(args):
             "b_sweep": sweep,
             "matmul_q8_0_narrow": sweep_mm,
             "attention_long_context": sweep_attn,
+            "matmul_q8_0_wide": sweep_wide,
             "llama_68m_step": extra_llama,
             "spec_grid": extra_spec,
             "e2e": e2e,
@@ -979,6 +1014,7 @@ def main(argv=None):
     ap.add_argument("--cpu-all-core-budget", type=float, default=8.0,
                     help="seconds of the all-core oracle run beside the single-core one (0: skip)")
     ap.add_argument("--no-matmul-sweep", action="store_true")
+    ap.add_argument("--no-wide-sweep", action="store_true", help="skip the wide tensor-core matmul timings")
     ap.add_argument("--no-attn-sweep", action="store_true",
                     help="skip the split-K attention at ctx 32768/65536 (allocates ~70 GB)")
     ap.add_argument("--no-extra", action="store_true",
