@@ -34,6 +34,9 @@ step       one llama-style decode step composed from the above
 Every function is pinned by ``tests/test_oracle_*.py`` against values the
 mathematics fixes (closed forms, invariants, brute force on tiny inputs,
 library routines for special cases).  ``step.decode_step`` is a composition
-of pinned functions; its composition itself is "parity unpinned" beyond the
-per-function pins (see its docstring).
+of pinned functions, and the composition is pinned too: with some of a
+layer's matrices zero it reduces to closed forms of the pinned pieces (the
+head of the normed embedding, the attention and FFN residuals), which fix the
+residual placement, the norm order, the gate / up order and the V slice (see
+its docstring).
 """
