@@ -402,7 +402,8 @@ SPEC_K = (0, 7, 31)
 
 
 def _step_graph_time(model, ms, b, T, seed, ws, flush, stream, iters, dev):
-    """Mean / median device time (ms) of graph replays of one (b, T) step."""
+    """Median and mean device time (ms) of graph replays of one (b, T) step,
+    the seq_lens drawn, and the per-replay times."""
     import torch
     bi, lens, toks = _meta(ms, b, T, seed)
     lg = torch.empty((b * T, ms.vocab), dtype=torch.float32, device=dev)
@@ -411,7 +412,7 @@ def _step_graph_time(model, ms, b, T, seed, ws, flush, stream, iters, dev):
         g.launch(toks, bi, lens)
     med, mean, ts = _time_device(lambda: g.launch(toks, bi, lens), iters, flush, stream)
     g.close()
-    return med, mean, lens
+    return med, mean, lens, ts
 
 
 def llama_step(flush, stream, dev, steps):
@@ -423,7 +424,7 @@ def llama_step(flush, stream, dev, steps):
     ws = model.workspace(8)
     out = {"workload": ms.name, "layers": ms.n_layers, "ctx": ms.ctx, "full_batch_size": ms.full_batch_size}
     for b in (1, 2, 4, 8):
-        med, mean, lens = _step_graph_time(model, ms, b, 1, 7, ws, flush, stream, steps, dev)
+        med, mean, lens, _ = _step_graph_time(model, ms, b, 1, 7, ws, flush, stream, steps, dev)
         tb, wb, kb = step_bytes(ms, b, 1, lens)
         out[f"b{b}"] = {"ms_per_step": round(mean, 5), "tokens_per_s": round(b / (mean * 1e-3), 1),
                         "step_frac": round(tb / (mean * 1e-3) / 1e9 / _peaks()[0], 4)}
@@ -445,7 +446,7 @@ def spec_grid(flush, stream, dev, iters=10):
     for b in SPEC_B:
         for K in SPEC_K:
             T = K + 1
-            med, mean, _ = _step_graph_time(model, ms, b, T, 11, ws, flush, stream, iters, dev)
+            med, mean, _, _ = _step_graph_time(model, ms, b, T, 11, ws, flush, stream, iters, dev)
             out.append({"b": b, "K": K, "n_tok": b * T, "ms_per_step": round(mean, 5),
                         "tokens_per_s": round(b * T / (mean * 1e-3), 1)})
     del model, ws
@@ -495,10 +496,13 @@ def run_dsb(args):
     sweep = {}
     if world == 1 and T == 1:
         for bb in B_SWEEP[args.workload]:
-            _, mean2, lens2 = _step_graph_time(model, ms, bb, 1, 7, ws, flush, stream, 20, dev)
+            _, mean2, lens2, ts2 = _step_graph_time(model, ms, bb, 1, 7, ws, flush, stream, 20, dev)
             tb2, _, _ = step_bytes(ms, bb, 1, lens2)
             sweep[str(bb)] = {"ms_per_step": round(mean2, 4), "tokens_per_s": round(bb / (mean2 * 1e-3), 1),
-                              "step_frac": round(tb2 / (mean2 * 1e-3) / 1e9 / peak, 4)}
+                              "step_frac": round(tb2 / (mean2 * 1e-3) / 1e9 / peak, 4), "replays": len(ts2),
+                              "ms_p50": round(float(np.percentile(ts2, 50)), 4),
+                              "ms_p90": round(float(np.percentile(ts2, 90)), 4),
+                              "ms_min": round(min(ts2), 4), "ms_max": round(max(ts2), 4)}
 
     # ---- dominant kernel roofline: the narrow q8_0 matmul, timed as it runs
     # in the step -- the step's own sequence of matmul launches (every layer's
